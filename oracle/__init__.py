@@ -1,0 +1,187 @@
+"""fp64 CPU oracle for paged GQA decode attention and the fp8 sliding-window variant.
+
+TEST INFRASTRUCTURE ONLY: the tests, the package's smoke check and the benchmark's
+CPU-baseline leg are the only callers.  The library path never imports this package, and
+this package imports nothing from the library.  The arithmetic lives in ``dap_oracle.c``
+(plain C, double precision, OpenMP over output rows); this module compiles it with gcc on
+first use and marshals numpy arrays.
+
+Inputs are raw bit patterns: bf16 tensors arrive as ``np.uint16`` arrays, the fp8 cache
+as ``np.uint8``.  Outputs are ``np.float64``.
+
+Every function is pinned by tests/test_oracle_pins.py (closed forms, brute force against
+torch's float64 scaled_dot_product_attention, page-permutation invariance, the e4m3 table
+against torch's float8_e4m3fn conversion).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dap_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile dap_oracle.c into oracle/_build/liboracle.so (gcc, -O2, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        LL = ctypes.c_longlong
+        D = ctypes.c_double
+        lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_value.restype = D
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_value.restype = D
+        lib.oracle_round_to_bf16.argtypes = [D]
+        lib.oracle_round_to_bf16.restype = D
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = I
+        lib.oracle_set_num_threads.argtypes = [I]
+        lib.oracle_set_num_threads.restype = None
+        lib.oracle_decode_paged.argtypes = [P, LL, LL, P, P, I, P, I, P, I, I, I, I, I, D, P]
+        lib.oracle_decode_paged.restype = I
+        lib.oracle_decode_paged_rows.argtypes = [P, LL, LL, P, P, I, P, I, P, I, I, I, I, I,
+                                                 D, P, I, P]
+        lib.oracle_decode_paged_rows.restype = I
+        lib.oracle_decode_contig.argtypes = [P, LL, LL, P, P, I, P, I, I, I, I, D, P]
+        lib.oracle_decode_contig.restype = I
+        lib.oracle_fp8_swa_range.argtypes = [P, P, P, P, P, I, I, I, I, I, I, D, I, I, P]
+        lib.oracle_fp8_swa_range.restype = None
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected bf16 bit patterns as uint16, got {a.dtype}")
+    return np.ascontiguousarray(a)
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def bf16_value(bits: int) -> float:
+    return _load().oracle_bf16_value(int(bits))
+
+
+def e4m3_value(byte: int) -> float:
+    return _load().oracle_e4m3_value(int(byte))
+
+
+def e4m3_table() -> np.ndarray:
+    lib = _load()
+    return np.array([lib.oracle_e4m3_value(b) for b in range(256)], dtype=np.float64)
+
+
+def round_to_bf16(x: float) -> float:
+    return _load().oracle_round_to_bf16(float(x))
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale: float) -> np.ndarray:
+    """Paged GQA decode.  q [B,Hq,D] u16, caches [P,ps,Hkv,D] u16, block_table [B,max_pages]
+    int32, seq_lens [B] int32.  Returns [B,Hq,D] float64."""
+    q = _u16(q); k_cache = _u16(k_cache); v_cache = _u16(v_cache)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, D = q.shape
+    P, ps, Hkv, D2 = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape and Hq % Hkv == 0
+    out = np.empty((B, Hq, D), dtype=np.float64)
+    bad = _load().oracle_decode_paged(_ptr(q), Hq * D, D, _ptr(k_cache), _ptr(v_cache), P,
+                                      _ptr(bt), bt.shape[1], _ptr(sl), B, Hq, Hkv, D, ps,
+                                      float(scale), _ptr(out))
+    if bad:
+        raise ValueError(f"{bad} output rows would read outside the given cache/table")
+    return out
+
+
+def decode_paged_rows(q, k_cache, v_cache, block_table, seq_lens, scale: float,
+                      rows) -> np.ndarray:
+    """Selected output rows of paged decode; rows[i] = b * Hq + h.  Returns [n, D]."""
+    q = _u16(q); k_cache = _u16(k_cache); v_cache = _u16(v_cache)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    B, Hq, D = q.shape
+    P, ps, Hkv, _ = k_cache.shape
+    out = np.empty((rows.shape[0], D), dtype=np.float64)
+    bad = _load().oracle_decode_paged_rows(_ptr(q), Hq * D, D, _ptr(k_cache), _ptr(v_cache),
+                                           P, _ptr(bt), bt.shape[1], _ptr(sl), B, Hq, Hkv, D,
+                                           ps, float(scale), _ptr(rows), rows.shape[0],
+                                           _ptr(out))
+    if bad:
+        raise ValueError(f"{bad} output rows would read outside the given cache/table")
+    return out
+
+
+def decode_contig(q, k, v, seq_lens, scale: float) -> np.ndarray:
+    """Contiguous GQA decode.  k, v [B,max_len,Hkv,D] u16.  Returns [B,Hq,D] float64."""
+    q = _u16(q); k = _u16(k); v = _u16(v)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, D = q.shape
+    B2, max_len, Hkv, D2 = k.shape
+    assert B2 == B and D2 == D and v.shape == k.shape and Hq % Hkv == 0
+    out = np.empty((B, Hq, D), dtype=np.float64)
+    bad = _load().oracle_decode_contig(_ptr(q), Hq * D, D, _ptr(k), _ptr(v), max_len,
+                                       _ptr(sl), B, Hq, Hkv, D, float(scale), _ptr(out))
+    if bad:
+        raise ValueError(f"{bad} sequences are longer than the contiguous cache")
+    return out
+
+
+def fp8_swa(q, kv_cache, inv_scale, indices, lens, block_size: int, scale: float,
+            tokens: tuple[int, int] | None = None) -> np.ndarray:
+    """fp8 sliding-window latent decode (K = V).  q [T,NH,HD] u16; kv_cache
+    [num_blocks,block_size,HD] u8; inv_scale [num_blocks*block_size] (or [...,1]) u16;
+    indices [T,W] int64; lens [T] int64.  Returns [T,NH,HD] float64 (only the rows of
+    ``tokens`` = (t0, t1) are filled when given; the rest are NaN)."""
+    q = _u16(q)
+    cache = np.ascontiguousarray(kv_cache, dtype=np.uint8)
+    inv = _u16(np.asarray(inv_scale).reshape(-1))
+    idx = np.ascontiguousarray(indices, dtype=np.int64)
+    ln = np.ascontiguousarray(lens, dtype=np.int64)
+    T, NH, HD = q.shape
+    NB, bs, HD2 = cache.shape
+    assert HD2 == HD and int(block_size) == bs and inv.shape[0] >= NB * bs
+    W = idx.shape[1]
+    t0, t1 = (0, T) if tokens is None else tokens
+    out = np.full((T, NH, HD), np.nan, dtype=np.float64)
+    _load().oracle_fp8_swa_range(_ptr(q), _ptr(cache), _ptr(inv), _ptr(idx), _ptr(ln), T, NH,
+                                 HD, W, NB, bs, float(scale), int(t0), int(t1), _ptr(out))
+    return out

@@ -1,0 +1,337 @@
+"""Pins for the fp64 CPU oracle: each check ties it to something other than itself.
+
+* scalar conversions against torch's own conversions (bf16 bits, e4m3 codes, fp32->bf16);
+* closed forms of attention: constant V, a single key, a shift of every key, q = 0;
+* brute force against torch's float64 scaled_dot_product_attention (with its own GQA
+  head expansion) on logical K/V gathered here through the block table;
+* page-permutation invariance and paged == contiguous;
+* the fp8 sliding-window variant against the fallback's semantics written with torch ops
+  (float8_e4m3fn view, bf16 multiply, boolean mask, float64 SDPA), plus its closed forms.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from paged_kv_cache_298_gb300 import inputs
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def as_f64(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.float64).numpy()
+
+
+# ---- scalar conversions --------------------------------------------------------------
+
+def test_bf16_value_all_codes():
+    codes = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    want = codes.view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.bf16_value(c) for c in range(65536)])
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all()
+
+
+def test_e4m3_table_matches_torch_float8():
+    want = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn)
+    want = want.to(torch.float64).numpy()
+    got = oracle.e4m3_table()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    assert np.array_equal(got[~np.isnan(got)], want[~np.isnan(want)])
+    # two NaN codes (S.1111.111), largest finite 448, smallest subnormal 2^-9
+    assert np.isnan(got).sum() == 2 and got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_round_to_bf16_matches_torch():
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(4000, generator=g, dtype=torch.float32) * 3
+    # exact ties: 9 significant bits with the last one set
+    ties = torch.tensor([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -(2.0 + 2 ** -7), 0.5 + 2 ** -9])
+    x = torch.cat([x, ties])
+    want = x.to(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.round_to_bf16(float(v)) for v in x])
+    assert np.array_equal(got, want)
+
+
+# ---- paged decode: brute force against torch SDPA ------------------------------------
+
+def gather_logical(case):
+    """Logical [B][L_b, Hkv, D] float64 K and V, gathered here by a direct table walk."""
+    k = as_f64(case.k_cache.float())
+    v = as_f64(case.v_cache.float())
+    table = case.block_table.numpy()
+    ks, vs = [], []
+    for b in range(case.B):
+        L = int(case.seq_lens[b])
+        t = np.arange(L)
+        pages = table[b, t // case.page_size]
+        slots = t % case.page_size
+        ks.append(k[pages, slots])
+        vs.append(v[pages, slots])
+    return ks, vs
+
+
+def sdpa_reference(case):
+    q = as_f64(case.q.float())
+    ks, vs = gather_logical(case)
+    out = np.zeros((case.B, case.Hq, case.D))
+    for b in range(case.B):
+        if ks[b].shape[0] == 0:
+            continue
+        qb = torch.from_numpy(q[b])[:, None, :]                 # [Hq, 1, D]
+        kb = torch.from_numpy(ks[b]).permute(1, 0, 2)           # [Hkv, L, D]
+        vb = torch.from_numpy(vs[b]).permute(1, 0, 2)
+        o = F.scaled_dot_product_attention(qb[None], kb[None], vb[None], scale=case.scale,
+                                           enable_gqa=True)
+        out[b] = o[0, :, 0, :].numpy()
+    return out
+
+
+def run_oracle(case):
+    return oracle.decode_paged(bits(case.q), bits(case.k_cache), bits(case.v_cache),
+                               case.block_table.numpy(), case.seq_lens.numpy(), case.scale)
+
+
+SHAPES = [
+    # B, Hq, Hkv, D, ps, lens
+    (2, 4, 2, 64, 16, [37, 100]),
+    (3, 8, 8, 64, 1, [5, 1, 9]),
+    (2, 8, 2, 128, 3, [7, 20]),
+    (4, 16, 2, 32, 8, [1, 8, 9, 33]),
+    (1, 6, 3, 64, 64, [130]),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_paged_matches_torch_sdpa_float64(shape):
+    B, Hq, Hkv, D, ps, lens = shape
+    case = inputs.make_paged_case(B, Hq, Hkv, D, ps, lens, 11 + len(lens) + D)
+    got = run_oracle(case)
+    want = sdpa_reference(case)
+    assert np.isfinite(got).all()
+    np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12)
+
+
+def test_tiny_workload_matches_sdpa():
+    case = inputs.tiny_paged()
+    assert tuple(case.block_table.shape) == (2, 7) and case.num_pages == 16
+    np.testing.assert_allclose(run_oracle(case), sdpa_reference(case), rtol=1e-11, atol=1e-12)
+
+
+def test_head_mapping_is_consecutive_groups():
+    # Hq=4, Hkv=2: heads 0,1 read kv head 0 and heads 2,3 read kv head 1.  Make the kv
+    # heads' V constant and different; the outputs then name the kv head each q head used.
+    case = inputs.make_paged_case(1, 4, 2, 64, 16, [20], 5)
+    case.v_cache[:, :, 0, :] = 1.0
+    case.v_cache[:, :, 1, :] = -2.0
+    out = run_oracle(case)
+    np.testing.assert_allclose(out[0, :2], 1.0, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(out[0, 2:], -2.0, rtol=0, atol=1e-13)
+
+
+# ---- paged decode: closed forms -------------------------------------------------------
+
+def test_constant_v_gives_v():
+    case = inputs.make_paged_case(2, 8, 2, 64, 16, [50, 3], 21, poison=False)
+    row = inputs.randn_bf16((2, 64), torch.Generator().manual_seed(3), "cpu")
+    case.v_cache[:] = row[None, None]
+    out = run_oracle(case)
+    for h in range(8):
+        np.testing.assert_allclose(out[:, h], np.broadcast_to(as_f64(row.float())[h // 4], (2, 64)),
+                                   rtol=0, atol=1e-13)
+
+
+def test_single_key_returns_its_value_row():
+    case = inputs.make_paged_case(3, 4, 1, 64, 16, [1, 1, 1], 22)
+    out = run_oracle(case)
+    ks, vs = gather_logical(case)
+    for b in range(3):
+        for h in range(4):
+            assert np.array_equal(out[b, h], vs[b][0, 0])
+
+
+def test_key_shift_leaves_output_unchanged():
+    # Values on a quarter grid keep k + u exact in bf16, so the shift is exact.
+    g = torch.Generator().manual_seed(23)
+    case = inputs.make_paged_case(2, 4, 2, 64, 16, [40, 17], 23, poison=False)
+    case.k_cache.copy_((torch.randint(-4, 5, case.k_cache.shape, generator=g) / 4).to(torch.bfloat16))
+    base = run_oracle(case)
+    u = (torch.randint(-2, 3, (2, 64), generator=g)).to(torch.bfloat16)
+    shifted = case.k_cache + u[None, None]
+    assert torch.equal(shifted.float(), case.k_cache.float() + u.float()[None, None])
+    case.k_cache.copy_(shifted)
+    np.testing.assert_allclose(run_oracle(case), base, rtol=1e-12, atol=1e-13)
+
+
+def test_zero_query_gives_mean_of_values():
+    case = inputs.make_paged_case(2, 4, 2, 64, 16, [37, 100], 24)
+    case.q.zero_()
+    out = run_oracle(case)
+    _, vs = gather_logical(case)
+    for b in range(2):
+        for h in range(4):
+            np.testing.assert_allclose(out[b, h], vs[b][:, h // 2].mean(axis=0), rtol=1e-12,
+                                       atol=1e-13)
+
+
+def test_empty_sequence_gives_zero_row():
+    case = inputs.make_paged_case(2, 4, 2, 64, 16, [0, 19], 25)
+    out = run_oracle(case)
+    assert np.array_equal(out[0], np.zeros((4, 64)))
+    np.testing.assert_allclose(out[1], sdpa_reference(case)[1], rtol=1e-11, atol=1e-12)
+
+
+def test_scale_enters_once():
+    # Doubling q with half the scale gives the same logits.
+    case = inputs.make_paged_case(1, 4, 2, 64, 16, [30], 26)
+    case.q.copy_((case.q.float() / 2).to(torch.bfloat16) * 2)   # keep q exactly halvable
+    base = run_oracle(case)
+    q2 = case.q.float() * 2
+    out = oracle.decode_paged(bits(q2.to(torch.bfloat16)), bits(case.k_cache), bits(case.v_cache),
+                              case.block_table.numpy(), case.seq_lens.numpy(), case.scale / 2)
+    np.testing.assert_allclose(out, base, rtol=1e-12, atol=1e-13)
+
+
+# ---- paged decode: invariants ---------------------------------------------------------
+
+def test_physical_page_permutation_is_invisible():
+    case = inputs.make_paged_case(3, 8, 2, 64, 16, [37, 100, 64], 27)
+    base = run_oracle(case)
+    perm = torch.randperm(case.num_pages, generator=torch.Generator().manual_seed(99))
+    inv = torch.argsort(perm)
+    k2 = case.k_cache[perm]
+    v2 = case.v_cache[perm]
+    t2 = inv[case.block_table.long()].to(torch.int32)
+    out = oracle.decode_paged(bits(case.q), bits(k2), bits(v2), t2.numpy(), case.seq_lens.numpy(),
+                              case.scale)
+    assert np.array_equal(out, base)
+
+
+def test_paged_equals_contiguous():
+    case = inputs.make_paged_case(3, 8, 2, 64, 16, [37, 100, 1], 28)
+    k, v = inputs.logical_kv(case)
+    out = oracle.decode_contig(bits(case.q), bits(k), bits(v), case.seq_lens.numpy(), case.scale)
+    assert np.array_equal(out, run_oracle(case))
+
+
+def test_selected_rows_equal_full_rows():
+    case = inputs.make_paged_case(3, 8, 2, 64, 16, [37, 100, 5], 29)
+    full = run_oracle(case).reshape(-1, 64)
+    rows = np.array([0, 5, 23, 9, 16])
+    got = oracle.decode_paged_rows(bits(case.q), bits(case.k_cache), bits(case.v_cache),
+                                   case.block_table.numpy(), case.seq_lens.numpy(), case.scale, rows)
+    assert np.array_equal(got, full[rows])
+
+
+def test_out_of_range_page_is_reported():
+    case = inputs.make_paged_case(1, 4, 2, 64, 16, [20], 30)
+    case.block_table[0, 1] = case.num_pages
+    with pytest.raises(ValueError):
+        run_oracle(case)
+
+
+# ---- fp8 sliding-window latent decode ---------------------------------------------------
+
+def fp8_torch_semantics(case):
+    """The fallback's semantics written with torch ops: clamp the slot, split it into
+    block and offset, view the bytes as float8_e4m3fn, multiply in bf16 by the inverse
+    scale, mask j >= len and slot < 0, then float64 SDPA with K = V."""
+    T, NH, HD, W, bs = case.T, case.NH, case.HD, case.W, case.block_size
+    idx = case.indices
+    safe = idx.clamp(min=0)
+    rows = case.kv_cache[safe // bs, safe % bs]                       # [T, W, HD] u8
+    deq = rows.view(torch.float8_e4m3fn).to(torch.bfloat16) * case.inv_scale[safe]
+    deq = deq.to(torch.bfloat16)
+    masked = (torch.arange(W)[None, :] >= case.lens[:, None]) | (idx < 0)
+    kv = deq.to(torch.float64)
+    q = case.q.to(torch.float64)
+    out = torch.zeros(T, NH, HD, dtype=torch.float64)
+    for t in range(T):
+        keep = ~masked[t]
+        if keep.sum() == 0:
+            continue
+        o = F.scaled_dot_product_attention(q[t][:, None, :], kv[t][keep][None],
+                                           kv[t][keep][None], scale=case.scale)
+        out[t] = o[:, 0, :]
+    return out.numpy()
+
+
+def run_fp8(case):
+    return oracle.fp8_swa(bits(case.q), case.kv_cache.numpy(), bits(case.inv_scale),
+                          case.indices.numpy(), case.lens.numpy(), case.block_size, case.scale)
+
+
+@pytest.mark.parametrize("shape", [(6, 16, 64, 4, 32, 16), (3, 8, 128, 2, 64, 40),
+                                   (4, 128, 512, 2, 256, 128)])
+def test_fp8_matches_torch_semantics(shape):
+    T, NH, HD, NB, bs, W = shape
+    case = inputs.make_fp8_case(T, NH, HD, NB, bs, W, 31 + HD)
+    # exercise the -1 padding inside the window too, not only after len
+    case.indices[0, 0] = -1
+    got = run_fp8(case)
+    np.testing.assert_allclose(got, fp8_torch_semantics(case), rtol=1e-11, atol=1e-12)
+
+
+def test_fp8_masked_rows_do_not_matter():
+    case = inputs.make_fp8_case(4, 16, 64, 4, 32, 16, 41, lens=[3, 16, 1, 8])
+    base = run_fp8(case)
+    # rewrite every cache row that no token attends to
+    used = set()
+    for t in range(4):
+        for j in range(int(case.lens[t])):
+            if case.indices[t, j] >= 0:
+                used.add(int(case.indices[t, j]))
+    flat = case.kv_cache.view(-1, 64)
+    for s in range(flat.shape[0]):
+        if s not in used:
+            flat[s] = 0x7E
+    # and what sits in the window past len
+    case.indices[0, 3:] = 5
+    assert np.array_equal(run_fp8(case), base)
+
+
+def test_fp8_single_row_and_constant_rows():
+    case = inputs.make_fp8_case(2, 8, 64, 2, 16, 8, 42, lens=[1, 8])
+    out = run_fp8(case)
+    s0 = int(case.indices[0, 0])
+    row = case.kv_cache.view(-1, 64)[s0].view(torch.float8_e4m3fn).to(torch.float64)
+    inv = float(case.inv_scale[s0, 0].float())
+    want = np.array([oracle.round_to_bf16(float(x) * inv) for x in row])
+    for h in range(8):
+        assert np.array_equal(out[0, h], want)
+    # token 1: every slot holds the same bytes and scale -> output is that row
+    flat = case.kv_cache.view(-1, 64)
+    for j in range(8):
+        s = int(case.indices[1, j])
+        flat[s] = flat[s0]
+        case.inv_scale[s] = case.inv_scale[s0]
+    out = run_fp8(case)
+    for h in range(8):
+        np.testing.assert_allclose(out[1, h], want, rtol=0, atol=1e-13)
+
+
+def test_fp8_empty_window_gives_zero():
+    case = inputs.make_fp8_case(3, 8, 64, 2, 16, 8, 43, lens=[0, 4, 2])
+    case.indices[1, :] = -1
+    out = run_fp8(case)
+    assert np.array_equal(out[0], np.zeros((8, 64))) and np.array_equal(out[1], np.zeros((8, 64)))
+    assert np.abs(out[2]).sum() > 0
+
+
+def test_fp8_with_unit_scales_is_mqa_decode():
+    # inv_scale = 1 and full windows: the variant is single-kv-head decode with K = V over
+    # the dequantised rows, which the (separately pinned) bf16 path also computes.
+    case = inputs.make_fp8_case(2, 8, 64, 2, 16, 8, 44, lens=[8, 8])
+    case.inv_scale[:] = 1.0
+    out = run_fp8(case)
+    flat = case.kv_cache.view(-1, 64)
+    rows = flat[case.indices.clamp(min=0)].view(torch.float8_e4m3fn).to(torch.bfloat16)  # [T,W,HD]
+    k = rows[:, :, None, :].contiguous()                                  # [T, W, 1, HD]
+    got = oracle.decode_contig(bits(case.q), bits(k), bits(k),
+                               np.full(2, 8, dtype=np.int32), case.scale)
+    np.testing.assert_allclose(out, got, rtol=1e-12, atol=1e-13)
