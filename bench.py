@@ -1,0 +1,402 @@
+#!/usr/bin/env python3
+"""Benchmark of paged GQA decode attention on GB300.
+
+One step = one decode_attn_paged call (split kernel + combine kernel) over the whole batch
+of the large ragged workload: B=128 sequences, Hq=32, Hkv=8, D=128, kv_len ~ U{256..4096},
+page_size 16, pages assigned by a seeded shuffle of a 2x pool.  Inputs are resident in HBM
+before the timed region; two (or more) independent copies of every input are rotated so
+that the bytes touched between two reads of the same copy exceed 2x L2 (cold KV).
+
+Printed (rank 0, one JSON line): achieved HBM GB/s of algorithmic bytes (K/V rows inside
+seq_lens, q, out, the block-table entries used, seq_lens) per step time, with the split
+kernel's own roofline, an end-to-end figure through host buffers, the fp64 oracle on a
+bounded sample of the same workload on the host cores, and the SM clocks seen meanwhile.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference] [--workload W]
+
+With N > 1 (torchrun, one process per GPU) every rank runs an independent replica (the
+path has no cross-GPU exchange); value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---- helpers -----------------------------------------------------------------------------
+
+def rank_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.idx), "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                c = [x.strip() for x in line.split(",")]
+                if len(c) < 9:
+                    continue
+                try:
+                    sm.append(float(c[1]))
+                    mx = float(c[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, c[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_298_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_key: str):
+    """DRAM bytes per split-kernel launch from the committed ncu summary, if it was taken
+    on the current kernel source for this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload_key)
+        if e and e.get("source_sha") == kernel_source_sha():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---- workloads ---------------------------------------------------------------------------
+
+def make_workload(name: str, device):
+    from paged_kv_cache_298_gb300 import inputs
+    if name == "ragged":
+        return inputs.ragged_paged(device=device)
+    if name == "llama":
+        return inputs.llama_paged(device=device)
+    if name in ("long1", "long4"):
+        return inputs.long_paged(B=int(name[-1]), device=device)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def algorithmic_bytes(case, rows=None) -> int:
+    """K/V rows inside seq_lens + q + out + block-table entries used + seq_lens.
+    `rows`: restrict to these sequences (for a CPU sample)."""
+    lens = case.seq_lens.cpu().to(torch.int64)
+    if rows is not None:
+        lens = lens[rows]
+    B = lens.numel()
+    kv = int(lens.sum()) * case.Hkv * case.D * 2 * 2
+    qo = 2 * B * case.Hq * case.D * 2
+    pages = int(((lens + case.page_size - 1) // case.page_size).sum()) * 4
+    return kv + qo + pages + B * 4
+
+
+def workload_config(case, S, copies, footprint):
+    lens = case.seq_lens.cpu()
+    return {"workload": case.name, "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "D": case.D,
+            "page_size": case.page_size, "kv_len_min": int(lens.min()), "kv_len_max": int(lens.max()),
+            "total_kv": int(lens.to(torch.int64).sum()), "num_splits": S, "kv_dtype": "bf16",
+            "cold_kv": f"{copies} rotated input copies of {footprint / 1e9:.2f} GB each (> 2x L2)"}
+
+
+# ---- the CPU oracle (reference arm and cpu_baseline) -------------------------------------
+
+class OracleRunner:
+    def __init__(self, case):
+        import oracle
+        self.oracle = oracle
+        self.case = case
+        self.q = bits(case.q)
+        self.k = bits(case.k_cache)
+        self.v = bits(case.v_cache)
+        self.table = case.block_table.cpu().numpy()
+        self.lens = case.seq_lens.cpu().numpy()
+
+    def run(self, rows):
+        """Oracle on the sequences `rows` (all heads).  Returns seconds."""
+        c = self.case
+        q = np.ascontiguousarray(self.q[rows])
+        t0 = time.perf_counter()
+        self.oracle.decode_paged(q, self.k, self.v, np.ascontiguousarray(self.table[rows]),
+                                 np.ascontiguousarray(self.lens[rows]), c.scale)
+        return time.perf_counter() - t0
+
+    def sample_rows(self, target_s: float):
+        """A prefix of the batch sized for about target_s seconds of oracle time."""
+        n = 1
+        dt = self.run(np.arange(1))
+        B = self.case.B
+        n = int(max(1, min(B, target_s / max(dt, 1e-4))))
+        return np.arange(n)
+
+
+def cpu_baseline(case, target_s=12.0):
+    r = OracleRunner(case)
+    rows = r.sample_rows(target_s / 2)
+    dt = r.run(rows)
+    nbytes = algorithmic_bytes(case, torch.as_tensor(rows))
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": r.oracle.num_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle (OpenMP) on sequences 0..{len(rows) - 1} of {case.B} (all heads), one pass,"
+                      f" {dt:.1f} s"}
+
+
+# ---- our arm -----------------------------------------------------------------------------
+
+def run_ours(args):
+    from paged_kv_cache_298_gb300 import binding
+    import torch.distributed as dist
+
+    rank, local, world = rank_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    binding.load()
+    case = make_workload(args.workload, dev)
+    hbm_peak, peak_src = peaks()
+    sms = binding.device_sm_count()
+    S = args.splits or binding.plan_splits(sms, case.B, case.Hq, case.Hkv, case.D, case.page_size,
+                                           case.max_kv_len, case.total_kv)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    footprint = sum(t.numel() * t.element_size() for t in (case.q, case.k_cache, case.v_cache,
+                                                           case.block_table, case.seq_lens))
+    copies = 1 + max(1, math.ceil(2 * l2 / footprint))
+    sets = [case] + [type(case)(case.q.clone(), case.k_cache.clone(), case.v_cache.clone(),
+                                case.block_table.clone(), case.seq_lens.clone(), case.page_size, case.scale,
+                                case.name) for _ in range(copies - 1)]
+    ws = [torch.empty(max(1, binding.workspace_bytes(case.B, case.Hq, case.D, S)), dtype=torch.uint8, device=dev)
+          for _ in sets]
+    outs = [torch.empty_like(case.q) for _ in sets]
+    maxlen = case.max_kv_len
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        c = sets[i % copies]
+        binding.decode_attn_paged(c.q, c.k_cache, c.v_cache, c.block_table, c.seq_lens, max_kv_len=maxlen,
+                                  scale=c.scale, num_splits=S, workspace=ws[i % copies], out=outs[i % copies])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if binding.get_device_errors(clear=True):
+        raise SystemExit("device error word set during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for i in range(K):
+        binding.set_trace_events(*ev[i])
+        step(i)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    binding.set_trace_events()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end) / K
+    split_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    combine_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    errs = binding.get_device_errors(clear=True)
+
+    # end to end through host buffers: q, block table and seq_lens in, out back, every step
+    from paged_kv_cache_298_gb300 import binding as b2
+    hq = case.q.cpu().pin_memory()
+    ht = case.block_table.cpu().pin_memory()
+    hl = case.seq_lens.cpu().pin_memory()
+    ho = torch.empty(case.q.shape, dtype=torch.bfloat16).pin_memory()
+    dq = [s.q for s in sets]
+    dt_ = [s.block_table for s in sets]
+    dl = [s.seq_lens for s in sets]
+
+    def e2e_step(i):
+        j = i % copies
+        dq[j].copy_(hq, non_blocking=True)
+        dt_[j].copy_(ht, non_blocking=True)
+        dl[j].copy_(hl, non_blocking=True)
+        c = sets[j]
+        b2.decode_attn_paged(dq[j], c.k_cache, c.v_cache, dt_[j], dl[j], max_kv_len=maxlen, scale=c.scale,
+                             num_splits=S, workspace=ws[j], out=outs[j])
+        ho.copy_(outs[j], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(K):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e2e_ms = e0.elapsed_time(e1) / K
+
+    nbytes = algorithmic_bytes(case)
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = t.tolist()
+    value = world * nbytes / (ms * 1e-3) / 1e9
+    e2e_value = world * nbytes / (e2e_ms * 1e-3) / 1e9
+    achieved = nbytes / (split_ms * 1e-3) / 1e9
+    line = {
+        "metric": "paged decode attention achieved HBM GB/s (algorithmic bytes), cold KV",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "us_per_call": round(ms * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(case, S, copies, footprint),
+        "pct_of_peak": round(100 * value / world / hbm_peak, 1),
+        "roofline": {"bound": "hbm", "kernel": "split_kernel", "achieved": round(achieved, 1),
+                     "peak": hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "split_kernel_ms": round(split_ms, 5),
+                     "combine_ms": round(combine_ms, 5), "algorithmic_bytes_per_launch": nbytes,
+                     "traffic": recorded_traffic(args.workload)},
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": hq.numel() * 2 + ht.numel() * 4 + hl.numel() * 4,
+                "d2h_bytes_per_step": ho.numel() * 2},
+        "gpu_launches": K * (2 if S > 1 else 1),
+        "device_errors": errs,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---- reference arm: the fp64 oracle on the host cores ----------------------------------
+
+def run_reference(args):
+    rank, _, world = rank_info()
+    if rank != 0:
+        return
+    case = make_workload(args.workload, "cpu")
+    r = OracleRunner(case)
+    rows = r.sample_rows(target_s=min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        r.run(rows)
+    times = [r.run(rows) for _ in range(args.steps)]
+    dt = statistics.mean(times)
+    nbytes = algorithmic_bytes(case, torch.as_tensor(rows))
+    value = nbytes / dt / 1e9
+    sample = (f"fp64 oracle (OpenMP) on sequences 0..{len(rows) - 1} of {case.B} (all heads) per step")
+    line = {
+        "impl": "reference",
+        "metric": "paged decode attention achieved HBM GB/s (algorithmic bytes), cold KV",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": workload_config(case, 0, 1, 0) | {"sample_sequences": len(rows)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": r.oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ragged", choices=["ragged", "llama", "long1", "long4"])
+    ap.add_argument("--splits", type=int, default=0, help="0 = planner")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+/*
+ * dap.h -- C ABI of the paged decode-attention library for NVIDIA GB300 (sm_103a).
+ *
+ * Single-token GQA decode attention over a paged KV cache, its contiguous-cache form,
+ * and the fp8 sliding-window latent (K = V) variant.  Plain pointers and sizes only.
+ *
+ * Conventions shared by every entry point:
+ *   - The caller owns every buffer.  The library allocates no device memory and never
+ *     synchronises the stream; all work is enqueued on `stream` (a cudaStream_t passed
+ *     as void*, NULL = the legacy default stream).
+ *   - "device" marks a device pointer; "host" a host value.  bf16 buffers are raw
+ *     IEEE bfloat16 bit patterns (passed as void*).
+ *   - Errors that the host can see (null pointers, bad sizes, unsupported shapes,
+ *     misaligned pointers, a workspace that is too small) are returned as a dap_status
+ *     before anything is launched.  A failed launch returns DAP_ERR_CUDA.
+ *   - Errors that only the device can see (a page index outside the pool, a sequence
+ *     length outside [0, max_kv_len], an fp8 slot outside the cache, a pipeline wait
+ *     that timed out) never trap: the kernel records a bit in a library-wide device
+ *     error word (read it with dap_get_device_errors) and keeps every access in bounds.
+ *
+ * Sources of the operation (web pages the library follows):
+ *   [A] AstrAI "CUDA Kernels" developer doc: section "Python Wrappers" (q/k/v are
+ *       [batch, seq_len, n_heads, head_dim], scale 1/sqrt(head_dim)) and section
+ *       "Q Scheduling and KV Addressing" (a KV policy translates a logical position to
+ *       a physical address; ContigKV / PagedKV).
+ *   [B] AstrAI csrc commit log: the split-KV commit (partition KV across blocks that
+ *       emit unnormalised (O, m, l) partials, merged by a combine kernel; split count
+ *       chosen to fill the device, single pass when batch*kv_head already fills it),
+ *       the split-planner commit (bandwidth saturates near 256-512 blocks), the
+ *       per-element page lookup commit (any page_size), the numerics commit (fmaf for
+ *       V accumulation, divide guard 1e-20, atol = rtol = 0.01).
+ *   [C] nvfp4-megamoe-kernel cutedsl/native_swa_decode.py: native_swa_decode_attention
+ *       and _fallback_batched_sdp (fp8 K = V sliding-window decode semantics).
+ */
+#ifndef DAP_H_
+#define DAP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DAP_OK = 0,
+    DAP_ERR_NULL = 1,        /* a required pointer is NULL */
+    DAP_ERR_SHAPE = 2,       /* a size or stride is out of range or inconsistent */
+    DAP_ERR_UNSUPPORTED = 3, /* a valid shape this build has no kernel for */
+    DAP_ERR_WORKSPACE = 4,   /* workspace missing or smaller than dap_workspace_bytes */
+    DAP_ERR_ALIGN = 5,       /* a pointer or stride breaks the 16-byte rule */
+    DAP_ERR_CUDA = 6         /* a CUDA runtime call or launch failed */
+} dap_status;
+
+/* Bits of the device error word. */
+#define DAP_DEVERR_TIMEOUT 0x1u  /* a pipeline wait gave up; the launch's output is invalid */
+#define DAP_DEVERR_SEQLEN 0x2u   /* seq_lens[b] < 0 or > max_kv_len; clamped */
+#define DAP_DEVERR_PAGE 0x4u     /* block_table entry outside [0, num_pages); read as zeros */
+#define DAP_DEVERR_SLOT 0x8u     /* fp8 slot index >= num_blocks*block_size; row skipped */
+
+/* Human-readable name of a status code.  Never NULL. */
+const char *dap_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int dap_version(void);
+
+/* Number of SMs of the current CUDA device (cudaDevAttrMultiProcessorCount), or -1 when
+ * no device is usable. */
+int dap_device_sm_count(void);
+
+/*
+ * Split planner [B: split-KV and split-planner commits].
+ * Returns the number of KV splits S >= 1 of the LONGEST sequence.  Every sequence is cut
+ * into chunks of `dap_chunk_tokens(max_kv_len, S)` tokens, so sequence b runs
+ * ceil(seq_lens[b] / chunk) splits (at least 1).  The plan fills `sm_count` SMs with
+ * work units of balanced size: it aims for enough (sequence, kv head, chunk) units that
+ * the largest unit is a small fraction of one SM's share of the KV bytes, and returns 1
+ * when batch*kv_heads units already fill the device.
+ *   sm_count   SMs available (dap_device_sm_count()).
+ *   total_kv   sum of seq_lens (host); 0 means "unknown", taken as B * max_kv_len.
+ * Pure host function; no CUDA call.
+ */
+int dap_plan_splits(int sm_count, int B, int Hq, int Hkv, int D, int page_size,
+                    int max_kv_len, long long total_kv);
+
+/* Tokens per split chunk for a plan: ceil(max_kv_len / num_splits) rounded up to the
+ * kernel's tile of 32 tokens (at least 32).  Pure host function. */
+int dap_chunk_tokens(int max_kv_len, int num_splits);
+
+/* Workspace bytes decode_attn_paged / decode_attn_contig need for `num_splits` splits:
+ * 0 when num_splits <= 1, else room for B*num_splits*Hq partial rows of (D + 2) floats
+ * (unnormalised acc, running max m, running sum l).  Pure host function. */
+size_t dap_workspace_bytes(int B, int Hq, int D, int num_splits);
+
+/*
+ * Paged GQA decode attention [A][B].
+ *   out[b,h,:] = sum_t softmax_t(scale * q[b,h,:] . K[b,t,h/G,:]) V[b,t,h/G,:],
+ *   t < seq_lens[b], G = Hq / Hkv (consecutive query heads share a kv head).
+ *
+ *   q            device bf16 [B, Hq, D], element strides (q_stride_b, q_stride_h, 1).
+ *   k_cache,     device bf16 [num_pages, page_size, Hkv, D], contiguous: logical position
+ *   v_cache      t of sequence b lives in page block_table[b, t / page_size], slot
+ *                t % page_size.
+ *   block_table  device int32 [B, max_pages], row-major.  Entries past a sequence's
+ *                last page are never read.
+ *   seq_lens     device int32 [B].  Each entry must lie in [0, max_kv_len].
+ *   max_kv_len   host: an upper bound of seq_lens (<= max_pages * page_size); it sets
+ *                the chunk length of the split plan.
+ *   scale        softmax scale applied in fp32 to q . k (normally 1/sqrt(D)).
+ *   num_splits   splits of the longest sequence; 0 = dap_plan_splits(...) with
+ *                total_kv unknown.
+ *   workspace    device scratch of at least dap_workspace_bytes(B, Hq, D, S) bytes,
+ *                16-byte aligned (may be NULL when S == 1).  Needs no initialisation;
+ *                its contents are undefined afterwards.
+ *   out          device bf16 [B, Hq, D], element strides (out_stride_b, out_stride_h, 1).
+ *                Written in full (an empty sequence gives a zero row).
+ *   Supported: D in {64, 128}; G in {1, 2, 4, 8}; any page_size >= 1.  q, out,
+ *   k_cache and v_cache 16-byte aligned; q/out strides multiples of 8 elements.
+ *   The result is bit-identical under any permutation of the physical pages for a fixed
+ *   num_splits (the summation order depends only on logical positions).
+ */
+dap_status decode_attn_paged(const void *q, long long q_stride_b, long long q_stride_h,
+                             const void *k_cache, const void *v_cache, int num_pages,
+                             int page_size, const int32_t *block_table, int max_pages,
+                             const int32_t *seq_lens, int max_kv_len, int B, int Hq, int Hkv,
+                             int D, float scale, int num_splits, void *workspace,
+                             size_t workspace_bytes, void *out, long long out_stride_b,
+                             long long out_stride_h, void *stream);
+
+/*
+ * Contiguous-cache GQA decode attention [A: ContigKV]: the same operation with
+ * k, v device bf16 [B, max_len, Hkv, D] contiguous; position t of sequence b is row
+ * (b, t).  seq_lens[b] must lie in [0, max_kv_len] and max_kv_len <= max_len.
+ * Everything else as decode_attn_paged.
+ */
+dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_stride_h,
+                              const void *k, const void *v, int max_len,
+                              const int32_t *seq_lens, int max_kv_len, int B, int Hq, int Hkv,
+                              int D, float scale, int num_splits, void *workspace,
+                              size_t workspace_bytes, void *out, long long out_stride_b,
+                              long long out_stride_h, void *stream);
+
+/*
+ * fp8 sliding-window latent decode, K = V [C].
+ *   For token t and window position j < W, slot = slot_idx[t, j]; the row takes part iff
+ *   j < lens[t] and slot >= 0.  Its value is bf16(e4m3(kv_cache[slot / block_size,
+ *   slot % block_size, :]) * inv_scale[slot]) (the fp8 code times the bf16 inverse scale,
+ *   rounded to bf16).  out[t, h, :] = sum_j softmax_j(scale * q[t,h,:] . kv_j) kv_j;
+ *   a token with no row gives a zero row.
+ *
+ *   q          device bf16 [T, NH, HD] contiguous.
+ *   kv_cache   device uint8 [num_blocks, block_size, HD] contiguous, OCP e4m3 (E4M3FN) codes.
+ *   inv_scale  device bf16 [num_blocks * block_size] (one per slot).
+ *   slot_idx   device int64 [T, W] row-major, -1 = padding.
+ *   lens       device int64 [T].
+ *   out        device bf16 [T, NH, HD] contiguous.
+ *   Supported: HD = 512, NH a multiple of 64 (NH <= 1024), 1 <= W <= 256.
+ *   Slots >= num_blocks*block_size are skipped and flagged (DAP_DEVERR_SLOT).
+ */
+dap_status decode_attn_paged_fp8(const void *q, const uint8_t *kv_cache, const void *inv_scale,
+                                 const int64_t *slot_idx, const int64_t *lens, int T, int NH,
+                                 int HD, int W, int num_blocks, int block_size, float scale,
+                                 void *out, void *stream);
+
+/* Tracing hook.  When set (non-NULL cudaEvent_t handles passed as void*), every following
+ * decode_attn_paged / decode_attn_contig call records `split_begin` just before its split
+ * kernel, `split_end` just after it and `combine_end` after the combine kernel (or right
+ * after split_end when there is none), all on the call's stream.  Pass NULLs to turn it
+ * off.  Process-wide, not thread-safe; meant for benchmarks and profilers. */
+void dap_set_trace_events(void *split_begin, void *split_end, void *combine_end);
+
+/* Read (and, when `clear` is nonzero, reset) the device error word of the current
+ * device.  Synchronises the device.  Returns DAP_ERR_CUDA if the read fails. */
+dap_status dap_get_device_errors(unsigned int *flags, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DAP_H_ */

@@ -1,0 +1,237 @@
+"""Thin Python binding of the C ABI in include/dap.h (ctypes; argument marshalling only).
+
+Every function here takes torch tensors, checks dtypes and devices, and passes raw
+pointers, sizes and the current CUDA stream to ``libdap.so``.  All arithmetic runs in the
+library's CUDA kernels: there is no fallback, and a missing or unloadable library raises
+``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libdap.so")
+_lock = threading.Lock()
+_lib = None
+
+DAP_OK = 0
+STATUS_NAMES = {0: "DAP_OK", 1: "DAP_ERR_NULL", 2: "DAP_ERR_SHAPE", 3: "DAP_ERR_UNSUPPORTED",
+                4: "DAP_ERR_WORKSPACE", 5: "DAP_ERR_ALIGN", 6: "DAP_ERR_CUDA"}
+DEVERR_TIMEOUT, DEVERR_SEQLEN, DEVERR_PAGE, DEVERR_SLOT = 0x1, 0x2, 0x4, 0x8
+
+# every symbol include/dap.h declares
+EXPORTS = ("dap_status_string", "dap_version", "dap_device_sm_count", "dap_plan_splits",
+           "dap_chunk_tokens", "dap_workspace_bytes", "decode_attn_paged", "decode_attn_contig",
+           "decode_attn_paged_fp8", "dap_set_trace_events", "dap_get_device_errors")
+
+
+class DapError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load(build_if_missing: bool = True):
+    """Load libdap.so (building it with nvcc when absent or stale, if allowed)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_missing:
+            from . import build as _build
+            try:
+                _build.build()
+            except Exception as e:  # no nvcc or a compile error: fail loudly
+                if not os.path.exists(_LIB_PATH):
+                    raise RuntimeError(f"libdap.so is missing and could not be built: {e}") from e
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libdap.so not found at {_LIB_PATH}; run __graft_entry__.build()")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, LL, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float, ctypes.c_size_t
+        lib.dap_status_string.argtypes = [I]
+        lib.dap_status_string.restype = ctypes.c_char_p
+        lib.dap_version.argtypes = []
+        lib.dap_version.restype = I
+        lib.dap_device_sm_count.argtypes = []
+        lib.dap_device_sm_count.restype = I
+        lib.dap_plan_splits.argtypes = [I, I, I, I, I, I, I, LL]
+        lib.dap_plan_splits.restype = I
+        lib.dap_chunk_tokens.argtypes = [I, I]
+        lib.dap_chunk_tokens.restype = I
+        lib.dap_workspace_bytes.argtypes = [I, I, I, I]
+        lib.dap_workspace_bytes.restype = SZ
+        lib.decode_attn_paged.argtypes = [P, LL, LL, P, P, I, I, P, I, P, I, I, I, I, I, F, I, P, SZ,
+                                          P, LL, LL, P]
+        lib.decode_attn_paged.restype = I
+        lib.decode_attn_contig.argtypes = [P, LL, LL, P, P, I, P, I, I, I, I, I, F, I, P, SZ, P, LL,
+                                           LL, P]
+        lib.decode_attn_contig.restype = I
+        lib.decode_attn_paged_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P, P]
+        lib.decode_attn_paged_fp8.restype = I
+        lib.dap_set_trace_events.argtypes = [P, P, P]
+        lib.dap_set_trace_events.restype = None
+        lib.dap_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
+        lib.dap_get_device_errors.restype = I
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().dap_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != DAP_OK:
+        raise DapError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+# ---- host planning -------------------------------------------------------------------
+
+def device_sm_count() -> int:
+    return load().dap_device_sm_count()
+
+
+def plan_splits(sm_count, B, Hq, Hkv, D, page_size, max_kv_len, total_kv=0) -> int:
+    return load().dap_plan_splits(sm_count, B, Hq, Hkv, D, page_size, max_kv_len, total_kv)
+
+
+def chunk_tokens(max_kv_len, num_splits) -> int:
+    return load().dap_chunk_tokens(max_kv_len, num_splits)
+
+
+def workspace_bytes(B, Hq, D, num_splits) -> int:
+    return load().dap_workspace_bytes(B, Hq, D, num_splits)
+
+
+def set_trace_events(split_begin=None, split_end=None, combine_end=None):
+    """Record torch.cuda.Event objects around the next calls' split / combine kernels."""
+    h = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)
+    load().dap_set_trace_events(h(split_begin), h(split_end), h(combine_end))
+
+
+def get_device_errors(clear: bool = True) -> int:
+    v = ctypes.c_uint(0)
+    _check(load().dap_get_device_errors(ctypes.byref(v), int(clear)), "dap_get_device_errors")
+    return v.value
+
+
+# ---- decode entry points ---------------------------------------------------------------
+
+def _bf16_3d(t, name):
+    _need(t.dtype == torch.bfloat16 and t.dim() == 3 and t.stride(2) == 1,
+          f"{name} must be a bf16 [*, *, D] tensor with unit stride in D")
+
+
+def decode_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, max_kv_len: int,
+                      scale: float | None = None, num_splits: int = 0, workspace=None, out=None,
+                      stream=None):
+    """Paged GQA decode (include/dap.h: decode_attn_paged).  Returns ``out`` [B, Hq, D]."""
+    _bf16_3d(q, "q")
+    B, Hq, D = q.shape
+    _need(k_cache.dtype == torch.bfloat16 and k_cache.dim() == 4 and k_cache.is_contiguous()
+          and v_cache.shape == k_cache.shape and v_cache.dtype == torch.bfloat16
+          and v_cache.is_contiguous(), "k_cache/v_cache must be contiguous bf16 [P, ps, Hkv, D]")
+    P, ps, Hkv, D2 = k_cache.shape
+    _need(D2 == D, "head dims differ")
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
+          and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
+    _need(seq_lens.dtype == torch.int32 and seq_lens.numel() == B and seq_lens.is_contiguous(),
+          "seq_lens must be contiguous int32 [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    _bf16_3d(out, "out")
+    lib = load()
+    S = num_splits if num_splits > 0 else lib.dap_plan_splits(lib.dap_device_sm_count(), B, Hq, Hkv, D,
+                                                              ps, int(max_kv_len), 0)
+    need = lib.dap_workspace_bytes(B, Hq, D, S)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.decode_attn_paged(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
+                               _ptr(block_table), block_table.shape[1], _ptr(seq_lens), int(max_kv_len),
+                               B, Hq, Hkv, D, float(scale), int(S), _ptr(workspace), wbytes, _ptr(out),
+                               out.stride(0), out.stride(1), _stream(stream))
+    _check(st, "decode_attn_paged")
+    return out
+
+
+def decode_attn_contig(q, k, v, seq_lens, *, max_kv_len: int, scale: float | None = None,
+                       num_splits: int = 0, workspace=None, out=None, stream=None):
+    """Contiguous-cache GQA decode (include/dap.h: decode_attn_contig); k, v [B, max_len, Hkv, D]."""
+    _bf16_3d(q, "q")
+    B, Hq, D = q.shape
+    _need(k.dtype == torch.bfloat16 and k.dim() == 4 and k.is_contiguous() and v.shape == k.shape
+          and v.dtype == torch.bfloat16 and v.is_contiguous() and k.shape[0] == B and k.shape[3] == D,
+          "k/v must be contiguous bf16 [B, max_len, Hkv, D]")
+    _, max_len, Hkv, _ = k.shape
+    _need(seq_lens.dtype == torch.int32 and seq_lens.numel() == B and seq_lens.is_contiguous(),
+          "seq_lens must be contiguous int32 [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    _bf16_3d(out, "out")
+    lib = load()
+    S = num_splits if num_splits > 0 else lib.dap_plan_splits(lib.dap_device_sm_count(), B, Hq, Hkv, D,
+                                                              max_len, int(max_kv_len), 0)
+    need = lib.dap_workspace_bytes(B, Hq, D, S)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.decode_attn_contig(_ptr(q), q.stride(0), q.stride(1), _ptr(k), _ptr(v), max_len,
+                                _ptr(seq_lens), int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S),
+                                _ptr(workspace), wbytes, _ptr(out), out.stride(0), out.stride(1),
+                                _stream(stream))
+    _check(st, "decode_attn_contig")
+    return out
+
+
+def decode_attn_paged_fp8(q, kv_cache, inv_scale, slot_idx, lens, *, scale: float | None = None,
+                          out=None, stream=None):
+    """fp8 sliding-window latent decode, K = V (include/dap.h: decode_attn_paged_fp8)."""
+    _need(q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(), "q must be contiguous bf16 [T, NH, HD]")
+    T, NH, HD = q.shape
+    _need(kv_cache.dtype == torch.uint8 and kv_cache.dim() == 3 and kv_cache.is_contiguous()
+          and kv_cache.shape[2] == HD, "kv_cache must be contiguous uint8 [num_blocks, block_size, HD]")
+    NB, bs, _ = kv_cache.shape
+    _need(inv_scale.dtype == torch.bfloat16 and inv_scale.is_contiguous() and inv_scale.numel() >= NB * bs,
+          "inv_scale must be contiguous bf16 with one entry per slot")
+    _need(slot_idx.dtype == torch.int64 and slot_idx.dim() == 2 and slot_idx.is_contiguous()
+          and slot_idx.shape[0] == T, "slot_idx must be contiguous int64 [T, W]")
+    _need(lens.dtype == torch.int64 and lens.numel() == T and lens.is_contiguous(), "lens must be int64 [T]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(HD)
+    if out is None:
+        out = torch.empty((T, NH, HD), dtype=torch.bfloat16, device=q.device)
+    _need(out.dtype == torch.bfloat16 and out.shape == q.shape and out.is_contiguous(), "out must match q")
+    st = load().decode_attn_paged_fp8(_ptr(q), _ptr(kv_cache), _ptr(inv_scale), _ptr(slot_idx), _ptr(lens),
+                                      T, NH, HD, slot_idx.shape[1], NB, bs, float(scale), _ptr(out),
+                                      _stream(stream))
+    _check(st, "decode_attn_paged_fp8")
+    return out

@@ -1,0 +1,272 @@
+// dap_api.cu -- the C ABI: argument validation, split planning, workspace sizing, the
+// device error word and the tensor-map encoder lookup.  Every host-detectable error is
+// returned before any CUDA call is made, so these checks also run on machines without
+// a GPU.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "dap.h"
+#include "dap_internal.h"
+
+namespace dap {
+
+TraceEvents g_trace = {nullptr, nullptr, nullptr};
+
+void *tensor_map_encoder() {
+    static void *fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = p;
+    });
+    return fn;
+}
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
+
+bool supported_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8; }
+
+// Shared checks of the two bf16 decode entry points.
+dap_status check_common(const void *q, long long q_sb, long long q_sh, const int32_t *seq_lens,
+                        int max_kv_len, int B, int Hq, int Hkv, int D, float scale, int num_splits,
+                        const void *out, long long o_sb, long long o_sh) {
+    if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || max_kv_len < 0 || num_splits < 0 ||
+        num_splits > 65536 || Hq % Hkv != 0 || !isfinite(scale) || q_sb < 0 || q_sh < 0 ||
+        o_sb < 0 || o_sh < 0)
+        return DAP_ERR_SHAPE;
+    if (B == 0) return DAP_OK;
+    if (!q || !seq_lens || !out) return DAP_ERR_NULL;
+    if (!(D == 64 || D == 128) || !supported_group(Hq / Hkv)) return DAP_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(out) || !aligned4(seq_lens) || (q_sb & 7) || (q_sh & 7) ||
+        (o_sb & 7) || (o_sh & 7))
+        return DAP_ERR_ALIGN;
+    return DAP_OK;
+}
+
+dap_status resolve_splits(int B, int Hq, int Hkv, int D, int page_size, int max_kv_len, int num_splits,
+                          void *workspace, size_t workspace_bytes, int *S_out, int *chunk_out) {
+    int S = num_splits;
+    if (S == 0) {
+        const int sms = dap_device_sm_count();
+        if (sms <= 0) return DAP_ERR_CUDA;
+        S = dap_plan_splits(sms, B, Hq, Hkv, D, page_size, max_kv_len, 0);
+    }
+    const int chunk = dap_chunk_tokens(max_kv_len, S);
+    // splits that could never hold a token are dropped: S chunks must cover max_kv_len
+    const int needed = max_kv_len > 0 ? (int)ceil_div_ll(max_kv_len, chunk) : 1;
+    S = std::max(1, std::min(S, needed));
+    if (S > 1) {
+        const size_t need = dap_workspace_bytes(B, Hq, D, S);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DAP_ERR_WORKSPACE;
+    }
+    *S_out = S;
+    *chunk_out = chunk;
+    return DAP_OK;
+}
+
+}  // namespace
+}  // namespace dap
+
+using namespace dap;
+
+extern "C" {
+
+const char *dap_status_string(int status) {
+    switch (status) {
+        case DAP_OK: return "ok";
+        case DAP_ERR_NULL: return "a required pointer is NULL";
+        case DAP_ERR_SHAPE: return "a size or stride is out of range or inconsistent";
+        case DAP_ERR_UNSUPPORTED: return "shape not supported by this build";
+        case DAP_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case DAP_ERR_ALIGN: return "pointer or stride breaks the 16-byte alignment rule";
+        case DAP_ERR_CUDA: return "a CUDA call or kernel launch failed";
+        default: return "unknown status";
+    }
+}
+
+int dap_version(void) { return 100; }
+
+int dap_device_sm_count(void) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return n;
+}
+
+int dap_chunk_tokens(int max_kv_len, int num_splits) {
+    const int S = std::max(1, num_splits);
+    const long long per = ceil_div_ll(std::max(1, max_kv_len), S);
+    const long long tiles = ceil_div_ll(per, kTileTokens);
+    return (int)std::max<long long>(kTileTokens, tiles * kTileTokens);
+}
+
+int dap_plan_splits(int sm_count, int B, int Hq, int Hkv, int D, int page_size, int max_kv_len,
+                    long long total_kv) {
+    (void)Hq;
+    (void)D;
+    (void)page_size;
+    if (sm_count <= 0 || B <= 0 || Hkv <= 0 || max_kv_len <= 0) return 1;
+    if (total_kv <= 0) total_kv = (long long)B * max_kv_len;
+    // KV rows (token x kv head) each SM streams if the work is spread evenly.  A work unit
+    // (sequence, kv head, chunk) should be a small fraction of that share so that the
+    // last units to finish leave little of the device idle; a unit also needs enough tiles
+    // to amortise its pipeline fill.
+    const long long share = ceil_div_ll(total_kv * Hkv, sm_count);
+    const long long min_chunk = 256;
+    const long long chunk_target = std::max(min_chunk, share / 16);
+    long long S = ceil_div_ll(max_kv_len, chunk_target);
+    const long long max_tiles = ceil_div_ll(max_kv_len, kTileTokens);
+    S = std::min(S, max_tiles);
+    S = std::min<long long>(S, 1024);
+    return (int)std::max<long long>(1, S);
+}
+
+size_t dap_workspace_bytes(int B, int Hq, int D, int num_splits) {
+    if (num_splits <= 1 || B <= 0 || Hq <= 0 || D <= 0) return 0;
+    return partial_acc_bytes(B, Hq, D, num_splits) + partial_ml_bytes(B, Hq, num_splits);
+}
+
+dap_status decode_attn_paged(const void *q, long long q_stride_b, long long q_stride_h,
+                             const void *k_cache, const void *v_cache, int num_pages, int page_size,
+                             const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                             int max_kv_len, int B, int Hq, int Hkv, int D, float scale,
+                             int num_splits, void *workspace, size_t workspace_bytes, void *out,
+                             long long out_stride_b, long long out_stride_h, void *stream) {
+    dap_status st = check_common(q, q_stride_b, q_stride_h, seq_lens, max_kv_len, B, Hq, Hkv, D,
+                                 scale, num_splits, out, out_stride_b, out_stride_h);
+    if (st != DAP_OK || B == 0) return st;
+    if (num_pages < 1 || page_size < 1 || max_pages < 1 ||
+        (long long)max_kv_len > (long long)max_pages * page_size)
+        return DAP_ERR_SHAPE;
+    if (!k_cache || !v_cache || !block_table) return DAP_ERR_NULL;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table)) return DAP_ERR_ALIGN;
+    DecodeArgs a;
+    a.paged = true;
+    a.q = q;
+    a.q_sb = q_stride_b;
+    a.q_sh = q_stride_h;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.num_pages = num_pages;
+    a.page_size = page_size;
+    a.max_len = 0;
+    a.block_table = block_table;
+    a.max_pages = max_pages;
+    a.seq_lens = seq_lens;
+    a.max_kv_len = max_kv_len;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.scale = scale;
+    a.workspace = workspace;
+    a.out = out;
+    a.o_sb = out_stride_b;
+    a.o_sh = out_stride_h;
+    st = resolve_splits(B, Hq, Hkv, D, page_size, max_kv_len, num_splits, workspace, workspace_bytes,
+                        &a.num_splits, &a.chunk);
+    if (st != DAP_OK) return st;
+    return launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_stride_h, const void *k,
+                              const void *v, int max_len, const int32_t *seq_lens, int max_kv_len,
+                              int B, int Hq, int Hkv, int D, float scale, int num_splits,
+                              void *workspace, size_t workspace_bytes, void *out,
+                              long long out_stride_b, long long out_stride_h, void *stream) {
+    dap_status st = check_common(q, q_stride_b, q_stride_h, seq_lens, max_kv_len, B, Hq, Hkv, D,
+                                 scale, num_splits, out, out_stride_b, out_stride_h);
+    if (st != DAP_OK || B == 0) return st;
+    if (max_len < 1 || max_kv_len > max_len) return DAP_ERR_SHAPE;
+    if (!k || !v) return DAP_ERR_NULL;
+    if (!aligned16(k) || !aligned16(v)) return DAP_ERR_ALIGN;
+    DecodeArgs a;
+    a.paged = false;
+    a.q = q;
+    a.q_sb = q_stride_b;
+    a.q_sh = q_stride_h;
+    a.k = k;
+    a.v = v;
+    a.num_pages = 0;
+    a.page_size = 0;
+    a.max_len = max_len;
+    a.block_table = nullptr;
+    a.max_pages = 0;
+    a.seq_lens = seq_lens;
+    a.max_kv_len = max_kv_len;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.scale = scale;
+    a.workspace = workspace;
+    a.out = out;
+    a.o_sb = out_stride_b;
+    a.o_sh = out_stride_h;
+    st = resolve_splits(B, Hq, Hkv, D, max_len, max_kv_len, num_splits, workspace, workspace_bytes,
+                        &a.num_splits, &a.chunk);
+    if (st != DAP_OK) return st;
+    return launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+dap_status decode_attn_paged_fp8(const void *q, const uint8_t *kv_cache, const void *inv_scale,
+                                 const int64_t *slot_idx, const int64_t *lens, int T, int NH, int HD,
+                                 int W, int num_blocks, int block_size, float scale, void *out,
+                                 void *stream) {
+    if (T < 0 || NH < 1 || HD < 1 || W < 1 || num_blocks < 1 || block_size < 1 || !isfinite(scale) ||
+        (long long)num_blocks * block_size > 0x7FFFFFFFLL)
+        return DAP_ERR_SHAPE;
+    if (T == 0) return DAP_OK;
+    if (!q || !kv_cache || !inv_scale || !slot_idx || !lens || !out) return DAP_ERR_NULL;
+    if (HD != 512 || NH % 64 != 0 || NH > 1024 || W > 256) return DAP_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(kv_cache) ||
+        (reinterpret_cast<uintptr_t>(inv_scale) & 1u) || (reinterpret_cast<uintptr_t>(slot_idx) & 7u) ||
+        (reinterpret_cast<uintptr_t>(lens) & 7u))
+        return DAP_ERR_ALIGN;
+    Fp8Args a;
+    a.q = q;
+    a.kv_cache = kv_cache;
+    a.inv_scale = inv_scale;
+    a.slot_idx = slot_idx;
+    a.lens = lens;
+    a.T = T;
+    a.NH = NH;
+    a.HD = HD;
+    a.W = W;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.scale = scale;
+    a.out = out;
+    return launch_fp8(a, static_cast<cudaStream_t>(stream));
+}
+
+void dap_set_trace_events(void *split_begin, void *split_end, void *combine_end) {
+    g_trace.split_begin = static_cast<cudaEvent_t>(split_begin);
+    g_trace.split_end = static_cast<cudaEvent_t>(split_end);
+    g_trace.combine_end = static_cast<cudaEvent_t>(combine_end);
+}
+
+dap_status dap_get_device_errors(unsigned int *flags, int clear) {
+    if (!flags) return DAP_ERR_NULL;
+    *flags = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return DAP_ERR_CUDA;
+    if (!read_errors_decode(flags, clear != 0)) return DAP_ERR_CUDA;
+    if (!read_errors_fp8(flags, clear != 0)) return DAP_ERR_CUDA;
+    return DAP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// dap_internal.h -- host-side interface between the C ABI (dap_api.cu) and the kernel
+// launchers (dap_decode.cu, dap_fp8.cu).  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dap.h"
+
+namespace dap {
+
+// Tokens per pipeline tile of the split kernel; the split chunk is a multiple of it.
+constexpr int kTileTokens = 32;
+
+// Everything a decode launch needs, already validated.
+struct DecodeArgs {
+    bool paged;
+    const void *q;
+    long long q_sb, q_sh;        // element strides
+    const void *k, *v;           // paged: [num_pages, ps, Hkv, D]; contig: [B, max_len, Hkv, D]
+    int num_pages, page_size;    // paged only
+    int max_len;                 // contig only
+    const int32_t *block_table;  // paged only
+    int max_pages;
+    const int32_t *seq_lens;
+    int max_kv_len;
+    int B, Hq, Hkv, D;
+    float scale;
+    int num_splits;              // resolved, >= 1
+    int chunk;                   // tokens per split chunk
+    void *workspace;
+    void *out;
+    long long o_sb, o_sh;
+};
+
+dap_status launch_decode(const DecodeArgs &a, cudaStream_t stream);
+
+// Events of dap_set_trace_events (nullptr when tracing is off).
+struct TraceEvents {
+    cudaEvent_t split_begin, split_end, combine_end;
+};
+extern TraceEvents g_trace;
+
+struct Fp8Args {
+    const void *q;
+    const uint8_t *kv_cache;
+    const void *inv_scale;
+    const int64_t *slot_idx;
+    const int64_t *lens;
+    int T, NH, HD, W, num_blocks, block_size;
+    float scale;
+    void *out;
+};
+
+dap_status launch_fp8(const Fp8Args &a, cudaStream_t stream);
+
+// Host readers of each translation unit's device error word (cudaMemcpyFromSymbol on the
+// current device); `clear` resets it.  Return false when the copy fails.
+bool read_errors_decode(unsigned int *flags, bool clear);
+bool read_errors_fp8(unsigned int *flags, bool clear);
+
+// Driver entry point for cuTensorMapEncodeTiled, fetched through the runtime so the
+// library does not link libcuda directly.  Returns nullptr if unavailable.
+void *tensor_map_encoder();
+
+// Offsets of the split partials inside the workspace.
+inline size_t partial_acc_bytes(int B, int Hq, int D, int S) {
+    return ((size_t)B * S * Hq * D * sizeof(float) + 255) & ~(size_t)255;
+}
+inline size_t partial_ml_bytes(int B, int Hq, int S) {
+    return ((size_t)B * S * Hq * 2 * sizeof(float) + 255) & ~(size_t)255;
+}
+
+}  // namespace dap

@@ -1,0 +1,200 @@
+"""GPU parity of the bf16 paged / contiguous decode kernels against the fp64 oracle.
+
+Every comparison is element by element: |gpu - oracle| <= 1e-2 + 1e-2 * |oracle| on the bf16
+output (AstrAI csrc log, numerics commit: atol = rtol = 0.01).  Integer-exact properties
+(page-permutation invariance, paged == contiguous, run-to-run) are checked bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_298_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+
+ATOL = RTOL = 1e-2
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def assert_close(out: torch.Tensor, ref: np.ndarray, what=""):
+    got = out.detach().float().cpu().double().numpy()
+    assert got.shape == ref.shape
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    excess = np.abs(got - ref) - (ATOL + RTOL * np.abs(ref))
+    i = np.unravel_index(np.argmax(excess), excess.shape)
+    assert excess.max() <= 0, f"{what}: worst at {i}: gpu {got[i]} oracle {ref[i]}"
+
+
+def oracle_paged(case):
+    return oracle.decode_paged(bits(case.q), bits(case.k_cache), bits(case.v_cache),
+                               case.block_table.cpu().numpy(), case.seq_lens.cpu().numpy(), case.scale)
+
+
+def gpu_paged(case, S=0, **kw):
+    return binding.decode_attn_paged(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                                     max_kv_len=case.max_kv_len, scale=case.scale, num_splits=S, **kw)
+
+
+@pytest.fixture(autouse=True)
+def _clean_errors():
+    binding.get_device_errors(clear=True)
+    yield
+
+
+def test_tiny_workload_all_split_counts():
+    case = inputs.tiny_paged().to("cuda")
+    ref = oracle_paged(case)
+    for S in [0, 1, 2, 3, 4]:
+        assert_close(gpu_paged(case, S), ref, f"S={S}")
+    assert binding.get_device_errors() == 0
+
+
+SHAPES = [
+    # B, Hq, Hkv, D, ps, lens
+    (3, 8, 8, 128, 16, [1, 33, 64]),            # G=1
+    (3, 16, 8, 128, 16, [5, 100, 257]),          # G=2
+    (4, 32, 8, 128, 16, [256, 17, 1000, 31]),    # G=4
+    (2, 64, 8, 128, 64, [300, 129]),             # G=8, page 64
+    (2, 8, 1, 128, 8, [77, 200]),                # G=8, one kv head
+    (3, 4, 2, 64, 16, [37, 100, 0]),             # D=64, empty sequence
+    (2, 8, 2, 64, 1, [40, 9]),                   # page size 1
+    (2, 16, 4, 64, 3, [50, 3]),                  # page size 3 (one-token boxes)
+    (2, 32, 4, 128, 100, [250, 99]),             # page size not a power of two
+    (2, 16, 2, 64, 32, [513, 64]),               # G=8, D=64
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"B{s[0]}_Hq{s[1]}_Hkv{s[2]}_D{s[3]}_ps{s[4]}" for s in SHAPES])
+def test_paged_parity(shape):
+    B, Hq, Hkv, D, ps, lens = shape
+    case = inputs.make_paged_case(B, Hq, Hkv, D, ps, lens, 1000 + sum(lens)).to("cuda")
+    ref = oracle_paged(case)
+    for S in [0, 1, 2, 5]:
+        assert_close(gpu_paged(case, S), ref, f"S={S}")
+    assert binding.get_device_errors() == 0
+
+
+def test_contiguous_matches_oracle_and_paged_bit_for_bit():
+    case = inputs.make_paged_case(4, 32, 8, 128, 16, [300, 1, 64, 129], 77).to("cuda")
+    k, v = inputs.logical_kv(case, max_len=320)
+    ref = oracle.decode_contig(bits(case.q), bits(k), bits(v), case.seq_lens.cpu().numpy(), case.scale)
+    for S in [1, 3]:
+        c = binding.decode_attn_contig(case.q, k, v, case.seq_lens, max_kv_len=case.max_kv_len,
+                                       num_splits=S)
+        assert_close(c, ref, f"contig S={S}")
+        assert torch.equal(c, gpu_paged(case, S))
+
+
+def test_page_permutation_is_bit_identical():
+    case = inputs.make_paged_case(5, 32, 8, 128, 16, [700, 33, 1024, 5, 260], 78).to("cuda")
+    perm = torch.randperm(case.num_pages, generator=torch.Generator().manual_seed(5)).cuda()
+    inv = torch.argsort(perm)
+    moved = inputs.PagedCase(case.q, case.k_cache[perm].contiguous(), case.v_cache[perm].contiguous(),
+                             inv[case.block_table.long()].to(torch.int32).contiguous(), case.seq_lens,
+                             case.page_size, case.scale)
+    for S in [1, 4, 9]:
+        assert torch.equal(gpu_paged(case, S), gpu_paged(moved, S)), f"S={S}"
+
+
+def test_split_count_sweep_stays_within_tolerance():
+    case = inputs.make_paged_case(2, 64, 8, 128, 64, [4096, 2500], 79).to("cuda")
+    ref = oracle_paged(case)
+    outs = []
+    for S in [1, 8, 32, 128]:
+        o = gpu_paged(case, S)
+        assert_close(o, ref, f"S={S}")
+        outs.append(o.float())
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() < 2e-2
+
+
+def test_strided_q_and_out_and_garbage_workspace():
+    case = inputs.make_paged_case(3, 16, 4, 128, 16, [90, 200, 7], 80).to("cuda")
+    ref = oracle_paged(case)
+    qbig = torch.zeros((3, 16, 3 * 128), dtype=torch.bfloat16, device="cuda")
+    qbig[:, :, 128:256] = case.q
+    q = qbig[:, :, 128:256]                      # stride_h = 384
+    obig = torch.full((3, 16, 2 * 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = obig[:, :, :128]
+    S = 4
+    ws = torch.full((binding.workspace_bytes(3, 16, 128, S),), 0xFF, dtype=torch.uint8, device="cuda")
+    binding.decode_attn_paged(q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                              max_kv_len=case.max_kv_len, num_splits=S, workspace=ws, out=out)
+    assert_close(out, ref, "strided")
+    assert torch.all(obig[:, :, 128:] == 7.0), "wrote outside the output rows"
+
+
+def test_repeat_runs_are_identical():
+    case = inputs.make_paged_case(4, 32, 8, 128, 16, [1000, 2000, 10, 555], 81).to("cuda")
+    a = gpu_paged(case, 0)
+    b = gpu_paged(case, 0)
+    assert torch.equal(a, b)
+
+
+def test_seq_len_above_bound_is_flagged_and_clamped():
+    case = inputs.make_paged_case(2, 8, 2, 64, 16, [64, 40], 82).to("cuda")
+    lens = torch.tensor([64, 40], dtype=torch.int32, device="cuda")
+    bad = torch.tensor([64, 41], dtype=torch.int32, device="cuda")   # 41 > max_kv_len = 40 below
+    out = binding.decode_attn_paged(case.q, case.k_cache, case.v_cache, case.block_table, bad,
+                                    max_kv_len=40, num_splits=1)
+    assert binding.get_device_errors() & binding.DEVERR_SEQLEN
+    ref = oracle.decode_paged(bits(case.q), bits(case.k_cache), bits(case.v_cache),
+                              case.block_table.cpu().numpy(), np.array([40, 40], np.int32), case.scale)
+    assert_close(out, ref, "clamped")
+    del lens
+
+
+def test_page_index_outside_pool_is_flagged():
+    case = inputs.make_paged_case(1, 8, 2, 64, 16, [40], 83).to("cuda")
+    table = case.block_table.clone()
+    table[0, 1] = case.num_pages + 5
+    out = binding.decode_attn_paged(case.q, case.k_cache, case.v_cache, table, case.seq_lens,
+                                    max_kv_len=40, num_splits=1)
+    torch.cuda.synchronize()
+    assert binding.get_device_errors() & binding.DEVERR_PAGE
+    del out
+
+
+# ---- the named workloads at full size: sampled rows against the oracle ------------------
+
+def sampled_rows(case, out, n=48, seed=0):
+    g = np.random.default_rng(seed)
+    rows = g.choice(case.B * case.Hq, size=min(n, case.B * case.Hq), replace=False)
+    ref = oracle.decode_paged_rows(bits(case.q), bits(case.k_cache), bits(case.v_cache),
+                                   case.block_table.cpu().numpy(), case.seq_lens.cpu().numpy(),
+                                   case.scale, rows)
+    got = out.reshape(-1, case.D)[torch.as_tensor(rows, device=out.device)]
+    assert torch.isfinite(out.float()).all()
+    assert_close(got, ref, case.name)
+
+
+def test_llama_workload_paged_and_contiguous():
+    case = inputs.llama_paged(device="cuda")
+    out = gpu_paged(case, 0)
+    sampled_rows(case, out)
+    k, v = inputs.logical_kv(case)
+    c = binding.decode_attn_contig(case.q, k, v, case.seq_lens, max_kv_len=case.max_kv_len)
+    assert torch.equal(c, out)
+
+
+def test_ragged_workload():
+    case = inputs.ragged_paged(device="cuda")
+    out = gpu_paged(case, 0)
+    sampled_rows(case, out, n=64)
+    assert binding.get_device_errors() == 0
+
+
+@pytest.mark.parametrize("B", [1, 4])
+def test_long_context_workload_split_sweep(B):
+    case = inputs.long_paged(B=B, device="cuda")
+    outs = {}
+    for S in [0, 1, 8, 32, 128]:
+        outs[S] = gpu_paged(case, S)
+        sampled_rows(case, outs[S], n=16, seed=S)
+    assert binding.get_device_errors() == 0
