@@ -257,6 +257,9 @@ def run_ours(args):
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for e in ev:   # torch creates the CUDA event on first record; the trace hook needs the handle
+        for x in e:
+            x.record(stream)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     if world > 1:
