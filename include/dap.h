@@ -49,7 +49,8 @@ typedef enum {
     DAP_ERR_UNSUPPORTED = 3, /* a valid shape this build has no kernel for */
     DAP_ERR_WORKSPACE = 4,   /* workspace missing or smaller than dap_workspace_bytes */
     DAP_ERR_ALIGN = 5,       /* a pointer or stride breaks the 16-byte rule */
-    DAP_ERR_CUDA = 6         /* a CUDA runtime call or launch failed */
+    DAP_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed */
+    DAP_ERR_SCRATCH_LIMIT = 7 /* needs more split scratch than DAP_NOALLOC_SCRATCH_BYTES */
 } dap_status;
 
 /* Bits of the device error word. */
@@ -161,6 +162,37 @@ dap_status decode_attn_paged_fp8(const void *q, const uint8_t *kv_cache, const v
                                  const int64_t *slot_idx, const int64_t *lens, int T, int NH,
                                  int HD, int W, int num_blocks, int block_size, float scale,
                                  void *out, void *stream);
+
+/*
+ * Paged GQA decode that allocates nothing and takes no workspace.  The web pages this
+ * library follows have no counterpart to it; it exists for callers that cannot hand the
+ * library scratch memory: hosts that reserve their whole device-memory budget up front and
+ * forbid later cudaMalloc calls (a cudaMalloc can synchronise the device and can fail in
+ * the middle of serving), and plugin-style interfaces that pass a kernel only its input and
+ * output buffers.
+ *
+ * Same operation, arguments and results as decode_attn_paged, without `workspace` and
+ * `workspace_bytes`.  The split partials live in one file-scope device array of
+ * DAP_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the library holds until the
+ * process exits.  Sizes:
+ *   - num_splits > 0 whose partials, dap_workspace_bytes(B, Hq, D, S), exceed
+ *     DAP_NOALLOC_SCRATCH_BYTES are rejected with DAP_ERR_SCRATCH_LIMIT (nothing launched);
+ *   - num_splits == 0 takes the planner's S and lowers it until the partials fit.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current) and caches it; make that first call before any stream
+ * capture.  The array keeps what the last call left in it; nothing in it has to start
+ * at zero, because every partial a call reads was written earlier in that same call.
+ * All calls share the one array, so calls that overlap on the GPU (on different streams,
+ * or from different host threads) race and corrupt each other's results: serialise them.
+ * Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define DAP_NOALLOC_SCRATCH_BYTES (16u << 20)
+dap_status decode_attn_paged_noalloc(const void *q, long long q_stride_b, long long q_stride_h,
+                                     const void *k_cache, const void *v_cache, int num_pages,
+                                     int page_size, const int32_t *block_table, int max_pages,
+                                     const int32_t *seq_lens, int max_kv_len, int B, int Hq,
+                                     int Hkv, int D, float scale, int num_splits, void *out,
+                                     long long out_stride_b, long long out_stride_h, void *stream);
 
 /* Tracing hook.  When set (non-NULL cudaEvent_t handles passed as void*), every following
  * decode_attn_paged / decode_attn_contig call records `split_begin` just before its split

@@ -21,13 +21,15 @@ _lib = None
 
 DAP_OK = 0
 STATUS_NAMES = {0: "DAP_OK", 1: "DAP_ERR_NULL", 2: "DAP_ERR_SHAPE", 3: "DAP_ERR_UNSUPPORTED",
-                4: "DAP_ERR_WORKSPACE", 5: "DAP_ERR_ALIGN", 6: "DAP_ERR_CUDA"}
+                4: "DAP_ERR_WORKSPACE", 5: "DAP_ERR_ALIGN", 6: "DAP_ERR_CUDA", 7: "DAP_ERR_SCRATCH_LIMIT"}
+NOALLOC_SCRATCH_BYTES = 16 << 20
 DEVERR_TIMEOUT, DEVERR_SEQLEN, DEVERR_PAGE, DEVERR_SLOT = 0x1, 0x2, 0x4, 0x8
 
 # every symbol include/dap.h declares
 EXPORTS = ("dap_status_string", "dap_version", "dap_device_sm_count", "dap_plan_splits",
            "dap_chunk_tokens", "dap_workspace_bytes", "decode_attn_paged", "decode_attn_contig",
-           "decode_attn_paged_fp8", "dap_set_trace_events", "dap_get_device_errors")
+           "decode_attn_paged_fp8", "decode_attn_paged_noalloc", "dap_set_trace_events",
+           "dap_get_device_errors")
 
 
 class DapError(RuntimeError):
@@ -77,6 +79,9 @@ def load(build_if_missing: bool = True):
         lib.decode_attn_contig.restype = I
         lib.decode_attn_paged_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P, P]
         lib.decode_attn_paged_fp8.restype = I
+        lib.decode_attn_paged_noalloc.argtypes = [P, LL, LL, P, P, I, I, P, I, P, I, I, I, I, I, F, I,
+                                                  P, LL, LL, P]
+        lib.decode_attn_paged_noalloc.restype = I
         lib.dap_set_trace_events.argtypes = [P, P, P]
         lib.dap_set_trace_events.restype = None
         lib.dap_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
@@ -178,6 +183,36 @@ def decode_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, max_kv_len:
                                B, Hq, Hkv, D, float(scale), int(S), _ptr(workspace), wbytes, _ptr(out),
                                out.stride(0), out.stride(1), _stream(stream))
     _check(st, "decode_attn_paged")
+    return out
+
+
+def decode_attn_paged_noalloc(q, k_cache, v_cache, block_table, seq_lens, *, max_kv_len: int,
+                              scale: float | None = None, num_splits: int = 0, out=None, stream=None):
+    """Paged GQA decode without a workspace (include/dap.h: decode_attn_paged_noalloc).
+
+    For callers that cannot give the library scratch memory: the split partials go to a
+    fixed 16 MiB device array inside the library.  Calls that overlap on the GPU race on
+    that array, so keep them on one stream.  Returns ``out`` [B, Hq, D]."""
+    _bf16_3d(q, "q")
+    B, Hq, D = q.shape
+    _need(k_cache.dtype == torch.bfloat16 and k_cache.dim() == 4 and k_cache.is_contiguous()
+          and v_cache.shape == k_cache.shape and v_cache.dtype == torch.bfloat16
+          and v_cache.is_contiguous(), "k_cache/v_cache must be contiguous bf16 [P, ps, Hkv, D]")
+    P, ps, Hkv, _ = k_cache.shape
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
+          and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
+    _need(seq_lens.dtype == torch.int32 and seq_lens.numel() == B and seq_lens.is_contiguous(),
+          "seq_lens must be contiguous int32 [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    _bf16_3d(out, "out")
+    st = load().decode_attn_paged_noalloc(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P,
+                                          ps, _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                          int(max_kv_len), B, Hq, Hkv, D, float(scale), int(num_splits),
+                                          _ptr(out), out.stride(0), out.stride(1), _stream(stream))
+    _check(st, "decode_attn_paged_noalloc")
     return out
 
 

@@ -94,6 +94,8 @@ const char *dap_status_string(int status) {
         case DAP_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case DAP_ERR_ALIGN: return "pointer or stride breaks the 16-byte alignment rule";
         case DAP_ERR_CUDA: return "a CUDA call or kernel launch failed";
+        case DAP_ERR_SCRATCH_LIMIT:
+            return "split partials exceed the no-allocation entry point's fixed scratch (DAP_NOALLOC_SCRATCH_BYTES)";
         default: return "unknown status";
     }
 }

@@ -31,7 +31,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(7):
+    for s in range(8):
         assert binding.status_string(s)
     assert binding.status_string(99) == "unknown status"
     assert lib.dap_version() >= 100
