@@ -155,7 +155,7 @@ dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_s
  *   slot_idx   device int64 [T, W] row-major, -1 = padding.
  *   lens       device int64 [T].
  *   out        device bf16 [T, NH, HD] contiguous.
- *   Supported: HD = 512, NH a multiple of 64 (NH <= 1024), 1 <= W <= 256.
+ *   Supported: HD = 512, NH a multiple of 128 (NH <= 1024), 1 <= W <= 128, T <= 65535.
  *   Slots >= num_blocks*block_size are skipped and flagged (DAP_DEVERR_SLOT).
  */
 dap_status decode_attn_paged_fp8(const void *q, const uint8_t *kv_cache, const void *inv_scale,

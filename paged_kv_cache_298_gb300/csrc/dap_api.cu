@@ -234,7 +234,7 @@ dap_status decode_attn_paged_fp8(const void *q, const uint8_t *kv_cache, const v
         return DAP_ERR_SHAPE;
     if (T == 0) return DAP_OK;
     if (!q || !kv_cache || !inv_scale || !slot_idx || !lens || !out) return DAP_ERR_NULL;
-    if (HD != 512 || NH % 64 != 0 || NH > 1024 || W > 256) return DAP_ERR_UNSUPPORTED;
+    if (HD != 512 || NH % 128 != 0 || NH > 1024 || W > 128 || T > 65535) return DAP_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(out) || !aligned16(kv_cache) ||
         (reinterpret_cast<uintptr_t>(inv_scale) & 1u) || (reinterpret_cast<uintptr_t>(slot_idx) & 7u) ||
         (reinterpret_cast<uintptr_t>(lens) & 7u))

@@ -1,4 +1,37 @@
-// dap_fp8.cu -- fp8 (e4m3) sliding-window latent decode attention, K = V.
+// dap_fp8.cu -- fp8 (e4m3) sliding-window latent decode attention, K = V, on the
+// sm_100-family tensor cores (tcgen05, accumulators in tensor memory).
+//
+// Operation (nvfp4-megamoe-kernel native_swa_decode.py, native_swa_decode_attention and
+// _fallback_batched_sdp): for decode token t the window slots are slot_idx[t, j], j < W; a
+// slot takes part iff j < lens[t] and slot >= 0; its row is
+//     kv_j = bf16( e4m3(kv_cache[slot / bs, slot % bs, :]) * inv_scale[slot] )
+// and keys and values are the same rows.  Every query head h of the token attends to them:
+//     out[t, h] = sum_j softmax_j(scale * q[t, h] . kv_j) kv_j.
+// A token with no row gives a zero row (the page's kernel stub normalises only when the
+// row sum is nonzero).
+//
+// Why tensor cores: 128 query heads share every row, so QK^T and PV are dense GEMMs with
+// M = 128 heads (the page's stub groups heads per CTA for the same reason and imports the
+// tcgen05 module, but leaves the tile loop empty).
+//
+// One CTA per (token, head group of 128, half of HD):
+//   1. the token's window is compacted to its n participating slots (order kept);
+//   2. the n rows are gathered, dequantised (e4m3 -> f16 -> f32, times the f32 inverse scale,
+//      rounded once to bf16: the same single rounding the page's fallback does) and stored
+//      in shared memory as a 128-byte-swizzled [hd block][row][64] tile; rows n..n16-1 are
+//      zero (n16 = n rounded up to 16);
+//   3. q[t, heads, :] streams in through TMA (128B swizzle) in eight 64-wide blocks over a
+//      3-stage ring, and one thread issues S = Q . KV^T (M=128, N=n16, K=512) into TMEM;
+//   4. each thread owns one head (one TMEM lane): base-2 softmax over its n scores, the
+//      probabilities rounded to bf16 into a swizzled P tile, l = their sum;
+//   5. O[:, half] = P . KV[:, half] (M=128, N=256, K=n16) reads the same KV tile as an
+//      MN-major operand;
+//   6. out = O / l in bf16.
+// The two CTAs of a token recompute S (cheap on tensor cores) so that O's 256 fp32
+// columns and S's columns fit tensor memory together.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "dap_device.cuh"
 #include "dap_internal.h"
 
@@ -15,10 +48,406 @@ bool read_errors_fp8(unsigned int *flags, bool clear) {
     return true;
 }
 
+namespace fp8 {
+
+constexpr int kHD = 512;            // latent width
+constexpr int kHeads = 128;         // heads per CTA = MMA M
+constexpr int kMaxRows = 128;       // window rows a CTA holds
+constexpr int kHalf = kHD / 2;      // output columns per CTA
+constexpr int kThreads = 128;
+constexpr int kQStages = 3;
+// shared-memory map (offsets from a 1024-byte aligned base)
+constexpr int kKvOff = 0;                                   // [8 blocks][128 rows][128 B]
+constexpr int kKvBlock = kMaxRows * 128;                    // 16 KB per 64-wide hd block
+constexpr int kQOff = kKvOff + 8 * kKvBlock;                // 131072
+constexpr int kQStage = kHeads * 128;                       // 16 KB: 128 heads x 64 bf16
+constexpr int kPOff = kQOff;                                // P reuses the Q ring after QK
+constexpr int kPBlock = kHeads * 128;                       // 16 KB per 64-wide row block
+constexpr int kRowsOff = kQOff + kQStages * kQStage;        // int32 slot per kept row
+constexpr int kInvOff = kRowsOff + kMaxRows * 4;            // f32 inverse scale per kept row
+constexpr int kCntOff = kInvOff + kMaxRows * 4;             // per-warp counts, n, abort
+constexpr int kBarOff = kCntOff + 64;                       // mbarriers
+constexpr int kNumBars = 2 * kQStages + 2;
+constexpr int kTmemOff = kBarOff + kNumBars * 8;
+constexpr int kSmemUsed = kTmemOff + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;                // slack to align the base
+constexpr int kTmemCols = 512;                              // O: cols [0,256), S: [256,384)
+constexpr int kSCol = 256;
+static_assert(kPOff + 2 * kPBlock <= kRowsOff, "P fits in the Q ring");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+// ---- tcgen05 / descriptor helpers ---------------------------------------------------------
+
+// Shared-memory matrix descriptor (sm_100 tcgen05 format): start address, leading and
+// stride byte offsets (all >> 4), descriptor version 1, layout type 2 = 128-byte swizzle.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, A K-major,
+// B K-major (b_mn_major = 0) or MN-major (1), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          bool accumulate) {
+    const uint32_t acc = accumulate ? 1u : 0u;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// Arrive (once) on `bar` when every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the tensor cores.
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Byte offset of 16-byte chunk `k` (0..7) of row `r` in a 128-byte-swizzled tile whose
+// rows are 128 bytes apart (chunk k of row r sits at chunk k ^ (r mod 8)).
+__device__ __forceinline__ uint32_t sw128_off(int r, int k) {
+    return (uint32_t)r * 128u + ((uint32_t)(k ^ (r & 7)) << 4);
+}
+
+struct Params {
+    const uint8_t *kv_cache;
+    const __nv_bfloat16 *inv_scale;
+    const int64_t *slot_idx;
+    const int64_t *lens;
+    __nv_bfloat16 *out;
+    int T, NH, W;
+    long long max_slots;
+    float qscale;  // scale * log2(e)
+};
+
+
+__global__ void __launch_bounds__(kThreads, 1)
+    swa_kernel(const __grid_constant__ CUtensorMap qmap, const Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the 128-byte swizzle is a function of address bits 4..9: tiles start 1024-aligned
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int col_half = blockIdx.x;    // which 256 output columns
+    const int hg = blockIdx.y;          // head group of 128
+    const int t = blockIdx.z;           // decode token
+
+    int *rows = reinterpret_cast<int *>(smem + kRowsOff);
+    float *invs = reinterpret_cast<float *>(smem + kInvOff);
+    int *cnt = reinterpret_cast<int *>(smem + kCntOff);     // [0..3] warp counts, [4] n, [5] abort
+    uint64_t *q_full = reinterpret_cast<uint64_t *>(smem + kBarOff);
+    uint64_t *q_free = q_full + kQStages;
+    uint64_t *mma_done = q_free + kQStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
+
+    if (tid == 0) {
+        for (int i = 0; i < kQStages; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_free[i], 1);
+        }
+        mbar_init(&mma_done[0], 1);
+        mbar_init(&mma_done[1], 1);
+        cnt[5] = 0;
+        fence_barrier_init();
+        prefetch_tensormap(&qmap);
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+
+    // ---- 1. compact the window: slots of the rows that take part, in window order ---------
+    long long len = p.lens[t];
+    len = len < 0 ? 0 : (len > p.W ? p.W : len);
+    int keep = 0;
+    long long slot = -1;
+    if (tid < p.W && tid < len) {
+        slot = p.slot_idx[(long long)t * p.W + tid];
+        if (slot >= p.max_slots) {
+            flag_error(DAP_DEVERR_SLOT);
+            slot = -1;
+        }
+        keep = slot >= 0;
+    }
+    const unsigned ball = __ballot_sync(0xFFFFFFFFu, keep);
+    if (lane == 0) cnt[warp] = __popc(ball);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += cnt[w];
+    const int n = cnt[0] + cnt[1] + cnt[2] + cnt[3];
+    if (keep) {
+        const int pos = base + __popc(ball & ((1u << lane) - 1u));
+        rows[pos] = (int)slot;
+        invs[pos] = __bfloat162float(p.inv_scale[slot]);
+    }
+    const int n16 = (n + 15) & ~15;
+
+    // ---- 3a. start streaming q (three of the eight 64-wide blocks) -------------------------
+    const int qrow = t * p.NH + hg * kHeads;
+    if (tid == 0 && n > 0) {
+        for (int kb = 0; kb < kQStages; ++kb) {
+            mbar_arrive_expect_tx(&q_full[kb], kQStage);
+            tma_load_2d(smem + kQOff + kb * kQStage, &qmap, kb * 64, qrow, &q_full[kb]);
+        }
+    }
+    __syncthreads();  // rows[] / invs[] complete
+
+    // ---- 2. gather + dequantise the rows into the swizzled KV tile -------------------------
+    if (n > 0) {
+        for (int item = tid; item < n16 * 32; item += kThreads) {
+            const int r = item >> 5;   // row
+            const int c = item & 31;   // 16-byte piece of the 512-byte fp8 row = 16 hd values
+            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+            if (r < n) {
+                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(p.kv_cache + (long long)rows[r] * kHD) + c);
+                const float inv = invs[r];
+                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                uint32_t o[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w4[i] >> (16 * j)) & 0xFFFFu);
+                        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+                        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * inv, f.y * inv);
+                        o[2 * i + j] = *reinterpret_cast<const uint32_t *>(&b);
+                    }
+                }
+                lo = make_uint4(o[0], o[1], o[2], o[3]);
+                hi = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            const int blk = c >> 2;            // 64-wide hd block
+            const int k0 = (c & 3) * 2;        // first 16-byte chunk inside the 128-byte row
+            uint8_t *tile = smem + kKvOff + blk * kKvBlock;
+            *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0)) = lo;
+            *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0 + 1)) = hi;
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    bool ok = true;
+    const uint32_t tS = tmem + kSCol;
+    // ---- 3b. S = Q . KV^T, one thread issues ------------------------------------------------
+    if (tid == 0 && n > 0) {
+        const uint32_t idS = idesc_bf16(kHeads, n16, 0);
+        for (int kb = 0; kb < 8 && ok; ++kb) {
+            const int st = kb % kQStages;
+            if (!mbar_wait(&q_full[st], (kb / kQStages) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t qa = smem_addr(smem + kQOff + st * kQStage);
+            const uint32_t kva = smem_addr(smem + kKvOff + kb * kKvBlock);
+#pragma unroll
+            for (int k16 = 0; k16 < 4; ++k16)
+                umma_bf16(tS, sw128_desc(qa + 32 * k16, 16, 1024), sw128_desc(kva + 32 * k16, 16, 1024), idS,
+                          (kb | k16) != 0);
+            umma_commit(&q_free[st]);
+            if (kb + kQStages < 8) {  // refill this stage once its MMAs have read it
+                if (!mbar_wait(&q_free[st], (kb / kQStages) & 1)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&q_full[st], kQStage);
+                tma_load_2d(smem + kQOff + st * kQStage, &qmap, (kb + kQStages) * 64, qrow, &q_full[st]);
+            }
+        }
+        umma_commit(&mma_done[0]);
+        if (!ok) cnt[5] = 1;
+    }
+
+    // ---- 4. softmax: thread = head = TMEM lane -------------------------------------------------
+    bool waited = true;
+    if (n > 0) waited = mbar_wait(&mma_done[0], 0);
+    const int good = __syncthreads_and(waited && cnt[5] == 0);
+    tc_fence_after();
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float l = 0.f;
+    if (good && n > 0) {
+        float m = -INFINITY;
+        for (int c0 = 0; c0 < n16; c0 += 32) {
+            float v[32];
+            tmem_ld32(tS + lane_base + c0, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (c0 + i < n) m = fmaxf(m, v[i] * p.qscale);
+        }
+        for (int c0 = 0; c0 < n16; c0 += 32) {
+            float v[32];
+            tmem_ld32(tS + lane_base + c0, v);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int j0 = c0 + 8 * g;
+                if (j0 >= n16) break;
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const float p0 = (j0 + e < n) ? ex2(v[8 * g + e] * p.qscale - m) : 0.f;
+                    const float p1 = (j0 + e + 1 < n) ? ex2(v[8 * g + e + 1] * p.qscale - m) : 0.f;
+                    const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
+                    const float2 r = __bfloat1622float2(b);
+                    l += r.x + r.y;  // the sum of the weights PV actually uses
+                    pk[e / 2] = *reinterpret_cast<const uint32_t *>(&b);
+                }
+                uint8_t *tile = smem + kPOff + (j0 >> 6) * kPBlock;
+                *reinterpret_cast<uint4 *>(tile + sw128_off(tid, (j0 & 63) >> 3)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- 5. O[:, half] = P . KV[:, half] ----------------------------------------------------------
+    if (tid == 0 && good && n > 0) {
+        const uint32_t idO = idesc_bf16(kHeads, kHalf, 1);
+        const uint32_t pa = smem_addr(smem + kPOff);
+        const uint32_t kvb = smem_addr(smem + kKvOff + col_half * 4 * kKvBlock);
+        for (int k16 = 0; k16 < n16 / 16; ++k16)
+            umma_bf16(tmem, sw128_desc(pa + (k16 >> 2) * kPBlock + (k16 & 3) * 32, 16, 1024),
+                      sw128_desc(kvb + k16 * 2048, kKvBlock, 1024), idO, k16 > 0);
+        umma_commit(&mma_done[0]);
+    }
+    bool waited2 = true;
+    if (good && n > 0) waited2 = mbar_wait(&mma_done[0], 1);
+    const int good2 = __syncthreads_and(good && waited2);
+    tc_fence_after();
+
+    // ---- 6. out = O / l --------------------------------------------------------------------------
+    if (good2) {
+        __nv_bfloat16 *orow = p.out + ((long long)t * p.NH + hg * kHeads + tid) * kHD + col_half * kHalf;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        for (int c0 = 0; c0 < kHalf; c0 += 32) {
+            float v[32];
+            if (n > 0) {
+                tmem_ld32(tmem + lane_base + c0, v);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i] * inv, v[2 * i + 1] * inv);
+                pk[i] = *reinterpret_cast<const uint32_t *>(&b);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+    } else if (tid == 0 && n > 0) {
+        // A wait gave up.  Let the copies and products still in flight land (bounded) before
+        // the tensor memory and the shared memory are released.
+        for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_full[i], 0);
+        umma_commit(&mma_done[1]);
+        (void)mbar_wait(&mma_done[1], 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+}  // namespace fp8
+
 dap_status launch_fp8(const Fp8Args &a, cudaStream_t stream) {
-    (void)a;
-    (void)stream;
-    return DAP_ERR_UNSUPPORTED;
+    typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                      const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                      CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                      CUtensorMapFloatOOBfill);
+    EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+    if (!enc) return DAP_ERR_CUDA;
+    // q as a [T*NH, 512] bf16 matrix; a box is 128 heads x 64 values (128 bytes), swizzled
+    CUtensorMap qmap;
+    const cuuint64_t dims[2] = {(cuuint64_t)fp8::kHD, (cuuint64_t)a.T * a.NH};
+    const cuuint64_t strides[1] = {(cuuint64_t)fp8::kHD * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)fp8::kHeads};
+    const cuuint32_t estr[2] = {1u, 1u};
+    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.q), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return DAP_ERR_CUDA;
+    fp8::Params p;
+    p.kv_cache = a.kv_cache;
+    p.inv_scale = static_cast<const __nv_bfloat16 *>(a.inv_scale);
+    p.slot_idx = a.slot_idx;
+    p.lens = a.lens;
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
+    p.T = a.T;
+    p.NH = a.NH;
+    p.W = a.W;
+    p.max_slots = (long long)a.num_blocks * a.block_size;
+    p.qscale = a.scale * 1.4426950408889634f;
+    if (cudaFuncSetAttribute(fp8::swa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fp8::kSmemBytes) !=
+        cudaSuccess)
+        return DAP_ERR_CUDA;
+    const dim3 grid(2, a.NH / fp8::kHeads, a.T);
+    fp8::swa_kernel<<<grid, fp8::kThreads, fp8::kSmemBytes, stream>>>(qmap, p);
+    return cudaGetLastError() == cudaSuccess ? DAP_OK : DAP_ERR_CUDA;
 }
 
 }  // namespace dap

@@ -119,6 +119,6 @@ def test_fp8_validation(lib):
         return f(FAKE, FAKE, FAKE, FAKE, FAKE, a["T"], a["NH"], a["HD"], a["W"], a["NB"], a["bs"], 0.04,
                  FAKE, None)
     assert call(T=-1) == 2 and call(W=0) == 2 and call(bs=0) == 2
-    assert call(HD=256) == 3 and call(NH=100) == 3 and call(W=300) == 3
+    assert call(HD=256) == 3 and call(NH=64) == 3 and call(W=129) == 3
     assert call(T=0) == 0
     assert f(None, FAKE, FAKE, FAKE, FAKE, 4, 128, 512, 128, 64, 256, 0.04, FAKE, None) == 1
