@@ -229,8 +229,7 @@ def run_ours(args):
     case = make_workload(args.workload, dev)
     hbm_peak, peak_src = peaks()
     sms = binding.device_sm_count()
-    S = args.splits or binding.plan_splits(sms, case.B, case.Hq, case.Hkv, case.D, case.page_size,
-                                           case.max_kv_len, case.total_kv)
+    S = args.splits  # 0 = the balanced schedule
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     footprint = sum(t.numel() * t.element_size() for t in (case.q, case.k_cache, case.v_cache,
                                                            case.block_table, case.seq_lens))
@@ -238,7 +237,8 @@ def run_ours(args):
     sets = [case] + [type(case)(case.q.clone(), case.k_cache.clone(), case.v_cache.clone(),
                                 case.block_table.clone(), case.seq_lens.clone(), case.page_size, case.scale,
                                 case.name) for _ in range(copies - 1)]
-    ws = [torch.empty(max(1, binding.workspace_bytes(case.B, case.Hq, case.D, S)), dtype=torch.uint8, device=dev)
+    ws = [torch.empty(max(1, binding.workspace_bytes(case.B, case.Hq, case.Hkv, case.D, S)), dtype=torch.uint8,
+                      device=dev)
           for _ in sets]
     outs = [torch.empty_like(case.q) for _ in sets]
     maxlen = case.max_kv_len
@@ -341,7 +341,7 @@ def run_ours(args):
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": hq.numel() * 2 + ht.numel() * 4 + hl.numel() * 4,
                 "d2h_bytes_per_step": ho.numel() * 2},
-        "gpu_launches": K * (2 if S > 1 else 1),
+        "gpu_launches": K * (2 if S != 1 else 1),
         "device_errors": errs,
         "clocks": clk,
     }
@@ -390,7 +390,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ragged", choices=["ragged", "llama", "long1", "long4"])
-    ap.add_argument("--splits", type=int, default=0, help="0 = planner")
+    ap.add_argument("--splits", type=int, default=0, help="0 = balanced schedule, S > 0 = per-sequence splits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

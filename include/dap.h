@@ -88,10 +88,14 @@ int dap_plan_splits(int sm_count, int B, int Hq, int Hkv, int D, int page_size,
  * kernel's tile of 32 tokens (at least 32).  Pure host function. */
 int dap_chunk_tokens(int max_kv_len, int num_splits);
 
-/* Workspace bytes decode_attn_paged / decode_attn_contig need for `num_splits` splits:
- * 0 when num_splits <= 1, else room for B*num_splits*Hq partial rows of (D + 2) floats
- * (unnormalised acc, running max m, running sum l).  Pure host function. */
-size_t dap_workspace_bytes(int B, int Hq, int D, int num_splits);
+/* Workspace bytes decode_attn_paged / decode_attn_contig need for `num_splits`:
+ *   num_splits == 1: 0;
+ *   num_splits >= 2: room for B*num_splits*Hq partial rows of (D + 2) floats (unnormalised
+ *                    acc, running max m, running sum l);
+ *   num_splits == 0: the balanced schedule's partial slots (two per persistent CTA, for at
+ *                    most 1024 CTAs) plus 8 bytes per (sequence, kv head); 0 when B > 4096.
+ * Pure host function. */
+size_t dap_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits);
 
 /*
  * Paged GQA decode attention [A][B].
@@ -108,15 +112,21 @@ size_t dap_workspace_bytes(int B, int Hq, int D, int num_splits);
  *   max_kv_len   host: an upper bound of seq_lens (<= max_pages * page_size); it sets
  *                the chunk length of the split plan.
  *   scale        softmax scale applied in fp32 to q . k (normally 1/sqrt(D)).
- *   num_splits   splits of the longest sequence; 0 = dap_plan_splits(...) with
- *                total_kv unknown.
- *   workspace    device scratch of at least dap_workspace_bytes(B, Hq, D, S) bytes,
- *                16-byte aligned (may be NULL when S == 1).  Needs no initialisation;
- *                its contents are undefined afterwards.
+ *   num_splits   0 = balanced schedule (recommended): a persistent grid of SMs x resident
+ *                CTAs cuts the flattened (sequence, kv head, 32-token tile) space into
+ *                equal contiguous ranges, whatever the length mix; splits of a sequence
+ *                are merged by a combine kernel.  (B > 4096 runs one CTA per sequence and
+ *                kv head instead.)  S > 0 = per-sequence schedule: every sequence is cut
+ *                into chunks of dap_chunk_tokens(max_kv_len, S) tokens, one CTA each
+ *                (dap_plan_splits suggests an S).
+ *   workspace    device scratch of at least dap_workspace_bytes(B, Hq, Hkv, D, num_splits)
+ *                bytes, 16-byte aligned (may be NULL when that is 0).  Needs no
+ *                initialisation; its contents are undefined afterwards.
  *   out          device bf16 [B, Hq, D], element strides (out_stride_b, out_stride_h, 1).
  *                Written in full (an empty sequence gives a zero row).
  *   Supported: D in {64, 128}; G in {1, 2, 4, 8}; any page_size >= 1.  q, out,
- *   k_cache and v_cache 16-byte aligned; q/out strides multiples of 8 elements.
+ *   k_cache and v_cache 16-byte aligned; q/out strides multiples of 8 elements, nonzero
+ *   where the extent they step over is above 1.
  *   The result is bit-identical under any permutation of the physical pages for a fixed
  *   num_splits (the summation order depends only on logical positions).
  */
@@ -175,9 +185,10 @@ dap_status decode_attn_paged_fp8(const void *q, const uint8_t *kv_cache, const v
  * `workspace_bytes`.  The split partials live in one file-scope device array of
  * DAP_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the library holds until the
  * process exits.  Sizes:
- *   - num_splits > 0 whose partials, dap_workspace_bytes(B, Hq, D, S), exceed
- *     DAP_NOALLOC_SCRATCH_BYTES are rejected with DAP_ERR_SCRATCH_LIMIT (nothing launched);
- *   - num_splits == 0 takes the planner's S and lowers it until the partials fit.
+ *   - a num_splits whose partials, dap_workspace_bytes(B, Hq, Hkv, D, num_splits), exceed
+ *     DAP_NOALLOC_SCRATCH_BYTES is rejected with DAP_ERR_SCRATCH_LIMIT (nothing launched),
+ *     except that num_splits == 0 whose balanced-schedule partials do not fit falls back
+ *     to the planner's per-sequence S, lowered until its partials fit.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
  * with that device current) and caches it; make that first call before any stream
  * capture.  The array keeps what the last call left in it; nothing in it has to start

@@ -69,7 +69,7 @@ def load(build_if_missing: bool = True):
         lib.dap_plan_splits.restype = I
         lib.dap_chunk_tokens.argtypes = [I, I]
         lib.dap_chunk_tokens.restype = I
-        lib.dap_workspace_bytes.argtypes = [I, I, I, I]
+        lib.dap_workspace_bytes.argtypes = [I, I, I, I, I]
         lib.dap_workspace_bytes.restype = SZ
         lib.decode_attn_paged.argtypes = [P, LL, LL, P, P, I, I, P, I, P, I, I, I, I, I, F, I, P, SZ,
                                           P, LL, LL, P]
@@ -128,8 +128,8 @@ def chunk_tokens(max_kv_len, num_splits) -> int:
     return load().dap_chunk_tokens(max_kv_len, num_splits)
 
 
-def workspace_bytes(B, Hq, D, num_splits) -> int:
-    return load().dap_workspace_bytes(B, Hq, D, num_splits)
+def workspace_bytes(B, Hq, Hkv, D, num_splits) -> int:
+    return load().dap_workspace_bytes(B, Hq, Hkv, D, num_splits)
 
 
 def set_trace_events(split_begin=None, split_end=None, combine_end=None):
@@ -154,7 +154,8 @@ def _bf16_3d(t, name):
 def decode_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, max_kv_len: int,
                       scale: float | None = None, num_splits: int = 0, workspace=None, out=None,
                       stream=None):
-    """Paged GQA decode (include/dap.h: decode_attn_paged).  Returns ``out`` [B, Hq, D]."""
+    """Paged GQA decode (include/dap.h: decode_attn_paged).  num_splits 0 = balanced
+    schedule, S > 0 = per-sequence splits.  Returns ``out`` [B, Hq, D]."""
     _bf16_3d(q, "q")
     B, Hq, D = q.shape
     _need(k_cache.dtype == torch.bfloat16 and k_cache.dim() == 4 and k_cache.is_contiguous()
@@ -172,9 +173,8 @@ def decode_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, max_kv_len:
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
     _bf16_3d(out, "out")
     lib = load()
-    S = num_splits if num_splits > 0 else lib.dap_plan_splits(lib.dap_device_sm_count(), B, Hq, Hkv, D,
-                                                              ps, int(max_kv_len), 0)
-    need = lib.dap_workspace_bytes(B, Hq, D, S)
+    S = int(num_splits)
+    need = lib.dap_workspace_bytes(B, Hq, Hkv, D, S)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -233,9 +233,8 @@ def decode_attn_contig(q, k, v, seq_lens, *, max_kv_len: int, scale: float | Non
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
     _bf16_3d(out, "out")
     lib = load()
-    S = num_splits if num_splits > 0 else lib.dap_plan_splits(lib.dap_device_sm_count(), B, Hq, Hkv, D,
-                                                              max_len, int(max_kv_len), 0)
-    need = lib.dap_workspace_bytes(B, Hq, D, S)
+    S = int(num_splits)
+    need = lib.dap_workspace_bytes(B, Hq, Hkv, D, S)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

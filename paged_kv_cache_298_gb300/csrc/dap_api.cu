@@ -49,6 +49,7 @@ dap_status check_common(const void *q, long long q_sb, long long q_sh, const int
         o_sb < 0 || o_sh < 0)
         return DAP_ERR_SHAPE;
     if (B == 0) return DAP_OK;
+    if ((Hq > 1 && (q_sh == 0 || o_sh == 0)) || (B > 1 && (q_sb == 0 || o_sb == 0))) return DAP_ERR_SHAPE;
     if (!q || !seq_lens || !out) return DAP_ERR_NULL;
     if (!(D == 64 || D == 128) || !supported_group(Hq / Hkv)) return DAP_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(out) || !aligned4(seq_lens) || (q_sb & 7) || (q_sh & 7) ||
@@ -59,18 +60,22 @@ dap_status check_common(const void *q, long long q_sb, long long q_sh, const int
 
 dap_status resolve_splits(int B, int Hq, int Hkv, int D, int page_size, int max_kv_len, int num_splits,
                           void *workspace, size_t workspace_bytes, int *S_out, int *chunk_out) {
+    (void)page_size;
     int S = num_splits;
-    if (S == 0) {
-        const int sms = dap_device_sm_count();
-        if (sms <= 0) return DAP_ERR_CUDA;
-        S = dap_plan_splits(sms, B, Hq, Hkv, D, page_size, max_kv_len, 0);
+    if (S == 0 && B <= kMaxBalancedBatch) {  // balanced persistent schedule
+        const size_t need = dap_workspace_bytes(B, Hq, Hkv, D, 0);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DAP_ERR_WORKSPACE;
+        *S_out = 0;
+        *chunk_out = 0;
+        return DAP_OK;
     }
+    if (S == 0) S = 1;  // so many sequences that one CTA per (sequence, kv head) fills the GPU
     const int chunk = dap_chunk_tokens(max_kv_len, S);
     // splits that could never hold a token are dropped: S chunks must cover max_kv_len
     const int needed = max_kv_len > 0 ? (int)ceil_div_ll(max_kv_len, chunk) : 1;
     S = std::max(1, std::min(S, needed));
     if (S > 1) {
-        const size_t need = dap_workspace_bytes(B, Hq, D, S);
+        const size_t need = dap_workspace_bytes(B, Hq, Hkv, D, S);
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DAP_ERR_WORKSPACE;
     }
     *S_out = S;
@@ -137,8 +142,14 @@ int dap_plan_splits(int sm_count, int B, int Hq, int Hkv, int D, int page_size, 
     return (int)std::max<long long>(1, S);
 }
 
-size_t dap_workspace_bytes(int B, int Hq, int D, int num_splits) {
-    if (num_splits <= 1 || B <= 0 || Hq <= 0 || D <= 0) return 0;
+size_t dap_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_splits < 0 || num_splits == 1) return 0;
+    if (num_splits == 0) {
+        if (B > kMaxBalancedBatch || Hq % Hkv != 0) return 0;
+        const int G = Hq / Hkv;
+        const int hg = balanced_kv_heads_per_unit(D, G);
+        return balanced_layout(B, std::max(1, Hkv / hg), balanced_heads_per_unit(D, G), D).bytes;
+    }
     return partial_acc_bytes(B, Hq, D, num_splits) + partial_ml_bytes(B, Hq, num_splits);
 }
 

@@ -4,35 +4,41 @@
 // 1/sqrt(head_dim); AstrAI csrc log, split-KV commit): for sequence b and query head h,
 //   out[b,h] = sum_t softmax_t(scale * q[b,h] . K[b,t,h/G]) V[b,t,h/G],   t < seq_lens[b].
 //
-// Work decomposition.  A CTA owns one work unit (sequence b, group of HG kv heads,
-// split s): the tokens [s*chunk, min(L_b, (s+1)*chunk)).  A sequence whose length fits one
-// chunk is finished in place (normalised bf16 row); otherwise the CTA writes an
-// unnormalised partial (acc, m, l) and the combine kernel merges the splits in split
-// order (csrc log, split-KV commit: "(O, m, l) partials, reduced by a combine kernel";
-// "single-pass direct-write" when one split suffices).  Units are numbered split-major,
-// so every sequence's first chunk is scheduled before any second chunk.
+// Work.  A "unit" is (sequence b, group of HG kv heads); its keys are cut into tiles of
+// BT = 32 tokens.  Two schedules share one per-tile pipeline:
+//   * balanced (num_splits == 0): a persistent grid of P CTAs (SMs x resident CTAs); the
+//     flattened (unit, tile) sequence of all T tiles is cut into P contiguous ranges of
+//     T/P tiles, so every CTA streams the same number of tiles whatever the length mix.  A
+//     range crosses unit boundaries without draining the pipeline.  A unit covered by one
+//     CTA is finished in place; a unit shared by several CTAs gets one partial (acc, m, l)
+//     from each (at most two per CTA: the unit its range starts in and the one it ends in),
+//     and the combine kernel merges them in CTA order;
+//   * per-sequence (num_splits = S > 0): a grid of (unit, split) CTAs, split s owning tokens
+//     [s*chunk, (s+1)*chunk) (AstrAI csrc log, split-KV commit: partition KV across
+//     gridDim.z blocks that emit unnormalised (O, m, l) partials, reduced by a combine
+//     kernel; single-pass direct write when one split suffices).
+// Either way the summation order depends only on logical positions and the schedule, so
+// the output is bit-identical under any permutation of the physical pages.
 //
-// Data movement.  K and V tiles of kTileTokens tokens are staged in shared memory by
-// 4-D TMA boxes over the cache viewed as [pages, page_size, Hkv, D] (contiguous cache:
-// [B, max_len, Hkv, D], one "page" per sequence).  A box covers R = gcd(page_size, 32)
-// tokens of one page, so any page size works and every page-table entry is read once
-// per box (csrc log, per-element page lookup commit: "works for any page_size").  One
-// producer warp resolves the page ids (prefetched one tile ahead), arms the stage's
-// mbarrier with the byte count and issues the boxes; NS stages keep NS-1 tiles in flight
-// (csrc log, multi-stage pipeline commit).  Out-of-range page ids are replaced by page 0
-// and flagged, so no access leaves the pool.
+// Data movement.  K and V tiles are staged in shared memory by 4-D TMA boxes over the
+// cache viewed as [pages, page_size, Hkv, D] (contiguous cache: [B, max_len, Hkv, D], one
+// "page" per sequence).  A box covers R = gcd(page_size, 32) tokens of one page and HG
+// kv heads, so any page size works (csrc log, per-element page lookup commit).  One
+// producer warp resolves page ids one tile ahead, arms the stage's mbarrier with the byte
+// count and issues the boxes; NS stages keep NS-1 tiles in flight (csrc log, multi-stage
+// pipeline commit).  Out-of-range page ids are replaced by page 0 and flagged.
 //
 // Arithmetic.  q is held in fp32 registers, pre-multiplied by scale*log2(e) in fp32 (the
 // bf16 q is never rescaled: csrc log, "apply scale in float32 after Q@K^T").  QK^T uses
-// packed fp32 FMAs (FFMA2) with LPR lanes per key row and a reduce-scatter across them;
-// the online softmax runs in base 2; PV accumulates with FFMA2 (fused multiply-add, csrc
-// log numerics commit: fmaf for V accumulation).  Rows past the sequence end are masked
-// to -inf before the max and never read in PV, so stale or poisoned shared memory cannot
-// leak into the result.  The summation order depends only on logical positions: the
-// output is bit-identical under any permutation of the physical pages.
+// packed fp32 FMAs with LPR lanes per key row and a reduce-scatter across them; the
+// online softmax runs in base 2; PV accumulates with packed fused multiply-adds (csrc log,
+// numerics commit: fmaf for V accumulation).  Rows past the sequence end are masked to
+// -inf before the max and never read in PV, so stale or poisoned shared memory cannot leak
+// into the result.  The final division is guarded (an empty sequence gives zeros).
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "dap_device.cuh"
 #include "dap_internal.h"
@@ -48,10 +54,13 @@ struct SplitParams {
     int max_kv_len;
     int B, Hq, Hkv;
     int page_size, num_pages, box_rows;
-    int num_splits, chunk;
-    float qscale;  // scale * log2(e)
+    int num_splits, chunk;  // per-sequence schedule
+    int num_ctas;           // balanced schedule: P
+    float qscale;           // scale * log2(e)
     float *o_part;
     float *ml_part;
+    int *unit_info;         // balanced: [units][2] = first tile, tiles
+    long long *total_tiles; // balanced: T
     __nv_bfloat16 *out;
     long long o_sb, o_sh;
 };
@@ -59,33 +68,42 @@ struct SplitParams {
 template <int D_, int G_, int HG_, int NWC_, int BT_, int NS_, int MINB_>
 struct SplitCfg {
     static constexpr int D = D_, G = G_, HG = HG_, NWC = NWC_, BT = BT_, NS = NS_;
-    static constexpr int MINB = MINB_;  // CTAs per SM the register budget must allow
-    static constexpr int WPH = NWC / HG;        // warps per kv head
-    static constexpr int RW = BT / WPH;         // tile rows per warp
+    static constexpr int MINB = MINB_;             // CTAs per SM the register budget allows
+    static constexpr int WPH = NWC / HG;           // warps per kv head
+    static constexpr int RW = BT / WPH;            // tile rows per warp
     static constexpr int DPL = (G <= 4) ? 16 : 8;  // QK dims per lane
-    static constexpr int CPL = DPL / 8;         // 16-byte chunks per lane
-    static constexpr int LPR = D / DPL;         // lanes per key row in QK
-    static constexpr int RPP = 32 / LPR;        // key rows per QK pass
+    static constexpr int CPL = DPL / 8;            // 16-byte chunks per lane
+    static constexpr int LPR = D / DPL;            // lanes per key row in QK
+    static constexpr int RPP = 32 / LPR;           // key rows per QK pass
     static constexpr int PASSES = RW / RPP;
-    static constexpr int DPV = D / 32;          // PV dims per lane
-    static constexpr int ROWB = D * 2;          // bytes of one (token, kv head) row
+    static constexpr int DPV = D / 32;             // PV dims per lane
+    static constexpr int ROWB = D * 2;             // bytes of one (token, kv head) row
+    static constexpr int HPU = HG * G;             // query heads per unit
     static constexpr int TILE_BYTES = BT * HG * ROWB;
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int QBYTES = HPU * ROWB;      // q of one unit
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES + QBYTES;
     static constexpr int PBUF_OFF = NS * STAGE_BYTES;
     static constexpr int PBUF_BYTES = NWC * RW * G * 4;
     static constexpr int ABUF_OFF = PBUF_OFF + PBUF_BYTES;
     static constexpr int ABUF_BYTES = NWC * G * 4;
-    static constexpr int MISC_OFF = ABUF_OFF + ABUF_BYTES;  // issued-tile count, abort flag
-    static constexpr int BAR_OFF = (MISC_OFF + 8 + 7) & ~7;
-    static constexpr int SMEM = BAR_OFF + 2 * NS * 8;
+    static constexpr int MRG_OFF = ABUF_OFF + ABUF_BYTES;   // per-warp (acc, m, l) for merging
+    static constexpr int MRG_BYTES = NWC * G * (D + 2) * 4;
+    static constexpr int HDR_OFF = MRG_OFF + MRG_BYTES;     // per-stage tile header
+    static constexpr int HDR_INTS = 8;
+    static constexpr int MISC_OFF = HDR_OFF + NS * HDR_INTS * 4;  // tiles, abort, issued
+    static constexpr int BAR_OFF = (MISC_OFF + 16 + 7) & ~7;        // full[NS], empty[NS], consumer
+    static constexpr int SMEM = BAR_OFF + (2 * NS + 1) * 8;
     static constexpr int THREADS = (NWC + 1) * 32;
     static_assert(NWC % HG == 0, "warps must split evenly over the kv heads of a CTA");
     static_assert(BT % WPH == 0 && RW % RPP == 0 && PASSES >= 1, "tile rows per warp");
     static_assert(G <= LPR, "one (row, head) score per lane after the reduction");
     static_assert(BT <= 32, "one box per producer lane");
-    static_assert(NWC * G * (D + 2) * 4 <= NS * STAGE_BYTES, "merge area fits the stages");
-    static_assert(TILE_BYTES % 128 == 0, "TMA destinations stay 128-byte aligned");
+    static_assert(TILE_BYTES % 128 == 0 && STAGE_BYTES % 128 == 0, "TMA destinations stay aligned");
 };
+
+// Tile header written by the producer into the stage (balanced schedule).
+enum : int { H_B = 0, H_KVG = 1, H_TOK0 = 2, H_NVALID = 3, H_FLAGS = 4, H_SLOT = 5 };
+enum : int { F_FIRST = 1, F_LAST = 2 };
 
 // Reduce-scatter G partial dot products across the LPR lanes of a key row: after
 // log2(LPR) exchange levels the lane holds the full sum for head head_of_lane(lane).
@@ -123,15 +141,213 @@ __device__ __forceinline__ int head_of_lane(int lane) {
     return h;
 }
 
+// ---- per-warp consumer state and the per-tile step --------------------------------------
+
+template <class C>
+struct Consumer {
+    float2 q2[C::G][C::CPL][4];
+    float2 acc[C::G][C::DPV / 2];
+    float m_run, l_run;
+    int hh, row0, qlane, rgrp, hsel, warp, lane;
+
+    __device__ __forceinline__ void init(int w, int l) {
+        warp = w;
+        lane = l;
+        hh = w % C::HG;
+        row0 = (w / C::HG) * C::RW;
+        qlane = l % C::LPR;
+        rgrp = l / C::LPR;
+        hsel = head_of_lane<C::G, C::LPR>(l);
+    }
+
+    __device__ __forceinline__ void reset() {
+        m_run = -INFINITY;
+        l_run = 0.f;
+#pragma unroll
+        for (int g = 0; g < C::G; ++g)
+#pragma unroll
+            for (int j = 0; j < C::DPV / 2; ++j) acc[g][j] = make_float2(0.f, 0.f);
+    }
+
+    // q rows of this warp's kv head: `qrow(g)` points at the D bf16 values of head g.
+    template <class QRow>
+    __device__ __forceinline__ void load_q(QRow qrow, float qscale) {
+#pragma unroll
+        for (int g = 0; g < C::G; ++g) {
+#pragma unroll
+            for (int i = 0; i < C::CPL; ++i) {
+                const uint4 w = qrow(g, qlane + i * C::LPR);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = bf16x2_to_float2(ws[j]);
+                    q2[g][i][j] = make_float2(f.x * qscale, f.y * qscale);
+                }
+            }
+        }
+    }
+
+    // One staged tile: rows [row0, row0 + RW) of the tile, nvalid rows valid in the tile.
+    __device__ __forceinline__ void tile(const uint8_t *sK, const uint8_t *sV, int nvalid, float *pbuf,
+                                         float *abuf) {
+        constexpr int G = C::G, HG = C::HG;
+        const int nv_w = min(max(nvalid - row0, 0), C::RW);
+        float sc[C::PASSES];
+#pragma unroll
+        for (int ps = 0; ps < C::PASSES; ++ps) {
+            const int r = ps * C::RPP + rgrp;
+            const uint8_t *krow = sK + ((row0 + r) * HG + hh) * C::ROWB;
+            float2 a2[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) a2[g] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < C::CPL; ++c) {
+                const uint4 w = lds128(krow + (qlane + c * C::LPR) * 16);
+                const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
+                const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    a2[g] = ffma2(q2[g][c][0], k0, a2[g]);
+                    a2[g] = ffma2(q2[g][c][1], k1, a2[g]);
+                    a2[g] = ffma2(q2[g][c][2], k2, a2[g]);
+                    a2[g] = ffma2(q2[g][c][3], k3, a2[g]);
+                }
+            }
+            float part[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) part[g] = a2[g].x + a2[g].y;
+            const float v = row_reduce_scatter<G, C::LPR>(part, lane);
+            sc[ps] = (r < nv_w) ? v : -INFINITY;
+        }
+        // online softmax (base 2) for head hsel
+        float mx = sc[0];
+#pragma unroll
+        for (int ps = 1; ps < C::PASSES; ++ps) mx = fmaxf(mx, sc[ps]);
+#pragma unroll
+        for (int m = C::LPR; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, m));
+        const float m_new = fmaxf(m_run, mx);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ex2(m_run - m_use);
+        float psum = 0.f;
+#pragma unroll
+        for (int ps = 0; ps < C::PASSES; ++ps) {
+            sc[ps] = ex2(sc[ps] - m_use);
+            psum += sc[ps];
+        }
+        l_run = l_run * alpha + psum;
+        m_run = m_new;
+#pragma unroll
+        for (int ps = 0; ps < C::PASSES; ++ps) pbuf[(ps * C::RPP + rgrp) * G + hsel] = sc[ps];
+        if (rgrp == 0) abuf[hsel] = alpha;
+        __syncwarp();
+        // PV
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float a = abuf[g];
+#pragma unroll
+            for (int j = 0; j < C::DPV / 2; ++j) acc[g][j] = __fmul2_rn(acc[g][j], make_float2(a, a));
+        }
+        const uint8_t *vbase = sV + (row0 * HG + hh) * C::ROWB + lane * C::DPV * 2;
+#pragma unroll 4
+        for (int r = 0; r < nv_w; ++r) {
+            const uint8_t *vrow = vbase + r * HG * C::ROWB;
+            float2 vv[C::DPV / 2];
+            if constexpr (C::DPV == 4) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(vrow);
+                vv[0] = bf16x2_to_float2(w.x);
+                vv[1] = bf16x2_to_float2(w.y);
+            } else {
+                const uint32_t w = *reinterpret_cast<const uint32_t *>(vrow);
+                vv[0] = bf16x2_to_float2(w);
+            }
+            const float *pr = pbuf + r * G;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float pg = pr[g];
+                const float2 pp = make_float2(pg, pg);
+#pragma unroll
+                for (int j = 0; j < C::DPV / 2; ++j) acc[g][j] = ffma2(pp, vv[j], acc[g][j]);
+            }
+        }
+        __syncwarp();
+    }
+
+    // End of a unit segment: merge the WPH warps of each kv head through `mrg` and hand each
+    // merged (acc, m, l) pair of elements to `emit(hl, g, d, a0, a1, M, l)`.  All NWC
+    // consumer warps must call this together; `sync()` is their barrier and returns false
+    // when it gave up (then nothing is emitted and finish returns false).
+    template <class Sync, class Emit>
+    __device__ __forceinline__ bool finish(float *mrg, Sync sync, Emit emit) {
+        constexpr int G = C::G, D = C::D, NWC = C::NWC;
+#pragma unroll
+        for (int m = C::LPR; m < 32; m <<= 1) l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, m);
+        float *macc = mrg;                  // [NWC][G][D]
+        float *mml = mrg + NWC * G * D;     // [NWC][G][2]
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int j = 0; j < C::DPV / 2; ++j)
+                *reinterpret_cast<float2 *>(macc + (warp * G + g) * D + lane * C::DPV + 2 * j) = acc[g][j];
+        if (rgrp == 0) {
+            mml[(warp * G + hsel) * 2 + 0] = m_run;
+            mml[(warp * G + hsel) * 2 + 1] = l_run;
+        }
+        if (!sync()) return false;
+        const int tid = warp * 32 + lane;
+        for (int e = tid * 2; e < C::HG * G * D; e += NWC * 32 * 2) {
+            const int hl = e / (G * D);
+            const int g = (e / D) % G;
+            const int d = e % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < C::WPH; ++w) M = fmaxf(M, mml[((w * C::HG + hl) * G + g) * 2]);
+            const float Mu = (M == -INFINITY) ? 0.f : M;
+            float a0 = 0.f, a1 = 0.f, lv = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::WPH; ++w) {
+                const int ww = w * C::HG + hl;
+                const float f = ex2(mml[(ww * G + g) * 2] - Mu);
+                lv = fmaf(f, mml[(ww * G + g) * 2 + 1], lv);
+                const float2 x = *reinterpret_cast<const float2 *>(macc + (ww * G + g) * D + d);
+                a0 = fmaf(f, x.x, a0);
+                a1 = fmaf(f, x.y, a1);
+            }
+            emit(hl, g, d, a0, a1, M, lv);
+        }
+        return sync();  // the merge area is free again
+    }
+};
+
+__device__ __forceinline__ void store_out_pair(__nv_bfloat16 *o, float a0, float a1, float l) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    *reinterpret_cast<__nv_bfloat162 *>(o) = __floats2bfloat162_rn(a0 * inv, a1 * inv);
+}
+
+
+// Barrier among the NWC consumer warps on an mbarrier (count NWC, one arrival per warp),
+// so that a wait is bounded like every other wait in the pipeline.
+struct ConsumerBarrier {
+    uint64_t *bar;
+    uint32_t phase;
+    __device__ __forceinline__ bool sync(int lane) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
+        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar, phase & 1));
+        ++phase;
+        return ok;
+    }
+};
+
+// ---- per-sequence schedule: one CTA per (unit, split) ------------------------------------
+
 template <class C, bool PAGED>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
     split_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                  const SplitParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    constexpr int D = C::D, G = C::G, HG = C::HG, NWC = C::NWC, BT = C::BT, NS = C::NS;
+    constexpr int G = C::G, HG = C::HG, NWC = C::NWC, BT = C::BT, NS = C::NS, D = C::D;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- work unit -------------------------------------------------------------------
     const int nkvg = p.Hkv / HG;
     const int units = p.B * nkvg;
     const int s = blockIdx.x / units;
@@ -163,14 +379,12 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     }
     __syncthreads();
 
-    if (warp == NWC) {
-        // ---- producer warp: page lookup + TMA issue ------------------------------------
+    if (warp == NWC) {  // ---- producer warp: page lookup + TMA issue
         if (lane == 0) {
             prefetch_tensormap(&mapK);
             prefetch_tensormap(&mapV);
         }
         const int R = PAGED ? p.box_rows : BT;
-        const int kvh0 = kvg * HG;
         const int32_t *table = PAGED ? p.block_table + (long long)b * p.max_pages : nullptr;
         auto lookup = [&](int tile) -> int {  // page id of this lane's box of `tile`
             if (!PAGED) return b;
@@ -201,11 +415,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
             __syncwarp();
             if (lane < nbox) {
                 uint8_t *sK = smem + st * C::STAGE_BYTES + lane * R * HG * C::ROWB;
-                uint8_t *sV = sK + C::TILE_BYTES;
                 const int tt = t + lane * R;
                 const int slot = PAGED ? tt % p.page_size : tt;
-                tma_load_4d(sK, &mapK, 0, kvh0, slot, pg, &full[st]);
-                tma_load_4d(sV, &mapV, 0, kvh0, slot, pg, &full[st]);
+                tma_load_4d(sK, &mapK, 0, kvg * HG, slot, pg, &full[st]);
+                tma_load_4d(sK + C::TILE_BYTES, &mapV, 0, kvg * HG, slot, pg, &full[st]);
             }
             issued = i + 1;
         }
@@ -214,220 +427,316 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
         return;
     }
 
-    // ---- consumer warps --------------------------------------------------------------
-    const int hh = warp % HG;           // kv head within the CTA's group
-    const int ph = warp / HG;           // row phase of this warp
-    const int kvh = kvg * HG + hh;
-    const int row0 = ph * C::RW;
-    const int qlane = lane % C::LPR;
-    const int rgrp = lane / C::LPR;
-    const int hsel = head_of_lane<G, C::LPR>(lane);
-
-    float2 q2[G][C::CPL][4];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const __nv_bfloat16 *qrow = p.q + (long long)b * p.q_sb + (long long)(kvh * G + g) * p.q_sh;
-#pragma unroll
-        for (int i = 0; i < C::CPL; ++i) {
-            const uint4 w = __ldg(reinterpret_cast<const uint4 *>(qrow + 8 * (qlane + i * C::LPR)));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 f = bf16x2_to_float2(ws[j]);
-                q2[g][i][j] = make_float2(f.x * p.qscale, f.y * p.qscale);
-            }
-        }
-    }
-
-    float m_run = -INFINITY, l_run = 0.f;
-    float2 acc[G][C::DPV / 2 > 0 ? C::DPV / 2 : 1];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int j = 0; j < C::DPV / 2; ++j) acc[g][j] = make_float2(0.f, 0.f);
+    // ---- consumer warps
+    Consumer<C> cs;
+    cs.init(warp, lane);
+    cs.reset();
+    const int kvh = kvg * HG + cs.hh;
+    const __nv_bfloat16 *qb = p.q + (long long)b * p.q_sb;
+    cs.load_q([&](int g, int chunk) {
+        return __ldg(reinterpret_cast<const uint4 *>(qb + (long long)(kvh * G + g) * p.q_sh + 8 * chunk));
+    }, p.qscale);
     float *pbuf = reinterpret_cast<float *>(smem + C::PBUF_OFF) + warp * C::RW * G;
     float *abuf = reinterpret_cast<float *>(smem + C::ABUF_OFF) + warp * G;
-
     int consumed = 0;
     for (int i = 0; i < ntiles; ++i) {
         const int st = i % NS;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (i / NS) & 1))) {  // warp-uniform
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (i / NS) & 1))) {
             misc[1] = 1;
             break;
         }
         const uint8_t *sK = smem + st * C::STAGE_BYTES;
-        const uint8_t *sV = sK + C::TILE_BYTES;
-        const int nvalid = min(BT, tok1 - (tok0 + i * BT));
-        const int nv_w = min(max(nvalid - row0, 0), C::RW);
-
-        // scores: one (row, head) value per lane per pass
-        float sc[C::PASSES];
-#pragma unroll
-        for (int ps = 0; ps < C::PASSES; ++ps) {
-            const int r = ps * C::RPP + rgrp;
-            const uint8_t *krow = sK + ((row0 + r) * HG + hh) * C::ROWB;
-            float2 a2[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) a2[g] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int c = 0; c < C::CPL; ++c) {
-                const uint4 w = lds128(krow + (qlane + c * C::LPR) * 16);
-                const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
-                const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    a2[g] = ffma2(q2[g][c][0], k0, a2[g]);
-                    a2[g] = ffma2(q2[g][c][1], k1, a2[g]);
-                    a2[g] = ffma2(q2[g][c][2], k2, a2[g]);
-                    a2[g] = ffma2(q2[g][c][3], k3, a2[g]);
-                }
-            }
-            float part[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) part[g] = a2[g].x + a2[g].y;
-            const float v = row_reduce_scatter<G, C::LPR>(part, lane);
-            sc[ps] = (r < nv_w) ? v : -INFINITY;
-        }
-
-        // online softmax (base 2) for head hsel
-        float mx = sc[0];
-#pragma unroll
-        for (int ps = 1; ps < C::PASSES; ++ps) mx = fmaxf(mx, sc[ps]);
-#pragma unroll
-        for (int m = C::LPR; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, m));
-        const float m_new = fmaxf(m_run, mx);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = ex2(m_run - m_use);
-        float psum = 0.f;
-#pragma unroll
-        for (int ps = 0; ps < C::PASSES; ++ps) {
-            sc[ps] = ex2(sc[ps] - m_use);
-            psum += sc[ps];
-        }
-        l_run = l_run * alpha + psum;
-        m_run = m_new;
-#pragma unroll
-        for (int ps = 0; ps < C::PASSES; ++ps) pbuf[(ps * C::RPP + rgrp) * G + hsel] = sc[ps];
-        if (rgrp == 0) abuf[hsel] = alpha;
-        __syncwarp();
-
-        // PV
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float a = abuf[g];
-#pragma unroll
-            for (int j = 0; j < C::DPV / 2; ++j) acc[g][j] = __fmul2_rn(acc[g][j], make_float2(a, a));
-        }
-        const uint8_t *vbase = sV + (row0 * HG + hh) * C::ROWB + lane * C::DPV * 2;
-#pragma unroll 4
-        for (int r = 0; r < nv_w; ++r) {
-            const uint8_t *vrow = vbase + r * HG * C::ROWB;
-            float2 vv[C::DPV / 2];
-            if constexpr (C::DPV == 4) {
-                const uint2 w = *reinterpret_cast<const uint2 *>(vrow);
-                vv[0] = bf16x2_to_float2(w.x);
-                vv[1] = bf16x2_to_float2(w.y);
-            } else {
-                const uint32_t w = *reinterpret_cast<const uint32_t *>(vrow);
-                vv[0] = bf16x2_to_float2(w);
-            }
-            const float *pr = pbuf + r * G;
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float pg = pr[g];
-                const float2 pp = make_float2(pg, pg);
-#pragma unroll
-                for (int j = 0; j < C::DPV / 2; ++j) acc[g][j] = ffma2(pp, vv[j], acc[g][j]);
-            }
-        }
-        __syncwarp();
+        cs.tile(sK, sK + C::TILE_BYTES, min(BT, tok1 - (tok0 + i * BT)), pbuf, abuf);
         if (lane == 0) mbar_arrive(&empty[st]);
         consumed = i + 1;
     }
-
-    // ---- merge the warps of each kv head and write --------------------------------------
-#pragma unroll
-    for (int m = C::LPR; m < 32; m <<= 1) l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, m);
-    __syncthreads();  // every consumer is done with the stages; producer has finished issuing
-    if (misc[1]) {
-        // A wait timed out.  Drain the copies still in flight (bounded), write nothing.
-        if (threadIdx.x == 0) {
+    __syncthreads();  // every consumer is done; the producer has finished issuing
+    if (misc[1]) {    // a wait timed out: drain the copies still in flight (bounded), write nothing
+        if (threadIdx.x == 0)
             for (int i = consumed; i < misc[0]; ++i) (void)mbar_wait(&full[i % NS], (i / NS) & 1);
-        }
         return;
     }
-    float *macc = reinterpret_cast<float *>(smem);                // [NWC][G][D]
-    float *mml = macc + NWC * G * D;                               // [NWC][G][2]
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int j = 0; j < C::DPV / 2; ++j)
-            *reinterpret_cast<float2 *>(macc + (warp * G + g) * D + lane * C::DPV + 2 * j) = acc[g][j];
-    if (rgrp == 0) {
-        mml[(warp * G + hsel) * 2 + 0] = m_run;
-        mml[(warp * G + hsel) * 2 + 1] = l_run;
-    }
-    named_sync(1, NWC * 32);
-
     const bool direct = (nsplit == 1);
-    for (int e = threadIdx.x * 2; e < HG * G * D; e += NWC * 32 * 2) {
-        const int hl = e / (G * D);
-        const int g = (e / D) % G;
-        const int d = e % D;
-        float M = -INFINITY;
+    cs.finish(reinterpret_cast<float *>(smem + C::MRG_OFF),
+              [] { named_sync(1, NWC * 32); return true; },
+              [&](int hl, int g, int d, float a0, float a1, float M, float lv) {
+                  const int hq = (kvg * HG + hl) * G + g;
+                  if (direct) {
+                      store_out_pair(p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh + d, a0, a1, lv);
+                  } else {
+                      const long long row = ((long long)b * p.num_splits + s) * p.Hq + hq;
+                      *reinterpret_cast<float2 *>(p.o_part + row * D + d) = make_float2(a0, a1);
+                      if (d == 0) *reinterpret_cast<float2 *>(p.ml_part + row * 2) = make_float2(M, lv);
+                  }
+              });
+}
+
+// ---- balanced schedule: persistent CTAs over equal ranges of the flattened tile space ---
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 #pragma unroll
-        for (int w = 0; w < C::WPH; ++w) M = fmaxf(M, mml[((w * HG + hl) * G + g) * 2]);
-        const float Mu = (M == -INFINITY) ? 0.f : M;
-        float a0 = 0.f, a1 = 0.f, lv = 0.f;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+template <class C, bool PAGED>
+__global__ void __launch_bounds__(C::THREADS, C::MINB)
+    balanced_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                    const __grid_constant__ CUtensorMap mapQ, const SplitParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int G = C::G, HG = C::HG, NWC = C::NWC, BT = C::BT, NS = C::NS, D = C::D, HPU = C::HPU;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x;
+    const int P = p.num_ctas;
+    const int nkvg = p.Hkv / HG;
+
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *empty = full + NS;
+    uint64_t *cbar = empty + NS;
+    volatile int *misc = reinterpret_cast<volatile int *>(smem + C::MISC_OFF);  // tiles, abort, issued
+    int *hdr_all = reinterpret_cast<int *>(smem + C::HDR_OFF);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NWC);
+        }
+        mbar_init(cbar, NWC);
+        misc[0] = 0;
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+    // the combine grid may start launching now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __syncthreads();
+
+    // tiles of a sequence (an empty sequence still takes one tile, which writes its zeros)
+    auto seq_len = [&](int b) -> int {
+        int L = __ldg(p.seq_lens + b);
+        if (L < 0 || L > p.max_kv_len) {
+            flag_error(DAP_DEVERR_SEQLEN);
+            L = min(max(L, 0), p.max_kv_len);
+        }
+        return L;
+    };
+    auto tiles_of = [](int L) { return max(1, (L + BT - 1) / BT); };
+
+    long long s_c = 0;
+    if (warp == NWC) {
+        long long total = 0;
+        for (int base = 0; base < p.B; base += 32) {
+            const int b = base + lane;
+            int tb = b < p.B ? tiles_of(seq_len(b)) : 0;
 #pragma unroll
-        for (int w = 0; w < C::WPH; ++w) {
-            const int ww = w * HG + hl;
-            const float f = ex2(mml[(ww * G + g) * 2] - Mu);
-            lv = fmaf(f, mml[(ww * G + g) * 2 + 1], lv);
-            const float2 x = *reinterpret_cast<const float2 *>(macc + (ww * G + g) * D + d);
-            a0 = fmaf(f, x.x, a0);
-            a1 = fmaf(f, x.y, a1);
+            for (int o = 16; o >= 1; o >>= 1) tb += __shfl_xor_sync(0xFFFFFFFFu, tb, o);
+            total += tb;
         }
-        const int hq = (kvg * HG + hl) * G + g;
-        if (direct) {
-            const float inv = lv > 0.f ? 1.f / lv : 0.f;
-            *reinterpret_cast<__nv_bfloat162 *>(p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh + d) =
-                __floats2bfloat162_rn(a0 * inv, a1 * inv);
-        } else {
-            const long long row = ((long long)b * p.num_splits + s) * p.Hq + hq;
-            *reinterpret_cast<float2 *>(p.o_part + row * D + d) = make_float2(a0, a1);
-            if (d == 0) *reinterpret_cast<float2 *>(p.ml_part + row * 2) = make_float2(M, lv);
+        const long long T = total * nkvg;
+        s_c = (long long)c * T / P;
+        const long long e_c = (long long)(c + 1) * T / P;
+        if (lane == 0) {
+            misc[0] = (int)(e_c - s_c);
+            if (c == 0) *p.total_tiles = T;
         }
+    }
+    __syncthreads();
+    const int ntiles = misc[0];
+
+    if (warp == NWC) {  // ---- producer warp
+        if (lane == 0) {
+            prefetch_tensormap(&mapK);
+            prefetch_tensormap(&mapV);
+            prefetch_tensormap(&mapQ);
+        }
+        int issued = 0;
+        if (ntiles > 0) {
+            // locate the unit holding tile s_c
+            long long before = 0;
+            int b = -1, tb = 1;
+            for (int base = 0; base < p.B && b < 0; base += 32) {
+                const int bb = base + lane;
+                const int t1 = bb < p.B ? tiles_of(seq_len(bb)) : 0;
+                const int w = t1 * nkvg;
+                const int incl = warp_incl_scan(w, lane);
+                const unsigned hit = __ballot_sync(0xFFFFFFFFu, bb < p.B && before + incl > s_c);
+                if (hit) {
+                    const int f = __ffs(hit) - 1;
+                    b = base + f;
+                    tb = __shfl_sync(0xFFFFFFFFu, t1, f);
+                    before += __shfl_sync(0xFFFFFFFFu, incl - w, f);
+                } else {
+                    before += __shfl_sync(0xFFFFFFFFu, incl, 31);
+                }
+            }
+            const long long rem = s_c - before;
+            int kvg = (int)(rem / tb);
+            int j = (int)(rem % tb);
+            int L = seq_len(b);
+            bool in_u0 = true;  // the cursor is still in the unit the range starts in
+            int seg_j0 = j;
+            const int R = PAGED ? p.box_rows : BT;
+
+            auto lookup = [&](int bb, int jj, int LL) -> int {  // page of this lane's box
+                if (!PAGED) return bb;
+                const int t = jj * BT + lane * R;
+                if (lane * R >= BT || t >= LL) return 0;
+                int pg = __ldg(p.block_table + (long long)bb * p.max_pages + t / p.page_size);
+                if (pg < 0 || pg >= p.num_pages) {
+                    flag_error(DAP_DEVERR_PAGE);
+                    pg = 0;
+                }
+                return pg;
+            };
+            int pg_next = lookup(b, j, L);
+            for (int i = 0; i < ntiles; ++i) {
+                const int st = i % NS;
+                const int pg = pg_next;
+                // cursor of the next tile
+                int nb = b, nk = kvg, nj = j + 1, nL = L, ntb = tb;
+                bool n_in_u0 = in_u0;
+                if (nj == tb) {
+                    nj = 0;
+                    n_in_u0 = false;
+                    if (++nk == nkvg) {
+                        nk = 0;
+                        ++nb;
+                        nL = (nb < p.B && i + 1 < ntiles) ? seq_len(nb) : 0;
+                        ntb = tiles_of(nL);
+                    }
+                }
+                if (i + 1 < ntiles) pg_next = lookup(nb, nj, nL);
+                if (i >= NS && !__all_sync(0xFFFFFFFFu, mbar_wait(&empty[st], ((i / NS) - 1) & 1))) {
+                    misc[1] = 1;
+                    break;
+                }
+                const bool first = (i == 0) || (j == 0);
+                const bool last = (i == ntiles - 1) || (j == tb - 1);
+                if (first) seg_j0 = j;
+                const int nvalid = max(0, min(BT, L - j * BT));
+                const int slot = (seg_j0 == 0 && j == tb - 1) ? -1 : 2 * c + (in_u0 ? 0 : 1);
+                const bool need_q = first && nvalid > 0;
+                const int nbox = PAGED ? (nvalid + R - 1) / R : (nvalid > 0 ? 1 : 0);
+                const uint32_t bytes = (uint32_t)(nbox * R * HG * C::ROWB * 2 + (need_q ? C::QBYTES : 0));
+                uint8_t *stage = smem + st * C::STAGE_BYTES;
+                if (lane == 0) {
+                    int *h = hdr_all + st * C::HDR_INTS;
+                    h[H_B] = b;
+                    h[H_KVG] = kvg;
+                    h[H_TOK0] = j * BT;
+                    h[H_NVALID] = nvalid;
+                    h[H_FLAGS] = (first ? F_FIRST : 0) | (last ? F_LAST : 0);
+                    h[H_SLOT] = slot;
+                    if (j == 0) {  // this CTA holds the unit's first tile: record where it starts
+                        p.unit_info[2 * (b * nkvg + kvg)] = (int)(s_c + i);
+                        p.unit_info[2 * (b * nkvg + kvg) + 1] = tb;
+                    }
+                    mbar_arrive_expect_tx(&full[st], bytes);
+                }
+                __syncwarp();
+                if (lane < nbox) {
+                    const int tt = j * BT + lane * R;
+                    const int slot_row = PAGED ? tt % p.page_size : tt;
+                    uint8_t *sK = stage + lane * R * HG * C::ROWB;
+                    tma_load_4d(sK, &mapK, 0, kvg * HG, slot_row, pg, &full[st]);
+                    tma_load_4d(sK + C::TILE_BYTES, &mapV, 0, kvg * HG, slot_row, pg, &full[st]);
+                }
+                if (need_q && lane == 0)
+                    tma_load_3d(stage + 2 * C::TILE_BYTES, &mapQ, 0, kvg * HPU, b, &full[st]);
+                b = nb;
+                kvg = nk;
+                j = nj;
+                L = nL;
+                tb = ntb;
+                in_u0 = n_in_u0;
+                issued = i + 1;
+            }
+        }
+        if (lane == 0) misc[2] = issued;
+        __syncthreads();  // pairs with the consumers' final __syncthreads
+        return;
+    }
+
+    // ---- consumer warps
+    Consumer<C> cs;
+    cs.init(warp, lane);
+    cs.reset();
+    float *pbuf = reinterpret_cast<float *>(smem + C::PBUF_OFF) + warp * C::RW * G;
+    float *abuf = reinterpret_cast<float *>(smem + C::ABUF_OFF) + warp * G;
+    float *mrg = reinterpret_cast<float *>(smem + C::MRG_OFF);
+    ConsumerBarrier cb{cbar, 0u};
+    int consumed = 0;
+    for (int i = 0; i < ntiles; ++i) {
+        const int st = i % NS;
+        if (__any_sync(0xFFFFFFFFu, misc[1] != 0)) break;  // another warp gave up
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (i / NS) & 1))) {
+            misc[1] = 1;
+            break;
+        }
+        const uint8_t *stage = smem + st * C::STAGE_BYTES;
+        const int *h = hdr_all + st * C::HDR_INTS;
+        const int b = h[H_B], kvg = h[H_KVG], nvalid = h[H_NVALID], flags = h[H_FLAGS], slot = h[H_SLOT];
+        if (flags & F_FIRST) {
+            cs.reset();
+            if (nvalid > 0) {
+                const uint8_t *sq = stage + 2 * C::TILE_BYTES + cs.hh * G * C::ROWB;
+                cs.load_q([&](int g, int chunk) { return lds128(sq + g * C::ROWB + chunk * 16); }, p.qscale);
+            }
+        }
+        cs.tile(stage, stage + C::TILE_BYTES, nvalid, pbuf, abuf);
+        if (lane == 0) mbar_arrive(&empty[st]);
+        consumed = i + 1;
+        if (flags & F_LAST) {
+            const bool ok = cs.finish(mrg, [&] { return cb.sync(lane); },
+                                      [&](int hl, int g, int d, float a0, float a1, float M, float lv) {
+                                          const int hl2 = hl * G + g;
+                                          if (slot < 0) {
+                                              const int hq = kvg * HPU + hl2;
+                                              store_out_pair(p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh + d,
+                                                             a0, a1, lv);
+                                          } else {
+                                              const long long row = (long long)slot * HPU + hl2;
+                                              *reinterpret_cast<float2 *>(p.o_part + row * D + d) = make_float2(a0, a1);
+                                              if (d == 0)
+                                                  *reinterpret_cast<float2 *>(p.ml_part + row * 2) = make_float2(M, lv);
+                                          }
+                                      });
+            if (!ok) {
+                misc[1] = 1;
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    if (misc[1] && threadIdx.x == 0) {  // a wait gave up: let the copies in flight land (bounded)
+        const int issued = misc[2];
+        for (int i = consumed; i < issued; ++i) (void)mbar_wait(&full[i % NS], (i / NS) & 1);
     }
 }
 
-// Merge the split partials of every (sequence, query head) with more than one split, in
-// split order: M = max_s m_s, out = sum_s 2^(m_s-M) acc_s / sum_s 2^(m_s-M) l_s.  One warp
-// per output row (AstrAI csrc log, split-KV commit: the combine kernel).
+// ---- combine kernels -------------------------------------------------------------------
+// Merge the partials of every output row that more than one CTA worked on, in a fixed
+// order: M = max_s m_s, out = sum_s 2^(m_s-M) acc_s / sum_s 2^(m_s-M) l_s (AstrAI csrc log,
+// split-KV commit: the combine kernel; numerics commit: guarded division).  One warp per
+// output row, lanes over D.  Both wait for the split grid (programmatic dependent launch).
+
 template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
-    constexpr int DPV = D / 32;
-    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= p.B * p.Hq) return;
-    const int b = gw / p.Hq, hq = gw - b * p.Hq;
-    const int L = min(max(p.seq_lens[b], 0), p.max_kv_len);
-    const int nsplit = max(1, (L + p.chunk - 1) / p.chunk);
-    if (nsplit == 1) return;
-    const long long row0 = (long long)b * p.num_splits * p.Hq + hq;
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p.ml_part[(row0 + (long long)s * p.Hq) * 2]);
-    const float Mu = (M == -INFINITY) ? 0.f : M;
+struct RowMerge {
+    static constexpr int DPV = D / 32;
     float acc[DPV];
+    float lsum, M, Mu;
+    __device__ __forceinline__ void begin(float m_max) {
+        M = m_max;
+        Mu = (M == -INFINITY) ? 0.f : M;
+        lsum = 0.f;
 #pragma unroll
-    for (int j = 0; j < DPV; ++j) acc[j] = 0.f;
-    float lsum = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-        const long long row = row0 + (long long)s * p.Hq;
-        const float2 ml = *reinterpret_cast<const float2 *>(p.ml_part + row * 2);
+        for (int j = 0; j < DPV; ++j) acc[j] = 0.f;
+    }
+    __device__ __forceinline__ void add(const float *o, float2 ml, int lane) {
         const float f = ex2(ml.x - Mu);
         lsum = fmaf(f, ml.y, lsum);
-        const float *o = p.o_part + row * D + lane * DPV;
+        o += lane * DPV;
         if constexpr (DPV == 4) {
             const float4 x = *reinterpret_cast<const float4 *>(o);
             acc[0] = fmaf(f, x.x, acc[0]);
@@ -440,48 +749,151 @@ __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
             acc[1] = fmaf(f, x.y, acc[1]);
         }
     }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    __nv_bfloat16 *o = p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh + lane * DPV;
+    __device__ __forceinline__ void store(__nv_bfloat16 *o, int lane) {
 #pragma unroll
-    for (int j = 0; j < DPV; j += 2)
-        *reinterpret_cast<__nv_bfloat162 *>(o + j) = __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
+        for (int j = 0; j < DPV; j += 2) store_out_pair(o + lane * DPV + j, acc[j], acc[j + 1], lsum);
+    }
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= p.B * p.Hq) return;
+    const int b = gw / p.Hq, hq = gw - b * p.Hq;
+    const int L = min(max(p.seq_lens[b], 0), p.max_kv_len);
+    const int nsplit = max(1, (L + p.chunk - 1) / p.chunk);
+    if (nsplit == 1) return;
+    const long long row0 = (long long)b * p.num_splits * p.Hq + hq;
+    float M = -INFINITY;
+    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, p.ml_part[(row0 + (long long)s * p.Hq) * 2]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    RowMerge<D> r;
+    r.begin(M);
+#pragma unroll 4
+    for (int s = 0; s < nsplit; ++s) {
+        const long long row = row0 + (long long)s * p.Hq;
+        r.add(p.o_part + row * D, *reinterpret_cast<const float2 *>(p.ml_part + row * 2), lane);
+    }
+    r.store(p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh, lane);
 }
 
-// ---- host side -----------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) combine_balanced_kernel(const SplitParams p, int hpu, int nkvg) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= p.B * nkvg * hpu) return;
+    const int u = gw / hpu, hl2 = gw - u * hpu;
+    const long long start = p.unit_info[2 * u], tb = p.unit_info[2 * u + 1];
+    const long long T = *p.total_tiles;
+    const long long P = p.num_ctas;
+    const int c_first = (int)(((start + 1) * P - 1) / T);
+    const int c_last = (int)(((start + tb) * P - 1) / T);
+    if (c_first == c_last) return;  // finished in place by one CTA
+    auto slot_of = [&](int c) -> int {
+        const long long s_c = (long long)c * T / P;
+        return 2 * c + ((c == c_first && s_c < start) ? 1 : 0);
+    };
+    auto nonempty = [&](int c) { return (long long)c * T / P < (long long)(c + 1) * T / P; };
+    float M = -INFINITY;
+    for (int c = c_first + lane; c <= c_last; c += 32)
+        if (nonempty(c)) M = fmaxf(M, p.ml_part[((long long)slot_of(c) * hpu + hl2) * 2]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    RowMerge<D> r;
+    r.begin(M);
+    for (int c = c_first; c <= c_last; ++c) {
+        if (!nonempty(c)) continue;
+        const long long row = (long long)slot_of(c) * hpu + hl2;
+        r.add(p.o_part + row * D, *reinterpret_cast<const float2 *>(p.ml_part + row * 2), lane);
+    }
+    const int b = u / nkvg, kvg = u - b * nkvg;
+    const int hq = kvg * hpu + hl2;
+    r.store(p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh, lane);
+}
+
+// ---- host side ----------------------------------------------------------------------------
 
 namespace {
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
 
-// [D, Hkv, rows, outer] bf16 view of a cache, box [D, HG, box_rows, 1].
-bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv, long long rows,
-                      long long outer, int HG, int box_rows) {
+bool encode_bf16(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+                 const cuuint64_t *strides_bytes, const cuuint32_t *box) {
     EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
     if (!enc) return false;
-    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows, (cuuint64_t)outer};
-    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2,
-                                   (cuuint64_t)rows * Hkv * D * 2};
-    const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)HG, (cuuint32_t)box_rows, 1u};
-    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
+               strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int gcd_int(int a, int b) {
-    while (b) {
-        const int t = a % b;
-        a = b;
-        b = t;
+// [D, Hkv, rows, outer] view of a cache, box [D, HG, box_rows, 1].
+bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv, long long rows, long long outer,
+                      int HG, int box_rows) {
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows, (cuuint64_t)outer};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)rows * Hkv * D * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)HG, (cuuint32_t)box_rows, 1u};
+    return encode_bf16(map, base, 4, dims, strides, box);
+}
+
+// [D, Hq, B] view of q with its strides, box [D, hpu, 1].
+bool encode_q_map(CUtensorMap *map, const DecodeArgs &a, int hpu) {
+    const cuuint64_t dims[3] = {(cuuint64_t)a.D, (cuuint64_t)a.Hq, (cuuint64_t)a.B};
+    // a stride over an extent of 1 is never used; give TMA a valid one
+    const long long sh = a.Hq > 1 ? a.q_sh : a.D;
+    const long long sb = a.B > 1 ? a.q_sb : (long long)a.Hq * sh;
+    const cuuint64_t strides[2] = {(cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)a.D, (cuuint32_t)hpu, 1u};
+    return encode_bf16(map, a.q, 3, dims, strides, box);
+}
+
+int gcd_int(int x, int y) {
+    while (y) {
+        const int t = x % y;
+        x = y;
+        y = t;
     }
-    return a;
+    return x;
+}
+
+std::mutex g_attr_mu;
+
+// Raise the dynamic shared-memory limit of `kern` once, and return its resident CTAs per SM.
+template <class K>
+int prepare_kernel(K kern, int threads, int smem, int *cached_occ) {
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    if (*cached_occ > 0) return *cached_occ;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem) != cudaSuccess) return 0;
+    *cached_occ = occ;
+    return occ;
+}
+
+template <class K, class... Args>
+cudaError_t launch_dependent(K kern, dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 template <class C, bool PAGED>
-dap_status launch_split(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
+dap_status launch_per_sequence(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
     const int R = PAGED ? gcd_int(a.page_size, C::BT) : C::BT;
     p.box_rows = R;
     CUtensorMap mk, mv;
@@ -491,33 +903,91 @@ dap_status launch_split(const DecodeArgs &a, SplitParams &p, cudaStream_t stream
         !encode_cache_map(&mv, a.v, a.D, a.Hkv, rows, outer, C::HG, R))
         return DAP_ERR_CUDA;
     auto kern = split_kernel<C, PAGED>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-        return DAP_ERR_CUDA;
+    static int occ = 0;
+    if (prepare_kernel(kern, C::THREADS, C::SMEM, &occ) <= 0) return DAP_ERR_CUDA;
     const long long grid = (long long)a.B * (a.Hkv / C::HG) * a.num_splits;
     if (grid > 0x7FFFFFFFLL) return DAP_ERR_SHAPE;
+    p.o_part = static_cast<float *>(a.workspace);
+    p.ml_part = a.num_splits > 1 ? reinterpret_cast<float *>(static_cast<char *>(a.workspace) +
+                                                             partial_acc_bytes(a.B, a.Hq, a.D, a.num_splits))
+                                 : nullptr;
     if (g_trace.split_begin) cudaEventRecord(g_trace.split_begin, stream);
     kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(mk, mv, p);
     if (cudaGetLastError() != cudaSuccess) return DAP_ERR_CUDA;
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
     if (a.num_splits > 1) {
-        const int rows_out = a.B * a.Hq;
-        if (a.D == 128)
-            combine_kernel<128><<<(rows_out + 7) / 8, 256, 0, stream>>>(p);
-        else
-            combine_kernel<64><<<(rows_out + 7) / 8, 256, 0, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return DAP_ERR_CUDA;
+        const dim3 cgrid((unsigned)((a.B * a.Hq + 7) / 8));
+        const cudaError_t e = a.D == 128 ? launch_dependent(combine_kernel<128>, cgrid, dim3(256), stream, p)
+                                         : launch_dependent(combine_kernel<64>, cgrid, dim3(256), stream, p);
+        if (e != cudaSuccess) return DAP_ERR_CUDA;
     }
     if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);
     return DAP_OK;
 }
 
+template <class C, bool PAGED>
+dap_status launch_balanced(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
+    const int R = PAGED ? gcd_int(a.page_size, C::BT) : C::BT;
+    p.box_rows = R;
+    CUtensorMap mk, mv, mq;
+    const long long rows = PAGED ? a.page_size : a.max_len;
+    const long long outer = PAGED ? a.num_pages : a.B;
+    if (!encode_cache_map(&mk, a.k, a.D, a.Hkv, rows, outer, C::HG, R) ||
+        !encode_cache_map(&mv, a.v, a.D, a.Hkv, rows, outer, C::HG, R) || !encode_q_map(&mq, a, C::HPU))
+        return DAP_ERR_CUDA;
+    auto kern = balanced_kernel<C, PAGED>;
+    static int occ = 0;
+    const int per_sm = prepare_kernel(kern, C::THREADS, C::SMEM, &occ);
+    const int sms = dap_device_sm_count();
+    if (per_sm <= 0 || sms <= 0) return DAP_ERR_CUDA;
+    const int P = std::min(sms * per_sm, kMaxPersistentCtas);
+    const int nkvg = a.Hkv / C::HG;
+    const BalancedLayout lay = balanced_layout(a.B, nkvg, C::HPU, a.D);
+    char *ws = static_cast<char *>(a.workspace);
+    p.o_part = reinterpret_cast<float *>(ws + lay.acc);
+    p.ml_part = reinterpret_cast<float *>(ws + lay.ml);
+    p.unit_info = reinterpret_cast<int *>(ws + lay.info);
+    p.total_tiles = reinterpret_cast<long long *>(ws + lay.total);
+    p.num_ctas = P;
+    if (g_trace.split_begin) cudaEventRecord(g_trace.split_begin, stream);
+    kern<<<P, C::THREADS, C::SMEM, stream>>>(mk, mv, mq, p);
+    if (cudaGetLastError() != cudaSuccess) return DAP_ERR_CUDA;
+    if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
+    const dim3 cgrid((unsigned)((a.B * nkvg * C::HPU + 7) / 8));
+    const cudaError_t e =
+        a.D == 128 ? launch_dependent(combine_balanced_kernel<128>, cgrid, dim3(256), stream, p, (int)C::HPU, nkvg)
+                   : launch_dependent(combine_balanced_kernel<64>, cgrid, dim3(256), stream, p, (int)C::HPU, nkvg);
+    if (e != cudaSuccess) return DAP_ERR_CUDA;
+    if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);
+    return DAP_OK;
+}
+
+// The tuned configuration of each (D, G): one kv head per CTA, four consumer warps,
+// 32-token tiles, four stages; three CTAs per SM (two for G = 8, whose q and accumulators
+// take more registers).
 template <int D, int G>
-dap_status dispatch_layout(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
-    using C = SplitCfg<D, G, 1, 4, 32, 4, (G <= 4 ? 3 : 2)>;
-    return a.paged ? launch_split<C, true>(a, p, stream) : launch_split<C, false>(a, p, stream);
+using CfgFor = SplitCfg<D, G, 1, 4, 32, 4, (G <= 4 ? 3 : 2)>;
+
+template <int D, int G>
+dap_status dispatch(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
+    using C = CfgFor<D, G>;
+    if (a.num_splits == 0)
+        return a.paged ? launch_balanced<C, true>(a, p, stream) : launch_balanced<C, false>(a, p, stream);
+    return a.paged ? launch_per_sequence<C, true>(a, p, stream) : launch_per_sequence<C, false>(a, p, stream);
 }
 
 }  // namespace
+
+int balanced_heads_per_unit(int D, int G) {
+    (void)D;
+    return G;  // CfgFor uses one kv head per unit
+}
+
+int balanced_kv_heads_per_unit(int D, int G) {
+    (void)D;
+    (void)G;
+    return 1;
+}
 
 bool read_errors_decode(unsigned int *flags, bool clear) {
     unsigned int v = 0;
@@ -531,7 +1001,7 @@ bool read_errors_decode(unsigned int *flags, bool clear) {
 }
 
 dap_status launch_decode(const DecodeArgs &a, cudaStream_t stream) {
-    SplitParams p;
+    SplitParams p = {};
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
     p.q_sb = a.q_sb;
     p.q_sh = a.q_sh;
@@ -544,35 +1014,28 @@ dap_status launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     p.Hkv = a.Hkv;
     p.page_size = a.paged ? a.page_size : a.max_len;
     p.num_pages = a.paged ? a.num_pages : a.B;
-    p.box_rows = 0;
     p.num_splits = a.num_splits;
     p.chunk = a.chunk;
     p.qscale = a.scale * 1.4426950408889634f;
-    p.o_part = static_cast<float *>(a.workspace);
-    p.ml_part = a.num_splits > 1
-                    ? reinterpret_cast<float *>(static_cast<char *>(a.workspace) +
-                                                partial_acc_bytes(a.B, a.Hq, a.D, a.num_splits))
-                    : nullptr;
     p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.o_sb = a.o_sb;
     p.o_sh = a.o_sh;
     const int G = a.Hq / a.Hkv;
     if (a.D == 128) {
         switch (G) {
-            case 1: return dispatch_layout<128, 1>(a, p, stream);
-            case 2: return dispatch_layout<128, 2>(a, p, stream);
-            case 4: return dispatch_layout<128, 4>(a, p, stream);
-            case 8: return dispatch_layout<128, 8>(a, p, stream);
+            case 1: return dispatch<128, 1>(a, p, stream);
+            case 2: return dispatch<128, 2>(a, p, stream);
+            case 4: return dispatch<128, 4>(a, p, stream);
+            case 8: return dispatch<128, 8>(a, p, stream);
         }
     } else if (a.D == 64) {
         switch (G) {
-            case 1: return dispatch_layout<64, 1>(a, p, stream);
-            case 2: return dispatch_layout<64, 2>(a, p, stream);
-            case 4: return dispatch_layout<64, 4>(a, p, stream);
-            case 8: return dispatch_layout<64, 8>(a, p, stream);
+            case 1: return dispatch<64, 1>(a, p, stream);
+            case 2: return dispatch<64, 2>(a, p, stream);
+            case 4: return dispatch<64, 4>(a, p, stream);
+            case 8: return dispatch<64, 8>(a, p, stream);
         }
     }
     return DAP_ERR_UNSUPPORTED;
 }
-
 }  // namespace dap

@@ -12,6 +12,32 @@ namespace dap {
 
 // Tokens per pipeline tile of the split kernel; the split chunk is a multiple of it.
 constexpr int kTileTokens = 32;
+// Balanced schedule: at most this many persistent CTAs (workspace is sized for it), and
+// batches above kMaxBalancedBatch sequences use the per-sequence schedule instead (their
+// units already fill the device, and every persistent CTA scans seq_lens once).
+constexpr int kMaxPersistentCtas = 1024;
+constexpr int kMaxBalancedBatch = 4096;
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace of the balanced schedule: per-CTA partial slots (two each), the first tile and
+// tile count of every unit, and the total tile count.
+struct BalancedLayout {
+    size_t acc, ml, info, total, bytes;
+};
+inline BalancedLayout balanced_layout(int B, int units_per_seq, int heads_per_unit, int D) {
+    BalancedLayout l;
+    const size_t slots = 2 * (size_t)kMaxPersistentCtas * heads_per_unit;
+    l.acc = 0;
+    l.ml = l.acc + align256(slots * D * sizeof(float));
+    l.info = l.ml + align256(slots * 2 * sizeof(float));
+    l.total = l.info + align256((size_t)B * units_per_seq * 2 * sizeof(int));
+    l.bytes = l.total + 256;
+    return l;
+}
+// Query heads and kv heads that one unit of the balanced schedule covers.
+int balanced_heads_per_unit(int D, int G);
+int balanced_kv_heads_per_unit(int D, int G);
 
 // Everything a decode launch needs, already validated.
 struct DecodeArgs {
@@ -27,8 +53,8 @@ struct DecodeArgs {
     int max_kv_len;
     int B, Hq, Hkv, D;
     float scale;
-    int num_splits;              // resolved, >= 1
-    int chunk;                   // tokens per split chunk
+    int num_splits;              // 0 = balanced schedule, else per-sequence splits (>= 1)
+    int chunk;                   // per-sequence: tokens per split chunk
     void *workspace;
     void *out;
     long long o_sb, o_sh;

@@ -46,11 +46,12 @@ extern "C" dap_status decode_attn_paged_noalloc(
                                  num_splits, nullptr, 0, out, out_stride_b, out_stride_h, stream);
     const size_t cap = DAP_NOALLOC_SCRATCH_BYTES;
     int S = num_splits;
-    if (S == 0) {
+    if (S == 0 && dap_workspace_bytes(B, Hq, Hkv, D, 0) > cap) {
+        // the balanced schedule's partials do not fit: plan per-sequence splits that do
         const int sms = dap_device_sm_count();
         if (sms <= 0) return DAP_ERR_CUDA;
         S = dap_plan_splits(sms, B, Hq, Hkv, D, page_size, max_kv_len, 0);
-        while (S > 1 && dap_workspace_bytes(B, Hq, D, S) > cap) --S;
+        while (S > 1 && dap_workspace_bytes(B, Hq, Hkv, D, S) > cap) --S;
     }
     void *scratch = nullptr;
     const dap_status st = scratch_address(&scratch);

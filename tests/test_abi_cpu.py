@@ -64,9 +64,15 @@ def test_plan_splits_properties():
 
 
 def test_workspace_bytes():
-    assert binding.workspace_bytes(16, 32, 128, 1) == 0
-    n = binding.workspace_bytes(16, 32, 128, 8)
+    assert binding.workspace_bytes(16, 32, 8, 128, 1) == 0
+    n = binding.workspace_bytes(16, 32, 8, 128, 8)
     assert n >= 16 * 8 * 32 * (128 + 2) * 4 and n % 256 == 0
+    # balanced schedule: two partial slots per persistent CTA (up to 1024) + unit records
+    bal = binding.workspace_bytes(128, 32, 8, 128, 0)
+    assert bal >= 2 * 1024 * 4 * (128 + 2) * 4 + 128 * 8 * 8
+    assert bal < 8 << 20
+    assert binding.workspace_bytes(5000, 32, 8, 128, 0) == 0      # huge batches run one CTA per unit
+    assert binding.workspace_bytes(16, 32, 8, 128, -1) == 0
 
 
 FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails validation first
@@ -92,7 +98,8 @@ def paged_call(lib, **kw):
     (dict(D=96), 3), (dict(Hq=48, Hkv=3), 3), (dict(Hq=64, Hkv=4), 3),
     (dict(q=ctypes.c_void_p((1 << 20) + 8)), 5), (dict(qsh=130), 5), (dict(osb=4100), 5),
     (dict(k=ctypes.c_void_p((1 << 20) + 4)), 5),
-    (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=16), 4),
+    (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=16), 4), (dict(S=0), 4),
+    (dict(qsh=0), 2), (dict(osb=0), 2),
 ])
 def test_paged_validation(lib, kw, status):
     assert paged_call(lib, **kw) == status

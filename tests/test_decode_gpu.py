@@ -84,7 +84,7 @@ def test_contiguous_matches_oracle_and_paged_bit_for_bit():
     case = inputs.make_paged_case(4, 32, 8, 128, 16, [300, 1, 64, 129], 77).to("cuda")
     k, v = inputs.logical_kv(case, max_len=320)
     ref = oracle.decode_contig(bits(case.q), bits(k), bits(v), case.seq_lens.cpu().numpy(), case.scale)
-    for S in [1, 3]:
+    for S in [0, 1, 3]:
         c = binding.decode_attn_contig(case.q, k, v, case.seq_lens, max_kv_len=case.max_kv_len,
                                        num_splits=S)
         assert_close(c, ref, f"contig S={S}")
@@ -98,7 +98,7 @@ def test_page_permutation_is_bit_identical():
     moved = inputs.PagedCase(case.q, case.k_cache[perm].contiguous(), case.v_cache[perm].contiguous(),
                              inv[case.block_table.long()].to(torch.int32).contiguous(), case.seq_lens,
                              case.page_size, case.scale)
-    for S in [1, 4, 9]:
+    for S in [0, 1, 4, 9]:
         assert torch.equal(gpu_paged(case, S), gpu_paged(moved, S)), f"S={S}"
 
 
@@ -114,6 +114,24 @@ def test_split_count_sweep_stays_within_tolerance():
         assert (o - outs[0]).abs().max().item() < 2e-2
 
 
+def test_balanced_schedule_many_short_and_empty_sequences():
+    # 300 sequences: the persistent CTAs' scan of seq_lens crosses many 32-wide chunks, some
+    # units are empty, many CTAs cover several whole units, and ranges start mid-unit.
+    lens = inputs.uniform_lengths(300, 0, 200, 84)
+    lens[7] = 0
+    lens[299] = 0
+    case = inputs.make_paged_case(300, 8, 2, 64, 16, lens, 84).to("cuda")
+    ref = oracle_paged(case)
+    assert_close(gpu_paged(case, 0), ref, "balanced B=300")
+    assert binding.get_device_errors() == 0
+
+
+def test_balanced_schedule_fewer_tiles_than_ctas():
+    # 3 tiles in all: most persistent CTAs get an empty range
+    case = inputs.make_paged_case(2, 16, 2, 128, 16, [40, 20], 85).to("cuda")
+    assert_close(gpu_paged(case, 0), oracle_paged(case), "tiny balanced")
+
+
 def test_strided_q_and_out_and_garbage_workspace():
     case = inputs.make_paged_case(3, 16, 4, 128, 16, [90, 200, 7], 80).to("cuda")
     ref = oracle_paged(case)
@@ -122,12 +140,12 @@ def test_strided_q_and_out_and_garbage_workspace():
     q = qbig[:, :, 128:256]                      # stride_h = 384
     obig = torch.full((3, 16, 2 * 128), 7.0, dtype=torch.bfloat16, device="cuda")
     out = obig[:, :, :128]
-    S = 4
-    ws = torch.full((binding.workspace_bytes(3, 16, 128, S),), 0xFF, dtype=torch.uint8, device="cuda")
-    binding.decode_attn_paged(q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
-                              max_kv_len=case.max_kv_len, num_splits=S, workspace=ws, out=out)
-    assert_close(out, ref, "strided")
-    assert torch.all(obig[:, :, 128:] == 7.0), "wrote outside the output rows"
+    for S in [0, 4]:
+        ws = torch.full((binding.workspace_bytes(3, 16, 4, 128, S),), 0xFF, dtype=torch.uint8, device="cuda")
+        binding.decode_attn_paged(q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                                  max_kv_len=case.max_kv_len, num_splits=S, workspace=ws, out=out)
+        assert_close(out, ref, f"strided S={S}")
+        assert torch.all(obig[:, :, 128:] == 7.0), "wrote outside the output rows"
 
 
 def test_repeat_runs_are_identical():

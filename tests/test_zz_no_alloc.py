@@ -51,7 +51,7 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point():
 def test_partials_beyond_the_scratch_are_refused():
     case = inputs.make_paged_case(4, 64, 8, 128, 64, [4096] * 4, 9003).to("cuda")
     S = 128
-    assert binding.workspace_bytes(4, 64, 128, S) > binding.NOALLOC_SCRATCH_BYTES
+    assert binding.workspace_bytes(4, 64, 8, 128, S) > binding.NOALLOC_SCRATCH_BYTES
     with pytest.raises(binding.DapError) as e:
         binding.decode_attn_paged_noalloc(case.q, case.k_cache, case.v_cache, case.block_table,
                                           case.seq_lens, max_kv_len=case.max_kv_len, num_splits=S)
