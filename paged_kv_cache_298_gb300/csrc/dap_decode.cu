@@ -39,6 +39,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "dap_device.cuh"
 #include "dap_internal.h"
@@ -87,7 +88,7 @@ struct SplitCfg {
     static constexpr int ABUF_OFF = PBUF_OFF + PBUF_BYTES;
     static constexpr int ABUF_BYTES = NWC * G * 4;
     static constexpr int MRG_OFF = ABUF_OFF + ABUF_BYTES;   // per-warp (acc, m, l) for merging
-    static constexpr int MRG_BYTES = NWC * G * (D + 2) * 4;
+    static constexpr int MRG_BYTES = NWC * G * (D / 2 + 2) * 4;  // merged in two halves of D
     static constexpr int HDR_OFF = MRG_OFF + MRG_BYTES;     // per-stage tile header
     static constexpr int HDR_INTS = 8;
     static constexpr int MISC_OFF = HDR_OFF + NS * HDR_INTS * 4;  // tiles, abort, issued
@@ -273,48 +274,56 @@ struct Consumer {
     }
 
     // End of a unit segment: merge the WPH warps of each kv head through `mrg` and hand each
-    // merged (acc, m, l) pair of elements to `emit(hl, g, d, a0, a1, M, l)`.  All NWC
+    // merged (acc, m, l) pair of elements to `emit(hl, g, d, a0, a1, M, l)`.  The merge runs
+    // over the two halves of D in turn so that the merge area stays small.  All NWC
     // consumer warps must call this together; `sync()` is their barrier and returns false
-    // when it gave up (then nothing is emitted and finish returns false).
+    // when it gave up (then finish returns false).
     template <class Sync, class Emit>
     __device__ __forceinline__ bool finish(float *mrg, Sync sync, Emit emit) {
-        constexpr int G = C::G, D = C::D, NWC = C::NWC;
+        constexpr int G = C::G, D = C::D, NWC = C::NWC, DH = D / 2;
 #pragma unroll
         for (int m = C::LPR; m < 32; m <<= 1) l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, m);
-        float *macc = mrg;                  // [NWC][G][D]
-        float *mml = mrg + NWC * G * D;     // [NWC][G][2]
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int j = 0; j < C::DPV / 2; ++j)
-                *reinterpret_cast<float2 *>(macc + (warp * G + g) * D + lane * C::DPV + 2 * j) = acc[g][j];
+        float *macc = mrg;                  // [NWC][G][D/2]
+        float *mml = mrg + NWC * G * DH;    // [NWC][G][2]
         if (rgrp == 0) {
             mml[(warp * G + hsel) * 2 + 0] = m_run;
             mml[(warp * G + hsel) * 2 + 1] = l_run;
         }
-        if (!sync()) return false;
         const int tid = warp * 32 + lane;
-        for (int e = tid * 2; e < C::HG * G * D; e += NWC * 32 * 2) {
-            const int hl = e / (G * D);
-            const int g = (e / D) % G;
-            const int d = e % D;
-            float M = -INFINITY;
+        const int dl = lane * C::DPV;       // first dim this lane accumulates
 #pragma unroll
-            for (int w = 0; w < C::WPH; ++w) M = fmaxf(M, mml[((w * C::HG + hl) * G + g) * 2]);
-            const float Mu = (M == -INFINITY) ? 0.f : M;
-            float a0 = 0.f, a1 = 0.f, lv = 0.f;
+        for (int half = 0; half < 2; ++half) {
+            if (dl / DH == half) {
 #pragma unroll
-            for (int w = 0; w < C::WPH; ++w) {
-                const int ww = w * C::HG + hl;
-                const float f = ex2(mml[(ww * G + g) * 2] - Mu);
-                lv = fmaf(f, mml[(ww * G + g) * 2 + 1], lv);
-                const float2 x = *reinterpret_cast<const float2 *>(macc + (ww * G + g) * D + d);
-                a0 = fmaf(f, x.x, a0);
-                a1 = fmaf(f, x.y, a1);
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int j = 0; j < C::DPV / 2; ++j)
+                        *reinterpret_cast<float2 *>(macc + (warp * G + g) * DH + dl - half * DH + 2 * j) = acc[g][j];
             }
-            emit(hl, g, d, a0, a1, M, lv);
+            if (!sync()) return false;
+            for (int e = tid * 2; e < C::HG * G * DH; e += NWC * 32 * 2) {
+                const int hl = e / (G * DH);
+                const int g = (e / DH) % G;
+                const int dd = e % DH;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < C::WPH; ++w) M = fmaxf(M, mml[((w * C::HG + hl) * G + g) * 2]);
+                const float Mu = (M == -INFINITY) ? 0.f : M;
+                float a0 = 0.f, a1 = 0.f, lv = 0.f;
+#pragma unroll
+                for (int w = 0; w < C::WPH; ++w) {
+                    const int ww = w * C::HG + hl;
+                    const float f = ex2(mml[(ww * G + g) * 2] - Mu);
+                    lv = fmaf(f, mml[(ww * G + g) * 2 + 1], lv);
+                    const float2 x = *reinterpret_cast<const float2 *>(macc + (ww * G + g) * DH + dd);
+                    a0 = fmaf(f, x.x, a0);
+                    a1 = fmaf(f, x.y, a1);
+                }
+                emit(hl, g, half * DH + dd, a0, a1, M, lv);
+            }
+            if (!sync()) return false;  // the merge area is free again
         }
-        return sync();  // the merge area is free again
+        return true;
     }
 };
 
@@ -724,29 +733,34 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
 template <int D>
 struct RowMerge {
     static constexpr int DPV = D / 32;
+    using Vec = typename std::conditional<DPV == 4, float4, float2>::type;
     float acc[DPV];
-    float lsum, M, Mu;
+    float lsum, Mu;
     __device__ __forceinline__ void begin(float m_max) {
-        M = m_max;
-        Mu = (M == -INFINITY) ? 0.f : M;
+        Mu = (m_max == -INFINITY) ? 0.f : m_max;
         lsum = 0.f;
 #pragma unroll
         for (int j = 0; j < DPV; ++j) acc[j] = 0.f;
     }
-    __device__ __forceinline__ void add(const float *o, float2 ml, int lane) {
-        const float f = ex2(ml.x - Mu);
-        lsum = fmaf(f, ml.y, lsum);
-        o += lane * DPV;
-        if constexpr (DPV == 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(o);
-            acc[0] = fmaf(f, x.x, acc[0]);
-            acc[1] = fmaf(f, x.y, acc[1]);
-            acc[2] = fmaf(f, x.z, acc[2]);
-            acc[3] = fmaf(f, x.w, acc[3]);
-        } else {
-            const float2 x = *reinterpret_cast<const float2 *>(o);
-            acc[0] = fmaf(f, x.x, acc[0]);
-            acc[1] = fmaf(f, x.y, acc[1]);
+    // add the partial rows o[0..n) (n <= 8), whose loads are all issued before any use
+    __device__ __forceinline__ void add_batch(const float *const *o, const float2 *ml, int n, int lane) {
+        Vec x[8];
+        float f[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (k < n) {
+                x[k] = *reinterpret_cast<const Vec *>(o[k] + lane * DPV);
+                f[k] = ex2(ml[k].x - Mu);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (k < n) {
+                lsum = fmaf(f[k], ml[k].y, lsum);
+                const float *xv = reinterpret_cast<const float *>(&x[k]);
+#pragma unroll
+                for (int j = 0; j < DPV; ++j) acc[j] = fmaf(f[k], xv[j], acc[j]);
+            }
         }
     }
     __device__ __forceinline__ void store(__nv_bfloat16 *o, int lane) {
@@ -772,10 +786,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
     RowMerge<D> r;
     r.begin(M);
-#pragma unroll 4
-    for (int s = 0; s < nsplit; ++s) {
-        const long long row = row0 + (long long)s * p.Hq;
-        r.add(p.o_part + row * D, *reinterpret_cast<const float2 *>(p.ml_part + row * 2), lane);
+    for (int s0 = 0; s0 < nsplit; s0 += 8) {
+        const float *o[8];
+        float2 ml[8];
+        const int n = min(8, nsplit - s0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const long long row = row0 + (long long)min(s0 + k, nsplit - 1) * p.Hq;
+            o[k] = p.o_part + row * D;
+            ml[k] = *reinterpret_cast<const float2 *>(p.ml_part + row * 2);
+        }
+        r.add_batch(o, ml, n, lane);
     }
     r.store(p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh, lane);
 }
@@ -793,22 +814,34 @@ __global__ void __launch_bounds__(256) combine_balanced_kernel(const SplitParams
     const int c_first = (int)(((start + 1) * P - 1) / T);
     const int c_last = (int)(((start + tb) * P - 1) / T);
     if (c_first == c_last) return;  // finished in place by one CTA
+    // partial slot of CTA c for this unit, or -1 when c's range is empty (only when T < P)
     auto slot_of = [&](int c) -> int {
-        const long long s_c = (long long)c * T / P;
+        const long long s_c = (long long)c * T / P, e_c = (long long)(c + 1) * T / P;
+        if (s_c == e_c) return -1;
         return 2 * c + ((c == c_first && s_c < start) ? 1 : 0);
     };
-    auto nonempty = [&](int c) { return (long long)c * T / P < (long long)(c + 1) * T / P; };
     float M = -INFINITY;
-    for (int c = c_first + lane; c <= c_last; c += 32)
-        if (nonempty(c)) M = fmaxf(M, p.ml_part[((long long)slot_of(c) * hpu + hl2) * 2]);
+    for (int c = c_first + lane; c <= c_last; c += 32) {
+        const int sl = slot_of(c);
+        if (sl >= 0) M = fmaxf(M, p.ml_part[((long long)sl * hpu + hl2) * 2]);
+    }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
     RowMerge<D> r;
     r.begin(M);
-    for (int c = c_first; c <= c_last; ++c) {
-        if (!nonempty(c)) continue;
-        const long long row = (long long)slot_of(c) * hpu + hl2;
-        r.add(p.o_part + row * D, *reinterpret_cast<const float2 *>(p.ml_part + row * 2), lane);
+    for (int c0 = c_first; c0 <= c_last;) {
+        const float *o[8];
+        float2 ml[8];
+        int n = 0;
+        for (; c0 <= c_last && n < 8; ++c0) {
+            const int sl = slot_of(c0);
+            if (sl < 0) continue;
+            const long long row = (long long)sl * hpu + hl2;
+            o[n] = p.o_part + row * D;
+            ml[n] = *reinterpret_cast<const float2 *>(p.ml_part + row * 2);
+            ++n;
+        }
+        r.add_batch(o, ml, n, lane);
     }
     const int b = u / nkvg, kvg = u - b * nkvg;
     const int hq = kvg * hpu + hl2;
