@@ -84,8 +84,8 @@ int dap_device_sm_count(void);
 int dap_plan_splits(int sm_count, int B, int Hq, int Hkv, int D, int page_size,
                     int max_kv_len, long long total_kv);
 
-/* Tokens per split chunk for a plan: ceil(max_kv_len / num_splits) rounded up to the
- * kernel's tile of 32 tokens (at least 32).  Pure host function. */
+/* Tokens per split chunk for a plan: ceil(max_kv_len / num_splits) rounded up to a
+ * multiple of 64 tokens (at least 64).  Pure host function. */
 int dap_chunk_tokens(int max_kv_len, int num_splits);
 
 /* Workspace bytes decode_attn_paged / decode_attn_contig need for `num_splits`:

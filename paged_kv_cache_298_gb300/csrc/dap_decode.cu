@@ -95,6 +95,8 @@ struct SplitCfg {
     static constexpr int BAR_OFF = (MISC_OFF + 16 + 7) & ~7;        // full[NS], empty[NS], consumer
     static constexpr int SMEM = BAR_OFF + (2 * NS + 1) * 8;
     static constexpr int THREADS = (NWC + 1) * 32;
+    static constexpr bool MMA = false;  // CUDA-core consumer
+    static constexpr bool SWZ = false;  // unswizzled [rows][HG][D] tiles, one box per K/V
     static_assert(NWC % HG == 0, "warps must split evenly over the kv heads of a CTA");
     static_assert(BT % WPH == 0 && RW % RPP == 0 && PASSES >= 1, "tile rows per warp");
     static_assert(G <= LPR, "one (row, head) score per lane after the reduction");
@@ -150,10 +152,13 @@ struct Consumer {
     float2 acc[C::G][C::DPV / 2];
     float m_run, l_run;
     int hh, row0, qlane, rgrp, hsel, warp, lane;
+    float *pbuf, *abuf;  // this warp's probabilities and rescale factors
 
-    __device__ __forceinline__ void init(int w, int l) {
+    __device__ __forceinline__ void init(int w, int l, uint8_t *smem) {
         warp = w;
         lane = l;
+        pbuf = reinterpret_cast<float *>(smem + C::PBUF_OFF) + w * C::RW * C::G;
+        abuf = reinterpret_cast<float *>(smem + C::ABUF_OFF) + w * C::G;
         hh = w % C::HG;
         row0 = (w / C::HG) * C::RW;
         qlane = l % C::LPR;
@@ -170,14 +175,14 @@ struct Consumer {
             for (int j = 0; j < C::DPV / 2; ++j) acc[g][j] = make_float2(0.f, 0.f);
     }
 
-    // q rows of this warp's kv head: `qrow(g)` points at the D bf16 values of head g.
-    template <class QRow>
-    __device__ __forceinline__ void load_q(QRow qrow, float qscale) {
+    // q of this warp's G heads: head g's D values start at base + g * hstride (global or
+    // shared memory).  Kept in fp32, pre-multiplied by scale * log2(e).
+    __device__ __forceinline__ void load_q(const __nv_bfloat16 *base, long long hstride, float qscale) {
 #pragma unroll
         for (int g = 0; g < C::G; ++g) {
 #pragma unroll
             for (int i = 0; i < C::CPL; ++i) {
-                const uint4 w = qrow(g, qlane + i * C::LPR);
+                const uint4 w = *reinterpret_cast<const uint4 *>(base + g * hstride + 8 * (qlane + i * C::LPR));
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -189,9 +194,9 @@ struct Consumer {
     }
 
     // One staged tile: rows [row0, row0 + RW) of the tile, nvalid rows valid in the tile.
-    __device__ __forceinline__ void tile(const uint8_t *sK, const uint8_t *sV, int nvalid, float *pbuf,
-                                         float *abuf) {
+    __device__ __forceinline__ void tile(uint8_t *stage, int nvalid) {
         constexpr int G = C::G, HG = C::HG;
+        const uint8_t *sK = stage, *sV = stage + C::TILE_BYTES;
         const int nv_w = min(max(nvalid - row0, 0), C::RW);
         float sc[C::PASSES];
 #pragma unroll
@@ -333,6 +338,236 @@ __device__ __forceinline__ void store_out_pair(__nv_bfloat16 *o, float a0, float
 }
 
 
+// ---- tensor-core consumer ---------------------------------------------------------------
+// For each 16-key slice a warp computes S^T = K . Q^T with mma.m16n8k16 (M = 16 keys,
+// N = 8 query heads of the kv head, padded with zero rows of q when G < 8, K = 16 dims per
+// step), runs the base-2 online softmax on the fragments (lane g/t holds keys g, g+8 for
+// heads 2t, 2t+1), transposes the bf16 probabilities into the B operand with movmatrix,
+// and accumulates O^T = V^T . P^T (M = 16 dims per step, N = 8 heads, K = 16 keys) in
+// registers.  Tiles are TMA-loaded with the 128-byte swizzle as [D/64][BT][128 B] so that
+// ldmatrix reads are conflict-free.  The scale multiplies S in fp32 (the bf16 q is never
+// rescaled: AstrAI csrc log, "apply scale in float32 after Q@K^T").
+
+template <int D_, int G_, int NWC_, int BT_, int NS_, int MINB_>
+struct MmaCfg {
+    static constexpr int D = D_, G = G_, HG = 1, NWC = NWC_, BT = BT_, NS = NS_, MINB = MINB_;
+    static constexpr bool MMA = true;
+    static constexpr bool SWZ = true;              // swizzled column blocks, one box each
+    static constexpr int WPH = NWC;                // every consumer warp serves the one kv head
+    static constexpr int KPW = BT / NWC;           // keys per warp per tile
+    static constexpr int ROWB = D * 2;
+    static constexpr int HPU = G;
+    static constexpr int NHALF = D / 64;           // 128-byte column blocks per row
+    static constexpr int TILE_BYTES = BT * ROWB;
+    static constexpr int QBYTES = G * ROWB;
+    static constexpr int STAGE_BYTES = (2 * TILE_BYTES + QBYTES + 1023) & ~1023;
+    static constexpr int MRG_OFF = NS * STAGE_BYTES;
+    static constexpr int MRG_BYTES = NWC * G * (D / 2 + 2) * 4;
+    static constexpr int HDR_OFF = MRG_OFF + MRG_BYTES;
+    static constexpr int HDR_INTS = 8;
+    static constexpr int MISC_OFF = HDR_OFF + NS * HDR_INTS * 4;
+    static constexpr int BAR_OFF = (MISC_OFF + 16 + 7) & ~7;
+    static constexpr int SMEM = BAR_OFF + (2 * NS + 1) * 8 + 1024;  // + slack to align the base
+    static constexpr int THREADS = (NWC + 1) * 32;
+    static_assert(KPW == 16, "one m16 key slice per warp per tile");
+    static_assert(G <= 8, "the query heads of a kv head fill at most N = 8");
+    static_assert(D % 64 == 0, "whole 128-byte column blocks");
+};
+
+template <class C>
+struct MmaConsumer {
+    static constexpr int D = C::D, G = C::G, KS = D / 16;
+    uint32_t qb[KS][2];  // Q^T B fragments: head g, dims 16k+2t.. and 16k+2t+8..
+    float acc[KS][4];    // O^T fragments: dims 16m+g, 16m+g+8 x heads 2t, 2t+1
+    float m_run[2], l_run[2];
+    float qscale;
+    int warp, lane, g, t, key0;
+    static constexpr int hh = 0;
+
+    __device__ __forceinline__ void init(int w, int l, uint8_t *) {
+        warp = w;
+        lane = l;
+        g = l >> 2;
+        t = l & 3;
+        key0 = w * C::KPW;
+    }
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            m_run[j] = -INFINITY;
+            l_run[j] = 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < KS; ++m)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[m][j] = 0.f;
+    }
+
+    __device__ __forceinline__ void load_q(const __nv_bfloat16 *base, long long hstride, float qs) {
+        qscale = qs;
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+            if (g < G) {
+                const __nv_bfloat16 *r = base + g * hstride + 16 * k + 2 * t;
+                qb[k][0] = *reinterpret_cast<const uint32_t *>(r);
+                qb[k][1] = *reinterpret_cast<const uint32_t *>(r + 8);
+            } else {
+                qb[k][0] = qb[k][1] = 0u;
+            }
+        }
+    }
+
+    // byte offset of (key, dim) in a swizzled [D/64][BT][128 B] tile
+    static __device__ __forceinline__ uint32_t off(int key, int dim) {
+        const int chunk = (dim & 63) >> 3;
+        return (uint32_t)((dim >> 6) * (C::BT * 128) + key * 128 + ((chunk ^ (key & 7)) << 4));
+    }
+
+    __device__ __forceinline__ void tile(uint8_t *stage, int nvalid) {
+        const int nv = nvalid - key0;
+        if (nv <= 0) return;  // no key of this slice is valid
+        uint8_t *sV = stage + C::TILE_BYTES;
+        if (nv < 16) {  // rows past the end may hold anything: zero their V so 0 * V stays 0
+            for (int i = lane; i < (16 - nv) * C::NHALF * 8; i += 32) {
+                const int row = key0 + nv + i / (C::NHALF * 8);
+                const int rest = i % (C::NHALF * 8);
+                *reinterpret_cast<uint4 *>(sV + (rest >> 3) * (C::BT * 128) + row * 128 + (rest & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+        const uint32_t kbase = smem_addr(stage), vbase = smem_addr(sV);
+        // S^T = K . Q^T
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int key = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int dcol = ((lane >> 4) & 1) * 8;
+#pragma unroll
+            for (int k = 0; k < KS; ++k) {
+                uint32_t a[4];
+                ldmatrix_x4(a, kbase + off(key, 16 * k + dcol));
+                mma_bf16_16816(c, a, qb[k][0], qb[k][1]);
+            }
+        }
+        // online softmax, base 2; keys g (c0, c1) and g + 8 (c2, c3)
+        const bool v0 = g < nv, v1 = g + 8 < nv;
+        float s[4];
+        s[0] = v0 ? c[0] * qscale : -INFINITY;
+        s[1] = v0 ? c[1] * qscale : -INFINITY;
+        s[2] = v1 ? c[2] * qscale : -INFINITY;
+        s[3] = v1 ? c[3] * qscale : -INFINITY;
+        float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xFFFFFFFFu, mx[0], o));
+            mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xFFFFFFFFu, mx[1], o));
+        }
+        float alpha[2], mu[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float m_new = fmaxf(m_run[j], mx[j]);
+            mu[j] = (m_new == -INFINITY) ? 0.f : m_new;
+            alpha[j] = ex2(m_run[j] - mu[j]);
+            m_run[j] = m_new;
+        }
+        const uint32_t w0 = pack_bf16x2(ex2(s[0] - mu[0]), ex2(s[1] - mu[1]));
+        const uint32_t w1 = pack_bf16x2(ex2(s[2] - mu[0]), ex2(s[3] - mu[1]));
+        {   // l sums the rounded probabilities PV actually uses
+            const float2 p0 = bf16x2_to_float2(w0), p1 = bf16x2_to_float2(w1);
+            l_run[0] = l_run[0] * alpha[0] + (p0.x + p1.x);
+            l_run[1] = l_run[1] * alpha[1] + (p0.y + p1.y);
+        }
+#pragma unroll
+        for (int m = 0; m < KS; ++m) {
+            acc[m][0] *= alpha[0];
+            acc[m][1] *= alpha[1];
+            acc[m][2] *= alpha[0];
+            acc[m][3] *= alpha[1];
+        }
+        const uint32_t b0 = movmatrix_trans(w0), b1 = movmatrix_trans(w1);
+        // O^T += V^T . P^T
+        {
+            const int key = key0 + (lane & 7) + ((lane >> 4) & 1) * 8;
+            const int dcol = ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int m = 0; m < KS; ++m) {
+                uint32_t a[4];
+                ldmatrix_x4_trans(a, vbase + off(key, 16 * m + dcol));
+                mma_bf16_16816(acc[m], a, b0, b1);
+            }
+        }
+    }
+
+    template <class Sync, class Emit>
+    __device__ __forceinline__ bool finish(float *mrg, Sync sync, Emit emit) {
+        constexpr int NWC = C::NWC, DH = D / 2;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l_run[0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[0], o);
+            l_run[1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[1], o);
+        }
+        float *macc = mrg;                 // [NWC][G][D/2]
+        float *mml = mrg + NWC * G * DH;   // [NWC][G][2]
+        if (g == 0) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                if (2 * t + j < G) {
+                    mml[(warp * G + 2 * t + j) * 2 + 0] = m_run[j];
+                    mml[(warp * G + 2 * t + j) * 2 + 1] = l_run[j];
+                }
+        }
+        const int tid = warp * 32 + lane;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int m = half * KS / 2; m < (half + 1) * KS / 2; ++m) {
+                const int d = 16 * m + g - half * DH;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (2 * t + j < G) {
+                        float *row = macc + (warp * G + 2 * t + j) * DH;
+                        row[d] = acc[m][j];
+                        row[d + 8] = acc[m][j + 2];
+                    }
+                }
+            }
+            if (!sync()) return false;
+            for (int e = tid * 2; e < G * DH; e += NWC * 32 * 2) {
+                const int hh2 = e / DH, dd = e % DH;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < NWC; ++w) M = fmaxf(M, mml[(w * G + hh2) * 2]);
+                const float Mu = (M == -INFINITY) ? 0.f : M;
+                float a0 = 0.f, a1 = 0.f, lv = 0.f;
+#pragma unroll
+                for (int w = 0; w < NWC; ++w) {
+                    const float f = ex2(mml[(w * G + hh2) * 2] - Mu);
+                    lv = fmaf(f, mml[(w * G + hh2) * 2 + 1], lv);
+                    const float2 x = *reinterpret_cast<const float2 *>(macc + (w * G + hh2) * DH + dd);
+                    a0 = fmaf(f, x.x, a0);
+                    a1 = fmaf(f, x.y, a1);
+                }
+                emit(0, hh2, half * DH + dd, a0, a1, M, lv);
+            }
+            if (!sync()) return false;
+        }
+        return true;
+    }
+};
+
+template <class C>
+using ConsumerOf = typename std::conditional<C::MMA, MmaConsumer<C>, Consumer<C>>::type;
+
+// 1024-byte aligned view of the dynamic shared memory (the 128-byte swizzle is a function
+// of address bits 4..9, so swizzled tiles must start on 1024-byte boundaries).
+template <class C>
+__device__ __forceinline__ uint8_t *aligned_smem(uint8_t *raw) {
+    if constexpr (C::SWZ) return raw + ((1024u - (smem_addr(raw) & 1023u)) & 1023u);
+    return raw;
+}
+
 // Barrier among the NWC consumer warps on an mbarrier (count NWC, one arrival per warp),
 // so that a wait is bounded like every other wait in the pipeline.
 struct ConsumerBarrier {
@@ -347,13 +582,33 @@ struct ConsumerBarrier {
     }
 };
 
+// The K and V boxes of one producer lane: box j of the stage covers tile rows
+// [j*R, (j+1)*R).  Swizzled configurations split every row into 128-byte column blocks.
+template <class C>
+__device__ __forceinline__ void issue_kv_box(uint8_t *stage, int j, int R, const CUtensorMap *mk,
+                                             const CUtensorMap *mv, int kvh0, int row, int page, uint64_t *bar) {
+    if constexpr (C::SWZ) {
+#pragma unroll
+        for (int h = 0; h < C::NHALF; ++h) {
+            uint8_t *dst = stage + h * (C::BT * 128) + j * R * 128;
+            tma_load_4d(dst, mk, 64 * h, kvh0, row, page, bar);
+            tma_load_4d(dst + C::TILE_BYTES, mv, 64 * h, kvh0, row, page, bar);
+        }
+    } else {
+        uint8_t *dst = stage + j * R * C::HG * C::ROWB;
+        tma_load_4d(dst, mk, 0, kvh0, row, page, bar);
+        tma_load_4d(dst + C::TILE_BYTES, mv, 0, kvh0, row, page, bar);
+    }
+}
+
 // ---- per-sequence schedule: one CTA per (unit, split) ------------------------------------
 
 template <class C, bool PAGED>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
     split_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                  const SplitParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = aligned_smem<C>(smem_raw);
     constexpr int G = C::G, HG = C::HG, NWC = C::NWC, BT = C::BT, NS = C::NS, D = C::D;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -423,11 +678,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
             if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
             __syncwarp();
             if (lane < nbox) {
-                uint8_t *sK = smem + st * C::STAGE_BYTES + lane * R * HG * C::ROWB;
                 const int tt = t + lane * R;
-                const int slot = PAGED ? tt % p.page_size : tt;
-                tma_load_4d(sK, &mapK, 0, kvg * HG, slot, pg, &full[st]);
-                tma_load_4d(sK + C::TILE_BYTES, &mapV, 0, kvg * HG, slot, pg, &full[st]);
+                issue_kv_box<C>(smem + st * C::STAGE_BYTES, lane, R, &mapK, &mapV, kvg * HG,
+                                PAGED ? tt % p.page_size : tt, pg, &full[st]);
             }
             issued = i + 1;
         }
@@ -437,16 +690,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     }
 
     // ---- consumer warps
-    Consumer<C> cs;
-    cs.init(warp, lane);
+    ConsumerOf<C> cs;
+    cs.init(warp, lane, smem);
     cs.reset();
     const int kvh = kvg * HG + cs.hh;
-    const __nv_bfloat16 *qb = p.q + (long long)b * p.q_sb;
-    cs.load_q([&](int g, int chunk) {
-        return __ldg(reinterpret_cast<const uint4 *>(qb + (long long)(kvh * G + g) * p.q_sh + 8 * chunk));
-    }, p.qscale);
-    float *pbuf = reinterpret_cast<float *>(smem + C::PBUF_OFF) + warp * C::RW * G;
-    float *abuf = reinterpret_cast<float *>(smem + C::ABUF_OFF) + warp * G;
+    cs.load_q(p.q + (long long)b * p.q_sb + (long long)kvh * G * p.q_sh, p.q_sh, p.qscale);
     int consumed = 0;
     for (int i = 0; i < ntiles; ++i) {
         const int st = i % NS;
@@ -454,8 +702,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
             misc[1] = 1;
             break;
         }
-        const uint8_t *sK = smem + st * C::STAGE_BYTES;
-        cs.tile(sK, sK + C::TILE_BYTES, min(BT, tok1 - (tok0 + i * BT)), pbuf, abuf);
+        cs.tile(smem + st * C::STAGE_BYTES, min(BT, tok1 - (tok0 + i * BT)));
         if (lane == 0) mbar_arrive(&empty[st]);
         consumed = i + 1;
     }
@@ -495,7 +742,8 @@ template <class C, bool PAGED>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
     balanced_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                     const __grid_constant__ CUtensorMap mapQ, const SplitParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = aligned_smem<C>(smem_raw);
     constexpr int G = C::G, HG = C::HG, NWC = C::NWC, BT = C::BT, NS = C::NS, D = C::D, HPU = C::HPU;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;
@@ -587,16 +835,19 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
             int seg_j0 = j;
             const int R = PAGED ? p.box_rows : BT;
 
-            auto lookup = [&](int bb, int jj, int LL) -> int {  // page of this lane's box
+            auto lookup_box = [&](int bb, int tt, int LL) -> int {  // page of the box at token tt
                 if (!PAGED) return bb;
-                const int t = jj * BT + lane * R;
-                if (lane * R >= BT || t >= LL) return 0;
-                int pg = __ldg(p.block_table + (long long)bb * p.max_pages + t / p.page_size);
+                if (tt >= LL) return 0;
+                int pg = __ldg(p.block_table + (long long)bb * p.max_pages + tt / p.page_size);
                 if (pg < 0 || pg >= p.num_pages) {
                     flag_error(DAP_DEVERR_PAGE);
                     pg = 0;
                 }
                 return pg;
+            };
+            auto lookup = [&](int bb, int jj, int LL) -> int {  // page of this lane's box
+                if (lane * R >= BT) return 0;
+                return lookup_box(bb, jj * BT + lane * R, LL);
             };
             int pg_next = lookup(b, j, L);
             for (int i = 0; i < ntiles; ++i) {
@@ -644,12 +895,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
                     mbar_arrive_expect_tx(&full[st], bytes);
                 }
                 __syncwarp();
-                if (lane < nbox) {
-                    const int tt = j * BT + lane * R;
-                    const int slot_row = PAGED ? tt % p.page_size : tt;
-                    uint8_t *sK = stage + lane * R * HG * C::ROWB;
-                    tma_load_4d(sK, &mapK, 0, kvg * HG, slot_row, pg, &full[st]);
-                    tma_load_4d(sK + C::TILE_BYTES, &mapV, 0, kvg * HG, slot_row, pg, &full[st]);
+                for (int jb = lane; jb < nbox; jb += 32) {
+                    const int tt = j * BT + jb * R;
+                    const int pgb = jb == lane ? pg : lookup_box(b, tt, L);
+                    issue_kv_box<C>(stage, jb, R, &mapK, &mapV, kvg * HG, PAGED ? tt % p.page_size : tt, pgb,
+                                    &full[st]);
                 }
                 if (need_q && lane == 0)
                     tma_load_3d(stage + 2 * C::TILE_BYTES, &mapQ, 0, kvg * HPU, b, &full[st]);
@@ -668,11 +918,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     }
 
     // ---- consumer warps
-    Consumer<C> cs;
-    cs.init(warp, lane);
+    ConsumerOf<C> cs;
+    cs.init(warp, lane, smem);
     cs.reset();
-    float *pbuf = reinterpret_cast<float *>(smem + C::PBUF_OFF) + warp * C::RW * G;
-    float *abuf = reinterpret_cast<float *>(smem + C::ABUF_OFF) + warp * G;
     float *mrg = reinterpret_cast<float *>(smem + C::MRG_OFF);
     ConsumerBarrier cb{cbar, 0u};
     int consumed = 0;
@@ -688,12 +936,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
         const int b = h[H_B], kvg = h[H_KVG], nvalid = h[H_NVALID], flags = h[H_FLAGS], slot = h[H_SLOT];
         if (flags & F_FIRST) {
             cs.reset();
-            if (nvalid > 0) {
-                const uint8_t *sq = stage + 2 * C::TILE_BYTES + cs.hh * G * C::ROWB;
-                cs.load_q([&](int g, int chunk) { return lds128(sq + g * C::ROWB + chunk * 16); }, p.qscale);
-            }
+            if (nvalid > 0)
+                cs.load_q(reinterpret_cast<const __nv_bfloat16 *>(stage + 2 * C::TILE_BYTES) + cs.hh * G * D, D,
+                          p.qscale);
         }
-        cs.tile(stage, stage + C::TILE_BYTES, nvalid, pbuf, abuf);
+        cs.tile(const_cast<uint8_t *>(stage), nvalid);
         if (lane == 0) mbar_arrive(&empty[st]);
         consumed = i + 1;
         if (flags & F_LAST) {
@@ -858,21 +1105,28 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapFloatOOBfill);
 
 bool encode_bf16(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
-                 const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+                 const cuuint64_t *strides_bytes, const cuuint32_t *box,
+                 CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
     EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
     if (!enc) return false;
     const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
-               strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [D, Hkv, rows, outer] view of a cache, box [D, HG, box_rows, 1].
+// [D, Hkv, rows, outer] view of a cache.  Box [D, HG, box_rows, 1] unswizzled, or, for the
+// swizzled layout, [64, 1, box_rows, 1] with the 128-byte swizzle (one column block).
+template <class C>
 bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv, long long rows, long long outer,
-                      int HG, int box_rows) {
+                      int box_rows) {
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows, (cuuint64_t)outer};
     const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)rows * Hkv * D * 2};
-    const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)HG, (cuuint32_t)box_rows, 1u};
+    if (C::SWZ) {
+        const cuuint32_t box[4] = {64u, 1u, (cuuint32_t)box_rows, 1u};
+        return encode_bf16(map, base, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)C::HG, (cuuint32_t)box_rows, 1u};
     return encode_bf16(map, base, 4, dims, strides, box);
 }
 
@@ -932,8 +1186,8 @@ dap_status launch_per_sequence(const DecodeArgs &a, SplitParams &p, cudaStream_t
     CUtensorMap mk, mv;
     const long long rows = PAGED ? a.page_size : a.max_len;
     const long long outer = PAGED ? a.num_pages : a.B;
-    if (!encode_cache_map(&mk, a.k, a.D, a.Hkv, rows, outer, C::HG, R) ||
-        !encode_cache_map(&mv, a.v, a.D, a.Hkv, rows, outer, C::HG, R))
+    if (!encode_cache_map<C>(&mk, a.k, a.D, a.Hkv, rows, outer, R) ||
+        !encode_cache_map<C>(&mv, a.v, a.D, a.Hkv, rows, outer, R))
         return DAP_ERR_CUDA;
     auto kern = split_kernel<C, PAGED>;
     static int occ = 0;
@@ -965,8 +1219,8 @@ dap_status launch_balanced(const DecodeArgs &a, SplitParams &p, cudaStream_t str
     CUtensorMap mk, mv, mq;
     const long long rows = PAGED ? a.page_size : a.max_len;
     const long long outer = PAGED ? a.num_pages : a.B;
-    if (!encode_cache_map(&mk, a.k, a.D, a.Hkv, rows, outer, C::HG, R) ||
-        !encode_cache_map(&mv, a.v, a.D, a.Hkv, rows, outer, C::HG, R) || !encode_q_map(&mq, a, C::HPU))
+    if (!encode_cache_map<C>(&mk, a.k, a.D, a.Hkv, rows, outer, R) ||
+        !encode_cache_map<C>(&mv, a.v, a.D, a.Hkv, rows, outer, R) || !encode_q_map(&mq, a, C::HPU))
         return DAP_ERR_CUDA;
     auto kern = balanced_kernel<C, PAGED>;
     static int occ = 0;
@@ -995,18 +1249,28 @@ dap_status launch_balanced(const DecodeArgs &a, SplitParams &p, cudaStream_t str
     return DAP_OK;
 }
 
-// The tuned configuration of each (D, G): one kv head per CTA, four consumer warps,
-// 32-token tiles, four stages; three CTAs per SM (two for G = 8, whose q and accumulators
-// take more registers).
+// Configurations.  Tensor-core consumer (page sizes that are multiples of 8, and the
+// contiguous cache): one kv head per CTA, four consumer warps of 16 keys each, 64-token
+// tiles in 128-byte-swizzled column blocks, three stages, two CTAs per SM.  CUDA-core
+// consumer (any other page size: boxes of fewer than 8 rows cannot start on the
+// 1024-byte boundaries the swizzle needs): 32-token tiles, four stages, three CTAs per SM
+// (two for G = 8).
 template <int D, int G>
-using CfgFor = SplitCfg<D, G, 1, 4, 32, 4, (G <= 4 ? 3 : 2)>;
+using MmaCfgFor = MmaCfg<D, G, 4, 64, 3, 2>;
+template <int D, int G>
+using CoreCfgFor = SplitCfg<D, G, 1, 4, 32, 4, (G <= 4 ? 3 : 2)>;
 
-template <int D, int G>
-dap_status dispatch(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
-    using C = CfgFor<D, G>;
+template <class C>
+dap_status run(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
     if (a.num_splits == 0)
         return a.paged ? launch_balanced<C, true>(a, p, stream) : launch_balanced<C, false>(a, p, stream);
     return a.paged ? launch_per_sequence<C, true>(a, p, stream) : launch_per_sequence<C, false>(a, p, stream);
+}
+
+template <int D, int G>
+dap_status dispatch(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
+    if (a.paged && a.page_size % 8 != 0) return run<CoreCfgFor<D, G>>(a, p, stream);
+    return run<MmaCfgFor<D, G>>(a, p, stream);
 }
 
 }  // namespace

@@ -10,8 +10,9 @@
 
 namespace dap {
 
-// Tokens per pipeline tile of the split kernel; the split chunk is a multiple of it.
-constexpr int kTileTokens = 32;
+// The per-sequence split chunk is a multiple of this many tokens (a multiple of every
+// kernel configuration's tile, so a TMA box never straddles a page).
+constexpr int kTileTokens = 64;
 // Balanced schedule: at most this many persistent CTAs (workspace is sized for it), and
 // batches above kMaxBalancedBatch sequences use the per-sequence schedule instead (their
 // units already fill the device, and every persistent CTA scans seq_lens once).

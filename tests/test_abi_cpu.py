@@ -41,18 +41,18 @@ def test_chunk_tokens_cover_and_round_to_tiles():
     for L in [0, 1, 31, 32, 33, 100, 2048, 32768]:
         for S in [1, 2, 3, 8, 32, 128]:
             c = binding.chunk_tokens(L, S)
-            assert c % 32 == 0 and c >= 32
+            assert c % 64 == 0 and c >= 64
             assert c * S >= L                       # S chunks cover the longest sequence
-            assert c - 32 < max(1, -(-L // S))      # and no chunk is a whole tile too long
+            assert c - 64 < max(1, -(-L // S))      # and no chunk is a whole tile too long
 
 
 def test_plan_splits_properties():
     # one SM-wave worth of long sequences is still split; huge batches are not
     assert binding.plan_splits(152, 1, 64, 8, 128, 64, 32768, 32768) > 8
     assert binding.plan_splits(152, 4096, 32, 8, 128, 16, 512, 4096 * 512) == 1
-    # never more splits than 32-token tiles of the longest sequence
+    # never more splits than 64-token chunks of the longest sequence
     for L in [1, 31, 100, 1000]:
-        assert binding.plan_splits(152, 1, 32, 1, 128, 16, L, L) <= -(-L // 32)
+        assert binding.plan_splits(152, 1, 32, 1, 128, 16, L, L) <= -(-L // 64)
     # degenerate inputs give one split
     assert binding.plan_splits(0, 1, 32, 8, 128, 16, 100, 100) == 1
     assert binding.plan_splits(152, 0, 32, 8, 128, 16, 100, 100) == 1

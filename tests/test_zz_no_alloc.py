@@ -49,7 +49,7 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point():
 
 
 def test_partials_beyond_the_scratch_are_refused():
-    case = inputs.make_paged_case(4, 64, 8, 128, 64, [4096] * 4, 9003).to("cuda")
+    case = inputs.make_paged_case(4, 64, 8, 128, 64, [8192] * 4, 9003).to("cuda")
     S = 128
     assert binding.workspace_bytes(4, 64, 8, 128, S) > binding.NOALLOC_SCRATCH_BYTES
     with pytest.raises(binding.DapError) as e:
