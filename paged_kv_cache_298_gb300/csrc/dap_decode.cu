@@ -1048,51 +1048,96 @@ __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
     r.store(p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh, lane);
 }
 
+// Balanced schedule: one CTA per output row.  Its threads resolve, in parallel, which
+// partial slot every CTA of the unit's range wrote (none for CTAs with an empty range) and
+// the row maximum; the four warps then split the partial-row loads, and the per-warp sums
+// are added through shared memory.
 template <int D>
-__global__ void __launch_bounds__(256) combine_balanced_kernel(const SplitParams p, int hpu, int nkvg) {
+__global__ void __launch_bounds__(128) combine_balanced_kernel(const SplitParams p, int hpu, int nkvg) {
+    constexpr int DPV = D / 32;
+    __shared__ int slots[kMaxPersistentCtas];
+    __shared__ float wts[kMaxPersistentCtas];
+    __shared__ float red[4][D + 2];
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= p.B * nkvg * hpu) return;
-    const int u = gw / hpu, hl2 = gw - u * hpu;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = blockIdx.x;
+    const int u = row / hpu, hl2 = row - u * hpu;
     const long long start = p.unit_info[2 * u], tb = p.unit_info[2 * u + 1];
     const long long T = *p.total_tiles;
     const long long P = p.num_ctas;
     const int c_first = (int)(((start + 1) * P - 1) / T);
     const int c_last = (int)(((start + tb) * P - 1) / T);
     if (c_first == c_last) return;  // finished in place by one CTA
-    // partial slot of CTA c for this unit, or -1 when c's range is empty (only when T < P)
-    auto slot_of = [&](int c) -> int {
-        const long long s_c = (long long)c * T / P, e_c = (long long)(c + 1) * T / P;
-        if (s_c == e_c) return -1;
-        return 2 * c + ((c == c_first && s_c < start) ? 1 : 0);
-    };
+    const int n = c_last - c_first + 1;
     float M = -INFINITY;
-    for (int c = c_first + lane; c <= c_last; c += 32) {
-        const int sl = slot_of(c);
-        if (sl >= 0) M = fmaxf(M, p.ml_part[((long long)sl * hpu + hl2) * 2]);
+    for (int i = tid; i < n; i += 128) {
+        const int c = c_first + i;
+        const long long s_c = (long long)c * T / P, e_c = (long long)(c + 1) * T / P;
+        const int sl = (s_c == e_c) ? -1 : 2 * c + ((c == c_first && s_c < start) ? 1 : 0);
+        slots[i] = sl;
+        const float m = sl >= 0 ? p.ml_part[((long long)sl * hpu + hl2) * 2] : -INFINITY;
+        wts[i] = m;
+        M = fmaxf(M, m);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-    RowMerge<D> r;
-    r.begin(M);
-    for (int c0 = c_first; c0 <= c_last;) {
-        const float *o[8];
-        float2 ml[8];
-        int n = 0;
-        for (; c0 <= c_last && n < 8; ++c0) {
-            const int sl = slot_of(c0);
-            if (sl < 0) continue;
-            const long long row = (long long)sl * hpu + hl2;
-            o[n] = p.o_part + row * D;
-            ml[n] = *reinterpret_cast<const float2 *>(p.ml_part + row * 2);
-            ++n;
+    if (lane == 0) red[warp][D] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(red[0][D], red[1][D]), fmaxf(red[2][D], red[3][D]));
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float lsum = 0.f;
+    for (int i = tid; i < n; i += 128) {
+        const int sl = slots[i];
+        float f = 0.f;
+        if (sl >= 0) {
+            f = ex2(wts[i] - Mu);
+            lsum = fmaf(f, p.ml_part[((long long)sl * hpu + hl2) * 2 + 1], lsum);
         }
-        r.add_batch(o, ml, n, lane);
+        wts[i] = f;
     }
-    const int b = u / nkvg, kvg = u - b * nkvg;
-    const int hq = kvg * hpu + hl2;
-    r.store(p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh, lane);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+    __syncthreads();  // wts complete; red[.][D] read by everyone
+    if (lane == 0) red[warp][D + 1] = lsum;
+    float acc[DPV];
+#pragma unroll
+    for (int j = 0; j < DPV; ++j) acc[j] = 0.f;
+    for (int i0 = warp; i0 < n; i0 += 4 * 8) {
+        float x[8][DPV];
+        float f[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = i0 + 4 * k;
+            const int sl = i < n ? slots[i] : -1;
+            f[k] = sl >= 0 ? wts[i] : 0.f;
+            if (sl >= 0) {
+                const float *o = p.o_part + ((long long)sl * hpu + hl2) * D + lane * DPV;
+#pragma unroll
+                for (int j = 0; j < DPV; ++j) x[k][j] = o[j];
+            } else {
+#pragma unroll
+                for (int j = 0; j < DPV; ++j) x[k][j] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+#pragma unroll
+            for (int j = 0; j < DPV; ++j) acc[j] = fmaf(f[k], x[k][j], acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < DPV; ++j) red[warp][lane * DPV + j] = acc[j];
+    __syncthreads();
+    if (warp == 0) {
+        const float L = red[0][D + 1] + red[1][D + 1] + red[2][D + 1] + red[3][D + 1];
+        float a[DPV];
+#pragma unroll
+        for (int j = 0; j < DPV; ++j)
+            a[j] = red[0][lane * DPV + j] + red[1][lane * DPV + j] + red[2][lane * DPV + j] + red[3][lane * DPV + j];
+        const int b = u / nkvg, kvg = u - b * nkvg;
+        __nv_bfloat16 *o = p.out + (long long)b * p.o_sb + (long long)(kvg * hpu + hl2) * p.o_sh + lane * DPV;
+#pragma unroll
+        for (int j = 0; j < DPV; j += 2) store_out_pair(o + j, a[j], a[j + 1], L);
+    }
 }
 
 // ---- host side ----------------------------------------------------------------------------
@@ -1227,8 +1272,11 @@ dap_status launch_balanced(const DecodeArgs &a, SplitParams &p, cudaStream_t str
     const int per_sm = prepare_kernel(kern, C::THREADS, C::SMEM, &occ);
     const int sms = dap_device_sm_count();
     if (per_sm <= 0 || sms <= 0) return DAP_ERR_CUDA;
-    const int P = std::min(sms * per_sm, kMaxPersistentCtas);
     const int nkvg = a.Hkv / C::HG;
+    // no more CTAs than the tiles there can be (each sequence takes at least one tile)
+    const long long max_tiles =
+        (long long)a.B * nkvg * std::max<long long>(1, (a.max_kv_len + C::BT - 1) / C::BT);
+    const int P = (int)std::min<long long>(std::min(sms * per_sm, kMaxPersistentCtas), max_tiles);
     const BalancedLayout lay = balanced_layout(a.B, nkvg, C::HPU, a.D);
     char *ws = static_cast<char *>(a.workspace);
     p.o_part = reinterpret_cast<float *>(ws + lay.acc);
@@ -1240,10 +1288,10 @@ dap_status launch_balanced(const DecodeArgs &a, SplitParams &p, cudaStream_t str
     kern<<<P, C::THREADS, C::SMEM, stream>>>(mk, mv, mq, p);
     if (cudaGetLastError() != cudaSuccess) return DAP_ERR_CUDA;
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
-    const dim3 cgrid((unsigned)((a.B * nkvg * C::HPU + 7) / 8));
+    const dim3 cgrid((unsigned)(a.B * nkvg * C::HPU));
     const cudaError_t e =
-        a.D == 128 ? launch_dependent(combine_balanced_kernel<128>, cgrid, dim3(256), stream, p, (int)C::HPU, nkvg)
-                   : launch_dependent(combine_balanced_kernel<64>, cgrid, dim3(256), stream, p, (int)C::HPU, nkvg);
+        a.D == 128 ? launch_dependent(combine_balanced_kernel<128>, cgrid, dim3(128), stream, p, (int)C::HPU, nkvg)
+                   : launch_dependent(combine_balanced_kernel<64>, cgrid, dim3(128), stream, p, (int)C::HPU, nkvg);
     if (e != cudaSuccess) return DAP_ERR_CUDA;
     if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);
     return DAP_OK;

@@ -127,9 +127,13 @@ def test_balanced_schedule_many_short_and_empty_sequences():
 
 
 def test_balanced_schedule_fewer_tiles_than_ctas():
-    # 3 tiles in all: most persistent CTAs get an empty range
-    case = inputs.make_paged_case(2, 16, 2, 128, 16, [40, 20], 85).to("cuda")
-    assert_close(gpu_paged(case, 0), oracle_paged(case), "tiny balanced")
+    # 4 tiles in all, but a loose max_kv_len bound sizes the grid for 64: most persistent
+    # CTAs get an empty range, and the combine must skip them
+    case = inputs.make_paged_case(2, 16, 2, 128, 16, [40, 20], 85, max_pages=64).to("cuda")
+    out = binding.decode_attn_paged(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                                    max_kv_len=1000, num_splits=0)
+    assert_close(out, oracle_paged(case), "tiny balanced")
+    assert binding.get_device_errors() == 0
 
 
 def test_strided_q_and_out_and_garbage_workspace():
