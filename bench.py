@@ -229,7 +229,8 @@ def run_ours(args):
     case = make_workload(args.workload, dev)
     hbm_peak, peak_src = peaks()
     sms = binding.device_sm_count()
-    S = args.splits  # 0 = the balanced schedule
+    S = args.splits if args.splits >= 0 else binding.plan_splits(
+        sms, case.B, case.Hq, case.Hkv, case.D, case.page_size, case.max_kv_len, case.total_kv)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     footprint = sum(t.numel() * t.element_size() for t in (case.q, case.k_cache, case.v_cache,
                                                            case.block_table, case.seq_lens))
@@ -390,7 +391,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ragged", choices=["ragged", "llama", "long1", "long4"])
-    ap.add_argument("--splits", type=int, default=0, help="0 = balanced schedule, S > 0 = per-sequence splits")
+    ap.add_argument("--splits", type=int, default=-1,
+                    help="-1 = the planner's choice, 0 = balanced schedule, S > 0 = per-sequence splits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

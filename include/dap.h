@@ -71,12 +71,12 @@ int dap_device_sm_count(void);
 
 /*
  * Split planner [B: split-KV and split-planner commits].
- * Returns the number of KV splits S >= 1 of the LONGEST sequence.  Every sequence is cut
- * into chunks of `dap_chunk_tokens(max_kv_len, S)` tokens, so sequence b runs
- * ceil(seq_lens[b] / chunk) splits (at least 1).  The plan fills `sm_count` SMs with
- * work units of balanced size: it aims for enough (sequence, kv head, chunk) units that
- * the largest unit is a small fraction of one SM's share of the KV bytes, and returns 1
- * when batch*kv_heads units already fill the device.
+ * Returns a recommended num_splits S >= 1 for the per-sequence schedule: every sequence is
+ * cut into chunks of dap_chunk_tokens(max_kv_len, S) tokens, so sequence b runs
+ * ceil(seq_lens[b] / chunk) splits (at least 1).  When B * Hkv (sequence, kv head) units
+ * are fewer than the GPU's resident CTAs (2 per SM), S is the number of chunks that fills
+ * one wave; otherwise S keeps the largest chunk near a tenth of one SM's share of the KV
+ * rows.  S never exceeds the number of 64-token chunks of the longest sequence.
  *   sm_count   SMs available (dap_device_sm_count()).
  *   total_kv   sum of seq_lens (host); 0 means "unknown", taken as B * max_kv_len.
  * Pure host function; no CUDA call.

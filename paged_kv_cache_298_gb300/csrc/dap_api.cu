@@ -128,16 +128,23 @@ int dap_plan_splits(int sm_count, int B, int Hq, int Hkv, int D, int page_size, 
     (void)page_size;
     if (sm_count <= 0 || B <= 0 || Hkv <= 0 || max_kv_len <= 0) return 1;
     if (total_kv <= 0) total_kv = (long long)B * max_kv_len;
-    // KV rows (token x kv head) each SM streams if the work is spread evenly.  A work unit
-    // (sequence, kv head, chunk) should be a small fraction of that share so that the
-    // last units to finish leave little of the device idle; a unit also needs enough tiles
-    // to amortise its pipeline fill.
-    const long long share = ceil_div_ll(total_kv * Hkv, sm_count);
-    const long long min_chunk = 256;
-    const long long chunk_target = std::max(min_chunk, share / 16);
-    long long S = ceil_div_ll(max_kv_len, chunk_target);
-    const long long max_tiles = ceil_div_ll(max_kv_len, kTileTokens);
-    S = std::min(S, max_tiles);
+    // Resident CTAs of the tensor-core configuration; one CTA per (sequence, kv head, chunk).
+    const long long slots = (long long)sm_count * 2;
+    const long long units = (long long)B * Hkv;
+    long long S;
+    if (units < slots) {
+        // Too few units to fill the GPU: cut every sequence into as many chunks as fit one
+        // wave, so equal-length batches finish together (AstrAI csrc log, split-KV commit:
+        // choose the split count to fill the device).
+        S = slots / units;
+    } else {
+        // Enough units: keep the largest unit a small fraction of one SM's share of the KV
+        // rows so the last units to finish leave little of the GPU idle.
+        const long long share = (total_kv * Hkv + sm_count - 1) / sm_count;
+        const long long chunk_target = std::max<long long>(256, share / 10);
+        S = ceil_div_ll(max_kv_len, chunk_target);
+    }
+    S = std::min(S, ceil_div_ll(max_kv_len, kTileTokens));
     S = std::min<long long>(S, 1024);
     return (int)std::max<long long>(1, S);
 }
