@@ -60,7 +60,7 @@ def bits(t: torch.Tensor) -> np.ndarray:
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples (20 ms) of SM clock and throttle reasons during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -75,7 +75,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-i", str(self.idx), "-lms", "200"], stdout=self.f,
+                                          "-i", str(self.idx), "-lms", "20"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -257,10 +257,6 @@ def run_ours(args):
         raise SystemExit("device error word set during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    for e in ev:   # torch creates the CUDA event on first record; the trace hook needs the handle
-        for x in e:
-            x.record(stream)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     if world > 1:
@@ -270,15 +266,27 @@ def run_ours(args):
     time.sleep(0.3)
     t_start.record(stream)
     for i in range(K):
-        binding.set_trace_events(*ev[i])
         step(i)
     t_end.record(stream)
     torch.cuda.synchronize()
-    binding.set_trace_events()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
     ms = t_start.elapsed_time(t_end) / K
+
+    # the split kernel's own duration: events around each launch (a separate loop, because an
+    # event between the two kernels stops the combine from overlapping the split kernel's tail)
+    KT = min(K, 50)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(KT)]
+    for e in ev:   # torch creates the CUDA event on first record; the trace hook needs the handle
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    for i in range(KT):
+        binding.set_trace_events(*ev[i])
+        step(i)
+    torch.cuda.synchronize()
+    binding.set_trace_events()
     split_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     combine_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     errs = binding.get_device_errors(clear=True)
@@ -354,12 +362,135 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---- fp8 sliding-window latent decode -----------------------------------------------------
+
+def fp8_counts(case):
+    """Participating rows per token (j < min(len, W), slot >= 0), from the inputs."""
+    idx = case.indices.cpu()
+    lens = case.lens.cpu().clamp(min=0, max=case.W)
+    j = torch.arange(case.W)[None, :]
+    return ((j < lens[:, None]) & (idx >= 0)).sum(dim=1)
+
+
+def fp8_algorithmic(case):
+    """Bytes: q + out + every participating fp8 row and its bf16 inverse scale + the slot
+    table + lens.  Flops: QK^T and PV, 2 * 2 * NH * rows * HD per token."""
+    n = fp8_counts(case)
+    rows = int(n.sum())
+    nbytes = 2 * case.T * case.NH * case.HD * 2 + rows * (case.HD + 2) + case.T * case.W * 8 + case.T * 8
+    flops = 4 * case.NH * case.HD * rows
+    return nbytes, flops, rows
+
+
+def run_fp8(args):
+    from paged_kv_cache_298_gb300 import binding, inputs
+    rank, local, world = rank_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load()
+    case = inputs.fp8_swa(device=dev)
+    hbm_peak, peak_src = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    parts = (case.q, case.kv_cache, case.inv_scale, case.indices, case.lens)
+    footprint = sum(t.numel() * t.element_size() for t in parts) + case.q.numel() * 2
+    copies = 1 + max(1, math.ceil(2 * l2 / footprint))
+    sets = [parts] + [tuple(t.clone() for t in parts) for _ in range(copies - 1)]
+    outs = [torch.empty_like(case.q) for _ in sets]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        q, kv, inv, idx, ln = sets[i % copies]
+        binding.decode_attn_paged_fp8(q, kv, inv, idx, ln, scale=case.scale, out=outs[i % copies])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    K = args.steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for i in range(K):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / K
+    KT = min(K, 50)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(KT)]
+    for i in range(KT):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    errs = binding.get_device_errors(clear=True)
+    nbytes, flops, rows = fp8_algorithmic(case)
+    value = world * nbytes / (ms * 1e-3) / 1e9
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    line = {
+        "metric": "fp8 sliding-window latent decode achieved HBM GB/s (algorithmic bytes), cold inputs",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "us_per_call": round(ms * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": case.name, "T": case.T, "NH": case.NH, "HD": case.HD, "W": case.W,
+                   "num_blocks": case.num_blocks, "block_size": case.block_size, "rows": rows,
+                   "kv_dtype": "fp8-e4m3", "cold": f"{copies} rotated input copies of {footprint / 1e6:.1f} MB"},
+        "roofline": {"bound": "hbm", "kernel": "swa_kernel", "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "kernel_ms": round(kern_ms, 5), "algorithmic_bytes_per_launch": nbytes,
+                     "tflops": round(flops / (kern_ms * 1e-3) / 1e12, 2), "traffic": None},
+        "gpu_launches": K, "device_errors": errs, "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        cq, ckv, cinv, cidx, cln = (t.cpu() for t in parts)
+        tt = time.perf_counter()
+        oracle.fp8_swa(bits(cq), ckv.numpy(), bits(cinv), cidx.numpy(), cln.numpy(), case.block_size, case.scale)
+        dt = time.perf_counter() - tt
+        line["cpu_baseline"] = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+                                "kind": "oracle", "sample": f"fp64 oracle (OpenMP), all {case.T} tokens, one pass, "
+                                                            f"{dt:.2f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ---- reference arm: the fp64 oracle on the host cores ----------------------------------
+
+def run_reference_fp8(args):
+    import oracle
+    from paged_kv_cache_298_gb300 import inputs
+    case = inputs.fp8_swa()
+    nbytes, _, _ = fp8_algorithmic(case)
+    a = (bits(case.q), case.kv_cache.numpy(), bits(case.inv_scale), case.indices.numpy(), case.lens.numpy())
+    for _ in range(args.warmup):
+        oracle.fp8_swa(*a, case.block_size, case.scale)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.fp8_swa(*a, case.block_size, case.scale)
+        times.append(time.perf_counter() - t0)
+    dt = statistics.mean(times)
+    value = nbytes / dt / 1e9
+    print(json.dumps({
+        "impl": "reference",
+        "metric": "fp8 sliding-window latent decode achieved HBM GB/s (algorithmic bytes), cold inputs",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": {"workload": case.name},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"fp64 oracle (OpenMP), all {case.T} tokens per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+        flush=True)
+
 
 def run_reference(args):
     rank, _, world = rank_info()
     if rank != 0:
         return
+    if args.workload == "fp8":
+        return run_reference_fp8(args)
     case = make_workload(args.workload, "cpu")
     r = OracleRunner(case)
     rows = r.sample_rows(target_s=min(8.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -387,10 +518,10 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="ragged", choices=["ragged", "llama", "long1", "long4"])
+    ap.add_argument("--workload", default="ragged", choices=["ragged", "llama", "long1", "long4", "fp8"])
     ap.add_argument("--splits", type=int, default=-1,
                     help="-1 = the planner's choice, 0 = balanced schedule, S > 0 = per-sequence splits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -399,6 +530,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "fp8":
+        run_fp8(args)
     else:
         run_ours(args)
 
