@@ -139,6 +139,17 @@ def recorded_traffic(workload_key: str):
     return None
 
 
+def job_throughput(ms_list, nbytes_per_rank, world, device):
+    """Whole-job GB/s for each timing in ms_list: every rank processed nbytes_per_rank, and
+    the job took as long as its slowest rank (max over ranks of each timing).  Returns
+    [(GB/s, max ms), ...].  With world > 1 it needs an initialised process group."""
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in ms_list], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [(world * nbytes_per_rank / (m * 1e-3) / 1e9, m) for m in t.tolist()]
+
+
 # ---- workloads ---------------------------------------------------------------------------
 
 def make_workload(name: str, device):
@@ -328,12 +339,7 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1) / K
 
     nbytes = algorithmic_bytes(case)
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = t.tolist()
-    value = world * nbytes / (ms * 1e-3) / 1e9
-    e2e_value = world * nbytes / (e2e_ms * 1e-3) / 1e9
+    (value, ms), (e2e_value, e2e_ms) = job_throughput([ms, e2e_ms], nbytes, world, dev)
     achieved = nbytes / (split_ms * 1e-3) / 1e9
     line = {
         "metric": "paged decode attention achieved HBM GB/s (algorithmic bytes), cold KV",
@@ -385,8 +391,11 @@ def fp8_algorithmic(case):
 def run_fp8(args):
     from paged_kv_cache_298_gb300 import binding, inputs
     rank, local, world = rank_info()
+    import torch.distributed as dist
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
     binding.load()
     case = inputs.fp8_swa(device=dev)
     hbm_peak, peak_src = peaks()
@@ -408,6 +417,9 @@ def run_fp8(args):
     K = args.steps
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
     t0.record(stream)
@@ -427,7 +439,9 @@ def run_fp8(args):
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     errs = binding.get_device_errors(clear=True)
     nbytes, flops, rows = fp8_algorithmic(case)
-    value = world * nbytes / (ms * 1e-3) / 1e9
+    if world > 1:
+        dist.barrier()
+    (value, ms), = job_throughput([ms], nbytes, world, dev)
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
     line = {
         "metric": "fp8 sliding-window latent decode achieved HBM GB/s (algorithmic bytes), cold inputs",
@@ -454,6 +468,8 @@ def run_fp8(args):
                                                             f"{dt:.2f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
 
 
 # ---- reference arm: the fp64 oracle on the host cores ----------------------------------
