@@ -21,7 +21,7 @@
 //      in shared memory as a 128-byte-swizzled [hd block][row][64] tile; rows n..n16-1 are
 //      zero (n16 = n rounded up to 16);
 //   3. q[t, heads, :] streams in through TMA (128B swizzle) in eight 64-wide blocks over a
-//      3-stage ring, and one thread issues S = Q . KV^T (M=128, N=n16, K=512) into TMEM;
+//      4-stage ring started before the gather, and one thread issues S = Q . KV^T (M=128, N=n16, K=512) into TMEM;
 //   4. each thread owns one head (one TMEM lane): base-2 softmax over its n scores, the
 //      probabilities rounded to bf16 into a swizzled P tile, l = their sum;
 //   5. O[:, half] = P . KV[:, half] (M=128, N=256, K=n16) reads the same KV tile as an
@@ -55,7 +55,7 @@ constexpr int kHeads = 128;         // heads per CTA = MMA M
 constexpr int kMaxRows = 128;       // window rows a CTA holds
 constexpr int kHalf = kHD / 2;      // output columns per CTA
 constexpr int kThreads = 128;
-constexpr int kQStages = 3;
+constexpr int kQStages = 4;
 // shared-memory map (offsets from a 1024-byte aligned base)
 constexpr int kKvOff = 0;                                   // [8 blocks][128 rows][128 B]
 constexpr int kKvBlock = kMaxRows * 128;                    // 16 KB per 64-wide hd block
@@ -197,7 +197,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&mma_done[1], 1);
         cnt[5] = 0;
         fence_barrier_init();
-        prefetch_tensormap(&qmap);
+        // start streaming q (the first kQStages of its eight 64-wide blocks) right away, so
+        // the copies overlap the window compaction and the gather
+        const int qrow0 = t * p.NH + hg * kHeads;
+        for (int kb = 0; kb < kQStages; ++kb) {
+            mbar_arrive_expect_tx(&q_full[kb], kQStage);
+            tma_load_2d(smem + kQOff + kb * kQStage, &qmap, kb * 64, qrow0, &q_full[kb]);
+        }
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -236,46 +242,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int n16 = (n + 15) & ~15;
 
-    // ---- 3a. start streaming q (three of the eight 64-wide blocks) -------------------------
     const int qrow = t * p.NH + hg * kHeads;
-    if (tid == 0 && n > 0) {
-        for (int kb = 0; kb < kQStages; ++kb) {
-            mbar_arrive_expect_tx(&q_full[kb], kQStage);
-            tma_load_2d(smem + kQOff + kb * kQStage, &qmap, kb * 64, qrow, &q_full[kb]);
-        }
-    }
     __syncthreads();  // rows[] / invs[] complete
 
     // ---- 2. gather + dequantise the rows into the swizzled KV tile -------------------------
+    // Each thread issues kBatch independent 16-byte loads before converting any of them, so
+    // the row gathers overlap instead of paying one memory round trip each.
     if (n > 0) {
-        for (int item = tid; item < n16 * 32; item += kThreads) {
-            const int r = item >> 5;   // row
-            const int c = item & 31;   // 16-byte piece of the 512-byte fp8 row = 16 hd values
-            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-            if (r < n) {
-                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(p.kv_cache + (long long)rows[r] * kHD) + c);
-                const float inv = invs[r];
-                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-                uint32_t o[8];
+        constexpr int kBatch = 16;
+        const int total = n16 * 32;  // 16-byte pieces: 32 per 512-byte fp8 row
+        for (int base0 = 0; base0 < total; base0 += kThreads * kBatch) {
+            uint4 raw[kBatch];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w4[i] >> (16 * j)) & 0xFFFFu);
-                        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
-                        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * inv, f.y * inv);
-                        o[2 * i + j] = *reinterpret_cast<const uint32_t *>(&b);
-                    }
-                }
-                lo = make_uint4(o[0], o[1], o[2], o[3]);
-                hi = make_uint4(o[4], o[5], o[6], o[7]);
+            for (int k = 0; k < kBatch; ++k) {
+                const int item = base0 + k * kThreads + tid;
+                const int r = item >> 5;
+                raw[k] = make_uint4(0u, 0u, 0u, 0u);
+                if (item < total && r < n)
+                    raw[k] = __ldg(reinterpret_cast<const uint4 *>(p.kv_cache + (long long)rows[r] * kHD) + (item & 31));
             }
-            const int blk = c >> 2;            // 64-wide hd block
-            const int k0 = (c & 3) * 2;        // first 16-byte chunk inside the 128-byte row
-            uint8_t *tile = smem + kKvOff + blk * kKvBlock;
-            *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0)) = lo;
-            *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0 + 1)) = hi;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int item = base0 + k * kThreads + tid;
+                if (item < total) {
+                    const int r = item >> 5;   // row
+                    const int c = item & 31;   // 16-byte piece = 16 hd values
+                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                    if (r < n) {
+                        const float inv = invs[r];
+                        const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+                        uint32_t o[8];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const __nv_fp8x2_storage_t pr =
+                                    (__nv_fp8x2_storage_t)((w4[i] >> (16 * j)) & 0xFFFFu);
+                                const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+                                const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * inv, f.y * inv);
+                                o[2 * i + j] = *reinterpret_cast<const uint32_t *>(&b);
+                            }
+                        }
+                        lo = make_uint4(o[0], o[1], o[2], o[3]);
+                        hi = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                    const int blk = c >> 2;       // 64-wide hd block
+                    const int k0 = (c & 3) * 2;   // first 16-byte chunk inside the 128-byte row
+                    uint8_t *tile = smem + kKvOff + blk * kKvBlock;
+                    *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0)) = lo;
+                    *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0 + 1)) = hi;
+                }
+            }
         }
     }
     fence_async_smem();
@@ -402,6 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_full[i], 0);
         umma_commit(&mma_done[1]);
         (void)mbar_wait(&mma_done[1], 0);
+    }
+    if (tid == 0 && n == 0) {
+        // no row: nothing consumed the q blocks started at the top; let them land
+        for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_full[i], 0);
     }
     tc_fence_before();
     __syncthreads();
