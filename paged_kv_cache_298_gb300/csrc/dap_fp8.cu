@@ -22,8 +22,9 @@
 //      zero (n16 = n rounded up to 16);
 //   3. q[t, heads, :] streams in through TMA (128B swizzle) in eight 64-wide blocks over a
 //      4-stage ring started before the gather, and one thread issues S = Q . KV^T (M=128, N=n16, K=512) into TMEM;
-//   4. each thread owns one head (one TMEM lane): base-2 softmax over its n scores, the
-//      probabilities rounded to bf16 into a swizzled P tile, l = their sum;
+//   4. two threads own each head (one TMEM lane, half of the score columns each): base-2
+//      softmax over its n scores, the probabilities rounded to bf16 into a swizzled P tile,
+//      l = their sum;
 //   5. O[:, half] = P . KV[:, half] (M=128, N=256, K=n16) reads the same KV tile as an
 //      MN-major operand;
 //   6. out = O / l in bf16.
@@ -54,26 +55,33 @@ constexpr int kHD = 512;            // latent width
 constexpr int kHeads = 128;         // heads per CTA = MMA M
 constexpr int kMaxRows = 128;       // window rows a CTA holds
 constexpr int kHalf = kHD / 2;      // output columns per CTA
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;            // 8 warps: warps w and w+4 share TMEM lanes
 constexpr int kQStages = 4;
 // shared-memory map (offsets from a 1024-byte aligned base)
-constexpr int kKvOff = 0;                                   // [8 blocks][128 rows][128 B]
-constexpr int kKvBlock = kMaxRows * 128;                    // 16 KB per 64-wide hd block
-constexpr int kQOff = kKvOff + 8 * kKvBlock;                // 131072
-constexpr int kQStage = kHeads * 128;                       // 16 KB: 128 heads x 64 bf16
-constexpr int kPOff = kQOff;                                // P reuses the Q ring after QK
+constexpr int kQOff = 0;                                    // q ring: 4 stages of 128 heads x 64
+constexpr int kQStage = kHeads * 128;                       // 16 KB per stage
+constexpr int kPOff = kQOff;                                // P reuses the ring after QK
 constexpr int kPBlock = kHeads * 128;                       // 16 KB per 64-wide row block
-constexpr int kRowsOff = kQOff + kQStages * kQStage;        // int32 slot per kept row
+constexpr int kOOff = kQOff;                                // bf16 output staging after PV (64 KB)
+constexpr int kXchOff = kPOff + 2 * kPBlock;                // softmax max/sum exchange (2 KB)
+constexpr int kKvOff = kQOff + kQStages * kQStage;          // 65536: [8 blocks][n16 rows][128 B]
+constexpr int kFitRows = 96;                                // windows of <= 96 rows leave room for
+constexpr int kQExtraOff = kKvOff + 8 * kFitRows * 128;     // q blocks 4..7 here (no ring refills)
+constexpr int kKvEnd = kKvOff + 8 * kMaxRows * 128;
+constexpr int kQExtraEnd = kQExtraOff + 4 * kQStage;
+constexpr int kRowsOff = kKvEnd > kQExtraEnd ? kKvEnd : kQExtraEnd;  // int32 slot per kept row
 constexpr int kInvOff = kRowsOff + kMaxRows * 4;            // f32 inverse scale per kept row
-constexpr int kCntOff = kInvOff + kMaxRows * 4;             // per-warp counts, n, abort
+constexpr int kCntOff = kInvOff + kMaxRows * 4;             // per-warp counts [0..7], abort [12]
 constexpr int kBarOff = kCntOff + 64;                       // mbarriers
-constexpr int kNumBars = 2 * kQStages + 2;
+constexpr int kNumBars = 3 * kQStages + 2;                  // q_full, q_free, q_extra, mma_done[2]
 constexpr int kTmemOff = kBarOff + kNumBars * 8;
 constexpr int kSmemUsed = kTmemOff + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;                // slack to align the base
 constexpr int kTmemCols = 512;                              // O: cols [0,256), S: [256,384)
 constexpr int kSCol = 256;
-static_assert(kPOff + 2 * kPBlock <= kRowsOff, "P fits in the Q ring");
+static_assert(kPOff + 2 * kPBlock <= kKvOff, "P fits in the q ring");
+static_assert(kOOff + kHeads * kHalf * 2 <= kKvOff, "the output staging fits in the q ring");
+static_assert(kXchOff + 4 * kHeads * 4 <= kKvOff, "the softmax exchange fits in the q ring");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // ---- tcgen05 / descriptor helpers ---------------------------------------------------------
@@ -144,12 +152,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 64 consecutive fp32 columns of this thread's TMEM lane (one load, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
         : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&b);
 }
 
 // Byte offset of 16-byte chunk `k` (0..7) of row `r` in a 128-byte-swizzled tile whose
@@ -185,17 +211,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *cnt = reinterpret_cast<int *>(smem + kCntOff);     // [0..3] warp counts, [4] n, [5] abort
     uint64_t *q_full = reinterpret_cast<uint64_t *>(smem + kBarOff);
     uint64_t *q_free = q_full + kQStages;
-    uint64_t *mma_done = q_free + kQStages;
+    uint64_t *q_extra = q_free + kQStages;
+    uint64_t *mma_done = q_extra + kQStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
 
     if (tid == 0) {
         for (int i = 0; i < kQStages; ++i) {
             mbar_init(&q_full[i], 1);
             mbar_init(&q_free[i], 1);
+            mbar_init(&q_extra[i], 1);
         }
         mbar_init(&mma_done[0], 1);
         mbar_init(&mma_done[1], 1);
-        cnt[5] = 0;
+        cnt[12] = 0;
         fence_barrier_init();
         // start streaming q (the first kQStages of its eight 64-wide blocks) right away, so
         // the copies overlap the window compaction and the gather
@@ -234,7 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     int base = 0;
     for (int w = 0; w < warp; ++w) base += cnt[w];
-    const int n = cnt[0] + cnt[1] + cnt[2] + cnt[3];
+    int n = 0;
+    for (int w = 0; w < kThreads / 32; ++w) n += cnt[w];
     if (keep) {
         const int pos = base + __popc(ball & ((1u << lane) - 1u));
         rows[pos] = (int)slot;
@@ -243,6 +272,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n16 = (n + 15) & ~15;
 
     const int qrow = t * p.NH + hg * kHeads;
+    const int kvb = n16 * 128;                  // bytes per 64-wide hd block of the KV tile
+    const bool q_all = n > 0 && n16 <= kFitRows;  // room for all eight q blocks at once
+    if (tid == 0 && q_all) {
+        for (int kb = kQStages; kb < 8; ++kb) {
+            mbar_arrive_expect_tx(&q_extra[kb - kQStages], kQStage);
+            tma_load_2d(smem + kQExtraOff + (kb - kQStages) * kQStage, &qmap, kb * 64, qrow, &q_extra[kb - kQStages]);
+        }
+    }
     __syncthreads();  // rows[] / invs[] complete
 
     // ---- 2. gather + dequantise the rows into the swizzled KV tile -------------------------
@@ -289,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int blk = c >> 2;       // 64-wide hd block
                     const int k0 = (c & 3) * 2;   // first 16-byte chunk inside the 128-byte row
-                    uint8_t *tile = smem + kKvOff + blk * kKvBlock;
+                    uint8_t *tile = smem + kKvOff + blk * kvb;
                     *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0)) = lo;
                     *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0 + 1)) = hi;
                 }
@@ -308,19 +345,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idS = idesc_bf16(kHeads, n16, 0);
         for (int kb = 0; kb < 8 && ok; ++kb) {
             const int st = kb % kQStages;
-            if (!mbar_wait(&q_full[st], (kb / kQStages) & 1)) {
+            const bool extra = q_all && kb >= kQStages;
+            if (!(extra ? mbar_wait(&q_extra[kb - kQStages], 0) : mbar_wait(&q_full[st], (kb / kQStages) & 1))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t qa = smem_addr(smem + kQOff + st * kQStage);
-            const uint32_t kva = smem_addr(smem + kKvOff + kb * kKvBlock);
+            const uint32_t qa = smem_addr(smem + (extra ? kQExtraOff + (kb - kQStages) * kQStage : kQOff + st * kQStage));
+            const uint32_t kva = smem_addr(smem + kKvOff + kb * kvb);
 #pragma unroll
             for (int k16 = 0; k16 < 4; ++k16)
                 umma_bf16(tS, sw128_desc(qa + 32 * k16, 16, 1024), sw128_desc(kva + 32 * k16, 16, 1024), idS,
                           (kb | k16) != 0);
-            umma_commit(&q_free[st]);
-            if (kb + kQStages < 8) {  // refill this stage once its MMAs have read it
+            if (!q_all && kb + kQStages < 8) {  // refill this stage once its MMAs have read it
+                umma_commit(&q_free[st]);
                 if (!mbar_wait(&q_free[st], (kb / kQStages) & 1)) {
                     ok = false;
                     break;
@@ -330,47 +368,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         umma_commit(&mma_done[0]);
-        if (!ok) cnt[5] = 1;
+        if (!ok) cnt[12] = 1;
     }
 
     // ---- 4. softmax: thread = head = TMEM lane -------------------------------------------------
     bool waited = true;
     if (n > 0) waited = mbar_wait(&mma_done[0], 0);
-    const int good = __syncthreads_and(waited && cnt[5] == 0);
+    const int good = __syncthreads_and(waited && cnt[12] == 0);
     tc_fence_after();
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // thread = (head hrow = TMEM lane, column half chalf): warps w and w + 4 read the same
+    // 32 lanes, the first the low 64 score columns, the second the high ones
+    const int hrow = tid & (kHeads - 1);
+    const int chalf = warp >> 2;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    float *xch = reinterpret_cast<float *>(smem + kXchOff);  // [2][128] max, then [2][128] sum
     float l = 0.f;
     if (good && n > 0) {
+        const int c0 = chalf * 64;
+        float v[64];
         float m = -INFINITY;
-        for (int c0 = 0; c0 < n16; c0 += 32) {
-            float v[32];
-            tmem_ld32(tS + lane_base + c0, v);
+        if (c0 < n16) {  // columns past n16 are read but masked
+            tmem_ld64(tS + lane_base + c0, v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
+            for (int i = 0; i < 64; ++i)
                 if (c0 + i < n) m = fmaxf(m, v[i] * p.qscale);
         }
-        for (int c0 = 0; c0 < n16; c0 += 32) {
-            float v[32];
-            tmem_ld32(tS + lane_base + c0, v);
+        xch[chalf * kHeads + hrow] = m;
+        __syncthreads();
+        m = fmaxf(xch[hrow], xch[kHeads + hrow]);
+        float lp = 0.f;
+        if (c0 < n16) {
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
+            for (int g = 0; g < 8; ++g) {
                 const int j0 = c0 + 8 * g;
-                if (j0 >= n16) break;
-                uint32_t pk[4];
+                if (j0 < n16) {
+                    uint32_t pk[4];
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const float p0 = (j0 + e < n) ? ex2(v[8 * g + e] * p.qscale - m) : 0.f;
-                    const float p1 = (j0 + e + 1 < n) ? ex2(v[8 * g + e + 1] * p.qscale - m) : 0.f;
-                    const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
-                    const float2 r = __bfloat1622float2(b);
-                    l += r.x + r.y;  // the sum of the weights PV actually uses
-                    pk[e / 2] = *reinterpret_cast<const uint32_t *>(&b);
+                    for (int e = 0; e < 8; e += 2) {
+                        const float p0 = (j0 + e < n) ? ex2(v[8 * g + e] * p.qscale - m) : 0.f;
+                        const float p1 = (j0 + e + 1 < n) ? ex2(v[8 * g + e + 1] * p.qscale - m) : 0.f;
+                        const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
+                        const float2 r = __bfloat1622float2(b);
+                        lp += r.x + r.y;  // the sum of the weights PV actually uses
+                        pk[e / 2] = *reinterpret_cast<const uint32_t *>(&b);
+                    }
+                    uint8_t *tile = smem + kPOff + (j0 >> 6) * kPBlock;
+                    *reinterpret_cast<uint4 *>(tile + sw128_off(hrow, (j0 & 63) >> 3)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
-                uint8_t *tile = smem + kPOff + (j0 >> 6) * kPBlock;
-                *reinterpret_cast<uint4 *>(tile + sw128_off(tid, (j0 & 63) >> 3)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
         }
+        xch[2 * kHeads + chalf * kHeads + hrow] = lp;
+        __syncthreads();
+        l = xch[2 * kHeads + hrow] + xch[3 * kHeads + hrow];
     }
     fence_async_smem();
     tc_fence_before();
@@ -381,10 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0 && good && n > 0) {
         const uint32_t idO = idesc_bf16(kHeads, kHalf, 1);
         const uint32_t pa = smem_addr(smem + kPOff);
-        const uint32_t kvb = smem_addr(smem + kKvOff + col_half * 4 * kKvBlock);
+        const uint32_t kvh = smem_addr(smem + kKvOff + col_half * 4 * kvb);
         for (int k16 = 0; k16 < n16 / 16; ++k16)
             umma_bf16(tmem, sw128_desc(pa + (k16 >> 2) * kPBlock + (k16 & 3) * 32, 16, 1024),
-                      sw128_desc(kvb + k16 * 2048, kKvBlock, 1024), idO, k16 > 0);
+                      sw128_desc(kvh + k16 * 2048, (uint32_t)kvb, 1024), idO, k16 > 0);
         umma_commit(&mma_done[0]);
     }
     bool waited2 = true;
@@ -393,37 +443,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
 
     // ---- 6. out = O / l --------------------------------------------------------------------------
+    // Each thread turns half of its head's 256 columns into bf16 in a staging area (16-byte
+    // chunk c of row h at chunk c ^ (h mod 32), conflict-free both ways); then the CTA writes
+    // the 128 rows out with fully coalesced 16-byte stores.
+    if (tid == 0 && n == 0) {
+        // no row: nothing consumed the q blocks started at the top; let them land before the
+        // staging area (the q ring) is written
+        for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_full[i], 0);
+    }
+    __syncthreads();
     if (good2) {
-        __nv_bfloat16 *orow = p.out + ((long long)t * p.NH + hg * kHeads + tid) * kHD + col_half * kHalf;
+        uint8_t *ostage = smem + kOOff;
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        for (int c0 = 0; c0 < kHalf; c0 += 32) {
-            float v[32];
+        for (int c0 = chalf * (kHalf / 2); c0 < (chalf + 1) * (kHalf / 2); c0 += 64) {
+            float v[64];
             if (n > 0) {
-                tmem_ld32(tmem + lane_base + c0, v);
+                tmem_ld64(tmem + lane_base + c0, v);
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                for (int i = 0; i < 64; ++i) v[i] = 0.f;
             }
-            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i] * inv, v[2 * i + 1] * inv);
-                pk[i] = *reinterpret_cast<const uint32_t *>(&b);
+            for (int q8 = 0; q8 < 8; ++q8) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) pk[i] = pack_bf16(v[8 * q8 + 2 * i] * inv, v[8 * q8 + 2 * i + 1] * inv);
+                const int ch = c0 / 8 + q8;  // 0..31
+                *reinterpret_cast<uint4 *>(ostage + hrow * (kHalf * 2) + ((ch ^ (hrow & 31)) << 4)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+        __syncthreads();
+        __nv_bfloat16 *obase = p.out + ((long long)t * p.NH + hg * kHeads) * kHD + col_half * kHalf;
+        for (int idx = tid; idx < kHeads * 32; idx += kThreads) {
+            const int row = idx >> 5, ch = idx & 31;
+            const uint4 val = *reinterpret_cast<const uint4 *>(ostage + row * (kHalf * 2) + ((ch ^ (row & 31)) << 4));
+            *reinterpret_cast<uint4 *>(obase + (long long)row * kHD + ch * 8) = val;
         }
     } else if (tid == 0 && n > 0) {
         // A wait gave up.  Let the copies and products still in flight land (bounded) before
         // the tensor memory and the shared memory are released.
         for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_full[i], 0);
+        if (q_all)
+            for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_extra[i], 0);
         umma_commit(&mma_done[1]);
         (void)mbar_wait(&mma_done[1], 0);
-    }
-    if (tid == 0 && n == 0) {
-        // no row: nothing consumed the q blocks started at the top; let them land
-        for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_full[i], 0);
     }
     tc_fence_before();
     __syncthreads();
