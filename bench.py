@@ -114,40 +114,34 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def kernel_source_sha() -> str:
+KERNEL_SOURCES = {"split_kernel": ("dap_decode.cu", "dap_device.cuh", "dap_internal.h"),
+                  "swa_kernel": ("dap_fp8.cu", "dap_device.cuh", "dap_internal.h")}
+
+
+def kernel_source_sha(kernel: str) -> str:
+    """Hash of the sources a kernel is built from (a recorded ncu figure is only reported
+    while they are unchanged)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_298_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_key: str):
-    """DRAM bytes per split-kernel launch from the committed ncu summary, if it was taken
-    on the current kernel source for this workload; else None."""
-    p = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+def recorded_traffic(kernel: str, workload_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel source for this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        e = d.get(workload_key)
-        if e and e.get("source_sha") == kernel_source_sha():
+        e = d.get(kernel, {}).get(workload_key)
+        if e and e.get("source_sha") == kernel_source_sha(kernel):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
     return None
-
-
-def job_throughput(ms_list, nbytes_per_rank, world, device):
-    """Whole-job GB/s for each timing in ms_list: every rank processed nbytes_per_rank, and
-    the job took as long as its slowest rank (max over ranks of each timing).  Returns
-    [(GB/s, max ms), ...].  With world > 1 it needs an initialised process group."""
-    import torch.distributed as dist
-    t = torch.tensor([float(x) for x in ms_list], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return [(world * nbytes_per_rank / (m * 1e-3) / 1e9, m) for m in t.tolist()]
 
 
 # ---- workloads ---------------------------------------------------------------------------
@@ -352,7 +346,7 @@ def run_ours(args):
                      "peak": hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "split_kernel_ms": round(split_ms, 5),
                      "combine_ms": round(combine_ms, 5), "algorithmic_bytes_per_launch": nbytes,
-                     "traffic": recorded_traffic(args.workload)},
+                     "traffic": recorded_traffic("split_kernel", args.workload)},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": hq.numel() * 2 + ht.numel() * 4 + hl.numel() * 4,
                 "d2h_bytes_per_step": ho.numel() * 2},
@@ -454,7 +448,8 @@ def run_fp8(args):
         "roofline": {"bound": "hbm", "kernel": "swa_kernel", "achieved": round(achieved, 1), "peak": hbm_peak,
                      "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                      "kernel_ms": round(kern_ms, 5), "algorithmic_bytes_per_launch": nbytes,
-                     "tflops": round(flops / (kern_ms * 1e-3) / 1e12, 2), "traffic": None},
+                     "tflops": round(flops / (kern_ms * 1e-3) / 1e12, 2),
+                     "traffic": recorded_traffic("swa_kernel", "fp8")},
         "gpu_launches": K, "device_errors": errs, "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
