@@ -144,6 +144,17 @@ def recorded_traffic(kernel: str, workload_key: str):
     return None
 
 
+def job_throughput(ms_list, nbytes_per_rank, world, device):
+    """Whole-job GB/s for each timing in ms_list: every rank processed nbytes_per_rank, and
+    the job took as long as its slowest rank (max over ranks of each timing).  Returns
+    [(GB/s, max ms), ...].  With world > 1 it needs an initialised process group."""
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in ms_list], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [(world * nbytes_per_rank / (m * 1e-3) / 1e9, m) for m in t.tolist()]
+
+
 # ---- workloads ---------------------------------------------------------------------------
 
 def make_workload(name: str, device):
