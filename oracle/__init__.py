@@ -73,6 +73,12 @@ def _load():
         lib.oracle_decode_contig.restype = I
         lib.oracle_fp8_swa_range.argtypes = [P, P, P, P, P, I, I, I, I, I, I, D, I, I, P]
         lib.oracle_fp8_swa_range.restype = None
+        lib.oracle_kv_append_paged.argtypes = [P, P, P, P, I, I, P, I, P, I, I, I]
+        lib.oracle_kv_append_paged.restype = I
+        lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+        lib.oracle_kv_append_fp8.argtypes = [P, P, P, P, I, I, I, I]
+        lib.oracle_kv_append_fp8.restype = I
         _lib = lib
         return lib
 
@@ -185,3 +191,36 @@ def fp8_swa(q, kv_cache, inv_scale, indices, lens, block_size: int, scale: float
     _load().oracle_fp8_swa_range(_ptr(q), _ptr(cache), _ptr(inv), _ptr(idx), _ptr(ln), T, NH,
                                  HD, W, NB, bs, float(scale), int(t0), int(t1), _ptr(out))
     return out
+
+
+def e4m3_from_float(x: float) -> int:
+    """Nearest E4M3FN code of a binary32 value (ties to even, saturating)."""
+    return int(_load().oracle_e4m3_from_float(float(x)))
+
+
+def kv_append_paged(k_new, v_new, k_cache, v_cache, block_table, pos):
+    """Return copies of the caches with each sequence's new K/V rows written at position
+    pos[b].  k_new, v_new [B,Hkv,D] u16; caches [P,ps,Hkv,D] u16."""
+    k_new = _u16(k_new); v_new = _u16(v_new)
+    kc = np.array(k_cache, dtype=np.uint16, copy=True)
+    vc = np.array(v_cache, dtype=np.uint16, copy=True)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    ps_ = np.ascontiguousarray(pos, dtype=np.int32)
+    B, Hkv, D = k_new.shape
+    P, page_size = kc.shape[0], kc.shape[1]
+    bad = _load().oracle_kv_append_paged(_ptr(k_new), _ptr(v_new), _ptr(kc), _ptr(vc), P, page_size,
+                                         _ptr(bt), bt.shape[1], _ptr(ps_), B, Hkv, D)
+    return kc, vc, bad
+
+
+def kv_append_fp8(rows, kv_cache, inv_scale, slots):
+    """Return copies of (kv_cache u8 [NB,bs,HD], inv_scale u16 [NB*bs]) with rows [T,HD]
+    quantised into their slots."""
+    rows = _u16(rows)
+    cache = np.array(kv_cache, dtype=np.uint8, copy=True)
+    inv = np.array(np.asarray(inv_scale).reshape(-1), dtype=np.uint16, copy=True)
+    sl = np.ascontiguousarray(slots, dtype=np.int64)
+    T, HD = rows.shape
+    NB, bs, _ = cache.shape
+    bad = _load().oracle_kv_append_fp8(_ptr(rows), _ptr(cache), _ptr(inv), _ptr(sl), T, HD, NB, bs)
+    return cache, inv, bad

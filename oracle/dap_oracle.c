@@ -313,3 +313,90 @@ void oracle_fp8_swa(const uint16_t *q, const uint8_t *kv_cache, const uint16_t *
     oracle_fp8_swa_range(q, kv_cache, inv_scale, indices, lens, T, NH, HD, W, num_blocks,
                          block_size, scale, 0, T, out);
 }
+
+/* ---- KV append (the step before decode) -------------------------------------------- */
+
+/* Paged append: for each sequence b and kv head h, the new token's K and V rows go to
+ * logical position pos[b] of sequence b, i.e. page block_table[b][pos / ps], slot pos % ps
+ * (the same translation decode reads through).  Caches are [num_pages, ps, Hkv, D] bf16
+ * bits; k_new / v_new are [B, Hkv, D].  Returns the number of rows that could not be
+ * placed (position or page out of range); those are skipped. */
+int oracle_kv_append_paged(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_cache,
+                           uint16_t *v_cache, int num_pages, int page_size,
+                           const int32_t *block_table, int max_pages, const int32_t *pos, int B,
+                           int Hkv, int D) {
+    int b, h, d, bad = 0;
+    for (b = 0; b < B; ++b) {
+        long long p = pos[b];
+        int32_t page;
+        if (p < 0 || p >= (long long)max_pages * page_size) { bad += Hkv; continue; }
+        page = block_table[(long long)b * max_pages + p / page_size];
+        if (page < 0 || page >= num_pages) { bad += Hkv; continue; }
+        for (h = 0; h < Hkv; ++h) {
+            long long dst = (((long long)page * page_size + p % page_size) * Hkv + h) * D;
+            long long src = ((long long)b * Hkv + h) * D;
+            for (d = 0; d < D; ++d) {
+                k_cache[dst + d] = k_new[src + d];
+                v_cache[dst + d] = v_new[src + d];
+            }
+        }
+    }
+    return bad;
+}
+
+/* Round a binary32 value to the nearest OCP E4M3FN code, ties to even, saturating to
+ * +-448 (the largest finite code); NaN gives 0x7F.  Written from the format: a code is
+ * (-1)^s * 2^(e-7) * (1 + m/8) for e in 1..15 (except e = 15, m = 7), and
+ * (-1)^s * 2^-6 * (m/8) for e = 0. */
+uint8_t oracle_e4m3_from_float(float x) {
+    int code, best = 0, sign = 0;
+    double ax, bestdiff = INFINITY;
+    if (isnan(x)) return 0x7F;
+    if (signbit(x)) { sign = 1; x = -x; }
+    ax = (double)x;
+    if (ax >= 448.0) return (uint8_t)((sign << 7) | 0x7E);
+    /* the finite non-negative codes 0x00..0x7E are increasing in value: take the nearest,
+     * an exact tie going to the code with an even mantissa (even code) */
+    for (code = 0; code <= 0x7E; ++code) {
+        double v = oracle_e4m3_value((uint8_t)code);
+        double diff = fabs(v - ax);
+        if (diff < bestdiff || (diff == bestdiff && (code & 1) == 0)) {
+            bestdiff = diff;
+            best = code;
+        }
+    }
+    return (uint8_t)((sign << 7) | best);
+}
+
+/* fp8 append of latent rows (K = V): row t (HD bf16 values) goes to slot slots[t] of the
+ * [num_blocks, block_size, HD] e4m3 cache with its dequantisation factor in inv_scale[slot]
+ * (the decode side computes e4m3 * inv_scale).  In binary32, as the kernel does:
+ *   amax = max |x|;  s = amax / 448 (1 when amax is 0);  s is stored as bf16 (RNE);
+ *   code = e4m3_rne_satfinite(x / s_stored)  (an IEEE binary32 division).
+ * Returns the number of rows skipped because their slot is outside the cache. */
+int oracle_kv_append_fp8(const uint16_t *rows, uint8_t *kv_cache, uint16_t *inv_scale,
+                         const int64_t *slots, int T, int HD, int num_blocks, int block_size) {
+    int t, d, bad = 0;
+    long long max_slots = (long long)num_blocks * block_size;
+    for (t = 0; t < T; ++t) {
+        int64_t slot = slots[t];
+        float amax = 0.0f, s, sb;
+        uint32_t u;
+        uint16_t sbits;
+        if (slot < 0 || slot >= max_slots) { ++bad; continue; }
+        for (d = 0; d < HD; ++d) {
+            float x = (float)oracle_bf16_value(rows[(long long)t * HD + d]);
+            if (fabsf(x) > amax) amax = fabsf(x);
+        }
+        s = amax > 0.0f ? amax / 448.0f : 1.0f;
+        sb = (float)oracle_round_to_bf16((double)s);
+        memcpy(&u, &sb, sizeof u);
+        sbits = (uint16_t)(u >> 16);
+        inv_scale[slot] = sbits;
+        for (d = 0; d < HD; ++d) {
+            float x = (float)oracle_bf16_value(rows[(long long)t * HD + d]);
+            kv_cache[slot * HD + d] = oracle_e4m3_from_float(x / sb);
+        }
+    }
+    return bad;
+}

@@ -335,3 +335,85 @@ def test_fp8_with_unit_scales_is_mqa_decode():
     got = oracle.decode_contig(bits(case.q), bits(k), bits(k),
                                np.full(2, 8, dtype=np.int32), case.scale)
     np.testing.assert_allclose(out, got, rtol=1e-12, atol=1e-13)
+
+
+# ---- KV append (the step before decode) -----------------------------------------------
+
+def test_e4m3_from_float_matches_torch_in_range():
+    g = torch.Generator().manual_seed(51)
+    x = torch.cat([torch.randn(3000, generator=g) * s for s in (0.01, 1.0, 30.0, 200.0)])
+    x = x.clamp(-447.9, 447.9)
+    # exact ties between neighbouring codes: 1 + 1/16 (between 1 and 1.125), 3 * 2^-10
+    # (between the subnormals 2^-9 and 2 * 2^-9), 0.5 * (256 + 288)
+    ties = torch.tensor([1.0625, -1.0625, 3 * 2.0 ** -10, 272.0, 0.0, -0.0, 2.0 ** -12])
+    x = torch.cat([x, ties])
+    want = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_from_float(float(v)) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, want)
+
+
+def test_e4m3_from_float_roundtrips_every_code_and_saturates():
+    table = oracle.e4m3_table()
+    for code in range(256):
+        if np.isnan(table[code]):
+            continue
+        assert oracle.e4m3_from_float(float(table[code])) == code or table[code] == 0.0
+    assert oracle.e4m3_from_float(1e6) == 0x7E and oracle.e4m3_from_float(-1e6) == 0xFE
+    assert oracle.e4m3_from_float(449.0) == 0x7E
+
+
+def test_kv_append_paged_places_rows_where_decode_reads_them():
+    case = inputs.make_paged_case(3, 8, 2, 64, 16, [16, 5, 31], 52, poison=False)
+    g = torch.Generator().manual_seed(53)
+    k_new = inputs.randn_bf16((3, 2, 64), g, "cpu")
+    v_new = inputs.randn_bf16((3, 2, 64), g, "cpu")
+    pos = case.seq_lens.numpy().copy()            # append at the current end
+    kc, vc, bad = oracle.kv_append_paged(bits(k_new), bits(v_new), bits(case.k_cache), bits(case.v_cache),
+                                         case.block_table.numpy(), pos)
+    assert bad == 0
+    grown = inputs.PagedCase(case.q, torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16),
+                             torch.from_numpy(vc.view(np.int16)).view(torch.bfloat16), case.block_table,
+                             case.seq_lens + 1, case.page_size, case.scale)
+    ks, vs = gather_logical(grown)
+    for b in range(3):
+        assert np.array_equal(ks[b][-1], as_f64(k_new[b].float()))
+        assert np.array_equal(vs[b][-1], as_f64(v_new[b].float()))
+        assert np.array_equal(ks[b][:-1], gather_logical(case)[0][b])   # nothing else moved
+    # a position beyond the table is refused, not written
+    _, _, bad = oracle.kv_append_paged(bits(k_new), bits(v_new), bits(case.k_cache), bits(case.v_cache),
+                                       case.block_table.numpy(), np.array([0, 10 ** 6, 1], np.int32))
+    assert bad == 2
+
+
+def test_kv_append_fp8_matches_torch_quantisation_and_error_bound():
+    g = torch.Generator().manual_seed(54)
+    T, HD, NB, bs = 6, 512, 2, 16
+    rows = inputs.randn_bf16((T, HD), g, "cpu") * torch.tensor([1.0, 0.001, 50.0, 1.0, 3.0, 0.0])[:, None]
+    rows = rows.to(torch.bfloat16)
+    cache = torch.zeros((NB, bs, HD), dtype=torch.uint8)
+    inv = torch.zeros(NB * bs, dtype=torch.bfloat16)
+    slots = np.array([3, 17, 0, 31, 8, 9], dtype=np.int64)
+    c2, i2, bad = oracle.kv_append_fp8(bits(rows), cache.numpy(), bits(inv), slots)
+    assert bad == 0
+    flat = c2.reshape(-1, HD)
+    for t in range(T):
+        x = rows[t].float()
+        amax = float(x.abs().max())
+        s_bits = i2[slots[t]]
+        s = float(torch.tensor(int(s_bits), dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float())
+        want_s = torch.tensor([amax / 448.0 if amax > 0 else 1.0], dtype=torch.float32).to(torch.bfloat16)
+        assert s == float(want_s.float())
+        y = x / torch.tensor(s, dtype=torch.float32)
+        codes = torch.from_numpy(flat[slots[t]].copy())
+        inrange = y.abs() <= 448.0
+        want = y[inrange].to(torch.float8_e4m3fn).view(torch.uint8)
+        assert torch.equal(codes[inrange], want)
+        assert torch.all(codes[~inrange] & 0x7F == 0x7E)           # saturated to +-448
+        deq = codes.view(torch.float8_e4m3fn).float() * s
+        err = (deq - x).abs()
+        assert torch.all(err <= x.abs() * 2.0 ** -4 + s * 2.0 ** -10 + 1e-30)
+    # untouched slots stay zero
+    used = set(slots.tolist())
+    for sl in range(NB * bs):
+        if sl not in used:
+            assert not flat[sl].any() and i2[sl] == 0
