@@ -174,6 +174,38 @@ dap_status decode_attn_paged_fp8(const void *q, const uint8_t *kv_cache, const v
                                  void *out, void *stream);
 
 /*
+ * Append the new decode token's K and V to a paged cache (the step before decode).
+ *   For every sequence b and kv head h: k_new[b, h, :] and v_new[b, h, :] are written to
+ *   logical position positions[b] of sequence b, i.e. page block_table[b, positions[b] /
+ *   page_size], slot positions[b] % page_size of the [num_pages, page_size, Hkv, D] caches
+ *   (the translation decode_attn_paged reads through; [A: ContigKV / PagedKV]).
+ *   k_new, v_new  device bf16 [B, Hkv, D] contiguous.
+ *   positions     device int32 [B] (normally the sequence length before the append).
+ *   Supported: D a multiple of 8; pointers 16-byte aligned.  A position outside
+ *   [0, max_pages * page_size) or a page outside the pool skips that sequence and sets
+ *   DAP_DEVERR_SEQLEN / DAP_DEVERR_PAGE.
+ */
+dap_status kv_append_paged(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                           int num_pages, int page_size, const int32_t *block_table,
+                           int max_pages, const int32_t *positions, int B, int Hkv, int D,
+                           void *stream);
+
+/*
+ * Quantise latent rows (K = V) into the fp8 cache that decode_attn_paged_fp8 reads [C].
+ *   Row t (HD bf16 values) goes to slot slots[t] of kv_cache [num_blocks, block_size, HD]
+ *   with its dequantisation factor in inv_scale[slot], so that the decode side's
+ *   e4m3(code) * inv_scale restores it.  In binary32: amax = max |x|; s = amax / 448 (1 for
+ *   an all-zero row), stored as bf16; code = e4m3(x / s_stored), round to nearest even,
+ *   saturating at +-448 (the quantiser multiplies by the multiplier 1/s and keeps amax in
+ *   the input domain, as the AstrAI doc's FP8 section describes).
+ *   rows       device bf16 [T, HD] contiguous.   slots  device int64 [T].
+ *   Supported: HD in {256, 512}.  A slot outside the cache is skipped (DAP_DEVERR_SLOT).
+ */
+dap_status kv_append_fp8(const void *rows, uint8_t *kv_cache, void *inv_scale,
+                         const int64_t *slots, int T, int HD, int num_blocks, int block_size,
+                         void *stream);
+
+/*
  * Paged GQA decode that allocates nothing and takes no workspace.  The web pages this
  * library follows have no counterpart to it; it exists for callers that cannot hand the
  * library scratch memory: hosts that reserve their whole device-memory budget up front and

@@ -28,8 +28,8 @@ DEVERR_TIMEOUT, DEVERR_SEQLEN, DEVERR_PAGE, DEVERR_SLOT = 0x1, 0x2, 0x4, 0x8
 # every symbol include/dap.h declares
 EXPORTS = ("dap_status_string", "dap_version", "dap_device_sm_count", "dap_plan_splits",
            "dap_chunk_tokens", "dap_workspace_bytes", "decode_attn_paged", "decode_attn_contig",
-           "decode_attn_paged_fp8", "decode_attn_paged_noalloc", "dap_set_trace_events",
-           "dap_get_device_errors")
+           "decode_attn_paged_fp8", "decode_attn_paged_noalloc", "kv_append_paged", "kv_append_fp8",
+           "dap_set_trace_events", "dap_get_device_errors")
 
 
 class DapError(RuntimeError):
@@ -82,6 +82,10 @@ def load(build_if_missing: bool = True):
         lib.decode_attn_paged_noalloc.argtypes = [P, LL, LL, P, P, I, I, P, I, P, I, I, I, I, I, F, I,
                                                   P, LL, LL, P]
         lib.decode_attn_paged_noalloc.restype = I
+        lib.kv_append_paged.argtypes = [P, P, P, P, I, I, P, I, P, I, I, I, P]
+        lib.kv_append_paged.restype = I
+        lib.kv_append_fp8.argtypes = [P, P, P, P, I, I, I, I, P]
+        lib.kv_append_fp8.restype = I
         lib.dap_set_trace_events.argtypes = [P, P, P]
         lib.dap_set_trace_events.restype = None
         lib.dap_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
@@ -269,3 +273,43 @@ def decode_attn_paged_fp8(q, kv_cache, inv_scale, slot_idx, lens, *, scale: floa
                                       _stream(stream))
     _check(st, "decode_attn_paged_fp8")
     return out
+
+
+# ---- cache writes ------------------------------------------------------------------------
+
+def kv_append_paged(k_new, v_new, k_cache, v_cache, block_table, positions, *, stream=None):
+    """Write each sequence's new K/V rows [B, Hkv, D] at positions[b] (include/dap.h:
+    kv_append_paged).  Returns (k_cache, v_cache), updated in place."""
+    _need(k_new.dtype == torch.bfloat16 and k_new.dim() == 3 and k_new.is_contiguous()
+          and v_new.shape == k_new.shape and v_new.dtype == torch.bfloat16 and v_new.is_contiguous(),
+          "k_new/v_new must be contiguous bf16 [B, Hkv, D]")
+    B, Hkv, D = k_new.shape
+    _need(k_cache.dtype == torch.bfloat16 and k_cache.dim() == 4 and k_cache.is_contiguous()
+          and v_cache.shape == k_cache.shape and v_cache.is_contiguous() and k_cache.shape[2:] == (Hkv, D),
+          "caches must be contiguous bf16 [P, ps, Hkv, D]")
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
+          and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
+    _need(positions.dtype == torch.int32 and positions.numel() == B and positions.is_contiguous(),
+          "positions must be contiguous int32 [B]")
+    st = load().kv_append_paged(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                k_cache.shape[1], _ptr(block_table), block_table.shape[1], _ptr(positions), B, Hkv,
+                                D, _stream(stream))
+    _check(st, "kv_append_paged")
+    return k_cache, v_cache
+
+
+def kv_append_fp8(rows, kv_cache, inv_scale, slots, *, stream=None):
+    """Quantise rows [T, HD] into their fp8 cache slots (include/dap.h: kv_append_fp8).
+    Returns (kv_cache, inv_scale), updated in place."""
+    _need(rows.dtype == torch.bfloat16 and rows.dim() == 2 and rows.is_contiguous(), "rows must be bf16 [T, HD]")
+    T, HD = rows.shape
+    _need(kv_cache.dtype == torch.uint8 and kv_cache.dim() == 3 and kv_cache.is_contiguous()
+          and kv_cache.shape[2] == HD, "kv_cache must be contiguous uint8 [num_blocks, block_size, HD]")
+    NB, bs, _ = kv_cache.shape
+    _need(inv_scale.dtype == torch.bfloat16 and inv_scale.is_contiguous() and inv_scale.numel() >= NB * bs,
+          "inv_scale must be contiguous bf16 with one entry per slot")
+    _need(slots.dtype == torch.int64 and slots.numel() == T and slots.is_contiguous(), "slots must be int64 [T]")
+    st = load().kv_append_fp8(_ptr(rows), _ptr(kv_cache), _ptr(inv_scale), _ptr(slots), T, HD, NB, bs,
+                              _stream(stream))
+    _check(st, "kv_append_fp8")
+    return kv_cache, inv_scale

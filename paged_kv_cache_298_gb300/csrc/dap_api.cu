@@ -274,6 +274,34 @@ dap_status decode_attn_paged_fp8(const void *q, const uint8_t *kv_cache, const v
     return launch_fp8(a, static_cast<cudaStream_t>(stream));
 }
 
+dap_status kv_append_paged(const void *k_new, const void *v_new, void *k_cache, void *v_cache, int num_pages,
+                           int page_size, const int32_t *block_table, int max_pages, const int32_t *positions, int B,
+                           int Hkv, int D, void *stream) {
+    if (B < 0 || Hkv < 1 || D < 1 || num_pages < 1 || page_size < 1 || max_pages < 1) return DAP_ERR_SHAPE;
+    if (B == 0) return DAP_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !positions) return DAP_ERR_NULL;
+    if (D % 8 != 0) return DAP_ERR_UNSUPPORTED;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned4(block_table) || !aligned4(positions))
+        return DAP_ERR_ALIGN;
+    return launch_append_paged(k_new, v_new, k_cache, v_cache, num_pages, page_size, block_table, max_pages,
+                               positions, B, Hkv, D, static_cast<cudaStream_t>(stream));
+}
+
+dap_status kv_append_fp8(const void *rows, uint8_t *kv_cache, void *inv_scale, const int64_t *slots, int T, int HD,
+                         int num_blocks, int block_size, void *stream) {
+    if (T < 0 || HD < 1 || num_blocks < 1 || block_size < 1 || (long long)num_blocks * block_size > 0x7FFFFFFFLL)
+        return DAP_ERR_SHAPE;
+    if (T == 0) return DAP_OK;
+    if (!rows || !kv_cache || !inv_scale || !slots) return DAP_ERR_NULL;
+    if (HD != 256 && HD != 512) return DAP_ERR_UNSUPPORTED;
+    if (!aligned16(rows) || !aligned16(kv_cache) || (reinterpret_cast<uintptr_t>(inv_scale) & 1u) ||
+        (reinterpret_cast<uintptr_t>(slots) & 7u))
+        return DAP_ERR_ALIGN;
+    return launch_append_fp8(rows, kv_cache, inv_scale, slots, T, HD, num_blocks, block_size,
+                             static_cast<cudaStream_t>(stream));
+}
+
 void dap_set_trace_events(void *split_begin, void *split_end, void *combine_end) {
     g_trace.split_begin = static_cast<cudaEvent_t>(split_begin);
     g_trace.split_end = static_cast<cudaEvent_t>(split_end);
@@ -286,6 +314,7 @@ dap_status dap_get_device_errors(unsigned int *flags, int clear) {
     if (cudaDeviceSynchronize() != cudaSuccess) return DAP_ERR_CUDA;
     if (!read_errors_decode(flags, clear != 0)) return DAP_ERR_CUDA;
     if (!read_errors_fp8(flags, clear != 0)) return DAP_ERR_CUDA;
+    if (!read_errors_append(flags, clear != 0)) return DAP_ERR_CUDA;
     return DAP_OK;
 }
 

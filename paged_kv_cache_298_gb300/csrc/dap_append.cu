@@ -1,0 +1,143 @@
+// dap_append.cu -- writing the new decode token into the caches (the step before decode).
+//
+// Paged append: each sequence's new K and V rows (one per kv head) go to its logical
+// position through the block table, the same translation the decode kernels read through
+// (AstrAI "CUDA Kernels" doc, "Q Scheduling and KV Addressing": a KV policy translates a
+// logical position into a physical address).
+//
+// fp8 append: a latent row (K = V) is quantised to OCP e4m3 with one scale per slot; the
+// decode side dequantises as code * inv_scale (nvfp4-megamoe-kernel native_swa_decode.py,
+// _fallback_batched_sdp).  Per slot, in binary32: amax = max |x|, s = amax / 448 (1 for an
+// all-zero row), stored as bf16; code = e4m3(x / s_stored), round to nearest even,
+// saturating at +-448 (AstrAI doc, FP8 section: quantize multiplies by the quantisation
+// multiplier, amax is kept in the input domain).
+//
+// One warp per row; every access is 16 bytes and coalesced.  Out-of-range positions, pages
+// and slots are skipped and flagged in the device error word.
+#include <cuda_fp8.h>
+
+#include "dap_device.cuh"
+#include "dap_internal.h"
+
+namespace dap {
+
+namespace {
+
+__global__ void __launch_bounds__(256)
+    append_paged_kernel(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new, __nv_bfloat16 *k_cache,
+                        __nv_bfloat16 *v_cache, int num_pages, int page_size, const int32_t *block_table,
+                        int max_pages, const int32_t *pos, int B, int Hkv, int D) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);  // (b, h)
+    const int lane = threadIdx.x & 31;
+    if (row >= B * Hkv) return;
+    const int b = row / Hkv, h = row - b * Hkv;
+    const long long p = pos[b];
+    if (p < 0 || p >= (long long)max_pages * page_size) {
+        if (lane == 0 && h == 0) flag_error(DAP_DEVERR_SEQLEN);
+        return;
+    }
+    const int page = block_table[(long long)b * max_pages + p / page_size];
+    if (page < 0 || page >= num_pages) {
+        if (lane == 0 && h == 0) flag_error(DAP_DEVERR_PAGE);
+        return;
+    }
+    const long long dst = (((long long)page * page_size + p % page_size) * Hkv + h) * D;
+    const long long src = (long long)row * D;
+    for (int c = lane; c < D / 8; c += 32) {
+        reinterpret_cast<uint4 *>(k_cache + dst)[c] = reinterpret_cast<const uint4 *>(k_new + src)[c];
+        reinterpret_cast<uint4 *>(v_cache + dst)[c] = reinterpret_cast<const uint4 *>(v_new + src)[c];
+    }
+}
+
+// HD / 256 groups of 8 values per lane (HD a multiple of 256).
+template <int HD>
+__global__ void __launch_bounds__(256)
+    append_fp8_kernel(const __nv_bfloat16 *rows, uint8_t *kv_cache, __nv_bfloat16 *inv_scale, const int64_t *slots,
+                      int T, long long max_slots) {
+    constexpr int NG = HD / 256;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const int64_t slot = slots[t];
+    if (slot < 0 || slot >= max_slots) {
+        if (lane == 0) flag_error(DAP_DEVERR_SLOT);
+        return;
+    }
+    float x[NG][8];
+    float amax = 0.f;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        const uint4 w = reinterpret_cast<const uint4 *>(rows + (long long)t * HD)[g * 32 + lane];
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = bf16x2_to_float2(ws[j]);
+            x[g][2 * j] = f.x;
+            x[g][2 * j + 1] = f.y;
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    const __nv_bfloat16 sb16 = __float2bfloat16_rn(s);
+    const float sb = __bfloat162float(sb16);
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        uint32_t packed[2];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float2 y = make_float2(__fdiv_rn(x[g][4 * half + 2 * j], sb),
+                                             __fdiv_rn(x[g][4 * half + 2 * j + 1], sb));
+                const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+                word |= (uint32_t)c << (16 * j);
+            }
+            packed[half] = word;
+        }
+        reinterpret_cast<uint2 *>(kv_cache + slot * HD)[g * 32 + lane] = make_uint2(packed[0], packed[1]);
+    }
+    if (lane == 0) inv_scale[slot] = sb16;
+}
+
+}  // namespace
+
+dap_status launch_append_paged(const void *k_new, const void *v_new, void *k_cache, void *v_cache, int num_pages,
+                               int page_size, const int32_t *block_table, int max_pages, const int32_t *pos, int B,
+                               int Hkv, int D, cudaStream_t stream) {
+    const int rows = B * Hkv;
+    append_paged_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(k_new), static_cast<const __nv_bfloat16 *>(v_new),
+        static_cast<__nv_bfloat16 *>(k_cache), static_cast<__nv_bfloat16 *>(v_cache), num_pages, page_size,
+        block_table, max_pages, pos, B, Hkv, D);
+    return cudaGetLastError() == cudaSuccess ? DAP_OK : DAP_ERR_CUDA;
+}
+
+dap_status launch_append_fp8(const void *rows, uint8_t *kv_cache, void *inv_scale, const int64_t *slots, int T,
+                             int HD, int num_blocks, int block_size, cudaStream_t stream) {
+    const long long max_slots = (long long)num_blocks * block_size;
+    const dim3 grid((unsigned)((T + 7) / 8));
+    const __nv_bfloat16 *r = static_cast<const __nv_bfloat16 *>(rows);
+    __nv_bfloat16 *inv = static_cast<__nv_bfloat16 *>(inv_scale);
+    switch (HD) {
+        case 256: append_fp8_kernel<256><<<grid, 256, 0, stream>>>(r, kv_cache, inv, slots, T, max_slots); break;
+        case 512: append_fp8_kernel<512><<<grid, 256, 0, stream>>>(r, kv_cache, inv, slots, T, max_slots); break;
+        default: return DAP_ERR_UNSUPPORTED;
+    }
+    return cudaGetLastError() == cudaSuccess ? DAP_OK : DAP_ERR_CUDA;
+}
+
+bool read_errors_append(unsigned int *flags, bool clear) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_errors, sizeof v) != cudaSuccess) return false;
+    if (clear) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(g_device_errors, &z, sizeof z) != cudaSuccess) return false;
+    }
+    *flags |= v;
+    return true;
+}
+
+}  // namespace dap

@@ -82,6 +82,13 @@ struct Fp8Args {
 
 dap_status launch_fp8(const Fp8Args &a, cudaStream_t stream);
 
+dap_status launch_append_paged(const void *k_new, const void *v_new, void *k_cache, void *v_cache, int num_pages,
+                               int page_size, const int32_t *block_table, int max_pages, const int32_t *pos, int B,
+                               int Hkv, int D, cudaStream_t stream);
+dap_status launch_append_fp8(const void *rows, uint8_t *kv_cache, void *inv_scale, const int64_t *slots, int T,
+                             int HD, int num_blocks, int block_size, cudaStream_t stream);
+bool read_errors_append(unsigned int *flags, bool clear);
+
 // Host readers of each translation unit's device error word (cudaMemcpyFromSymbol on the
 // current device); `clear` resets it.  Return false when the copy fails.
 bool read_errors_decode(unsigned int *flags, bool clear);

@@ -129,3 +129,16 @@ def test_fp8_validation(lib):
     assert call(HD=256) == 3 and call(NH=64) == 3 and call(W=129) == 3
     assert call(T=0) == 0
     assert f(None, FAKE, FAKE, FAKE, FAKE, 4, 128, 512, 128, 64, 256, 0.04, FAKE, None) == 1
+
+
+def test_append_validation(lib):
+    f = lib.kv_append_paged
+    assert f(FAKE, FAKE, FAKE, FAKE, 8, 16, FAKE, 4, FAKE, -1, 2, 64, None) == 2
+    assert f(FAKE, FAKE, FAKE, FAKE, 8, 16, FAKE, 4, FAKE, 2, 2, 60, None) == 3
+    assert f(None, FAKE, FAKE, FAKE, 8, 16, FAKE, 4, FAKE, 2, 2, 64, None) == 1
+    assert f(None, None, None, None, 8, 16, None, 4, None, 0, 2, 64, None) == 0
+    assert f(ctypes.c_void_p((1 << 20) + 2), FAKE, FAKE, FAKE, 8, 16, FAKE, 4, FAKE, 2, 2, 64, None) == 5
+    g = lib.kv_append_fp8
+    assert g(FAKE, FAKE, FAKE, FAKE, 4, 384, 2, 16, None) == 3
+    assert g(FAKE, FAKE, FAKE, FAKE, -1, 512, 2, 16, None) == 2
+    assert g(FAKE, None, FAKE, FAKE, 4, 512, 2, 16, None) == 1
