@@ -478,6 +478,72 @@ def run_fp8(args):
         dist.destroy_process_group()
 
 
+# ---- cache appends (the step before decode) ----------------------------------------------
+
+def run_append(args):
+    """Times the two append kernels on the decode step of the ragged batch (one new token
+    per sequence: B=128 x Hkv=8 rows of D=128) and of the fp8 workload (T=64 latent rows of
+    HD=512).  Bytes: new rows read + cache rows written + the indices they go through."""
+    from paged_kv_cache_298_gb300 import binding, inputs
+    dev = torch.device("cuda", 0)
+    binding.load()
+    case = inputs.ragged_paged(device=dev)
+    g = torch.Generator(device=dev).manual_seed(298010)
+    k_new = inputs.randn_bf16((case.B, case.Hkv, case.D), g, dev)
+    v_new = inputs.randn_bf16((case.B, case.Hkv, case.D), g, dev)
+    pos = case.seq_lens.clone()   # one past the end; every table has room (2x pool, full pages)
+    pos = torch.minimum(pos, torch.tensor(case.max_pages * case.page_size - 1, device=dev, dtype=torch.int32))
+    f = inputs.fp8_swa(device=dev)
+    rows = inputs.randn_bf16((f.T, f.HD), g, dev)
+    slots = torch.randperm(f.num_blocks * f.block_size, generator=torch.Generator().manual_seed(298011))[:f.T]
+    slots = slots.to(torch.int64).to(dev)
+    K, W = args.steps, args.warmup
+
+    def timed(fn):
+        """Device time per call: the calls are captured in a CUDA graph of 50 and replayed, so
+        the Python binding's host cost (about 10 us a call) does not starve the GPU."""
+        for _ in range(W):
+            fn()
+        torch.cuda.synchronize()
+        graph, per = torch.cuda.CUDAGraph(), 50
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                for _ in range(per):
+                    fn()
+        torch.cuda.current_stream().wait_stream(s)
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = max(1, K // per)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (reps * per)
+
+    ms_paged = timed(lambda: binding.kv_append_paged(k_new, v_new, case.k_cache, case.v_cache, case.block_table, pos))
+    ms_fp8 = timed(lambda: binding.kv_append_fp8(rows, f.kv_cache, f.inv_scale, slots))
+    b_paged = 2 * 2 * k_new.numel() * 2 + case.B * 4 * 2
+    b_fp8 = rows.numel() * 2 + rows.numel() + f.T * (2 + 8)
+    hbm_peak, peak_src = peaks()
+    print(json.dumps({
+        "metric": "paged KV append achieved HBM GB/s (algorithmic bytes)",
+        "value": round(b_paged / (ms_paged * 1e-3) / 1e9, 1), "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W,
+        "ms_per_step": round(ms_paged, 5), "us_per_call": round(ms_paged * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "append one decode token: ragged B=128 Hkv=8 D=128 page 16; fp8 T=64 HD=512",
+                   "bytes_per_call": b_paged},
+        "fp8_append": {"us_per_call": round(ms_fp8 * 1e3, 2), "bytes_per_call": b_fp8,
+                       "GB/s": round(b_fp8 / (ms_fp8 * 1e-3) / 1e9, 1)},
+        "roofline": {"bound": "latency", "peak": hbm_peak, "peak_source": f"{peak_src} hbm_gbs",
+                     "note": "a 1 MB / 0.1 MB problem: launch and memory latency, not HBM bandwidth, set the time"},
+        "timing": "CUDA graph of 50 calls, replayed",
+        "gpu_launches": 2 * 50 * max(1, K // 50), "device_errors": binding.get_device_errors()}), flush=True)
+
+
 # ---- reference arm: the fp64 oracle on the host cores ----------------------------------
 
 def run_reference_fp8(args):
@@ -543,7 +609,7 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="ragged", choices=["ragged", "llama", "long1", "long4", "fp8"])
+    ap.add_argument("--workload", default="ragged", choices=["ragged", "llama", "long1", "long4", "fp8", "append"])
     ap.add_argument("--splits", type=int, default=-1,
                     help="-1 = the planner's choice, 0 = balanced schedule, S > 0 = per-sequence splits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -554,6 +620,8 @@ def main():
         run_reference(args)
     elif args.workload == "fp8":
         run_fp8(args)
+    elif args.workload == "append":
+        run_append(args)
     else:
         run_ours(args)
 
