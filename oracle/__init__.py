@@ -79,6 +79,10 @@ def _load():
         lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
         lib.oracle_kv_append_fp8.argtypes = [P, P, P, P, I, I, I, I]
         lib.oracle_kv_append_fp8.restype = I
+        lib.oracle_decode_paged_multi.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, D, P]
+        lib.oracle_decode_paged_multi.restype = I
+        lib.oracle_q_tile_map.argtypes = [P, I, I, P, P, P, I]
+        lib.oracle_q_tile_map.restype = I
         _lib = lib
         return lib
 
@@ -224,3 +228,34 @@ def kv_append_fp8(rows, kv_cache, inv_scale, slots):
     NB, bs, _ = cache.shape
     bad = _load().oracle_kv_append_fp8(_ptr(rows), _ptr(cache), _ptr(inv), _ptr(sl), T, HD, NB, bs)
     return cache, inv, bad
+
+
+def decode_paged_multi(q, k_cache, v_cache, block_table, seq_lens, qo_indptr, scale: float) -> np.ndarray:
+    """Multi-token decode: q packed [total_q, Hq, D] u16, qo_indptr [B+1]; token i of
+    sequence b attends keys up to position seq_lens[b] - q_len_b + i.  Returns float64
+    [total_q, Hq, D]."""
+    q = _u16(q); k_cache = _u16(k_cache); v_cache = _u16(v_cache)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qi = np.ascontiguousarray(qo_indptr, dtype=np.int32)
+    total, Hq, D = q.shape
+    P, ps, Hkv, _ = k_cache.shape
+    B = sl.shape[0]
+    out = np.empty((total, Hq, D), dtype=np.float64)
+    bad = _load().oracle_decode_paged_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), P, _ptr(bt), bt.shape[1],
+                                            _ptr(sl), _ptr(qi), B, Hq, Hkv, D, ps, float(scale), _ptr(out))
+    if bad:
+        raise ValueError(f"{bad} output rows would read outside the given cache/table")
+    return out
+
+
+def q_tile_map(q_lens, tokens_per_tile: int):
+    """(qo_indptr, tile_batch, tile_index) of the packed-Q work map."""
+    ql = np.ascontiguousarray(q_lens, dtype=np.int32)
+    B = ql.shape[0]
+    cap = int(sum((int(x) + tokens_per_tile - 1) // tokens_per_tile for x in ql)) + 1
+    qi = np.zeros(B + 1, np.int32)
+    tb = np.zeros(cap, np.int32)
+    ti = np.zeros(cap, np.int32)
+    n = _load().oracle_q_tile_map(_ptr(ql), B, int(tokens_per_tile), _ptr(qi), _ptr(tb), _ptr(ti), cap)
+    return qi, tb[:n], ti[:n]

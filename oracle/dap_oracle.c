@@ -400,3 +400,56 @@ int oracle_kv_append_fp8(const uint16_t *rows, uint8_t *kv_cache, uint16_t *inv_
     }
     return bad;
 }
+
+/* ---- multi-token decode ---------------------------------------------------------------- */
+
+/* Several new tokens per sequence (already in the cache): sequence b has q_len_b =
+ * qo_indptr[b+1] - qo_indptr[b] new tokens at positions seq_lens[b] - q_len_b + i, and
+ * token i attends the keys t <= its own position (causal among the new tokens).  q and out
+ * are packed [total_q, Hq, D] (token r = qo_indptr[b] + i).  Everything else as
+ * oracle_decode_paged.  Returns the number of rows that failed the bounds checks. */
+int oracle_decode_paged_multi(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                              int num_pages, const int32_t *block_table, int max_pages,
+                              const int32_t *seq_lens, const int32_t *qo_indptr, int B, int Hq,
+                              int Hkv, int D, int page_size, double scale, double *out) {
+    int bad = 0, b;
+    for (b = 0; b < B; ++b) {
+        int q0 = qo_indptr[b], qlen = qo_indptr[b + 1] - qo_indptr[b], L = seq_lens[b], i;
+        for (i = 0; i < qlen; ++i) {
+            int upto = L - qlen + i + 1; /* keys 0 .. position of token i */
+            int32_t one = upto < 0 ? 0 : upto, h, d;
+            for (h = 0; h < Hq; ++h) {
+                double *o = out + ((long long)(q0 + i) * Hq + h) * D;
+                /* reuse the single-token row with the sequence cut at this token */
+                if (paged_row(q + (long long)(q0 + i) * Hq * D, 0, D, k_cache,
+                              v_cache, num_pages, block_table + (long long)b * max_pages, max_pages,
+                              &one, Hq, Hkv, D, page_size, scale, 0, h, o) != 0) {
+                    for (d = 0; d < D; ++d) o[d] = NAN;
+                    ++bad;
+                }
+            }
+        }
+    }
+    return bad;
+}
+
+/* The packed-Q work map (AstrAI "CUDA Kernels" doc, "Q Scheduling and KV Addressing"):
+ * qo_indptr is the prefix sum of the q lengths; every sequence's tokens are cut into tiles
+ * of `tokens_per_tile`, and tile w covers tile index tile_index[w] of sequence
+ * tile_batch[w].  Returns the number of tiles, or -1 when max_tiles is too small. */
+int oracle_q_tile_map(const int32_t *q_lens, int B, int tokens_per_tile, int32_t *qo_indptr,
+                      int32_t *tile_batch, int32_t *tile_index, int max_tiles) {
+    int b, n = 0, j;
+    qo_indptr[0] = 0;
+    for (b = 0; b < B; ++b) {
+        int tiles = (q_lens[b] + tokens_per_tile - 1) / tokens_per_tile;
+        qo_indptr[b + 1] = qo_indptr[b] + q_lens[b];
+        for (j = 0; j < tiles; ++j) {
+            if (n >= max_tiles) return -1;
+            tile_batch[n] = b;
+            tile_index[n] = j;
+            ++n;
+        }
+    }
+    return n;
+}

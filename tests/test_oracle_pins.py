@@ -417,3 +417,47 @@ def test_kv_append_fp8_matches_torch_quantisation_and_error_bound():
     for sl in range(NB * bs):
         if sl not in used:
             assert not flat[sl].any() and i2[sl] == 0
+
+
+# ---- multi-token decode ----------------------------------------------------------------
+
+def test_q_tile_map_matches_the_pages_worked_example():
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "q_tile_map_astrai.json")))
+    qi, tb, ti = oracle.q_tile_map(g["q_lens"], g["tokens_per_tile"])
+    assert qi.tolist() == g["qo_indptr"]
+    assert tb.tolist() == g["q_tile_to_batch"]
+    assert ti.tolist() == g["q_tile_to_index"]
+
+
+def multi_case(lens, qlens, seed, Hq=8, Hkv=2, D=64, ps=16):
+    case = inputs.make_paged_case(len(lens), Hq, Hkv, D, ps, lens, seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    q = inputs.randn_bf16((sum(qlens), Hq, D), g, "cpu")
+    qi = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    return case, q, qi
+
+
+def test_multi_token_with_one_token_each_is_single_token_decode():
+    case, _, qi = multi_case([37, 100, 5], [1, 1, 1], 70)
+    got = oracle.decode_paged_multi(bits(case.q), bits(case.k_cache), bits(case.v_cache), case.block_table.numpy(),
+                                    case.seq_lens.numpy(), qi, case.scale)
+    assert np.array_equal(got, run_oracle(case))
+
+
+def test_multi_token_matches_causal_sdpa_float64():
+    lens, qlens = [37, 100, 5, 64], [3, 4, 5, 1]
+    case, q, qi = multi_case(lens, qlens, 71)
+    got = oracle.decode_paged_multi(bits(q), bits(case.k_cache), bits(case.v_cache), case.block_table.numpy(),
+                                    case.seq_lens.numpy(), qi, case.scale)
+    ks, vs = gather_logical(case)
+    qd = as_f64(q.float())
+    for b, (L, n) in enumerate(zip(lens, qlens)):
+        kb = torch.from_numpy(ks[b]).permute(1, 0, 2)[None]     # [1, Hkv, L, D]
+        vb = torch.from_numpy(vs[b]).permute(1, 0, 2)[None]
+        qb = torch.from_numpy(qd[qi[b]:qi[b + 1]]).permute(1, 0, 2)[None]   # [1, Hq, n, D]
+        pos = torch.arange(L - n, L)[:, None]
+        mask = torch.arange(L)[None, :] <= pos                   # [n, L]: token i sees keys <= its position
+        o = F.scaled_dot_product_attention(qb, kb, vb, attn_mask=mask, scale=case.scale, enable_gqa=True)
+        np.testing.assert_allclose(got[qi[b]:qi[b + 1]], o[0].permute(1, 0, 2).numpy(), rtol=1e-11, atol=1e-12)
