@@ -544,6 +544,203 @@ def run_append(args):
         "gpu_launches": 2 * 50 * max(1, K // 50), "device_errors": binding.get_device_errors()}), flush=True)
 
 
+# ---- multi-token decode (speculative verification) ----------------------------------------
+
+def multi_algorithmic(case, rows=None) -> int:
+    """K/V rows each sequence's last new token attends (every tile of a sequence reads a
+    prefix of them; with one tile per (sequence, kv head) each row is read once) + q + out +
+    block-table entries + seq_lens + the work map.  `rows`: restrict to these sequences."""
+    kv = case.kv
+    lens = kv.seq_lens.cpu().to(torch.int64)
+    ql = torch.as_tensor(case.q_lens, dtype=torch.int64)
+    if rows is not None:
+        lens, ql = lens[rows], ql[rows]
+    B = lens.numel()
+    nkv = int(lens.sum()) * kv.Hkv * kv.D * 2 * 2
+    qo = 2 * int(ql.sum()) * kv.Hq * kv.D * 2
+    pages = int(((lens + kv.page_size - 1) // kv.page_size).sum()) * 4
+    return nkv + qo + pages + B * 4 + (B + 1) * 4 + 2 * 4 * B
+
+
+class MultiOracle:
+    def __init__(self, case):
+        import oracle
+        self.oracle = oracle
+        self.case = case
+        kv = case.kv
+        self.q = bits(case.q)
+        self.k = bits(kv.k_cache)
+        self.v = bits(kv.v_cache)
+        self.table = kv.block_table.cpu().numpy()
+        self.lens = kv.seq_lens.cpu().numpy()
+        self.qi = np.concatenate([[0], np.cumsum(case.q_lens)]).astype(np.int64)
+
+    def run(self, seqs):
+        qrows = np.concatenate([np.arange(self.qi[b], self.qi[b + 1]) for b in seqs])
+        qi = np.concatenate([[0], np.cumsum([self.case.q_lens[b] for b in seqs])]).astype(np.int32)
+        t0 = time.perf_counter()
+        self.oracle.decode_paged_multi(np.ascontiguousarray(self.q[qrows]), self.k, self.v,
+                                       np.ascontiguousarray(self.table[seqs]), np.ascontiguousarray(self.lens[seqs]),
+                                       qi, self.case.kv.scale)
+        return time.perf_counter() - t0
+
+    def sample(self, target_s):
+        dt = self.run(np.arange(1))
+        return np.arange(int(max(1, min(len(self.case.q_lens), target_s / max(dt, 1e-4)))))
+
+
+def run_multi(args):
+    from paged_kv_cache_298_gb300 import binding, inputs
+    dev = torch.device("cuda", 0)
+    binding.load()
+    case = inputs.spec_verify_paged(device=dev)
+    kv = case.kv
+    hbm_peak, peak_src = peaks()
+    plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, dev)
+    sms = binding.device_sm_count()
+    S = args.splits if args.splits > 0 else binding.plan_splits(sms, plan.num_tiles, kv.Hq, kv.Hkv, kv.D,
+                                                                kv.page_size, kv.max_kv_len, 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    footprint = sum(t.numel() * t.element_size() for t in (case.q, kv.k_cache, kv.v_cache, kv.block_table,
+                                                           kv.seq_lens))
+    copies = 1 + max(1, math.ceil(2 * l2 / footprint))
+    sets = [case] + [inputs.MultiCase(case.q.clone(), inputs.PagedCase(
+        kv.q, kv.k_cache.clone(), kv.v_cache.clone(), kv.block_table.clone(), kv.seq_lens.clone(), kv.page_size,
+        kv.scale, kv.name), case.q_lens) for _ in range(copies - 1)]
+    ws = [torch.empty(max(1, binding.workspace_bytes_multi(case.total_q, kv.Hq, kv.D, S)), dtype=torch.uint8,
+                      device=dev) for _ in sets]
+    outs = [torch.empty_like(case.q) for _ in sets]
+    maxlen = kv.max_kv_len
+    stream = torch.cuda.current_stream()
+
+    def step(i, q=None, table=None, lens=None, pl=None):
+        c = sets[i % copies]
+        binding.decode_attn_paged_multi(c.q if q is None else q, c.kv.k_cache, c.kv.v_cache,
+                                        c.kv.block_table if table is None else table,
+                                        c.kv.seq_lens if lens is None else lens, plan if pl is None else pl,
+                                        max_kv_len=maxlen, scale=kv.scale, num_splits=S, workspace=ws[i % copies],
+                                        out=outs[i % copies])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if binding.get_device_errors(clear=True):
+        raise SystemExit("device error word set during warm-up")
+    K = args.steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(0)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for i in range(K):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / K
+
+    KT = min(K, 50)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(KT)]
+    for e in ev:
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    for i in range(KT):
+        binding.set_trace_events(*ev[i])
+        step(i)
+    torch.cuda.synchronize()
+    binding.set_trace_events()
+    kern_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    combine_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    errs = binding.get_device_errors(clear=True)
+
+    # end to end: q, block table, seq_lens and the work map in from pinned host memory, out back
+    hq = case.q.cpu().pin_memory()
+    ht = kv.block_table.cpu().pin_memory()
+    hl = kv.seq_lens.cpu().pin_memory()
+    hmap = [plan.qo_indptr.cpu().pin_memory(), plan.tile_batch.cpu().pin_memory(),
+            plan.tile_index.cpu().pin_memory()]
+    ho = torch.empty(case.q.shape, dtype=torch.bfloat16).pin_memory()
+    plans = [binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, dev) for _ in sets]
+
+    def e2e_step(i):
+        j = i % copies
+        c = sets[j]
+        c.q.copy_(hq, non_blocking=True)
+        c.kv.block_table.copy_(ht, non_blocking=True)
+        c.kv.seq_lens.copy_(hl, non_blocking=True)
+        for d, h in zip((plans[j].qo_indptr, plans[j].tile_batch, plans[j].tile_index), hmap):
+            d.copy_(h, non_blocking=True)
+        step(i, pl=plans[j])
+        ho.copy_(outs[j], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+
+    nbytes = multi_algorithmic(case)
+    lens = kv.seq_lens.cpu().tolist()
+    flops = sum(4 * kv.Hq * kv.D * sum(L - ql + i + 1 for i in range(ql)) for L, ql in zip(lens, case.q_lens))
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    h2d = hq.numel() * 2 + ht.numel() * 4 + hl.numel() * 4 + sum(h.numel() * 4 for h in hmap)
+    line = {
+        "metric": "multi-token paged decode achieved HBM GB/s (algorithmic bytes), cold KV",
+        "value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "us_per_call": round(ms * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": kv.name, "B": len(case.q_lens), "q_len": case.q_lens[0], "total_q": case.total_q,
+                   "Hq": kv.Hq, "Hkv": kv.Hkv, "D": kv.D, "page_size": kv.page_size, "total_kv": kv.total_kv,
+                   "num_tiles": plan.num_tiles, "num_splits": S, "kv_dtype": "bf16",
+                   "cold_kv": f"{copies} rotated input copies of {footprint / 1e9:.2f} GB each (> 2x L2)"},
+        "attention_tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+        "roofline": {"bound": "hbm", "kernel": "multi_kernel", "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "multi_kernel_ms": round(kern_ms, 5), "combine_ms": round(combine_ms, 5),
+                     "algorithmic_bytes_per_launch": nbytes, "traffic": None},
+        "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ho.numel() * 2},
+        "gpu_launches": K * (2 if S > 1 else 1), "device_errors": errs, "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        r = MultiOracle(case)
+        seqs = r.sample(6.0)
+        dt = r.run(seqs)
+        line["cpu_baseline"] = {"value": multi_algorithmic(case, torch.as_tensor(seqs)) / dt / 1e9, "unit": "GB/s",
+                                "cores": r.oracle.num_threads(), "kind": "oracle",
+                                "sample": f"fp64 oracle (OpenMP) on sequences 0..{len(seqs) - 1} of "
+                                          f"{len(case.q_lens)} (all new tokens and heads), one pass, {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_multi(args):
+    from paged_kv_cache_298_gb300 import inputs
+    case = inputs.spec_verify_paged()
+    r = MultiOracle(case)
+    seqs = r.sample(min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        r.run(seqs)
+    dt = statistics.mean(r.run(seqs) for _ in range(args.steps))
+    value = multi_algorithmic(case, torch.as_tensor(seqs)) / dt / 1e9
+    print(json.dumps({
+        "impl": "reference",
+        "metric": "multi-token paged decode achieved HBM GB/s (algorithmic bytes), cold KV",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": {"workload": case.kv.name, "sample_sequences": len(seqs)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": r.oracle.num_threads(), "kind": "oracle",
+                         "sample": f"fp64 oracle (OpenMP) on sequences 0..{len(seqs) - 1} per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+        flush=True)
+
+
 # ---- reference arm: the fp64 oracle on the host cores ----------------------------------
 
 def run_reference_fp8(args):
@@ -579,6 +776,8 @@ def run_reference(args):
         return
     if args.workload == "fp8":
         return run_reference_fp8(args)
+    if args.workload == "multi":
+        return run_reference_multi(args)
     case = make_workload(args.workload, "cpu")
     r = OracleRunner(case)
     rows = r.sample_rows(target_s=min(8.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -609,7 +808,7 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="ragged", choices=["ragged", "llama", "long1", "long4", "fp8", "append"])
+    ap.add_argument("--workload", default="ragged", choices=["ragged", "llama", "long1", "long4", "fp8", "append", "multi"])
     ap.add_argument("--splits", type=int, default=-1,
                     help="-1 = the planner's choice, 0 = balanced schedule, S > 0 = per-sequence splits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -622,6 +821,8 @@ def main():
         run_fp8(args)
     elif args.workload == "append":
         run_append(args)
+    elif args.workload == "multi":
+        run_multi(args)
     else:
         run_ours(args)
 

@@ -56,8 +56,9 @@ typedef enum {
 /* Bits of the device error word. */
 #define DAP_DEVERR_TIMEOUT 0x1u  /* a pipeline wait gave up; the launch's output is invalid */
 #define DAP_DEVERR_SEQLEN 0x2u   /* seq_lens[b] < 0 or > max_kv_len; clamped */
-#define DAP_DEVERR_PAGE 0x4u     /* block_table entry outside [0, num_pages); read as zeros */
+#define DAP_DEVERR_PAGE 0x4u     /* block_table entry outside [0, num_pages); page 0 read instead */
 #define DAP_DEVERR_SLOT 0x8u     /* fp8 slot index >= num_blocks*block_size; row skipped */
+#define DAP_DEVERR_QMAP 0x10u    /* multi-token work map names no token of a sequence; tile skipped */
 
 /* Human-readable name of a status code.  Never NULL. */
 const char *dap_status_string(int status);
@@ -150,6 +151,66 @@ dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_s
                               int D, float scale, int num_splits, void *workspace,
                               size_t workspace_bytes, void *out, long long out_stride_b,
                               long long out_stride_h, void *stream);
+
+/*
+ * Multi-token decode: several new tokens per sequence (speculative-decoding verification,
+ * chunked short prefill) attending the paged cache causally [A: "Q Scheduling and KV
+ * Addressing", the packed-q work map].
+ *
+ * The new tokens of all sequences are packed back to back: qo_indptr[0] = 0 and
+ * qo_indptr[b+1] = qo_indptr[b] + q_len[b]; total_q = qo_indptr[B].  The caches already hold
+ * the new tokens' K and V (append them first), so sequence b has seq_lens[b] >= q_len[b]
+ * keys and its token i (0 <= i < q_len[b]) sits at position p = seq_lens[b] - q_len[b] + i:
+ *   out[qo_indptr[b] + i, h, :] = sum_{t <= p} softmax_t(scale * q[.., h, :] . K[b,t,h/G,:])
+ *                                 V[b,t,h/G,:].
+ * (With q_len[b] = 1 this is decode_attn_paged.)  A token with p < 0 (q_len[b] > seq_lens[b],
+ * flagged DAP_DEVERR_SEQLEN) gives a zero row.
+ *
+ * Work map: every sequence's tokens are cut into tiles of tokens_per_tile =
+ * dap_multi_tokens_per_tile(Hq, Hkv) = 16 / G tokens (16 query columns of G heads each per
+ * tile); tile w covers tokens [tile_index[w] * tokens_per_tile, ...) of sequence
+ * tile_batch[w].  dap_q_tile_map builds it on the host:
+ *   q_lens      host int32 [B], each >= 0.
+ *   qo_indptr   host int32 [B + 1] (written).
+ *   tile_batch, tile_index   host int32 [max_tiles] (written).
+ * Returns the number of tiles, or -1 when max_tiles is too small or an input is invalid.
+ * Pure host functions; no CUDA call.
+ */
+int dap_multi_tokens_per_tile(int Hq, int Hkv);
+int dap_q_tile_map(const int32_t *q_lens, int B, int tokens_per_tile, int32_t *qo_indptr,
+                   int32_t *tile_batch, int32_t *tile_index, int max_tiles);
+
+/* Workspace bytes of decode_attn_paged_multi: 0 for num_splits <= 1, else room for
+ * total_q * num_splits * Hq partial rows of (D + 2) floats.  Pure host function. */
+size_t dap_workspace_bytes_multi(int total_q, int Hq, int D, int num_splits);
+
+/*
+ *   q            device bf16 [total_q, Hq, D], element strides (q_stride_t, q_stride_h, 1).
+ *   k_cache, v_cache, block_table, num_pages, page_size, max_pages: as decode_attn_paged.
+ *   seq_lens     device int32 [B], in [q_len[b], max_kv_len].
+ *   qo_indptr    device int32 [B + 1]; tile_batch, tile_index device int32 [num_tiles]: the
+ *                work map above (copies of dap_q_tile_map's output).
+ *   num_splits   >= 1: the per-sequence schedule of decode_attn_paged, per tile: the tile's
+ *                keys (up to its last token's position) are cut into chunks of
+ *                dap_chunk_tokens(max_kv_len, num_splits) keys, one CTA per (tile, kv head,
+ *                chunk), merged by a combine kernel.  0 = the library picks
+ *                dap_plan_splits(SMs, num_tiles, Hq, Hkv, D, page_size, max_kv_len, 0).
+ *   workspace    device, >= dap_workspace_bytes_multi(total_q, Hq, D, S) bytes for the
+ *                split count S used, 16-byte aligned.
+ *   out          device bf16 [total_q, Hq, D], strides (out_stride_t, out_stride_h, 1).
+ *   Supported: D in {64, 128}; G in {1, 2, 4, 8}; page_size a multiple of 8; alignment and
+ *   strides as decode_attn_paged.  A work-map entry that names no token of its sequence is
+ *   skipped and flagged (DAP_DEVERR_QMAP).
+ */
+dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long long q_stride_h,
+                                   const void *k_cache, const void *v_cache, int num_pages,
+                                   int page_size, const int32_t *block_table, int max_pages,
+                                   const int32_t *seq_lens, const int32_t *qo_indptr,
+                                   const int32_t *tile_batch, const int32_t *tile_index,
+                                   int num_tiles, int total_q, int max_kv_len, int B, int Hq,
+                                   int Hkv, int D, float scale, int num_splits, void *workspace,
+                                   size_t workspace_bytes, void *out, long long out_stride_t,
+                                   long long out_stride_h, void *stream);
 
 /*
  * fp8 sliding-window latent decode, K = V [C].

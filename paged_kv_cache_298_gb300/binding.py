@@ -23,13 +23,14 @@ DAP_OK = 0
 STATUS_NAMES = {0: "DAP_OK", 1: "DAP_ERR_NULL", 2: "DAP_ERR_SHAPE", 3: "DAP_ERR_UNSUPPORTED",
                 4: "DAP_ERR_WORKSPACE", 5: "DAP_ERR_ALIGN", 6: "DAP_ERR_CUDA", 7: "DAP_ERR_SCRATCH_LIMIT"}
 NOALLOC_SCRATCH_BYTES = 16 << 20
-DEVERR_TIMEOUT, DEVERR_SEQLEN, DEVERR_PAGE, DEVERR_SLOT = 0x1, 0x2, 0x4, 0x8
+DEVERR_TIMEOUT, DEVERR_SEQLEN, DEVERR_PAGE, DEVERR_SLOT, DEVERR_QMAP = 0x1, 0x2, 0x4, 0x8, 0x10
 
 # every symbol include/dap.h declares
 EXPORTS = ("dap_status_string", "dap_version", "dap_device_sm_count", "dap_plan_splits",
            "dap_chunk_tokens", "dap_workspace_bytes", "decode_attn_paged", "decode_attn_contig",
            "decode_attn_paged_fp8", "decode_attn_paged_noalloc", "kv_append_paged", "kv_append_fp8",
-           "dap_set_trace_events", "dap_get_device_errors")
+           "dap_set_trace_events", "dap_get_device_errors", "dap_multi_tokens_per_tile",
+           "dap_q_tile_map", "dap_workspace_bytes_multi", "decode_attn_paged_multi")
 
 
 class DapError(RuntimeError):
@@ -86,6 +87,15 @@ def load(build_if_missing: bool = True):
         lib.kv_append_paged.restype = I
         lib.kv_append_fp8.argtypes = [P, P, P, P, I, I, I, I, P]
         lib.kv_append_fp8.restype = I
+        lib.dap_multi_tokens_per_tile.argtypes = [I, I]
+        lib.dap_multi_tokens_per_tile.restype = I
+        lib.dap_q_tile_map.argtypes = [P, I, I, P, P, P, I]
+        lib.dap_q_tile_map.restype = I
+        lib.dap_workspace_bytes_multi.argtypes = [I, I, I, I]
+        lib.dap_workspace_bytes_multi.restype = SZ
+        lib.decode_attn_paged_multi.argtypes = [P, LL, LL, P, P, I, I, P, I, P, P, P, P, I, I, I, I, I, I,
+                                                I, F, I, P, SZ, P, LL, LL, P]
+        lib.decode_attn_paged_multi.restype = I
         lib.dap_set_trace_events.argtypes = [P, P, P]
         lib.dap_set_trace_events.restype = None
         lib.dap_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
@@ -272,6 +282,89 @@ def decode_attn_paged_fp8(q, kv_cache, inv_scale, slot_idx, lens, *, scale: floa
                                       T, NH, HD, slot_idx.shape[1], NB, bs, float(scale), _ptr(out),
                                       _stream(stream))
     _check(st, "decode_attn_paged_fp8")
+    return out
+
+
+# ---- multi-token decode ------------------------------------------------------------------
+
+def multi_tokens_per_tile(Hq: int, Hkv: int) -> int:
+    return load().dap_multi_tokens_per_tile(int(Hq), int(Hkv))
+
+
+def workspace_bytes_multi(total_q, Hq, D, num_splits) -> int:
+    return load().dap_workspace_bytes_multi(int(total_q), int(Hq), int(D), int(num_splits))
+
+
+def q_tile_map(q_lens, tokens_per_tile: int):
+    """Host work map of the packed new tokens (include/dap.h: dap_q_tile_map).
+    Returns int32 CPU tensors (qo_indptr [B+1], tile_batch [n], tile_index [n])."""
+    ql = torch.as_tensor(q_lens, dtype=torch.int32).cpu().contiguous().reshape(-1)
+    B = ql.numel()
+    cap = sum((int(x) + tokens_per_tile - 1) // tokens_per_tile for x in ql.tolist() if x > 0)
+    qi = torch.zeros(B + 1, dtype=torch.int32)
+    tb = torch.zeros(max(cap, 1), dtype=torch.int32)
+    ti = torch.zeros(max(cap, 1), dtype=torch.int32)
+    n = load().dap_q_tile_map(_ptr(ql), B, int(tokens_per_tile), _ptr(qi), _ptr(tb), _ptr(ti), cap)
+    _need(n >= 0, "invalid q_lens or tokens_per_tile")
+    return qi, tb[:n].clone(), ti[:n].clone()
+
+
+class MultiPlan:
+    """The work map of one batch of new-token counts, copied to the device once so that
+    repeated decode calls on the same counts pass it straight to the library."""
+
+    def __init__(self, q_lens, Hq: int, Hkv: int, device):
+        self.tokens_per_tile = multi_tokens_per_tile(Hq, Hkv)
+        _need(self.tokens_per_tile > 0, "Hq must be a multiple of Hkv with G <= 16")
+        qi, tb, ti = q_tile_map(q_lens, self.tokens_per_tile)
+        self.B = qi.numel() - 1
+        self.total_q = int(qi[-1])
+        self.num_tiles = tb.numel()
+        self.qo_indptr = qi.to(device)
+        self.tile_batch = tb.to(device)
+        self.tile_index = ti.to(device)
+
+
+def decode_attn_paged_multi(q, k_cache, v_cache, block_table, seq_lens, plan: MultiPlan, *, max_kv_len: int,
+                            scale: float | None = None, num_splits: int = 0, workspace=None, out=None,
+                            stream=None):
+    """Multi-token causal decode over a paged cache (include/dap.h: decode_attn_paged_multi).
+    q [total_q, Hq, D] holds the new tokens of all sequences back to back; ``plan`` is the
+    MultiPlan of their counts.  num_splits 0 = the library's planner (resolved here so the
+    workspace can be sized).  Returns ``out`` [total_q, Hq, D]."""
+    _bf16_3d(q, "q")
+    total_q, Hq, D = q.shape
+    _need(total_q == plan.total_q, "q rows differ from the plan's token count")
+    _need(k_cache.dtype == torch.bfloat16 and k_cache.dim() == 4 and k_cache.is_contiguous()
+          and v_cache.shape == k_cache.shape and v_cache.dtype == torch.bfloat16
+          and v_cache.is_contiguous(), "k_cache/v_cache must be contiguous bf16 [P, ps, Hkv, D]")
+    P, ps, Hkv, D2 = k_cache.shape
+    _need(D2 == D, "head dims differ")
+    B = plan.B
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
+          and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
+    _need(seq_lens.dtype == torch.int32 and seq_lens.numel() == B and seq_lens.is_contiguous(),
+          "seq_lens must be contiguous int32 [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((total_q, Hq, D), dtype=torch.bfloat16, device=q.device)
+    _bf16_3d(out, "out")
+    lib = load()
+    S = int(num_splits)
+    if S == 0 and plan.num_tiles > 0:
+        S = lib.dap_plan_splits(lib.dap_device_sm_count(), plan.num_tiles, Hq, Hkv, D, ps, int(max_kv_len), 0)
+    need = lib.dap_workspace_bytes_multi(total_q, Hq, D, S)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.decode_attn_paged_multi(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
+                                     _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                     _ptr(plan.qo_indptr), _ptr(plan.tile_batch), _ptr(plan.tile_index),
+                                     plan.num_tiles, total_q, int(max_kv_len), B, Hq, Hkv, D, float(scale),
+                                     int(S), _ptr(workspace), wbytes, _ptr(out), out.stride(0), out.stride(1),
+                                     _stream(stream))
+    _check(st, "decode_attn_paged_multi")
     return out
 
 

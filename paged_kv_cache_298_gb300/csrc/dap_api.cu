@@ -174,7 +174,7 @@ dap_status decode_attn_paged(const void *q, long long q_stride_b, long long q_st
         return DAP_ERR_SHAPE;
     if (!k_cache || !v_cache || !block_table) return DAP_ERR_NULL;
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table)) return DAP_ERR_ALIGN;
-    DecodeArgs a;
+    DecodeArgs a = {};
     a.paged = true;
     a.q = q;
     a.q_sb = q_stride_b;
@@ -214,7 +214,7 @@ dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_s
     if (max_len < 1 || max_kv_len > max_len) return DAP_ERR_SHAPE;
     if (!k || !v) return DAP_ERR_NULL;
     if (!aligned16(k) || !aligned16(v)) return DAP_ERR_ALIGN;
-    DecodeArgs a;
+    DecodeArgs a = {};
     a.paged = false;
     a.q = q;
     a.q_sb = q_stride_b;
@@ -241,6 +241,111 @@ dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_s
                         &a.num_splits, &a.chunk);
     if (st != DAP_OK) return st;
     return launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+int dap_multi_tokens_per_tile(int Hq, int Hkv) {
+    if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return 0;
+    return multi_tokens_per_tile(Hq / Hkv);
+}
+
+int dap_q_tile_map(const int32_t *q_lens, int B, int tokens_per_tile, int32_t *qo_indptr, int32_t *tile_batch,
+                   int32_t *tile_index, int max_tiles) {
+    if (B < 0 || tokens_per_tile < 1 || max_tiles < 0 || (B > 0 && (!q_lens || !qo_indptr))) return -1;
+    if (B == 0) {
+        if (qo_indptr) qo_indptr[0] = 0;
+        return 0;
+    }
+    long long total = 0;
+    int n = 0;
+    qo_indptr[0] = 0;
+    for (int b = 0; b < B; ++b) {
+        const int len = q_lens[b];
+        if (len < 0) return -1;
+        total += len;
+        if (total > 0x7FFFFFFFLL) return -1;
+        qo_indptr[b + 1] = (int32_t)total;
+        const int tiles = (int)ceil_div_ll(len, tokens_per_tile);
+        for (int j = 0; j < tiles; ++j) {
+            if (n >= max_tiles || !tile_batch || !tile_index) return -1;
+            tile_batch[n] = b;
+            tile_index[n] = j;
+            ++n;
+        }
+    }
+    return n;
+}
+
+size_t dap_workspace_bytes_multi(int total_q, int Hq, int D, int num_splits) {
+    if (total_q <= 0 || Hq <= 0 || D <= 0 || num_splits <= 1) return 0;
+    return partial_acc_bytes(total_q, Hq, D, num_splits) + partial_ml_bytes(total_q, Hq, num_splits);
+}
+
+dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long long q_stride_h,
+                                   const void *k_cache, const void *v_cache, int num_pages, int page_size,
+                                   const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                                   const int32_t *qo_indptr, const int32_t *tile_batch,
+                                   const int32_t *tile_index, int num_tiles, int total_q, int max_kv_len,
+                                   int B, int Hq, int Hkv, int D, float scale, int num_splits, void *workspace,
+                                   size_t workspace_bytes, void *out, long long out_stride_t,
+                                   long long out_stride_h, void *stream) {
+    if (total_q < 0 || num_tiles < 0 || B < 0) return DAP_ERR_SHAPE;
+    if (total_q == 0 && num_tiles == 0) return DAP_OK;
+    // tokens without tiles, tiles without tokens, or more tiles than tokens
+    if (B == 0 || total_q == 0 || num_tiles == 0 || num_tiles > total_q) return DAP_ERR_SHAPE;
+    dap_status st = check_common(q, q_stride_t, q_stride_h, seq_lens, max_kv_len, total_q, Hq, Hkv, D, scale,
+                                 num_splits, out, out_stride_t, out_stride_h);
+    if (st != DAP_OK) return st;
+    if (num_pages < 1 || page_size < 1 || max_pages < 1 ||
+        (long long)max_kv_len > (long long)max_pages * page_size)
+        return DAP_ERR_SHAPE;
+    if (!k_cache || !v_cache || !block_table || !qo_indptr || !tile_batch || !tile_index) return DAP_ERR_NULL;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table) || !aligned4(qo_indptr) ||
+        !aligned4(tile_batch) || !aligned4(tile_index))
+        return DAP_ERR_ALIGN;
+    if (page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
+    int S = num_splits;
+    if (S == 0) {
+        const int sms = dap_device_sm_count();
+        if (sms <= 0) return DAP_ERR_CUDA;
+        S = dap_plan_splits(sms, num_tiles, Hq, Hkv, D, page_size, max_kv_len, 0);
+    }
+    const int chunk = dap_chunk_tokens(max_kv_len, S);
+    const int needed = max_kv_len > 0 ? (int)ceil_div_ll(max_kv_len, chunk) : 1;
+    S = std::max(1, std::min(S, needed));
+    if (S > 1) {
+        const size_t need = dap_workspace_bytes_multi(total_q, Hq, D, S);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DAP_ERR_WORKSPACE;
+    }
+    DecodeArgs a = {};
+    a.paged = true;
+    a.q = q;
+    a.q_sb = q_stride_t;
+    a.q_sh = q_stride_h;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.num_pages = num_pages;
+    a.page_size = page_size;
+    a.block_table = block_table;
+    a.max_pages = max_pages;
+    a.seq_lens = seq_lens;
+    a.max_kv_len = max_kv_len;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.scale = scale;
+    a.num_splits = S;
+    a.chunk = chunk;
+    a.workspace = workspace;
+    a.out = out;
+    a.o_sb = out_stride_t;
+    a.o_sh = out_stride_h;
+    a.qo_indptr = qo_indptr;
+    a.tile_batch = tile_batch;
+    a.tile_index = tile_index;
+    a.num_tiles = num_tiles;
+    a.total_q = total_q;
+    return launch_decode_multi(a, static_cast<cudaStream_t>(stream));
 }
 
 dap_status decode_attn_paged_fp8(const void *q, const uint8_t *kv_cache, const void *inv_scale,

@@ -59,9 +59,14 @@ struct DecodeArgs {
     void *workspace;
     void *out;
     long long o_sb, o_sh;
+    // multi-token decode only: packed-q work map (q_sb / o_sb are then token strides)
+    const int32_t *qo_indptr, *tile_batch, *tile_index;
+    int num_tiles, total_q;
 };
 
 dap_status launch_decode(const DecodeArgs &a, cudaStream_t stream);
+dap_status launch_decode_multi(const DecodeArgs &a, cudaStream_t stream);
+int multi_tokens_per_tile(int G);
 
 // Events of dap_set_trace_events (nullptr when tracing is off).
 struct TraceEvents {

@@ -136,6 +136,32 @@ def make_paged_case(B, Hq, Hkv, D, page_size, seq_lens, seed, *, pool_factor=2.0
                      1.0 / math.sqrt(D), name)
 
 
+@dataclass
+class MultiCase:
+    """A multi-token decode problem: the paged caches of a PagedCase (already holding the
+    new tokens' K/V, so seq_lens counts them) and q packed [total_q, Hq, D], sequence b's
+    q_lens[b] rows back to back."""
+    q: torch.Tensor
+    kv: PagedCase
+    q_lens: list
+
+    @property
+    def total_q(self):
+        return self.q.shape[0]
+
+    def to(self, device) -> "MultiCase":
+        return MultiCase(self.q.to(device), self.kv.to(device), list(self.q_lens))
+
+
+def make_multi_case(B, Hq, Hkv, D, page_size, seq_lens, q_lens, seed, *, device="cpu", poison=True,
+                    name="") -> MultiCase:
+    """Caches as make_paged_case (same seed), q [sum(q_lens), Hq, D] N(0,1) bf16 from seed + 200."""
+    assert len(q_lens) == B and all(x >= 0 for x in q_lens)
+    kv = make_paged_case(B, Hq, Hkv, D, page_size, seq_lens, seed, device=device, poison=poison, name=name)
+    q = randn_bf16((int(sum(q_lens)), Hq, D), _gen(seed + 200, device), device)
+    return MultiCase(q, kv, [int(x) for x in q_lens])
+
+
 def logical_kv(case: PagedCase, max_len=None):
     """The contiguous [B, max_len, Hkv, D] copies of K and V that the paged pool holds
     (rows past a sequence's length are zero).  A data move, used to build the contiguous
@@ -255,6 +281,16 @@ def long_paged(B=1, device="cpu") -> PagedCase:
     return make_paged_case(B, 64, 8, 128, 64, [32768] * B, 298004, device=device,
                            name=f"long-context GQA decode B={B} Hq=64 Hkv=8 D=128 ps=64 "
                                 f"L=32768")
+
+
+def spec_verify_paged(device="cpu", B=128, q_len=4) -> MultiCase:
+    """Speculative-decoding verification: the ragged decode batch (B=128, Hq=32, Hkv=8,
+    D=128, page_size 16, kv_len U{256..4096}) with q_len new tokens per sequence attending
+    causally."""
+    lens = uniform_lengths(B, 256, 4096, 298003)
+    return make_multi_case(B, 32, 8, 128, 16, lens, [q_len] * B, 298006, device=device,
+                           name=f"multi-token GQA decode B={B} q_len={q_len} Hq=32 Hkv=8 D=128 ps=16 "
+                                f"L~U[256,4096]")
 
 
 def fp8_swa(device="cpu") -> Fp8Case:

@@ -142,3 +142,76 @@ def test_append_validation(lib):
     assert g(FAKE, FAKE, FAKE, FAKE, 4, 384, 2, 16, None) == 3
     assert g(FAKE, FAKE, FAKE, FAKE, -1, 512, 2, 16, None) == 2
     assert g(FAKE, None, FAKE, FAKE, 4, 512, 2, 16, None) == 1
+
+
+# ---- multi-token decode: host work map and validation -------------------------------------
+
+def test_multi_tokens_per_tile(lib):
+    assert [binding.multi_tokens_per_tile(8 * g, 8) for g in (1, 2, 4, 8)] == [16, 8, 4, 2]
+    assert binding.multi_tokens_per_tile(30, 8) == 0 and binding.multi_tokens_per_tile(8, 0) == 0
+
+
+def test_q_tile_map_matches_the_pages_worked_example():
+    import json
+    with open(os.path.join(ROOT, "tests", "golden", "q_tile_map_astrai.json")) as f:
+        g = json.load(f)
+    qi, tb, ti = binding.q_tile_map(g["q_lens"], g["tokens_per_tile"])
+    assert qi.tolist() == g["qo_indptr"]
+    assert tb.tolist() == g["q_tile_to_batch"] and ti.tolist() == g["q_tile_to_index"]
+
+
+def test_q_tile_map_matches_the_oracle_on_random_counts():
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(5)
+    for tpt in (2, 4, 8, 16):
+        lens = rng.integers(0, 40, size=23)
+        lens[[0, 7]] = 0
+        qi, tb, ti = binding.q_tile_map(lens, tpt)
+        oqi, otb, oti = oracle.q_tile_map(lens, tpt)
+        assert qi.tolist() == oqi.tolist() and tb.tolist() == otb.tolist() and ti.tolist() == oti.tolist()
+
+
+def test_q_tile_map_rejects_bad_input(lib):
+    lens = (ctypes.c_int32 * 3)(4, -1, 2)
+    qi = (ctypes.c_int32 * 4)()
+    tb = (ctypes.c_int32 * 8)()
+    ti = (ctypes.c_int32 * 8)()
+    assert lib.dap_q_tile_map(lens, 3, 4, qi, tb, ti, 8) == -1            # negative count
+    lens = (ctypes.c_int32 * 3)(4, 9, 2)
+    assert lib.dap_q_tile_map(lens, 3, 4, qi, tb, ti, 4) == -1            # needs 5 tiles
+    assert lib.dap_q_tile_map(lens, 3, 0, qi, tb, ti, 8) == -1            # zero tile size
+    assert lib.dap_q_tile_map(lens, 3, 4, qi, tb, ti, 5) == 5
+
+
+def test_workspace_bytes_multi():
+    assert binding.workspace_bytes_multi(64, 32, 128, 1) == 0
+    n = binding.workspace_bytes_multi(64, 32, 128, 5)
+    assert n >= 64 * 5 * 32 * (128 + 2) * 4 and n % 256 == 0
+
+
+def multi_call(lib, **kw):
+    a = dict(q=FAKE, qst=32 * 128, qsh=128, k=FAKE, v=FAKE, P=64, ps=16, table=FAKE, maxp=8, lens=FAKE,
+             qi=FAKE, tb=FAKE, ti=FAKE, ntiles=2, totq=8, maxlen=100, B=2, Hq=32, Hkv=8, D=128, scale=0.088,
+             S=1, ws=None, wsb=0, out=FAKE, ost=32 * 128, osh=128)
+    a.update(kw)
+    return lib.decode_attn_paged_multi(a["q"], a["qst"], a["qsh"], a["k"], a["v"], a["P"], a["ps"], a["table"],
+                                       a["maxp"], a["lens"], a["qi"], a["tb"], a["ti"], a["ntiles"], a["totq"],
+                                       a["maxlen"], a["B"], a["Hq"], a["Hkv"], a["D"], a["scale"], a["S"],
+                                       a["ws"], a["wsb"], a["out"], a["ost"], a["osh"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(totq=-1), 2), (dict(ntiles=0), 2), (dict(totq=0), 2), (dict(ntiles=9), 2), (dict(B=0), 2),
+    (dict(Hq=30), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(S=-1), 2), (dict(qsh=0), 2),
+    (dict(q=None), 1), (dict(qi=None), 1), (dict(tb=None), 1), (dict(ti=None), 1), (dict(table=None), 1),
+    (dict(D=96), 3), (dict(ps=12, maxlen=90), 3), (dict(Hq=64, Hkv=4), 3),
+    (dict(qi=ctypes.c_void_p((1 << 20) + 2)), 5), (dict(qst=4100), 5),
+    (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=16), 4),
+])
+def test_multi_validation(lib, kw, status):
+    assert multi_call(lib, **kw) == status
+
+
+def test_multi_empty_is_a_no_op(lib):
+    assert multi_call(lib, totq=0, ntiles=0, q=None, out=None, k=None, qi=None, tb=None, ti=None) == 0
