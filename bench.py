@@ -114,7 +114,8 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-KERNEL_SOURCES = {"split_kernel": ("dap_decode.cu", "dap_device.cuh", "dap_internal.h"),
+KERNEL_SOURCES = {"split_kernel": ("dap_decode.cu", "dap_tile.cuh", "dap_device.cuh", "dap_internal.h"),
+                  "multi_kernel": ("dap_multi.cu", "dap_tile.cuh", "dap_device.cuh", "dap_internal.h"),
                   "swa_kernel": ("dap_fp8.cu", "dap_device.cuh", "dap_internal.h")}
 
 
@@ -144,6 +145,11 @@ def recorded_traffic(kernel: str, workload_key: str):
     return None
 
 
+def workload_key(args) -> str:
+    """Key of the workload in the recorded-traffic table (the batch size when not the default)."""
+    return args.workload if not getattr(args, "batch", 0) else f"{args.workload}_b{args.batch}"
+
+
 def job_throughput(ms_list, nbytes_per_rank, world, device):
     """Whole-job GB/s for each timing in ms_list: every rank processed nbytes_per_rank, and
     the job took as long as its slowest rank (max over ranks of each timing).  Returns
@@ -157,10 +163,10 @@ def job_throughput(ms_list, nbytes_per_rank, world, device):
 
 # ---- workloads ---------------------------------------------------------------------------
 
-def make_workload(name: str, device):
+def make_workload(name: str, device, batch=None):
     from paged_kv_cache_298_gb300 import inputs
     if name == "ragged":
-        return inputs.ragged_paged(device=device)
+        return inputs.ragged_paged(device=device, B=batch or 128)
     if name == "llama":
         return inputs.llama_paged(device=device)
     if name in ("long1", "long4"):
@@ -242,7 +248,7 @@ def run_ours(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     binding.load()
-    case = make_workload(args.workload, dev)
+    case = make_workload(args.workload, dev, args.batch)
     hbm_peak, peak_src = peaks()
     sms = binding.device_sm_count()
     S = args.splits if args.splits >= 0 else binding.plan_splits(
@@ -357,7 +363,7 @@ def run_ours(args):
                      "peak": hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "split_kernel_ms": round(split_ms, 5),
                      "combine_ms": round(combine_ms, 5), "algorithmic_bytes_per_launch": nbytes,
-                     "traffic": recorded_traffic("split_kernel", args.workload)},
+                     "traffic": recorded_traffic("split_kernel", workload_key(args))},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": hq.numel() * 2 + ht.numel() * 4 + hl.numel() * 4,
                 "d2h_bytes_per_step": ho.numel() * 2},
@@ -593,13 +599,13 @@ def run_multi(args):
     from paged_kv_cache_298_gb300 import binding, inputs
     dev = torch.device("cuda", 0)
     binding.load()
-    case = inputs.spec_verify_paged(device=dev)
+    case = inputs.spec_verify_paged(device=dev, B=args.batch or 128)
     kv = case.kv
     hbm_peak, peak_src = peaks()
     plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, dev)
     sms = binding.device_sm_count()
     S = args.splits if args.splits > 0 else binding.plan_splits(sms, plan.num_tiles, kv.Hq, kv.Hkv, kv.D,
-                                                                kv.page_size, kv.max_kv_len, 0)
+                                                                kv.page_size, kv.max_kv_len, kv.total_kv)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     footprint = sum(t.numel() * t.element_size() for t in (case.q, kv.k_cache, kv.v_cache, kv.block_table,
                                                            kv.seq_lens))
@@ -704,7 +710,8 @@ def run_multi(args):
         "roofline": {"bound": "hbm", "kernel": "multi_kernel", "achieved": round(achieved, 1), "peak": hbm_peak,
                      "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                      "multi_kernel_ms": round(kern_ms, 5), "combine_ms": round(combine_ms, 5),
-                     "algorithmic_bytes_per_launch": nbytes, "traffic": None},
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "traffic": recorded_traffic("multi_kernel", workload_key(args))},
         "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ho.numel() * 2},
         "gpu_launches": K * (2 if S > 1 else 1), "device_errors": errs, "clocks": clk,
@@ -812,6 +819,9 @@ def main():
     ap.add_argument("--splits", type=int, default=-1,
                     help="-1 = the planner's choice, 0 = balanced schedule, S > 0 = per-sequence splits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="ragged / multi workloads: number of sequences (0 = the workload's own, 128); "
+                         "smaller batches are for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

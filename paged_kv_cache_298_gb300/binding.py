@@ -326,12 +326,13 @@ class MultiPlan:
 
 
 def decode_attn_paged_multi(q, k_cache, v_cache, block_table, seq_lens, plan: MultiPlan, *, max_kv_len: int,
-                            scale: float | None = None, num_splits: int = 0, workspace=None, out=None,
-                            stream=None):
+                            scale: float | None = None, num_splits: int = 0, total_kv: int = 0, workspace=None,
+                            out=None, stream=None):
     """Multi-token causal decode over a paged cache (include/dap.h: decode_attn_paged_multi).
     q [total_q, Hq, D] holds the new tokens of all sequences back to back; ``plan`` is the
-    MultiPlan of their counts.  num_splits 0 = the library's planner (resolved here so the
-    workspace can be sized).  Returns ``out`` [total_q, Hq, D]."""
+    MultiPlan of their counts.  num_splits 0 = the planner's choice (dap_plan_splits over the
+    plan's tiles, given the host-known sum of seq_lens ``total_kv`` if any), resolved here so
+    the workspace can be sized.  Returns ``out`` [total_q, Hq, D]."""
     _bf16_3d(q, "q")
     total_q, Hq, D = q.shape
     _need(total_q == plan.total_q, "q rows differ from the plan's token count")
@@ -353,7 +354,8 @@ def decode_attn_paged_multi(q, k_cache, v_cache, block_table, seq_lens, plan: Mu
     lib = load()
     S = int(num_splits)
     if S == 0 and plan.num_tiles > 0:
-        S = lib.dap_plan_splits(lib.dap_device_sm_count(), plan.num_tiles, Hq, Hkv, D, ps, int(max_kv_len), 0)
+        S = lib.dap_plan_splits(lib.dap_device_sm_count(), plan.num_tiles, Hq, Hkv, D, ps, int(max_kv_len),
+                                int(total_kv))
     need = lib.dap_workspace_bytes_multi(total_q, Hq, D, S)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

@@ -420,6 +420,7 @@ dap_status dap_get_device_errors(unsigned int *flags, int clear) {
     if (!read_errors_decode(flags, clear != 0)) return DAP_ERR_CUDA;
     if (!read_errors_fp8(flags, clear != 0)) return DAP_ERR_CUDA;
     if (!read_errors_append(flags, clear != 0)) return DAP_ERR_CUDA;
+    if (!read_errors_multi(flags, clear != 0)) return DAP_ERR_CUDA;
     return DAP_OK;
 }
 

@@ -5,7 +5,8 @@
 //   out[b,h] = sum_t softmax_t(scale * q[b,h] . K[b,t,h/G]) V[b,t,h/G],   t < seq_lens[b].
 //
 // Work.  A "unit" is (sequence b, group of HG kv heads); its keys are cut into tiles of
-// BT = 32 tokens.  Two schedules share one per-tile pipeline:
+// BT tokens (64 for the tensor-core consumer, 32 for the CUDA-core one).  Two schedules
+// share one per-tile pipeline:
 //   * balanced (num_splits == 0): a persistent grid of P CTAs (SMs x resident CTAs); the
 //     flattened (unit, tile) sequence of all T tiles is cut into P contiguous ranges of
 //     T/P tiles, so every CTA streams the same number of tiles whatever the length mix.  A
@@ -22,52 +23,30 @@
 //
 // Data movement.  K and V tiles are staged in shared memory by 4-D TMA boxes over the
 // cache viewed as [pages, page_size, Hkv, D] (contiguous cache: [B, max_len, Hkv, D], one
-// "page" per sequence).  A box covers R = gcd(page_size, 32) tokens of one page and HG
-// kv heads, so any page size works (csrc log, per-element page lookup commit).  One
-// producer warp resolves page ids one tile ahead, arms the stage's mbarrier with the byte
-// count and issues the boxes; NS stages keep NS-1 tiles in flight (csrc log, multi-stage
-// pipeline commit).  Out-of-range page ids are replaced by page 0 and flagged.
+// "page" per sequence).  A box covers R = gcd(page_size, BT) tokens of one page, so any
+// page size works (csrc log, per-element page lookup commit); page sizes that are
+// multiples of 8 use 128-byte-swizzled boxes of 64 dims.  One producer warp resolves page
+// ids one tile ahead, arms the stage's mbarrier with the byte count and issues the boxes;
+// NS stages keep NS-1 tiles in flight (csrc log, multi-stage pipeline commit).
+// Out-of-range page ids are replaced by page 0 and flagged.
 //
-// Arithmetic.  q is held in fp32 registers, pre-multiplied by scale*log2(e) in fp32 (the
-// bf16 q is never rescaled: csrc log, "apply scale in float32 after Q@K^T").  QK^T uses
-// packed fp32 FMAs with LPR lanes per key row and a reduce-scatter across them; the
-// online softmax runs in base 2; PV accumulates with packed fused multiply-adds (csrc log,
-// numerics commit: fmaf for V accumulation).  Rows past the sequence end are masked to
-// -inf before the max and never read in PV, so stale or poisoned shared memory cannot leak
-// into the result.  The final division is guarded (an empty sequence gives zeros).
+// Arithmetic.  Tensor-core consumer (swizzled tiles): per 16-key slice a warp computes
+// S^T = K . Q^T with mma.m16n8k16 (the G heads of the kv head in N), the base-2 online
+// softmax on the fragments, and O^T += V^T . P^T with the bf16 probabilities as B operand.
+// CUDA-core consumer (other page sizes): q in fp32 registers, packed fp32 FMAs with LPR
+// lanes per key row.  Both apply the scale in fp32 after the dot product (csrc log, "apply
+// scale in float32 after Q@K^T"), accumulate V with fused multiply-adds (numerics commit),
+// mask rows past the sequence end to -inf before the max and keep them out of PV, and guard
+// the final division (an empty sequence gives zeros).
 #include <math.h>
 
 #include <algorithm>
 #include <mutex>
 #include <type_traits>
 
-#include "dap_device.cuh"
-#include "dap_internal.h"
+#include "dap_tile.cuh"
 
 namespace dap {
-
-struct SplitParams {
-    const __nv_bfloat16 *q;
-    long long q_sb, q_sh;
-    const int32_t *block_table;
-    int max_pages;
-    const int32_t *seq_lens;
-    int max_kv_len;
-    int B, Hq, Hkv;
-    int page_size, num_pages, box_rows;
-    int num_splits, chunk;  // per-sequence schedule
-    int num_ctas;           // balanced schedule: P
-    float qscale;           // scale * log2(e)
-    float *o_part;
-    float *ml_part;
-    int *unit_info;         // balanced: [units][2] = first tile, tiles
-    long long *total_tiles; // balanced: T
-    __nv_bfloat16 *out;
-    long long o_sb, o_sh;
-    // multi-token decode: packed q / out rows are tokens; q_sb / o_sb are the token strides
-    const int32_t *qo_indptr, *tile_batch, *tile_index;
-    int num_tiles, total_q;
-};
 
 template <int D_, int G_, int HG_, int NWC_, int BT_, int NS_, int MINB_>
 struct SplitCfg {
@@ -335,12 +314,6 @@ struct Consumer {
     }
 };
 
-__device__ __forceinline__ void store_out_pair(__nv_bfloat16 *o, float a0, float a1, float l) {
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    *reinterpret_cast<__nv_bfloat162 *>(o) = __floats2bfloat162_rn(a0 * inv, a1 * inv);
-}
-
-
 // ---- tensor-core consumer ---------------------------------------------------------------
 // For each 16-key slice a warp computes S^T = K . Q^T with mma.m16n8k16 (M = 16 keys,
 // N = 8 query heads of the kv head, padded with zero rows of q when G < 8, K = 16 dims per
@@ -562,292 +535,6 @@ struct MmaConsumer {
 
 template <class C>
 using ConsumerOf = typename std::conditional<C::MMA, MmaConsumer<C>, Consumer<C>>::type;
-
-// 1024-byte aligned view of the dynamic shared memory (the 128-byte swizzle is a function
-// of address bits 4..9, so swizzled tiles must start on 1024-byte boundaries).
-template <class C>
-__device__ __forceinline__ uint8_t *aligned_smem(uint8_t *raw) {
-    if constexpr (C::SWZ) return raw + ((1024u - (smem_addr(raw) & 1023u)) & 1023u);
-    return raw;
-}
-
-// ---- multi-token consumer ---------------------------------------------------------------
-// The query columns are (token, head) pairs: 16 columns = QT = 16 / G new tokens x G heads
-// of the kv head (two n8 tiles).  Per 16-key slice: S^T = K . Q^T for each n tile, a causal
-// mask per column (key position <= the column's token position), the online softmax per
-// column, movmatrix into the B operands and O^T += V^T . P^T.  q is read from global memory
-// (the per-sequence schedule gives each CTA one unit), and the four warps merge their
-// partial states in quarters of D.
-
-template <int D_, int G_>
-struct MultiCfg {
-    static constexpr int D = D_, G = G_, HG = 1, NWC = 4, BT = 64, NS = 3, MINB = 2;
-    static constexpr bool MMA = true, SWZ = true;
-    static constexpr int NT = 2;                    // n8 tiles of query columns
-    static constexpr int NCOL = 8 * NT;             // 16 columns
-    static constexpr int QT = NCOL / G;             // new tokens per work tile
-    static constexpr int WPH = NWC, KPW = BT / NWC;
-    static constexpr int ROWB = D * 2, HPU = G, NHALF = D / 64;
-    static constexpr int TILE_BYTES = BT * ROWB;
-    static constexpr int QBYTES = 0;
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int NPART = 4;                 // merge in quarters of D
-    static constexpr int MRG_OFF = NS * STAGE_BYTES;
-    static constexpr int MRG_BYTES = NWC * NCOL * (D / NPART + 2) * 4;
-    static constexpr int HDR_OFF = MRG_OFF + MRG_BYTES;
-    static constexpr int HDR_INTS = 8;
-    static constexpr int MISC_OFF = HDR_OFF + NS * HDR_INTS * 4;
-    static constexpr int BAR_OFF = (MISC_OFF + 16 + 7) & ~7;
-    static constexpr int SMEM = BAR_OFF + (2 * NS + 1) * 8 + 1024;
-    static constexpr int THREADS = (NWC + 1) * 32;
-    static_assert(KPW == 16 && NCOL % G == 0 && STAGE_BYTES % 1024 == 0, "multi-token tiling");
-};
-
-template <class C>
-struct MultiConsumer {
-    static constexpr int D = C::D, G = C::G, KS = D / 16, NT = C::NT;
-    uint32_t qb[KS][NT][2];
-    float acc[KS][NT][4];
-    float m_run[NT][2], l_run[NT][2];
-    float qscale;
-    int warp, lane, g, t, key0, nq, p_base;
-    static constexpr int hh = 0;
-
-    __device__ __forceinline__ void init(int w, int l, uint8_t *) {
-        warp = w;
-        lane = l;
-        g = l >> 2;
-        t = l & 3;
-        key0 = w * C::KPW;
-    }
-
-    __device__ __forceinline__ void reset() {
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                m_run[n][j] = -INFINITY;
-                l_run[n][j] = 0.f;
-            }
-#pragma unroll
-        for (int m = 0; m < KS; ++m)
-#pragma unroll
-            for (int n = 0; n < NT; ++n)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[m][n][j] = 0.f;
-    }
-
-    // q of the tile's tokens: token i, head h at base + i * tstride + h * hstride
-    __device__ __forceinline__ void load_q(const __nv_bfloat16 *base, long long tstride, long long hstride,
-                                           int ntok, int pos0, float qs) {
-        qscale = qs;
-        nq = ntok;
-        p_base = pos0;
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            const int c = n * 8 + g;
-            const int ti = c / G, hc = c % G;
-#pragma unroll
-            for (int k = 0; k < KS; ++k) {
-                if (ti < ntok) {
-                    const __nv_bfloat16 *r = base + ti * tstride + hc * hstride + 16 * k + 2 * t;
-                    qb[k][n][0] = *reinterpret_cast<const uint32_t *>(r);
-                    qb[k][n][1] = *reinterpret_cast<const uint32_t *>(r + 8);
-                } else {
-                    qb[k][n][0] = qb[k][n][1] = 0u;
-                }
-            }
-        }
-    }
-
-    static __device__ __forceinline__ uint32_t off(int key, int dim) {
-        const int chunk = (dim & 63) >> 3;
-        return (uint32_t)((dim >> 6) * (C::BT * 128) + key * 128 + ((chunk ^ (key & 7)) << 4));
-    }
-
-    // tile_pos: absolute position of the tile's first key
-    __device__ __forceinline__ void tile(uint8_t *stage, int nvalid, int tile_pos) {
-        const int nv = nvalid - key0;
-        if (nv <= 0) return;
-        uint8_t *sV = stage + C::TILE_BYTES;
-        if (nv < 16) {
-            for (int i = lane; i < (16 - nv) * C::NHALF * 8; i += 32) {
-                const int row = key0 + nv + i / (C::NHALF * 8);
-                const int rest = i % (C::NHALF * 8);
-                *reinterpret_cast<uint4 *>(sV + (rest >> 3) * (C::BT * 128) + row * 128 + (rest & 7) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
-        const uint32_t kbase = smem_addr(stage), vbase = smem_addr(sV);
-        float c[NT][4];
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) c[n][j] = 0.f;
-        {
-            const int key = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int dcol = ((lane >> 4) & 1) * 8;
-#pragma unroll
-            for (int k = 0; k < KS; ++k) {
-                uint32_t a[4];
-                ldmatrix_x4(a, kbase + off(key, 16 * k + dcol));
-#pragma unroll
-                for (int n = 0; n < NT; ++n) mma_bf16_16816(c[n], a, qb[k][n][0], qb[k][n][1]);
-            }
-        }
-        const int kpos0 = tile_pos + key0 + g, kpos1 = kpos0 + 8;  // absolute key positions
-        uint32_t b0[NT], b1[NT];
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            float s[4];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int col = n * 8 + 2 * t + j;
-                const int ti = col / G;
-                const int lim = p_base + ti;  // this column's token sees keys <= lim
-                const bool col_ok = ti < nq;
-                s[j] = (col_ok && g < nv && kpos0 <= lim) ? c[n][j] * qscale : -INFINITY;
-                s[j + 2] = (col_ok && g + 8 < nv && kpos1 <= lim) ? c[n][j + 2] * qscale : -INFINITY;
-            }
-            float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xFFFFFFFFu, mx[0], o));
-                mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xFFFFFFFFu, mx[1], o));
-            }
-            float alpha[2], mu[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float m_new = fmaxf(m_run[n][j], mx[j]);
-                mu[j] = (m_new == -INFINITY) ? 0.f : m_new;
-                alpha[j] = ex2(m_run[n][j] - mu[j]);
-                m_run[n][j] = m_new;
-            }
-            const uint32_t w0 = pack_bf16x2(ex2(s[0] - mu[0]), ex2(s[1] - mu[1]));
-            const uint32_t w1 = pack_bf16x2(ex2(s[2] - mu[0]), ex2(s[3] - mu[1]));
-            const float2 p0 = bf16x2_to_float2(w0), p1 = bf16x2_to_float2(w1);
-            l_run[n][0] = l_run[n][0] * alpha[0] + (p0.x + p1.x);
-            l_run[n][1] = l_run[n][1] * alpha[1] + (p0.y + p1.y);
-#pragma unroll
-            for (int m = 0; m < KS; ++m) {
-                acc[m][n][0] *= alpha[0];
-                acc[m][n][1] *= alpha[1];
-                acc[m][n][2] *= alpha[0];
-                acc[m][n][3] *= alpha[1];
-            }
-            b0[n] = movmatrix_trans(w0);
-            b1[n] = movmatrix_trans(w1);
-        }
-        {
-            const int key = key0 + (lane & 7) + ((lane >> 4) & 1) * 8;
-            const int dcol = ((lane >> 3) & 1) * 8;
-#pragma unroll
-            for (int m = 0; m < KS; ++m) {
-                uint32_t a[4];
-                ldmatrix_x4_trans(a, vbase + off(key, 16 * m + dcol));
-#pragma unroll
-                for (int n = 0; n < NT; ++n) mma_bf16_16816(acc[m][n], a, b0[n], b1[n]);
-            }
-        }
-    }
-
-    // merge the four warps per column in C::NPART parts of D; emit(col, d, a0, a1, M, l)
-    template <class Sync, class Emit>
-    __device__ __forceinline__ bool finish(float *mrg, Sync sync, Emit emit) {
-        constexpr int NWC = C::NWC, NC = C::NCOL, DP = D / C::NPART, MP = KS / C::NPART;
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                l_run[n][0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[n][0], o);
-                l_run[n][1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[n][1], o);
-            }
-        float *macc = mrg;               // [NWC][NC][DP]
-        float *mml = mrg + NWC * NC * DP;  // [NWC][NC][2]
-        if (g == 0) {
-#pragma unroll
-            for (int n = 0; n < NT; ++n)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    mml[(warp * NC + n * 8 + 2 * t + j) * 2 + 0] = m_run[n][j];
-                    mml[(warp * NC + n * 8 + 2 * t + j) * 2 + 1] = l_run[n][j];
-                }
-        }
-        const int tid = warp * 32 + lane;
-#pragma unroll
-        for (int part = 0; part < C::NPART; ++part) {
-#pragma unroll
-            for (int m = part * MP; m < (part + 1) * MP; ++m) {
-                const int d = 16 * m + g - part * DP;
-#pragma unroll
-                for (int n = 0; n < NT; ++n)
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        float *row = macc + (warp * NC + n * 8 + 2 * t + j) * DP;
-                        row[d] = acc[m][n][j];
-                        row[d + 8] = acc[m][n][j + 2];
-                    }
-            }
-            if (!sync()) return false;
-            for (int e = tid * 2; e < NC * DP; e += NWC * 32 * 2) {
-                const int col = e / DP, dd = e % DP;
-                if (col / G < nq) {
-                    float M = -INFINITY;
-#pragma unroll
-                    for (int w = 0; w < NWC; ++w) M = fmaxf(M, mml[(w * NC + col) * 2]);
-                    const float Mu = (M == -INFINITY) ? 0.f : M;
-                    float a0 = 0.f, a1 = 0.f, lv = 0.f;
-#pragma unroll
-                    for (int w = 0; w < NWC; ++w) {
-                        const float f = ex2(mml[(w * NC + col) * 2] - Mu);
-                        lv = fmaf(f, mml[(w * NC + col) * 2 + 1], lv);
-                        const float2 x = *reinterpret_cast<const float2 *>(macc + (w * NC + col) * DP + dd);
-                        a0 = fmaf(f, x.x, a0);
-                        a1 = fmaf(f, x.y, a1);
-                    }
-                    emit(col, part * DP + dd, a0, a1, M, lv);
-                }
-            }
-            if (!sync()) return false;
-        }
-        return true;
-    }
-};
-
-// Barrier among the NWC consumer warps on an mbarrier (count NWC, one arrival per warp),
-// so that a wait is bounded like every other wait in the pipeline.
-struct ConsumerBarrier {
-    uint64_t *bar;
-    uint32_t phase;
-    __device__ __forceinline__ bool sync(int lane) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar);
-        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar, phase & 1));
-        ++phase;
-        return ok;
-    }
-};
-
-// The K and V boxes of one producer lane: box j of the stage covers tile rows
-// [j*R, (j+1)*R).  Swizzled configurations split every row into 128-byte column blocks.
-template <class C>
-__device__ __forceinline__ void issue_kv_box(uint8_t *stage, int j, int R, const CUtensorMap *mk,
-                                             const CUtensorMap *mv, int kvh0, int row, int page, uint64_t *bar) {
-    if constexpr (C::SWZ) {
-#pragma unroll
-        for (int h = 0; h < C::NHALF; ++h) {
-            uint8_t *dst = stage + h * (C::BT * 128) + j * R * 128;
-            tma_load_4d(dst, mk, 64 * h, kvh0, row, page, bar);
-            tma_load_4d(dst + C::TILE_BYTES, mv, 64 * h, kvh0, row, page, bar);
-        }
-    } else {
-        uint8_t *dst = stage + j * R * C::HG * C::ROWB;
-        tma_load_4d(dst, mk, 0, kvh0, row, page, bar);
-        tma_load_4d(dst + C::TILE_BYTES, mv, 0, kvh0, row, page, bar);
-    }
-}
 
 // ---- per-sequence schedule: one CTA per (unit, split) ------------------------------------
 
@@ -1226,45 +913,6 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
 // output row, lanes over D.  Both wait for the split grid (programmatic dependent launch).
 
 template <int D>
-struct RowMerge {
-    static constexpr int DPV = D / 32;
-    using Vec = typename std::conditional<DPV == 4, float4, float2>::type;
-    float acc[DPV];
-    float lsum, Mu;
-    __device__ __forceinline__ void begin(float m_max) {
-        Mu = (m_max == -INFINITY) ? 0.f : m_max;
-        lsum = 0.f;
-#pragma unroll
-        for (int j = 0; j < DPV; ++j) acc[j] = 0.f;
-    }
-    // add the partial rows o[0..n) (n <= 8), whose loads are all issued before any use
-    __device__ __forceinline__ void add_batch(const float *const *o, const float2 *ml, int n, int lane) {
-        Vec x[8];
-        float f[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            if (k < n) {
-                x[k] = *reinterpret_cast<const Vec *>(o[k] + lane * DPV);
-                f[k] = ex2(ml[k].x - Mu);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            if (k < n) {
-                lsum = fmaf(f[k], ml[k].y, lsum);
-                const float *xv = reinterpret_cast<const float *>(&x[k]);
-#pragma unroll
-                for (int j = 0; j < DPV; ++j) acc[j] = fmaf(f[k], xv[j], acc[j]);
-            }
-        }
-    }
-    __device__ __forceinline__ void store(__nv_bfloat16 *o, int lane) {
-#pragma unroll
-        for (int j = 0; j < DPV; j += 2) store_out_pair(o + lane * DPV + j, acc[j], acc[j + 1], lsum);
-    }
-};
-
-template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -1390,290 +1038,7 @@ __global__ void __launch_bounds__(128) combine_balanced_kernel(const SplitParams
 
 // ---- host side ----------------------------------------------------------------------------
 
-// ---- multi-token decode: one CTA per (q tile, kv head, split) ----------------------------
-// The packed-q work map (AstrAI "CUDA Kernels" doc, "Q Scheduling and KV Addressing"): q
-// holds the new tokens of all sequences back to back, qo_indptr is the prefix sum of their
-// counts, and work tile w covers tokens [tile_index[w] * QT, +QT) of sequence tile_batch[w].
-// Token i of a sequence with q_len new tokens and L cached keys (the new ones included)
-// sits at position L - q_len + i and attends keys 0 .. that position.  The tile's KV range
-// ends after its last token's position and is cut into chunks of p.chunk keys.
-
-struct MultiTile {
-    int b, q0, qlen, i0, ntok, pos0, kv_end;
-};
-
-// The tile's sequence, tokens and KV range; false for a work-map entry that names no token
-// (flagged).  Shared by the attention kernel and its combine so both agree on the splits.
-__device__ __forceinline__ bool multi_tile(const SplitParams &p, int b, int tindex, int qt, bool report,
-                                           MultiTile *t) {
-    if (b < 0 || b >= p.B) {
-        if (report) flag_error(DAP_DEVERR_QMAP);
-        return false;
-    }
-    t->b = b;
-    t->q0 = p.qo_indptr[b];
-    t->qlen = p.qo_indptr[b + 1] - t->q0;
-    t->i0 = tindex * qt;
-    t->ntok = min(qt, t->qlen - t->i0);
-    if (tindex < 0 || t->ntok <= 0 || t->q0 < 0 || t->q0 + t->qlen > p.total_q) {
-        if (report) flag_error(DAP_DEVERR_QMAP);
-        return false;
-    }
-    int L = p.seq_lens[b];
-    if (L < 0 || L > p.max_kv_len || t->qlen > L) {
-        if (report) flag_error(DAP_DEVERR_SEQLEN);
-        L = min(max(L, 0), p.max_kv_len);
-    }
-    t->pos0 = L - t->qlen + t->i0;  // negative for tokens that would sit before the cache start
-    t->kv_end = max(0, t->pos0 + t->ntok);
-    return true;
-}
-
-template <class C>
-__global__ void __launch_bounds__(C::THREADS, C::MINB)
-    multi_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
-                 const SplitParams p) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = aligned_smem<C>(smem_raw);
-    constexpr int G = C::G, NWC = C::NWC, BT = C::BT, NS = C::NS, D = C::D;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    const int units = p.num_tiles * p.Hkv;
-    const int s = blockIdx.x / units;
-    const int rem = blockIdx.x - s * units;
-    const int w = rem / p.Hkv;
-    const int kvh = rem - w * p.Hkv;
-    MultiTile tl;
-    if (!multi_tile(p, p.tile_batch[w], p.tile_index[w], C::QT, threadIdx.x == 0 && s == 0 && kvh == 0, &tl))
-        return;
-    const int nsplit = max(1, (tl.kv_end + p.chunk - 1) / p.chunk);
-    if (s >= nsplit) return;
-    const int tok0 = s * p.chunk;
-    const int tok1 = min(tl.kv_end, tok0 + p.chunk);
-    const int ntiles = tok1 > tok0 ? (tok1 - tok0 + BT - 1) / BT : 0;
-
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *empty = full + NS;
-    int *misc = reinterpret_cast<int *>(smem + C::MISC_OFF);  // [0] tiles issued, [1] abort
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], NWC);
-        }
-        misc[0] = 0;
-        misc[1] = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    if (warp == NWC) {  // ---- producer warp: page lookup + TMA issue (as in split_kernel)
-        if (lane == 0) {
-            prefetch_tensormap(&mapK);
-            prefetch_tensormap(&mapV);
-        }
-        const int R = p.box_rows;
-        const int32_t *table = p.block_table + (long long)tl.b * p.max_pages;
-        auto lookup = [&](int tile) -> int {
-            const int t = tok0 + tile * BT + lane * R;
-            if (lane * R >= BT || t >= tok1) return 0;
-            int pg = __ldg(table + t / p.page_size);
-            if (pg < 0 || pg >= p.num_pages) {
-                flag_error(DAP_DEVERR_PAGE);
-                pg = 0;
-            }
-            return pg;
-        };
-        int pg_next = ntiles > 0 ? lookup(0) : 0;
-        int issued = 0;
-        for (int i = 0; i < ntiles; ++i) {
-            const int st = i % NS;
-            const int pg = pg_next;
-            if (i + 1 < ntiles) pg_next = lookup(i + 1);
-            if (i >= NS && !__all_sync(0xFFFFFFFFu, mbar_wait(&empty[st], ((i / NS) - 1) & 1))) {
-                misc[1] = 1;
-                break;
-            }
-            const int t = tok0 + i * BT;
-            const int nvalid = min(BT, tok1 - t);
-            const int nbox = (nvalid + R - 1) / R;
-            const uint32_t bytes = (uint32_t)(nbox * R * C::ROWB * 2);
-            if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
-            __syncwarp();
-            if (lane < nbox) {
-                const int tt = t + lane * R;
-                issue_kv_box<C>(smem + st * C::STAGE_BYTES, lane, R, &mapK, &mapV, kvh, tt % p.page_size, pg,
-                                &full[st]);
-            }
-            issued = i + 1;
-        }
-        if (lane == 0) misc[0] = issued;
-        __syncthreads();
-        return;
-    }
-
-    // ---- consumer warps
-    MultiConsumer<C> cs;
-    cs.init(warp, lane, smem);
-    cs.reset();
-    cs.load_q(p.q + (long long)(tl.q0 + tl.i0) * p.q_sb + (long long)kvh * G * p.q_sh, p.q_sb, p.q_sh, tl.ntok,
-              tl.pos0, p.qscale);
-    int consumed = 0;
-    for (int i = 0; i < ntiles; ++i) {
-        const int st = i % NS;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (i / NS) & 1))) {
-            misc[1] = 1;
-            break;
-        }
-        const int t = tok0 + i * BT;
-        cs.tile(smem + st * C::STAGE_BYTES, min(BT, tok1 - t), t);
-        if (lane == 0) mbar_arrive(&empty[st]);
-        consumed = i + 1;
-    }
-    __syncthreads();
-    if (misc[1]) {
-        if (threadIdx.x == 0)
-            for (int i = consumed; i < misc[0]; ++i) (void)mbar_wait(&full[i % NS], (i / NS) & 1);
-        return;
-    }
-    const bool direct = (nsplit == 1);
-    const int r0 = tl.q0 + tl.i0;
-    cs.finish(reinterpret_cast<float *>(smem + C::MRG_OFF), [] { named_sync(1, NWC * 32); return true; },
-              [&](int col, int d, float a0, float a1, float M, float lv) {
-                  const long long r = r0 + col / G;
-                  const int hq = kvh * G + col % G;
-                  if (direct) {
-                      store_out_pair(p.out + r * p.o_sb + (long long)hq * p.o_sh + d, a0, a1, lv);
-                  } else {
-                      const long long row = (r * p.num_splits + s) * p.Hq + hq;
-                      *reinterpret_cast<float2 *>(p.o_part + row * D + d) = make_float2(a0, a1);
-                      if (d == 0) *reinterpret_cast<float2 *>(p.ml_part + row * 2) = make_float2(M, lv);
-                  }
-              });
-}
-
-// Merge the split partials of every (token, head) row, one warp per row.  The row's
-// sequence is found by binary search of qo_indptr; the split count follows from the row's
-// tile exactly as in multi_kernel.
-template <int D>
-__global__ void __launch_bounds__(256) combine_multi_kernel(const SplitParams p, int qt) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= p.total_q * p.Hq) return;
-    const int r = gw / p.Hq, hq = gw - r * p.Hq;
-    int lo = 0, hi = p.B;  // qo_indptr[lo] <= r < qo_indptr[hi] for a well-formed map
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (p.qo_indptr[mid] <= r) lo = mid;
-        else hi = mid;
-    }
-    MultiTile tl;
-    if (!multi_tile(p, lo, (r - p.qo_indptr[lo]) / qt, qt, false, &tl)) return;
-    const int nsplit = max(1, (tl.kv_end + p.chunk - 1) / p.chunk);
-    if (nsplit == 1) return;
-    const long long row0 = (long long)r * p.num_splits * p.Hq + hq;
-    float M = -INFINITY;
-    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, p.ml_part[(row0 + (long long)s * p.Hq) * 2]);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-    RowMerge<D> m;
-    m.begin(M);
-    for (int s0 = 0; s0 < nsplit; s0 += 8) {
-        const float *o[8];
-        float2 ml[8];
-        const int n = min(8, nsplit - s0);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const long long row = row0 + (long long)min(s0 + k, nsplit - 1) * p.Hq;
-            o[k] = p.o_part + row * D;
-            ml[k] = *reinterpret_cast<const float2 *>(p.ml_part + row * 2);
-        }
-        m.add_batch(o, ml, n, lane);
-    }
-    m.store(p.out + (long long)r * p.o_sb + (long long)hq * p.o_sh, lane);
-}
-
 namespace {
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                  CUtensorMapFloatOOBfill);
-
-bool encode_bf16(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
-                 const cuuint64_t *strides_bytes, const cuuint32_t *box,
-                 CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
-    EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
-    if (!enc) return false;
-    const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
-               strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// [D, Hkv, rows, outer] view of a cache.  Box [D, HG, box_rows, 1] unswizzled, or, for the
-// swizzled layout, [64, 1, box_rows, 1] with the 128-byte swizzle (one column block).
-template <class C>
-bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv, long long rows, long long outer,
-                      int box_rows) {
-    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows, (cuuint64_t)outer};
-    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)rows * Hkv * D * 2};
-    if (C::SWZ) {
-        const cuuint32_t box[4] = {64u, 1u, (cuuint32_t)box_rows, 1u};
-        return encode_bf16(map, base, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
-    }
-    const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)C::HG, (cuuint32_t)box_rows, 1u};
-    return encode_bf16(map, base, 4, dims, strides, box);
-}
-
-// [D, Hq, B] view of q with its strides, box [D, hpu, 1].
-bool encode_q_map(CUtensorMap *map, const DecodeArgs &a, int hpu) {
-    const cuuint64_t dims[3] = {(cuuint64_t)a.D, (cuuint64_t)a.Hq, (cuuint64_t)a.B};
-    // a stride over an extent of 1 is never used; give TMA a valid one
-    const long long sh = a.Hq > 1 ? a.q_sh : a.D;
-    const long long sb = a.B > 1 ? a.q_sb : (long long)a.Hq * sh;
-    const cuuint64_t strides[2] = {(cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)a.D, (cuuint32_t)hpu, 1u};
-    return encode_bf16(map, a.q, 3, dims, strides, box);
-}
-
-int gcd_int(int x, int y) {
-    while (y) {
-        const int t = x % y;
-        x = y;
-        y = t;
-    }
-    return x;
-}
-
-std::mutex g_attr_mu;
-
-// Raise the dynamic shared-memory limit of `kern` once, and return its resident CTAs per SM.
-template <class K>
-int prepare_kernel(K kern, int threads, int smem, int *cached_occ) {
-    std::lock_guard<std::mutex> lock(g_attr_mu);
-    if (*cached_occ > 0) return *cached_occ;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem) != cudaSuccess) return 0;
-    *cached_occ = occ;
-    return occ;
-}
-
-template <class K, class... Args>
-cudaError_t launch_dependent(K kern, dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
-}
 
 template <class C, bool PAGED>
 dap_status launch_per_sequence(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
@@ -1772,89 +1137,7 @@ dap_status dispatch(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
     return run<MmaCfgFor<D, G>>(a, p, stream);
 }
 
-template <int D, int G>
-dap_status launch_multi(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
-    using C = MultiCfg<D, G>;
-    const int R = gcd_int(a.page_size, C::BT);
-    p.box_rows = R;
-    CUtensorMap mk, mv;
-    if (!encode_cache_map<C>(&mk, a.k, a.D, a.Hkv, a.page_size, a.num_pages, R) ||
-        !encode_cache_map<C>(&mv, a.v, a.D, a.Hkv, a.page_size, a.num_pages, R))
-        return DAP_ERR_CUDA;
-    auto kern = multi_kernel<C>;
-    static int occ = 0;
-    if (prepare_kernel(kern, C::THREADS, C::SMEM, &occ) <= 0) return DAP_ERR_CUDA;
-    const long long grid = (long long)a.num_tiles * a.Hkv * a.num_splits;
-    if (grid > 0x7FFFFFFFLL) return DAP_ERR_SHAPE;
-    p.o_part = static_cast<float *>(a.workspace);
-    p.ml_part = a.num_splits > 1 ? reinterpret_cast<float *>(static_cast<char *>(a.workspace) +
-                                                             partial_acc_bytes(a.total_q, a.Hq, a.D, a.num_splits))
-                                 : nullptr;
-    if (g_trace.split_begin) cudaEventRecord(g_trace.split_begin, stream);
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(mk, mv, p);
-    if (cudaGetLastError() != cudaSuccess) return DAP_ERR_CUDA;
-    if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
-    if (a.num_splits > 1) {
-        const dim3 cgrid((unsigned)(((long long)a.total_q * a.Hq + 7) / 8));
-        if (launch_dependent(combine_multi_kernel<D>, cgrid, dim3(256), stream, p, (int)C::QT) != cudaSuccess)
-            return DAP_ERR_CUDA;
-    }
-    if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);
-    return DAP_OK;
-}
-
-SplitParams make_params(const DecodeArgs &a) {
-    SplitParams p = {};
-    p.q = static_cast<const __nv_bfloat16 *>(a.q);
-    p.q_sb = a.q_sb;
-    p.q_sh = a.q_sh;
-    p.block_table = a.block_table;
-    p.max_pages = a.max_pages;
-    p.seq_lens = a.seq_lens;
-    p.max_kv_len = a.max_kv_len;
-    p.B = a.B;
-    p.Hq = a.Hq;
-    p.Hkv = a.Hkv;
-    p.page_size = a.paged ? a.page_size : a.max_len;
-    p.num_pages = a.paged ? a.num_pages : a.B;
-    p.num_splits = a.num_splits;
-    p.chunk = a.chunk;
-    p.qscale = a.scale * 1.4426950408889634f;
-    p.out = static_cast<__nv_bfloat16 *>(a.out);
-    p.o_sb = a.o_sb;
-    p.o_sh = a.o_sh;
-    p.qo_indptr = a.qo_indptr;
-    p.tile_batch = a.tile_batch;
-    p.tile_index = a.tile_index;
-    p.num_tiles = a.num_tiles;
-    p.total_q = a.total_q;
-    return p;
-}
-
 }  // namespace
-
-int multi_tokens_per_tile(int G) { return G >= 1 && G <= 16 ? 16 / G : 0; }
-
-dap_status launch_decode_multi(const DecodeArgs &a, cudaStream_t stream) {
-    SplitParams p = make_params(a);
-    const int G = a.Hq / a.Hkv;
-    if (a.D == 128) {
-        switch (G) {
-            case 1: return launch_multi<128, 1>(a, p, stream);
-            case 2: return launch_multi<128, 2>(a, p, stream);
-            case 4: return launch_multi<128, 4>(a, p, stream);
-            case 8: return launch_multi<128, 8>(a, p, stream);
-        }
-    } else if (a.D == 64) {
-        switch (G) {
-            case 1: return launch_multi<64, 1>(a, p, stream);
-            case 2: return launch_multi<64, 2>(a, p, stream);
-            case 4: return launch_multi<64, 4>(a, p, stream);
-            case 8: return launch_multi<64, 8>(a, p, stream);
-        }
-    }
-    return DAP_ERR_UNSUPPORTED;
-}
 
 int balanced_heads_per_unit(int D, int G) {
     (void)D;

@@ -92,6 +92,7 @@ dap_status launch_append_paged(const void *k_new, const void *v_new, void *k_cac
                                int Hkv, int D, cudaStream_t stream);
 dap_status launch_append_fp8(const void *rows, uint8_t *kv_cache, void *inv_scale, const int64_t *slots, int T,
                              int HD, int num_blocks, int block_size, cudaStream_t stream);
+bool read_errors_multi(unsigned int *flags, bool clear);
 bool read_errors_append(unsigned int *flags, bool clear);
 
 // Host readers of each translation unit's device error word (cudaMemcpyFromSymbol on the

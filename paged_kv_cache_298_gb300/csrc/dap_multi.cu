@@ -1,0 +1,532 @@
+// dap_multi.cu -- multi-token causal decode over the paged KV cache.
+//
+// Several new tokens per sequence (speculative-decoding verification, chunked short
+// prefill) attend the cache causally.  The tokens of all sequences are packed back to back
+// and cut into work tiles by the packed-q work map of the AstrAI "CUDA Kernels" doc
+// ("Q Scheduling and KV Addressing": qo_indptr, q_tile_to_batch, q_tile_to_index).  A
+// tile holds 16 / G tokens so that its tokens x the G heads of one kv head make 16 query
+// columns: the tensor-core N dimension, against which every K/V tile staged by TMA is
+// used once for all of the tile's tokens.  The producer warp and the stage ring are the
+// single-token per-sequence schedule's; the consumer adds a causal mask per column.
+#include "dap_tile.cuh"
+
+namespace dap {
+
+// ---- multi-token consumer ---------------------------------------------------------------
+// The query columns are (token, head) pairs: 16 columns = QT = 16 / G new tokens x G heads
+// of the kv head (two n8 tiles).  Per 16-key slice: S^T = K . Q^T for each n tile, a causal
+// mask per column (key position <= the column's token position), the online softmax per
+// column, movmatrix into the B operands and O^T += V^T . P^T.  q is read from global memory
+// (the per-sequence schedule gives each CTA one unit), and the four warps merge their
+// partial states in quarters of D.
+
+template <int D_, int G_>
+struct MultiCfg {
+    static constexpr int D = D_, G = G_, HG = 1, NWC = 4, BT = 64, NS = 3, MINB = 2;
+    static constexpr bool MMA = true, SWZ = true;
+    static constexpr int NT = 2;                    // n8 tiles of query columns
+    static constexpr int NCOL = 8 * NT;             // 16 columns
+    static constexpr int QT = NCOL / G;             // new tokens per work tile
+    static constexpr int WPH = NWC, KPW = BT / NWC;
+    static constexpr int ROWB = D * 2, HPU = G, NHALF = D / 64;
+    static constexpr int TILE_BYTES = BT * ROWB;
+    static constexpr int QBYTES = 0;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int NPART = 4;                 // merge in quarters of D
+    static constexpr int MRG_OFF = NS * STAGE_BYTES;
+    static constexpr int MRG_BYTES = NWC * NCOL * (D / NPART + 2) * 4;
+    static constexpr int HDR_OFF = MRG_OFF + MRG_BYTES;
+    static constexpr int HDR_INTS = 8;
+    static constexpr int MISC_OFF = HDR_OFF + NS * HDR_INTS * 4;
+    static constexpr int BAR_OFF = (MISC_OFF + 16 + 7) & ~7;
+    static constexpr int SMEM = BAR_OFF + (2 * NS + 1) * 8 + 1024;
+    static constexpr int THREADS = (NWC + 1) * 32;
+    static_assert(KPW == 16 && NCOL % G == 0 && STAGE_BYTES % 1024 == 0, "multi-token tiling");
+};
+
+template <class C>
+struct MultiConsumer {
+    static constexpr int D = C::D, G = C::G, KS = D / 16, NT = C::NT;
+    uint32_t qb[KS][NT][2];
+    float acc[KS][NT][4];
+    float m_run[NT][2], l_run[NT][2];
+    float qscale;
+    int warp, lane, g, t, key0, nq, p_base;
+    static constexpr int hh = 0;
+
+    __device__ __forceinline__ void init(int w, int l, uint8_t *) {
+        warp = w;
+        lane = l;
+        g = l >> 2;
+        t = l & 3;
+        key0 = w * C::KPW;
+    }
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                m_run[n][j] = -INFINITY;
+                l_run[n][j] = 0.f;
+            }
+#pragma unroll
+        for (int m = 0; m < KS; ++m)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[m][n][j] = 0.f;
+    }
+
+    // q of the tile's tokens: token i, head h at base + i * tstride + h * hstride
+    __device__ __forceinline__ void load_q(const __nv_bfloat16 *base, long long tstride, long long hstride,
+                                           int ntok, int pos0, float qs) {
+        qscale = qs;
+        nq = ntok;
+        p_base = pos0;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int c = n * 8 + g;
+            const int ti = c / G, hc = c % G;
+#pragma unroll
+            for (int k = 0; k < KS; ++k) {
+                if (ti < ntok) {
+                    const __nv_bfloat16 *r = base + ti * tstride + hc * hstride + 16 * k + 2 * t;
+                    qb[k][n][0] = *reinterpret_cast<const uint32_t *>(r);
+                    qb[k][n][1] = *reinterpret_cast<const uint32_t *>(r + 8);
+                } else {
+                    qb[k][n][0] = qb[k][n][1] = 0u;
+                }
+            }
+        }
+    }
+
+    static __device__ __forceinline__ uint32_t off(int key, int dim) {
+        const int chunk = (dim & 63) >> 3;
+        return (uint32_t)((dim >> 6) * (C::BT * 128) + key * 128 + ((chunk ^ (key & 7)) << 4));
+    }
+
+    // tile_pos: absolute position of the tile's first key
+    __device__ __forceinline__ void tile(uint8_t *stage, int nvalid, int tile_pos) {
+        const int nv = nvalid - key0;
+        if (nv <= 0) return;
+        uint8_t *sV = stage + C::TILE_BYTES;
+        if (nv < 16) {
+            for (int i = lane; i < (16 - nv) * C::NHALF * 8; i += 32) {
+                const int row = key0 + nv + i / (C::NHALF * 8);
+                const int rest = i % (C::NHALF * 8);
+                *reinterpret_cast<uint4 *>(sV + (rest >> 3) * (C::BT * 128) + row * 128 + (rest & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+        const uint32_t kbase = smem_addr(stage), vbase = smem_addr(sV);
+        float c[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) c[n][j] = 0.f;
+        {
+            const int key = key0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int dcol = ((lane >> 4) & 1) * 8;
+#pragma unroll
+            for (int k = 0; k < KS; ++k) {
+                uint32_t a[4];
+                ldmatrix_x4(a, kbase + off(key, 16 * k + dcol));
+#pragma unroll
+                for (int n = 0; n < NT; ++n) mma_bf16_16816(c[n], a, qb[k][n][0], qb[k][n][1]);
+            }
+        }
+        const int kpos0 = tile_pos + key0 + g, kpos1 = kpos0 + 8;  // absolute key positions
+        uint32_t b0[NT], b1[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            float s[4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int col = n * 8 + 2 * t + j;
+                const int ti = col / G;
+                const int lim = p_base + ti;  // this column's token sees keys <= lim
+                const bool col_ok = ti < nq;
+                s[j] = (col_ok && g < nv && kpos0 <= lim) ? c[n][j] * qscale : -INFINITY;
+                s[j + 2] = (col_ok && g + 8 < nv && kpos1 <= lim) ? c[n][j + 2] * qscale : -INFINITY;
+            }
+            float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xFFFFFFFFu, mx[0], o));
+                mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xFFFFFFFFu, mx[1], o));
+            }
+            float alpha[2], mu[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float m_new = fmaxf(m_run[n][j], mx[j]);
+                mu[j] = (m_new == -INFINITY) ? 0.f : m_new;
+                alpha[j] = ex2(m_run[n][j] - mu[j]);
+                m_run[n][j] = m_new;
+            }
+            const uint32_t w0 = pack_bf16x2(ex2(s[0] - mu[0]), ex2(s[1] - mu[1]));
+            const uint32_t w1 = pack_bf16x2(ex2(s[2] - mu[0]), ex2(s[3] - mu[1]));
+            const float2 p0 = bf16x2_to_float2(w0), p1 = bf16x2_to_float2(w1);
+            l_run[n][0] = l_run[n][0] * alpha[0] + (p0.x + p1.x);
+            l_run[n][1] = l_run[n][1] * alpha[1] + (p0.y + p1.y);
+#pragma unroll
+            for (int m = 0; m < KS; ++m) {
+                acc[m][n][0] *= alpha[0];
+                acc[m][n][1] *= alpha[1];
+                acc[m][n][2] *= alpha[0];
+                acc[m][n][3] *= alpha[1];
+            }
+            b0[n] = movmatrix_trans(w0);
+            b1[n] = movmatrix_trans(w1);
+        }
+        {
+            const int key = key0 + (lane & 7) + ((lane >> 4) & 1) * 8;
+            const int dcol = ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int m = 0; m < KS; ++m) {
+                uint32_t a[4];
+                ldmatrix_x4_trans(a, vbase + off(key, 16 * m + dcol));
+#pragma unroll
+                for (int n = 0; n < NT; ++n) mma_bf16_16816(acc[m][n], a, b0[n], b1[n]);
+            }
+        }
+    }
+
+    // merge the four warps per column in C::NPART parts of D; emit(col, d, a0, a1, M, l)
+    template <class Sync, class Emit>
+    __device__ __forceinline__ bool finish(float *mrg, Sync sync, Emit emit) {
+        constexpr int NWC = C::NWC, NC = C::NCOL, DP = D / C::NPART, MP = KS / C::NPART;
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                l_run[n][0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[n][0], o);
+                l_run[n][1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[n][1], o);
+            }
+        float *macc = mrg;               // [NWC][NC][DP]
+        float *mml = mrg + NWC * NC * DP;  // [NWC][NC][2]
+        if (g == 0) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    mml[(warp * NC + n * 8 + 2 * t + j) * 2 + 0] = m_run[n][j];
+                    mml[(warp * NC + n * 8 + 2 * t + j) * 2 + 1] = l_run[n][j];
+                }
+        }
+        const int tid = warp * 32 + lane;
+#pragma unroll
+        for (int part = 0; part < C::NPART; ++part) {
+#pragma unroll
+            for (int m = part * MP; m < (part + 1) * MP; ++m) {
+                const int d = 16 * m + g - part * DP;
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        float *row = macc + (warp * NC + n * 8 + 2 * t + j) * DP;
+                        row[d] = acc[m][n][j];
+                        row[d + 8] = acc[m][n][j + 2];
+                    }
+            }
+            if (!sync()) return false;
+            for (int e = tid * 2; e < NC * DP; e += NWC * 32 * 2) {
+                const int col = e / DP, dd = e % DP;
+                if (col / G < nq) {
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int w = 0; w < NWC; ++w) M = fmaxf(M, mml[(w * NC + col) * 2]);
+                    const float Mu = (M == -INFINITY) ? 0.f : M;
+                    float a0 = 0.f, a1 = 0.f, lv = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NWC; ++w) {
+                        const float f = ex2(mml[(w * NC + col) * 2] - Mu);
+                        lv = fmaf(f, mml[(w * NC + col) * 2 + 1], lv);
+                        const float2 x = *reinterpret_cast<const float2 *>(macc + (w * NC + col) * DP + dd);
+                        a0 = fmaf(f, x.x, a0);
+                        a1 = fmaf(f, x.y, a1);
+                    }
+                    emit(col, part * DP + dd, a0, a1, M, lv);
+                }
+            }
+            if (!sync()) return false;
+        }
+        return true;
+    }
+};
+
+// ---- multi-token decode: one CTA per (q tile, kv head, split) ----------------------------
+// The packed-q work map (AstrAI "CUDA Kernels" doc, "Q Scheduling and KV Addressing"): q
+// holds the new tokens of all sequences back to back, qo_indptr is the prefix sum of their
+// counts, and work tile w covers tokens [tile_index[w] * QT, +QT) of sequence tile_batch[w].
+// Token i of a sequence with q_len new tokens and L cached keys (the new ones included)
+// sits at position L - q_len + i and attends keys 0 .. that position.  The tile's KV range
+// ends after its last token's position and is cut into chunks of p.chunk keys.
+
+struct MultiTile {
+    int b, q0, qlen, i0, ntok, pos0, kv_end;
+};
+
+// The tile's sequence, tokens and KV range; false for a work-map entry that names no token
+// (flagged).  Shared by the attention kernel and its combine so both agree on the splits.
+__device__ __forceinline__ bool multi_tile(const SplitParams &p, int b, int tindex, int qt, bool report,
+                                           MultiTile *t) {
+    if (b < 0 || b >= p.B) {
+        if (report) flag_error(DAP_DEVERR_QMAP);
+        return false;
+    }
+    t->b = b;
+    t->q0 = p.qo_indptr[b];
+    t->qlen = p.qo_indptr[b + 1] - t->q0;
+    t->i0 = tindex * qt;
+    t->ntok = min(qt, t->qlen - t->i0);
+    if (tindex < 0 || t->ntok <= 0 || t->q0 < 0 || t->q0 + t->qlen > p.total_q) {
+        if (report) flag_error(DAP_DEVERR_QMAP);
+        return false;
+    }
+    int L = p.seq_lens[b];
+    if (L < 0 || L > p.max_kv_len || t->qlen > L) {
+        if (report) flag_error(DAP_DEVERR_SEQLEN);
+        L = min(max(L, 0), p.max_kv_len);
+    }
+    t->pos0 = L - t->qlen + t->i0;  // negative for tokens that would sit before the cache start
+    t->kv_end = max(0, t->pos0 + t->ntok);
+    return true;
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, C::MINB)
+    multi_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                 const SplitParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = aligned_smem<C>(smem_raw);
+    constexpr int G = C::G, NWC = C::NWC, BT = C::BT, NS = C::NS, D = C::D;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int units = p.num_tiles * p.Hkv;
+    const int s = blockIdx.x / units;
+    const int rem = blockIdx.x - s * units;
+    const int w = rem / p.Hkv;
+    const int kvh = rem - w * p.Hkv;
+    MultiTile tl;
+    if (!multi_tile(p, p.tile_batch[w], p.tile_index[w], C::QT, threadIdx.x == 0 && s == 0 && kvh == 0, &tl))
+        return;
+    const int nsplit = max(1, (tl.kv_end + p.chunk - 1) / p.chunk);
+    if (s >= nsplit) return;
+    const int tok0 = s * p.chunk;
+    const int tok1 = min(tl.kv_end, tok0 + p.chunk);
+    const int ntiles = tok1 > tok0 ? (tok1 - tok0 + BT - 1) / BT : 0;
+
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *empty = full + NS;
+    int *misc = reinterpret_cast<int *>(smem + C::MISC_OFF);  // [0] tiles issued, [1] abort
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NWC);
+        }
+        misc[0] = 0;
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == NWC) {  // ---- producer warp: page lookup + TMA issue (as in split_kernel)
+        if (lane == 0) {
+            prefetch_tensormap(&mapK);
+            prefetch_tensormap(&mapV);
+        }
+        const int R = p.box_rows;
+        const int32_t *table = p.block_table + (long long)tl.b * p.max_pages;
+        auto lookup = [&](int tile) -> int {
+            const int t = tok0 + tile * BT + lane * R;
+            if (lane * R >= BT || t >= tok1) return 0;
+            int pg = __ldg(table + t / p.page_size);
+            if (pg < 0 || pg >= p.num_pages) {
+                flag_error(DAP_DEVERR_PAGE);
+                pg = 0;
+            }
+            return pg;
+        };
+        int pg_next = ntiles > 0 ? lookup(0) : 0;
+        int issued = 0;
+        for (int i = 0; i < ntiles; ++i) {
+            const int st = i % NS;
+            const int pg = pg_next;
+            if (i + 1 < ntiles) pg_next = lookup(i + 1);
+            if (i >= NS && !__all_sync(0xFFFFFFFFu, mbar_wait(&empty[st], ((i / NS) - 1) & 1))) {
+                misc[1] = 1;
+                break;
+            }
+            const int t = tok0 + i * BT;
+            const int nvalid = min(BT, tok1 - t);
+            const int nbox = (nvalid + R - 1) / R;
+            const uint32_t bytes = (uint32_t)(nbox * R * C::ROWB * 2);
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
+            __syncwarp();
+            if (lane < nbox) {
+                const int tt = t + lane * R;
+                issue_kv_box<C>(smem + st * C::STAGE_BYTES, lane, R, &mapK, &mapV, kvh, tt % p.page_size, pg,
+                                &full[st]);
+            }
+            issued = i + 1;
+        }
+        if (lane == 0) misc[0] = issued;
+        __syncthreads();
+        return;
+    }
+
+    // ---- consumer warps
+    MultiConsumer<C> cs;
+    cs.init(warp, lane, smem);
+    cs.reset();
+    cs.load_q(p.q + (long long)(tl.q0 + tl.i0) * p.q_sb + (long long)kvh * G * p.q_sh, p.q_sb, p.q_sh, tl.ntok,
+              tl.pos0, p.qscale);
+    int consumed = 0;
+    for (int i = 0; i < ntiles; ++i) {
+        const int st = i % NS;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (i / NS) & 1))) {
+            misc[1] = 1;
+            break;
+        }
+        const int t = tok0 + i * BT;
+        cs.tile(smem + st * C::STAGE_BYTES, min(BT, tok1 - t), t);
+        if (lane == 0) mbar_arrive(&empty[st]);
+        consumed = i + 1;
+    }
+    __syncthreads();
+    if (misc[1]) {
+        if (threadIdx.x == 0)
+            for (int i = consumed; i < misc[0]; ++i) (void)mbar_wait(&full[i % NS], (i / NS) & 1);
+        return;
+    }
+    const bool direct = (nsplit == 1);
+    const int r0 = tl.q0 + tl.i0;
+    cs.finish(reinterpret_cast<float *>(smem + C::MRG_OFF), [] { named_sync(1, NWC * 32); return true; },
+              [&](int col, int d, float a0, float a1, float M, float lv) {
+                  const long long r = r0 + col / G;
+                  const int hq = kvh * G + col % G;
+                  if (direct) {
+                      store_out_pair(p.out + r * p.o_sb + (long long)hq * p.o_sh + d, a0, a1, lv);
+                  } else {
+                      const long long row = (r * p.num_splits + s) * p.Hq + hq;
+                      *reinterpret_cast<float2 *>(p.o_part + row * D + d) = make_float2(a0, a1);
+                      if (d == 0) *reinterpret_cast<float2 *>(p.ml_part + row * 2) = make_float2(M, lv);
+                  }
+              });
+}
+
+// Merge the split partials of every (token, head) row, one warp per row.  The row's
+// sequence is found by binary search of qo_indptr; the split count follows from the row's
+// tile exactly as in multi_kernel.
+template <int D>
+__global__ void __launch_bounds__(256) combine_multi_kernel(const SplitParams p, int qt) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= p.total_q * p.Hq) return;
+    const int r = gw / p.Hq, hq = gw - r * p.Hq;
+    int lo = 0, hi = p.B;  // qo_indptr[lo] <= r < qo_indptr[hi] for a well-formed map
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.qo_indptr[mid] <= r) lo = mid;
+        else hi = mid;
+    }
+    MultiTile tl;
+    if (!multi_tile(p, lo, (r - p.qo_indptr[lo]) / qt, qt, false, &tl)) return;
+    const int nsplit = max(1, (tl.kv_end + p.chunk - 1) / p.chunk);
+    if (nsplit == 1) return;
+    const long long row0 = (long long)r * p.num_splits * p.Hq + hq;
+    float M = -INFINITY;
+    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, p.ml_part[(row0 + (long long)s * p.Hq) * 2]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    RowMerge<D> m;
+    m.begin(M);
+    for (int s0 = 0; s0 < nsplit; s0 += 8) {
+        const float *o[8];
+        float2 ml[8];
+        const int n = min(8, nsplit - s0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const long long row = row0 + (long long)min(s0 + k, nsplit - 1) * p.Hq;
+            o[k] = p.o_part + row * D;
+            ml[k] = *reinterpret_cast<const float2 *>(p.ml_part + row * 2);
+        }
+        m.add_batch(o, ml, n, lane);
+    }
+    m.store(p.out + (long long)r * p.o_sb + (long long)hq * p.o_sh, lane);
+}
+
+namespace {
+
+template <int D, int G>
+dap_status launch_multi(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
+    using C = MultiCfg<D, G>;
+    const int R = gcd_int(a.page_size, C::BT);
+    p.box_rows = R;
+    CUtensorMap mk, mv;
+    if (!encode_cache_map<C>(&mk, a.k, a.D, a.Hkv, a.page_size, a.num_pages, R) ||
+        !encode_cache_map<C>(&mv, a.v, a.D, a.Hkv, a.page_size, a.num_pages, R))
+        return DAP_ERR_CUDA;
+    auto kern = multi_kernel<C>;
+    static int occ = 0;
+    if (prepare_kernel(kern, C::THREADS, C::SMEM, &occ) <= 0) return DAP_ERR_CUDA;
+    const long long grid = (long long)a.num_tiles * a.Hkv * a.num_splits;
+    if (grid > 0x7FFFFFFFLL) return DAP_ERR_SHAPE;
+    p.o_part = static_cast<float *>(a.workspace);
+    p.ml_part = a.num_splits > 1 ? reinterpret_cast<float *>(static_cast<char *>(a.workspace) +
+                                                             partial_acc_bytes(a.total_q, a.Hq, a.D, a.num_splits))
+                                 : nullptr;
+    if (g_trace.split_begin) cudaEventRecord(g_trace.split_begin, stream);
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(mk, mv, p);
+    if (cudaGetLastError() != cudaSuccess) return DAP_ERR_CUDA;
+    if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
+    if (a.num_splits > 1) {
+        const dim3 cgrid((unsigned)(((long long)a.total_q * a.Hq + 7) / 8));
+        if (launch_dependent(combine_multi_kernel<D>, cgrid, dim3(256), stream, p, (int)C::QT) != cudaSuccess)
+            return DAP_ERR_CUDA;
+    }
+    if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);
+    return DAP_OK;
+}
+
+}  // namespace
+
+int multi_tokens_per_tile(int G) { return G >= 1 && G <= 16 ? 16 / G : 0; }
+
+dap_status launch_decode_multi(const DecodeArgs &a, cudaStream_t stream) {
+    SplitParams p = make_params(a);
+    const int G = a.Hq / a.Hkv;
+    if (a.D == 128) {
+        switch (G) {
+            case 1: return launch_multi<128, 1>(a, p, stream);
+            case 2: return launch_multi<128, 2>(a, p, stream);
+            case 4: return launch_multi<128, 4>(a, p, stream);
+            case 8: return launch_multi<128, 8>(a, p, stream);
+        }
+    } else if (a.D == 64) {
+        switch (G) {
+            case 1: return launch_multi<64, 1>(a, p, stream);
+            case 2: return launch_multi<64, 2>(a, p, stream);
+            case 4: return launch_multi<64, 4>(a, p, stream);
+            case 8: return launch_multi<64, 8>(a, p, stream);
+        }
+    }
+    return DAP_ERR_UNSUPPORTED;
+}
+
+bool read_errors_multi(unsigned int *flags, bool clear) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_errors, sizeof v) != cudaSuccess) return false;
+    if (clear) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(g_device_errors, &z, sizeof z) != cudaSuccess) return false;
+    }
+    *flags |= v;
+    return true;
+}
+
+}  // namespace dap

@@ -1,0 +1,242 @@
+// dap_tile.cuh -- pieces shared by the bf16 paged decode kernels: the single-token
+// schedules (dap_decode.cu) and the multi-token one (dap_multi.cu).  Launch parameters,
+// the shared-memory alignment rule of the swizzled tiles, the TMA issue of one K/V box,
+// the consumer-warp barrier, the normalised bf16 store, the row merge of split partials
+// and the host-side tensor-map encoding and launch helpers.
+#pragma once
+
+#include <math.h>
+
+#include <mutex>
+#include <type_traits>
+
+#include "dap_device.cuh"
+#include "dap_internal.h"
+
+namespace dap {
+
+struct SplitParams {
+    const __nv_bfloat16 *q;
+    long long q_sb, q_sh;
+    const int32_t *block_table;
+    int max_pages;
+    const int32_t *seq_lens;
+    int max_kv_len;
+    int B, Hq, Hkv;
+    int page_size, num_pages, box_rows;
+    int num_splits, chunk;  // per-sequence schedule
+    int num_ctas;           // balanced schedule: P
+    float qscale;           // scale * log2(e)
+    float *o_part;
+    float *ml_part;
+    int *unit_info;         // balanced: [units][2] = first tile, tiles
+    long long *total_tiles; // balanced: T
+    __nv_bfloat16 *out;
+    long long o_sb, o_sh;
+    // multi-token decode: packed q / out rows are tokens; q_sb / o_sb are the token strides
+    const int32_t *qo_indptr, *tile_batch, *tile_index;
+    int num_tiles, total_q;
+};
+
+__device__ __forceinline__ void store_out_pair(__nv_bfloat16 *o, float a0, float a1, float l) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    *reinterpret_cast<__nv_bfloat162 *>(o) = __floats2bfloat162_rn(a0 * inv, a1 * inv);
+}
+
+// 1024-byte aligned view of the dynamic shared memory (the 128-byte swizzle is a function
+// of address bits 4..9, so swizzled tiles must start on 1024-byte boundaries).
+template <class C>
+__device__ __forceinline__ uint8_t *aligned_smem(uint8_t *raw) {
+    if constexpr (C::SWZ) return raw + ((1024u - (smem_addr(raw) & 1023u)) & 1023u);
+    return raw;
+}
+
+// Barrier among the NWC consumer warps on an mbarrier (count NWC, one arrival per warp),
+// so that a wait is bounded like every other wait in the pipeline.
+struct ConsumerBarrier {
+    uint64_t *bar;
+    uint32_t phase;
+    __device__ __forceinline__ bool sync(int lane) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
+        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar, phase & 1));
+        ++phase;
+        return ok;
+    }
+};
+
+// The K and V boxes of one producer lane: box j of the stage covers tile rows
+// [j*R, (j+1)*R).  Swizzled configurations split every row into 128-byte column blocks.
+template <class C>
+__device__ __forceinline__ void issue_kv_box(uint8_t *stage, int j, int R, const CUtensorMap *mk,
+                                             const CUtensorMap *mv, int kvh0, int row, int page, uint64_t *bar) {
+    if constexpr (C::SWZ) {
+#pragma unroll
+        for (int h = 0; h < C::NHALF; ++h) {
+            uint8_t *dst = stage + h * (C::BT * 128) + j * R * 128;
+            tma_load_4d(dst, mk, 64 * h, kvh0, row, page, bar);
+            tma_load_4d(dst + C::TILE_BYTES, mv, 64 * h, kvh0, row, page, bar);
+        }
+    } else {
+        uint8_t *dst = stage + j * R * C::HG * C::ROWB;
+        tma_load_4d(dst, mk, 0, kvh0, row, page, bar);
+        tma_load_4d(dst + C::TILE_BYTES, mv, 0, kvh0, row, page, bar);
+    }
+}
+
+// Merge of split partials for one output row, one warp, lanes over D: M = max_s m_s,
+// out = sum_s 2^(m_s-M) acc_s / sum_s 2^(m_s-M) l_s (AstrAI csrc log, split-KV commit: the
+// combine kernel; numerics commit: guarded division).
+template <int D>
+struct RowMerge {
+    static constexpr int DPV = D / 32;
+    using Vec = typename std::conditional<DPV == 4, float4, float2>::type;
+    float acc[DPV];
+    float lsum, Mu;
+    __device__ __forceinline__ void begin(float m_max) {
+        Mu = (m_max == -INFINITY) ? 0.f : m_max;
+        lsum = 0.f;
+#pragma unroll
+        for (int j = 0; j < DPV; ++j) acc[j] = 0.f;
+    }
+    // add the partial rows o[0..n) (n <= 8), whose loads are all issued before any use
+    __device__ __forceinline__ void add_batch(const float *const *o, const float2 *ml, int n, int lane) {
+        Vec x[8];
+        float f[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (k < n) {
+                x[k] = *reinterpret_cast<const Vec *>(o[k] + lane * DPV);
+                f[k] = ex2(ml[k].x - Mu);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (k < n) {
+                lsum = fmaf(f[k], ml[k].y, lsum);
+                const float *xv = reinterpret_cast<const float *>(&x[k]);
+#pragma unroll
+                for (int j = 0; j < DPV; ++j) acc[j] = fmaf(f[k], xv[j], acc[j]);
+            }
+        }
+    }
+    __device__ __forceinline__ void store(__nv_bfloat16 *o, int lane) {
+#pragma unroll
+        for (int j = 0; j < DPV; j += 2) store_out_pair(o + lane * DPV + j, acc[j], acc[j + 1], lsum);
+    }
+};
+
+// ---- host side ----------------------------------------------------------------------------
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+bool encode_bf16(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+                 const cuuint64_t *strides_bytes, const cuuint32_t *box,
+                 CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
+    EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+    if (!enc) return false;
+    const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), dims,
+               strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [D, Hkv, rows, outer] view of a cache.  Box [D, HG, box_rows, 1] unswizzled, or, for the
+// swizzled layout, [64, 1, box_rows, 1] with the 128-byte swizzle (one column block).
+template <class C>
+bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv, long long rows, long long outer,
+                      int box_rows) {
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows, (cuuint64_t)outer};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)rows * Hkv * D * 2};
+    if (C::SWZ) {
+        const cuuint32_t box[4] = {64u, 1u, (cuuint32_t)box_rows, 1u};
+        return encode_bf16(map, base, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)C::HG, (cuuint32_t)box_rows, 1u};
+    return encode_bf16(map, base, 4, dims, strides, box);
+}
+
+// [D, Hq, B] view of q with its strides, box [D, hpu, 1].
+bool encode_q_map(CUtensorMap *map, const DecodeArgs &a, int hpu) {
+    const cuuint64_t dims[3] = {(cuuint64_t)a.D, (cuuint64_t)a.Hq, (cuuint64_t)a.B};
+    // a stride over an extent of 1 is never used; give TMA a valid one
+    const long long sh = a.Hq > 1 ? a.q_sh : a.D;
+    const long long sb = a.B > 1 ? a.q_sb : (long long)a.Hq * sh;
+    const cuuint64_t strides[2] = {(cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)a.D, (cuuint32_t)hpu, 1u};
+    return encode_bf16(map, a.q, 3, dims, strides, box);
+}
+
+int gcd_int(int x, int y) {
+    while (y) {
+        const int t = x % y;
+        x = y;
+        y = t;
+    }
+    return x;
+}
+
+std::mutex g_attr_mu;
+
+// Raise the dynamic shared-memory limit of `kern` once, and return its resident CTAs per SM.
+template <class K>
+int prepare_kernel(K kern, int threads, int smem, int *cached_occ) {
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    if (*cached_occ > 0) return *cached_occ;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem) != cudaSuccess) return 0;
+    *cached_occ = occ;
+    return occ;
+}
+
+template <class K, class... Args>
+cudaError_t launch_dependent(K kern, dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+SplitParams make_params(const DecodeArgs &a) {
+    SplitParams p = {};
+    p.q = static_cast<const __nv_bfloat16 *>(a.q);
+    p.q_sb = a.q_sb;
+    p.q_sh = a.q_sh;
+    p.block_table = a.block_table;
+    p.max_pages = a.max_pages;
+    p.seq_lens = a.seq_lens;
+    p.max_kv_len = a.max_kv_len;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.page_size = a.paged ? a.page_size : a.max_len;
+    p.num_pages = a.paged ? a.num_pages : a.B;
+    p.num_splits = a.num_splits;
+    p.chunk = a.chunk;
+    p.qscale = a.scale * 1.4426950408889634f;
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
+    p.o_sb = a.o_sb;
+    p.o_sh = a.o_sh;
+    p.qo_indptr = a.qo_indptr;
+    p.tile_batch = a.tile_batch;
+    p.tile_index = a.tile_index;
+    p.num_tiles = a.num_tiles;
+    p.total_q = a.total_q;
+    return p;
+}
+
+}  // namespace
+}  // namespace dap
