@@ -108,7 +108,7 @@ size_t dap_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits);
  *   v_cache      t of sequence b lives in page block_table[b, t / page_size], slot
  *                t % page_size.
  *   block_table  device int32 [B, max_pages], row-major.  Entries past a sequence's
- *                last page are never read.
+ *                last page are never used (they may be read, within the table).
  *   seq_lens     device int32 [B].  Each entry must lie in [0, max_kv_len].
  *   max_kv_len   host: an upper bound of seq_lens (<= max_pages * page_size); it sets
  *                the chunk length of the split plan.

@@ -83,6 +83,10 @@ def _load():
         lib.oracle_decode_paged_multi.restype = I
         lib.oracle_q_tile_map.argtypes = [P, I, I, P, P, P, I]
         lib.oracle_q_tile_map.restype = I
+        lib.oracle_decode_paged_fp8kv.argtypes = [P, LL, LL, P, P, P, P, I, P, I, P, I, I, I, I, I, D, P]
+        lib.oracle_decode_paged_fp8kv.restype = I
+        lib.oracle_kv_append_paged_fp8.argtypes = [P, P, P, P, P, P, I, I, P, I, P, I, I, I]
+        lib.oracle_kv_append_paged_fp8.restype = I
         _lib = lib
         return lib
 
@@ -259,3 +263,43 @@ def q_tile_map(q_lens, tokens_per_tile: int):
     ti = np.zeros(cap, np.int32)
     n = _load().oracle_q_tile_map(_ptr(ql), B, int(tokens_per_tile), _ptr(qi), _ptr(tb), _ptr(ti), cap)
     return qi, tb[:n], ti[:n]
+
+
+def decode_paged_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens, scale: float) -> np.ndarray:
+    """Paged GQA decode over an e4m3 cache: codes [P, ps, Hkv, D] uint8, factors
+    [P, Hkv, ps] bf16 bits (uint16); K = e4m3(code) * factor exactly.  q [B, Hq, D] u16.
+    Returns float64 [B, Hq, D]."""
+    q = _u16(q)
+    kc = np.ascontiguousarray(k_codes, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
+    ks = _u16(k_scale)
+    vs = _u16(v_scale)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, D = q.shape
+    P, ps, Hkv, _ = kc.shape
+    assert ks.shape == (P, Hkv, ps) and vs.shape == (P, Hkv, ps) and vc.shape == kc.shape
+    out = np.empty((B, Hq, D), dtype=np.float64)
+    bad = _load().oracle_decode_paged_fp8kv(_ptr(q), Hq * D, D, _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), P, _ptr(bt),
+                                            bt.shape[1], _ptr(sl), B, Hq, Hkv, D, ps, float(scale), _ptr(out))
+    if bad:
+        raise ValueError(f"{bad} output rows would read outside the given cache/table")
+    return out
+
+
+def kv_append_paged_fp8(k_new, v_new, k_codes, v_codes, k_scale, v_scale, block_table, pos):
+    """Quantise k_new / v_new [B, Hkv, D] (u16 bits) into the e4m3 GQA cache at pos[b]; the
+    code arrays and factor arrays are updated in place (numpy).  Returns rows skipped."""
+    kn = _u16(k_new)
+    vn = _u16(v_new)
+    for a in (k_codes, v_codes):
+        assert a.dtype == np.uint8 and a.flags.c_contiguous
+    for a in (k_scale, v_scale):
+        assert a.dtype == np.uint16 and a.flags.c_contiguous
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    ps_ = np.ascontiguousarray(pos, dtype=np.int32)
+    B, Hkv, D = kn.shape
+    P, page_size = k_codes.shape[0], k_codes.shape[1]
+    return _load().oracle_kv_append_paged_fp8(_ptr(kn), _ptr(vn), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
+                                              _ptr(v_scale), P, page_size, _ptr(bt), bt.shape[1], _ptr(ps_), B,
+                                              Hkv, D)

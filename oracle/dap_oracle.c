@@ -453,3 +453,123 @@ int oracle_q_tile_map(const int32_t *q_lens, int B, int tokens_per_tile, int32_t
     }
     return n;
 }
+
+/* ---- paged GQA decode over an fp8 cache ------------------------------------------------ */
+
+/* The GQA decode above with K and V held as OCP e4m3 codes and one dequantisation factor
+ * per (slot, kv head) for each (the fp8 cache convention of nvfp4-megamoe-kernel
+ * native_swa_decode.py, applied to the GQA cache: the decoded value is the code's value
+ * times the bf16 factor):
+ *   K[b, t, kh, d] = e4m3(k_codes[page, slot, kh, d]) * bf16(k_scale[page, kh, slot]),
+ *   page = block_table[b][t / ps], slot = t % ps, likewise V with v_codes and v_scale;
+ * the product is taken exactly (in double).  Codes are [num_pages, ps, Hkv, D] bytes;
+ * the factors [num_pages, Hkv, ps] bf16 bits.  Then s_t = scale * q . K_t and
+ * out = sum_t softmax(s)_t V_t as in oracle_decode_paged (zero row for an empty sequence).
+ * Returns the number of rows that failed the bounds checks (left NaN). */
+static int paged_row_fp8kv(const uint16_t *q, long long q_stride_b, long long q_stride_h,
+                           const uint8_t *k_codes, const uint8_t *v_codes, const uint16_t *k_scale,
+                           const uint16_t *v_scale, int num_pages, const int32_t *block_table,
+                           int max_pages, const int32_t *seq_lens, int Hq, int Hkv, int D,
+                           int page_size, double scale, int b, int h, double *out) {
+    int G = Hq / Hkv, kh = h / G, L = seq_lens[b], t, d;
+    double *qd, *s, *vrow, mx = -INFINITY, z = 0.0;
+    long long *rowoff, *scaleoff;
+    if (L < 0 || (long long)L > (long long)max_pages * page_size) return -1;
+    for (t = 0; t < L; ++t) {
+        int32_t page = block_table[(long long)b * max_pages + t / page_size];
+        if (page < 0 || page >= num_pages) return -1;
+    }
+    for (d = 0; d < D; ++d) out[d] = 0.0;
+    if (L == 0) return 0;
+    qd = (double *)malloc(sizeof(double) * (size_t)D);
+    vrow = (double *)malloc(sizeof(double) * (size_t)D);
+    s = (double *)malloc(sizeof(double) * (size_t)L);
+    rowoff = (long long *)malloc(sizeof(long long) * (size_t)L);
+    scaleoff = (long long *)malloc(sizeof(long long) * (size_t)L);
+    for (d = 0; d < D; ++d) qd[d] = oracle_bf16_value(q[b * q_stride_b + h * q_stride_h + d]);
+    for (t = 0; t < L; ++t) {
+        long long page = block_table[(long long)b * max_pages + t / page_size];
+        int slot = t % page_size;
+        rowoff[t] = ((page * page_size + slot) * Hkv + kh) * D;
+        scaleoff[t] = (page * Hkv + kh) * page_size + slot;
+    }
+    for (t = 0; t < L; ++t) {
+        double ks = oracle_bf16_value(k_scale[scaleoff[t]]), dot = 0.0;
+        for (d = 0; d < D; ++d) dot += qd[d] * (oracle_e4m3_value(k_codes[rowoff[t] + d]) * ks);
+        s[t] = scale * dot;
+        if (s[t] > mx) mx = s[t];
+    }
+    for (t = 0; t < L; ++t) {
+        double w = exp(s[t] - mx), vs = oracle_bf16_value(v_scale[scaleoff[t]]);
+        z += w;
+        for (d = 0; d < D; ++d) vrow[d] = oracle_e4m3_value(v_codes[rowoff[t] + d]) * vs;
+        for (d = 0; d < D; ++d) out[d] += w * vrow[d];
+    }
+    for (d = 0; d < D; ++d) out[d] /= z;
+    free(qd); free(vrow); free(s); free(rowoff); free(scaleoff);
+    return 0;
+}
+
+int oracle_decode_paged_fp8kv(const uint16_t *q, long long q_stride_b, long long q_stride_h,
+                              const uint8_t *k_codes, const uint8_t *v_codes, const uint16_t *k_scale,
+                              const uint16_t *v_scale, int num_pages, const int32_t *block_table,
+                              int max_pages, const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
+                              int page_size, double scale, double *out) {
+    int bad = 0;
+    long long i, n = (long long)B * Hq;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (i = 0; i < n; ++i) {
+        int b = (int)(i / Hq), h = (int)(i % Hq), d;
+        double *o = out + i * D;
+        if (paged_row_fp8kv(q, q_stride_b, q_stride_h, k_codes, v_codes, k_scale, v_scale, num_pages,
+                            block_table, max_pages, seq_lens, Hq, Hkv, D, page_size, scale, b, h, o) != 0) {
+            for (d = 0; d < D; ++d) o[d] = NAN;
+            ++bad;
+        }
+    }
+    return bad;
+}
+
+/* fp8 append for the GQA cache: every (sequence b, kv head h) row of k_new / v_new
+ * [B, Hkv, D] bf16 is quantised by the per-row rule of oracle_kv_append_fp8 (amax / 448
+ * stored as bf16, codes e4m3(x / factor) RNE saturating) and written at logical position
+ * pos[b]: codes to [page, slot, h, :] of the [num_pages, ps, Hkv, D] caches, factors to
+ * [page, h, slot] of the [num_pages, Hkv, ps] scale arrays.  Returns the number of rows
+ * skipped (position or page out of range). */
+static void quantise_row(const uint16_t *x, int n, uint8_t *codes, uint16_t *factor) {
+    float amax = 0.0f, s, sb;
+    uint32_t u;
+    int d;
+    for (d = 0; d < n; ++d) {
+        float v = (float)oracle_bf16_value(x[d]);
+        if (fabsf(v) > amax) amax = fabsf(v);
+    }
+    s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    sb = (float)oracle_round_to_bf16((double)s);
+    memcpy(&u, &sb, sizeof u);
+    *factor = (uint16_t)(u >> 16);
+    for (d = 0; d < n; ++d) codes[d] = oracle_e4m3_from_float((float)oracle_bf16_value(x[d]) / sb);
+}
+
+int oracle_kv_append_paged_fp8(const uint16_t *k_new, const uint16_t *v_new, uint8_t *k_codes,
+                               uint8_t *v_codes, uint16_t *k_scale, uint16_t *v_scale, int num_pages,
+                               int page_size, const int32_t *block_table, int max_pages,
+                               const int32_t *pos, int B, int Hkv, int D) {
+    int b, h, bad = 0;
+    for (b = 0; b < B; ++b) {
+        long long p = pos[b], page;
+        int slot;
+        if (p < 0 || p >= (long long)max_pages * page_size) { bad += Hkv; continue; }
+        page = block_table[(long long)b * max_pages + p / page_size];
+        if (page < 0 || page >= num_pages) { bad += Hkv; continue; }
+        slot = (int)(p % page_size);
+        for (h = 0; h < Hkv; ++h) {
+            long long src = ((long long)b * Hkv + h) * D;
+            long long dst = ((page * page_size + slot) * Hkv + h) * D;
+            long long f = (page * Hkv + h) * page_size + slot;
+            quantise_row(k_new + src, D, k_codes + dst, k_scale + f);
+            quantise_row(v_new + src, D, v_codes + dst, v_scale + f);
+        }
+    }
+    return bad;
+}

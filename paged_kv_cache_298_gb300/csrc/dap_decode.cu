@@ -553,7 +553,17 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     const int rem = blockIdx.x - s * units;
     const int b = rem / nkvg;
     const int kvg = rem - b * nkvg;
+    // the sequence length and the producer's page ids of the first tile are loaded together
+    // (table entries from position s * chunk on; those past the sequence's end are read
+    // within the table but not used)
     int L = p.seq_lens[b];
+    const int R = PAGED ? p.box_rows : BT;
+    int pg_first = 0;
+    if (PAGED && warp == NWC && lane * R < BT) {
+        const long long t = (long long)s * p.chunk + lane * R;
+        if (t < (long long)p.max_pages * p.page_size)
+            pg_first = __ldg(p.block_table + (long long)b * p.max_pages + t / p.page_size);
+    }
     if (L < 0 || L > p.max_kv_len) {
         if (threadIdx.x == 0 && s == 0 && kvg == 0) flag_error(DAP_DEVERR_SEQLEN);
         L = min(max(L, 0), p.max_kv_len);
@@ -583,13 +593,12 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
             prefetch_tensormap(&mapK);
             prefetch_tensormap(&mapV);
         }
-        const int R = PAGED ? p.box_rows : BT;
         const int32_t *table = PAGED ? p.block_table + (long long)b * p.max_pages : nullptr;
         auto lookup = [&](int tile) -> int {  // page id of this lane's box of `tile`
             if (!PAGED) return b;
             const int t = tok0 + tile * BT + lane * R;
             if (lane * R >= BT || t >= tok1) return 0;
-            int pg = __ldg(table + t / p.page_size);
+            int pg = tile == 0 ? pg_first : __ldg(table + t / p.page_size);
             if (pg < 0 || pg >= p.num_pages) {
                 flag_error(DAP_DEVERR_PAGE);
                 pg = 0;

@@ -269,24 +269,25 @@ struct MultiTile {
     int b, q0, qlen, i0, ntok, pos0, kv_end;
 };
 
-// The tile's sequence, tokens and KV range; false for a work-map entry that names no token
+// The tile's tokens and KV range from its work-map entry (sequence b, tile index) and the
+// values q0 = qo_indptr[b], q1 = qo_indptr[b + 1], L = seq_lens[b] (loaded by the caller,
+// from sequence 0 when b is out of range); false for an entry that names no token
 // (flagged).  Shared by the attention kernel and its combine so both agree on the splits.
-__device__ __forceinline__ bool multi_tile(const SplitParams &p, int b, int tindex, int qt, bool report,
-                                           MultiTile *t) {
+__device__ __forceinline__ bool multi_tile(const SplitParams &p, int b, int tindex, int q0, int q1, int L,
+                                           int qt, bool report, MultiTile *t) {
     if (b < 0 || b >= p.B) {
         if (report) flag_error(DAP_DEVERR_QMAP);
         return false;
     }
     t->b = b;
-    t->q0 = p.qo_indptr[b];
-    t->qlen = p.qo_indptr[b + 1] - t->q0;
+    t->q0 = q0;
+    t->qlen = q1 - q0;
     t->i0 = tindex * qt;
     t->ntok = min(qt, t->qlen - t->i0);
-    if (tindex < 0 || t->ntok <= 0 || t->q0 < 0 || t->q0 + t->qlen > p.total_q) {
+    if (tindex < 0 || t->ntok <= 0 || q0 < 0 || q1 > p.total_q) {
         if (report) flag_error(DAP_DEVERR_QMAP);
         return false;
     }
-    int L = p.seq_lens[b];
     if (L < 0 || L > p.max_kv_len || t->qlen > L) {
         if (report) flag_error(DAP_DEVERR_SEQLEN);
         L = min(max(L, 0), p.max_kv_len);
@@ -310,9 +311,22 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     const int rem = blockIdx.x - s * units;
     const int w = rem / p.Hkv;
     const int kvh = rem - w * p.Hkv;
+    // Every load the schedule needs before the first TMA is issued at once: the work-map
+    // entry, then its sequence's q range and length together with the producer's page ids
+    // of the first tile (read from position s * chunk on; entries past the sequence's end
+    // are read within the table but not used).
+    const int wb = p.tile_batch[w], wi = p.tile_index[w];
+    const int bb = (wb >= 0 && wb < p.B) ? wb : 0;
+    const int q0 = p.qo_indptr[bb], q1 = p.qo_indptr[bb + 1], Lraw = p.seq_lens[bb];
+    const int R = p.box_rows;
+    int pg_first = 0;
+    if (warp == NWC && lane * R < BT) {
+        const long long t = (long long)s * p.chunk + lane * R;
+        if (t < (long long)p.max_pages * p.page_size)
+            pg_first = __ldg(p.block_table + (long long)bb * p.max_pages + t / p.page_size);
+    }
     MultiTile tl;
-    if (!multi_tile(p, p.tile_batch[w], p.tile_index[w], C::QT, threadIdx.x == 0 && s == 0 && kvh == 0, &tl))
-        return;
+    if (!multi_tile(p, wb, wi, q0, q1, Lraw, C::QT, threadIdx.x == 0 && s == 0 && kvh == 0, &tl)) return;
     const int nsplit = max(1, (tl.kv_end + p.chunk - 1) / p.chunk);
     if (s >= nsplit) return;
     const int tok0 = s * p.chunk;
@@ -338,12 +352,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
             prefetch_tensormap(&mapK);
             prefetch_tensormap(&mapV);
         }
-        const int R = p.box_rows;
         const int32_t *table = p.block_table + (long long)tl.b * p.max_pages;
         auto lookup = [&](int tile) -> int {
             const int t = tok0 + tile * BT + lane * R;
             if (lane * R >= BT || t >= tok1) return 0;
-            int pg = __ldg(table + t / p.page_size);
+            int pg = tile == 0 ? pg_first : __ldg(table + t / p.page_size);
             if (pg < 0 || pg >= p.num_pages) {
                 flag_error(DAP_DEVERR_PAGE);
                 pg = 0;
@@ -434,8 +447,9 @@ __global__ void __launch_bounds__(256) combine_multi_kernel(const SplitParams p,
         if (p.qo_indptr[mid] <= r) lo = mid;
         else hi = mid;
     }
+    const int q0 = p.qo_indptr[lo], q1 = p.qo_indptr[lo + 1];
     MultiTile tl;
-    if (!multi_tile(p, lo, (r - p.qo_indptr[lo]) / qt, qt, false, &tl)) return;
+    if (!multi_tile(p, lo, (r - q0) / qt, q0, q1, p.seq_lens[lo], qt, false, &tl)) return;
     const int nsplit = max(1, (tl.kv_end + p.chunk - 1) / p.chunk);
     if (nsplit == 1) return;
     const long long row0 = (long long)r * p.num_splits * p.Hq + hq;

@@ -18,6 +18,11 @@ target device for large ones; the same tensors are copied to whichever side need
   so saturation never applies), stored as uint8; per-slot inverse scales U[0.5, 2)
   rounded to bf16; per-token window lengths U{1..W}; the first len slots of a token are
   distinct uniform slots of the cache, the rest -1.
+* e4m3 GQA cache: the paged pool and table above; K and V codes float32 N(0, 1) converted
+  to float8_e4m3fn by torch; per-(page, kv head, slot) factors U[0.5, 2) rounded to bf16;
+  poisoning writes the NaN code 0x7F and NaN factors.
+* Multi-token decode: the paged pool above holding every new token already; q packed
+  [sum(q_lens), Hq, D], N(0, 1) bf16 (seed + 200).
 """
 from __future__ import annotations
 
@@ -162,6 +167,96 @@ def make_multi_case(B, Hq, Hkv, D, page_size, seq_lens, q_lens, seed, *, device=
     return MultiCase(q, kv, [int(x) for x in q_lens])
 
 
+@dataclass
+class Fp8KvCase:
+    """A paged GQA decode problem over an e4m3 cache.  q [B,Hq,D] bf16; k_codes / v_codes
+    [P,ps,Hkv,D] uint8 (OCP e4m3 codes); k_scale / v_scale [P,Hkv,ps] bf16 dequantisation
+    factors; block_table [B,max_pages] int32; seq_lens [B] int32."""
+    q: torch.Tensor
+    k_codes: torch.Tensor
+    v_codes: torch.Tensor
+    k_scale: torch.Tensor
+    v_scale: torch.Tensor
+    block_table: torch.Tensor
+    seq_lens: torch.Tensor
+    page_size: int
+    scale: float
+    name: str = ""
+
+    @property
+    def B(self):
+        return self.q.shape[0]
+
+    @property
+    def Hq(self):
+        return self.q.shape[1]
+
+    @property
+    def D(self):
+        return self.q.shape[2]
+
+    @property
+    def Hkv(self):
+        return self.k_codes.shape[2]
+
+    @property
+    def max_kv_len(self):
+        return int(self.seq_lens.max().item()) if self.seq_lens.numel() else 0
+
+    @property
+    def total_kv(self):
+        return int(self.seq_lens.to(torch.int64).sum().item())
+
+    def to(self, device) -> "Fp8KvCase":
+        return Fp8KvCase(self.q.to(device), self.k_codes.to(device), self.v_codes.to(device),
+                         self.k_scale.to(device), self.v_scale.to(device), self.block_table.to(device),
+                         self.seq_lens.to(device), self.page_size, self.scale, self.name)
+
+
+E4M3_NAN_CODE = 0x7F
+
+
+def make_fp8kv_case(B, Hq, Hkv, D, page_size, seq_lens, seed, *, device="cpu", poison=True,
+                    name="") -> Fp8KvCase:
+    """Block table, pool and q as make_paged_case (same seed); codes are float32 N(0,1)
+    converted to float8_e4m3fn by torch (RNE, no saturation at these values), factors
+    U[0.5, 2) rounded to bf16 (seed + 300).  With poison=True unused pages and in-page
+    rows past a sequence's end hold the NaN code 0x7F and NaN factors."""
+    base = make_paged_case(B, Hq, Hkv, D, page_size, seq_lens, seed, device=device, poison=False, name=name)
+    P = base.num_pages
+    g = _gen(seed + 300, device)
+    def codes():
+        x = torch.randn((P, page_size, Hkv, D), generator=g, device=device, dtype=torch.float32)
+        return x.to(torch.float8_e4m3fn).view(torch.uint8)
+    def factors():
+        u = torch.rand((P, Hkv, page_size), generator=g, device=device, dtype=torch.float32)
+        return (0.5 + 1.5 * u).to(torch.bfloat16)
+    kc, vc = codes(), codes()
+    ks, vs = factors(), factors()
+    if poison:
+        lens = [int(x) for x in seq_lens]
+        need = [(L + page_size - 1) // page_size for L in lens]
+        table = base.block_table.cpu()
+        used = torch.zeros(P, dtype=torch.bool)
+        for b in range(B):
+            used[table[b, :need[b]].long()] = True
+        nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16).view(torch.bfloat16).item()
+        unused = (~used).nonzero().flatten().to(device)
+        for c in (kc, vc):
+            c[unused] = E4M3_NAN_CODE
+        for f in (ks, vs):
+            f[unused] = nan
+        for b in range(B):
+            tail = lens[b] % page_size
+            if need[b] and tail:
+                last = int(table[b, need[b] - 1])
+                for c in (kc, vc):
+                    c[last, tail:] = E4M3_NAN_CODE
+                for f in (ks, vs):
+                    f[last, :, tail:] = nan
+    return Fp8KvCase(base.q, kc, vc, ks, vs, base.block_table, base.seq_lens, page_size, base.scale, name)
+
+
 def logical_kv(case: PagedCase, max_len=None):
     """The contiguous [B, max_len, Hkv, D] copies of K and V that the paged pool holds
     (rows past a sequence's length are zero).  A data move, used to build the contiguous
@@ -291,6 +386,14 @@ def spec_verify_paged(device="cpu", B=128, q_len=4) -> MultiCase:
     return make_multi_case(B, 32, 8, 128, 16, lens, [q_len] * B, 298006, device=device,
                            name=f"multi-token GQA decode B={B} q_len={q_len} Hq=32 Hkv=8 D=128 ps=16 "
                                 f"L~U[256,4096]")
+
+
+def ragged_fp8kv(device="cpu", B=128) -> Fp8KvCase:
+    """The ragged decode batch (B=128, Hq=32, Hkv=8, D=128, page 16, kv_len U{256..4096})
+    with an e4m3 K/V cache and per-(slot, kv head) bf16 factors."""
+    lens = uniform_lengths(B, 256, 4096, 298003)
+    return make_fp8kv_case(B, 32, 8, 128, 16, lens, 298007, device=device,
+                           name=f"ragged GQA decode, e4m3 KV, B={B} Hq=32 Hkv=8 D=128 ps=16 L~U[256,4096]")
 
 
 def fp8_swa(device="cpu") -> Fp8Case:

@@ -461,3 +461,122 @@ def test_multi_token_matches_causal_sdpa_float64():
         mask = torch.arange(L)[None, :] <= pos                   # [n, L]: token i sees keys <= its position
         o = F.scaled_dot_product_attention(qb, kb, vb, attn_mask=mask, scale=case.scale, enable_gqa=True)
         np.testing.assert_allclose(got[qi[b]:qi[b + 1]], o[0].permute(1, 0, 2).numpy(), rtol=1e-11, atol=1e-12)
+
+
+# ---- paged GQA decode over an e4m3 cache -----------------------------------------------
+
+def fp8kv_decoded(case):
+    """Logical float64 K and V per sequence, decoded by torch: float8_e4m3fn view of the
+    codes times the bf16 factor of (page, kv head, slot)."""
+    kval = case.k_codes.view(torch.float8_e4m3fn).to(torch.float64)
+    vval = case.v_codes.view(torch.float8_e4m3fn).to(torch.float64)
+    ksc = case.k_scale.to(torch.float64).permute(0, 2, 1)[..., None]   # [P, ps, Hkv, 1]
+    vsc = case.v_scale.to(torch.float64).permute(0, 2, 1)[..., None]
+    k = (kval * ksc).numpy()
+    v = (vval * vsc).numpy()
+    table = case.block_table.numpy()
+    ks, vs = [], []
+    for b in range(case.B):
+        t = np.arange(int(case.seq_lens[b]))
+        ks.append(k[table[b, t // case.page_size], t % case.page_size])
+        vs.append(v[table[b, t // case.page_size], t % case.page_size])
+    return ks, vs
+
+
+def run_fp8kv(case, scale=None):
+    return oracle.decode_paged_fp8kv(bits(case.q), case.k_codes.numpy(), case.v_codes.numpy(), bits(case.k_scale),
+                                     bits(case.v_scale), case.block_table.numpy(), case.seq_lens.numpy(),
+                                     case.scale if scale is None else scale)
+
+
+FP8KV_SHAPES = [
+    (2, 4, 2, 64, 16, [37, 100]),
+    (3, 8, 8, 128, 8, [5, 1, 9]),
+    (2, 32, 8, 128, 16, [70, 20]),
+    (1, 16, 2, 128, 64, [130]),
+]
+
+
+@pytest.mark.parametrize("shape", FP8KV_SHAPES)
+def test_fp8kv_matches_torch_float8_and_sdpa_float64(shape):
+    B, Hq, Hkv, D, ps, lens = shape
+    case = inputs.make_fp8kv_case(B, Hq, Hkv, D, ps, lens, 61 + D + len(lens))
+    got = run_fp8kv(case)
+    ks, vs = fp8kv_decoded(case)
+    q = as_f64(case.q.float())
+    for b in range(B):
+        kb = torch.from_numpy(ks[b]).permute(1, 0, 2)[None]
+        vb = torch.from_numpy(vs[b]).permute(1, 0, 2)[None]
+        o = F.scaled_dot_product_attention(torch.from_numpy(q[b])[None, :, None, :], kb, vb, scale=case.scale,
+                                           enable_gqa=True)[0, :, 0, :].numpy()
+        np.testing.assert_allclose(got[b], o, rtol=1e-11, atol=1e-12)
+
+
+def test_fp8kv_with_power_of_two_factors_is_the_bf16_decode():
+    # codes times a power of two are exact in bf16: the fp8 decode must then be the bf16
+    # decode of a cache holding those values
+    case = inputs.make_fp8kv_case(3, 8, 2, 64, 16, [40, 17, 64], 71, poison=False)
+    g = torch.Generator().manual_seed(72)
+    for f in (case.k_scale, case.v_scale):
+        f.copy_(torch.pow(2.0, torch.randint(-3, 4, f.shape, generator=g).float()).to(torch.bfloat16))
+    kval = (case.k_codes.view(torch.float8_e4m3fn).float() * case.k_scale.float().permute(0, 2, 1)[..., None])
+    vval = (case.v_codes.view(torch.float8_e4m3fn).float() * case.v_scale.float().permute(0, 2, 1)[..., None])
+    assert torch.equal(kval.to(torch.bfloat16).float(), kval)
+    bf = inputs.PagedCase(case.q, kval.to(torch.bfloat16), vval.to(torch.bfloat16), case.block_table,
+                          case.seq_lens, case.page_size, case.scale)
+    np.testing.assert_allclose(run_fp8kv(case), run_oracle(bf), rtol=1e-13, atol=1e-14)
+
+
+def test_fp8kv_factors_scale_the_output_and_the_logits():
+    case = inputs.make_fp8kv_case(2, 8, 2, 64, 16, [33, 50], 73, poison=False)
+    base = run_fp8kv(case)
+    doubled = inputs.Fp8KvCase(case.q, case.k_codes, case.v_codes, case.k_scale,
+                               (case.v_scale.float() * 2).to(torch.bfloat16), case.block_table, case.seq_lens,
+                               case.page_size, case.scale)
+    np.testing.assert_allclose(run_fp8kv(doubled), 2 * base, rtol=1e-13, atol=1e-14)
+    # every key factor times 4 is the softmax scale times 4
+    k4 = inputs.Fp8KvCase(case.q, case.k_codes, case.v_codes, (case.k_scale.float() * 4).to(torch.bfloat16),
+                          case.v_scale, case.block_table, case.seq_lens, case.page_size, case.scale)
+    np.testing.assert_allclose(run_fp8kv(k4), run_fp8kv(case, scale=4 * case.scale), rtol=1e-12, atol=1e-13)
+
+
+def test_fp8kv_page_permutation_and_empty_sequence():
+    case = inputs.make_fp8kv_case(3, 8, 4, 64, 8, [0, 23, 64], 74, poison=False)
+    got = run_fp8kv(case)
+    assert np.all(got[0] == 0)
+    P = case.k_codes.shape[0]
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(75))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(P)
+    moved = inputs.Fp8KvCase(case.q, case.k_codes[perm], case.v_codes[perm], case.k_scale[perm], case.v_scale[perm],
+                             inv[case.block_table.long()].to(torch.int32), case.seq_lens, case.page_size, case.scale)
+    np.testing.assert_array_equal(run_fp8kv(moved), got)
+
+
+def test_kv_append_paged_fp8_places_and_quantises_rows():
+    case = inputs.make_fp8kv_case(3, 8, 2, 64, 16, [16, 5, 31], 76, poison=False)
+    g = torch.Generator().manual_seed(77)
+    k_new = (inputs.randn_bf16((3, 2, 64), g, "cpu").float() * torch.tensor([1.0, 30.0, 0.01])[:, None, None])
+    k_new = k_new.to(torch.bfloat16)
+    v_new = inputs.randn_bf16((3, 2, 64), g, "cpu")
+    kc, vc = case.k_codes.numpy().copy(), case.v_codes.numpy().copy()
+    ks, vs = bits(case.k_scale).copy(), bits(case.v_scale).copy()
+    pos = case.seq_lens.numpy().copy()
+    assert oracle.kv_append_paged_fp8(bits(k_new), bits(v_new), kc, vc, ks, vs, case.block_table.numpy(), pos) == 0
+    table = case.block_table.numpy()
+    for b in range(3):
+        page, slot = table[b, pos[b] // 16], pos[b] % 16
+        for h in range(2):
+            for new, codes, fac in ((k_new, kc, ks), (v_new, vc, vs)):
+                x = new[b, h].float()
+                amax = float(x.abs().max())
+                s = torch.tensor([amax / 448.0], dtype=torch.float32).to(torch.bfloat16)
+                assert fac[page, h, slot] == int(s.view(torch.int16)) & 0xFFFF
+                want = (x / s.float()).to(torch.float8_e4m3fn).view(torch.uint8)
+                assert np.array_equal(codes[page, slot, h], want.numpy())
+    # every other slot is untouched
+    changed = (kc != case.k_codes.numpy()).any(axis=(2, 3))
+    assert changed.sum() <= 3
+    # a position beyond the table is refused
+    assert oracle.kv_append_paged_fp8(bits(k_new), bits(v_new), kc, vc, ks, vs, table,
+                                      np.array([0, 10 ** 6, 1], np.int32)) == 2
