@@ -42,6 +42,15 @@
  *   at or past num_blocks * bs is treated like a padded slot (the page's fallback
  *   would raise an indexing error there).
  *
+ *   GQA decode over an e4m3 cache (the fp8 cache convention of native_swa_decode.py, one
+ *   dequantisation factor per (slot, kv head) for K and for V): the paged decode above with
+ *   K = e4m3(code) * factor and V likewise, the product exact; the matching append
+ *   quantises each (sequence, kv head) row by the fp8 append rule further down.
+ *
+ *   multi-token decode and the packed-q work map (AstrAI "CUDA Kernels", "Q Scheduling and
+ *   KV Addressing"): token i of the q_len new tokens of sequence b sits at position
+ *   seq_lens[b] - q_len + i and attends the keys up to it.
+ *
  * Parity pins (tests/test_oracle_pins.py) tie each function to something other than
  * itself: closed forms (constant V, a single key, a key shift, q = 0), brute force
  * against torch's float64 scaled_dot_product_attention, page-permutation invariance,
