@@ -116,6 +116,7 @@ class ClockSampler:
 
 KERNEL_SOURCES = {"split_kernel": ("dap_decode.cu", "dap_tile.cuh", "dap_device.cuh", "dap_internal.h"),
                   "multi_kernel": ("dap_multi.cu", "dap_tile.cuh", "dap_device.cuh", "dap_internal.h"),
+                  "fp8kv_kernel": ("dap_fp8kv.cu", "dap_tile.cuh", "dap_device.cuh", "dap_internal.h"),
                   "swa_kernel": ("dap_fp8.cu", "dap_device.cuh", "dap_internal.h")}
 
 
@@ -748,6 +749,188 @@ def run_reference_multi(args):
         flush=True)
 
 
+# ---- GQA decode over an e4m3 cache --------------------------------------------------------
+
+def fp8kv_algorithmic(case, rows=None) -> int:
+    """e4m3 K/V codes of the rows inside seq_lens + their two bf16 factors per kv head + q +
+    out + block-table entries + seq_lens.  `rows`: restrict to these sequences."""
+    lens = case.seq_lens.cpu().to(torch.int64)
+    if rows is not None:
+        lens = lens[rows]
+    B = lens.numel()
+    kv = int(lens.sum()) * case.Hkv * (2 * case.D + 2 * 2)
+    qo = 2 * B * case.Hq * case.D * 2
+    pages = int(((lens + case.page_size - 1) // case.page_size).sum()) * 4
+    return kv + qo + pages + B * 4
+
+
+class Fp8KvOracle:
+    def __init__(self, case):
+        import oracle
+        self.oracle = oracle
+        self.case = case
+        self.q = bits(case.q)
+        self.kc = case.k_codes.cpu().numpy()
+        self.vc = case.v_codes.cpu().numpy()
+        self.ks = bits(case.k_scale)
+        self.vs = bits(case.v_scale)
+        self.table = case.block_table.cpu().numpy()
+        self.lens = case.seq_lens.cpu().numpy()
+
+    def run(self, rows):
+        t0 = time.perf_counter()
+        self.oracle.decode_paged_fp8kv(np.ascontiguousarray(self.q[rows]), self.kc, self.vc, self.ks, self.vs,
+                                       np.ascontiguousarray(self.table[rows]), np.ascontiguousarray(self.lens[rows]),
+                                       self.case.scale)
+        return time.perf_counter() - t0
+
+    def sample(self, target_s):
+        dt = self.run(np.arange(1))
+        return np.arange(int(max(1, min(self.case.B, target_s / max(dt, 1e-4)))))
+
+
+def run_fp8kv(args):
+    from paged_kv_cache_298_gb300 import binding, inputs
+    dev = torch.device("cuda", 0)
+    binding.load()
+    case = inputs.ragged_fp8kv(device=dev, B=args.batch or 128)
+    hbm_peak, peak_src = peaks()
+    sms = binding.device_sm_count()
+    S = args.splits if args.splits > 0 else binding.plan_splits(sms, case.B, case.Hq, case.Hkv, case.D,
+                                                                case.page_size, case.max_kv_len, case.total_kv)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    parts = ("q", "k_codes", "v_codes", "k_scale", "v_scale", "block_table", "seq_lens")
+    footprint = sum(getattr(case, n).numel() * getattr(case, n).element_size() for n in parts)
+    copies = 1 + max(1, math.ceil(2 * l2 / footprint))
+    sets = [case] + [inputs.Fp8KvCase(*[getattr(case, n).clone() for n in parts], case.page_size, case.scale,
+                                      case.name) for _ in range(copies - 1)]
+    ws = [torch.empty(max(1, binding.workspace_bytes(case.B, case.Hq, case.Hkv, case.D, S) if S > 1 else 1),
+                      dtype=torch.uint8, device=dev) for _ in sets]
+    outs = [torch.empty_like(case.q) for _ in sets]
+    maxlen = case.max_kv_len
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        j = i % copies
+        c = sets[j]
+        binding.decode_attn_paged_fp8kv(c.q, c.k_codes, c.v_codes, c.k_scale, c.v_scale, c.block_table, c.seq_lens,
+                                        max_kv_len=maxlen, scale=c.scale, num_splits=S, workspace=ws[j], out=outs[j])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if binding.get_device_errors(clear=True):
+        raise SystemExit("device error word set during warm-up")
+    K = args.steps
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(0)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(stream)
+    for i in range(K):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / K
+
+    KT = min(K, 50)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(KT)]
+    for e in ev:
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    for i in range(KT):
+        binding.set_trace_events(*ev[i])
+        step(i)
+    torch.cuda.synchronize()
+    binding.set_trace_events()
+    kern_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    combine_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    errs = binding.get_device_errors(clear=True)
+
+    # end to end: q, block table and seq_lens in from pinned host memory, out back
+    hq = case.q.cpu().pin_memory()
+    ht = case.block_table.cpu().pin_memory()
+    hl = case.seq_lens.cpu().pin_memory()
+    ho = torch.empty(case.q.shape, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step(i):
+        j = i % copies
+        c = sets[j]
+        c.q.copy_(hq, non_blocking=True)
+        c.block_table.copy_(ht, non_blocking=True)
+        c.seq_lens.copy_(hl, non_blocking=True)
+        step(i)
+        ho.copy_(outs[j], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+
+    nbytes = fp8kv_algorithmic(case)
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    lens = case.seq_lens.cpu()
+    line = {
+        "metric": "paged decode attention over an e4m3 KV cache, achieved HBM GB/s (algorithmic bytes), cold KV",
+        "value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "us_per_call": round(ms * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": case.name, "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "D": case.D,
+                   "page_size": case.page_size, "kv_len_min": int(lens.min()), "kv_len_max": int(lens.max()),
+                   "total_kv": case.total_kv, "num_splits": S, "kv_dtype": "e4m3 + bf16 factor per (slot, kv head)",
+                   "cold_kv": f"{copies} rotated input copies of {footprint / 1e9:.2f} GB each (> 2x L2)"},
+        "kv_tokens_per_s": round(case.total_kv / (ms * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": "fp8kv_kernel", "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "fp8kv_kernel_ms": round(kern_ms, 5), "combine_ms": round(combine_ms, 5),
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "traffic": recorded_traffic("fp8kv_kernel", workload_key(args))},
+        "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": hq.numel() * 2 + ht.numel() * 4 + hl.numel() * 4,
+                "d2h_bytes_per_step": ho.numel() * 2},
+        "gpu_launches": K * (2 if S > 1 else 1), "device_errors": errs, "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        r = Fp8KvOracle(case)
+        rows = r.sample(6.0)
+        dt = r.run(rows)
+        line["cpu_baseline"] = {"value": fp8kv_algorithmic(case, torch.as_tensor(rows)) / dt / 1e9, "unit": "GB/s",
+                                "cores": r.oracle.num_threads(), "kind": "oracle",
+                                "sample": f"fp64 oracle (OpenMP) on sequences 0..{len(rows) - 1} of {case.B} "
+                                          f"(all heads), one pass, {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_fp8kv(args):
+    from paged_kv_cache_298_gb300 import inputs
+    case = inputs.ragged_fp8kv()
+    r = Fp8KvOracle(case)
+    rows = r.sample(min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        r.run(rows)
+    dt = statistics.mean(r.run(rows) for _ in range(args.steps))
+    value = fp8kv_algorithmic(case, torch.as_tensor(rows)) / dt / 1e9
+    print(json.dumps({
+        "impl": "reference",
+        "metric": "paged decode attention over an e4m3 KV cache, achieved HBM GB/s (algorithmic bytes), cold KV",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": {"workload": case.name, "sample_sequences": len(rows)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": r.oracle.num_threads(), "kind": "oracle",
+                         "sample": f"fp64 oracle (OpenMP) on sequences 0..{len(rows) - 1} per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+        flush=True)
+
+
 # ---- reference arm: the fp64 oracle on the host cores ----------------------------------
 
 def run_reference_fp8(args):
@@ -785,6 +968,8 @@ def run_reference(args):
         return run_reference_fp8(args)
     if args.workload == "multi":
         return run_reference_multi(args)
+    if args.workload == "fp8kv":
+        return run_reference_fp8kv(args)
     case = make_workload(args.workload, "cpu")
     r = OracleRunner(case)
     rows = r.sample_rows(target_s=min(8.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -815,7 +1000,7 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="ragged", choices=["ragged", "llama", "long1", "long4", "fp8", "append", "multi"])
+    ap.add_argument("--workload", default="ragged", choices=["ragged", "llama", "long1", "long4", "fp8", "append", "multi", "fp8kv"])
     ap.add_argument("--splits", type=int, default=-1,
                     help="-1 = the planner's choice, 0 = balanced schedule, S > 0 = per-sequence splits")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -833,6 +1018,8 @@ def main():
         run_append(args)
     elif args.workload == "multi":
         run_multi(args)
+    elif args.workload == "fp8kv":
+        run_fp8kv(args)
     else:
         run_ours(args)
 

@@ -1,8 +1,9 @@
 /*
  * dap.h -- C ABI of the paged decode-attention library for NVIDIA GB300 (sm_103a).
  *
- * Single-token GQA decode attention over a paged KV cache, its contiguous-cache form,
- * and the fp8 sliding-window latent (K = V) variant.  Plain pointers and sizes only.
+ * Single-token GQA decode attention over a paged KV cache (bf16 or fp8 e4m3), its
+ * contiguous-cache form, multi-token causal decode, the fp8 sliding-window latent (K = V)
+ * variant, and the cache appends that feed them.  Plain pointers and sizes only.
  *
  * Conventions shared by every entry point:
  *   - The caller owns every buffer.  The library allocates no device memory and never
@@ -151,6 +152,51 @@ dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_s
                               int D, float scale, int num_splits, void *workspace,
                               size_t workspace_bytes, void *out, long long out_stride_b,
                               long long out_stride_h, void *stream);
+
+/*
+ * Paged GQA decode over an fp8 (OCP e4m3) K/V cache.  The fp8 cache convention of [C]
+ * (codes plus a bf16 dequantisation factor: value = e4m3(code) * factor), applied to the
+ * GQA cache with one factor per (slot, kv head) for K and one for V:
+ *   K[b, t, h, :] = e4m3(k_codes[page, slot, h, :]) * k_scale[page, h, slot],
+ *   page = block_table[b, t / page_size], slot = t % page_size; V likewise;
+ *   out[b, hq, :] = sum_t softmax_t(scale * q[b, hq, :] . K[b, t, hq/G, :]) V[b, t, hq/G, :].
+ *
+ *   k_codes, v_codes  device uint8 [num_pages, page_size, Hkv, D] contiguous (e4m3 codes).
+ *   k_scale, v_scale  device bf16 [num_pages, Hkv, page_size] contiguous (one factor per
+ *                     slot and kv head; kv-head-major inside a page so that a page's
+ *                     factors of one head are contiguous).
+ *   num_splits        >= 1: per-sequence splits as decode_attn_paged; 0 = the library picks
+ *                     dap_plan_splits(SMs, B, Hq, Hkv, D, page_size, max_kv_len, 0).
+ *   workspace         >= dap_workspace_bytes(B, Hq, Hkv, D, S) for the S used.
+ *   q, out, block_table, seq_lens, max_kv_len, scale, strides: as decode_attn_paged.
+ *   Supported: D = 128; G in {1, 2, 4, 8}; page_size a multiple of 8; codes and factor
+ *   arrays 16-byte aligned.  q is used in f16 after an exact power-of-two shift (so any
+ *   finite bf16 q is representable); the result is within the bf16 path's tolerance of
+ *   the exact dequantised attention.
+ */
+dap_status decode_attn_paged_fp8kv(const void *q, long long q_stride_b, long long q_stride_h,
+                                   const uint8_t *k_codes, const uint8_t *v_codes,
+                                   const void *k_scale, const void *v_scale, int num_pages,
+                                   int page_size, const int32_t *block_table, int max_pages,
+                                   const int32_t *seq_lens, int max_kv_len, int B, int Hq, int Hkv,
+                                   int D, float scale, int num_splits, void *workspace,
+                                   size_t workspace_bytes, void *out, long long out_stride_b,
+                                   long long out_stride_h, void *stream);
+
+/*
+ * Append the new token's K and V to the fp8 GQA cache that decode_attn_paged_fp8kv reads.
+ * Every (sequence b, kv head h) row of k_new / v_new is quantised as kv_append_fp8 does
+ * (amax / 448 stored as bf16, codes e4m3(x / factor) RNE, saturating) and written at
+ * logical position positions[b] through the block table: codes to [page, slot, h, :],
+ * factors to [page, h, slot].
+ *   k_new, v_new  device bf16 [B, Hkv, D] contiguous.  positions  device int32 [B].
+ *   Supported: D in {64, 128, 256}.  A position outside [0, max_pages * page_size) or a page
+ *   outside the pool skips that sequence and sets DAP_DEVERR_SEQLEN / DAP_DEVERR_PAGE.
+ */
+dap_status kv_append_paged_fp8(const void *k_new, const void *v_new, uint8_t *k_codes,
+                               uint8_t *v_codes, void *k_scale, void *v_scale, int num_pages,
+                               int page_size, const int32_t *block_table, int max_pages,
+                               const int32_t *positions, int B, int Hkv, int D, void *stream);
 
 /*
  * Multi-token decode: several new tokens per sequence (speculative-decoding verification,

@@ -30,7 +30,8 @@ EXPORTS = ("dap_status_string", "dap_version", "dap_device_sm_count", "dap_plan_
            "dap_chunk_tokens", "dap_workspace_bytes", "decode_attn_paged", "decode_attn_contig",
            "decode_attn_paged_fp8", "decode_attn_paged_noalloc", "kv_append_paged", "kv_append_fp8",
            "dap_set_trace_events", "dap_get_device_errors", "dap_multi_tokens_per_tile",
-           "dap_q_tile_map", "dap_workspace_bytes_multi", "decode_attn_paged_multi")
+           "dap_q_tile_map", "dap_workspace_bytes_multi", "decode_attn_paged_multi",
+           "decode_attn_paged_fp8kv", "kv_append_paged_fp8")
 
 
 class DapError(RuntimeError):
@@ -96,6 +97,11 @@ def load(build_if_missing: bool = True):
         lib.decode_attn_paged_multi.argtypes = [P, LL, LL, P, P, I, I, P, I, P, P, P, P, I, I, I, I, I, I,
                                                 I, F, I, P, SZ, P, LL, LL, P]
         lib.decode_attn_paged_multi.restype = I
+        lib.decode_attn_paged_fp8kv.argtypes = [P, LL, LL, P, P, P, P, I, I, P, I, P, I, I, I, I, I, F, I, P, SZ,
+                                                P, LL, LL, P]
+        lib.decode_attn_paged_fp8kv.restype = I
+        lib.kv_append_paged_fp8.argtypes = [P, P, P, P, P, P, I, I, P, I, P, I, I, I, P]
+        lib.kv_append_paged_fp8.restype = I
         lib.dap_set_trace_events.argtypes = [P, P, P]
         lib.dap_set_trace_events.restype = None
         lib.dap_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
@@ -285,6 +291,54 @@ def decode_attn_paged_fp8(q, kv_cache, inv_scale, slot_idx, lens, *, scale: floa
     return out
 
 
+# ---- GQA decode over an fp8 (e4m3) cache -----------------------------------------------
+
+def _fp8kv_cache(k_codes, v_codes, k_scale, v_scale):
+    _need(k_codes.dtype == torch.uint8 and k_codes.dim() == 4 and k_codes.is_contiguous()
+          and v_codes.shape == k_codes.shape and v_codes.dtype == torch.uint8 and v_codes.is_contiguous(),
+          "k_codes/v_codes must be contiguous uint8 [P, ps, Hkv, D]")
+    P, ps, Hkv, D = k_codes.shape
+    for f in (k_scale, v_scale):
+        _need(f.dtype == torch.bfloat16 and f.is_contiguous() and tuple(f.shape) == (P, Hkv, ps),
+              "k_scale/v_scale must be contiguous bf16 [P, Hkv, ps]")
+    return P, ps, Hkv, D
+
+
+def decode_attn_paged_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens, *, max_kv_len: int,
+                            scale: float | None = None, num_splits: int = 0, total_kv: int = 0, workspace=None,
+                            out=None, stream=None):
+    """Paged GQA decode over an e4m3 K/V cache (include/dap.h: decode_attn_paged_fp8kv).
+    num_splits 0 = the planner's choice (given the host-known sum of seq_lens ``total_kv``
+    if any), resolved here so the workspace can be sized.  Returns ``out`` [B, Hq, D]."""
+    _bf16_3d(q, "q")
+    B, Hq, D = q.shape
+    P, ps, Hkv, D2 = _fp8kv_cache(k_codes, v_codes, k_scale, v_scale)
+    _need(D2 == D, "head dims differ")
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
+          and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
+    _need(seq_lens.dtype == torch.int32 and seq_lens.numel() == B and seq_lens.is_contiguous(),
+          "seq_lens must be contiguous int32 [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    _bf16_3d(out, "out")
+    lib = load()
+    S = int(num_splits)
+    if S == 0 and B > 0:
+        S = lib.dap_plan_splits(lib.dap_device_sm_count(), B, Hq, Hkv, D, ps, int(max_kv_len), int(total_kv))
+    need = lib.dap_workspace_bytes(B, Hq, Hkv, D, S) if S >= 2 else 0
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.decode_attn_paged_fp8kv(_ptr(q), q.stride(0), q.stride(1), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
+                                     _ptr(v_scale), P, ps, _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                     int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S), _ptr(workspace), wbytes,
+                                     _ptr(out), out.stride(0), out.stride(1), _stream(stream))
+    _check(st, "decode_attn_paged_fp8kv")
+    return out
+
+
 # ---- multi-token decode ------------------------------------------------------------------
 
 def multi_tokens_per_tile(Hq: int, Hkv: int) -> int:
@@ -408,3 +462,24 @@ def kv_append_fp8(rows, kv_cache, inv_scale, slots, *, stream=None):
                               _stream(stream))
     _check(st, "kv_append_fp8")
     return kv_cache, inv_scale
+
+
+def kv_append_paged_fp8(k_new, v_new, k_codes, v_codes, k_scale, v_scale, block_table, positions, *, stream=None):
+    """Quantise each sequence's new K/V rows [B, Hkv, D] into the e4m3 GQA cache at
+    positions[b] (include/dap.h: kv_append_paged_fp8).  Returns the four cache arrays,
+    updated in place."""
+    _need(k_new.dtype == torch.bfloat16 and k_new.dim() == 3 and k_new.is_contiguous()
+          and v_new.shape == k_new.shape and v_new.dtype == torch.bfloat16 and v_new.is_contiguous(),
+          "k_new/v_new must be contiguous bf16 [B, Hkv, D]")
+    B, Hkv, D = k_new.shape
+    P, ps, Hkv2, D2 = _fp8kv_cache(k_codes, v_codes, k_scale, v_scale)
+    _need((Hkv2, D2) == (Hkv, D), "cache heads / dims differ from the new rows")
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
+          and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
+    _need(positions.dtype == torch.int32 and positions.numel() == B and positions.is_contiguous(),
+          "positions must be contiguous int32 [B]")
+    st = load().kv_append_paged_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
+                                    _ptr(v_scale), P, ps, _ptr(block_table), block_table.shape[1], _ptr(positions), B,
+                                    Hkv, D, _stream(stream))
+    _check(st, "kv_append_paged_fp8")
+    return k_codes, v_codes, k_scale, v_scale

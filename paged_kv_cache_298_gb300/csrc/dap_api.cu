@@ -348,6 +348,82 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
     return launch_decode_multi(a, static_cast<cudaStream_t>(stream));
 }
 
+dap_status decode_attn_paged_fp8kv(const void *q, long long q_stride_b, long long q_stride_h,
+                                   const uint8_t *k_codes, const uint8_t *v_codes, const void *k_scale,
+                                   const void *v_scale, int num_pages, int page_size, const int32_t *block_table,
+                                   int max_pages, const int32_t *seq_lens, int max_kv_len, int B, int Hq, int Hkv,
+                                   int D, float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                                   void *out, long long out_stride_b, long long out_stride_h, void *stream) {
+    dap_status st = check_common(q, q_stride_b, q_stride_h, seq_lens, max_kv_len, B, Hq, Hkv, D, scale, num_splits,
+                                 out, out_stride_b, out_stride_h);
+    if (st != DAP_OK || B == 0) return st;
+    if (num_pages < 1 || page_size < 1 || max_pages < 1 ||
+        (long long)max_kv_len > (long long)max_pages * page_size)
+        return DAP_ERR_SHAPE;
+    if (!k_codes || !v_codes || !k_scale || !v_scale || !block_table) return DAP_ERR_NULL;
+    if (D != 128 || page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
+    if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scale) || !aligned16(v_scale) ||
+        !aligned4(block_table))
+        return DAP_ERR_ALIGN;
+    int S = num_splits;
+    if (S == 0) {
+        const int sms = dap_device_sm_count();
+        if (sms <= 0) return DAP_ERR_CUDA;
+        S = dap_plan_splits(sms, B, Hq, Hkv, D, page_size, max_kv_len, 0);
+    }
+    const int chunk = dap_chunk_tokens(max_kv_len, S);
+    const int needed = max_kv_len > 0 ? (int)ceil_div_ll(max_kv_len, chunk) : 1;
+    S = std::max(1, std::min(S, needed));
+    if (S > 1) {
+        const size_t need = dap_workspace_bytes(B, Hq, Hkv, D, S);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DAP_ERR_WORKSPACE;
+    }
+    DecodeArgs a = {};
+    a.paged = true;
+    a.q = q;
+    a.q_sb = q_stride_b;
+    a.q_sh = q_stride_h;
+    a.k = k_codes;
+    a.v = v_codes;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.num_pages = num_pages;
+    a.page_size = page_size;
+    a.block_table = block_table;
+    a.max_pages = max_pages;
+    a.seq_lens = seq_lens;
+    a.max_kv_len = max_kv_len;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.scale = scale;
+    a.num_splits = S;
+    a.chunk = chunk;
+    a.workspace = workspace;
+    a.out = out;
+    a.o_sb = out_stride_b;
+    a.o_sh = out_stride_h;
+    return launch_decode_fp8kv(a, static_cast<cudaStream_t>(stream));
+}
+
+dap_status kv_append_paged_fp8(const void *k_new, const void *v_new, uint8_t *k_codes, uint8_t *v_codes,
+                               void *k_scale, void *v_scale, int num_pages, int page_size,
+                               const int32_t *block_table, int max_pages, const int32_t *positions, int B, int Hkv,
+                               int D, void *stream) {
+    if (B < 0 || Hkv < 1 || D < 1 || num_pages < 1 || page_size < 1 || max_pages < 1) return DAP_ERR_SHAPE;
+    if (B == 0) return DAP_OK;
+    if (!(D == 64 || D == 128 || D == 256)) return DAP_ERR_UNSUPPORTED;
+    if (!k_new || !v_new || !k_codes || !v_codes || !k_scale || !v_scale || !block_table || !positions)
+        return DAP_ERR_NULL;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_codes) || !aligned16(v_codes) ||
+        (reinterpret_cast<uintptr_t>(k_scale) & 1u) || (reinterpret_cast<uintptr_t>(v_scale) & 1u) ||
+        !aligned4(block_table) || !aligned4(positions))
+        return DAP_ERR_ALIGN;
+    return launch_append_paged_fp8(k_new, v_new, k_codes, v_codes, k_scale, v_scale, num_pages, page_size,
+                                   block_table, max_pages, positions, B, Hkv, D, static_cast<cudaStream_t>(stream));
+}
+
 dap_status decode_attn_paged_fp8(const void *q, const uint8_t *kv_cache, const void *inv_scale,
                                  const int64_t *slot_idx, const int64_t *lens, int T, int NH, int HD,
                                  int W, int num_blocks, int block_size, float scale, void *out,
@@ -421,6 +497,7 @@ dap_status dap_get_device_errors(unsigned int *flags, int clear) {
     if (!read_errors_fp8(flags, clear != 0)) return DAP_ERR_CUDA;
     if (!read_errors_append(flags, clear != 0)) return DAP_ERR_CUDA;
     if (!read_errors_multi(flags, clear != 0)) return DAP_ERR_CUDA;
+    if (!read_errors_fp8kv(flags, clear != 0)) return DAP_ERR_CUDA;
     return DAP_OK;
 }
 

@@ -12,8 +12,12 @@
 // saturating at +-448 (AstrAI doc, FP8 section: quantize multiplies by the quantisation
 // multiplier, amax is kept in the input domain).
 //
-// One warp per row; every access is 16 bytes and coalesced.  Out-of-range positions, pages
-// and slots are skipped and flagged in the device error word.
+// GQA fp8 append: the same quantiser per (sequence, kv head) row of the K and the V cache,
+// one factor per (slot, kv head) each.
+//
+// One warp per row; accesses are coalesced (16 bytes per lane; 2 to 8 for the GQA fp8
+// codes).  Out-of-range positions, pages and slots are skipped and flagged in the device
+// error word.
 #include <cuda_fp8.h>
 
 #include "dap_device.cuh"
@@ -102,7 +106,99 @@ __global__ void __launch_bounds__(256)
     if (lane == 0) inv_scale[slot] = sb16;
 }
 
+// fp8 append for the GQA cache: one warp per (sequence, kv head) row of D values, VPL =
+// D / 32 per lane; the K row and the V row are quantised one after the other by the rule
+// above.  Codes go to [page, slot, h, :] of the [num_pages, ps, Hkv, D] caches, the
+// factors to [page, h, slot] of the [num_pages, Hkv, ps] arrays.
+template <int VPL>
+__device__ __forceinline__ void quantise_row(const __nv_bfloat16 *src, uint8_t *codes, __nv_bfloat16 *factor,
+                                             int lane) {
+    float x[VPL];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; i += 2) {
+        const float2 f = bf16x2_to_float2(reinterpret_cast<const uint32_t *>(src + lane * VPL)[i / 2]);
+        x[i] = f.x;
+        x[i + 1] = f.y;
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    const __nv_bfloat16 sb16 = __float2bfloat16_rn(s);
+    const float sb = __bfloat162float(sb16);
+    uint8_t c[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; i += 2) {
+        const __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(x[i], sb), __fdiv_rn(x[i + 1], sb)), __NV_SATFINITE, __NV_E4M3);
+        c[i] = (uint8_t)(two & 0xFF);
+        c[i + 1] = (uint8_t)(two >> 8);
+    }
+    if constexpr (VPL == 2) {
+        reinterpret_cast<uint16_t *>(codes)[lane] = (uint16_t)(c[0] | (c[1] << 8));
+    } else {
+#pragma unroll
+        for (int i = 0; i < VPL; i += 4)
+            reinterpret_cast<uint32_t *>(codes + lane * VPL)[i / 4] =
+                (uint32_t)c[i] | ((uint32_t)c[i + 1] << 8) | ((uint32_t)c[i + 2] << 16) | ((uint32_t)c[i + 3] << 24);
+    }
+    if (lane == 0) *factor = sb16;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256)
+    append_paged_fp8_kernel(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new, uint8_t *k_codes,
+                            uint8_t *v_codes, __nv_bfloat16 *k_scale, __nv_bfloat16 *v_scale, int num_pages,
+                            int page_size, const int32_t *block_table, int max_pages, const int32_t *pos, int B,
+                            int Hkv) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);  // (b, h)
+    const int lane = threadIdx.x & 31;
+    if (row >= B * Hkv) return;
+    const int b = row / Hkv, h = row - b * Hkv;
+    const long long p = pos[b];
+    if (p < 0 || p >= (long long)max_pages * page_size) {
+        if (lane == 0 && h == 0) flag_error(DAP_DEVERR_SEQLEN);
+        return;
+    }
+    const int page = block_table[(long long)b * max_pages + p / page_size];
+    if (page < 0 || page >= num_pages) {
+        if (lane == 0 && h == 0) flag_error(DAP_DEVERR_PAGE);
+        return;
+    }
+    const long long slot = p % page_size;
+    const long long dst = (((long long)page * page_size + slot) * Hkv + h) * D;
+    const long long f = ((long long)page * Hkv + h) * page_size + slot;
+    quantise_row<D / 32>(k_new + (long long)row * D, k_codes + dst, k_scale + f, lane);
+    quantise_row<D / 32>(v_new + (long long)row * D, v_codes + dst, v_scale + f, lane);
+}
+
 }  // namespace
+
+dap_status launch_append_paged_fp8(const void *k_new, const void *v_new, uint8_t *k_codes, uint8_t *v_codes,
+                                   void *k_scale, void *v_scale, int num_pages, int page_size,
+                                   const int32_t *block_table, int max_pages, const int32_t *pos, int B, int Hkv,
+                                   int D, cudaStream_t stream) {
+    const dim3 grid((unsigned)((B * Hkv + 7) / 8));
+    const __nv_bfloat16 *kn = static_cast<const __nv_bfloat16 *>(k_new), *vn = static_cast<const __nv_bfloat16 *>(v_new);
+    __nv_bfloat16 *ks = static_cast<__nv_bfloat16 *>(k_scale), *vs = static_cast<__nv_bfloat16 *>(v_scale);
+    switch (D) {
+        case 64:
+            append_paged_fp8_kernel<64><<<grid, 256, 0, stream>>>(kn, vn, k_codes, v_codes, ks, vs, num_pages, page_size,
+                                                                  block_table, max_pages, pos, B, Hkv);
+            break;
+        case 128:
+            append_paged_fp8_kernel<128><<<grid, 256, 0, stream>>>(kn, vn, k_codes, v_codes, ks, vs, num_pages,
+                                                                   page_size, block_table, max_pages, pos, B, Hkv);
+            break;
+        case 256:
+            append_paged_fp8_kernel<256><<<grid, 256, 0, stream>>>(kn, vn, k_codes, v_codes, ks, vs, num_pages,
+                                                                   page_size, block_table, max_pages, pos, B, Hkv);
+            break;
+        default: return DAP_ERR_UNSUPPORTED;
+    }
+    return cudaGetLastError() == cudaSuccess ? DAP_OK : DAP_ERR_CUDA;
+}
 
 dap_status launch_append_paged(const void *k_new, const void *v_new, void *k_cache, void *v_cache, int num_pages,
                                int page_size, const int32_t *block_table, int max_pages, const int32_t *pos, int B,

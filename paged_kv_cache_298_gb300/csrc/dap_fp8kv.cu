@@ -1,0 +1,524 @@
+// dap_fp8kv.cu -- GQA decode attention over a paged e4m3 (fp8) K/V cache.
+//
+// Operation: the paged GQA decode of dap_decode.cu with K and V stored as OCP e4m3 codes
+// [num_pages, page_size, Hkv, 128] and one bf16 dequantisation factor per (slot, kv head)
+// for each, laid out [num_pages, Hkv, page_size]: the key of logical position t is
+// e4m3(code) * factor (the decode side of the fp8 cache convention of
+// nvfp4-megamoe-kernel native_swa_decode.py, applied per kv head), likewise the value.
+//
+// Schedule and data movement: the per-sequence split schedule of dap_decode.cu (one CTA
+// per (sequence, kv head, split), split partials merged by the shared combine kernel).
+// Per 64-key tile the producer warp issues four TMA boxes per page run: the K and V code
+// rows (128 bytes each, 128-byte swizzled) and the two factor runs of the kv head, which
+// the [pages, Hkv, page_size] layout keeps contiguous.  Half the bytes of the bf16 cache
+// per key, so six stages keep as many bytes in flight as three bf16 stages.
+//
+// Arithmetic (tensor cores, mma.m16n8k16 in f16): every e4m3 value is an f16 value, so
+// the codes are converted exactly (cvt e4m3x2 -> f16x2) in registers, straight from the
+// swizzled tile.  QK: A = the codes of 16 keys, B = q in f16; the factor of each key and
+// the softmax scale are applied to the fp32 scores (scale after the dot product, as the
+// AstrAI csrc log's numerics commit asks).  The dot product runs over the head dims in a
+// permuted order that lets every lane read 32 contiguous code bytes per key row; q is
+// loaded in the same order.  q is converted to f16 after an exact power-of-two shift that
+// keeps its largest element below 2^15, the shift going back into the scale.  PV: the V
+// codes of 8 keys x 8 dims are moved into the A operand by movmatrix (transposing them),
+// the dims again in a permuted order that the epilogue undoes; the probabilities times
+// each key's V factor form the f16 B operand, measured in a per-warp power-of-two unit
+// (the largest factor seen so far) so they stay within [0, 1); the accumulator is rescaled
+// exactly when the unit grows and multiplied back at the end.
+#include <cuda_fp8.h>
+
+#include "dap_tile.cuh"
+
+namespace dap {
+namespace f8kv {
+
+constexpr int kD = 128;
+
+// e4m3 pair (low byte first) -> f16 pair; exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int G_>
+struct Cfg {
+    static constexpr int D = kD, G = G_, NWC = 4, BT = 64, NS = 6, MINB = 2;
+    static constexpr bool SWZ = true;
+    static constexpr int THREADS = (NWC + 1) * 32;
+    static constexpr int KPW = BT / NWC;                  // 16 keys per consumer warp
+    static constexpr int CODE_BYTES = BT * D;             // one tile of K (or V) codes
+    // The tile's K factors, then its V factors: box j (R <= 64 factors, 2R bytes) lands in
+    // its own 128-byte slot, a tensor copy's shared destination being 128-byte aligned.
+    static constexpr int FSLOT = 128;
+    static constexpr int KS_OFF = 2 * CODE_BYTES;
+    static constexpr int VS_OFF = KS_OFF + (BT / 8) * FSLOT;   // at most BT / 8 boxes (R >= 8)
+    static constexpr int STAGE_BYTES = (VS_OFF + (BT / 8) * FSLOT + 1023) & ~1023;
+    static constexpr int MRG_BYTES = NWC * G * (D / 2 + 2) * 4;  // aliases stage 0 after the last tile
+    static constexpr int MISC_OFF = NS * STAGE_BYTES;
+    static constexpr int BAR_OFF = MISC_OFF + 16;
+    static constexpr int SMEM = BAR_OFF + 2 * NS * 8 + 1024;
+    static_assert(KPW == 16 && MRG_BYTES <= STAGE_BYTES && FSLOT >= 2 * BT, "fp8 tiling");
+};
+
+template <class C>
+struct Consumer {
+    static constexpr int D = C::D, G = C::G, KS = D / 16;
+    uint32_t qb[KS][2];  // q (f16) B fragments, head g, dims 32t+4m .. +3 for step m
+    float acc[KS][4];    // O^T: dims dlo(m,g), dlo+2 x heads 2t, 2t+1, in units of 2^vexp
+    float m_run[2], l_run[2];
+    float qscale;
+    int vexp;
+    int warp, lane, g, t, key0;
+    int f0, f1;  // byte offsets of the factors of keys g and g + 8 inside a factor block
+
+    // R: rows per TMA box (a power of two, 8..64)
+    __device__ __forceinline__ void init(int w, int l, int R) {
+        warp = w;
+        lane = l;
+        g = l >> 2;
+        t = l & 3;
+        key0 = w * C::KPW;
+        const int rb = __ffs(R) - 1;
+        const int r0 = key0 + g, r1 = r0 + 8;
+        f0 = (r0 >> rb) * C::FSLOT + (r0 & (R - 1)) * 2;
+        f1 = (r1 >> rb) * C::FSLOT + (r1 & (R - 1)) * 2;
+    }
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            m_run[j] = -INFINITY;
+            l_run[j] = 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < KS; ++m)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[m][j] = 0.f;
+        vexp = -200;
+    }
+
+    // q of the G heads (head g at base + g * hstride); qs = scale * log2(e).
+    __device__ __forceinline__ void load_q(const __nv_bfloat16 *base, long long hstride, float qs) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (g < G) v = reinterpret_cast<const uint4 *>(base + g * hstride + 32 * t)[i];
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float2 f = bf16x2_to_float2(w[k]);
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        int ex = 0;
+        (void)frexpf(amax, &ex);           // amax < 2^ex
+        const int e = max(0, ex - 15);      // amax * 2^-e < 2^15: f16 keeps every bf16 value
+        const float sh = ldexpf(1.f, -e);
+#pragma unroll
+        for (int m = 0; m < KS; ++m) {
+            const float2 lo = bf16x2_to_float2(w[2 * m]), hi = bf16x2_to_float2(w[2 * m + 1]);
+            qb[m][0] = pack_f16x2(lo.x * sh, lo.y * sh);
+            qb[m][1] = pack_f16x2(hi.x * sh, hi.y * sh);
+        }
+        qscale = qs * ldexpf(1.f, e);
+    }
+
+    // 32 code bytes of `row` for this lane (dims 32t .. 32t+31) from a 128-byte-swizzled tile
+    __device__ __forceinline__ void row_words(const uint8_t *tile, int row, uint32_t (&w)[8]) const {
+        const uint4 a = lds128(tile + row * 128 + (((2 * t) ^ (row & 7)) << 4));
+        const uint4 b = lds128(tile + row * 128 + (((2 * t + 1) ^ (row & 7)) << 4));
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    }
+
+    __device__ __forceinline__ void tile(const uint8_t *stage, int nvalid) {
+        const int nv = nvalid - key0;
+        if (nv <= 0) return;
+        const int r0 = key0 + g, r1 = key0 + g + 8;
+        const bool v0 = g < nv, v1 = g + 8 < nv;
+        const float kfac0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::KS_OFF + f0));
+        const float kfac1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::KS_OFF + f1));
+        const float vfac0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::VS_OFF + f0));
+        const float vfac1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::VS_OFF + f1));
+        // S^T = K . Q^T (keys g, g+8 x heads 2t, 2t+1)
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            uint32_t k0[8], k1[8];
+            row_words(stage, r0, k0);
+            row_words(stage, r1, k1);
+#pragma unroll
+            for (int m = 0; m < KS; ++m) {
+                const uint32_t a[4] = {e4m3x2_to_f16x2(k0[m]), e4m3x2_to_f16x2(k1[m]), e4m3x2_to_f16x2(k0[m] >> 16),
+                                       e4m3x2_to_f16x2(k1[m] >> 16)};
+                mma_f16_16816(c, a, qb[m][0], qb[m][1]);
+            }
+        }
+        const float ks0 = v0 ? kfac0 * qscale : 0.f;
+        const float ks1 = v1 ? kfac1 * qscale : 0.f;
+        float s[4];
+        s[0] = v0 ? c[0] * ks0 : -INFINITY;
+        s[1] = v0 ? c[1] * ks0 : -INFINITY;
+        s[2] = v1 ? c[2] * ks1 : -INFINITY;
+        s[3] = v1 ? c[3] * ks1 : -INFINITY;
+        float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
+        float vm = fmaxf(v0 ? vfac0 : 0.f, v1 ? vfac1 : 0.f);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xFFFFFFFFu, mx[0], o));
+            mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xFFFFFFFFu, mx[1], o));
+            vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o));
+        }
+        // the V-factor unit: a power of two at or above every factor seen
+        float rescale = 1.f;
+        {
+            int e = 0;
+            (void)frexpf(vm, &e);  // vm < 2^e (vm == 0 leaves e = 0)
+            if (vm > 0.f && e > vexp) {
+                rescale = ldexpf(1.f, vexp - e);
+                vexp = e;
+            }
+        }
+        const float vu = vexp > -150 ? ldexpf(1.f, -vexp) : 0.f;  // no positive factor yet: nothing to add
+        float alpha[2], mu[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float m_new = fmaxf(m_run[j], mx[j]);
+            mu[j] = (m_new == -INFINITY) ? 0.f : m_new;
+            alpha[j] = ex2(m_run[j] - mu[j]);
+            m_run[j] = m_new;
+        }
+        const float p0 = ex2(s[0] - mu[0]), p1 = ex2(s[1] - mu[1]);
+        const float p2 = ex2(s[2] - mu[0]), p3 = ex2(s[3] - mu[1]);
+        l_run[0] = l_run[0] * alpha[0] + (p0 + p2);
+        l_run[1] = l_run[1] * alpha[1] + (p1 + p3);
+        const float vs0 = v0 ? vfac0 * vu : 0.f;
+        const float vs1 = v1 ? vfac1 * vu : 0.f;
+        const uint32_t b0 = movmatrix_trans(pack_f16x2(p0 * vs0, p1 * vs0));
+        const uint32_t b1 = movmatrix_trans(pack_f16x2(p2 * vs1, p3 * vs1));
+        const float f0 = alpha[0] * rescale, f1 = alpha[1] * rescale;
+#pragma unroll
+        for (int m = 0; m < KS; ++m) {
+            acc[m][0] *= f0;
+            acc[m][1] *= f1;
+            acc[m][2] *= f0;
+            acc[m][3] *= f1;
+        }
+        // O^T += V^T . P'^T; rows past the end read as code 0 so 0 * V stays 0
+        {
+            uint32_t w0[8], w1[8];
+            row_words(stage + C::CODE_BYTES, r0, w0);
+            row_words(stage + C::CODE_BYTES, r1, w1);
+#pragma unroll
+            for (int m = 0; m < KS; ++m) {
+                const uint32_t x0 = v0 ? w0[m] : 0u, x1 = v1 ? w1[m] : 0u;
+                const uint32_t a[4] = {movmatrix_trans(e4m3x2_to_f16x2(x0)), movmatrix_trans(e4m3x2_to_f16x2(x0 >> 16)),
+                                       movmatrix_trans(e4m3x2_to_f16x2(x1)), movmatrix_trans(e4m3x2_to_f16x2(x1 >> 16))};
+                mma_f16_16816(acc[m], a, b0, b1);
+            }
+        }
+    }
+
+    // Merge the four warps per head in two halves of D (the row merge of the bf16 path);
+    // emit(head, d, a0, a1, M, l) gets dims d, d+1 in natural order.
+    template <class Sync, class Emit>
+    __device__ __forceinline__ bool finish(float *mrg, Sync sync, Emit emit) {
+        constexpr int NWC = C::NWC, DH = D / 2;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l_run[0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[0], o);
+            l_run[1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[1], o);
+        }
+        const float unit = ldexpf(1.f, vexp);
+        float *macc = mrg;                // [NWC][G][D/2]
+        float *mml = mrg + NWC * G * DH;  // [NWC][G][2]
+        if (g == 0) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                if (2 * t + j < G) {
+                    mml[(warp * G + 2 * t + j) * 2 + 0] = m_run[j];
+                    mml[(warp * G + 2 * t + j) * 2 + 1] = l_run[j];
+                }
+        }
+        const int tid = warp * 32 + lane;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            if ((g >> 2) == half) {  // this lane's dims 32(g/2) + 4m + (g&1) (+2) lie in this half
+#pragma unroll
+                for (int m = 0; m < KS; ++m) {
+                    const int dlo = 32 * (g >> 1) + 4 * m + (g & 1) - half * DH;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        if (2 * t + j < G) {
+                            float *row = macc + (warp * G + 2 * t + j) * DH;
+                            row[dlo] = acc[m][j] * unit;
+                            row[dlo + 2] = acc[m][j + 2] * unit;
+                        }
+                    }
+                }
+            }
+            if (!sync()) return false;
+            for (int e = tid * 2; e < G * DH; e += NWC * 32 * 2) {
+                const int hh = e / DH, dd = e % DH;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < NWC; ++w) M = fmaxf(M, mml[(w * G + hh) * 2]);
+                const float Mu = (M == -INFINITY) ? 0.f : M;
+                float a0 = 0.f, a1 = 0.f, lv = 0.f;
+#pragma unroll
+                for (int w = 0; w < NWC; ++w) {
+                    const float f = ex2(mml[(w * G + hh) * 2] - Mu);
+                    lv = fmaf(f, mml[(w * G + hh) * 2 + 1], lv);
+                    const float2 x = *reinterpret_cast<const float2 *>(macc + (w * G + hh) * DH + dd);
+                    a0 = fmaf(f, x.x, a0);
+                    a1 = fmaf(f, x.y, a1);
+                }
+                emit(hh, half * DH + dd, a0, a1, M, lv);
+            }
+            if (!sync()) return false;
+        }
+        return true;
+    }
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, C::MINB)
+    fp8kv_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                 const __grid_constant__ CUtensorMap mapKS, const __grid_constant__ CUtensorMap mapVS,
+                 const SplitParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = aligned_smem<C>(smem_raw);
+    constexpr int G = C::G, NWC = C::NWC, BT = C::BT, NS = C::NS, D = C::D;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int units = p.B * p.Hkv;
+    const int s = blockIdx.x / units;
+    const int rem = blockIdx.x - s * units;
+    const int b = rem / p.Hkv;
+    const int kvh = rem - b * p.Hkv;
+    int L = p.seq_lens[b];
+    const int R = p.box_rows;
+    int pg_first = 0;  // loaded with the length (entries past the end are read, not used)
+    if (warp == NWC && lane * R < BT) {
+        const long long t = (long long)s * p.chunk + lane * R;
+        if (t < (long long)p.max_pages * p.page_size)
+            pg_first = __ldg(p.block_table + (long long)b * p.max_pages + t / p.page_size);
+    }
+    if (L < 0 || L > p.max_kv_len) {
+        if (threadIdx.x == 0 && s == 0 && kvh == 0) flag_error(DAP_DEVERR_SEQLEN);
+        L = min(max(L, 0), p.max_kv_len);
+    }
+    const int nsplit = max(1, (L + p.chunk - 1) / p.chunk);
+    if (s >= nsplit) return;
+    const int tok0 = s * p.chunk;
+    const int tok1 = min(L, tok0 + p.chunk);
+    const int ntiles = tok1 > tok0 ? (tok1 - tok0 + BT - 1) / BT : 0;
+
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *empty = full + NS;
+    int *misc = reinterpret_cast<int *>(smem + C::MISC_OFF);  // [0] tiles issued, [1] abort
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NWC);
+        }
+        misc[0] = 0;
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == NWC) {  // ---- producer warp
+        if (lane == 0) {
+            prefetch_tensormap(&mapK);
+            prefetch_tensormap(&mapV);
+            prefetch_tensormap(&mapKS);
+            prefetch_tensormap(&mapVS);
+        }
+        const int32_t *table = p.block_table + (long long)b * p.max_pages;
+        auto lookup = [&](int tile) -> int {
+            const int t = tok0 + tile * BT + lane * R;
+            if (lane * R >= BT || t >= tok1) return 0;
+            int pg = tile == 0 ? pg_first : __ldg(table + t / p.page_size);
+            if (pg < 0 || pg >= p.num_pages) {
+                flag_error(DAP_DEVERR_PAGE);
+                pg = 0;
+            }
+            return pg;
+        };
+        int pg_next = ntiles > 0 ? lookup(0) : 0;
+        int issued = 0;
+        for (int i = 0; i < ntiles; ++i) {
+            const int st = i % NS;
+            const int pg = pg_next;
+            if (i + 1 < ntiles) pg_next = lookup(i + 1);
+            if (i >= NS && !__all_sync(0xFFFFFFFFu, mbar_wait(&empty[st], ((i / NS) - 1) & 1))) {
+                misc[1] = 1;
+                break;
+            }
+            const int t = tok0 + i * BT;
+            const int nbox = (min(BT, tok1 - t) + R - 1) / R;
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)(nbox * R * (2 * D + 4)));
+            __syncwarp();
+            if (lane < nbox) {
+                uint8_t *stage = smem + st * C::STAGE_BYTES;
+                const int row = (t + lane * R) % p.page_size;
+                tma_load_4d(stage + lane * R * D, &mapK, 0, kvh, row, pg, &full[st]);
+                tma_load_4d(stage + C::CODE_BYTES + lane * R * D, &mapV, 0, kvh, row, pg, &full[st]);
+                tma_load_3d(stage + C::KS_OFF + lane * C::FSLOT, &mapKS, row, kvh, pg, &full[st]);
+                tma_load_3d(stage + C::VS_OFF + lane * C::FSLOT, &mapVS, row, kvh, pg, &full[st]);
+            }
+            issued = i + 1;
+        }
+        if (lane == 0) misc[0] = issued;
+        __syncthreads();
+        return;
+    }
+
+    // ---- consumer warps
+    Consumer<C> cs;
+    cs.init(warp, lane, R);
+    cs.reset();
+    cs.load_q(p.q + (long long)b * p.q_sb + (long long)kvh * G * p.q_sh, p.q_sh, p.qscale);
+    int consumed = 0;
+    for (int i = 0; i < ntiles; ++i) {
+        const int st = i % NS;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[st], (i / NS) & 1))) {
+            misc[1] = 1;
+            break;
+        }
+        cs.tile(smem + st * C::STAGE_BYTES, min(BT, tok1 - (tok0 + i * BT)));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        consumed = i + 1;
+    }
+    __syncthreads();  // every tile consumed; stage 0 is free for the merge
+    if (misc[1]) {
+        if (threadIdx.x == 0)
+            for (int i = consumed; i < misc[0]; ++i) (void)mbar_wait(&full[i % NS], (i / NS) & 1);
+        return;
+    }
+    const bool direct = (nsplit == 1);
+    cs.finish(reinterpret_cast<float *>(smem), [] { named_sync(1, NWC * 32); return true; },
+              [&](int hh, int d, float a0, float a1, float M, float lv) {
+                  const int hq = kvh * G + hh;
+                  if (direct) {
+                      store_out_pair(p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh + d, a0, a1, lv);
+                  } else {
+                      const long long row = ((long long)b * p.num_splits + s) * p.Hq + hq;
+                      *reinterpret_cast<float2 *>(p.o_part + row * D + d) = make_float2(a0, a1);
+                      if (d == 0) *reinterpret_cast<float2 *>(p.ml_part + row * 2) = make_float2(M, lv);
+                  }
+              });
+}
+
+// ---- host side -------------------------------------------------------------------------
+
+namespace {
+
+bool encode_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, int rank, const cuuint64_t *dims,
+                const cuuint64_t *strides_bytes, const cuuint32_t *box, CUtensorMapSwizzle swz) {
+    EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+    if (!enc) return false;
+    const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+    return enc(map, dtype, (cuuint32_t)rank, const_cast<void *>(base), dims, strides_bytes, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// codes [P, ps, Hkv, 128] bytes viewed as [128, Hkv, ps, P]; box [128, 1, R, 1], 128-byte swizzle
+bool encode_codes(CUtensorMap *map, const void *base, int Hkv, int ps, int P, int R) {
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)Hkv, (cuuint64_t)ps, (cuuint64_t)P};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD, (cuuint64_t)Hkv * kD, (cuuint64_t)ps * Hkv * kD};
+    const cuuint32_t box[4] = {(cuuint32_t)kD, 1u, (cuuint32_t)R, 1u};
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// factors [P, Hkv, ps] bf16 viewed as [ps, Hkv, P]; box [R, 1, 1]
+bool encode_factors(CUtensorMap *map, const void *base, int Hkv, int ps, int P, int R) {
+    const cuuint64_t dims[3] = {(cuuint64_t)ps, (cuuint64_t)Hkv, (cuuint64_t)P};
+    const cuuint64_t strides[2] = {(cuuint64_t)ps * 2, (cuuint64_t)Hkv * ps * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)R, 1u, 1u};
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, 3, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+template <int G>
+dap_status launch_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
+    using C = Cfg<G>;
+    const int R = gcd_int(a.page_size, C::BT);
+    p.box_rows = R;
+    CUtensorMap mk, mv, mks, mvs;
+    if (!encode_codes(&mk, a.k, a.Hkv, a.page_size, a.num_pages, R) ||
+        !encode_codes(&mv, a.v, a.Hkv, a.page_size, a.num_pages, R) ||
+        !encode_factors(&mks, a.k_scale, a.Hkv, a.page_size, a.num_pages, R) ||
+        !encode_factors(&mvs, a.v_scale, a.Hkv, a.page_size, a.num_pages, R))
+        return DAP_ERR_CUDA;
+    auto kern = fp8kv_kernel<C>;
+    static int occ = 0;
+    if (prepare_kernel(kern, C::THREADS, C::SMEM, &occ) <= 0) return DAP_ERR_CUDA;
+    const long long grid = (long long)a.B * a.Hkv * a.num_splits;
+    if (grid > 0x7FFFFFFFLL) return DAP_ERR_SHAPE;
+    p.o_part = static_cast<float *>(a.workspace);
+    p.ml_part = a.num_splits > 1 ? reinterpret_cast<float *>(static_cast<char *>(a.workspace) +
+                                                             partial_acc_bytes(a.B, a.Hq, a.D, a.num_splits))
+                                 : nullptr;
+    if (g_trace.split_begin) cudaEventRecord(g_trace.split_begin, stream);
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(mk, mv, mks, mvs, p);
+    if (cudaGetLastError() != cudaSuccess) return DAP_ERR_CUDA;
+    if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
+    if (a.num_splits > 1) {
+        const dim3 cgrid((unsigned)(((long long)a.B * a.Hq + 7) / 8));
+        if (launch_dependent(combine_kernel<kD>, cgrid, dim3(256), stream, p) != cudaSuccess) return DAP_ERR_CUDA;
+    }
+    if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);
+    return DAP_OK;
+}
+
+}  // namespace
+}  // namespace f8kv
+
+dap_status launch_decode_fp8kv(const DecodeArgs &a, cudaStream_t stream) {
+    if (a.D != f8kv::kD) return DAP_ERR_UNSUPPORTED;
+    SplitParams p = make_params(a);
+    switch (a.Hq / a.Hkv) {
+        case 1: return f8kv::launch_g<1>(a, p, stream);
+        case 2: return f8kv::launch_g<2>(a, p, stream);
+        case 4: return f8kv::launch_g<4>(a, p, stream);
+        case 8: return f8kv::launch_g<8>(a, p, stream);
+    }
+    return DAP_ERR_UNSUPPORTED;
+}
+
+bool read_errors_fp8kv(unsigned int *flags, bool clear) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_errors, sizeof v) != cudaSuccess) return false;
+    if (clear) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(g_device_errors, &z, sizeof z) != cudaSuccess) return false;
+    }
+    *flags |= v;
+    return true;
+}
+
+}  // namespace dap

@@ -59,6 +59,8 @@ struct DecodeArgs {
     void *workspace;
     void *out;
     long long o_sb, o_sh;
+    // e4m3 cache only: bf16 dequantisation factors [num_pages, Hkv, page_size] of k and v
+    const void *k_scale, *v_scale;
     // multi-token decode only: packed-q work map (q_sb / o_sb are then token strides)
     const int32_t *qo_indptr, *tile_batch, *tile_index;
     int num_tiles, total_q;
@@ -66,6 +68,7 @@ struct DecodeArgs {
 
 dap_status launch_decode(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_multi(const DecodeArgs &a, cudaStream_t stream);
+dap_status launch_decode_fp8kv(const DecodeArgs &a, cudaStream_t stream);
 int multi_tokens_per_tile(int G);
 
 // Events of dap_set_trace_events (nullptr when tracing is off).
@@ -92,7 +95,12 @@ dap_status launch_append_paged(const void *k_new, const void *v_new, void *k_cac
                                int Hkv, int D, cudaStream_t stream);
 dap_status launch_append_fp8(const void *rows, uint8_t *kv_cache, void *inv_scale, const int64_t *slots, int T,
                              int HD, int num_blocks, int block_size, cudaStream_t stream);
+dap_status launch_append_paged_fp8(const void *k_new, const void *v_new, uint8_t *k_codes, uint8_t *v_codes,
+                                   void *k_scale, void *v_scale, int num_pages, int page_size,
+                                   const int32_t *block_table, int max_pages, const int32_t *pos, int B, int Hkv,
+                                   int D, cudaStream_t stream);
 bool read_errors_multi(unsigned int *flags, bool clear);
+bool read_errors_fp8kv(unsigned int *flags, bool clear);
 bool read_errors_append(unsigned int *flags, bool clear);
 
 // Host readers of each translation unit's device error word (cudaMemcpyFromSymbol on the

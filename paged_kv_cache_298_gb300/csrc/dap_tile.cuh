@@ -126,6 +126,40 @@ struct RowMerge {
     }
 };
 
+// Per-sequence schedule: merge the splits of every (sequence, head) row that more than one
+// CTA worked on, one warp per row; waits for the split grid (programmatic dependent launch).
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= p.B * p.Hq) return;
+    const int b = gw / p.Hq, hq = gw - b * p.Hq;
+    const int L = min(max(p.seq_lens[b], 0), p.max_kv_len);
+    const int nsplit = max(1, (L + p.chunk - 1) / p.chunk);
+    if (nsplit == 1) return;
+    const long long row0 = (long long)b * p.num_splits * p.Hq + hq;
+    float M = -INFINITY;
+    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, p.ml_part[(row0 + (long long)s * p.Hq) * 2]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    RowMerge<D> r;
+    r.begin(M);
+    for (int s0 = 0; s0 < nsplit; s0 += 8) {
+        const float *o[8];
+        float2 ml[8];
+        const int n = min(8, nsplit - s0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const long long row = row0 + (long long)min(s0 + k, nsplit - 1) * p.Hq;
+            o[k] = p.o_part + row * D;
+            ml[k] = *reinterpret_cast<const float2 *>(p.ml_part + row * 2);
+        }
+        r.add_batch(o, ml, n, lane);
+    }
+    r.store(p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh, lane);
+}
+
 // ---- host side ----------------------------------------------------------------------------
 
 namespace {

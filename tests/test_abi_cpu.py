@@ -215,3 +215,46 @@ def test_multi_validation(lib, kw, status):
 
 def test_multi_empty_is_a_no_op(lib):
     assert multi_call(lib, totq=0, ntiles=0, q=None, out=None, k=None, qi=None, tb=None, ti=None) == 0
+
+
+# ---- fp8 (e4m3) GQA cache: validation --------------------------------------------------
+
+def fp8kv_call(lib, **kw):
+    a = dict(q=FAKE, qsb=32 * 128, qsh=128, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE, P=64, ps=16, table=FAKE, maxp=8,
+             lens=FAKE, maxlen=100, B=2, Hq=32, Hkv=8, D=128, scale=0.088, S=1, ws=None, wsb=0, out=FAKE,
+             osb=32 * 128, osh=128)
+    a.update(kw)
+    return lib.decode_attn_paged_fp8kv(a["q"], a["qsb"], a["qsh"], a["kc"], a["vc"], a["ks"], a["vs"], a["P"],
+                                       a["ps"], a["table"], a["maxp"], a["lens"], a["maxlen"], a["B"], a["Hq"],
+                                       a["Hkv"], a["D"], a["scale"], a["S"], a["ws"], a["wsb"], a["out"], a["osb"],
+                                       a["osh"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=-1), 2), (dict(Hq=30), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(S=-1), 2), (dict(P=0), 2),
+    (dict(kc=None), 1), (dict(ks=None), 1), (dict(vs=None), 1), (dict(table=None), 1), (dict(q=None), 1),
+    (dict(D=64, qsb=32 * 64, qsh=64, osb=32 * 64, osh=64), 3), (dict(ps=12, maxlen=90), 3), (dict(Hq=64, Hkv=4), 3),
+    (dict(ks=ctypes.c_void_p((1 << 20) + 8)), 5), (dict(kc=ctypes.c_void_p((1 << 20) + 4)), 5),
+    (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=64), 4),
+])
+def test_fp8kv_validation(lib, kw, status):
+    assert fp8kv_call(lib, **kw) == status
+
+
+def test_fp8kv_empty_batch_is_a_no_op(lib):
+    assert fp8kv_call(lib, B=0, q=None, out=None, kc=None, vc=None, ks=None, vs=None, lens=None, table=None) == 0
+
+
+def test_append_paged_fp8_validation(lib):
+    f = lib.kv_append_paged_fp8
+    ok = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, 16, FAKE, 4, FAKE, 2, 2, 128, None]
+    def call(i=None, v=None):
+        a = list(ok)
+        if i is not None:
+            a[i] = v
+        return f(*a)
+    assert call(11, -1) == 2 and call(6, 0) == 2
+    assert call(13, 96) == 3
+    assert call(0, None) == 1 and call(4, None) == 1
+    assert call(11, 0) == 0
+    assert call(2, ctypes.c_void_p((1 << 20) + 4)) == 5 and call(4, ctypes.c_void_p((1 << 20) + 1)) == 5
