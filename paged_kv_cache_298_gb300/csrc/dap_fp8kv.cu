@@ -13,21 +13,21 @@
 // the [pages, Hkv, page_size] layout keeps contiguous.  Half the bytes of the bf16 cache
 // per key, so six stages keep as many bytes in flight as three bf16 stages.
 //
-// Arithmetic (tensor cores, mma.m16n8k16 in f16): every e4m3 value is an f16 value, so
-// the codes are converted exactly (cvt e4m3x2 -> f16x2) in registers, straight from the
-// swizzled tile.  QK: A = the codes of 16 keys, B = q in f16; the factor of each key and
-// the softmax scale are applied to the fp32 scores (scale after the dot product, as the
-// AstrAI csrc log's numerics commit asks).  The dot product runs over the head dims in a
-// permuted order that lets every lane read 32 contiguous code bytes per key row; q is
-// loaded in the same order.  q is converted to f16 after an exact power-of-two shift that
-// keeps its largest element below 2^15, the shift going back into the scale.  PV: the V
-// codes of 8 keys x 8 dims are moved into the A operand by movmatrix (transposing them),
-// the dims again in a permuted order that the epilogue undoes; the probabilities times
-// each key's V factor form the f16 B operand, measured in a per-warp power-of-two unit
-// (the largest factor seen so far) so they stay within [0, 1); the accumulator is rescaled
-// exactly when the unit grows and multiplied back at the end.
-#include <cuda_fp8.h>
-
+// Arithmetic (tensor cores, mma.m16n8k16 in f16): an e4m3 code's sign and 7 magnitude bits
+// placed into f16 bits 15 and 13..7 give an f16 equal to the code's value times 2^-8, so
+// four codes become two f16 pairs with five integer operations, exactly, straight from the
+// swizzled tile.  QK: A = the codes of 16 keys, B = q in f16; the factor of each key, the
+// 2^8 and the softmax scale are applied to the fp32 scores (scale after the dot product, as
+// the AstrAI csrc log's numerics commit asks).  The dot product runs over the head dims in
+// the order the conversion yields (pairs of dims 4j, 4j+2 and 4j+1, 4j+3 of each lane's 32
+// contiguous bytes); q is loaded in the same order, converted to f16 after an exact
+// power-of-two shift that keeps its largest element below 2^15 (the shift goes back into
+// the scale).  PV: the V codes of 8 keys x 8 dims are moved into the A operand by
+// movmatrix (transposing them), the dims in the same permuted order, which the epilogue
+// undoes; the probabilities times each key's V factor form the f16 B operand, measured in
+// a per-warp power-of-two unit (above the largest factor seen so far) so they stay within
+// [0, 1); the accumulator is rescaled exactly when the unit grows and multiplied back at
+// the end.
 #include "dap_tile.cuh"
 
 namespace dap {
@@ -35,11 +35,20 @@ namespace f8kv {
 
 constexpr int kD = 128;
 
-// e4m3 pair (low byte first) -> f16 pair; exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Four e4m3 codes [c0 c1 c2 c3] (low byte first) -> two f16 pairs (c0, c2) and (c1, c3),
+// each the code's value times 2^-8, exactly: a code's sign goes to the f16 sign bit and its
+// 7 magnitude bits (4 exponent, 3 mantissa) to f16 bits 13..7, so the f16 exponent equals
+// the e4m3 one (bias 15 against 7) and subnormals map to subnormals.  (The NaN codes 0x7F /
+// 0xFF read as +-480 * 2^-8; the cache writers never produce them.)
+__device__ __forceinline__ uint32_t e4m3_pair02(uint32_t w) {
+    return ((w << 8) & 0x80008000u) | ((w << 7) & 0x3F803F80u);
 }
+__device__ __forceinline__ uint32_t e4m3_pair13(uint32_t w) {
+    return (w & 0x80008000u) | ((w >> 1) & 0x3F803F80u);
+}
+
+// 2^(E - 127) for a biased exponent E in 1..254 (exact)
+__device__ __forceinline__ float pow2_biased(int E) { return __int_as_float(E << 23); }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     const __half2 v = __floats2half2_rn(lo, hi);
@@ -56,7 +65,7 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)
 
 template <int G_>
 struct Cfg {
-    static constexpr int D = kD, G = G_, NWC = 4, BT = 64, NS = 6, MINB = 2;
+    static constexpr int D = kD, G = G_, NWC = 4, BT = 64, NS = 4, MINB = 3;
     static constexpr bool SWZ = true;
     static constexpr int THREADS = (NWC + 1) * 32;
     static constexpr int KPW = BT / NWC;                  // 16 keys per consumer warp
@@ -77,13 +86,15 @@ struct Cfg {
 template <class C>
 struct Consumer {
     static constexpr int D = C::D, G = C::G, KS = D / 16;
-    uint32_t qb[KS][2];  // q (f16) B fragments, head g, dims 32t+4m .. +3 for step m
-    float acc[KS][4];    // O^T: dims dlo(m,g), dlo+2 x heads 2t, 2t+1, in units of 2^vexp
+    // The dot product over dims runs in the order the code conversion yields: at step m the
+    // k indices 2t, 2t+1 are dims 32t+4m+0, +2 and 2t+8, 2t+9 are dims 32t+4m+1, +3.
+    uint32_t qb[KS][2];  // q (f16) B fragments of head g in that order
+    float acc[KS][4];    // O^T: dims dlo(m,g), dlo+1 x heads 2t, 2t+1, in units of 2^(vE-127-8)
     float m_run[2], l_run[2];
-    float qscale;
-    int vexp;
+    float qscale;        // scale * log2(e) * 2^qshift * 2^8 (the 2^-8 of the K conversion)
+    int vE;              // biased exponent of the V-factor unit (0 = none yet)
     int warp, lane, g, t, key0;
-    int f0, f1;  // byte offsets of the factors of keys g and g + 8 inside a factor block
+    int f0, f1;          // byte offsets of the factors of keys g and g + 8 inside a factor block
 
     // R: rows per TMA box (a power of two, 8..64)
     __device__ __forceinline__ void init(int w, int l, int R) {
@@ -108,7 +119,7 @@ struct Consumer {
         for (int m = 0; m < KS; ++m)
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[m][j] = 0.f;
-        vexp = -200;
+        vE = 0;
     }
 
     // q of the G heads (head g at base + g * hstride); qs = scale * log2(e).
@@ -131,17 +142,17 @@ struct Consumer {
         }
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        int ex = 0;
-        (void)frexpf(amax, &ex);           // amax < 2^ex
-        const int e = max(0, ex - 15);      // amax * 2^-e < 2^15: f16 keeps every bf16 value
-        const float sh = ldexpf(1.f, -e);
+        // shift so that amax * 2^-e < 2^15: f16 then holds every bf16 element exactly
+        const int eb = (__float_as_int(amax) >> 23) & 0xFF;  // amax < 2^(eb - 126)
+        const int e = max(0, eb - 126 - 15);
+        const float sh = pow2_biased(127 - e);
 #pragma unroll
         for (int m = 0; m < KS; ++m) {
             const float2 lo = bf16x2_to_float2(w[2 * m]), hi = bf16x2_to_float2(w[2 * m + 1]);
-            qb[m][0] = pack_f16x2(lo.x * sh, lo.y * sh);
-            qb[m][1] = pack_f16x2(hi.x * sh, hi.y * sh);
+            qb[m][0] = pack_f16x2(lo.x * sh, hi.x * sh);  // dims 4m+0, 4m+2 (of 32t..)
+            qb[m][1] = pack_f16x2(lo.y * sh, hi.y * sh);  // dims 4m+1, 4m+3
         }
-        qscale = qs * ldexpf(1.f, e);
+        qscale = qs * pow2_biased(127 + e + 8);
     }
 
     // 32 code bytes of `row` for this lane (dims 32t .. 32t+31) from a 128-byte-swizzled tile
@@ -161,21 +172,31 @@ struct Consumer {
         const float kfac1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::KS_OFF + f1));
         const float vfac0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::VS_OFF + f0));
         const float vfac1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::VS_OFF + f1));
-        // S^T = K . Q^T (keys g, g+8 x heads 2t, 2t+1)
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        // the V rows are read up front so their latency hides under QK and the softmax
+        uint32_t w0[8], w1[8];
+        row_words(stage + C::CODE_BYTES, r0, w0);
+        row_words(stage + C::CODE_BYTES, r1, w1);
+        // S^T = K . Q^T (keys g, g+8 x heads 2t, 2t+1), K in units of 2^-8; two independent
+        // accumulation chains (even / odd k-steps) halve the dependent MMA latency
+        float c[4];
         {
             uint32_t k0[8], k1[8];
             row_words(stage, r0, k0);
             row_words(stage, r1, k1);
+            float ce[4] = {0.f, 0.f, 0.f, 0.f}, co[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int m = 0; m < KS; ++m) {
-                const uint32_t a[4] = {e4m3x2_to_f16x2(k0[m]), e4m3x2_to_f16x2(k1[m]), e4m3x2_to_f16x2(k0[m] >> 16),
-                                       e4m3x2_to_f16x2(k1[m] >> 16)};
-                mma_f16_16816(c, a, qb[m][0], qb[m][1]);
+            for (int m = 0; m < KS; m += 2) {
+                const uint32_t a[4] = {e4m3_pair02(k0[m]), e4m3_pair02(k1[m]), e4m3_pair13(k0[m]),
+                                       e4m3_pair13(k1[m])};
+                mma_f16_16816(ce, a, qb[m][0], qb[m][1]);
+                const uint32_t b[4] = {e4m3_pair02(k0[m + 1]), e4m3_pair02(k1[m + 1]), e4m3_pair13(k0[m + 1]),
+                                       e4m3_pair13(k1[m + 1])};
+                mma_f16_16816(co, b, qb[m + 1][0], qb[m + 1][1]);
             }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) c[j] = ce[j] + co[j];
         }
-        const float ks0 = v0 ? kfac0 * qscale : 0.f;
-        const float ks1 = v1 ? kfac1 * qscale : 0.f;
+        const float ks0 = kfac0 * qscale, ks1 = kfac1 * qscale;
         float s[4];
         s[0] = v0 ? c[0] * ks0 : -INFINITY;
         s[1] = v0 ? c[1] * ks0 : -INFINITY;
@@ -189,17 +210,16 @@ struct Consumer {
             mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xFFFFFFFFu, mx[1], o));
             vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o));
         }
-        // the V-factor unit: a power of two at or above every factor seen
+        // V-factor unit: a power of two above every factor seen (vm < 2^(E - 127))
         float rescale = 1.f;
         {
-            int e = 0;
-            (void)frexpf(vm, &e);  // vm < 2^e (vm == 0 leaves e = 0)
-            if (vm > 0.f && e > vexp) {
-                rescale = ldexpf(1.f, vexp - e);
-                vexp = e;
+            const int E = min(254, ((__float_as_int(vm) >> 23) & 0xFF) + 1);
+            if (vm > 0.f && E > vE) {
+                rescale = vE - E + 127 >= 1 ? pow2_biased(vE - E + 127) : 0.f;
+                vE = E;
             }
         }
-        const float vu = vexp > -150 ? ldexpf(1.f, -vexp) : 0.f;  // no positive factor yet: nothing to add
+        const float vu = vE > 0 ? pow2_biased(254 - vE) : 0.f;  // 2^(127 - vE): factor -> [0, 1)
         float alpha[2], mu[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -216,24 +236,29 @@ struct Consumer {
         const float vs1 = v1 ? vfac1 * vu : 0.f;
         const uint32_t b0 = movmatrix_trans(pack_f16x2(p0 * vs0, p1 * vs0));
         const uint32_t b1 = movmatrix_trans(pack_f16x2(p2 * vs1, p3 * vs1));
-        const float f0 = alpha[0] * rescale, f1 = alpha[1] * rescale;
+        const float fa = alpha[0] * rescale, fb = alpha[1] * rescale;
+        if (__any_sync(0xFFFFFFFFu, fa != 1.f || fb != 1.f)) {
 #pragma unroll
-        for (int m = 0; m < KS; ++m) {
-            acc[m][0] *= f0;
-            acc[m][1] *= f1;
-            acc[m][2] *= f0;
-            acc[m][3] *= f1;
+            for (int m = 0; m < KS; ++m) {
+                acc[m][0] *= fa;
+                acc[m][1] *= fb;
+                acc[m][2] *= fa;
+                acc[m][3] *= fb;
+            }
         }
         // O^T += V^T . P'^T; rows past the end read as code 0 so 0 * V stays 0
         {
-            uint32_t w0[8], w1[8];
-            row_words(stage + C::CODE_BYTES, r0, w0);
-            row_words(stage + C::CODE_BYTES, r1, w1);
+            if (nv < 16) {
+#pragma unroll
+                for (int m = 0; m < KS; ++m) {
+                    w0[m] = v0 ? w0[m] : 0u;
+                    w1[m] = v1 ? w1[m] : 0u;
+                }
+            }
 #pragma unroll
             for (int m = 0; m < KS; ++m) {
-                const uint32_t x0 = v0 ? w0[m] : 0u, x1 = v1 ? w1[m] : 0u;
-                const uint32_t a[4] = {movmatrix_trans(e4m3x2_to_f16x2(x0)), movmatrix_trans(e4m3x2_to_f16x2(x0 >> 16)),
-                                       movmatrix_trans(e4m3x2_to_f16x2(x1)), movmatrix_trans(e4m3x2_to_f16x2(x1 >> 16))};
+                const uint32_t a[4] = {movmatrix_trans(e4m3_pair02(w0[m])), movmatrix_trans(e4m3_pair13(w0[m])),
+                                       movmatrix_trans(e4m3_pair02(w1[m])), movmatrix_trans(e4m3_pair13(w1[m]))};
                 mma_f16_16816(acc[m], a, b0, b1);
             }
         }
@@ -249,7 +274,8 @@ struct Consumer {
             l_run[0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[0], o);
             l_run[1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[1], o);
         }
-        const float unit = ldexpf(1.f, vexp);
+        // back from units of 2^(vE - 127) (V factors) and 2^-8 (V codes)
+        const float unit = vE > 0 ? pow2_biased(min(vE + 8, 254)) : 0.f;
         float *macc = mrg;                // [NWC][G][D/2]
         float *mml = mrg + NWC * G * DH;  // [NWC][G][2]
         if (g == 0) {
@@ -263,16 +289,16 @@ struct Consumer {
         const int tid = warp * 32 + lane;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            if ((g >> 2) == half) {  // this lane's dims 32(g/2) + 4m + (g&1) (+2) lie in this half
+            if ((g >> 2) == half) {  // this lane's dims 32(g/2) + 4m + 2(g&1) (+1) lie in this half
 #pragma unroll
                 for (int m = 0; m < KS; ++m) {
-                    const int dlo = 32 * (g >> 1) + 4 * m + (g & 1) - half * DH;
+                    const int dlo = 32 * (g >> 1) + 4 * m + 2 * (g & 1) - half * DH;
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         if (2 * t + j < G) {
                             float *row = macc + (warp * G + 2 * t + j) * DH;
                             row[dlo] = acc[m][j] * unit;
-                            row[dlo + 2] = acc[m][j + 2] * unit;
+                            row[dlo + 1] = acc[m][j + 2] * unit;
                         }
                     }
                 }
