@@ -63,38 +63,44 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int G_>
+// HG kv heads per CTA (2 when Hkv is even): one TMA box carries both heads' rows of a page
+// run, the shared tile is head-major [box][head][row][128 B], and every consumer warp runs
+// the heads as independent streams over the same 16 keys.
+template <int G_, int HG_>
 struct Cfg {
-    static constexpr int D = kD, G = G_, NWC = 4, BT = 64, NS = 4, MINB = 3;
+    static constexpr int D = kD, G = G_, HG = HG_, NWC = 4, BT = 64;
+    static constexpr int NS = HG == 2 ? 3 : 4, MINB = HG == 2 ? 2 : 3;
     static constexpr bool SWZ = true;
     static constexpr int THREADS = (NWC + 1) * 32;
     static constexpr int KPW = BT / NWC;                  // 16 keys per consumer warp
-    static constexpr int CODE_BYTES = BT * D;             // one tile of K (or V) codes
-    // The tile's K factors, then its V factors: box j (R <= 64 factors, 2R bytes) lands in
-    // its own 128-byte slot, a tensor copy's shared destination being 128-byte aligned.
-    static constexpr int FSLOT = 128;
+    static constexpr int CODE_BYTES = BT * HG * D;        // one tile of K (or V) codes
+    // The tile's K factors, then its V factors: box j (HG x R factors, R <= 64) lands in its
+    // own slot, a tensor copy's shared destination being 128-byte aligned.
+    static constexpr int FSLOT = 128 * HG;
     static constexpr int KS_OFF = 2 * CODE_BYTES;
     static constexpr int VS_OFF = KS_OFF + (BT / 8) * FSLOT;   // at most BT / 8 boxes (R >= 8)
     static constexpr int STAGE_BYTES = (VS_OFF + (BT / 8) * FSLOT + 1023) & ~1023;
-    static constexpr int MRG_BYTES = NWC * G * (D / 2 + 2) * 4;  // aliases stage 0 after the last tile
+    static constexpr int MRG_BYTES = NWC * HG * G * (D / 2 + 2) * 4;  // aliases stage 0 after the last tile
     static constexpr int MISC_OFF = NS * STAGE_BYTES;
     static constexpr int BAR_OFF = MISC_OFF + 16;
     static constexpr int SMEM = BAR_OFF + 2 * NS * 8 + 1024;
-    static_assert(KPW == 16 && MRG_BYTES <= STAGE_BYTES && FSLOT >= 2 * BT, "fp8 tiling");
+    static_assert(KPW == 16 && MRG_BYTES <= STAGE_BYTES && FSLOT >= 2 * HG * BT, "fp8 tiling");
 };
 
 template <class C>
 struct Consumer {
-    static constexpr int D = C::D, G = C::G, KS = D / 16;
+    static constexpr int D = C::D, G = C::G, HG = C::HG, KS = D / 16;
     // The dot product over dims runs in the order the code conversion yields: at step m the
     // k indices 2t, 2t+1 are dims 32t+4m+0, +2 and 2t+8, 2t+9 are dims 32t+4m+1, +3.
-    uint32_t qb[KS][2];  // q (f16) B fragments of head g in that order
-    float acc[KS][4];    // O^T: dims dlo(m,g), dlo+1 x heads 2t, 2t+1, in units of 2^(vE-127-8)
-    float m_run[2], l_run[2];
-    float qscale;        // scale * log2(e) * 2^qshift * 2^8 (the 2^-8 of the K conversion)
-    int vE;              // biased exponent of the V-factor unit (0 = none yet)
+    uint32_t qb[HG][KS][2];  // q (f16) B fragments of head g of each kv head, in that order
+    float acc[HG][KS][4];    // O^T: dims dlo(m,g), dlo+1 x heads 2t, 2t+1, in units of 2^(vE-127-8)
+    float m_run[HG][2], l_run[HG][2];
+    float qscale[HG];        // scale * log2(e) * 2^qshift * 2^8 (the 2^-8 of the K conversion)
+    int vE[HG];              // biased exponent of the V-factor unit (0 = none yet)
     int warp, lane, g, t, key0;
-    int f0, f1;          // byte offsets of the factors of keys g and g + 8 inside a factor block
+    int line0, line1;        // 128-byte line of keys g, g+8 of head 0 inside a code tile
+    int f0, f1;              // byte offsets of the factors of keys g, g+8 of head 0 in a factor block
+    int hline, hfac;         // per-head strides of the two (R lines, 2R bytes)
 
     // R: rows per TMA box (a power of two, 8..64)
     __device__ __forceinline__ void init(int w, int l, int R) {
@@ -105,25 +111,32 @@ struct Consumer {
         key0 = w * C::KPW;
         const int rb = __ffs(R) - 1;
         const int r0 = key0 + g, r1 = r0 + 8;
+        line0 = (r0 >> rb) * (HG * R) + (r0 & (R - 1));
+        line1 = (r1 >> rb) * (HG * R) + (r1 & (R - 1));
         f0 = (r0 >> rb) * C::FSLOT + (r0 & (R - 1)) * 2;
         f1 = (r1 >> rb) * C::FSLOT + (r1 & (R - 1)) * 2;
+        hline = R;
+        hfac = 2 * R;
     }
 
     __device__ __forceinline__ void reset() {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            m_run[j] = -INFINITY;
-            l_run[j] = 0.f;
+        for (int h = 0; h < HG; ++h) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                m_run[h][j] = -INFINITY;
+                l_run[h][j] = 0.f;
+            }
+#pragma unroll
+            for (int m = 0; m < KS; ++m)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[h][m][j] = 0.f;
+            vE[h] = 0;
         }
-#pragma unroll
-        for (int m = 0; m < KS; ++m)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[m][j] = 0.f;
-        vE = 0;
     }
 
-    // q of the G heads (head g at base + g * hstride); qs = scale * log2(e).
-    __device__ __forceinline__ void load_q(const __nv_bfloat16 *base, long long hstride, float qs) {
+    // q of the G query heads of kv head h (head g at base + g * hstride); qs = scale * log2(e).
+    __device__ __forceinline__ void load_q(int h, const __nv_bfloat16 *base, long long hstride, float qs) {
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -149,16 +162,16 @@ struct Consumer {
 #pragma unroll
         for (int m = 0; m < KS; ++m) {
             const float2 lo = bf16x2_to_float2(w[2 * m]), hi = bf16x2_to_float2(w[2 * m + 1]);
-            qb[m][0] = pack_f16x2(lo.x * sh, hi.x * sh);  // dims 4m+0, 4m+2 (of 32t..)
-            qb[m][1] = pack_f16x2(lo.y * sh, hi.y * sh);  // dims 4m+1, 4m+3
+            qb[h][m][0] = pack_f16x2(lo.x * sh, hi.x * sh);  // dims 4m+0, 4m+2 (of 32t..)
+            qb[h][m][1] = pack_f16x2(lo.y * sh, hi.y * sh);  // dims 4m+1, 4m+3
         }
-        qscale = qs * pow2_biased(127 + e + 8);
+        qscale[h] = qs * pow2_biased(127 + e + 8);
     }
 
-    // 32 code bytes of `row` for this lane (dims 32t .. 32t+31) from a 128-byte-swizzled tile
-    __device__ __forceinline__ void row_words(const uint8_t *tile, int row, uint32_t (&w)[8]) const {
-        const uint4 a = lds128(tile + row * 128 + (((2 * t) ^ (row & 7)) << 4));
-        const uint4 b = lds128(tile + row * 128 + (((2 * t + 1) ^ (row & 7)) << 4));
+    // 32 code bytes of a 128-byte line for this lane (dims 32t .. 32t+31), 128-byte swizzled
+    __device__ __forceinline__ void line_words(const uint8_t *tile, int line, uint32_t (&w)[8]) const {
+        const uint4 a = lds128(tile + line * 128 + (((2 * t) ^ (line & 7)) << 4));
+        const uint4 b = lds128(tile + line * 128 + (((2 * t + 1) ^ (line & 7)) << 4));
         w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
         w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
     }
@@ -166,88 +179,83 @@ struct Consumer {
     __device__ __forceinline__ void tile(const uint8_t *stage, int nvalid) {
         const int nv = nvalid - key0;
         if (nv <= 0) return;
-        const int r0 = key0 + g, r1 = key0 + g + 8;
         const bool v0 = g < nv, v1 = g + 8 < nv;
-        const float kfac0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::KS_OFF + f0));
-        const float kfac1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::KS_OFF + f1));
-        const float vfac0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::VS_OFF + f0));
-        const float vfac1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::VS_OFF + f1));
-        // the V rows are read up front so their latency hides under QK and the softmax
-        uint32_t w0[8], w1[8];
-        row_words(stage + C::CODE_BYTES, r0, w0);
-        row_words(stage + C::CODE_BYTES, r1, w1);
-        // S^T = K . Q^T (keys g, g+8 x heads 2t, 2t+1), K in units of 2^-8; two independent
-        // accumulation chains (even / odd k-steps) halve the dependent MMA latency
-        float c[4];
-        {
-            uint32_t k0[8], k1[8];
-            row_words(stage, r0, k0);
-            row_words(stage, r1, k1);
-            float ce[4] = {0.f, 0.f, 0.f, 0.f}, co[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int m = 0; m < KS; m += 2) {
-                const uint32_t a[4] = {e4m3_pair02(k0[m]), e4m3_pair02(k1[m]), e4m3_pair13(k0[m]),
-                                       e4m3_pair13(k1[m])};
-                mma_f16_16816(ce, a, qb[m][0], qb[m][1]);
-                const uint32_t b[4] = {e4m3_pair02(k0[m + 1]), e4m3_pair02(k1[m + 1]), e4m3_pair13(k0[m + 1]),
-                                       e4m3_pair13(k1[m + 1])};
-                mma_f16_16816(co, b, qb[m + 1][0], qb[m + 1][1]);
+        for (int h = 0; h < HG; ++h) {
+            const uint8_t *sK = stage, *sV = stage + C::CODE_BYTES;
+            const int l0 = line0 + h * hline, l1 = line1 + h * hline;
+            const int o0 = f0 + h * hfac, o1 = f1 + h * hfac;
+            const float kfac0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::KS_OFF + o0));
+            const float kfac1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::KS_OFF + o1));
+            const float vfac0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::VS_OFF + o0));
+            const float vfac1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::VS_OFF + o1));
+            uint32_t w0[8], w1[8];
+            line_words(sV, l0, w0);
+            line_words(sV, l1, w1);
+            // S^T = K . Q^T (keys g, g+8 x heads 2t, 2t+1), K in units of 2^-8
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                uint32_t k0[8], k1[8];
+                line_words(sK, l0, k0);
+                line_words(sK, l1, k1);
+#pragma unroll
+                for (int m = 0; m < KS; ++m) {
+                    const uint32_t a[4] = {e4m3_pair02(k0[m]), e4m3_pair02(k1[m]), e4m3_pair13(k0[m]),
+                                           e4m3_pair13(k1[m])};
+                    mma_f16_16816(c, a, qb[h][m][0], qb[h][m][1]);
+                }
             }
+            const float ks0 = kfac0 * qscale[h], ks1 = kfac1 * qscale[h];
+            float s[4];
+            s[0] = v0 ? c[0] * ks0 : -INFINITY;
+            s[1] = v0 ? c[1] * ks0 : -INFINITY;
+            s[2] = v1 ? c[2] * ks1 : -INFINITY;
+            s[3] = v1 ? c[3] * ks1 : -INFINITY;
+            float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
+            float vm = fmaxf(v0 ? vfac0 : 0.f, v1 ? vfac1 : 0.f);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) c[j] = ce[j] + co[j];
-        }
-        const float ks0 = kfac0 * qscale, ks1 = kfac1 * qscale;
-        float s[4];
-        s[0] = v0 ? c[0] * ks0 : -INFINITY;
-        s[1] = v0 ? c[1] * ks0 : -INFINITY;
-        s[2] = v1 ? c[2] * ks1 : -INFINITY;
-        s[3] = v1 ? c[3] * ks1 : -INFINITY;
-        float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
-        float vm = fmaxf(v0 ? vfac0 : 0.f, v1 ? vfac1 : 0.f);
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xFFFFFFFFu, mx[0], o));
-            mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xFFFFFFFFu, mx[1], o));
-            vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o));
-        }
-        // V-factor unit: a power of two above every factor seen (vm < 2^(E - 127))
-        float rescale = 1.f;
-        {
-            const int E = min(254, ((__float_as_int(vm) >> 23) & 0xFF) + 1);
-            if (vm > 0.f && E > vE) {
-                rescale = vE - E + 127 >= 1 ? pow2_biased(vE - E + 127) : 0.f;
-                vE = E;
+            for (int o = 4; o < 32; o <<= 1) {
+                mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xFFFFFFFFu, mx[0], o));
+                mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xFFFFFFFFu, mx[1], o));
+                vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o));
             }
-        }
-        const float vu = vE > 0 ? pow2_biased(254 - vE) : 0.f;  // 2^(127 - vE): factor -> [0, 1)
-        float alpha[2], mu[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float m_new = fmaxf(m_run[j], mx[j]);
-            mu[j] = (m_new == -INFINITY) ? 0.f : m_new;
-            alpha[j] = ex2(m_run[j] - mu[j]);
-            m_run[j] = m_new;
-        }
-        const float p0 = ex2(s[0] - mu[0]), p1 = ex2(s[1] - mu[1]);
-        const float p2 = ex2(s[2] - mu[0]), p3 = ex2(s[3] - mu[1]);
-        l_run[0] = l_run[0] * alpha[0] + (p0 + p2);
-        l_run[1] = l_run[1] * alpha[1] + (p1 + p3);
-        const float vs0 = v0 ? vfac0 * vu : 0.f;
-        const float vs1 = v1 ? vfac1 * vu : 0.f;
-        const uint32_t b0 = movmatrix_trans(pack_f16x2(p0 * vs0, p1 * vs0));
-        const uint32_t b1 = movmatrix_trans(pack_f16x2(p2 * vs1, p3 * vs1));
-        const float fa = alpha[0] * rescale, fb = alpha[1] * rescale;
-        if (__any_sync(0xFFFFFFFFu, fa != 1.f || fb != 1.f)) {
-#pragma unroll
-            for (int m = 0; m < KS; ++m) {
-                acc[m][0] *= fa;
-                acc[m][1] *= fb;
-                acc[m][2] *= fa;
-                acc[m][3] *= fb;
+            // V-factor unit: a power of two above every factor seen (vm < 2^(E - 127))
+            float rescale = 1.f;
+            {
+                const int E = min(254, ((__float_as_int(vm) >> 23) & 0xFF) + 1);
+                if (vm > 0.f && E > vE[h]) {
+                    rescale = vE[h] - E + 127 >= 1 ? pow2_biased(vE[h] - E + 127) : 0.f;
+                    vE[h] = E;
+                }
             }
-        }
-        // O^T += V^T . P'^T; rows past the end read as code 0 so 0 * V stays 0
-        {
+            const float vu = vE[h] > 0 ? pow2_biased(254 - vE[h]) : 0.f;  // 2^(127 - vE): factor -> [0, 1)
+            float alpha[2], mu[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float m_new = fmaxf(m_run[h][j], mx[j]);
+                mu[j] = (m_new == -INFINITY) ? 0.f : m_new;
+                alpha[j] = ex2(m_run[h][j] - mu[j]);
+                m_run[h][j] = m_new;
+            }
+            const float p0 = ex2(s[0] - mu[0]), p1 = ex2(s[1] - mu[1]);
+            const float p2 = ex2(s[2] - mu[0]), p3 = ex2(s[3] - mu[1]);
+            l_run[h][0] = l_run[h][0] * alpha[0] + (p0 + p2);
+            l_run[h][1] = l_run[h][1] * alpha[1] + (p1 + p3);
+            const float vs0 = v0 ? vfac0 * vu : 0.f;
+            const float vs1 = v1 ? vfac1 * vu : 0.f;
+            const uint32_t b0 = movmatrix_trans(pack_f16x2(p0 * vs0, p1 * vs0));
+            const uint32_t b1 = movmatrix_trans(pack_f16x2(p2 * vs1, p3 * vs1));
+            const float fa = alpha[0] * rescale, fb = alpha[1] * rescale;
+            if (__any_sync(0xFFFFFFFFu, fa != 1.f || fb != 1.f)) {
+#pragma unroll
+                for (int m = 0; m < KS; ++m) {
+                    acc[h][m][0] *= fa;
+                    acc[h][m][1] *= fb;
+                    acc[h][m][2] *= fa;
+                    acc[h][m][3] *= fb;
+                }
+            }
+            // O^T += V^T . P'^T; rows past the end read as code 0 so 0 * V stays 0
             if (nv < 16) {
 #pragma unroll
                 for (int m = 0; m < KS; ++m) {
@@ -259,67 +267,74 @@ struct Consumer {
             for (int m = 0; m < KS; ++m) {
                 const uint32_t a[4] = {movmatrix_trans(e4m3_pair02(w0[m])), movmatrix_trans(e4m3_pair13(w0[m])),
                                        movmatrix_trans(e4m3_pair02(w1[m])), movmatrix_trans(e4m3_pair13(w1[m]))};
-                mma_f16_16816(acc[m], a, b0, b1);
+                mma_f16_16816(acc[h][m], a, b0, b1);
             }
         }
     }
 
-    // Merge the four warps per head in two halves of D (the row merge of the bf16 path);
-    // emit(head, d, a0, a1, M, l) gets dims d, d+1 in natural order.
+    // Merge the four warps per (kv head, query head) in two halves of D (the row merge of
+    // the bf16 path); emit(kv head in unit, query head, d, a0, a1, M, l) gets dims d, d+1 in
+    // natural order.
     template <class Sync, class Emit>
     __device__ __forceinline__ bool finish(float *mrg, Sync sync, Emit emit) {
-        constexpr int NWC = C::NWC, DH = D / 2;
+        constexpr int NWC = C::NWC, DH = D / 2, NR = HG * G;  // rows per warp
+        float *macc = mrg;                 // [NWC][HG * G][D/2]
+        float *mml = mrg + NWC * NR * DH;  // [NWC][HG * G][2]
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            l_run[0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[0], o);
-            l_run[1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[1], o);
-        }
-        // back from units of 2^(vE - 127) (V factors) and 2^-8 (V codes)
-        const float unit = vE > 0 ? pow2_biased(min(vE + 8, 254)) : 0.f;
-        float *macc = mrg;                // [NWC][G][D/2]
-        float *mml = mrg + NWC * G * DH;  // [NWC][G][2]
-        if (g == 0) {
+        for (int h = 0; h < HG; ++h) {
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-                if (2 * t + j < G) {
-                    mml[(warp * G + 2 * t + j) * 2 + 0] = m_run[j];
-                    mml[(warp * G + 2 * t + j) * 2 + 1] = l_run[j];
-                }
+            for (int o = 4; o < 32; o <<= 1) {
+                l_run[h][0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[h][0], o);
+                l_run[h][1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[h][1], o);
+            }
+            if (g == 0) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    if (2 * t + j < G) {
+                        mml[(warp * NR + h * G + 2 * t + j) * 2 + 0] = m_run[h][j];
+                        mml[(warp * NR + h * G + 2 * t + j) * 2 + 1] = l_run[h][j];
+                    }
+            }
         }
         const int tid = warp * 32 + lane;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             if ((g >> 2) == half) {  // this lane's dims 32(g/2) + 4m + 2(g&1) (+1) lie in this half
 #pragma unroll
-                for (int m = 0; m < KS; ++m) {
-                    const int dlo = 32 * (g >> 1) + 4 * m + 2 * (g & 1) - half * DH;
+                for (int h = 0; h < HG; ++h) {
+                    // back from units of 2^(vE - 127) (V factors) and 2^-8 (V codes)
+                    const float unit = vE[h] > 0 ? pow2_biased(min(vE[h] + 8, 254)) : 0.f;
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        if (2 * t + j < G) {
-                            float *row = macc + (warp * G + 2 * t + j) * DH;
-                            row[dlo] = acc[m][j] * unit;
-                            row[dlo + 1] = acc[m][j + 2] * unit;
+                    for (int m = 0; m < KS; ++m) {
+                        const int dlo = 32 * (g >> 1) + 4 * m + 2 * (g & 1) - half * DH;
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            if (2 * t + j < G) {
+                                float *row = macc + (warp * NR + h * G + 2 * t + j) * DH;
+                                row[dlo] = acc[h][m][j] * unit;
+                                row[dlo + 1] = acc[h][m][j + 2] * unit;
+                            }
                         }
                     }
                 }
             }
             if (!sync()) return false;
-            for (int e = tid * 2; e < G * DH; e += NWC * 32 * 2) {
-                const int hh = e / DH, dd = e % DH;
+            for (int e = tid * 2; e < NR * DH; e += NWC * 32 * 2) {
+                const int rr = e / DH, dd = e % DH;
                 float M = -INFINITY;
 #pragma unroll
-                for (int w = 0; w < NWC; ++w) M = fmaxf(M, mml[(w * G + hh) * 2]);
+                for (int w = 0; w < NWC; ++w) M = fmaxf(M, mml[(w * NR + rr) * 2]);
                 const float Mu = (M == -INFINITY) ? 0.f : M;
                 float a0 = 0.f, a1 = 0.f, lv = 0.f;
 #pragma unroll
                 for (int w = 0; w < NWC; ++w) {
-                    const float f = ex2(mml[(w * G + hh) * 2] - Mu);
-                    lv = fmaf(f, mml[(w * G + hh) * 2 + 1], lv);
-                    const float2 x = *reinterpret_cast<const float2 *>(macc + (w * G + hh) * DH + dd);
+                    const float f = ex2(mml[(w * NR + rr) * 2] - Mu);
+                    lv = fmaf(f, mml[(w * NR + rr) * 2 + 1], lv);
+                    const float2 x = *reinterpret_cast<const float2 *>(macc + (w * NR + rr) * DH + dd);
                     a0 = fmaf(f, x.x, a0);
                     a1 = fmaf(f, x.y, a1);
                 }
-                emit(hh, half * DH + dd, a0, a1, M, lv);
+                emit(rr / G, rr % G, half * DH + dd, a0, a1, M, lv);
             }
             if (!sync()) return false;
         }
@@ -334,14 +349,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
                  const SplitParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = aligned_smem<C>(smem_raw);
-    constexpr int G = C::G, NWC = C::NWC, BT = C::BT, NS = C::NS, D = C::D;
+    constexpr int G = C::G, HG = C::HG, NWC = C::NWC, BT = C::BT, NS = C::NS, D = C::D;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int units = p.B * p.Hkv;
+    const int nkvg = p.Hkv / HG;
+    const int units = p.B * nkvg;
     const int s = blockIdx.x / units;
     const int rem = blockIdx.x - s * units;
-    const int b = rem / p.Hkv;
-    const int kvh = rem - b * p.Hkv;
+    const int b = rem / nkvg;
+    const int kvg = rem - b * nkvg;
     int L = p.seq_lens[b];
     const int R = p.box_rows;
     int pg_first = 0;  // loaded with the length (entries past the end are read, not used)
@@ -351,7 +367,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
             pg_first = __ldg(p.block_table + (long long)b * p.max_pages + t / p.page_size);
     }
     if (L < 0 || L > p.max_kv_len) {
-        if (threadIdx.x == 0 && s == 0 && kvh == 0) flag_error(DAP_DEVERR_SEQLEN);
+        if (threadIdx.x == 0 && s == 0 && kvg == 0) flag_error(DAP_DEVERR_SEQLEN);
         L = min(max(L, 0), p.max_kv_len);
     }
     const int nsplit = max(1, (L + p.chunk - 1) / p.chunk);
@@ -404,15 +420,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
             }
             const int t = tok0 + i * BT;
             const int nbox = (min(BT, tok1 - t) + R - 1) / R;
-            if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)(nbox * R * (2 * D + 4)));
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)(nbox * R * HG * (2 * D + 4)));
             __syncwarp();
             if (lane < nbox) {
                 uint8_t *stage = smem + st * C::STAGE_BYTES;
                 const int row = (t + lane * R) % p.page_size;
-                tma_load_4d(stage + lane * R * D, &mapK, 0, kvh, row, pg, &full[st]);
-                tma_load_4d(stage + C::CODE_BYTES + lane * R * D, &mapV, 0, kvh, row, pg, &full[st]);
-                tma_load_3d(stage + C::KS_OFF + lane * C::FSLOT, &mapKS, row, kvh, pg, &full[st]);
-                tma_load_3d(stage + C::VS_OFF + lane * C::FSLOT, &mapVS, row, kvh, pg, &full[st]);
+                tma_load_4d(stage + lane * R * HG * D, &mapK, 0, row, kvg * HG, pg, &full[st]);
+                tma_load_4d(stage + C::CODE_BYTES + lane * R * HG * D, &mapV, 0, row, kvg * HG, pg, &full[st]);
+                tma_load_3d(stage + C::KS_OFF + lane * C::FSLOT, &mapKS, row, kvg * HG, pg, &full[st]);
+                tma_load_3d(stage + C::VS_OFF + lane * C::FSLOT, &mapVS, row, kvg * HG, pg, &full[st]);
             }
             issued = i + 1;
         }
@@ -425,7 +441,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     Consumer<C> cs;
     cs.init(warp, lane, R);
     cs.reset();
-    cs.load_q(p.q + (long long)b * p.q_sb + (long long)kvh * G * p.q_sh, p.q_sh, p.qscale);
+#pragma unroll
+    for (int h = 0; h < HG; ++h)
+        cs.load_q(h, p.q + (long long)b * p.q_sb + (long long)(kvg * HG + h) * G * p.q_sh, p.q_sh, p.qscale);
     int consumed = 0;
     for (int i = 0; i < ntiles; ++i) {
         const int st = i % NS;
@@ -446,8 +464,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     }
     const bool direct = (nsplit == 1);
     cs.finish(reinterpret_cast<float *>(smem), [] { named_sync(1, NWC * 32); return true; },
-              [&](int hh, int d, float a0, float a1, float M, float lv) {
-                  const int hq = kvh * G + hh;
+              [&](int hl, int hh, int d, float a0, float a1, float M, float lv) {
+                  const int hq = (kvg * HG + hl) * G + hh;
                   if (direct) {
                       store_out_pair(p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh + d, a0, a1, lv);
                   } else {
@@ -472,38 +490,39 @@ bool encode_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, i
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// codes [P, ps, Hkv, 128] bytes viewed as [128, Hkv, ps, P]; box [128, 1, R, 1], 128-byte swizzle
-bool encode_codes(CUtensorMap *map, const void *base, int Hkv, int ps, int P, int R) {
-    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)Hkv, (cuuint64_t)ps, (cuuint64_t)P};
-    const cuuint64_t strides[3] = {(cuuint64_t)kD, (cuuint64_t)Hkv * kD, (cuuint64_t)ps * Hkv * kD};
-    const cuuint32_t box[4] = {(cuuint32_t)kD, 1u, (cuuint32_t)R, 1u};
+// codes [P, ps, Hkv, 128] bytes viewed as [128, ps, Hkv, P] (the head dim outside the slot
+// dim); box [128, R, HG, 1] lands head-major, 128-byte swizzled
+bool encode_codes(CUtensorMap *map, const void *base, int Hkv, int ps, int P, int R, int HG) {
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)ps, (cuuint64_t)Hkv, (cuuint64_t)P};
+    const cuuint64_t strides[3] = {(cuuint64_t)Hkv * kD, (cuuint64_t)kD, (cuuint64_t)ps * Hkv * kD};
+    const cuuint32_t box[4] = {(cuuint32_t)kD, (cuuint32_t)R, (cuuint32_t)HG, 1u};
     return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// factors [P, Hkv, ps] bf16 viewed as [ps, Hkv, P]; box [R, 1, 1]
-bool encode_factors(CUtensorMap *map, const void *base, int Hkv, int ps, int P, int R) {
+// factors [P, Hkv, ps] bf16 viewed as [ps, Hkv, P]; box [R, HG, 1]
+bool encode_factors(CUtensorMap *map, const void *base, int Hkv, int ps, int P, int R, int HG) {
     const cuuint64_t dims[3] = {(cuuint64_t)ps, (cuuint64_t)Hkv, (cuuint64_t)P};
     const cuuint64_t strides[2] = {(cuuint64_t)ps * 2, (cuuint64_t)Hkv * ps * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)R, 1u, 1u};
+    const cuuint32_t box[3] = {(cuuint32_t)R, (cuuint32_t)HG, 1u};
     return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, 3, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <int G>
+template <int G, int HG>
 dap_status launch_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
-    using C = Cfg<G>;
+    using C = Cfg<G, HG>;
     const int R = gcd_int(a.page_size, C::BT);
     p.box_rows = R;
     CUtensorMap mk, mv, mks, mvs;
-    if (!encode_codes(&mk, a.k, a.Hkv, a.page_size, a.num_pages, R) ||
-        !encode_codes(&mv, a.v, a.Hkv, a.page_size, a.num_pages, R) ||
-        !encode_factors(&mks, a.k_scale, a.Hkv, a.page_size, a.num_pages, R) ||
-        !encode_factors(&mvs, a.v_scale, a.Hkv, a.page_size, a.num_pages, R))
+    if (!encode_codes(&mk, a.k, a.Hkv, a.page_size, a.num_pages, R, HG) ||
+        !encode_codes(&mv, a.v, a.Hkv, a.page_size, a.num_pages, R, HG) ||
+        !encode_factors(&mks, a.k_scale, a.Hkv, a.page_size, a.num_pages, R, HG) ||
+        !encode_factors(&mvs, a.v_scale, a.Hkv, a.page_size, a.num_pages, R, HG))
         return DAP_ERR_CUDA;
     auto kern = fp8kv_kernel<C>;
     static int occ = 0;
     if (prepare_kernel(kern, C::THREADS, C::SMEM, &occ) <= 0) return DAP_ERR_CUDA;
-    const long long grid = (long long)a.B * a.Hkv * a.num_splits;
+    const long long grid = (long long)a.B * (a.Hkv / HG) * a.num_splits;
     if (grid > 0x7FFFFFFFLL) return DAP_ERR_SHAPE;
     p.o_part = static_cast<float *>(a.workspace);
     p.ml_part = a.num_splits > 1 ? reinterpret_cast<float *>(static_cast<char *>(a.workspace) +
@@ -527,11 +546,12 @@ dap_status launch_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
 dap_status launch_decode_fp8kv(const DecodeArgs &a, cudaStream_t stream) {
     if (a.D != f8kv::kD) return DAP_ERR_UNSUPPORTED;
     SplitParams p = make_params(a);
+    const bool pair = a.Hkv % 2 == 0;  // two kv heads per CTA when they pair up
     switch (a.Hq / a.Hkv) {
-        case 1: return f8kv::launch_g<1>(a, p, stream);
-        case 2: return f8kv::launch_g<2>(a, p, stream);
-        case 4: return f8kv::launch_g<4>(a, p, stream);
-        case 8: return f8kv::launch_g<8>(a, p, stream);
+        case 1: return pair ? f8kv::launch_g<1, 2>(a, p, stream) : f8kv::launch_g<1, 1>(a, p, stream);
+        case 2: return pair ? f8kv::launch_g<2, 2>(a, p, stream) : f8kv::launch_g<2, 1>(a, p, stream);
+        case 4: return pair ? f8kv::launch_g<4, 2>(a, p, stream) : f8kv::launch_g<4, 1>(a, p, stream);
+        case 8: return pair ? f8kv::launch_g<8, 2>(a, p, stream) : f8kv::launch_g<8, 1>(a, p, stream);
     }
     return DAP_ERR_UNSUPPORTED;
 }
