@@ -79,10 +79,12 @@ def _load():
         lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
         lib.oracle_kv_append_fp8.argtypes = [P, P, P, P, I, I, I, I]
         lib.oracle_kv_append_fp8.restype = I
-        lib.oracle_decode_paged_multi.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, D, P]
+        lib.oracle_decode_paged_multi.argtypes = [P, P, P, I, P, I, P, P, P, LL, I, I, I, I, I, D, P]
         lib.oracle_decode_paged_multi.restype = I
         lib.oracle_q_tile_map.argtypes = [P, I, I, P, P, P, I]
         lib.oracle_q_tile_map.restype = I
+        lib.oracle_decode_paged_masked.argtypes = [P, LL, LL, P, P, I, P, I, P, P, LL, I, I, I, I, I, D, P]
+        lib.oracle_decode_paged_masked.restype = I
         lib.oracle_decode_paged_fp8kv.argtypes = [P, LL, LL, P, P, P, P, I, P, I, P, I, I, I, I, I, D, P]
         lib.oracle_decode_paged_fp8kv.restype = I
         lib.oracle_kv_append_paged_fp8.argtypes = [P, P, P, P, P, P, I, I, P, I, P, I, I, I]
@@ -234,10 +236,12 @@ def kv_append_fp8(rows, kv_cache, inv_scale, slots):
     return cache, inv, bad
 
 
-def decode_paged_multi(q, k_cache, v_cache, block_table, seq_lens, qo_indptr, scale: float) -> np.ndarray:
+def decode_paged_multi(q, k_cache, v_cache, block_table, seq_lens, qo_indptr, scale: float,
+                       mask=None) -> np.ndarray:
     """Multi-token decode: q packed [total_q, Hq, D] u16, qo_indptr [B+1]; token i of
-    sequence b attends keys up to position seq_lens[b] - q_len_b + i.  Returns float64
-    [total_q, Hq, D]."""
+    sequence b attends keys up to position seq_lens[b] - q_len_b + i, and, with a mask
+    [total_q, >= max kv_len] (bool / uint8, nonzero = keep), only the kept ones.  Returns
+    float64 [total_q, Hq, D]."""
     q = _u16(q); k_cache = _u16(k_cache); v_cache = _u16(v_cache)
     bt = np.ascontiguousarray(block_table, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
@@ -246,8 +250,13 @@ def decode_paged_multi(q, k_cache, v_cache, block_table, seq_lens, qo_indptr, sc
     P, ps, Hkv, _ = k_cache.shape
     B = sl.shape[0]
     out = np.empty((total, Hq, D), dtype=np.float64)
+    m = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint8)
+    if m is not None:
+        assert m.ndim == 2 and m.shape[0] == total
     bad = _load().oracle_decode_paged_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), P, _ptr(bt), bt.shape[1],
-                                            _ptr(sl), _ptr(qi), B, Hq, Hkv, D, ps, float(scale), _ptr(out))
+                                            _ptr(sl), _ptr(qi), None if m is None else _ptr(m),
+                                            0 if m is None else m.shape[1], B, Hq, Hkv, D, ps, float(scale),
+                                            _ptr(out))
     if bad:
         raise ValueError(f"{bad} output rows would read outside the given cache/table")
     return out
@@ -303,3 +312,22 @@ def kv_append_paged_fp8(k_new, v_new, k_codes, v_codes, k_scale, v_scale, block_
     return _load().oracle_kv_append_paged_fp8(_ptr(kn), _ptr(vn), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
                                               _ptr(v_scale), P, page_size, _ptr(bt), bt.shape[1], _ptr(ps_), B,
                                               Hkv, D)
+
+
+def decode_paged_masked(q, k_cache, v_cache, block_table, seq_lens, mask, scale: float) -> np.ndarray:
+    """Masked paged decode: mask [B, >= max kv_len] (bool / uint8, nonzero = keep); key t of
+    sequence b takes part iff t < seq_lens[b] and mask[b, t].  Returns float64 [B, Hq, D]."""
+    q = _u16(q); k_cache = _u16(k_cache); v_cache = _u16(v_cache)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    m = np.ascontiguousarray(mask, dtype=np.uint8)
+    B, Hq, D = q.shape
+    P, ps, Hkv, _ = k_cache.shape
+    assert m.ndim == 2 and m.shape[0] == B
+    out = np.empty((B, Hq, D), dtype=np.float64)
+    bad = _load().oracle_decode_paged_masked(_ptr(q), Hq * D, D, _ptr(k_cache), _ptr(v_cache), P, _ptr(bt),
+                                             bt.shape[1], _ptr(sl), _ptr(m), m.shape[1], B, Hq, Hkv, D, ps,
+                                             float(scale), _ptr(out))
+    if bad:
+        raise ValueError(f"{bad} output rows would read outside the given cache/table")
+    return out

@@ -149,12 +149,30 @@ static void attend_one(const double *q, const uint16_t *const *krows,
  * (q_stride_b, q_stride_h, 1); caches are [num_pages, ps, Hkv, D]; block_table is
  * [B, max_pages].  Returns 0, or -1 when the row would read outside the given buffers
  * (a page index outside [0, num_pages) or seq_len beyond max_pages * ps). */
+static int paged_row_keep(const uint16_t *q, long long q_stride_b, long long q_stride_h,
+                          const uint16_t *k_cache, const uint16_t *v_cache, int num_pages,
+                          const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                          int Hq, int Hkv, int D, int page_size, double scale, int b, int h,
+                          const uint8_t *keep, double *out);
+
 static int paged_row(const uint16_t *q, long long q_stride_b, long long q_stride_h,
                      const uint16_t *k_cache, const uint16_t *v_cache, int num_pages,
                      const int32_t *block_table, int max_pages, const int32_t *seq_lens,
                      int Hq, int Hkv, int D, int page_size, double scale, int b, int h,
                      double *out) {
-    int G = Hq / Hkv, kh = h / G, L = seq_lens[b], t, d, rc = 0;
+    return paged_row_keep(q, q_stride_b, q_stride_h, k_cache, v_cache, num_pages, block_table, max_pages,
+                          seq_lens, Hq, Hkv, D, page_size, scale, b, h, NULL, out);
+}
+
+/* The same row over the kept keys only: key t takes part iff keep == NULL or keep[t] != 0
+ * (a bool mask with True = keep, [CK] "Python Wrappers" interface); no kept key gives a
+ * zero row. */
+static int paged_row_keep(const uint16_t *q, long long q_stride_b, long long q_stride_h,
+                          const uint16_t *k_cache, const uint16_t *v_cache, int num_pages,
+                          const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                          int Hq, int Hkv, int D, int page_size, double scale, int b, int h,
+                          const uint8_t *keep, double *out) {
+    int G = Hq / Hkv, kh = h / G, L = seq_lens[b], t, d, rc = 0, n = 0;
     double *qd, *s;
     const uint16_t **kr, **vr;
     if (L < 0 || (long long)L > (long long)max_pages * page_size) return -1;
@@ -168,11 +186,13 @@ static int paged_row(const uint16_t *q, long long q_stride_b, long long q_stride
         int slot = t % page_size;
         long long row;
         if (page < 0 || page >= num_pages) { rc = -1; break; }
+        if (keep && !keep[t]) continue;
         row = (((long long)page * page_size + slot) * Hkv + kh) * D;
-        kr[t] = k_cache + row;
-        vr[t] = v_cache + row;
+        kr[n] = k_cache + row;
+        vr[n] = v_cache + row;
+        ++n;
     }
-    if (rc == 0) attend_one(qd, kr, vr, L, D, scale, s, out);
+    if (rc == 0) attend_one(qd, kr, vr, n, D, scale, s, out);
     free(qd); free(s); free(kr); free(vr);
     return rc;
 }
@@ -192,6 +212,31 @@ int oracle_decode_paged(const uint16_t *q, long long q_stride_b, long long q_str
         double *o = out + i * D;
         if (paged_row(q, q_stride_b, q_stride_h, k_cache, v_cache, num_pages, block_table,
                       max_pages, seq_lens, Hq, Hkv, D, page_size, scale, b, h, o) != 0) {
+            for (d = 0; d < D; ++d) o[d] = NAN;
+            ++bad;
+        }
+    }
+    return bad;
+}
+
+/* Masked paged decode ([CK] "Python Wrappers": mask 2-D [batch, kv_len], bool, True =
+ * keep): key t of sequence b takes part iff t < seq_lens[b] and mask[b * mask_stride + t]
+ * != 0.  A sequence with no kept key gives a zero row.  Everything else as
+ * oracle_decode_paged. */
+int oracle_decode_paged_masked(const uint16_t *q, long long q_stride_b, long long q_stride_h,
+                               const uint16_t *k_cache, const uint16_t *v_cache, int num_pages,
+                               const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                               const uint8_t *mask, long long mask_stride, int B, int Hq, int Hkv, int D,
+                               int page_size, double scale, double *out) {
+    int bad = 0;
+    long long i, n = (long long)B * Hq;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (i = 0; i < n; ++i) {
+        int b = (int)(i / Hq), h = (int)(i % Hq), d;
+        double *o = out + i * D;
+        if (paged_row_keep(q, q_stride_b, q_stride_h, k_cache, v_cache, num_pages, block_table, max_pages,
+                           seq_lens, Hq, Hkv, D, page_size, scale, b, h, mask + (long long)b * mask_stride,
+                           o) != 0) {
             for (d = 0; d < D; ++d) o[d] = NAN;
             ++bad;
         }
@@ -419,20 +464,24 @@ int oracle_kv_append_fp8(const uint16_t *rows, uint8_t *kv_cache, uint16_t *inv_
  * oracle_decode_paged.  Returns the number of rows that failed the bounds checks. */
 int oracle_decode_paged_multi(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                               int num_pages, const int32_t *block_table, int max_pages,
-                              const int32_t *seq_lens, const int32_t *qo_indptr, int B, int Hq,
-                              int Hkv, int D, int page_size, double scale, double *out) {
+                              const int32_t *seq_lens, const int32_t *qo_indptr, const uint8_t *mask,
+                              long long mask_stride, int B, int Hq, int Hkv, int D, int page_size,
+                              double scale, double *out) {
     int bad = 0, b;
     for (b = 0; b < B; ++b) {
         int q0 = qo_indptr[b], qlen = qo_indptr[b + 1] - qo_indptr[b], L = seq_lens[b], i;
         for (i = 0; i < qlen; ++i) {
             int upto = L - qlen + i + 1; /* keys 0 .. position of token i */
             int32_t one = upto < 0 ? 0 : upto, h, d;
+            /* an optional mask row of the packed token (3-D mask [batch, q_len, kv_len] with the
+             * q rows packed; True = keep) applies together with the causal rule */
+            const uint8_t *keep = mask ? mask + (long long)(q0 + i) * mask_stride : NULL;
             for (h = 0; h < Hq; ++h) {
                 double *o = out + ((long long)(q0 + i) * Hq + h) * D;
                 /* reuse the single-token row with the sequence cut at this token */
-                if (paged_row(q + (long long)(q0 + i) * Hq * D, 0, D, k_cache,
-                              v_cache, num_pages, block_table + (long long)b * max_pages, max_pages,
-                              &one, Hq, Hkv, D, page_size, scale, 0, h, o) != 0) {
+                if (paged_row_keep(q + (long long)(q0 + i) * Hq * D, 0, D, k_cache,
+                                   v_cache, num_pages, block_table + (long long)b * max_pages, max_pages,
+                                   &one, Hq, Hkv, D, page_size, scale, 0, h, keep, o) != 0) {
                     for (d = 0; d < D; ++d) o[d] = NAN;
                     ++bad;
                 }

@@ -580,3 +580,85 @@ def test_kv_append_paged_fp8_places_and_quantises_rows():
     # a position beyond the table is refused
     assert oracle.kv_append_paged_fp8(bits(k_new), bits(v_new), kc, vc, ks, vs, table,
                                       np.array([0, 10 ** 6, 1], np.int32)) == 2
+
+
+# ---- masked decode ----------------------------------------------------------------------
+
+def random_mask(B, width, seed, p_keep=0.6):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.rand((B, width), generator=g) < p_keep).to(torch.uint8)
+
+
+def run_masked(case, mask):
+    return oracle.decode_paged_masked(bits(case.q), bits(case.k_cache), bits(case.v_cache), case.block_table.numpy(),
+                                      case.seq_lens.numpy(), mask.numpy(), case.scale)
+
+
+@pytest.mark.parametrize("shape", SHAPES[:4])
+def test_masked_matches_torch_sdpa_with_bool_mask(shape):
+    B, Hq, Hkv, D, ps, lens = shape
+    case = inputs.make_paged_case(B, Hq, Hkv, D, ps, lens, 81 + D)
+    mask = random_mask(B, max(lens) + 3, 82)
+    mask[:, 0] = 1                       # keep one key per sequence so SDPA stays defined
+    got = run_masked(case, mask)
+    q = as_f64(case.q.float())
+    ks, vs = gather_logical(case)
+    for b in range(B):
+        L = lens[b]
+        kb = torch.from_numpy(ks[b]).permute(1, 0, 2)[None]
+        vb = torch.from_numpy(vs[b]).permute(1, 0, 2)[None]
+        am = mask[b, :L].bool()[None, None, None, :]
+        o = F.scaled_dot_product_attention(torch.from_numpy(q[b])[None, :, None, :], kb, vb, attn_mask=am,
+                                           scale=case.scale, enable_gqa=True)[0, :, 0, :].numpy()
+        np.testing.assert_allclose(got[b], o, rtol=1e-11, atol=1e-12)
+
+
+def test_masked_equals_decode_over_the_kept_keys_only():
+    case = inputs.make_paged_case(3, 8, 2, 64, 16, [50, 9, 130], 83, poison=False)
+    mask = random_mask(3, 130, 84, p_keep=0.3)
+    got = run_masked(case, mask)
+    ks, vs = gather_logical(case)
+    for b in range(3):
+        L = int(case.seq_lens[b])
+        keep = mask[b, :L].numpy().astype(bool)
+        n = int(keep.sum())
+        # a contiguous cache holding only the kept keys, in order
+        k = torch.from_numpy(ks[b][keep]).to(torch.bfloat16)[None]
+        v = torch.from_numpy(vs[b][keep]).to(torch.bfloat16)[None]
+        want = oracle.decode_contig(bits(case.q[b:b + 1]), bits(k), bits(v), np.array([n], np.int32), case.scale)
+        np.testing.assert_allclose(got[b], want[0], rtol=1e-13, atol=1e-14)
+
+
+def test_all_ones_and_all_zero_masks():
+    case = inputs.make_paged_case(2, 8, 2, 64, 16, [40, 77], 85)
+    ones = torch.ones((2, 80), dtype=torch.uint8)
+    np.testing.assert_array_equal(run_masked(case, ones), run_oracle(case))
+    zeros = torch.zeros((2, 80), dtype=torch.uint8)
+    assert np.all(run_masked(case, zeros) == 0)
+
+
+def test_multi_token_mask_joins_the_causal_rule():
+    kv, qt, qi = multi_case([40, 90], [3, 5], 86)
+    mask = random_mask(8, 96, 87)
+    mask[:, 0] = 1
+    got = oracle.decode_paged_multi(bits(qt), bits(kv.k_cache), bits(kv.v_cache), kv.block_table.numpy(),
+                                    kv.seq_lens.numpy(), qi, kv.scale, mask=mask.numpy())
+    ks, vs = gather_logical(kv)
+    q = as_f64(qt.float())
+    for b, (L, ql) in enumerate(zip([40, 90], [3, 5])):
+        kb = torch.from_numpy(ks[b]).permute(1, 0, 2)[None]
+        vb = torch.from_numpy(vs[b]).permute(1, 0, 2)[None]
+        for i in range(ql):
+            r = qi[b] + i
+            pos = L - ql + i
+            am = (torch.arange(L) <= pos) & mask[r, :L].bool()
+            o = F.scaled_dot_product_attention(torch.from_numpy(q[r])[None, :, None, :], kb, vb,
+                                               attn_mask=am[None, None, None, :], scale=kv.scale,
+                                               enable_gqa=True)[0, :, 0, :].numpy()
+            np.testing.assert_allclose(got[r], o, rtol=1e-11, atol=1e-12)
+    ones = np.ones((8, 96), np.uint8)
+    plain = oracle.decode_paged_multi(bits(qt), bits(kv.k_cache), bits(kv.v_cache), kv.block_table.numpy(),
+                                      kv.seq_lens.numpy(), qi, kv.scale)
+    np.testing.assert_array_equal(oracle.decode_paged_multi(bits(qt), bits(kv.k_cache), bits(kv.v_cache),
+                                                            kv.block_table.numpy(), kv.seq_lens.numpy(), qi,
+                                                            kv.scale, mask=ones), plain)
