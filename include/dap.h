@@ -241,6 +241,12 @@ size_t dap_workspace_bytes_multi(int total_q, int Hq, int D, int num_splits);
  *                dap_chunk_tokens(max_kv_len, num_splits) keys, one CTA per (tile, kv head,
  *                chunk), merged by a combine kernel.  0 = the library picks
  *                dap_plan_splits(SMs, num_tiles, Hq, Hkv, D, page_size, max_kv_len, 0).
+ *   mask         device uint8 [total_q, mask_stride] or NULL: the 3-D bool mask [batch,
+ *                q_len, kv_len] of [A: "Python Wrappers"] with its q rows packed like q
+ *                (row qo_indptr[b] + i; nonzero = keep).  Token i keeps key t only if t is
+ *                at or before its position and its mask byte is set (causal and mask
+ *                together).  mask_stride >= max_kv_len, a multiple of 16; mask 16-byte
+ *                aligned.  A token with no key left gives a zero row.
  *   workspace    device, >= dap_workspace_bytes_multi(total_q, Hq, D, S) bytes for the
  *                split count S used, 16-byte aligned.
  *   out          device bf16 [total_q, Hq, D], strides (out_stride_t, out_stride_h, 1).
@@ -253,10 +259,32 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
                                    int page_size, const int32_t *block_table, int max_pages,
                                    const int32_t *seq_lens, const int32_t *qo_indptr,
                                    const int32_t *tile_batch, const int32_t *tile_index,
-                                   int num_tiles, int total_q, int max_kv_len, int B, int Hq,
-                                   int Hkv, int D, float scale, int num_splits, void *workspace,
+                                   int num_tiles, int total_q, const uint8_t *mask,
+                                   long long mask_stride, int max_kv_len, int B, int Hq, int Hkv,
+                                   int D, float scale, int num_splits, void *workspace,
                                    size_t workspace_bytes, void *out, long long out_stride_t,
                                    long long out_stride_h, void *stream);
+
+/*
+ * Masked paged GQA decode [A: "Python Wrappers", the 2-D bool mask [batch, kv_len], True =
+ * keep]: decode_attn_paged where key t of sequence b takes part only if
+ * mask[b * mask_stride + t] is nonzero.  A sequence with no key left gives a zero row.
+ *   mask         device uint8 [B, mask_stride]; mask_stride >= max_kv_len, a multiple of 16;
+ *                mask 16-byte aligned (bytes past seq_lens[b] are not used).
+ *   num_splits   >= 1: per-sequence splits as decode_attn_paged; 0 = the library picks
+ *                dap_plan_splits(SMs, B, Hq, Hkv, D, page_size, max_kv_len, 0).
+ *   workspace    >= dap_workspace_bytes(B, Hq, Hkv, D, S) for the S used.
+ *   Everything else as decode_attn_paged.  Supported: D in {64, 128}; G in {1, 2, 4, 8};
+ *   page_size a multiple of 8.
+ */
+dap_status decode_attn_paged_masked(const void *q, long long q_stride_b, long long q_stride_h,
+                                    const void *k_cache, const void *v_cache, int num_pages,
+                                    int page_size, const int32_t *block_table, int max_pages,
+                                    const int32_t *seq_lens, const uint8_t *mask,
+                                    long long mask_stride, int max_kv_len, int B, int Hq, int Hkv,
+                                    int D, float scale, int num_splits, void *workspace,
+                                    size_t workspace_bytes, void *out, long long out_stride_b,
+                                    long long out_stride_h, void *stream);
 
 /*
  * fp8 sliding-window latent decode, K = V [C].

@@ -31,7 +31,7 @@ EXPORTS = ("dap_status_string", "dap_version", "dap_device_sm_count", "dap_plan_
            "decode_attn_paged_fp8", "decode_attn_paged_noalloc", "kv_append_paged", "kv_append_fp8",
            "dap_set_trace_events", "dap_get_device_errors", "dap_multi_tokens_per_tile",
            "dap_q_tile_map", "dap_workspace_bytes_multi", "decode_attn_paged_multi",
-           "decode_attn_paged_fp8kv", "kv_append_paged_fp8")
+           "decode_attn_paged_fp8kv", "kv_append_paged_fp8", "decode_attn_paged_masked")
 
 
 class DapError(RuntimeError):
@@ -94,8 +94,11 @@ def load(build_if_missing: bool = True):
         lib.dap_q_tile_map.restype = I
         lib.dap_workspace_bytes_multi.argtypes = [I, I, I, I]
         lib.dap_workspace_bytes_multi.restype = SZ
-        lib.decode_attn_paged_multi.argtypes = [P, LL, LL, P, P, I, I, P, I, P, P, P, P, I, I, I, I, I, I,
+        lib.decode_attn_paged_multi.argtypes = [P, LL, LL, P, P, I, I, P, I, P, P, P, P, I, I, P, LL, I, I, I, I,
                                                 I, F, I, P, SZ, P, LL, LL, P]
+        lib.decode_attn_paged_masked.argtypes = [P, LL, LL, P, P, I, I, P, I, P, P, LL, I, I, I, I, I, F, I, P, SZ,
+                                                 P, LL, LL, P]
+        lib.decode_attn_paged_masked.restype = I
         lib.decode_attn_paged_multi.restype = I
         lib.decode_attn_paged_fp8kv.argtypes = [P, LL, LL, P, P, P, P, I, I, P, I, P, I, I, I, I, I, F, I, P, SZ,
                                                 P, LL, LL, P]
@@ -291,6 +294,47 @@ def decode_attn_paged_fp8(q, kv_cache, inv_scale, slot_idx, lens, *, scale: floa
     return out
 
 
+def decode_attn_paged_masked(q, k_cache, v_cache, block_table, seq_lens, mask, *, max_kv_len: int,
+                             scale: float | None = None, num_splits: int = 0, total_kv: int = 0, workspace=None,
+                             out=None, stream=None):
+    """Masked paged GQA decode (include/dap.h: decode_attn_paged_masked): mask [B, >=
+    max_kv_len] bool/uint8, nonzero = keep, rows 16-byte strided.  num_splits 0 = the
+    planner's choice, resolved here so the workspace can be sized.  Returns ``out``."""
+    _bf16_3d(q, "q")
+    B, Hq, D = q.shape
+    _need(k_cache.dtype == torch.bfloat16 and k_cache.dim() == 4 and k_cache.is_contiguous()
+          and v_cache.shape == k_cache.shape and v_cache.dtype == torch.bfloat16
+          and v_cache.is_contiguous(), "k_cache/v_cache must be contiguous bf16 [P, ps, Hkv, D]")
+    P, ps, Hkv, D2 = k_cache.shape
+    _need(D2 == D, "head dims differ")
+    _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
+          and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
+    _need(seq_lens.dtype == torch.int32 and seq_lens.numel() == B and seq_lens.is_contiguous(),
+          "seq_lens must be contiguous int32 [B]")
+    mask = _mask(mask, B, int(max_kv_len))
+    _need(mask is not None, "mask is required")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    _bf16_3d(out, "out")
+    lib = load()
+    S = int(num_splits)
+    if S == 0 and B > 0:
+        S = lib.dap_plan_splits(lib.dap_device_sm_count(), B, Hq, Hkv, D, ps, int(max_kv_len), int(total_kv))
+    need = lib.dap_workspace_bytes(B, Hq, Hkv, D, S) if S >= 2 else 0
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.decode_attn_paged_masked(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
+                                      _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(mask),
+                                      mask.stride(0), int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S),
+                                      _ptr(workspace), wbytes, _ptr(out), out.stride(0), out.stride(1),
+                                      _stream(stream))
+    _check(st, "decode_attn_paged_masked")
+    return out
+
+
 # ---- GQA decode over an fp8 (e4m3) cache -----------------------------------------------
 
 def _fp8kv_cache(k_codes, v_codes, k_scale, v_scale):
@@ -379,9 +423,19 @@ class MultiPlan:
         self.tile_index = ti.to(device)
 
 
+def _mask(mask, rows, max_kv_len):
+    if mask is None:
+        return None
+    _need(mask.dtype in (torch.uint8, torch.bool) and mask.dim() == 2 and mask.shape[0] == rows
+          and mask.stride(1) == 1 and mask.stride(0) >= max(1, max_kv_len) and mask.stride(0) % 16 == 0,
+          "mask must be bool/uint8 [rows, >= max_kv_len] with unit inner stride and a row stride "
+          "that is a multiple of 16 bytes")
+    return mask
+
+
 def decode_attn_paged_multi(q, k_cache, v_cache, block_table, seq_lens, plan: MultiPlan, *, max_kv_len: int,
-                            scale: float | None = None, num_splits: int = 0, total_kv: int = 0, workspace=None,
-                            out=None, stream=None):
+                            scale: float | None = None, num_splits: int = 0, total_kv: int = 0, mask=None,
+                            workspace=None, out=None, stream=None):
     """Multi-token causal decode over a paged cache (include/dap.h: decode_attn_paged_multi).
     q [total_q, Hq, D] holds the new tokens of all sequences back to back; ``plan`` is the
     MultiPlan of their counts.  num_splits 0 = the planner's choice (dap_plan_splits over the
@@ -414,12 +468,13 @@ def decode_attn_paged_multi(q, k_cache, v_cache, block_table, seq_lens, plan: Mu
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    mask = _mask(mask, total_q, int(max_kv_len))
     st = lib.decode_attn_paged_multi(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
                                      _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
                                      _ptr(plan.qo_indptr), _ptr(plan.tile_batch), _ptr(plan.tile_index),
-                                     plan.num_tiles, total_q, int(max_kv_len), B, Hq, Hkv, D, float(scale),
-                                     int(S), _ptr(workspace), wbytes, _ptr(out), out.stride(0), out.stride(1),
-                                     _stream(stream))
+                                     plan.num_tiles, total_q, _ptr(mask), 0 if mask is None else mask.stride(0),
+                                     int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S), _ptr(workspace), wbytes,
+                                     _ptr(out), out.stride(0), out.stride(1), _stream(stream))
     _check(st, "decode_attn_paged_multi")
     return out
 

@@ -83,6 +83,15 @@ dap_status resolve_splits(int B, int Hq, int Hkv, int D, int page_size, int max_
     return DAP_OK;
 }
 
+// A bool mask (NULL = none): rows of mask_stride bytes, each covering at least max_kv_len
+// keys, 16-byte aligned rows (it is read by TMA).
+dap_status check_mask(const uint8_t *mask, long long mask_stride, int max_kv_len) {
+    if (!mask) return DAP_OK;
+    if (mask_stride < max_kv_len || mask_stride < 1 || mask_stride > (1LL << 32)) return DAP_ERR_SHAPE;
+    if (!aligned16(mask) || (mask_stride & 15)) return DAP_ERR_ALIGN;
+    return DAP_OK;
+}
+
 }  // namespace
 }  // namespace dap
 
@@ -284,10 +293,10 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
                                    const void *k_cache, const void *v_cache, int num_pages, int page_size,
                                    const int32_t *block_table, int max_pages, const int32_t *seq_lens,
                                    const int32_t *qo_indptr, const int32_t *tile_batch,
-                                   const int32_t *tile_index, int num_tiles, int total_q, int max_kv_len,
-                                   int B, int Hq, int Hkv, int D, float scale, int num_splits, void *workspace,
-                                   size_t workspace_bytes, void *out, long long out_stride_t,
-                                   long long out_stride_h, void *stream) {
+                                   const int32_t *tile_index, int num_tiles, int total_q, const uint8_t *mask,
+                                   long long mask_stride, int max_kv_len, int B, int Hq, int Hkv, int D,
+                                   float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                                   void *out, long long out_stride_t, long long out_stride_h, void *stream) {
     if (total_q < 0 || num_tiles < 0 || B < 0) return DAP_ERR_SHAPE;
     if (total_q == 0 && num_tiles == 0) return DAP_OK;
     // tokens without tiles, tiles without tokens, or more tiles than tokens
@@ -303,6 +312,7 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
         !aligned4(tile_batch) || !aligned4(tile_index))
         return DAP_ERR_ALIGN;
     if (page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
+    if ((st = check_mask(mask, mask_stride, max_kv_len)) != DAP_OK) return st;
     int S = num_splits;
     if (S == 0) {
         const int sms = dap_device_sm_count();
@@ -345,7 +355,70 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
     a.tile_index = tile_index;
     a.num_tiles = num_tiles;
     a.total_q = total_q;
+    a.mask = mask;
+    a.mask_stride = mask_stride;
     return launch_decode_multi(a, static_cast<cudaStream_t>(stream));
+}
+
+dap_status decode_attn_paged_masked(const void *q, long long q_stride_b, long long q_stride_h, const void *k_cache,
+                                    const void *v_cache, int num_pages, int page_size, const int32_t *block_table,
+                                    int max_pages, const int32_t *seq_lens, const uint8_t *mask,
+                                    long long mask_stride, int max_kv_len, int B, int Hq, int Hkv, int D,
+                                    float scale, int num_splits, void *workspace, size_t workspace_bytes,
+                                    void *out, long long out_stride_b, long long out_stride_h, void *stream) {
+    dap_status st = check_common(q, q_stride_b, q_stride_h, seq_lens, max_kv_len, B, Hq, Hkv, D, scale, num_splits,
+                                 out, out_stride_b, out_stride_h);
+    if (st != DAP_OK || B == 0) return st;
+    if (num_pages < 1 || page_size < 1 || max_pages < 1 ||
+        (long long)max_kv_len > (long long)max_pages * page_size)
+        return DAP_ERR_SHAPE;
+    if (!k_cache || !v_cache || !block_table) return DAP_ERR_NULL;
+    if (!mask) return DAP_ERR_NULL;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table)) return DAP_ERR_ALIGN;
+    if (page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
+    if ((st = check_mask(mask, mask_stride, max_kv_len)) != DAP_OK) return st;
+    int S = num_splits;
+    if (S == 0) {
+        const int sms = dap_device_sm_count();
+        if (sms <= 0) return DAP_ERR_CUDA;
+        S = dap_plan_splits(sms, B, Hq, Hkv, D, page_size, max_kv_len, 0);
+    }
+    const int chunk = dap_chunk_tokens(max_kv_len, S);
+    const int needed = max_kv_len > 0 ? (int)ceil_div_ll(max_kv_len, chunk) : 1;
+    S = std::max(1, std::min(S, needed));
+    if (S > 1) {
+        const size_t need = dap_workspace_bytes(B, Hq, Hkv, D, S);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DAP_ERR_WORKSPACE;
+    }
+    DecodeArgs a = {};
+    a.paged = true;
+    a.q = q;
+    a.q_sb = q_stride_b;
+    a.q_sh = q_stride_h;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.num_pages = num_pages;
+    a.page_size = page_size;
+    a.block_table = block_table;
+    a.max_pages = max_pages;
+    a.seq_lens = seq_lens;
+    a.max_kv_len = max_kv_len;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.scale = scale;
+    a.num_splits = S;
+    a.chunk = chunk;
+    a.workspace = workspace;
+    a.out = out;
+    a.o_sb = out_stride_b;
+    a.o_sh = out_stride_h;
+    a.num_tiles = B;  // one token per sequence, no work map
+    a.total_q = B;
+    a.mask = mask;
+    a.mask_stride = mask_stride;
+    return launch_decode_masked(a, static_cast<cudaStream_t>(stream));
 }
 
 dap_status decode_attn_paged_fp8kv(const void *q, long long q_stride_b, long long q_stride_h,

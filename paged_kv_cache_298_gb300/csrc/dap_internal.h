@@ -61,13 +61,18 @@ struct DecodeArgs {
     long long o_sb, o_sh;
     // e4m3 cache only: bf16 dequantisation factors [num_pages, Hkv, page_size] of k and v
     const void *k_scale, *v_scale;
-    // multi-token decode only: packed-q work map (q_sb / o_sb are then token strides)
+    // multi-token decode only: packed-q work map (q_sb / o_sb are then token strides); none
+    // (all NULL) for masked single-token decode
     const int32_t *qo_indptr, *tile_batch, *tile_index;
     int num_tiles, total_q;
+    // optional bool mask [total_q, mask_stride] bytes (nonzero = keep)
+    const uint8_t *mask;
+    long long mask_stride;
 };
 
 dap_status launch_decode(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_multi(const DecodeArgs &a, cudaStream_t stream);
+dap_status launch_decode_masked(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_fp8kv(const DecodeArgs &a, cudaStream_t stream);
 int multi_tokens_per_tile(int G);
 

@@ -8,6 +8,8 @@
 // columns: the tensor-core N dimension, against which every K/V tile staged by TMA is
 // used once for all of the tile's tokens.  The producer warp and the stage ring are the
 // single-token per-sequence schedule's; the consumer adds a causal mask per column.
+#include <string.h>
+
 #include "dap_tile.cuh"
 
 namespace dap {
@@ -20,18 +22,21 @@ namespace dap {
 // (the per-sequence schedule gives each CTA one unit), and the four warps merge their
 // partial states in quarters of D.
 
-template <int D_, int G_>
+// NT n8 tiles of query columns (2 for multi-token decode; 1 for masked single-token decode,
+// whose tiles hold one token); MASK: a bool mask tile rides with every K/V tile.
+template <int D_, int G_, int NT_ = 2, bool MASK_ = false>
 struct MultiCfg {
     static constexpr int D = D_, G = G_, HG = 1, NWC = 4, BT = 64, NS = 3, MINB = 2;
-    static constexpr bool MMA = true, SWZ = true;
-    static constexpr int NT = 2;                    // n8 tiles of query columns
-    static constexpr int NCOL = 8 * NT;             // 16 columns
+    static constexpr bool MMA = true, SWZ = true, MASK = MASK_;
+    static constexpr int NT = NT_;
+    static constexpr int NCOL = 8 * NT;             // query columns
     static constexpr int QT = NCOL / G;             // new tokens per work tile
     static constexpr int WPH = NWC, KPW = BT / NWC;
     static constexpr int ROWB = D * 2, HPU = G, NHALF = D / 64;
     static constexpr int TILE_BYTES = BT * ROWB;
     static constexpr int QBYTES = 0;
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int MASK_OFF = 2 * TILE_BYTES;  // [QT tokens][BT keys] bytes, 1024-aligned
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES + (MASK ? 1024 : 0);
     static constexpr int NPART = 4;                 // merge in quarters of D
     static constexpr int MRG_OFF = NS * STAGE_BYTES;
     static constexpr int MRG_BYTES = NWC * NCOL * (D / NPART + 2) * 4;
@@ -41,7 +46,8 @@ struct MultiCfg {
     static constexpr int BAR_OFF = (MISC_OFF + 16 + 7) & ~7;
     static constexpr int SMEM = BAR_OFF + (2 * NS + 1) * 8 + 1024;
     static constexpr int THREADS = (NWC + 1) * 32;
-    static_assert(KPW == 16 && NCOL % G == 0 && STAGE_BYTES % 1024 == 0, "multi-token tiling");
+    static_assert(KPW == 16 && NCOL % G == 0 && QT >= 1 && STAGE_BYTES % 1024 == 0 && QT * BT <= 1024,
+                  "multi-token tiling");
 };
 
 template <class C>
@@ -148,9 +154,15 @@ struct MultiConsumer {
                 const int col = n * 8 + 2 * t + j;
                 const int ti = col / G;
                 const int lim = p_base + ti;  // this column's token sees keys <= lim
-                const bool col_ok = ti < nq;
-                s[j] = (col_ok && g < nv && kpos0 <= lim) ? c[n][j] * qscale : -INFINITY;
-                s[j + 2] = (col_ok && g + 8 < nv && kpos1 <= lim) ? c[n][j + 2] * qscale : -INFINITY;
+                bool keep0 = ti < nq && g < nv && kpos0 <= lim;
+                bool keep1 = ti < nq && g + 8 < nv && kpos1 <= lim;
+                if constexpr (C::MASK) {  // the token's mask bytes of keys g, g+8 of this slice
+                    const uint8_t *mk = stage + C::MASK_OFF + ti * C::BT + key0 + g;
+                    keep0 = keep0 && mk[0] != 0;
+                    keep1 = keep1 && mk[8] != 0;
+                }
+                s[j] = keep0 ? c[n][j] * qscale : -INFINITY;
+                s[j + 2] = keep1 ? c[n][j + 2] * qscale : -INFINITY;
             }
             float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
 #pragma unroll
@@ -300,7 +312,7 @@ __device__ __forceinline__ bool multi_tile(const SplitParams &p, int b, int tind
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
     multi_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
-                 const SplitParams p) {
+                 const __grid_constant__ CUtensorMap mapM, const SplitParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = aligned_smem<C>(smem_raw);
     constexpr int G = C::G, NWC = C::NWC, BT = C::BT, NS = C::NS, D = C::D;
@@ -315,9 +327,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     // entry, then its sequence's q range and length together with the producer's page ids
     // of the first tile (read from position s * chunk on; entries past the sequence's end
     // are read within the table but not used).
-    const int wb = p.tile_batch[w], wi = p.tile_index[w];
+    // (no work map: one token per sequence, tile w = sequence w)
+    const int wb = p.tile_batch ? p.tile_batch[w] : w, wi = p.tile_index ? p.tile_index[w] : 0;
     const int bb = (wb >= 0 && wb < p.B) ? wb : 0;
-    const int q0 = p.qo_indptr[bb], q1 = p.qo_indptr[bb + 1], Lraw = p.seq_lens[bb];
+    const int q0 = p.qo_indptr ? p.qo_indptr[bb] : bb, q1 = p.qo_indptr ? p.qo_indptr[bb + 1] : bb + 1;
+    const int Lraw = p.seq_lens[bb];
     const int R = p.box_rows;
     int pg_first = 0;
     if (warp == NWC && lane * R < BT) {
@@ -351,6 +365,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
         if (lane == 0) {
             prefetch_tensormap(&mapK);
             prefetch_tensormap(&mapV);
+            if (C::MASK) prefetch_tensormap(&mapM);
         }
         const int32_t *table = p.block_table + (long long)tl.b * p.max_pages;
         auto lookup = [&](int tile) -> int {
@@ -376,7 +391,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
             const int t = tok0 + i * BT;
             const int nvalid = min(BT, tok1 - t);
             const int nbox = (nvalid + R - 1) / R;
-            const uint32_t bytes = (uint32_t)(nbox * R * C::ROWB * 2);
+            const uint32_t bytes = (uint32_t)(nbox * R * C::ROWB * 2 + (C::MASK ? C::QT * BT : 0));
             if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
             __syncwarp();
             if (lane < nbox) {
@@ -384,6 +399,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
                 issue_kv_box<C>(smem + st * C::STAGE_BYTES, lane, R, &mapK, &mapV, kvh, tt % p.page_size, pg,
                                 &full[st]);
             }
+            // the tile's mask bytes: keys [t, t + 64) of the tile's tokens (zeros past the ends)
+            if (C::MASK && lane == 31)
+                tma_load_3d(smem + st * C::STAGE_BYTES + C::MASK_OFF, &mapM, t, tl.q0 + tl.i0, 0, &full[st]);
             issued = i + 1;
         }
         if (lane == 0) misc[0] = issued;
@@ -441,13 +459,18 @@ __global__ void __launch_bounds__(256) combine_multi_kernel(const SplitParams p,
     const int lane = threadIdx.x & 31;
     if (gw >= p.total_q * p.Hq) return;
     const int r = gw / p.Hq, hq = gw - r * p.Hq;
-    int lo = 0, hi = p.B;  // qo_indptr[lo] <= r < qo_indptr[hi] for a well-formed map
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (p.qo_indptr[mid] <= r) lo = mid;
-        else hi = mid;
+    int lo = r, q0 = r, q1 = r + 1;  // no work map: row r is sequence r's one token
+    if (p.qo_indptr) {
+        int hi = p.B;  // qo_indptr[lo] <= r < qo_indptr[hi] for a well-formed map
+        lo = 0;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.qo_indptr[mid] <= r) lo = mid;
+            else hi = mid;
+        }
+        q0 = p.qo_indptr[lo];
+        q1 = p.qo_indptr[lo + 1];
     }
-    const int q0 = p.qo_indptr[lo], q1 = p.qo_indptr[lo + 1];
     MultiTile tl;
     if (!multi_tile(p, lo, (r - q0) / qt, q0, q1, p.seq_lens[lo], qt, false, &tl)) return;
     const int nsplit = max(1, (tl.kv_end + p.chunk - 1) / p.chunk);
@@ -476,14 +499,29 @@ __global__ void __launch_bounds__(256) combine_multi_kernel(const SplitParams p,
 
 namespace {
 
-template <int D, int G>
+// mask [rows, mask_stride] bytes viewed as [mask_stride, rows, 1]; box [64, QT, 1]
+bool encode_mask_map(CUtensorMap *map, const void *base, long long stride, long long rows, int qt) {
+    EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)stride, (cuuint64_t)rows, 1u};
+    const cuuint64_t strides[2] = {(cuuint64_t)stride, (cuuint64_t)(stride * rows)};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)qt, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int G, int NT, bool MASK>
 dap_status launch_multi(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
-    using C = MultiCfg<D, G>;
+    using C = MultiCfg<D, G, NT, MASK>;
     const int R = gcd_int(a.page_size, C::BT);
     p.box_rows = R;
-    CUtensorMap mk, mv;
+    CUtensorMap mk, mv, mm;
+    memset(&mm, 0, sizeof mm);
     if (!encode_cache_map<C>(&mk, a.k, a.D, a.Hkv, a.page_size, a.num_pages, R) ||
-        !encode_cache_map<C>(&mv, a.v, a.D, a.Hkv, a.page_size, a.num_pages, R))
+        !encode_cache_map<C>(&mv, a.v, a.D, a.Hkv, a.page_size, a.num_pages, R) ||
+        (MASK && !encode_mask_map(&mm, a.mask, a.mask_stride, a.total_q, C::QT)))
         return DAP_ERR_CUDA;
     auto kern = multi_kernel<C>;
     static int occ = 0;
@@ -495,7 +533,7 @@ dap_status launch_multi(const DecodeArgs &a, SplitParams &p, cudaStream_t stream
                                                              partial_acc_bytes(a.total_q, a.Hq, a.D, a.num_splits))
                                  : nullptr;
     if (g_trace.split_begin) cudaEventRecord(g_trace.split_begin, stream);
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(mk, mv, p);
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(mk, mv, mm, p);
     if (cudaGetLastError() != cudaSuccess) return DAP_ERR_CUDA;
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
     if (a.num_splits > 1) {
@@ -511,25 +549,38 @@ dap_status launch_multi(const DecodeArgs &a, SplitParams &p, cudaStream_t stream
 
 int multi_tokens_per_tile(int G) { return G >= 1 && G <= 16 ? 16 / G : 0; }
 
-dap_status launch_decode_multi(const DecodeArgs &a, cudaStream_t stream) {
-    SplitParams p = make_params(a);
-    const int G = a.Hq / a.Hkv;
-    if (a.D == 128) {
-        switch (G) {
-            case 1: return launch_multi<128, 1>(a, p, stream);
-            case 2: return launch_multi<128, 2>(a, p, stream);
-            case 4: return launch_multi<128, 4>(a, p, stream);
-            case 8: return launch_multi<128, 8>(a, p, stream);
-        }
-    } else if (a.D == 64) {
-        switch (G) {
-            case 1: return launch_multi<64, 1>(a, p, stream);
-            case 2: return launch_multi<64, 2>(a, p, stream);
-            case 4: return launch_multi<64, 4>(a, p, stream);
-            case 8: return launch_multi<64, 8>(a, p, stream);
-        }
+namespace {
+
+template <int D, int NT, bool MASK>
+dap_status dispatch_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
+    switch (a.Hq / a.Hkv) {
+        case 1: return launch_multi<D, 1, NT, MASK>(a, p, stream);
+        case 2: return launch_multi<D, 2, NT, MASK>(a, p, stream);
+        case 4: return launch_multi<D, 4, NT, MASK>(a, p, stream);
+        case 8: return launch_multi<D, 8, NT, MASK>(a, p, stream);
     }
     return DAP_ERR_UNSUPPORTED;
+}
+
+template <int NT, bool MASK>
+dap_status dispatch_d(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
+    if (a.D == 128) return dispatch_g<128, NT, MASK>(a, p, stream);
+    if (a.D == 64) return dispatch_g<64, NT, MASK>(a, p, stream);
+    return DAP_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+dap_status launch_decode_multi(const DecodeArgs &a, cudaStream_t stream) {
+    SplitParams p = make_params(a);
+    return a.mask ? dispatch_d<2, true>(a, p, stream) : dispatch_d<2, false>(a, p, stream);
+}
+
+// Masked single-token decode: one token per sequence with no work map (tile w = sequence w),
+// one n8 tile of query columns (G heads of the one token).
+dap_status launch_decode_masked(const DecodeArgs &a, cudaStream_t stream) {
+    SplitParams p = make_params(a);
+    return dispatch_d<1, true>(a, p, stream);
 }
 
 bool read_errors_multi(unsigned int *flags, bool clear) {

@@ -197,8 +197,9 @@ def multi_call(lib, **kw):
     a.update(kw)
     return lib.decode_attn_paged_multi(a["q"], a["qst"], a["qsh"], a["k"], a["v"], a["P"], a["ps"], a["table"],
                                        a["maxp"], a["lens"], a["qi"], a["tb"], a["ti"], a["ntiles"], a["totq"],
-                                       a["maxlen"], a["B"], a["Hq"], a["Hkv"], a["D"], a["scale"], a["S"],
-                                       a["ws"], a["wsb"], a["out"], a["ost"], a["osh"], None)
+                                       a.get("mask"), a.get("mst", 0), a["maxlen"], a["B"], a["Hq"], a["Hkv"],
+                                       a["D"], a["scale"], a["S"], a["ws"], a["wsb"], a["out"], a["ost"], a["osh"],
+                                       None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -208,6 +209,7 @@ def multi_call(lib, **kw):
     (dict(D=96), 3), (dict(ps=12, maxlen=90), 3), (dict(Hq=64, Hkv=4), 3),
     (dict(qi=ctypes.c_void_p((1 << 20) + 2)), 5), (dict(qst=4100), 5),
     (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=16), 4),
+    (dict(mask=FAKE, mst=96), 2), (dict(mask=FAKE, mst=120), 5), (dict(mask=ctypes.c_void_p((1 << 20) + 4), mst=128), 5),
 ])
 def test_multi_validation(lib, kw, status):
     assert multi_call(lib, **kw) == status
@@ -258,3 +260,29 @@ def test_append_paged_fp8_validation(lib):
     assert call(0, None) == 1 and call(4, None) == 1
     assert call(11, 0) == 0
     assert call(2, ctypes.c_void_p((1 << 20) + 4)) == 5 and call(4, ctypes.c_void_p((1 << 20) + 1)) == 5
+
+
+def masked_call(lib, **kw):
+    a = dict(q=FAKE, qsb=32 * 128, qsh=128, k=FAKE, v=FAKE, P=64, ps=16, table=FAKE, maxp=8, lens=FAKE, mask=FAKE,
+             mst=128, maxlen=100, B=2, Hq=32, Hkv=8, D=128, scale=0.088, S=1, ws=None, wsb=0, out=FAKE,
+             osb=32 * 128, osh=128)
+    a.update(kw)
+    return lib.decode_attn_paged_masked(a["q"], a["qsb"], a["qsh"], a["k"], a["v"], a["P"], a["ps"], a["table"],
+                                        a["maxp"], a["lens"], a["mask"], a["mst"], a["maxlen"], a["B"], a["Hq"],
+                                        a["Hkv"], a["D"], a["scale"], a["S"], a["ws"], a["wsb"], a["out"], a["osb"],
+                                        a["osh"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=-1), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(mst=96), 2), (dict(S=-1), 2),
+    (dict(mask=None), 1), (dict(q=None), 1), (dict(table=None), 1),
+    (dict(D=96), 3), (dict(ps=12, maxlen=90), 3),
+    (dict(mst=120), 5), (dict(mask=ctypes.c_void_p((1 << 20) + 8)), 5),
+    (dict(S=4), 4),
+])
+def test_masked_validation(lib, kw, status):
+    assert masked_call(lib, **kw) == status
+
+
+def test_masked_empty_batch_is_a_no_op(lib):
+    assert masked_call(lib, B=0, q=None, out=None, lens=None, mask=None, k=None, table=None) == 0
