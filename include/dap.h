@@ -126,9 +126,10 @@ size_t dap_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits);
  *                initialisation; its contents are undefined afterwards.
  *   out          device bf16 [B, Hq, D], element strides (out_stride_b, out_stride_h, 1).
  *                Written in full (an empty sequence gives a zero row).
- *   Supported: D in {64, 128}; G in {1, 2, 4, 8}; any page_size >= 1.  q, out,
- *   k_cache and v_cache 16-byte aligned; q/out strides multiples of 8 elements, nonzero
- *   where the extent they step over is above 1.
+ *   Supported: D in {32, 64, 128, 256}; G in {1, 2, 4, 8}; any page_size >= 1 for D in
+ *   {64, 128}, a multiple of 8 for D in {32, 256}.  q, out, k_cache and v_cache 16-byte
+ *   aligned; q/out strides multiples of 8 elements, nonzero where the extent they step
+ *   over is above 1.
  *   The result is bit-identical under any permutation of the physical pages for a fixed
  *   num_splits (the summation order depends only on logical positions).
  */

@@ -51,7 +51,7 @@ dap_status check_common(const void *q, long long q_sb, long long q_sh, const int
     if (B == 0) return DAP_OK;
     if ((Hq > 1 && (q_sh == 0 || o_sh == 0)) || (B > 1 && (q_sb == 0 || o_sb == 0))) return DAP_ERR_SHAPE;
     if (!q || !seq_lens || !out) return DAP_ERR_NULL;
-    if (!(D == 64 || D == 128) || !supported_group(Hq / Hkv)) return DAP_ERR_UNSUPPORTED;
+    if (!(D == 32 || D == 64 || D == 128 || D == 256) || !supported_group(Hq / Hkv)) return DAP_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(out) || !aligned4(seq_lens) || (q_sb & 7) || (q_sh & 7) ||
         (o_sb & 7) || (o_sh & 7))
         return DAP_ERR_ALIGN;
@@ -183,6 +183,7 @@ dap_status decode_attn_paged(const void *q, long long q_stride_b, long long q_st
         return DAP_ERR_SHAPE;
     if (!k_cache || !v_cache || !block_table) return DAP_ERR_NULL;
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table)) return DAP_ERR_ALIGN;
+    if ((D == 32 || D == 256) && page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
     DecodeArgs a = {};
     a.paged = true;
     a.q = q;
@@ -311,7 +312,7 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table) || !aligned4(qo_indptr) ||
         !aligned4(tile_batch) || !aligned4(tile_index))
         return DAP_ERR_ALIGN;
-    if (page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
+    if (page_size % 8 != 0 || !(D == 64 || D == 128)) return DAP_ERR_UNSUPPORTED;
     if ((st = check_mask(mask, mask_stride, max_kv_len)) != DAP_OK) return st;
     int S = num_splits;
     if (S == 0) {
@@ -375,7 +376,7 @@ dap_status decode_attn_paged_masked(const void *q, long long q_stride_b, long lo
     if (!k_cache || !v_cache || !block_table) return DAP_ERR_NULL;
     if (!mask) return DAP_ERR_NULL;
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table)) return DAP_ERR_ALIGN;
-    if (page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
+    if (page_size % 8 != 0 || !(D == 64 || D == 128)) return DAP_ERR_UNSUPPORTED;
     if ((st = check_mask(mask, mask_stride, max_kv_len)) != DAP_OK) return st;
     int S = num_splits;
     if (S == 0) {

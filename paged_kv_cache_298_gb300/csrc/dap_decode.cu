@@ -333,7 +333,9 @@ struct MmaCfg {
     static constexpr int KPW = BT / NWC;           // keys per warp per tile
     static constexpr int ROWB = D * 2;
     static constexpr int HPU = G;
-    static constexpr int NHALF = D / 64;           // 128-byte column blocks per row
+    static constexpr int SWB = D >= 64 ? 128 : 64;  // swizzled column block: 128 B (64 B at D = 32)
+    static constexpr int NBLK = ROWB / SWB;         // column blocks per row
+    static constexpr int CPB = SWB / 16;            // 16-byte chunks per block row
     static constexpr int TILE_BYTES = BT * ROWB;
     static constexpr int QBYTES = G * ROWB;
     static constexpr int STAGE_BYTES = (2 * TILE_BYTES + QBYTES + 1023) & ~1023;
@@ -347,7 +349,7 @@ struct MmaCfg {
     static constexpr int THREADS = (NWC + 1) * 32;
     static_assert(KPW == 16, "one m16 key slice per warp per tile");
     static_assert(G <= 8, "the query heads of a kv head fill at most N = 8");
-    static_assert(D % 64 == 0, "whole 128-byte column blocks");
+    static_assert(D % 32 == 0 && ROWB % SWB == 0, "whole swizzled column blocks");
 };
 
 template <class C>
@@ -394,10 +396,13 @@ struct MmaConsumer {
         }
     }
 
-    // byte offset of (key, dim) in a swizzled [D/64][BT][128 B] tile
+    // byte offset of (key, dim) in a swizzled [NBLK][BT][SWB] tile: the 128-byte swizzle XORs
+    // the 16-byte chunk index with key & 7, the 64-byte one with (key >> 1) & 3
     static __device__ __forceinline__ uint32_t off(int key, int dim) {
-        const int chunk = (dim & 63) >> 3;
-        return (uint32_t)((dim >> 6) * (C::BT * 128) + key * 128 + ((chunk ^ (key & 7)) << 4));
+        const int byte = dim * 2;
+        const int chunk = (byte % C::SWB) >> 4;
+        const int sw = C::SWB == 128 ? (key & 7) : ((key >> 1) & 3);
+        return (uint32_t)((byte / C::SWB) * (C::BT * C::SWB) + key * C::SWB + ((chunk ^ sw) << 4));
     }
 
     __device__ __forceinline__ void tile(uint8_t *stage, int nvalid) {
@@ -405,11 +410,11 @@ struct MmaConsumer {
         if (nv <= 0) return;  // no key of this slice is valid
         uint8_t *sV = stage + C::TILE_BYTES;
         if (nv < 16) {  // rows past the end may hold anything: zero their V so 0 * V stays 0
-            for (int i = lane; i < (16 - nv) * C::NHALF * 8; i += 32) {
-                const int row = key0 + nv + i / (C::NHALF * 8);
-                const int rest = i % (C::NHALF * 8);
-                *reinterpret_cast<uint4 *>(sV + (rest >> 3) * (C::BT * 128) + row * 128 + (rest & 7) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
+            for (int i = lane; i < (16 - nv) * C::NBLK * C::CPB; i += 32) {
+                const int row = key0 + nv + i / (C::NBLK * C::CPB);
+                const int rest = i % (C::NBLK * C::CPB);
+                *reinterpret_cast<uint4 *>(sV + (rest / C::CPB) * (C::BT * C::SWB) + row * C::SWB +
+                                           (rest % C::CPB) * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -1009,8 +1014,7 @@ __global__ void __launch_bounds__(128) combine_balanced_kernel(const SplitParams
             a[j] = red[0][lane * DPV + j] + red[1][lane * DPV + j] + red[2][lane * DPV + j] + red[3][lane * DPV + j];
         const int b = u / nkvg, kvg = u - b * nkvg;
         __nv_bfloat16 *o = p.out + (long long)b * p.o_sb + (long long)(kvg * hpu + hl2) * p.o_sh + lane * DPV;
-#pragma unroll
-        for (int j = 0; j < DPV; j += 2) store_out_pair(o + j, a[j], a[j + 1], L);
+        store_row_part<DPV>(o, a, L);
     }
 }
 
@@ -1043,8 +1047,7 @@ dap_status launch_per_sequence(const DecodeArgs &a, SplitParams &p, cudaStream_t
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
     if (a.num_splits > 1) {
         const dim3 cgrid((unsigned)((a.B * a.Hq + 7) / 8));
-        const cudaError_t e = a.D == 128 ? launch_dependent(combine_kernel<128>, cgrid, dim3(256), stream, p)
-                                         : launch_dependent(combine_kernel<64>, cgrid, dim3(256), stream, p);
+        const cudaError_t e = launch_dependent(combine_kernel<C::D>, cgrid, dim3(256), stream, p);
         if (e != cudaSuccess) return DAP_ERR_CUDA;
     }
     if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);
@@ -1084,8 +1087,7 @@ dap_status launch_balanced(const DecodeArgs &a, SplitParams &p, cudaStream_t str
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
     const dim3 cgrid((unsigned)(a.B * nkvg * C::HPU));
     const cudaError_t e =
-        a.D == 128 ? launch_dependent(combine_balanced_kernel<128>, cgrid, dim3(128), stream, p, (int)C::HPU, nkvg)
-                   : launch_dependent(combine_balanced_kernel<64>, cgrid, dim3(128), stream, p, (int)C::HPU, nkvg);
+        launch_dependent(combine_balanced_kernel<C::D>, cgrid, dim3(128), stream, p, (int)C::HPU, nkvg);
     if (e != cudaSuccess) return DAP_ERR_CUDA;
     if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);
     return DAP_OK;
@@ -1097,8 +1099,12 @@ dap_status launch_balanced(const DecodeArgs &a, SplitParams &p, cudaStream_t str
 // consumer (any other page size: boxes of fewer than 8 rows cannot start on the
 // 1024-byte boundaries the swizzle needs): 32-token tiles, four stages, three CTAs per SM
 // (two for G = 8).
+// D = 256: 32-token tiles and two consumer warps keep a stage near 34 KB (two CTAs per
+// SM); D = 32: six stages of 8 KB at three CTAs per SM.
 template <int D, int G>
-using MmaCfgFor = MmaCfg<D, G, 4, 64, 3, 2>;
+using MmaCfgFor = typename std::conditional<
+    D == 256, MmaCfg<256, G, 2, 32, 3, 2>,
+    typename std::conditional<D == 32, MmaCfg<32, G, 4, 64, 6, 3>, MmaCfg<D, G, 4, 64, 3, 2>>::type>::type;
 template <int D, int G>
 using CoreCfgFor = SplitCfg<D, G, 1, 4, 32, 4, (G <= 4 ? 3 : 2)>;
 
@@ -1111,8 +1117,22 @@ dap_status run(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
 
 template <int D, int G>
 dap_status dispatch(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
-    if (a.paged && a.page_size % 8 != 0) return run<CoreCfgFor<D, G>>(a, p, stream);
+    if (a.paged && a.page_size % 8 != 0) {
+        if constexpr (D == 64 || D == 128) return run<CoreCfgFor<D, G>>(a, p, stream);
+        return DAP_ERR_UNSUPPORTED;  // head dims 32 and 256 need page sizes that are multiples of 8
+    }
     return run<MmaCfgFor<D, G>>(a, p, stream);
+}
+
+template <int D>
+dap_status dispatch_groups(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
+    switch (a.Hq / a.Hkv) {
+        case 1: return dispatch<D, 1>(a, p, stream);
+        case 2: return dispatch<D, 2>(a, p, stream);
+        case 4: return dispatch<D, 4>(a, p, stream);
+        case 8: return dispatch<D, 8>(a, p, stream);
+    }
+    return DAP_ERR_UNSUPPORTED;
 }
 
 }  // namespace
@@ -1141,21 +1161,11 @@ bool read_errors_decode(unsigned int *flags, bool clear) {
 
 dap_status launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     SplitParams p = make_params(a);
-    const int G = a.Hq / a.Hkv;
-    if (a.D == 128) {
-        switch (G) {
-            case 1: return dispatch<128, 1>(a, p, stream);
-            case 2: return dispatch<128, 2>(a, p, stream);
-            case 4: return dispatch<128, 4>(a, p, stream);
-            case 8: return dispatch<128, 8>(a, p, stream);
-        }
-    } else if (a.D == 64) {
-        switch (G) {
-            case 1: return dispatch<64, 1>(a, p, stream);
-            case 2: return dispatch<64, 2>(a, p, stream);
-            case 4: return dispatch<64, 4>(a, p, stream);
-            case 8: return dispatch<64, 8>(a, p, stream);
-        }
+    switch (a.D) {
+        case 32: return dispatch_groups<32>(a, p, stream);
+        case 64: return dispatch_groups<64>(a, p, stream);
+        case 128: return dispatch_groups<128>(a, p, stream);
+        case 256: return dispatch_groups<256>(a, p, stream);
     }
     return DAP_ERR_UNSUPPORTED;
 }

@@ -32,7 +32,7 @@ struct MultiCfg {
     static constexpr int NCOL = 8 * NT;             // query columns
     static constexpr int QT = NCOL / G;             // new tokens per work tile
     static constexpr int WPH = NWC, KPW = BT / NWC;
-    static constexpr int ROWB = D * 2, HPU = G, NHALF = D / 64;
+    static constexpr int ROWB = D * 2, HPU = G, SWB = 128, NBLK = ROWB / SWB, CPB = SWB / 16;
     static constexpr int TILE_BYTES = BT * ROWB;
     static constexpr int QBYTES = 0;
     static constexpr int MASK_OFF = 2 * TILE_BYTES;  // [QT tokens][BT keys] bytes, 1024-aligned
@@ -118,9 +118,9 @@ struct MultiConsumer {
         if (nv <= 0) return;
         uint8_t *sV = stage + C::TILE_BYTES;
         if (nv < 16) {
-            for (int i = lane; i < (16 - nv) * C::NHALF * 8; i += 32) {
-                const int row = key0 + nv + i / (C::NHALF * 8);
-                const int rest = i % (C::NHALF * 8);
+            for (int i = lane; i < (16 - nv) * C::NBLK * 8; i += 32) {
+                const int row = key0 + nv + i / (C::NBLK * 8);
+                const int rest = i % (C::NBLK * 8);
                 *reinterpret_cast<uint4 *>(sV + (rest >> 3) * (C::BT * 128) + row * 128 + (rest & 7) * 16) =
                     make_uint4(0u, 0u, 0u, 0u);
             }

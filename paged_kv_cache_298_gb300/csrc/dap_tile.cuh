@@ -72,10 +72,10 @@ __device__ __forceinline__ void issue_kv_box(uint8_t *stage, int j, int R, const
                                              const CUtensorMap *mv, int kvh0, int row, int page, uint64_t *bar) {
     if constexpr (C::SWZ) {
 #pragma unroll
-        for (int h = 0; h < C::NHALF; ++h) {
-            uint8_t *dst = stage + h * (C::BT * 128) + j * R * 128;
-            tma_load_4d(dst, mk, 64 * h, kvh0, row, page, bar);
-            tma_load_4d(dst + C::TILE_BYTES, mv, 64 * h, kvh0, row, page, bar);
+        for (int h = 0; h < C::NBLK; ++h) {
+            uint8_t *dst = stage + h * (C::BT * C::SWB) + j * R * C::SWB;
+            tma_load_4d(dst, mk, (C::SWB / 2) * h, kvh0, row, page, bar);
+            tma_load_4d(dst + C::TILE_BYTES, mv, (C::SWB / 2) * h, kvh0, row, page, bar);
         }
     } else {
         uint8_t *dst = stage + j * R * C::HG * C::ROWB;
@@ -87,10 +87,43 @@ __device__ __forceinline__ void issue_kv_box(uint8_t *stage, int j, int R, const
 // Merge of split partials for one output row, one warp, lanes over D: M = max_s m_s,
 // out = sum_s 2^(m_s-M) acc_s / sum_s 2^(m_s-M) l_s (AstrAI csrc log, split-KV commit: the
 // combine kernel; numerics commit: guarded division).
+// DPV consecutive floats of a partial row (DPV = D / 32 in 1..8), vector loads where they fit.
+template <int DPV>
+__device__ __forceinline__ void load_row_part(const float *src, float (&x)[DPV]) {
+    if constexpr (DPV % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < DPV; j += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(src + j);
+            x[j] = v.x;
+            x[j + 1] = v.y;
+            x[j + 2] = v.z;
+            x[j + 3] = v.w;
+        }
+    } else if constexpr (DPV == 2) {
+        const float2 v = *reinterpret_cast<const float2 *>(src);
+        x[0] = v.x;
+        x[1] = v.y;
+    } else {
+#pragma unroll
+        for (int j = 0; j < DPV; ++j) x[j] = src[j];
+    }
+}
+
+// Normalise and store one lane's DPV output values (bf16, round to nearest even).
+template <int DPV>
+__device__ __forceinline__ void store_row_part(__nv_bfloat16 *o, const float (&a)[DPV], float l) {
+    if constexpr (DPV == 1) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        *o = __float2bfloat16_rn(a[0] * inv);
+    } else {
+#pragma unroll
+        for (int j = 0; j < DPV; j += 2) store_out_pair(o + j, a[j], a[j + 1], l);
+    }
+}
+
 template <int D>
 struct RowMerge {
     static constexpr int DPV = D / 32;
-    using Vec = typename std::conditional<DPV == 4, float4, float2>::type;
     float acc[DPV];
     float lsum, Mu;
     __device__ __forceinline__ void begin(float m_max) {
@@ -101,12 +134,12 @@ struct RowMerge {
     }
     // add the partial rows o[0..n) (n <= 8), whose loads are all issued before any use
     __device__ __forceinline__ void add_batch(const float *const *o, const float2 *ml, int n, int lane) {
-        Vec x[8];
+        float x[8][DPV];
         float f[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             if (k < n) {
-                x[k] = *reinterpret_cast<const Vec *>(o[k] + lane * DPV);
+                load_row_part<DPV>(o[k] + lane * DPV, x[k]);
                 f[k] = ex2(ml[k].x - Mu);
             }
         }
@@ -114,16 +147,12 @@ struct RowMerge {
         for (int k = 0; k < 8; ++k) {
             if (k < n) {
                 lsum = fmaf(f[k], ml[k].y, lsum);
-                const float *xv = reinterpret_cast<const float *>(&x[k]);
 #pragma unroll
-                for (int j = 0; j < DPV; ++j) acc[j] = fmaf(f[k], xv[j], acc[j]);
+                for (int j = 0; j < DPV; ++j) acc[j] = fmaf(f[k], x[k][j], acc[j]);
             }
         }
     }
-    __device__ __forceinline__ void store(__nv_bfloat16 *o, int lane) {
-#pragma unroll
-        for (int j = 0; j < DPV; j += 2) store_out_pair(o + lane * DPV + j, acc[j], acc[j + 1], lsum);
-    }
+    __device__ __forceinline__ void store(__nv_bfloat16 *o, int lane) { store_row_part<DPV>(o + lane * DPV, acc, lsum); }
 };
 
 // Per-sequence schedule: merge the splits of every (sequence, head) row that more than one
@@ -187,9 +216,10 @@ bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv, long l
                       int box_rows) {
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows, (cuuint64_t)outer};
     const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)rows * Hkv * D * 2};
-    if (C::SWZ) {
-        const cuuint32_t box[4] = {64u, 1u, (cuuint32_t)box_rows, 1u};
-        return encode_bf16(map, base, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if constexpr (C::SWZ) {
+        const cuuint32_t box[4] = {(cuuint32_t)(C::SWB / 2), 1u, (cuuint32_t)box_rows, 1u};
+        return encode_bf16(map, base, 4, dims, strides, box,
+                           C::SWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     }
     const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)C::HG, (cuuint32_t)box_rows, 1u};
     return encode_bf16(map, base, 4, dims, strides, box);

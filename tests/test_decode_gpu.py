@@ -67,6 +67,10 @@ SHAPES = [
     (2, 16, 4, 64, 3, [50, 3]),                  # page size 3 (one-token boxes)
     (2, 32, 4, 128, 100, [250, 99]),             # page size not a power of two
     (2, 16, 2, 64, 32, [513, 64]),               # G=8, D=64
+    (3, 8, 2, 256, 16, [300, 17, 64]),           # D=256 (32-token tiles, two consumer warps)
+    (2, 64, 8, 256, 8, [100, 513]),              # D=256, G=8, page 8
+    (3, 16, 16, 32, 16, [1, 200, 65]),           # D=32 (64-byte swizzle), G=1
+    (2, 32, 4, 32, 32, [700, 5]),                # D=32, G=8
 ]
 
 
@@ -220,3 +224,22 @@ def test_long_context_workload_split_sweep(B):
         outs[S] = gpu_paged(case, S)
         sampled_rows(case, outs[S], n=16, seed=S)
     assert binding.get_device_errors() == 0
+
+
+@pytest.mark.parametrize("D", [32, 256])
+def test_contiguous_head_dims_32_and_256(D):
+    case = inputs.make_paged_case(3, 16, 4, D, 16, [150, 1, 64], 79 + D).to("cuda")
+    k, v = inputs.logical_kv(case, max_len=160)
+    ref = oracle.decode_contig(bits(case.q), bits(k), bits(v), case.seq_lens.cpu().numpy(), case.scale)
+    for S in [0, 1, 3]:
+        c = binding.decode_attn_contig(case.q, k, v, case.seq_lens, max_kv_len=case.max_kv_len, num_splits=S)
+        assert_close(c, ref, f"contig D={D} S={S}")
+        assert torch.equal(c, gpu_paged(case, S))
+
+
+@pytest.mark.parametrize("D", [32, 256])
+def test_head_dims_32_and_256_refuse_unaligned_pages(D):
+    case = inputs.make_paged_case(2, 8, 2, D, 12, [30, 50], 81).to("cuda")
+    with pytest.raises(binding.DapError) as e:
+        gpu_paged(case, 1)
+    assert e.value.status == 3
