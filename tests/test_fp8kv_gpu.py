@@ -56,6 +56,9 @@ SHAPES = [
     (3, 32, 8, 16, [257, 1000, 17]),        # G=4
     (2, 64, 8, 64, [128, 777]),             # G=8, page 64
     (5, 16, 2, 32, [1, 2, 63, 64, 65]),     # G=8, lengths around one tile
+    (3, 12, 3, 16, [40, 300, 129]),         # G=4, odd kv head count: one kv head per CTA
+    (2, 8, 1, 256, [1000, 257]),            # one kv head, 256-token pages
+    (3, 16, 4, 48, [100, 47, 400]),         # page 48: boxes of 16 rows
 ]
 
 
