@@ -558,6 +558,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     const int rem = blockIdx.x - s * units;
     const int b = rem / nkvg;
     const int kvg = rem - b * nkvg;
+    // Launched as a programmatic dependent: the CTA may be resident before the previous
+    // kernel on the stream has finished, so nothing that kernel may write is read before
+    // this wait; the combine that follows may be launched as soon as every CTA is here.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // the sequence length and the producer's page ids of the first tile are loaded together
     // (table entries from position s * chunk on; those past the sequence's end are read
     // within the table but not used)
@@ -1042,8 +1047,9 @@ dap_status launch_per_sequence(const DecodeArgs &a, SplitParams &p, cudaStream_t
                                                              partial_acc_bytes(a.B, a.Hq, a.D, a.num_splits))
                                  : nullptr;
     if (g_trace.split_begin) cudaEventRecord(g_trace.split_begin, stream);
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(mk, mv, p);
-    if (cudaGetLastError() != cudaSuccess) return DAP_ERR_CUDA;
+    if (launch_dependent_smem(kern, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, stream, mk, mv, p) !=
+        cudaSuccess)
+        return DAP_ERR_CUDA;
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
     if (a.num_splits > 1) {
         const dim3 cgrid((unsigned)((a.B * a.Hq + 7) / 8));

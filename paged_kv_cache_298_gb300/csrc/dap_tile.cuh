@@ -159,6 +159,8 @@ struct RowMerge {
 // CTA worked on, one warp per row; waits for the split grid (programmatic dependent launch).
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const SplitParams p) {
+    // the next decode call may be launched now (it waits for this grid before its reads)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -257,6 +259,23 @@ int prepare_kernel(K kern, int threads, int smem, int *cached_occ) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem) != cudaSuccess) return 0;
     *cached_occ = occ;
     return occ;
+}
+
+// A launch that may overlap the previous kernel on the stream (programmatic dependent
+// launch); the kernel orders its own reads with griddepcontrol.wait.
+template <class K, class... Args>
+cudaError_t launch_dependent_smem(K kern, dim3 grid, dim3 block, int smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 template <class K, class... Args>
