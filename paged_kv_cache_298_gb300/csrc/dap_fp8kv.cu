@@ -13,21 +13,18 @@
 // the [pages, Hkv, page_size] layout keeps contiguous.  Half the bytes of the bf16 cache
 // per key, so six stages keep as many bytes in flight as three bf16 stages.
 //
-// Arithmetic (tensor cores, mma.m16n8k16 in f16): an e4m3 code's sign and 7 magnitude bits
-// placed into f16 bits 15 and 13..7 give an f16 equal to the code's value times 2^-8, so
-// four codes become two f16 pairs with five integer operations, exactly, straight from the
-// swizzled tile.  QK: A = the codes of 16 keys, B = q in f16; the factor of each key, the
-// 2^8 and the softmax scale are applied to the fp32 scores (scale after the dot product, as
-// the AstrAI csrc log's numerics commit asks).  The dot product runs over the head dims in
-// the order the conversion yields (pairs of dims 4j, 4j+2 and 4j+1, 4j+3 of each lane's 32
-// contiguous bytes); q is loaded in the same order, converted to f16 after an exact
-// power-of-two shift that keeps its largest element below 2^15 (the shift goes back into
-// the scale).  PV: the V codes of 8 keys x 8 dims are moved into the A operand by
-// movmatrix (transposing them), the dims in the same permuted order, which the epilogue
-// undoes; the probabilities times each key's V factor form the f16 B operand, measured in
-// a per-warp power-of-two unit (above the largest factor seen so far) so they stay within
-// [0, 1); the accumulator is rescaled exactly when the unit grows and multiplied back at
-// the end.
+// Arithmetic (tensor cores, mma.m16n8k16 in f16): every e4m3 value is an f16 value, so the
+// hardware conversion (two e4m3 codes -> one f16 pair) turns codes into operands exactly,
+// straight from the swizzled tile.  QK: A = the codes of 16 keys, B = q in f16; the factor
+// of each key and the softmax scale are applied to the fp32 scores (scale after the dot
+// product, as the AstrAI csrc log's numerics commit asks); q is converted to f16 after an
+// exact power-of-two shift that keeps its largest element below 2^15 (the shift goes back
+// into the scale).  PV: the A operand wants pairs of keys of one dim, so each lane reads
+// 16 dims of four key rows and byte-interleaves two keys' codes before the conversion (dims
+// 16g+2m, 16g+2m+1 in rows g, g+8 of step m); the probabilities times each key's V factor
+// form the f16 B operand, measured in a per-warp power-of-two unit (above the largest
+// factor seen so far) so they stay within [0, 1); the accumulator is rescaled exactly when
+// the unit grows and multiplied back at the end.
 #include "dap_tile.cuh"
 
 namespace dap {
@@ -35,16 +32,18 @@ namespace f8kv {
 
 constexpr int kD = 128;
 
-// Four e4m3 codes [c0 c1 c2 c3] (low byte first) -> two f16 pairs (c0, c2) and (c1, c3),
-// each the code's value times 2^-8, exactly: a code's sign goes to the f16 sign bit and its
-// 7 magnitude bits (4 exponent, 3 mantissa) to f16 bits 13..7, so the f16 exponent equals
-// the e4m3 one (bias 15 against 7) and subnormals map to subnormals.  (The NaN codes 0x7F /
-// 0xFF read as +-480 * 2^-8; the cache writers never produce them.)
-__device__ __forceinline__ uint32_t e4m3_pair02(uint32_t w) {
-    return ((w << 8) & 0x80008000u) | ((w << 7) & 0x3F803F80u);
+// Four e4m3 codes [c0 c1 c2 c3] (low byte first) -> the f16 pairs (c0, c1) and (c2, c3),
+// exactly (the NaN codes 0x7F / 0xFF become f16 NaNs; the cache writers never produce them)
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
-__device__ __forceinline__ uint32_t e4m3_pair13(uint32_t w) {
-    return (w & 0x80008000u) | ((w >> 1) & 0x3F803F80u);
+
+// word i (0..3) of a 16-byte vector
+__device__ __forceinline__ uint32_t u4_word(const uint4 &v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
 // 2^(E - 127) for a biased exponent E in 1..254 (exact)
@@ -90,15 +89,14 @@ struct Cfg {
 template <class C>
 struct Consumer {
     static constexpr int D = C::D, G = C::G, HG = C::HG, KS = D / 16;
-    // The dot product over dims runs in the order the code conversion yields: at step m the
-    // k indices 2t, 2t+1 are dims 32t+4m+0, +2 and 2t+8, 2t+9 are dims 32t+4m+1, +3.
-    uint32_t qb[HG][KS][2];  // q (f16) B fragments of head g of each kv head, in that order
-    float acc[HG][KS][4];    // O^T: dims dlo(m,g), dlo+1 x heads 2t, 2t+1, in units of 2^(vE-127-8)
+    uint32_t qb[HG][KS][2];  // q (f16) B fragments of head g of each kv head: dims 32t+4m+0, 1 | +2, 3
+    float acc[HG][KS][4];    // O^T: dims 16g+2m, +1 x heads 2t, 2t+1, in units of 2^(vE-127)
     float m_run[HG][2], l_run[HG][2];
-    float qscale[HG];        // scale * log2(e) * 2^qshift * 2^8 (the 2^-8 of the K conversion)
+    float qscale[HG];        // scale * log2(e) * 2^qshift
     int vE[HG];              // biased exponent of the V-factor unit (0 = none yet)
     int warp, lane, g, t, key0;
     int line0, line1;        // 128-byte line of keys g, g+8 of head 0 inside a code tile
+    int vline0, vline2;      // lines of keys 2t and 2t+8 of head 0 (keys 2t+1, 2t+9: the next lines)
     int f0, f1;              // byte offsets of the factors of keys g, g+8 of head 0 in a factor block
     int hline, hfac;         // per-head strides of the two (R lines, 2R bytes)
 
@@ -113,6 +111,10 @@ struct Consumer {
         const int r0 = key0 + g, r1 = r0 + 8;
         line0 = (r0 >> rb) * (HG * R) + (r0 & (R - 1));
         line1 = (r1 >> rb) * (HG * R) + (r1 & (R - 1));
+        // an even row and the next one share a box (boxes are multiples of 8 rows)
+        const int r2 = key0 + 2 * t, r3 = r2 + 8;
+        vline0 = (r2 >> rb) * (HG * R) + (r2 & (R - 1));
+        vline2 = (r3 >> rb) * (HG * R) + (r3 & (R - 1));
         f0 = (r0 >> rb) * C::FSLOT + (r0 & (R - 1)) * 2;
         f1 = (r1 >> rb) * C::FSLOT + (r1 & (R - 1)) * 2;
         hline = R;
@@ -162,10 +164,10 @@ struct Consumer {
 #pragma unroll
         for (int m = 0; m < KS; ++m) {
             const float2 lo = bf16x2_to_float2(w[2 * m]), hi = bf16x2_to_float2(w[2 * m + 1]);
-            qb[h][m][0] = pack_f16x2(lo.x * sh, hi.x * sh);  // dims 4m+0, 4m+2 (of 32t..)
-            qb[h][m][1] = pack_f16x2(lo.y * sh, hi.y * sh);  // dims 4m+1, 4m+3
+            qb[h][m][0] = pack_f16x2(lo.x * sh, lo.y * sh);  // dims 4m+0, 4m+1 (of 32t..)
+            qb[h][m][1] = pack_f16x2(hi.x * sh, hi.y * sh);  // dims 4m+2, 4m+3
         }
-        qscale[h] = qs * pow2_biased(127 + e + 8);
+        qscale[h] = qs * pow2_biased(127 + e);
     }
 
     // 32 code bytes of a 128-byte line for this lane (dims 32t .. 32t+31), 128-byte swizzled
@@ -189,10 +191,15 @@ struct Consumer {
             const float kfac1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::KS_OFF + o1));
             const float vfac0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::VS_OFF + o0));
             const float vfac1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::VS_OFF + o1));
-            uint32_t w0[8], w1[8];
-            line_words(sV, l0, w0);
-            line_words(sV, l1, w1);
-            // S^T = K . Q^T (keys g, g+8 x heads 2t, 2t+1), K in units of 2^-8
+            // V: dims 16g .. 16g+15 of keys 2t, 2t+1, 2t+8, 2t+9 (128-byte swizzle: line & 7 =
+            // key & 7, the boxes being multiples of 8 rows)
+            uint4 vw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int ln = (j < 2 ? vline0 : vline2) + (j & 1) + h * hline;
+                vw[j] = lds128(sV + ln * 128 + ((g ^ (ln & 7)) << 4));
+            }
+            // S^T = K . Q^T (keys g, g+8 x heads 2t, 2t+1)
             float c[4] = {0.f, 0.f, 0.f, 0.f};
             {
                 uint32_t k0[8], k1[8];
@@ -200,8 +207,9 @@ struct Consumer {
                 line_words(sK, l1, k1);
 #pragma unroll
                 for (int m = 0; m < KS; ++m) {
-                    const uint32_t a[4] = {e4m3_pair02(k0[m]), e4m3_pair02(k1[m]), e4m3_pair13(k0[m]),
-                                           e4m3_pair13(k1[m])};
+                    uint32_t a[4];
+                    e4m3x4_to_f16(k0[m], a[0], a[2]);
+                    e4m3x4_to_f16(k1[m], a[1], a[3]);
                     mma_f16_16816(c, a, qb[h][m][0], qb[h][m][1]);
                 }
             }
@@ -258,15 +266,20 @@ struct Consumer {
             // O^T += V^T . P'^T; rows past the end read as code 0 so 0 * V stays 0
             if (nv < 16) {
 #pragma unroll
-                for (int m = 0; m < KS; ++m) {
-                    w0[m] = v0 ? w0[m] : 0u;
-                    w1[m] = v1 ? w1[m] : 0u;
-                }
+                for (int j = 0; j < 4; ++j)
+                    if (2 * t + (j & 1) + 8 * (j >> 1) >= nv) vw[j] = make_uint4(0u, 0u, 0u, 0u);
             }
+            // A rows g, g+8 = dims 16g+2m, 16g+2m+1; k = keys: byte-interleave keys 2t, 2t+1
+            // (and 2t+8, 2t+9) so that one conversion yields a key pair of one dim
 #pragma unroll
             for (int m = 0; m < KS; ++m) {
-                const uint32_t a[4] = {movmatrix_trans(e4m3_pair02(w0[m])), movmatrix_trans(e4m3_pair13(w0[m])),
-                                       movmatrix_trans(e4m3_pair02(w1[m])), movmatrix_trans(e4m3_pair13(w1[m]))};
+                const int wi = m >> 1;
+                const uint32_t sel = (m & 1) ? 0x7362u : 0x5140u;
+                const uint32_t ab = __byte_perm(u4_word(vw[0], wi), u4_word(vw[1], wi), sel);
+                const uint32_t cd = __byte_perm(u4_word(vw[2], wi), u4_word(vw[3], wi), sel);
+                uint32_t a[4];
+                e4m3x4_to_f16(ab, a[0], a[1]);
+                e4m3x4_to_f16(cd, a[2], a[3]);
                 mma_f16_16816(acc[h][m], a, b0, b1);
             }
         }
@@ -299,14 +312,14 @@ struct Consumer {
         const int tid = warp * 32 + lane;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            if ((g >> 2) == half) {  // this lane's dims 32(g/2) + 4m + 2(g&1) (+1) lie in this half
+            if ((g >> 2) == half) {  // this lane's dims 16g .. 16g+15 lie in this half
 #pragma unroll
                 for (int h = 0; h < HG; ++h) {
-                    // back from units of 2^(vE - 127) (V factors) and 2^-8 (V codes)
-                    const float unit = vE[h] > 0 ? pow2_biased(min(vE[h] + 8, 254)) : 0.f;
+                    // back from units of 2^(vE - 127) (V factors); dims 16g+2m, +1
+                    const float unit = vE[h] > 0 ? pow2_biased(vE[h]) : 0.f;
 #pragma unroll
                     for (int m = 0; m < KS; ++m) {
-                        const int dlo = 32 * (g >> 1) + 4 * m + 2 * (g & 1) - half * DH;
+                        const int dlo = 16 * g + 2 * m - half * DH;
 #pragma unroll
                         for (int j = 0; j < 2; ++j) {
                             if (2 * t + j < G) {
