@@ -63,15 +63,16 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)
 }
 
 // HG kv heads per CTA (2 when Hkv is even): one TMA box carries both heads' rows of a page
-// run, the shared tile is head-major [box][head][row][128 B], and every consumer warp runs
-// the heads as independent streams over the same 16 keys.
-template <int G_, int HG_>
+// run and the shared tile is head-major [box][head][row][128 B].  Consumer warp w serves
+// the 16-key slice w % 4 of every tile for HPW kv heads (the heads as independent streams),
+// so a CTA runs 4 * HG / HPW consumer warps.
+template <int G_, int HG_, int HPW_ = 1>
 struct Cfg {
-    static constexpr int D = kD, G = G_, HG = HG_, NWC = 4, BT = 64;
+    static constexpr int D = kD, G = G_, HG = HG_, HPW = HPW_, KW = 4, NWC = KW * (HG / HPW), BT = 64;
     static constexpr int NS = HG == 2 ? 3 : 4, MINB = HG == 2 ? 2 : 3;
     static constexpr bool SWZ = true;
     static constexpr int THREADS = (NWC + 1) * 32;
-    static constexpr int KPW = BT / NWC;                  // 16 keys per consumer warp
+    static constexpr int KPW = BT / KW;                   // 16 keys per consumer warp
     static constexpr int CODE_BYTES = BT * HG * D;        // one tile of K (or V) codes
     // The tile's K factors, then its V factors: box j (HG x R factors, R <= 64) lands in its
     // own slot, a tensor copy's shared destination being 128-byte aligned.
@@ -79,25 +80,25 @@ struct Cfg {
     static constexpr int KS_OFF = 2 * CODE_BYTES;
     static constexpr int VS_OFF = KS_OFF + (BT / 8) * FSLOT;   // at most BT / 8 boxes (R >= 8)
     static constexpr int STAGE_BYTES = (VS_OFF + (BT / 8) * FSLOT + 1023) & ~1023;
-    static constexpr int MRG_BYTES = NWC * HG * G * (D / 2 + 2) * 4;  // aliases stage 0 after the last tile
+    static constexpr int MRG_BYTES = KW * HG * G * (D / 2 + 2) * 4;  // aliases stage 0 after the last tile
     static constexpr int MISC_OFF = NS * STAGE_BYTES;
     static constexpr int BAR_OFF = MISC_OFF + 16;
     static constexpr int SMEM = BAR_OFF + 2 * NS * 8 + 1024;
-    static_assert(KPW == 16 && MRG_BYTES <= STAGE_BYTES && FSLOT >= 2 * HG * BT, "fp8 tiling");
+    static_assert(KPW == 16 && HG % HPW == 0 && MRG_BYTES <= STAGE_BYTES && FSLOT >= 2 * HG * BT, "fp8 tiling");
 };
 
 template <class C>
 struct Consumer {
-    static constexpr int D = C::D, G = C::G, HG = C::HG, KS = D / 16;
-    uint32_t qb[HG][KS][2];  // q (f16) B fragments of head g of each kv head: dims 32t+4m+0, 1 | +2, 3
-    float acc[HG][KS][4];    // O^T: dims 16g+2m, +1 x heads 2t, 2t+1, in units of 2^(vE-127)
-    float m_run[HG][2], l_run[HG][2];
-    float qscale[HG];        // scale * log2(e) * 2^qshift
-    int vE[HG];              // biased exponent of the V-factor unit (0 = none yet)
-    int warp, lane, g, t, key0;
-    int line0, line1;        // 128-byte line of keys g, g+8 of head 0 inside a code tile
-    int vline0, vline2;      // lines of keys 2t and 2t+8 of head 0 (keys 2t+1, 2t+9: the next lines)
-    int f0, f1;              // byte offsets of the factors of keys g, g+8 of head 0 in a factor block
+    static constexpr int D = C::D, G = C::G, HG = C::HG, HW = C::HPW, KS = D / 16;
+    uint32_t qb[HW][KS][2];  // q (f16) B fragments of head g of each kv head: dims 32t+4m+0, 1 | +2, 3
+    float acc[HW][KS][4];    // O^T: dims 16g+2m, +1 x heads 2t, 2t+1, in units of 2^(vE-127)
+    float m_run[HW][2], l_run[HW][2];
+    float qscale[HW];        // scale * log2(e) * 2^qshift
+    int vE[HW];              // biased exponent of the V-factor unit (0 = none yet)
+    int warp, lane, g, t, kw, hw0, key0;  // key slice kw, first kv head hw0 (within the CTA's HG)
+    int line0, line1;        // 128-byte line of keys g, g+8 of head hw0 inside a code tile
+    int vline0, vline2;      // lines of keys 2t and 2t+8 of head hw0 (keys 2t+1, 2t+9: the next lines)
+    int f0, f1;              // byte offsets of the factors of keys g, g+8 of head hw0 in a factor block
     int hline, hfac;         // per-head strides of the two (R lines, 2R bytes)
 
     // R: rows per TMA box (a power of two, 8..64)
@@ -106,7 +107,9 @@ struct Consumer {
         lane = l;
         g = l >> 2;
         t = l & 3;
-        key0 = w * C::KPW;
+        kw = w % C::KW;
+        hw0 = (w / C::KW) * HW;
+        key0 = kw * C::KPW;
         const int rb = __ffs(R) - 1;
         const int r0 = key0 + g, r1 = r0 + 8;
         line0 = (r0 >> rb) * (HG * R) + (r0 & (R - 1));
@@ -119,11 +122,17 @@ struct Consumer {
         f1 = (r1 >> rb) * C::FSLOT + (r1 & (R - 1)) * 2;
         hline = R;
         hfac = 2 * R;
+        line0 += hw0 * hline;
+        line1 += hw0 * hline;
+        vline0 += hw0 * hline;
+        vline2 += hw0 * hline;
+        f0 += hw0 * hfac;
+        f1 += hw0 * hfac;
     }
 
     __device__ __forceinline__ void reset() {
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
+        for (int h = 0; h < HW; ++h) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 m_run[h][j] = -INFINITY;
@@ -137,7 +146,8 @@ struct Consumer {
         }
     }
 
-    // q of the G query heads of kv head h (head g at base + g * hstride); qs = scale * log2(e).
+    // q of the G query heads of the warp's kv head h (head g at base + g * hstride);
+    // qs = scale * log2(e).
     __device__ __forceinline__ void load_q(int h, const __nv_bfloat16 *base, long long hstride, float qs) {
         uint32_t w[16];
 #pragma unroll
@@ -183,7 +193,7 @@ struct Consumer {
         if (nv <= 0) return;
         const bool v0 = g < nv, v1 = g + 8 < nv;
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
+        for (int h = 0; h < HW; ++h) {
             const uint8_t *sK = stage, *sV = stage + C::CODE_BYTES;
             const int l0 = line0 + h * hline, l1 = line1 + h * hline;
             const int o0 = f0 + h * hfac, o1 = f1 + h * hfac;
@@ -285,16 +295,16 @@ struct Consumer {
         }
     }
 
-    // Merge the four warps per (kv head, query head) in two halves of D (the row merge of
-    // the bf16 path); emit(kv head in unit, query head, d, a0, a1, M, l) gets dims d, d+1 in
-    // natural order.
+    // Merge the four key slices per (kv head, query head) in two halves of D (the row merge
+    // of the bf16 path); emit(kv head in unit, query head, d, a0, a1, M, l) gets dims d, d+1
+    // in natural order.
     template <class Sync, class Emit>
     __device__ __forceinline__ bool finish(float *mrg, Sync sync, Emit emit) {
-        constexpr int NWC = C::NWC, DH = D / 2, NR = HG * G;  // rows per warp
-        float *macc = mrg;                 // [NWC][HG * G][D/2]
-        float *mml = mrg + NWC * NR * DH;  // [NWC][HG * G][2]
+        constexpr int NWC = C::NWC, KW = C::KW, DH = D / 2, NR = HG * G;  // rows per key slice
+        float *macc = mrg;                // [KW][HG * G][D/2]
+        float *mml = mrg + KW * NR * DH;  // [KW][HG * G][2]
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
+        for (int h = 0; h < HW; ++h) {
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) {
                 l_run[h][0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[h][0], o);
@@ -304,8 +314,8 @@ struct Consumer {
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
                     if (2 * t + j < G) {
-                        mml[(warp * NR + h * G + 2 * t + j) * 2 + 0] = m_run[h][j];
-                        mml[(warp * NR + h * G + 2 * t + j) * 2 + 1] = l_run[h][j];
+                        mml[(kw * NR + (hw0 + h) * G + 2 * t + j) * 2 + 0] = m_run[h][j];
+                        mml[(kw * NR + (hw0 + h) * G + 2 * t + j) * 2 + 1] = l_run[h][j];
                     }
             }
         }
@@ -314,7 +324,7 @@ struct Consumer {
         for (int half = 0; half < 2; ++half) {
             if ((g >> 2) == half) {  // this lane's dims 16g .. 16g+15 lie in this half
 #pragma unroll
-                for (int h = 0; h < HG; ++h) {
+                for (int h = 0; h < HW; ++h) {
                     // back from units of 2^(vE - 127) (V factors); dims 16g+2m, +1
                     const float unit = vE[h] > 0 ? pow2_biased(vE[h]) : 0.f;
 #pragma unroll
@@ -323,7 +333,7 @@ struct Consumer {
 #pragma unroll
                         for (int j = 0; j < 2; ++j) {
                             if (2 * t + j < G) {
-                                float *row = macc + (warp * NR + h * G + 2 * t + j) * DH;
+                                float *row = macc + (kw * NR + (hw0 + h) * G + 2 * t + j) * DH;
                                 row[dlo] = acc[h][m][j] * unit;
                                 row[dlo + 1] = acc[h][m][j + 2] * unit;
                             }
@@ -336,11 +346,11 @@ struct Consumer {
                 const int rr = e / DH, dd = e % DH;
                 float M = -INFINITY;
 #pragma unroll
-                for (int w = 0; w < NWC; ++w) M = fmaxf(M, mml[(w * NR + rr) * 2]);
+                for (int w = 0; w < KW; ++w) M = fmaxf(M, mml[(w * NR + rr) * 2]);
                 const float Mu = (M == -INFINITY) ? 0.f : M;
                 float a0 = 0.f, a1 = 0.f, lv = 0.f;
 #pragma unroll
-                for (int w = 0; w < NWC; ++w) {
+                for (int w = 0; w < KW; ++w) {
                     const float f = ex2(mml[(w * NR + rr) * 2] - Mu);
                     lv = fmaf(f, mml[(w * NR + rr) * 2 + 1], lv);
                     const float2 x = *reinterpret_cast<const float2 *>(macc + (w * NR + rr) * DH + dd);
@@ -455,8 +465,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     cs.init(warp, lane, R);
     cs.reset();
 #pragma unroll
-    for (int h = 0; h < HG; ++h)
-        cs.load_q(h, p.q + (long long)b * p.q_sb + (long long)(kvg * HG + h) * G * p.q_sh, p.q_sh, p.qscale);
+    for (int h = 0; h < C::HPW; ++h)
+        cs.load_q(h, p.q + (long long)b * p.q_sb + (long long)(kvg * HG + cs.hw0 + h) * G * p.q_sh, p.q_sh,
+                  p.qscale);
     int consumed = 0;
     for (int i = 0; i < ntiles; ++i) {
         const int st = i % NS;
