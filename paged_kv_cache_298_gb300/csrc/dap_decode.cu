@@ -1052,9 +1052,7 @@ dap_status launch_per_sequence(const DecodeArgs &a, SplitParams &p, cudaStream_t
         return DAP_ERR_CUDA;
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
     if (a.num_splits > 1) {
-        const dim3 cgrid((unsigned)((a.B * a.Hq + 7) / 8));
-        const cudaError_t e = launch_dependent(combine_kernel<C::D>, cgrid, dim3(256), stream, p);
-        if (e != cudaSuccess) return DAP_ERR_CUDA;
+        if (launch_combine<C::D>(p, a.B, a.Hq, a.num_splits, stream) != cudaSuccess) return DAP_ERR_CUDA;
     }
     if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);
     return DAP_OK;

@@ -7,11 +7,12 @@
 // nvfp4-megamoe-kernel native_swa_decode.py, applied per kv head), likewise the value.
 //
 // Schedule and data movement: the per-sequence split schedule of dap_decode.cu (one CTA
-// per (sequence, kv head, split), split partials merged by the shared combine kernel).
-// Per 64-key tile the producer warp issues four TMA boxes per page run: the K and V code
-// rows (128 bytes each, 128-byte swizzled) and the two factor runs of the kv head, which
-// the [pages, Hkv, page_size] layout keeps contiguous.  Half the bytes of the bf16 cache
-// per key, so six stages keep as many bytes in flight as three bf16 stages.
+// per (sequence, pair of kv heads, split), split partials merged by the shared combine
+// kernel).  Per 64-key tile the producer warp issues four TMA boxes per page run: the K and
+// V code rows of both kv heads (128 bytes per row and head, 128-byte swizzled) and the two
+// factor runs of the head pair, which the [pages, Hkv, page_size] layout keeps contiguous.
+// A stage carries as many bytes as a bf16 stage of one kv head, so three stages at two
+// CTAs per SM keep the same bytes in flight.
 //
 // Arithmetic (tensor cores, mma.m16n8k16 in f16): every e4m3 value is an f16 value, so the
 // hardware conversion (two e4m3 codes -> one f16 pair) turns codes into operands exactly,
@@ -557,8 +558,7 @@ dap_status launch_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
     if (cudaGetLastError() != cudaSuccess) return DAP_ERR_CUDA;
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
     if (a.num_splits > 1) {
-        const dim3 cgrid((unsigned)(((long long)a.B * a.Hq + 7) / 8));
-        if (launch_dependent(combine_kernel<kD>, cgrid, dim3(256), stream, p) != cudaSuccess) return DAP_ERR_CUDA;
+        if (launch_combine<kD>(p, a.B, a.Hq, a.num_splits, stream) != cudaSuccess) return DAP_ERR_CUDA;
     }
     if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);
     return DAP_OK;

@@ -79,7 +79,7 @@ def test_paged_parity(shape):
     B, Hq, Hkv, D, ps, lens = shape
     case = inputs.make_paged_case(B, Hq, Hkv, D, ps, lens, 1000 + sum(lens)).to("cuda")
     ref = oracle_paged(case)
-    for S in [0, 1, 2, 5]:
+    for S in [0, 1, 2, 5, 20]:    # 20: more than 16 splits, the CTA-per-row combine
         assert_close(gpu_paged(case, S), ref, f"S={S}")
     assert binding.get_device_errors() == 0
 
