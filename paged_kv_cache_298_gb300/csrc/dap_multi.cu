@@ -323,6 +323,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     const int rem = blockIdx.x - s * units;
     const int w = rem / p.Hkv;
     const int kvh = rem - w * p.Hkv;
+    // Launched as a programmatic dependent of the previous kernel on the stream: nothing
+    // global is read before the wait (that kernel may still write the inputs); the combine
+    // of this call may launch at once (it waits for this grid before its reads).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // Every load the schedule needs before the first TMA is issued at once: the work-map
     // entry, then its sequence's q range and length together with the producer's page ids
     // of the first tile (read from position s * chunk on; entries past the sequence's end
@@ -449,52 +454,98 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
               });
 }
 
-// Merge the split partials of every (token, head) row, one warp per row.  The row's
-// sequence is found by binary search of qo_indptr; the split count follows from the row's
-// tile exactly as in multi_kernel.
-template <int D>
+// Merge of the split partials of every (token, head) row whose tile took more than one
+// split: one warp per (token, HPW consecutive heads), which share the token's sequence and
+// so its split count.  The sequence of token r is the last b with qo_indptr[b] <= r, found
+// by a 32-way search (one load per lane and step: two dependent loads for up to 1024
+// sequences, the last step also yielding qo_indptr[b] and qo_indptr[b + 1]).  The
+// partials are merged online in split order, SB splits per batch of loads: M = the running
+// max of the m_s, the sums rescaled by 2^(M_old - M_new) when it grows (AstrAI csrc log,
+// split-KV commit: the combine kernel; numerics commit: guarded division).  Waits for the
+// attention grid (programmatic dependent launch).
+template <int D, int HPW, int SB>
 __global__ void __launch_bounds__(256) combine_multi_kernel(const SplitParams p, int qt) {
+    // the next kernel on the stream may be launched now (it waits for this grid before its
+    // reads)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    constexpr int DPV = D / 32;
     const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (gw >= p.total_q * p.Hq) return;
-    const int r = gw / p.Hq, hq = gw - r * p.Hq;
-    int lo = r, q0 = r, q1 = r + 1;  // no work map: row r is sequence r's one token
+    const int ngroups = p.Hq / HPW;
+    if (gw >= p.total_q * ngroups) return;
+    const int r = gw / ngroups, hq0 = (gw - r * ngroups) * HPW;
+    int b = r, q0 = r, q1 = r + 1;  // no work map: row r is sequence r's one token
     if (p.qo_indptr) {
-        int hi = p.B;  // qo_indptr[lo] <= r < qo_indptr[hi] for a well-formed map
-        lo = 0;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (p.qo_indptr[mid] <= r) lo = mid;
-            else hi = mid;
+        int lo = 0, hi = p.B;  // qo_indptr[lo] <= r < qo_indptr[hi] for a well-formed map
+        while (hi - lo > 31) {
+            const int step = (hi - lo + 31) >> 5;
+            const int x = lo + lane * step;
+            const bool le = x < hi && p.qo_indptr[x] <= r;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, le);
+            const int j = bal ? 31 - __clz(bal) : 0;
+            lo += j * step;
+            hi = min(lo + step, hi);
         }
-        q0 = p.qo_indptr[lo];
-        q1 = p.qo_indptr[lo + 1];
+        const int x = lo + lane;  // entries lo .. hi (hi - lo <= 31, hi <= B)
+        const int v = x <= hi ? p.qo_indptr[x] : 0x7FFFFFFF;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, x < hi && v <= r);
+        const int j = bal ? 31 - __clz(bal) : 0;
+        q0 = __shfl_sync(0xFFFFFFFFu, v, j);
+        q1 = __shfl_sync(0xFFFFFFFFu, v, j + 1);
+        b = lo + j;
     }
     MultiTile tl;
-    if (!multi_tile(p, lo, (r - q0) / qt, q0, q1, p.seq_lens[lo], qt, false, &tl)) return;
+    if (!multi_tile(p, b, (r - q0) / qt, q0, q1, p.seq_lens[b], qt, false, &tl)) return;
     const int nsplit = max(1, (tl.kv_end + p.chunk - 1) / p.chunk);
     if (nsplit == 1) return;
-    const long long row0 = (long long)r * p.num_splits * p.Hq + hq;
-    float M = -INFINITY;
-    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, p.ml_part[(row0 + (long long)s * p.Hq) * 2]);
+    const long long rbase = (long long)r * p.num_splits * p.Hq + hq0;  // row (r, s, hq) = (r S + s) Hq + hq
+    float acc[HPW][DPV], lsum[HPW], Mrun[HPW];
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-    RowMerge<D> m;
-    m.begin(M);
-    for (int s0 = 0; s0 < nsplit; s0 += 8) {
-        const float *o[8];
-        float2 ml[8];
-        const int n = min(8, nsplit - s0);
+    for (int h = 0; h < HPW; ++h) {
+        lsum[h] = 0.f;
+        Mrun[h] = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const long long row = row0 + (long long)min(s0 + k, nsplit - 1) * p.Hq;
-            o[k] = p.o_part + row * D;
-            ml[k] = *reinterpret_cast<const float2 *>(p.ml_part + row * 2);
-        }
-        m.add_batch(o, ml, n, lane);
+        for (int j = 0; j < DPV; ++j) acc[h][j] = 0.f;
     }
-    m.store(p.out + (long long)r * p.o_sb + (long long)hq * p.o_sh, lane);
+    for (int s0 = 0; s0 < nsplit; s0 += SB) {
+        const int n = min(SB, nsplit - s0);
+        float x[HPW][SB][DPV];
+        float2 ml[HPW][SB];
+#pragma unroll
+        for (int h = 0; h < HPW; ++h)
+#pragma unroll
+            for (int k = 0; k < SB; ++k)
+                if (k < n) {
+                    const long long row = rbase + (long long)(s0 + k) * p.Hq + h;
+                    load_row_part<DPV>(p.o_part + row * D + lane * DPV, x[h][k]);
+                    ml[h][k] = *reinterpret_cast<const float2 *>(p.ml_part + row * 2);
+                }
+#pragma unroll
+        for (int h = 0; h < HPW; ++h) {
+            float Mn = Mrun[h];
+#pragma unroll
+            for (int k = 0; k < SB; ++k)
+                if (k < n) Mn = fmaxf(Mn, ml[h][k].x);
+            const float Mu = (Mn == -INFINITY) ? 0.f : Mn;
+            const float sc = ex2(Mrun[h] - Mu);  // 0 while nothing was added
+            lsum[h] *= sc;
+#pragma unroll
+            for (int j = 0; j < DPV; ++j) acc[h][j] *= sc;
+#pragma unroll
+            for (int k = 0; k < SB; ++k)
+                if (k < n) {
+                    const float f = ex2(ml[h][k].x - Mu);
+                    lsum[h] = fmaf(f, ml[h][k].y, lsum[h]);
+#pragma unroll
+                    for (int j = 0; j < DPV; ++j) acc[h][j] = fmaf(f, x[h][k][j], acc[h][j]);
+                }
+            Mrun[h] = Mn;
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < HPW; ++h)
+        store_row_part<DPV>(p.out + (long long)r * p.o_sb + (long long)(hq0 + h) * p.o_sh + lane * DPV, acc[h], lsum[h]);
 }
 
 namespace {
@@ -533,13 +584,20 @@ dap_status launch_multi(const DecodeArgs &a, SplitParams &p, cudaStream_t stream
                                                              partial_acc_bytes(a.total_q, a.Hq, a.D, a.num_splits))
                                  : nullptr;
     if (g_trace.split_begin) cudaEventRecord(g_trace.split_begin, stream);
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(mk, mv, mm, p);
-    if (cudaGetLastError() != cudaSuccess) return DAP_ERR_CUDA;
+    if (launch_dependent_smem(kern, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, stream, mk, mv, mm, p) !=
+        cudaSuccess)
+        return DAP_ERR_CUDA;
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
     if (a.num_splits > 1) {
-        const dim3 cgrid((unsigned)(((long long)a.total_q * a.Hq + 7) / 8));
-        if (launch_dependent(combine_multi_kernel<D>, cgrid, dim3(256), stream, p, (int)C::QT) != cudaSuccess)
-            return DAP_ERR_CUDA;
+        // one warp per (token, HPW heads), SB splits per batch of loads
+        constexpr int HPW_MAX = 4, SB = 1;
+        const int hpw = a.Hq % HPW_MAX == 0 ? HPW_MAX : a.Hq % 2 == 0 ? 2 : 1;
+        const dim3 cgrid((unsigned)(((long long)a.total_q * (a.Hq / hpw) + 7) / 8));
+        const cudaError_t e =
+            hpw == HPW_MAX ? launch_dependent(combine_multi_kernel<D, HPW_MAX, SB>, cgrid, dim3(256), stream, p, (int)C::QT)
+            : hpw == 2     ? launch_dependent(combine_multi_kernel<D, 2, SB>, cgrid, dim3(256), stream, p, (int)C::QT)
+                           : launch_dependent(combine_multi_kernel<D, 1, SB>, cgrid, dim3(256), stream, p, (int)C::QT);
+        if (e != cudaSuccess) return DAP_ERR_CUDA;
     }
     if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);
     return DAP_OK;
