@@ -382,6 +382,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     const int rem = blockIdx.x - s * units;
     const int b = rem / nkvg;
     const int kvg = rem - b * nkvg;
+    // Launched as a programmatic dependent of the previous kernel on the stream: nothing
+    // global is read before the wait (that kernel may still write the inputs); the combine
+    // of this call may launch at once (it waits for this grid before its reads).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int L = p.seq_lens[b];
     const int R = p.box_rows;
     int pg_first = 0;  // loaded with the length (entries past the end are read, not used)
@@ -554,8 +559,9 @@ dap_status launch_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
                                                              partial_acc_bytes(a.B, a.Hq, a.D, a.num_splits))
                                  : nullptr;
     if (g_trace.split_begin) cudaEventRecord(g_trace.split_begin, stream);
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM, stream>>>(mk, mv, mks, mvs, p);
-    if (cudaGetLastError() != cudaSuccess) return DAP_ERR_CUDA;
+    if (launch_dependent_smem(kern, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, stream, mk, mv, mks, mvs, p) !=
+        cudaSuccess)
+        return DAP_ERR_CUDA;
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
     if (a.num_splits > 1) {
         if (launch_combine<kD>(p, a.B, a.Hq, a.num_splits, stream) != cudaSuccess) return DAP_ERR_CUDA;
