@@ -80,6 +80,23 @@ def test_parity_across_groups_and_dims(B, Hq, Hkv, D, ps, lens, qlens):
     assert binding.get_device_errors() == 0
 
 
+@pytest.mark.parametrize("B", [70, 1100])
+def test_many_sequences_with_empty_ones(B):
+    """More sequences than one 32-wide step of the combine's qo_indptr search covers (70:
+    two steps; 1100: three), with runs of sequences that have no new token (repeated
+    offsets), checked against the oracle on every token."""
+    rng = np.random.default_rng(4700 + B)
+    qlens = rng.integers(0, 4, size=B)
+    qlens[rng.integers(0, B, size=B // 4)] = 0
+    qlens[0] = qlens[-1] = 2
+    lens = rng.integers(4, 90, size=B)
+    case = inputs.make_multi_case(B, 8, 2, 64, 16, lens.tolist(), qlens.tolist(), 4700 + B).to("cuda")
+    ref = oracle_multi(case)
+    for S in [2, 3]:
+        assert_close(gpu_multi(case, S), ref, f"B={B} S={S}")
+    assert binding.get_device_errors() == 0
+
+
 def test_one_new_token_each_matches_single_token_decode():
     case = inputs.make_multi_case(5, 32, 8, 128, 16, [1, 70, 129, 640, 2000], [1] * 5, 4200).to("cuda")
     kv = case.kv
