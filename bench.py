@@ -334,31 +334,22 @@ def run_ours(args):
     dt_ = [s.block_table for s in sets]
     dl = [s.seq_lens for s in sets]
 
-    def e2e_step(i):
+    def h2d(i):
         j = i % copies
         dq[j].copy_(hq, non_blocking=True)
         dt_[j].copy_(ht, non_blocking=True)
         dl[j].copy_(hl, non_blocking=True)
+
+    def call(i):
+        j = i % copies
         c = sets[j]
         b2.decode_attn_paged(dq[j], c.k_cache, c.v_cache, dt_[j], dl[j], max_kv_len=maxlen, scale=c.scale,
                              num_splits=S, workspace=ws[j], out=outs[j])
-        ho.copy_(outs[j], non_blocking=True)
 
-    for i in range(args.warmup):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for i in range(K):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    e2e_ms = e0.elapsed_time(e1) / K
+    def d2h(i):
+        ho.copy_(outs[i % copies], non_blocking=True)
+
+    e2e_ms, e2e_sched = time_e2e(h2d, call, d2h, K, args.warmup, copies, stream, world)
 
     nbytes = algorithmic_bytes(case)
     (value, ms), (e2e_value, e2e_ms) = job_throughput([ms, e2e_ms], nbytes, world, dev)
@@ -375,7 +366,7 @@ def run_ours(args):
                      "frac": round(achieved / hbm_peak, 4), "split_kernel_ms": round(split_ms, 5),
                      "combine_ms": round(combine_ms, 5), "algorithmic_bytes_per_launch": nbytes,
                      "traffic": recorded_traffic("split_kernel", workload_key(args))},
-        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+        "e2e": {"schedule": e2e_sched, "value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": hq.numel() * 2 + ht.numel() * 4 + hl.numel() * 4,
                 "d2h_bytes_per_step": ho.numel() * 2},
         "gpu_launches": K * (2 if S != 1 else 1),
@@ -481,28 +472,21 @@ def run_fp8(args):
     hln = case.lens.cpu().pin_memory()
     ho = torch.empty(case.q.shape, dtype=torch.bfloat16).pin_memory()
 
-    def e2e_step(i):
-        j = i % copies
-        q, kv, inv, idx, ln = sets[j]
+    def h2d(i):
+        q, kv, inv, idx, ln = sets[i % copies]
         q.copy_(hq, non_blocking=True)
         idx.copy_(hidx, non_blocking=True)
         ln.copy_(hln, non_blocking=True)
-        binding.decode_attn_paged_fp8(q, kv, inv, idx, ln, scale=case.scale, out=outs[j])
-        ho.copy_(outs[j], non_blocking=True)
 
-    for i in range(args.warmup):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for i in range(K):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K
+    def call(i):
+        j = i % copies
+        q, kv, inv, idx, ln = sets[j]
+        binding.decode_attn_paged_fp8(q, kv, inv, idx, ln, scale=case.scale, out=outs[j])
+
+    def d2h(i):
+        ho.copy_(outs[i % copies], non_blocking=True)
+
+    e2e_ms, e2e_sched = time_e2e(h2d, call, d2h, K, args.warmup, copies, stream, world)
     if world > 1:
         dist.barrier()
     (value, ms), (e2e_value, e2e_ms) = job_throughput([ms, e2e_ms], nbytes, world, dev)
@@ -521,7 +505,7 @@ def run_fp8(args):
                      "algorithmic_bytes_per_launch": nbytes,
                      "tflops": round(flops / (kern_ms * 1e-3) / 1e12, 2),
                      "traffic": recorded_traffic("swa_kernel", "fp8")},
-        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+        "e2e": {"schedule": e2e_sched, "value": round(e2e_value, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": hq.numel() * 2 + hidx.numel() * 8 + hln.numel() * 8,
                 "d2h_bytes_per_step": ho.numel() * 2},
         "gpu_launches": K, "device_errors": errs, "clocks": clk,
@@ -612,14 +596,90 @@ def run_append(args):
         "gpu_launches": 2 * 50 * max(1, K // 50), "device_errors": binding.get_device_errors()}), flush=True)
 
 
+# ---- end to end through host buffers ------------------------------------------------------
+
+def time_e2e(h2d, compute, d2h, K, W, copies, stream, world=1):
+    """Milliseconds per end-to-end step and the schedule that gave them.  Step i copies its
+    inputs in from pinned host memory (`h2d(i)`), runs the library call (`compute(i)`, on
+    `stream`) and copies its result back (`d2h(i)`); every step does all three inside the
+    timed region.  Two schedules are timed and the faster is reported, as a serving loop
+    would pick: "serial" (all three on `stream`, step after step: the fewest host calls,
+    best when a step is host-bound) and "pipelined" (the copies in on one stream, the
+    kernels on `stream`, the copies out on a third, so that step i + 1's inputs and step
+    i - 1's result travel while step i computes; step i's kernels wait for its inputs, the
+    device slot i % copies is refilled only after step i - copies has read it and its
+    output overwritten only after that step's result was copied out)."""
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def events(n):  # created (torch does so on first record) before the timed region
+        ev = [torch.cuda.Event(enable_timing=False) for _ in range(n)]
+        for e in ev:
+            e.record(stream)
+        return ev
+
+    def serial(n):
+        for i in range(n):
+            h2d(i)
+            compute(i)
+            d2h(i)
+
+    def pipelined(n, ready, done, read, start):
+        start.record(stream)
+        up.wait_event(start)
+        down.wait_event(start)
+        for i in range(n):
+            with torch.cuda.stream(up):
+                if i >= copies:
+                    up.wait_event(done[i - copies])
+                h2d(i)
+                ready[i].record(up)
+            stream.wait_event(ready[i])
+            if i >= copies:
+                stream.wait_event(read[i - copies])
+            compute(i)
+            done[i].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(done[i])
+                d2h(i)
+                read[i].record(down)
+        stream.wait_event(read[n - 1])
+
+    def timed(fn, *ev):
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn(K, *ev)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        return e0.elapsed_time(e1) / K
+
+    serial(W)
+    pipelined(W, events(W), events(W), events(W), events(1)[0])
+    res = {"serial": timed(serial),
+           "pipelined": timed(pipelined, events(K), events(K), events(K), events(1)[0])}
+    if world > 1:  # every rank reports the schedule rank 0 found faster
+        pick = torch.tensor([0 if res["serial"] <= res["pipelined"] else 1], dtype=torch.int32,
+                            device=torch.device("cuda", torch.cuda.current_device()))
+        dist.broadcast(pick, 0)
+        best = "serial" if int(pick.item()) == 0 else "pipelined"
+    else:
+        best = min(res, key=res.get)
+    return res[best], best
+
+
 # ---- shared single-GPU measurement of a decode step ------------------------------------------
 
-def measure_step(binding, step, e2e_step, K, W, stream):
+def measure_step(binding, step, e2e, K, W, stream, copies):
     """Times `step(i)` (inputs resident, rotated copies chosen by the caller): K untraced steps
     bracketed by CUDA events with the clocks sampled meanwhile; then the library's own launch
     events around its attention kernel and its combine over min(K, 50) steps (a separate loop:
-    an event between the two kernels stops their overlap); then `e2e_step(i)` (host copies
-    in and out inside) over K steps.  Returns a dict of per-step milliseconds and the clocks."""
+    an event between the two kernels stops their overlap); then the end-to-end step given as
+    `e2e` = (copies in, call, copy out) over K steps (`time_e2e`).  Returns a dict of
+    per-step milliseconds and the clocks."""
     for i in range(W):
         step(i)
     torch.cuda.synchronize()
@@ -651,16 +711,8 @@ def measure_step(binding, step, e2e_step, K, W, stream):
     kern_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     combine_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     errs = binding.get_device_errors(clear=True)
-    for i in range(W):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(K):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    return {"ms": ms, "kern_ms": kern_ms, "combine_ms": combine_ms, "e2e_ms": e0.elapsed_time(e1) / K,
+    e2e_ms, e2e_sched = time_e2e(*e2e, K, W, copies, stream)
+    return {"ms": ms, "kern_ms": kern_ms, "combine_ms": combine_ms, "e2e_ms": e2e_ms, "e2e_schedule": e2e_sched,
             "errors": errs, "clocks": clk}
 
 
@@ -748,7 +800,7 @@ def run_multi(args):
     ho = torch.empty(case.q.shape, dtype=torch.bfloat16).pin_memory()
     plans = [binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, dev) for _ in sets]
 
-    def e2e_step(i):
+    def h2d(i):
         j = i % copies
         c = sets[j]
         c.q.copy_(hq, non_blocking=True)
@@ -756,10 +808,12 @@ def run_multi(args):
         c.kv.seq_lens.copy_(hl, non_blocking=True)
         for d, h in zip((plans[j].qo_indptr, plans[j].tile_batch, plans[j].tile_index), hmap):
             d.copy_(h, non_blocking=True)
-        step(i, pl=plans[j])
-        ho.copy_(outs[j], non_blocking=True)
 
-    r = measure_step(binding, step, e2e_step, args.steps, args.warmup, stream)
+    def d2h(i):
+        ho.copy_(outs[i % copies], non_blocking=True)
+
+    r = measure_step(binding, step, (h2d, lambda i: step(i, pl=plans[i % copies]), d2h), args.steps, args.warmup,
+                     stream, copies)
     K, ms, kern_ms, combine_ms, e2e_ms = args.steps, r["ms"], r["kern_ms"], r["combine_ms"], r["e2e_ms"]
     errs, clk = r["errors"], r["clocks"]
 
@@ -783,7 +837,7 @@ def run_multi(args):
                      "multi_kernel_ms": round(kern_ms, 5), "combine_ms": round(combine_ms, 5),
                      "algorithmic_bytes_per_launch": nbytes,
                      "traffic": recorded_traffic("multi_kernel", workload_key(args))},
-        "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+        "e2e": {"schedule": r["e2e_schedule"], "value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ho.numel() * 2},
         "gpu_launches": K * (2 if S > 1 else 1), "device_errors": errs, "clocks": clk,
     }
@@ -893,16 +947,16 @@ def run_fp8kv(args):
     hl = case.seq_lens.cpu().pin_memory()
     ho = torch.empty(case.q.shape, dtype=torch.bfloat16).pin_memory()
 
-    def e2e_step(i):
-        j = i % copies
-        c = sets[j]
+    def h2d(i):
+        c = sets[i % copies]
         c.q.copy_(hq, non_blocking=True)
         c.block_table.copy_(ht, non_blocking=True)
         c.seq_lens.copy_(hl, non_blocking=True)
-        step(i)
-        ho.copy_(outs[j], non_blocking=True)
 
-    r = measure_step(binding, step, e2e_step, args.steps, args.warmup, stream)
+    def d2h(i):
+        ho.copy_(outs[i % copies], non_blocking=True)
+
+    r = measure_step(binding, step, (h2d, step, d2h), args.steps, args.warmup, stream, copies)
     K, ms, kern_ms, combine_ms, e2e_ms = args.steps, r["ms"], r["kern_ms"], r["combine_ms"], r["e2e_ms"]
     errs, clk = r["errors"], r["clocks"]
 
@@ -924,7 +978,7 @@ def run_fp8kv(args):
                      "fp8kv_kernel_ms": round(kern_ms, 5), "combine_ms": round(combine_ms, 5),
                      "algorithmic_bytes_per_launch": nbytes,
                      "traffic": recorded_traffic("fp8kv_kernel", workload_key(args))},
-        "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+        "e2e": {"schedule": r["e2e_schedule"], "value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": hq.numel() * 2 + ht.numel() * 4 + hl.numel() * 4,
                 "d2h_bytes_per_step": ho.numel() * 2},
         "gpu_launches": K * (2 if S > 1 else 1), "device_errors": errs, "clocks": clk,
@@ -1015,17 +1069,17 @@ def run_masked(args):
     hm = mask.cpu().pin_memory()
     ho = torch.empty(case.q.shape, dtype=torch.bfloat16).pin_memory()
 
-    def e2e_step(i):
-        j = i % copies
-        c, m = sets[j]
+    def h2d(i):
+        c, m = sets[i % copies]
         c.q.copy_(hq, non_blocking=True)
         c.block_table.copy_(ht, non_blocking=True)
         c.seq_lens.copy_(hl, non_blocking=True)
         m.copy_(hm, non_blocking=True)
-        step(i)
-        ho.copy_(outs[j], non_blocking=True)
 
-    r = measure_step(binding, step, e2e_step, args.steps, args.warmup, stream)
+    def d2h(i):
+        ho.copy_(outs[i % copies], non_blocking=True)
+
+    r = measure_step(binding, step, (h2d, step, d2h), args.steps, args.warmup, stream, copies)
     nbytes = masked_algorithmic(case)
     achieved = nbytes / (r["kern_ms"] * 1e-3) / 1e9
     line = {
@@ -1040,7 +1094,7 @@ def run_masked(args):
                      "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "kernel_ms": round(r["kern_ms"], 5),
                      "combine_ms": round(r["combine_ms"], 5), "algorithmic_bytes_per_launch": nbytes,
                      "traffic": recorded_traffic("multi_kernel", "masked")},
-        "e2e": {"value": round(nbytes / (r["e2e_ms"] * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"schedule": r["e2e_schedule"], "value": round(nbytes / (r["e2e_ms"] * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(r["e2e_ms"], 5),
                 "h2d_bytes_per_step": hq.numel() * 2 + ht.numel() * 4 + hl.numel() * 4 + hm.numel(),
                 "d2h_bytes_per_step": ho.numel() * 2},
