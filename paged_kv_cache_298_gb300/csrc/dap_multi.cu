@@ -183,12 +183,15 @@ struct MultiConsumer {
             const float2 p0 = bf16x2_to_float2(w0), p1 = bf16x2_to_float2(w1);
             l_run[n][0] = l_run[n][0] * alpha[0] + (p0.x + p1.x);
             l_run[n][1] = l_run[n][1] * alpha[1] + (p0.y + p1.y);
+            // the running max rarely moves after the first tiles: rescale only when it did
+            if (__any_sync(0xFFFFFFFFu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-            for (int m = 0; m < KS; ++m) {
-                acc[m][n][0] *= alpha[0];
-                acc[m][n][1] *= alpha[1];
-                acc[m][n][2] *= alpha[0];
-                acc[m][n][3] *= alpha[1];
+                for (int m = 0; m < KS; ++m) {
+                    acc[m][n][0] *= alpha[0];
+                    acc[m][n][1] *= alpha[1];
+                    acc[m][n][2] *= alpha[0];
+                    acc[m][n][3] *= alpha[1];
+                }
             }
             b0[n] = movmatrix_trans(w0);
             b1[n] = movmatrix_trans(w1);
