@@ -140,6 +140,26 @@ def test_balanced_schedule_fewer_tiles_than_ctas():
     assert binding.get_device_errors() == 0
 
 
+@pytest.mark.parametrize("max_kv_len", [0, 64])
+def test_every_sequence_empty_gives_zero_rows(max_kv_len):
+    case = inputs.make_paged_case(4, 16, 4, 128, 16, [0, 0, 0, 0], 86, max_pages=4).to("cuda")
+    for S in [0, 1, 3]:
+        out = torch.full_like(case.q, 5.0)
+        binding.decode_attn_paged(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                                  max_kv_len=max_kv_len, num_splits=S, out=out)
+        assert (out.float() == 0).all(), f"S={S}"
+    assert binding.get_device_errors() == 0
+
+
+def test_thousands_of_short_sequences_per_sequence_schedule():
+    # 2048 sequences of 1..40 keys at S = 2: a grid of 8192 CTAs, most sequences in one chunk
+    lens = inputs.uniform_lengths(2048, 1, 40, 87)
+    case = inputs.make_paged_case(2048, 8, 2, 64, 16, lens, 87).to("cuda")
+    ref = oracle_paged(case)
+    assert_close(gpu_paged(case, 2), ref, "B=2048")
+    assert binding.get_device_errors() == 0
+
+
 def test_strided_q_and_out_and_garbage_workspace():
     case = inputs.make_paged_case(3, 16, 4, 128, 16, [90, 200, 7], 80).to("cuda")
     ref = oracle_paged(case)

@@ -89,6 +89,16 @@ def test_wide_factor_range_and_q_beyond_f16():
         assert_close(gpu_fp8kv(case, S), ref, f"S={S}")
 
 
+def test_every_sequence_empty_gives_zero_rows():
+    case = inputs.make_fp8kv_case(3, 16, 4, 128, 16, [0, 0, 0], 5250).to("cuda")
+    for S in [1, 3]:
+        out = torch.full_like(case.q, 5.0)
+        binding.decode_attn_paged_fp8kv(case.q, case.k_codes, case.v_codes, case.k_scale, case.v_scale,
+                                        case.block_table, case.seq_lens, max_kv_len=16, num_splits=S, out=out)
+        assert (out.float() == 0).all(), f"S={S}"
+    assert binding.get_device_errors() == 0
+
+
 def test_strided_q_and_out():
     case = inputs.make_fp8kv_case(2, 16, 4, 128, 16, [90, 400], 5300).to("cuda")
     big_q = torch.zeros(2, 24, 136, dtype=torch.bfloat16, device="cuda")
