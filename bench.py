@@ -1206,7 +1206,8 @@ def run_reference(args):
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": workload_config(case, 0, 1, 0) | {"sample_sequences": len(rows)},
+        "config": workload_config(case, 0, 1, 0) | {"sample_sequences": len(rows),
+                                                   "cold_kv": "host memory (oracle on the CPU cores)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": r.oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
