@@ -15,21 +15,26 @@
 // tcgen05 module, but leaves the tile loop empty).
 //
 // One CTA per (token, head group of 128, half of HD):
-//   1. the token's window is compacted to its n participating slots (order kept);
+//   1. q[t, heads, :] streams in by TMA (128B swizzle, eight 64-wide blocks through a
+//      4-stage ring started at entry) and moves on into tensor memory (head = TMEM lane, two
+//      bf16 per column): blocks 0..3 once the token's window has been compacted to its n
+//      participating slots (order kept), 4..7 (the ring refilled meanwhile) after step 2;
 //   2. the n rows are gathered, dequantised (e4m3 -> f16 -> f32, times the f32 inverse scale,
 //      rounded once to bf16: the same single rounding the page's fallback does) and stored
 //      in shared memory as a 128-byte-swizzled [hd block][row][64] tile; rows n..n16-1 are
 //      zero (n16 = n rounded up to 16);
-//   3. q[t, heads, :] streams in through TMA (128B swizzle) in eight 64-wide blocks over a
-//      4-stage ring started before the gather, and one thread issues S = Q . KV^T (M=128, N=n16, K=512) into TMEM;
+//   3. one thread issues S = Q . KV^T (M=128, N=n16, K=512) into TMEM, A (q) read from
+//      tensor memory, B (the rows) from shared memory;
 //   4. two threads own each head (one TMEM lane, half of the score columns each): base-2
 //      softmax over its n scores, the probabilities rounded to bf16 into a swizzled P tile,
 //      l = their sum;
 //   5. O[:, half] = P . KV[:, half] (M=128, N=256, K=n16) reads the same KV tile as an
-//      MN-major operand;
+//      MN-major operand, into the tensor-memory columns q held;
 //   6. out = O / l in bf16.
-// The two CTAs of a token recompute S (cheap on tensor cores) so that O's 256 fp32
-// columns and S's columns fit tensor memory together.
+// Holding q in tensor memory (the ring only passes it through) leaves shared memory to a
+// whole 128-row KV tile, so no window waits for q blocks to be refilled after its first
+// products.  The two CTAs of a token recompute S (cheap on tensor
+// cores) so that O's 256 fp32 columns and S's columns fit tensor memory together.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -55,33 +60,29 @@ constexpr int kHD = 512;            // latent width
 constexpr int kHeads = 128;         // heads per CTA = MMA M
 constexpr int kMaxRows = 128;       // window rows a CTA holds
 constexpr int kHalf = kHD / 2;      // output columns per CTA
-constexpr int kThreads = 256;            // 8 warps: warps w and w+4 share TMEM lanes
+constexpr int kThreads = 256;       // 8 warps: warps w and w+4 share TMEM lanes
 constexpr int kQStages = 4;
 // shared-memory map (offsets from a 1024-byte aligned base)
 constexpr int kQOff = 0;                                    // q ring: 4 stages of 128 heads x 64
 constexpr int kQStage = kHeads * 128;                       // 16 KB per stage
-constexpr int kPOff = kQOff;                                // P reuses the ring after QK
+constexpr int kPOff = kQOff;                                // P: 2 blocks of 128 heads x 64, after q
+constexpr int kKvOff = kQOff + kQStages * kQStage;          // 65536: KV tile [8 blocks][n16 rows][128 B]
+constexpr int kOOff = kKvOff;                               // bf16 output staging after PV (64 KB)
 constexpr int kPBlock = kHeads * 128;                       // 16 KB per 64-wide row block
-constexpr int kOOff = kQOff;                                // bf16 output staging after PV (64 KB)
-constexpr int kXchOff = kPOff + 2 * kPBlock;                // softmax max/sum exchange (2 KB)
-constexpr int kKvOff = kQOff + kQStages * kQStage;          // 65536: [8 blocks][n16 rows][128 B]
-constexpr int kFitRows = 96;                                // windows of <= 96 rows leave room for
-constexpr int kQExtraOff = kKvOff + 8 * kFitRows * 128;     // q blocks 4..7 here (no ring refills)
-constexpr int kKvEnd = kKvOff + 8 * kMaxRows * 128;
-constexpr int kQExtraEnd = kQExtraOff + 4 * kQStage;
-constexpr int kRowsOff = kKvEnd > kQExtraEnd ? kKvEnd : kQExtraEnd;  // int32 slot per kept row
+constexpr int kXchOff = kKvOff + 8 * kMaxRows * 128;        // softmax max/sum exchange (2 KB)
+constexpr int kRowsOff = kXchOff + 4 * kHeads * 4;          // int32 slot per kept row
 constexpr int kInvOff = kRowsOff + kMaxRows * 4;            // f32 inverse scale per kept row
 constexpr int kCntOff = kInvOff + kMaxRows * 4;             // per-warp counts [0..7], abort [12]
 constexpr int kBarOff = kCntOff + 64;                       // mbarriers
-constexpr int kNumBars = 3 * kQStages + 2;                  // q_full, q_free, q_extra, mma_done[2]
+constexpr int kNumBars = kQStages + 2;                      // q_full[4], mma_done[2]
 constexpr int kTmemOff = kBarOff + kNumBars * 8;
 constexpr int kSmemUsed = kTmemOff + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;                // slack to align the base
-constexpr int kTmemCols = 512;                              // O: cols [0,256), S: [256,384)
+constexpr int kTmemCols = 512;  // q: cols [0,256) (two bf16 per column) until S is complete,
+                                // then O: [0,256); S: [256,384)
 constexpr int kSCol = 256;
+static_assert(kOOff + kHeads * kHalf * 2 <= kXchOff, "the output staging fits in the KV tile");
 static_assert(kPOff + 2 * kPBlock <= kKvOff, "P fits in the q ring");
-static_assert(kOOff + kHeads * kHalf * 2 <= kKvOff, "the output staging fits in the q ring");
-static_assert(kXchOff + 4 * kHeads * 4 <= kKvOff, "the softmax exchange fits in the q ring");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // ---- tcgen05 / descriptor helpers ---------------------------------------------------------
@@ -113,6 +114,18 @@ __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint6
         "setp.ne.u32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// D (+)= A . B with A read from tensor memory (lane = row, two bf16 per 32-bit column).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                                 bool accumulate) {
+    const uint32_t acc = accumulate ? 1u : 0u;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(acc)
         : "memory");
 }
 
@@ -152,6 +165,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane from registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // 64 consecutive fp32 columns of this thread's TMEM lane (one load, one wait).
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
     uint32_t r[64];
@@ -165,17 +190,17 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
     for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
         : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&b);
 }
 
 // Byte offset of 16-byte chunk `k` (0..7) of row `r` in a 128-byte-swizzled tile whose
@@ -196,6 +221,30 @@ struct Params {
 };
 
 
+// Moves the four q blocks of ring round `round` (blocks 4 round .. 4 round + 3) into tensor
+// memory: thread (head h, half c) waits for each stage, reads its 32 values (64 bytes, four
+// 128B-swizzled chunks) of row h and stores them at columns 32 block + 16 c of lane h (two
+// bf16 per column, the lower index in the low half).  A wait that gives up sets the abort
+// word; the caller still reaches every barrier.
+__device__ __forceinline__ void q_to_tmem(uint8_t *smem, uint64_t *q_full, uint32_t tmem_lane, int h, int c,
+                                          int round, int *cnt) {
+#pragma unroll
+    for (int st = 0; st < kQStages; ++st) {
+        if (!mbar_wait(&q_full[st], round & 1)) cnt[12] = 1;
+        const uint8_t *blk = smem + kQOff + st * kQStage;
+        uint32_t r[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(blk + sw128_off(h, 4 * c + i));
+            r[4 * i] = v.x;
+            r[4 * i + 1] = v.y;
+            r[4 * i + 2] = v.z;
+            r[4 * i + 3] = v.w;
+        }
+        tmem_st16(tmem_lane + (round * kQStages + st) * 32 + 16 * c, r);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     swa_kernel(const __grid_constant__ CUtensorMap qmap, const Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -208,29 +257,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     int *rows = reinterpret_cast<int *>(smem + kRowsOff);
     float *invs = reinterpret_cast<float *>(smem + kInvOff);
-    int *cnt = reinterpret_cast<int *>(smem + kCntOff);     // [0..3] warp counts, [4] n, [5] abort
+    int *cnt = reinterpret_cast<int *>(smem + kCntOff);     // [0..7] warp counts, [12] abort
     uint64_t *q_full = reinterpret_cast<uint64_t *>(smem + kBarOff);
-    uint64_t *q_free = q_full + kQStages;
-    uint64_t *q_extra = q_free + kQStages;
-    uint64_t *mma_done = q_extra + kQStages;
+    uint64_t *mma_done = q_full + kQStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
 
+    // thread = (head hrow = TMEM lane, half qhalf of q's 512 values / of the score columns):
+    // warps w and w + 4 serve the same 32 lanes
+    const int hrow = tid & (kHeads - 1);
+    const int chalf = warp >> 2;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+
+    const int qrow = t * p.NH + hg * kHeads;
     if (tid == 0) {
-        for (int i = 0; i < kQStages; ++i) {
-            mbar_init(&q_full[i], 1);
-            mbar_init(&q_free[i], 1);
-            mbar_init(&q_extra[i], 1);
-        }
+        for (int i = 0; i < kQStages; ++i) mbar_init(&q_full[i], 1);
         mbar_init(&mma_done[0], 1);
         mbar_init(&mma_done[1], 1);
         cnt[12] = 0;
         fence_barrier_init();
-        // start streaming q (the first kQStages of its eight 64-wide blocks) right away, so
-        // the copies overlap the window compaction and the gather
-        const int qrow0 = t * p.NH + hg * kHeads;
+        // ---- 1a. q's first four 64-wide blocks, right away: they travel during the compaction
         for (int kb = 0; kb < kQStages; ++kb) {
             mbar_arrive_expect_tx(&q_full[kb], kQStage);
-            tma_load_2d(smem + kQOff + kb * kQStage, &qmap, kb * 64, qrow0, &q_full[kb]);
+            tma_load_2d(smem + kQOff + kb * kQStage, &qmap, kb * 64, qrow, &q_full[kb]);
         }
     }
     if (warp == 0) {
@@ -241,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
 
-    // ---- 1. compact the window: slots of the rows that take part, in window order ---------
+    // ---- 1b. compact the window: slots of the rows that take part, in window order ---------
     long long len = p.lens[t];
     len = len < 0 ? 0 : (len > p.W ? p.W : len);
     int keep = 0;
@@ -270,17 +318,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         invs[pos] = __bfloat162float(p.inv_scale[slot]);
     }
     const int n16 = (n + 15) & ~15;
-
-    const int qrow = t * p.NH + hg * kHeads;
-    const int kvb = n16 * 128;                  // bytes per 64-wide hd block of the KV tile
-    const bool q_all = n > 0 && n16 <= kFitRows;  // room for all eight q blocks at once
-    if (tid == 0 && q_all) {
-        for (int kb = kQStages; kb < 8; ++kb) {
-            mbar_arrive_expect_tx(&q_extra[kb - kQStages], kQStage);
-            tma_load_2d(smem + kQExtraOff + (kb - kQStages) * kQStage, &qmap, kb * 64, qrow, &q_extra[kb - kQStages]);
+    const int kvb = n16 * 128;  // bytes per 64-wide hd block of the KV tile
+    // q blocks 0..3 from the ring into tensor memory (q_to_tmem), then the ring refilled
+    // with blocks 4..7 by thread 0 once every thread has read its stage
+    q_to_tmem(smem, q_full, tmem + lane_base, hrow, chalf, 0, cnt);
+    __syncthreads();  // rows[] / invs[] complete; the ring is read
+    if (tid == 0) {
+        for (int kb = 0; kb < kQStages; ++kb) {
+            mbar_arrive_expect_tx(&q_full[kb], kQStage);
+            tma_load_2d(smem + kQOff + kb * kQStage, &qmap, (kb + kQStages) * 64, qrow, &q_full[kb]);
         }
     }
-    __syncthreads();  // rows[] / invs[] complete
 
     // ---- 2. gather + dequantise the rows into the swizzled KV tile -------------------------
     // Each thread issues kBatch independent 16-byte loads before converting any of them, so
@@ -333,42 +381,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
+    q_to_tmem(smem, q_full, tmem + lane_base, hrow, chalf, 1, cnt);  // blocks 4..7
+    tmem_wait_st();  // this thread's q columns are in tensor memory
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    bool ok = true;
     const uint32_t tS = tmem + kSCol;
-    // ---- 3b. S = Q . KV^T, one thread issues ------------------------------------------------
+    // ---- 3. S = Q . KV^T, one thread issues; A = q from tensor memory ------------------------
     if (tid == 0 && n > 0) {
         const uint32_t idS = idesc_bf16(kHeads, n16, 0);
-        for (int kb = 0; kb < 8 && ok; ++kb) {
-            const int st = kb % kQStages;
-            const bool extra = q_all && kb >= kQStages;
-            if (!(extra ? mbar_wait(&q_extra[kb - kQStages], 0) : mbar_wait(&q_full[st], (kb / kQStages) & 1))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t qa = smem_addr(smem + (extra ? kQExtraOff + (kb - kQStages) * kQStage : kQOff + st * kQStage));
+        for (int kb = 0; kb < 8; ++kb) {
             const uint32_t kva = smem_addr(smem + kKvOff + kb * kvb);
 #pragma unroll
-            for (int k16 = 0; k16 < 4; ++k16)
-                umma_bf16(tS, sw128_desc(qa + 32 * k16, 16, 1024), sw128_desc(kva + 32 * k16, 16, 1024), idS,
-                          (kb | k16) != 0);
-            if (!q_all && kb + kQStages < 8) {  // refill this stage once its MMAs have read it
-                umma_commit(&q_free[st]);
-                if (!mbar_wait(&q_free[st], (kb / kQStages) & 1)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&q_full[st], kQStage);
-                tma_load_2d(smem + kQOff + st * kQStage, &qmap, (kb + kQStages) * 64, qrow, &q_full[st]);
-            }
+            for (int k16 = 0; k16 < 4; ++k16)  // 16 values = 8 columns of q per product
+                umma_bf16_tmem_a(tS, tmem + kb * 32 + k16 * 8, sw128_desc(kva + 32 * k16, 16, 1024), idS,
+                                 (kb | k16) != 0);
         }
         umma_commit(&mma_done[0]);
-        if (!ok) cnt[12] = 1;
     }
 
     // ---- 4. softmax: thread = head = TMEM lane -------------------------------------------------
@@ -376,11 +407,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n > 0) waited = mbar_wait(&mma_done[0], 0);
     const int good = __syncthreads_and(waited && cnt[12] == 0);
     tc_fence_after();
-    // thread = (head hrow = TMEM lane, column half chalf): warps w and w + 4 read the same
-    // 32 lanes, the first the low 64 score columns, the second the high ones
-    const int hrow = tid & (kHeads - 1);
-    const int chalf = warp >> 2;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     float *xch = reinterpret_cast<float *>(smem + kXchOff);  // [2][128] max, then [2][128] sum
     float l = 0.f;
     if (good && n > 0) {
@@ -427,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
 
-    // ---- 5. O[:, half] = P . KV[:, half] ----------------------------------------------------------
+    // ---- 5. O[:, half] = P . KV[:, half], into the columns q held (S is complete) --------------
     if (tid == 0 && good && n > 0) {
         const uint32_t idO = idesc_bf16(kHeads, kHalf, 1);
         const uint32_t pa = smem_addr(smem + kPOff);
@@ -443,15 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
 
     // ---- 6. out = O / l --------------------------------------------------------------------------
-    // Each thread turns half of its head's 256 columns into bf16 in a staging area (16-byte
-    // chunk c of row h at chunk c ^ (h mod 32), conflict-free both ways); then the CTA writes
-    // the 128 rows out with fully coalesced 16-byte stores.
-    if (tid == 0 && n == 0) {
-        // no row: nothing consumed the q blocks started at the top; let them land before the
-        // staging area (the q ring) is written
-        for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_full[i], 0);
-    }
-    __syncthreads();
+    // Each thread turns half of its head's 256 columns into bf16 in a staging area (the KV
+    // tile, read by no one now; 16-byte chunk c of row h at chunk c ^ (h mod 32),
+    // conflict-free both ways); then the CTA writes the 128 rows out with fully coalesced
+    // 16-byte stores.
     if (good2) {
         uint8_t *ostage = smem + kOOff;
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -480,12 +501,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint4 val = *reinterpret_cast<const uint4 *>(ostage + row * (kHalf * 2) + ((ch ^ (row & 31)) << 4));
             *reinterpret_cast<uint4 *>(obase + (long long)row * kHD + ch * 8) = val;
         }
-    } else if (tid == 0 && n > 0) {
+    } else if (tid == 0) {
         // A wait gave up.  Let the copies and products still in flight land (bounded) before
         // the tensor memory and the shared memory are released.
-        for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_full[i], 0);
-        if (q_all)
-            for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_extra[i], 0);
+        for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_full[i], 1);
         umma_commit(&mma_done[1]);
         (void)mbar_wait(&mma_done[1], 0);
     }
