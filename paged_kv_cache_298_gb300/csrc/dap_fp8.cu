@@ -290,12 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- 1b. compact the window: slots of the rows that take part, in window order ---------
+    // (the slot is loaded together with the length, not after it)
+    long long slot = -1;
+    if (tid < p.W) slot = p.slot_idx[(long long)t * p.W + tid];
     long long len = p.lens[t];
     len = len < 0 ? 0 : (len > p.W ? p.W : len);
     int keep = 0;
-    long long slot = -1;
-    if (tid < p.W && tid < len) {
-        slot = p.slot_idx[(long long)t * p.W + tid];
+    if (tid < len) {
         if (slot >= p.max_slots) {
             flag_error(DAP_DEVERR_SLOT);
             slot = -1;
@@ -319,65 +320,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int n16 = (n + 15) & ~15;
     const int kvb = n16 * 128;  // bytes per 64-wide hd block of the KV tile
-    // q blocks 0..3 from the ring into tensor memory (q_to_tmem), then the ring refilled
-    // with blocks 4..7 by thread 0 once every thread has read its stage
+    __syncthreads();  // rows[] / invs[] complete
+
+    // ---- 2. gather + dequantise the rows into the swizzled KV tile -------------------------
+    // Every thread issues all its 16-byte loads (at most kBatch: one pass covers 128 rows)
+    // before converting any of them; while they travel, q blocks 0..3 move from the ring
+    // into tensor memory (q_to_tmem) and thread 0 refills the ring with blocks 4..7 once
+    // every thread has read its stage.
+    constexpr int kBatch = 16;
+    static_assert(kMaxRows * 32 <= kThreads * kBatch, "one pass of loads covers the window");
+    const int total = n16 * 32;  // 16-byte pieces: 32 per 512-byte fp8 row
+    uint4 raw[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+        const int item = k * kThreads + tid;
+        const int r = item >> 5;
+        raw[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (item < total && r < n)
+            raw[k] = __ldg(reinterpret_cast<const uint4 *>(p.kv_cache + (long long)rows[r] * kHD) + (item & 31));
+    }
     q_to_tmem(smem, q_full, tmem + lane_base, hrow, chalf, 0, cnt);
-    __syncthreads();  // rows[] / invs[] complete; the ring is read
+    __syncthreads();  // the ring is read
     if (tid == 0) {
         for (int kb = 0; kb < kQStages; ++kb) {
             mbar_arrive_expect_tx(&q_full[kb], kQStage);
             tma_load_2d(smem + kQOff + kb * kQStage, &qmap, (kb + kQStages) * 64, qrow, &q_full[kb]);
         }
     }
-
-    // ---- 2. gather + dequantise the rows into the swizzled KV tile -------------------------
-    // Each thread issues kBatch independent 16-byte loads before converting any of them, so
-    // the row gathers overlap instead of paying one memory round trip each.
     if (n > 0) {
-        constexpr int kBatch = 16;
-        const int total = n16 * 32;  // 16-byte pieces: 32 per 512-byte fp8 row
-        for (int base0 = 0; base0 < total; base0 += kThreads * kBatch) {
-            uint4 raw[kBatch];
 #pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int item = base0 + k * kThreads + tid;
-                const int r = item >> 5;
-                raw[k] = make_uint4(0u, 0u, 0u, 0u);
-                if (item < total && r < n)
-                    raw[k] = __ldg(reinterpret_cast<const uint4 *>(p.kv_cache + (long long)rows[r] * kHD) + (item & 31));
-            }
+        for (int k = 0; k < kBatch; ++k) {
+            const int item = k * kThreads + tid;
+            if (item < total) {
+                const int r = item >> 5;   // row
+                const int c = item & 31;   // 16-byte piece = 16 hd values
+                uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                if (r < n) {
+                    const float inv = invs[r];
+                    const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+                    uint32_t o[8];
 #pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                const int item = base0 + k * kThreads + tid;
-                if (item < total) {
-                    const int r = item >> 5;   // row
-                    const int c = item & 31;   // 16-byte piece = 16 hd values
-                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                    if (r < n) {
-                        const float inv = invs[r];
-                        const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-                        uint32_t o[8];
+                    for (int i = 0; i < 4; ++i) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                            for (int j = 0; j < 2; ++j) {
-                                const __nv_fp8x2_storage_t pr =
-                                    (__nv_fp8x2_storage_t)((w4[i] >> (16 * j)) & 0xFFFFu);
-                                const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
-                                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
-                                const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * inv, f.y * inv);
-                                o[2 * i + j] = *reinterpret_cast<const uint32_t *>(&b);
-                            }
+                        for (int j = 0; j < 2; ++j) {
+                            const __nv_fp8x2_storage_t pr =
+                                (__nv_fp8x2_storage_t)((w4[i] >> (16 * j)) & 0xFFFFu);
+                            const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+                            const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * inv, f.y * inv);
+                            o[2 * i + j] = *reinterpret_cast<const uint32_t *>(&b);
                         }
-                        lo = make_uint4(o[0], o[1], o[2], o[3]);
-                        hi = make_uint4(o[4], o[5], o[6], o[7]);
                     }
-                    const int blk = c >> 2;       // 64-wide hd block
-                    const int k0 = (c & 3) * 2;   // first 16-byte chunk inside the 128-byte row
-                    uint8_t *tile = smem + kKvOff + blk * kvb;
-                    *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0)) = lo;
-                    *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0 + 1)) = hi;
+                    lo = make_uint4(o[0], o[1], o[2], o[3]);
+                    hi = make_uint4(o[4], o[5], o[6], o[7]);
                 }
+                const int blk = c >> 2;       // 64-wide hd block
+                const int k0 = (c & 3) * 2;   // first 16-byte chunk inside the 128-byte row
+                uint8_t *tile = smem + kKvOff + blk * kvb;
+                *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0)) = lo;
+                *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0 + 1)) = hi;
             }
         }
     }
