@@ -254,6 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col_half = blockIdx.x;    // which 256 output columns
     const int hg = blockIdx.y;          // head group of 128
     const int t = blockIdx.z;           // decode token
+    // Launched as a programmatic dependent of the previous kernel on the stream: nothing
+    // global is read before the wait (that kernel may still write q, the cache or the
+    // slot table); the next launch may start at once (it waits the same way).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     int *rows = reinterpret_cast<int *>(smem + kRowsOff);
     float *invs = reinterpret_cast<float *>(smem + kInvOff);
@@ -551,8 +556,17 @@ dap_status launch_fp8(const Fp8Args &a, cudaStream_t stream) {
     if (cudaFuncSetAttribute(fp8::swa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fp8::kSmemBytes) !=
         cudaSuccess)
         return DAP_ERR_CUDA;
-    const dim3 grid(2, a.NH / fp8::kHeads, a.T);
-    fp8::swa_kernel<<<grid, fp8::kThreads, fp8::kSmemBytes, stream>>>(qmap, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, a.NH / fp8::kHeads, a.T);
+    cfg.blockDim = dim3(fp8::kThreads);
+    cfg.dynamicSmemBytes = fp8::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fp8::swa_kernel, qmap, p) != cudaSuccess) return DAP_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DAP_OK : DAP_ERR_CUDA;
 }
 
