@@ -31,6 +31,11 @@ __global__ void __launch_bounds__(256)
     append_paged_kernel(const __nv_bfloat16 *k_new, const __nv_bfloat16 *v_new, __nv_bfloat16 *k_cache,
                         __nv_bfloat16 *v_cache, int num_pages, int page_size, const int32_t *block_table,
                         int max_pages, const int32_t *pos, int B, int Hkv, int D) {
+    // launched as a programmatic dependent: nothing global is read before the previous
+    // kernel on the stream is done; the next launch (the decode that reads these rows
+    // waits the same way) may start at once
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);  // (b, h)
     const int lane = threadIdx.x & 31;
     if (row >= B * Hkv) return;
@@ -58,6 +63,11 @@ template <int HD>
 __global__ void __launch_bounds__(256)
     append_fp8_kernel(const __nv_bfloat16 *rows, uint8_t *kv_cache, __nv_bfloat16 *inv_scale, const int64_t *slots,
                       int T, long long max_slots) {
+    // launched as a programmatic dependent: nothing global is read before the previous
+    // kernel on the stream is done; the next launch (the decode that reads these rows
+    // waits the same way) may start at once
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int NG = HD / 256;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -152,6 +162,11 @@ __global__ void __launch_bounds__(256)
                             uint8_t *v_codes, __nv_bfloat16 *k_scale, __nv_bfloat16 *v_scale, int num_pages,
                             int page_size, const int32_t *block_table, int max_pages, const int32_t *pos, int B,
                             int Hkv) {
+    // launched as a programmatic dependent: nothing global is read before the previous
+    // kernel on the stream is done; the next launch (the decode that reads these rows
+    // waits the same way) may start at once
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);  // (b, h)
     const int lane = threadIdx.x & 31;
     if (row >= B * Hkv) return;
@@ -173,6 +188,21 @@ __global__ void __launch_bounds__(256)
     quantise_row<D / 32>(v_new + (long long)row * D, v_codes + dst, v_scale + f, lane);
 }
 
+// Launch with programmatic stream serialization (the kernels order their own reads).
+template <class K, class... Args>
+cudaError_t launch_pdl(K kern, dim3 grid, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 }  // namespace
 
 dap_status launch_append_paged_fp8(const void *k_new, const void *v_new, uint8_t *k_codes, uint8_t *v_codes,
@@ -184,16 +214,19 @@ dap_status launch_append_paged_fp8(const void *k_new, const void *v_new, uint8_t
     __nv_bfloat16 *ks = static_cast<__nv_bfloat16 *>(k_scale), *vs = static_cast<__nv_bfloat16 *>(v_scale);
     switch (D) {
         case 64:
-            append_paged_fp8_kernel<64><<<grid, 256, 0, stream>>>(kn, vn, k_codes, v_codes, ks, vs, num_pages, page_size,
-                                                                  block_table, max_pages, pos, B, Hkv);
+            if (launch_pdl(append_paged_fp8_kernel<64>, grid, stream, kn, vn, k_codes, v_codes, ks, vs, num_pages,
+                           page_size, block_table, max_pages, pos, B, Hkv) != cudaSuccess)
+                return DAP_ERR_CUDA;
             break;
         case 128:
-            append_paged_fp8_kernel<128><<<grid, 256, 0, stream>>>(kn, vn, k_codes, v_codes, ks, vs, num_pages,
-                                                                   page_size, block_table, max_pages, pos, B, Hkv);
+            if (launch_pdl(append_paged_fp8_kernel<128>, grid, stream, kn, vn, k_codes, v_codes, ks, vs, num_pages,
+                           page_size, block_table, max_pages, pos, B, Hkv) != cudaSuccess)
+                return DAP_ERR_CUDA;
             break;
         case 256:
-            append_paged_fp8_kernel<256><<<grid, 256, 0, stream>>>(kn, vn, k_codes, v_codes, ks, vs, num_pages,
-                                                                   page_size, block_table, max_pages, pos, B, Hkv);
+            if (launch_pdl(append_paged_fp8_kernel<256>, grid, stream, kn, vn, k_codes, v_codes, ks, vs, num_pages,
+                           page_size, block_table, max_pages, pos, B, Hkv) != cudaSuccess)
+                return DAP_ERR_CUDA;
             break;
         default: return DAP_ERR_UNSUPPORTED;
     }
@@ -204,10 +237,11 @@ dap_status launch_append_paged(const void *k_new, const void *v_new, void *k_cac
                                int page_size, const int32_t *block_table, int max_pages, const int32_t *pos, int B,
                                int Hkv, int D, cudaStream_t stream) {
     const int rows = B * Hkv;
-    append_paged_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(k_new), static_cast<const __nv_bfloat16 *>(v_new),
-        static_cast<__nv_bfloat16 *>(k_cache), static_cast<__nv_bfloat16 *>(v_cache), num_pages, page_size,
-        block_table, max_pages, pos, B, Hkv, D);
+    if (launch_pdl(append_paged_kernel, dim3((unsigned)((rows + 7) / 8)), stream,
+                   static_cast<const __nv_bfloat16 *>(k_new), static_cast<const __nv_bfloat16 *>(v_new),
+                   static_cast<__nv_bfloat16 *>(k_cache), static_cast<__nv_bfloat16 *>(v_cache), num_pages, page_size,
+                   block_table, max_pages, pos, B, Hkv, D) != cudaSuccess)
+        return DAP_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DAP_OK : DAP_ERR_CUDA;
 }
 
@@ -218,8 +252,14 @@ dap_status launch_append_fp8(const void *rows, uint8_t *kv_cache, void *inv_scal
     const __nv_bfloat16 *r = static_cast<const __nv_bfloat16 *>(rows);
     __nv_bfloat16 *inv = static_cast<__nv_bfloat16 *>(inv_scale);
     switch (HD) {
-        case 256: append_fp8_kernel<256><<<grid, 256, 0, stream>>>(r, kv_cache, inv, slots, T, max_slots); break;
-        case 512: append_fp8_kernel<512><<<grid, 256, 0, stream>>>(r, kv_cache, inv, slots, T, max_slots); break;
+        case 256:
+            if (launch_pdl(append_fp8_kernel<256>, grid, stream, r, kv_cache, inv, slots, T, max_slots) != cudaSuccess)
+                return DAP_ERR_CUDA;
+            break;
+        case 512:
+            if (launch_pdl(append_fp8_kernel<512>, grid, stream, r, kv_cache, inv, slots, T, max_slots) != cudaSuccess)
+                return DAP_ERR_CUDA;
+            break;
         default: return DAP_ERR_UNSUPPORTED;
     }
     return cudaGetLastError() == cudaSuccess ? DAP_OK : DAP_ERR_CUDA;
