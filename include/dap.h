@@ -384,6 +384,14 @@ void dap_set_trace_events(void *split_begin, void *split_end, void *combine_end)
  * device.  Synchronises the device.  Returns DAP_ERR_CUDA if the read fails. */
 dap_status dap_get_device_errors(unsigned int *flags, int clear);
 
+/* Diagnostic for the failure path of every pipeline wait: launches one thread on `stream`
+ * (a cudaStream_t, NULL = the default stream) that waits, through the same bounded wait
+ * the decode kernels use, on a shared-memory barrier nothing ever arrives on.  After its
+ * limit (about 2e9 SM cycles, near one second) the wait gives up, sets DAP_DEVERR_TIMEOUT
+ * in the device error word and the kernel returns normally, so the context stays usable.
+ * Asynchronous; returns DAP_ERR_CUDA if the launch fails.  For tests only. */
+dap_status dap_selftest_wait_timeout(void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,8 @@ EXPORTS = ("dap_status_string", "dap_version", "dap_device_sm_count", "dap_plan_
            "decode_attn_paged_fp8", "decode_attn_paged_noalloc", "kv_append_paged", "kv_append_fp8",
            "dap_set_trace_events", "dap_get_device_errors", "dap_multi_tokens_per_tile",
            "dap_q_tile_map", "dap_workspace_bytes_multi", "decode_attn_paged_multi",
-           "decode_attn_paged_fp8kv", "kv_append_paged_fp8", "decode_attn_paged_masked")
+           "decode_attn_paged_fp8kv", "kv_append_paged_fp8", "decode_attn_paged_masked",
+           "dap_selftest_wait_timeout")
 
 
 class DapError(RuntimeError):
@@ -109,6 +110,8 @@ def load(build_if_missing: bool = True):
         lib.dap_set_trace_events.restype = None
         lib.dap_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
         lib.dap_get_device_errors.restype = I
+        lib.dap_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
+        lib.dap_selftest_wait_timeout.restype = I
         _lib = lib
         return lib
 
@@ -165,6 +168,12 @@ def get_device_errors(clear: bool = True) -> int:
     v = ctypes.c_uint(0)
     _check(load().dap_get_device_errors(ctypes.byref(v), int(clear)), "dap_get_device_errors")
     return v.value
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """include/dap.h: dap_selftest_wait_timeout (one bounded wait that runs out on purpose;
+    about a second later the device error word holds DEVERR_TIMEOUT)."""
+    _check(load().dap_selftest_wait_timeout(_stream(stream)), "dap_selftest_wait_timeout")
 
 
 # ---- decode entry points ---------------------------------------------------------------

@@ -563,6 +563,10 @@ void dap_set_trace_events(void *split_begin, void *split_end, void *combine_end)
     g_trace.combine_end = static_cast<cudaEvent_t>(combine_end);
 }
 
+dap_status dap_selftest_wait_timeout(void *stream) {
+    return launch_selftest_wait(static_cast<cudaStream_t>(stream));
+}
+
 dap_status dap_get_device_errors(unsigned int *flags, int clear) {
     if (!flags) return DAP_ERR_NULL;
     *flags = 0;

@@ -1152,6 +1152,24 @@ int balanced_kv_heads_per_unit(int D, int G) {
     return 1;
 }
 
+namespace {
+
+// One thread waits on a barrier that nothing arrives on: the bounded wait gives up and
+// flags DAP_DEVERR_TIMEOUT (the failure path of every pipeline wait, run on purpose).
+__global__ void selftest_wait_kernel() {
+    __shared__ uint64_t bar;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    (void)mbar_wait(&bar, 0);
+}
+
+}  // namespace
+
+dap_status launch_selftest_wait(cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 1, 0, stream>>>();
+    return cudaGetLastError() == cudaSuccess ? DAP_OK : DAP_ERR_CUDA;
+}
+
 bool read_errors_decode(unsigned int *flags, bool clear) {
     unsigned int v = 0;
     if (cudaMemcpyFromSymbol(&v, g_device_errors, sizeof v) != cudaSuccess) return false;

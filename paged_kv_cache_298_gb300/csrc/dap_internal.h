@@ -111,6 +111,7 @@ bool read_errors_append(unsigned int *flags, bool clear);
 // Host readers of each translation unit's device error word (cudaMemcpyFromSymbol on the
 // current device); `clear` resets it.  Return false when the copy fails.
 bool read_errors_decode(unsigned int *flags, bool clear);
+dap_status launch_selftest_wait(cudaStream_t stream);
 bool read_errors_fp8(unsigned int *flags, bool clear);
 
 // Driver entry point for cuTensorMapEncodeTiled, fetched through the runtime so the

@@ -196,6 +196,18 @@ def test_seq_len_above_bound_is_flagged_and_clamped():
     del lens
 
 
+def test_wait_that_runs_out_is_flagged_and_the_context_stays_usable():
+    """The failure path of the pipeline waits, run on purpose: a bounded wait on a barrier
+    nothing arrives on gives up after its limit (about a second), flags DEVERR_TIMEOUT and
+    returns; a decode on the same context afterwards runs clean and matches the oracle."""
+    binding.selftest_wait_timeout()
+    torch.cuda.synchronize()
+    assert binding.get_device_errors(clear=True) & binding.DEVERR_TIMEOUT
+    case = inputs.make_paged_case(2, 8, 2, 64, 16, [40, 90], 88).to("cuda")
+    assert_close(gpu_paged(case, 2), oracle_paged(case), "after the timeout")
+    assert binding.get_device_errors() == 0
+
+
 def test_page_index_outside_pool_is_flagged():
     case = inputs.make_paged_case(1, 8, 2, 64, 16, [40], 83).to("cuda")
     table = case.block_table.clone()
