@@ -2,8 +2,9 @@
  * dap.h -- C ABI of the paged decode-attention library for NVIDIA GB300 (sm_103a).
  *
  * Single-token GQA decode attention over a paged KV cache (bf16 or fp8 e4m3), its
- * contiguous-cache form, multi-token causal decode, the fp8 sliding-window latent (K = V)
- * variant, and the cache appends that feed them.  Plain pointers and sizes only.
+ * contiguous-cache form, multi-token causal decode, masked decode (bool masks, with the
+ * causal rule), the fp8 sliding-window latent (K = V) variant, and the cache appends that
+ * feed them.  Plain pointers and sizes only.
  *
  * Conventions shared by every entry point:
  *   - The caller owns every buffer.  The library allocates no device memory and never
@@ -11,6 +12,11 @@
  *     as void*, NULL = the legacy default stream).
  *   - "device" marks a device pointer; "host" a host value.  bf16 buffers are raw
  *     IEEE bfloat16 bit patterns (passed as void*).
+ *   - Kernels are launched as programmatic dependents (CUDA programmatic dependent
+ *     launch): each waits for the work before it on the stream to complete before it
+ *     reads or writes global memory, so stream order holds as for ordinary launches, but
+ *     its launch and prologue may overlap the end of the previous kernel.  Events recorded
+ *     between two calls still mark the boundary.
  *   - Errors that the host can see (null pointers, bad sizes, unsupported shapes,
  *     misaligned pointers, a workspace that is too small) are returned as a dap_status
  *     before anything is launched.  A failed launch returns DAP_ERR_CUDA.
