@@ -13,7 +13,7 @@
  *   - "device" marks a device pointer; "host" a host value.  bf16 buffers are raw
  *     IEEE bfloat16 bit patterns (passed as void*).
  *   - Kernels are launched as programmatic dependents (CUDA programmatic dependent
- *     launch; all but the persistent kernel of the balanced schedule): each waits for the
+ *     launch; all but the persistent kernel of the balanced schedule and the self-test): each waits for the
  *     work before it on the stream to complete before it reads or writes global memory,
  *     so stream order holds as for ordinary launches, but its launch and prologue may
  *     overlap the end of the previous kernel.  Events recorded between two calls still
