@@ -13,11 +13,11 @@
  *   - "device" marks a device pointer; "host" a host value.  bf16 buffers are raw
  *     IEEE bfloat16 bit patterns (passed as void*).
  *   - Kernels are launched as programmatic dependents (CUDA programmatic dependent
- *     launch; all but the persistent kernel of the balanced schedule and the self-test): each waits for the
- *     work before it on the stream to complete before it reads or writes global memory,
- *     so stream order holds as for ordinary launches, but its launch and prologue may
- *     overlap the end of the previous kernel.  Events recorded between two calls still
- *     mark the boundary.
+ *     launch; all but the balanced schedule's persistent kernel and the self-test): each
+ *     waits for the work before it on the stream to complete before it reads or writes
+ *     global memory, so stream order holds as for ordinary launches, but its launch and
+ *     prologue may overlap the end of the previous kernel.  Events recorded between two
+ *     calls still mark the boundary.
  *   - Errors that the host can see (null pointers, bad sizes, unsupported shapes,
  *     misaligned pointers, a workspace that is too small) are returned as a dap_status
  *     before anything is launched.  A failed launch returns DAP_ERR_CUDA.
