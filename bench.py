@@ -238,14 +238,26 @@ def repeat_for(run, target_s=10.0):
     return total / n, n
 
 
-def cpu_baseline(case, target_s=10.0):
+def cpu_baseline(case, target_s=10.0, single_s=3.0):
+    """The oracle on the host cores (OpenMP over all of them), plus the same oracle on one
+    thread over a smaller sample."""
     r = OracleRunner(case)
     rows = r.sample_rows(target_s)
     dt, passes = repeat_for(lambda: r.run(rows), target_s)
     nbytes = algorithmic_bytes(case, torch.as_tensor(rows))
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": r.oracle.num_threads(), "kind": "oracle",
+    cores = r.oracle.num_threads()
+    r.oracle.set_num_threads(1)
+    try:
+        rows1 = r.sample_rows(single_s)
+        dt1, passes1 = repeat_for(lambda: r.run(rows1), single_s)
+    finally:
+        r.oracle.set_num_threads(cores)
+    nbytes1 = algorithmic_bytes(case, torch.as_tensor(rows1))
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"fp64 oracle (OpenMP) on sequences 0..{len(rows) - 1} of {case.B} (all heads), "
-                      f"{passes} passes of {dt:.2f} s"}
+                      f"{passes} passes of {dt:.2f} s",
+            "single_thread": {"value": nbytes1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"sequences 0..{len(rows1) - 1}, {passes1} passes of {dt1:.2f} s"}}
 
 
 # ---- our arm -----------------------------------------------------------------------------
