@@ -558,6 +558,24 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     const int rem = blockIdx.x - s * units;
     const int b = rem / nkvg;
     const int kvg = rem - b * nkvg;
+    // The pipeline barriers and the tensor maps touch nothing the previous kernel writes:
+    // they are set up before the wait below, overlapping that kernel's end.
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *empty = full + NS;
+    int *misc = reinterpret_cast<int *>(smem + C::MISC_OFF);  // [0] tiles issued, [1] abort
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NWC);
+        }
+        misc[0] = 0;
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+    if (warp == NWC && lane == 0) {
+        prefetch_tensormap(&mapK);
+        prefetch_tensormap(&mapV);
+    }
     // Launched as a programmatic dependent: the CTA may be resident before the previous
     // kernel on the stream has finished, so nothing that kernel may write is read before
     // this wait; the combine that follows may be launched as soon as every CTA is here.
@@ -583,26 +601,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     const int tok0 = s * p.chunk;
     const int tok1 = min(L, tok0 + p.chunk);
     const int ntiles = tok1 > tok0 ? (tok1 - tok0 + BT - 1) / BT : 0;
-
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *empty = full + NS;
-    int *misc = reinterpret_cast<int *>(smem + C::MISC_OFF);  // [0] tiles issued, [1] abort
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], NWC);
-        }
-        misc[0] = 0;
-        misc[1] = 0;
-        fence_barrier_init();
-    }
     __syncthreads();
 
     if (warp == NWC) {  // ---- producer warp: page lookup + TMA issue
-        if (lane == 0) {
-            prefetch_tensormap(&mapK);
-            prefetch_tensormap(&mapV);
-        }
         const int32_t *table = PAGED ? p.block_table + (long long)b * p.max_pages : nullptr;
         auto lookup = [&](int tile) -> int {  // page id of this lane's box of `tile`
             if (!PAGED) return b;
