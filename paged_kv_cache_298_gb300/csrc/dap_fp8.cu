@@ -254,12 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col_half = blockIdx.x;    // which 256 output columns
     const int hg = blockIdx.y;          // head group of 128
     const int t = blockIdx.z;           // decode token
-    // Launched as a programmatic dependent of the previous kernel on the stream: nothing
-    // global is read before the wait (that kernel may still write q, the cache or the
-    // slot table); the next launch may start at once (it waits the same way).
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
     int *rows = reinterpret_cast<int *>(smem + kRowsOff);
     float *invs = reinterpret_cast<float *>(smem + kInvOff);
     int *cnt = reinterpret_cast<int *>(smem + kCntOff);     // [0..7] warp counts, [12] abort
@@ -272,19 +266,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hrow = tid & (kHeads - 1);
     const int chalf = warp >> 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-
     const int qrow = t * p.NH + hg * kHeads;
+
+    // Barriers and tensor memory touch nothing the previous kernel writes: they are set up
+    // before the wait below, overlapping that kernel's end.
     if (tid == 0) {
         for (int i = 0; i < kQStages; ++i) mbar_init(&q_full[i], 1);
         mbar_init(&mma_done[0], 1);
         mbar_init(&mma_done[1], 1);
         cnt[12] = 0;
         fence_barrier_init();
-        // ---- 1a. q's first four 64-wide blocks, right away: they travel during the compaction
-        for (int kb = 0; kb < kQStages; ++kb) {
-            mbar_arrive_expect_tx(&q_full[kb], kQStage);
-            tma_load_2d(smem + kQOff + kb * kQStage, &qmap, kb * 64, qrow, &q_full[kb]);
-        }
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -292,6 +283,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                      "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // Launched as a programmatic dependent of the previous kernel on the stream: nothing
+    // global is read before the wait (that kernel may still write q, the cache or the
+    // slot table); the next launch may start at once (it waits the same way).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // ---- 1a. q's first four 64-wide blocks, right away: they travel during the compaction
+    if (tid == 0) {
+        for (int kb = 0; kb < kQStages; ++kb) {
+            mbar_arrive_expect_tx(&q_full[kb], kQStage);
+            tma_load_2d(smem + kQOff + kb * kQStage, &qmap, kb * 64, qrow, &q_full[kb]);
+        }
     }
 
     // ---- 1b. compact the window: slots of the rows that take part, in window order ---------
