@@ -85,7 +85,8 @@ int dap_device_sm_count(void);
  * ceil(seq_lens[b] / chunk) splits (at least 1).  When B * Hkv (sequence, kv head) units
  * are fewer than the GPU's resident CTAs (2 per SM), S is the number of chunks that fills
  * one wave; otherwise S keeps the largest chunk near a tenth of one SM's share of the KV
- * rows.  S never exceeds the number of 64-token chunks of the longest sequence.
+ * rows.  S never exceeds the number of 64-token chunks of the longest sequence.  Every decode
+ * entry point runs this plan when given num_splits = 0 (see dap_resolve_splits).
  *   sm_count   SMs available (dap_device_sm_count()).
  *   total_kv   sum of seq_lens (host); 0 means "unknown", taken as B * max_kv_len.
  * Pure host function; no CUDA call.
@@ -97,12 +98,34 @@ int dap_plan_splits(int sm_count, int B, int Hq, int Hkv, int D, int page_size,
  * multiple of 64 tokens (at least 64).  Pure host function. */
 int dap_chunk_tokens(int max_kv_len, int num_splits);
 
-/* Workspace bytes decode_attn_paged / decode_attn_contig need for `num_splits`:
+/* num_splits value selecting the balanced persistent schedule of decode_attn_paged /
+ * decode_attn_contig / decode_attn_paged_noalloc (see decode_attn_paged). */
+#define DAP_SPLITS_BALANCED (-1)
+
+/*
+ * The split count a decode call runs for the num_splits it is given (every decode entry
+ * point resolves its argument this way, with sm_count = dap_device_sm_count() and
+ * total_kv = 0):
+ *   num_splits == 0: dap_plan_splits(sm_count, B, Hq, Hkv, D, page_size, max_kv_len, total_kv);
+ *   num_splits >= 1: num_splits;
+ *   then lowered to the number of dap_chunk_tokens-long chunks that can hold a token
+ *   (ceil(max_kv_len / chunk), at least 1), so no split is empty for every sequence.
+ *   num_splits == DAP_SPLITS_BALANCED returns DAP_SPLITS_BALANCED (1 when B > 4096: so many
+ *   sequences fill the device with one CTA per sequence and kv head).
+ * Returns 0 for invalid arguments (num_splits < -1, B < 0, ...).  Size the workspace with
+ * dap_workspace_bytes(B, Hq, Hkv, D, <the value returned>).  Pure host function.
+ */
+int dap_resolve_splits(int num_splits, int sm_count, int B, int Hq, int Hkv, int D, int page_size,
+                       int max_kv_len, long long total_kv);
+
+/* Workspace bytes a decode call needs for a resolved split count (dap_resolve_splits):
  *   num_splits == 1: 0;
  *   num_splits >= 2: room for B*num_splits*Hq partial rows of (D + 2) floats (unnormalised
  *                    acc, running max m, running sum l);
- *   num_splits == 0: the balanced schedule's partial slots (two per persistent CTA, for at
- *                    most 1024 CTAs) plus 8 bytes per (sequence, kv head); 0 when B > 4096.
+ *   num_splits == DAP_SPLITS_BALANCED: the balanced schedule's partial slots (two per
+ *                    persistent CTA, for at most 1024 CTAs) plus 8 bytes per (sequence,
+ *                    kv head); 0 when B > 4096;
+ *   num_splits == 0: 0 (0 is not a split count: resolve it first).
  * Pure host function. */
 size_t dap_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits);
 
@@ -121,16 +144,21 @@ size_t dap_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits);
  *   max_kv_len   host: an upper bound of seq_lens (<= max_pages * page_size); it sets
  *                the chunk length of the split plan.
  *   scale        softmax scale applied in fp32 to q . k (normally 1/sqrt(D)).
- *   num_splits   0 = balanced schedule (recommended): a persistent grid of SMs x resident
- *                CTAs cuts the flattened (sequence, kv head, 32-token tile) space into
- *                equal contiguous ranges, whatever the length mix; splits of a sequence
- *                are merged by a combine kernel.  (B > 4096 runs one CTA per sequence and
- *                kv head instead.)  S > 0 = per-sequence schedule: every sequence is cut
- *                into chunks of dap_chunk_tokens(max_kv_len, S) tokens, one CTA each
- *                (dap_plan_splits suggests an S).
- *   workspace    device scratch of at least dap_workspace_bytes(B, Hq, Hkv, D, num_splits)
- *                bytes, 16-byte aligned (may be NULL when that is 0).  Needs no
- *                initialisation; its contents are undefined afterwards.
+ *   num_splits   S > 0 = per-sequence schedule: every sequence is cut into chunks of
+ *                dap_chunk_tokens(max_kv_len, S) tokens, one CTA each, and the splits of a
+ *                sequence are merged by a combine kernel.  0 = the same schedule with the
+ *                planner's S (dap_plan_splits with total_kv = 0; a caller that knows the
+ *                summed lengths can pass its own plan instead).  DAP_SPLITS_BALANCED =
+ *                balanced schedule: a persistent grid of SMs x resident CTAs cuts the
+ *                flattened (sequence, kv head, 64-token tile) space into equal contiguous
+ *                ranges, whatever the length mix, and a combine kernel merges the pieces
+ *                of a sequence (B > 4096 runs one CTA per sequence and kv head instead).
+ *                The planner's schedule measures faster on most batches; the balanced one
+ *                on a single long sequence.
+ *   workspace    device scratch of at least dap_workspace_bytes(B, Hq, Hkv, D,
+ *                dap_resolve_splits(num_splits, ...)) bytes, 16-byte aligned (may be NULL
+ *                when that is 0).  Needs no initialisation; its contents are undefined
+ *                afterwards.
  *   out          device bf16 [B, Hq, D], element strides (out_stride_b, out_stride_h, 1).
  *                Written in full (an empty sequence gives a zero row).
  *   Supported: D in {32, 64, 128, 256}; G in {1, 2, 4, 8}; any page_size >= 1 for D in
@@ -173,8 +201,9 @@ dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_s
  *   k_scale, v_scale  device bf16 [num_pages, Hkv, page_size] contiguous (one factor per
  *                     slot and kv head; kv-head-major inside a page so that a page's
  *                     factors of one head are contiguous).
- *   num_splits        >= 1: per-sequence splits as decode_attn_paged; 0 = the library picks
- *                     dap_plan_splits(SMs, B, Hq, Hkv, D, page_size, max_kv_len, 0).
+ *   num_splits        >= 1: per-sequence splits as decode_attn_paged; 0 = the planner's S
+ *                     (dap_resolve_splits(0, SMs, B, Hq, Hkv, D, page_size, max_kv_len, 0)).
+ *                     DAP_SPLITS_BALANCED is not supported here.
  *   workspace         >= dap_workspace_bytes(B, Hq, Hkv, D, S) for the S used.
  *   q, out, block_table, seq_lens, max_kv_len, scale, strides: as decode_attn_paged.
  *   Supported: D = 128; G in {1, 2, 4, 8}; page_size a multiple of 8; codes and factor
@@ -247,8 +276,9 @@ size_t dap_workspace_bytes_multi(int total_q, int Hq, int D, int num_splits);
  *   num_splits   >= 1: the per-sequence schedule of decode_attn_paged, per tile: the tile's
  *                keys (up to its last token's position) are cut into chunks of
  *                dap_chunk_tokens(max_kv_len, num_splits) keys, one CTA per (tile, kv head,
- *                chunk), merged by a combine kernel.  0 = the library picks
- *                dap_plan_splits(SMs, num_tiles, Hq, Hkv, D, page_size, max_kv_len, 0).
+ *                chunk), merged by a combine kernel.  0 = the planner's S over the tiles
+ *                (dap_resolve_splits(0, SMs, num_tiles, Hq, Hkv, D, page_size, max_kv_len,
+ *                0)).  DAP_SPLITS_BALANCED is not supported here.
  *   mask         device uint8 [total_q, mask_stride] or NULL: the 3-D bool mask [batch,
  *                q_len, kv_len] of [A: "Python Wrappers"] with its q rows packed like q
  *                (row qo_indptr[b] + i; nonzero = keep).  Token i keeps key t only if t is
@@ -279,8 +309,9 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
  * mask[b * mask_stride + t] is nonzero.  A sequence with no key left gives a zero row.
  *   mask         device uint8 [B, mask_stride]; mask_stride >= max_kv_len, a multiple of 16;
  *                mask 16-byte aligned (bytes past seq_lens[b] are not used).
- *   num_splits   >= 1: per-sequence splits as decode_attn_paged; 0 = the library picks
- *                dap_plan_splits(SMs, B, Hq, Hkv, D, page_size, max_kv_len, 0).
+ *   num_splits   >= 1: per-sequence splits as decode_attn_paged; 0 = the planner's S
+ *                (dap_resolve_splits(0, SMs, B, Hq, Hkv, D, page_size, max_kv_len, 0)).
+ *                DAP_SPLITS_BALANCED is not supported here.
  *   workspace    >= dap_workspace_bytes(B, Hq, Hkv, D, S) for the S used.
  *   Everything else as decode_attn_paged.  Supported: D in {64, 128}; G in {1, 2, 4, 8};
  *   page_size a multiple of 8.
@@ -360,16 +391,20 @@ dap_status kv_append_fp8(const void *rows, uint8_t *kv_cache, void *inv_scale,
  * `workspace_bytes`.  The split partials live in one file-scope device array of
  * DAP_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the library holds until the
  * process exits.  Sizes:
- *   - a num_splits whose partials, dap_workspace_bytes(B, Hq, Hkv, D, num_splits), exceed
- *     DAP_NOALLOC_SCRATCH_BYTES is rejected with DAP_ERR_SCRATCH_LIMIT (nothing launched),
- *     except that num_splits == 0 whose balanced-schedule partials do not fit falls back
- *     to the planner's per-sequence S, lowered until its partials fit.
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current) and caches it; make that first call before any stream
- * capture.  The array keeps what the last call left in it; nothing in it has to start
- * at zero, because every partial a call reads was written earlier in that same call.
- * All calls share the one array, so calls that overlap on the GPU (on different streams,
- * or from different host threads) race and corrupt each other's results: serialise them.
+ *   - num_splits == 0 runs the planner's S (as decode_attn_paged does), lowered until its
+ *     partials, dap_workspace_bytes(B, Hq, Hkv, D, S), fit the array;
+ *   - a num_splits >= 1, or DAP_SPLITS_BALANCED, whose partials exceed the array is
+ *     rejected with DAP_ERR_SCRATCH_LIMIT (nothing launched).
+ * Start-up: under CUDA's lazy module loading (the runtime's default) the array is reserved
+ * on a device only when the first call on that device loads the library's module and looks
+ * up the array's address (cudaGetSymbolAddress, with that device current), so that first
+ * call can still take 16 MiB of device memory and fail with DAP_ERR_CUDA if there is none.
+ * Make one call per device at start-up, before serving and before any stream capture (or
+ * run with CUDA_MODULE_LOADING=EAGER); later calls reserve nothing.
+ * The array keeps what the last call left in it; nothing in it has to start at zero,
+ * because every partial a call reads was written earlier in that same call.  All calls
+ * share the one array, so calls that overlap on the GPU (on different streams, or from
+ * different host threads) race and corrupt each other's results: serialise them.
  * Calls no cudaMalloc, cudaFree or other allocating routine.
  */
 #define DAP_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -27,7 +27,7 @@ DEVERR_TIMEOUT, DEVERR_SEQLEN, DEVERR_PAGE, DEVERR_SLOT, DEVERR_QMAP = 0x1, 0x2,
 
 # every symbol include/dap.h declares
 EXPORTS = ("dap_status_string", "dap_version", "dap_device_sm_count", "dap_plan_splits",
-           "dap_chunk_tokens", "dap_workspace_bytes", "decode_attn_paged", "decode_attn_contig",
+           "dap_chunk_tokens", "dap_resolve_splits", "dap_workspace_bytes", "decode_attn_paged", "decode_attn_contig",
            "decode_attn_paged_fp8", "decode_attn_paged_noalloc", "kv_append_paged", "kv_append_fp8",
            "dap_set_trace_events", "dap_get_device_errors", "dap_multi_tokens_per_tile",
            "dap_q_tile_map", "dap_workspace_bytes_multi", "decode_attn_paged_multi",
@@ -35,10 +35,20 @@ EXPORTS = ("dap_status_string", "dap_version", "dap_device_sm_count", "dap_plan_
            "dap_selftest_wait_timeout")
 
 
+SPLITS_BALANCED = -1   # include/dap.h: DAP_SPLITS_BALANCED
+
+
 class DapError(RuntimeError):
-    def __init__(self, status: int, what: str):
+    """A library status other than DAP_OK (``status`` is its code), or, with status None, a
+    tensor the binding refused before calling the library (not a CUDA tensor, or on another
+    device than q)."""
+
+    def __init__(self, status, what: str):
         self.status = status
-        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+        if status is None:
+            super().__init__(what)
+        else:
+            super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
 
 
 def library_path() -> str:
@@ -72,6 +82,8 @@ def load(build_if_missing: bool = True):
         lib.dap_plan_splits.restype = I
         lib.dap_chunk_tokens.argtypes = [I, I]
         lib.dap_chunk_tokens.restype = I
+        lib.dap_resolve_splits.argtypes = [I, I, I, I, I, I, I, I, LL]
+        lib.dap_resolve_splits.restype = I
         lib.dap_workspace_bytes.argtypes = [I, I, I, I, I]
         lib.dap_workspace_bytes.restype = SZ
         lib.decode_attn_paged.argtypes = [P, LL, LL, P, P, I, I, P, I, P, I, I, I, I, I, F, I, P, SZ,
@@ -129,10 +141,50 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
+def _device_of(what: str, first, **others) -> torch.device:
+    """The CUDA device of `first`; every other tensor given must be a CUDA tensor on it.
+    Raises DapError (status None) before the library sees a pointer it could not use: a CPU
+    tensor or one on another GPU would reach the kernels as a foreign address."""
+    if not getattr(first, "is_cuda", False):
+        raise DapError(None, f"{what}: the first tensor must be a CUDA tensor")
+    dev = first.device
+    for name, t in others.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise DapError(None, f"{what}: {name} is not a CUDA tensor")
+        if t.device != dev:
+            raise DapError(None, f"{what}: {name} is on {t.device}, the call's tensors on {dev}")
+    return dev
+
+
+def _stream(stream, dev: torch.device):
+    """The stream handle for a call on `dev`: the given stream (which must belong to `dev`)
+    or that device's current stream."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(dev)
+    elif stream.device != dev:
+        raise DapError(None, f"the stream belongs to {stream.device}, the call's tensors to {dev}")
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _splits(lib, num_splits, units, Hq, Hkv, D, page_size, max_kv_len, total_kv):
+    """(split count passed to the library, split count it runs) for a call on the current
+    device.  num_splits 0 is the planner's choice: the library resolves it with the summed
+    lengths unknown; when the caller knows them (`total_kv`), the plan is made here with
+    them and passed as an explicit count."""
+    S = int(num_splits)
+    sms = lib.dap_device_sm_count() if S == 0 else 0
+    if S == 0 and total_kv:
+        S = lib.dap_resolve_splits(0, sms, units, Hq, Hkv, D, page_size, int(max_kv_len), int(total_kv))
+    run = lib.dap_resolve_splits(S, sms, units, Hq, Hkv, D, page_size, int(max_kv_len), 0)
+    return S, run
+
+
+def _workspace(workspace, need: int, dev):
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    return workspace, (0 if workspace is None else workspace.numel() * workspace.element_size())
 
 
 def _need(cond: bool, msg: str):
@@ -154,6 +206,12 @@ def chunk_tokens(max_kv_len, num_splits) -> int:
     return load().dap_chunk_tokens(max_kv_len, num_splits)
 
 
+def resolve_splits(num_splits, sm_count, B, Hq, Hkv, D, page_size, max_kv_len, total_kv=0) -> int:
+    """include/dap.h: dap_resolve_splits (the split count a decode call runs)."""
+    return load().dap_resolve_splits(int(num_splits), int(sm_count), int(B), int(Hq), int(Hkv), int(D),
+                                     int(page_size), int(max_kv_len), int(total_kv))
+
+
 def workspace_bytes(B, Hq, Hkv, D, num_splits) -> int:
     return load().dap_workspace_bytes(B, Hq, Hkv, D, num_splits)
 
@@ -173,7 +231,8 @@ def get_device_errors(clear: bool = True) -> int:
 def selftest_wait_timeout(stream=None) -> None:
     """include/dap.h: dap_selftest_wait_timeout (one bounded wait that runs out on purpose;
     about a second later the device error word holds DEVERR_TIMEOUT)."""
-    _check(load().dap_selftest_wait_timeout(_stream(stream)), "dap_selftest_wait_timeout")
+    dev = torch.device("cuda", torch.cuda.current_device()) if stream is None else stream.device
+    _check(load().dap_selftest_wait_timeout(_stream(stream, dev)), "dap_selftest_wait_timeout")
 
 
 # ---- decode entry points ---------------------------------------------------------------
@@ -183,37 +242,42 @@ def _bf16_3d(t, name):
           f"{name} must be a bf16 [*, *, D] tensor with unit stride in D")
 
 
-def decode_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, max_kv_len: int,
-                      scale: float | None = None, num_splits: int = 0, workspace=None, out=None,
-                      stream=None):
-    """Paged GQA decode (include/dap.h: decode_attn_paged).  num_splits 0 = balanced
-    schedule, S > 0 = per-sequence splits.  Returns ``out`` [B, Hq, D]."""
-    _bf16_3d(q, "q")
-    B, Hq, D = q.shape
+def _paged_cache(q, k_cache, v_cache, block_table, seq_lens, B):
     _need(k_cache.dtype == torch.bfloat16 and k_cache.dim() == 4 and k_cache.is_contiguous()
           and v_cache.shape == k_cache.shape and v_cache.dtype == torch.bfloat16
           and v_cache.is_contiguous(), "k_cache/v_cache must be contiguous bf16 [P, ps, Hkv, D]")
-    P, ps, Hkv, D2 = k_cache.shape
-    _need(D2 == D, "head dims differ")
+    _need(k_cache.shape[3] == q.shape[2], "head dims differ")
     _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
           and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
     _need(seq_lens.dtype == torch.int32 and seq_lens.numel() == B and seq_lens.is_contiguous(),
           "seq_lens must be contiguous int32 [B]")
+    return k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+
+
+def decode_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, max_kv_len: int,
+                      scale: float | None = None, num_splits: int = 0, total_kv: int = 0, workspace=None,
+                      out=None, stream=None):
+    """Paged GQA decode (include/dap.h: decode_attn_paged).  num_splits S > 0 = per-sequence
+    splits, 0 = the planner's S (made with the summed lengths ``total_kv`` when given),
+    SPLITS_BALANCED = the balanced persistent schedule.  Returns ``out`` [B, Hq, D]."""
+    _bf16_3d(q, "q")
+    B, Hq, D = q.shape
+    dev = _device_of("decode_attn_paged", q, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
+                     seq_lens=seq_lens, workspace=workspace, out=out)
+    P, ps, Hkv = _paged_cache(q, k_cache, v_cache, block_table, seq_lens, B)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     _bf16_3d(out, "out")
     lib = load()
-    S = int(num_splits)
-    need = lib.dap_workspace_bytes(B, Hq, Hkv, D, S)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.decode_attn_paged(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
-                               _ptr(block_table), block_table.shape[1], _ptr(seq_lens), int(max_kv_len),
-                               B, Hq, Hkv, D, float(scale), int(S), _ptr(workspace), wbytes, _ptr(out),
-                               out.stride(0), out.stride(1), _stream(stream))
+    with torch.cuda.device(dev):
+        S, run = _splits(lib, num_splits, B, Hq, Hkv, D, ps, max_kv_len, total_kv)
+        workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes(B, Hq, Hkv, D, run), dev)
+        st = lib.decode_attn_paged(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
+                                   _ptr(block_table), block_table.shape[1], _ptr(seq_lens), int(max_kv_len),
+                                   B, Hq, Hkv, D, float(scale), int(S), _ptr(workspace), wbytes, _ptr(out),
+                                   out.stride(0), out.stride(1), _stream(stream, dev))
     _check(st, "decode_attn_paged")
     return out
 
@@ -223,36 +287,36 @@ def decode_attn_paged_noalloc(q, k_cache, v_cache, block_table, seq_lens, *, max
     """Paged GQA decode without a workspace (include/dap.h: decode_attn_paged_noalloc).
 
     For callers that cannot give the library scratch memory: the split partials go to a
-    fixed 16 MiB device array inside the library.  Calls that overlap on the GPU race on
-    that array, so keep them on one stream.  Returns ``out`` [B, Hq, D]."""
+    fixed 16 MiB device array inside the library (num_splits 0 = the planner's S, lowered
+    until its partials fit).  The first call on a device reserves that array (make it at
+    start-up); calls that overlap on the GPU race on it, so keep them on one stream.
+    Returns ``out`` [B, Hq, D]."""
     _bf16_3d(q, "q")
     B, Hq, D = q.shape
-    _need(k_cache.dtype == torch.bfloat16 and k_cache.dim() == 4 and k_cache.is_contiguous()
-          and v_cache.shape == k_cache.shape and v_cache.dtype == torch.bfloat16
-          and v_cache.is_contiguous(), "k_cache/v_cache must be contiguous bf16 [P, ps, Hkv, D]")
-    P, ps, Hkv, _ = k_cache.shape
-    _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
-          and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
-    _need(seq_lens.dtype == torch.int32 and seq_lens.numel() == B and seq_lens.is_contiguous(),
-          "seq_lens must be contiguous int32 [B]")
+    dev = _device_of("decode_attn_paged_noalloc", q, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
+                     seq_lens=seq_lens, out=out)
+    P, ps, Hkv = _paged_cache(q, k_cache, v_cache, block_table, seq_lens, B)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     _bf16_3d(out, "out")
-    st = load().decode_attn_paged_noalloc(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P,
-                                          ps, _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
-                                          int(max_kv_len), B, Hq, Hkv, D, float(scale), int(num_splits),
-                                          _ptr(out), out.stride(0), out.stride(1), _stream(stream))
+    with torch.cuda.device(dev):
+        st = load().decode_attn_paged_noalloc(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P,
+                                              ps, _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                              int(max_kv_len), B, Hq, Hkv, D, float(scale), int(num_splits),
+                                              _ptr(out), out.stride(0), out.stride(1), _stream(stream, dev))
     _check(st, "decode_attn_paged_noalloc")
     return out
 
 
 def decode_attn_contig(q, k, v, seq_lens, *, max_kv_len: int, scale: float | None = None,
-                       num_splits: int = 0, workspace=None, out=None, stream=None):
-    """Contiguous-cache GQA decode (include/dap.h: decode_attn_contig); k, v [B, max_len, Hkv, D]."""
+                       num_splits: int = 0, total_kv: int = 0, workspace=None, out=None, stream=None):
+    """Contiguous-cache GQA decode (include/dap.h: decode_attn_contig); k, v [B, max_len, Hkv, D].
+    num_splits as decode_attn_paged."""
     _bf16_3d(q, "q")
     B, Hq, D = q.shape
+    dev = _device_of("decode_attn_contig", q, k=k, v=v, seq_lens=seq_lens, workspace=workspace, out=out)
     _need(k.dtype == torch.bfloat16 and k.dim() == 4 and k.is_contiguous() and v.shape == k.shape
           and v.dtype == torch.bfloat16 and v.is_contiguous() and k.shape[0] == B and k.shape[3] == D,
           "k/v must be contiguous bf16 [B, max_len, Hkv, D]")
@@ -262,18 +326,16 @@ def decode_attn_contig(q, k, v, seq_lens, *, max_kv_len: int, scale: float | Non
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     _bf16_3d(out, "out")
     lib = load()
-    S = int(num_splits)
-    need = lib.dap_workspace_bytes(B, Hq, Hkv, D, S)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.decode_attn_contig(_ptr(q), q.stride(0), q.stride(1), _ptr(k), _ptr(v), max_len,
-                                _ptr(seq_lens), int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S),
-                                _ptr(workspace), wbytes, _ptr(out), out.stride(0), out.stride(1),
-                                _stream(stream))
+    with torch.cuda.device(dev):
+        S, run = _splits(lib, num_splits, B, Hq, Hkv, D, max_len, max_kv_len, total_kv)
+        workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes(B, Hq, Hkv, D, run), dev)
+        st = lib.decode_attn_contig(_ptr(q), q.stride(0), q.stride(1), _ptr(k), _ptr(v), max_len,
+                                    _ptr(seq_lens), int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S),
+                                    _ptr(workspace), wbytes, _ptr(out), out.stride(0), out.stride(1),
+                                    _stream(stream, dev))
     _check(st, "decode_attn_contig")
     return out
 
@@ -281,6 +343,8 @@ def decode_attn_contig(q, k, v, seq_lens, *, max_kv_len: int, scale: float | Non
 def decode_attn_paged_fp8(q, kv_cache, inv_scale, slot_idx, lens, *, scale: float | None = None,
                           out=None, stream=None):
     """fp8 sliding-window latent decode, K = V (include/dap.h: decode_attn_paged_fp8)."""
+    dev = _device_of("decode_attn_paged_fp8", q, kv_cache=kv_cache, inv_scale=inv_scale, slot_idx=slot_idx,
+                     lens=lens, out=out)
     _need(q.dtype == torch.bfloat16 and q.dim() == 3 and q.is_contiguous(), "q must be contiguous bf16 [T, NH, HD]")
     T, NH, HD = q.shape
     _need(kv_cache.dtype == torch.uint8 and kv_cache.dim() == 3 and kv_cache.is_contiguous()
@@ -294,11 +358,12 @@ def decode_attn_paged_fp8(q, kv_cache, inv_scale, slot_idx, lens, *, scale: floa
     if scale is None:
         scale = 1.0 / math.sqrt(HD)
     if out is None:
-        out = torch.empty((T, NH, HD), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((T, NH, HD), dtype=torch.bfloat16, device=dev)
     _need(out.dtype == torch.bfloat16 and out.shape == q.shape and out.is_contiguous(), "out must match q")
-    st = load().decode_attn_paged_fp8(_ptr(q), _ptr(kv_cache), _ptr(inv_scale), _ptr(slot_idx), _ptr(lens),
-                                      T, NH, HD, slot_idx.shape[1], NB, bs, float(scale), _ptr(out),
-                                      _stream(stream))
+    with torch.cuda.device(dev):
+        st = load().decode_attn_paged_fp8(_ptr(q), _ptr(kv_cache), _ptr(inv_scale), _ptr(slot_idx), _ptr(lens),
+                                          T, NH, HD, slot_idx.shape[1], NB, bs, float(scale), _ptr(out),
+                                          _stream(stream, dev))
     _check(st, "decode_attn_paged_fp8")
     return out
 
@@ -308,38 +373,28 @@ def decode_attn_paged_masked(q, k_cache, v_cache, block_table, seq_lens, mask, *
                              out=None, stream=None):
     """Masked paged GQA decode (include/dap.h: decode_attn_paged_masked): mask [B, >=
     max_kv_len] bool/uint8, nonzero = keep, rows 16-byte strided.  num_splits 0 = the
-    planner's choice, resolved here so the workspace can be sized.  Returns ``out``."""
+    planner's choice (made with ``total_kv`` when given).  Returns ``out``."""
     _bf16_3d(q, "q")
     B, Hq, D = q.shape
-    _need(k_cache.dtype == torch.bfloat16 and k_cache.dim() == 4 and k_cache.is_contiguous()
-          and v_cache.shape == k_cache.shape and v_cache.dtype == torch.bfloat16
-          and v_cache.is_contiguous(), "k_cache/v_cache must be contiguous bf16 [P, ps, Hkv, D]")
-    P, ps, Hkv, D2 = k_cache.shape
-    _need(D2 == D, "head dims differ")
-    _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
-          and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
-    _need(seq_lens.dtype == torch.int32 and seq_lens.numel() == B and seq_lens.is_contiguous(),
-          "seq_lens must be contiguous int32 [B]")
+    dev = _device_of("decode_attn_paged_masked", q, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
+                     seq_lens=seq_lens, mask=mask, workspace=workspace, out=out)
+    P, ps, Hkv = _paged_cache(q, k_cache, v_cache, block_table, seq_lens, B)
     mask = _mask(mask, B, int(max_kv_len))
     _need(mask is not None, "mask is required")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     _bf16_3d(out, "out")
     lib = load()
-    S = int(num_splits)
-    if S == 0 and B > 0:
-        S = lib.dap_plan_splits(lib.dap_device_sm_count(), B, Hq, Hkv, D, ps, int(max_kv_len), int(total_kv))
-    need = lib.dap_workspace_bytes(B, Hq, Hkv, D, S) if S >= 2 else 0
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.decode_attn_paged_masked(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
-                                      _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(mask),
-                                      mask.stride(0), int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S),
-                                      _ptr(workspace), wbytes, _ptr(out), out.stride(0), out.stride(1),
-                                      _stream(stream))
+    with torch.cuda.device(dev):
+        S, run = _splits(lib, num_splits, B, Hq, Hkv, D, ps, max_kv_len, total_kv)
+        workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes(B, Hq, Hkv, D, run), dev)
+        st = lib.decode_attn_paged_masked(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
+                                          _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(mask),
+                                          mask.stride(0), int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S),
+                                          _ptr(workspace), wbytes, _ptr(out), out.stride(0), out.stride(1),
+                                          _stream(stream, dev))
     _check(st, "decode_attn_paged_masked")
     return out
 
@@ -361,10 +416,12 @@ def decode_attn_paged_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, 
                             scale: float | None = None, num_splits: int = 0, total_kv: int = 0, workspace=None,
                             out=None, stream=None):
     """Paged GQA decode over an e4m3 K/V cache (include/dap.h: decode_attn_paged_fp8kv).
-    num_splits 0 = the planner's choice (given the host-known sum of seq_lens ``total_kv``
-    if any), resolved here so the workspace can be sized.  Returns ``out`` [B, Hq, D]."""
+    num_splits 0 = the planner's choice (made with the host-known sum of seq_lens
+    ``total_kv`` when given).  Returns ``out`` [B, Hq, D]."""
     _bf16_3d(q, "q")
     B, Hq, D = q.shape
+    dev = _device_of("decode_attn_paged_fp8kv", q, k_codes=k_codes, v_codes=v_codes, k_scale=k_scale,
+                     v_scale=v_scale, block_table=block_table, seq_lens=seq_lens, workspace=workspace, out=out)
     P, ps, Hkv, D2 = _fp8kv_cache(k_codes, v_codes, k_scale, v_scale)
     _need(D2 == D, "head dims differ")
     _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
@@ -374,20 +431,17 @@ def decode_attn_paged_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, 
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     _bf16_3d(out, "out")
     lib = load()
-    S = int(num_splits)
-    if S == 0 and B > 0:
-        S = lib.dap_plan_splits(lib.dap_device_sm_count(), B, Hq, Hkv, D, ps, int(max_kv_len), int(total_kv))
-    need = lib.dap_workspace_bytes(B, Hq, Hkv, D, S) if S >= 2 else 0
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.decode_attn_paged_fp8kv(_ptr(q), q.stride(0), q.stride(1), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
-                                     _ptr(v_scale), P, ps, _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
-                                     int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S), _ptr(workspace), wbytes,
-                                     _ptr(out), out.stride(0), out.stride(1), _stream(stream))
+    with torch.cuda.device(dev):
+        S, run = _splits(lib, num_splits, B, Hq, Hkv, D, ps, max_kv_len, total_kv)
+        workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes(B, Hq, Hkv, D, run), dev)
+        st = lib.decode_attn_paged_fp8kv(_ptr(q), q.stride(0), q.stride(1), _ptr(k_codes), _ptr(v_codes),
+                                         _ptr(k_scale), _ptr(v_scale), P, ps, _ptr(block_table), block_table.shape[1],
+                                         _ptr(seq_lens), int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S),
+                                         _ptr(workspace), wbytes, _ptr(out), out.stride(0), out.stride(1),
+                                         _stream(stream, dev))
     _check(st, "decode_attn_paged_fp8kv")
     return out
 
@@ -447,43 +501,33 @@ def decode_attn_paged_multi(q, k_cache, v_cache, block_table, seq_lens, plan: Mu
                             workspace=None, out=None, stream=None):
     """Multi-token causal decode over a paged cache (include/dap.h: decode_attn_paged_multi).
     q [total_q, Hq, D] holds the new tokens of all sequences back to back; ``plan`` is the
-    MultiPlan of their counts.  num_splits 0 = the planner's choice (dap_plan_splits over the
-    plan's tiles, given the host-known sum of seq_lens ``total_kv`` if any), resolved here so
-    the workspace can be sized.  Returns ``out`` [total_q, Hq, D]."""
+    MultiPlan of their counts.  num_splits 0 = the planner's choice over the plan's tiles
+    (made with the host-known sum of seq_lens ``total_kv`` when given).  Returns ``out``
+    [total_q, Hq, D]."""
     _bf16_3d(q, "q")
     total_q, Hq, D = q.shape
     _need(total_q == plan.total_q, "q rows differ from the plan's token count")
-    _need(k_cache.dtype == torch.bfloat16 and k_cache.dim() == 4 and k_cache.is_contiguous()
-          and v_cache.shape == k_cache.shape and v_cache.dtype == torch.bfloat16
-          and v_cache.is_contiguous(), "k_cache/v_cache must be contiguous bf16 [P, ps, Hkv, D]")
-    P, ps, Hkv, D2 = k_cache.shape
-    _need(D2 == D, "head dims differ")
+    dev = _device_of("decode_attn_paged_multi", q, k_cache=k_cache, v_cache=v_cache, block_table=block_table,
+                     seq_lens=seq_lens, qo_indptr=plan.qo_indptr, tile_batch=plan.tile_batch,
+                     tile_index=plan.tile_index, mask=mask, workspace=workspace, out=out)
     B = plan.B
-    _need(block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.is_contiguous()
-          and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
-    _need(seq_lens.dtype == torch.int32 and seq_lens.numel() == B and seq_lens.is_contiguous(),
-          "seq_lens must be contiguous int32 [B]")
+    P, ps, Hkv = _paged_cache(q, k_cache, v_cache, block_table, seq_lens, B)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty((total_q, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((total_q, Hq, D), dtype=torch.bfloat16, device=dev)
     _bf16_3d(out, "out")
     lib = load()
-    S = int(num_splits)
-    if S == 0 and plan.num_tiles > 0:
-        S = lib.dap_plan_splits(lib.dap_device_sm_count(), plan.num_tiles, Hq, Hkv, D, ps, int(max_kv_len),
-                                int(total_kv))
-    need = lib.dap_workspace_bytes_multi(total_q, Hq, D, S)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     mask = _mask(mask, total_q, int(max_kv_len))
-    st = lib.decode_attn_paged_multi(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
-                                     _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
-                                     _ptr(plan.qo_indptr), _ptr(plan.tile_batch), _ptr(plan.tile_index),
-                                     plan.num_tiles, total_q, _ptr(mask), 0 if mask is None else mask.stride(0),
-                                     int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S), _ptr(workspace), wbytes,
-                                     _ptr(out), out.stride(0), out.stride(1), _stream(stream))
+    with torch.cuda.device(dev):
+        S, run = _splits(lib, num_splits, max(plan.num_tiles, 0), Hq, Hkv, D, ps, max_kv_len, total_kv)
+        workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes_multi(total_q, Hq, D, run), dev)
+        st = lib.decode_attn_paged_multi(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
+                                         _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                         _ptr(plan.qo_indptr), _ptr(plan.tile_batch), _ptr(plan.tile_index),
+                                         plan.num_tiles, total_q, _ptr(mask), 0 if mask is None else mask.stride(0),
+                                         int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S), _ptr(workspace),
+                                         wbytes, _ptr(out), out.stride(0), out.stride(1), _stream(stream, dev))
     _check(st, "decode_attn_paged_multi")
     return out
 
@@ -493,6 +537,8 @@ def decode_attn_paged_multi(q, k_cache, v_cache, block_table, seq_lens, plan: Mu
 def kv_append_paged(k_new, v_new, k_cache, v_cache, block_table, positions, *, stream=None):
     """Write each sequence's new K/V rows [B, Hkv, D] at positions[b] (include/dap.h:
     kv_append_paged).  Returns (k_cache, v_cache), updated in place."""
+    dev = _device_of("kv_append_paged", k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache,
+                     block_table=block_table, positions=positions)
     _need(k_new.dtype == torch.bfloat16 and k_new.dim() == 3 and k_new.is_contiguous()
           and v_new.shape == k_new.shape and v_new.dtype == torch.bfloat16 and v_new.is_contiguous(),
           "k_new/v_new must be contiguous bf16 [B, Hkv, D]")
@@ -504,9 +550,10 @@ def kv_append_paged(k_new, v_new, k_cache, v_cache, block_table, positions, *, s
           and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
     _need(positions.dtype == torch.int32 and positions.numel() == B and positions.is_contiguous(),
           "positions must be contiguous int32 [B]")
-    st = load().kv_append_paged(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
-                                k_cache.shape[1], _ptr(block_table), block_table.shape[1], _ptr(positions), B, Hkv,
-                                D, _stream(stream))
+    with torch.cuda.device(dev):
+        st = load().kv_append_paged(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                    k_cache.shape[1], _ptr(block_table), block_table.shape[1], _ptr(positions), B,
+                                    Hkv, D, _stream(stream, dev))
     _check(st, "kv_append_paged")
     return k_cache, v_cache
 
@@ -514,6 +561,7 @@ def kv_append_paged(k_new, v_new, k_cache, v_cache, block_table, positions, *, s
 def kv_append_fp8(rows, kv_cache, inv_scale, slots, *, stream=None):
     """Quantise rows [T, HD] into their fp8 cache slots (include/dap.h: kv_append_fp8).
     Returns (kv_cache, inv_scale), updated in place."""
+    dev = _device_of("kv_append_fp8", rows, kv_cache=kv_cache, inv_scale=inv_scale, slots=slots)
     _need(rows.dtype == torch.bfloat16 and rows.dim() == 2 and rows.is_contiguous(), "rows must be bf16 [T, HD]")
     T, HD = rows.shape
     _need(kv_cache.dtype == torch.uint8 and kv_cache.dim() == 3 and kv_cache.is_contiguous()
@@ -522,8 +570,9 @@ def kv_append_fp8(rows, kv_cache, inv_scale, slots, *, stream=None):
     _need(inv_scale.dtype == torch.bfloat16 and inv_scale.is_contiguous() and inv_scale.numel() >= NB * bs,
           "inv_scale must be contiguous bf16 with one entry per slot")
     _need(slots.dtype == torch.int64 and slots.numel() == T and slots.is_contiguous(), "slots must be int64 [T]")
-    st = load().kv_append_fp8(_ptr(rows), _ptr(kv_cache), _ptr(inv_scale), _ptr(slots), T, HD, NB, bs,
-                              _stream(stream))
+    with torch.cuda.device(dev):
+        st = load().kv_append_fp8(_ptr(rows), _ptr(kv_cache), _ptr(inv_scale), _ptr(slots), T, HD, NB, bs,
+                                  _stream(stream, dev))
     _check(st, "kv_append_fp8")
     return kv_cache, inv_scale
 
@@ -532,6 +581,8 @@ def kv_append_paged_fp8(k_new, v_new, k_codes, v_codes, k_scale, v_scale, block_
     """Quantise each sequence's new K/V rows [B, Hkv, D] into the e4m3 GQA cache at
     positions[b] (include/dap.h: kv_append_paged_fp8).  Returns the four cache arrays,
     updated in place."""
+    dev = _device_of("kv_append_paged_fp8", k_new, v_new=v_new, k_codes=k_codes, v_codes=v_codes, k_scale=k_scale,
+                     v_scale=v_scale, block_table=block_table, positions=positions)
     _need(k_new.dtype == torch.bfloat16 and k_new.dim() == 3 and k_new.is_contiguous()
           and v_new.shape == k_new.shape and v_new.dtype == torch.bfloat16 and v_new.is_contiguous(),
           "k_new/v_new must be contiguous bf16 [B, Hkv, D]")
@@ -542,8 +593,9 @@ def kv_append_paged_fp8(k_new, v_new, k_codes, v_codes, k_scale, v_scale, block_
           and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
     _need(positions.dtype == torch.int32 and positions.numel() == B and positions.is_contiguous(),
           "positions must be contiguous int32 [B]")
-    st = load().kv_append_paged_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
-                                    _ptr(v_scale), P, ps, _ptr(block_table), block_table.shape[1], _ptr(positions), B,
-                                    Hkv, D, _stream(stream))
+    with torch.cuda.device(dev):
+        st = load().kv_append_paged_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
+                                        _ptr(v_scale), P, ps, _ptr(block_table), block_table.shape[1],
+                                        _ptr(positions), B, Hkv, D, _stream(stream, dev))
     _check(st, "kv_append_paged_fp8")
     return k_codes, v_codes, k_scale, v_scale

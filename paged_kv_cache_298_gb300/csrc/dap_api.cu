@@ -40,14 +40,16 @@ long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 
 bool supported_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8; }
 
-// Shared checks of the two bf16 decode entry points.
+// Shared checks of the decode entry points.  `balanced_ok`: the entry point has the
+// balanced schedule, so num_splits may be DAP_SPLITS_BALANCED.
 dap_status check_common(const void *q, long long q_sb, long long q_sh, const int32_t *seq_lens,
                         int max_kv_len, int B, int Hq, int Hkv, int D, float scale, int num_splits,
-                        const void *out, long long o_sb, long long o_sh) {
-    if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || max_kv_len < 0 || num_splits < 0 ||
+                        const void *out, long long o_sb, long long o_sh, bool balanced_ok = false) {
+    if (B < 0 || Hq < 1 || Hkv < 1 || D < 1 || max_kv_len < 0 || num_splits < DAP_SPLITS_BALANCED ||
         num_splits > 65536 || Hq % Hkv != 0 || !isfinite(scale) || q_sb < 0 || q_sh < 0 ||
         o_sb < 0 || o_sh < 0)
         return DAP_ERR_SHAPE;
+    if (num_splits == DAP_SPLITS_BALANCED && !balanced_ok) return DAP_ERR_UNSUPPORTED;
     if (B == 0) return DAP_OK;
     if ((Hq > 1 && (q_sh == 0 || o_sh == 0)) || (B > 1 && (q_sb == 0 || o_sb == 0))) return DAP_ERR_SHAPE;
     if (!q || !seq_lens || !out) return DAP_ERR_NULL;
@@ -58,28 +60,32 @@ dap_status check_common(const void *q, long long q_sb, long long q_sh, const int
     return DAP_OK;
 }
 
-dap_status resolve_splits(int B, int Hq, int Hkv, int D, int page_size, int max_kv_len, int num_splits,
-                          void *workspace, size_t workspace_bytes, int *S_out, int *chunk_out) {
-    (void)page_size;
-    int S = num_splits;
-    if (S == 0 && B <= kMaxBalancedBatch) {  // balanced persistent schedule
-        const size_t need = dap_workspace_bytes(B, Hq, Hkv, D, 0);
+// The split count of a call (dap_resolve_splits on the current device) and its chunk, after
+// checking the workspace against it.  `units` is the number of rows the planner schedules
+// (sequences, or the work map's tiles).  On return *S_out is 0 for the balanced schedule,
+// else the per-sequence S >= 1.
+dap_status resolve_splits(int units, int rows, int Hq, int Hkv, int D, int page_size, int max_kv_len, int num_splits,
+                          void *workspace, size_t workspace_bytes, bool multi, int *S_out, int *chunk_out) {
+    int sms = 0;
+    if (num_splits == 0) {
+        sms = dap_device_sm_count();
+        if (sms <= 0) return DAP_ERR_CUDA;
+    }
+    const int S = dap_resolve_splits(num_splits, sms, units, Hq, Hkv, D, page_size, max_kv_len, 0);
+    if (S == 0) return DAP_ERR_SHAPE;
+    if (S == DAP_SPLITS_BALANCED) {
+        const size_t need = dap_workspace_bytes(rows, Hq, Hkv, D, DAP_SPLITS_BALANCED);
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DAP_ERR_WORKSPACE;
         *S_out = 0;
         *chunk_out = 0;
         return DAP_OK;
     }
-    if (S == 0) S = 1;  // so many sequences that one CTA per (sequence, kv head) fills the GPU
-    const int chunk = dap_chunk_tokens(max_kv_len, S);
-    // splits that could never hold a token are dropped: S chunks must cover max_kv_len
-    const int needed = max_kv_len > 0 ? (int)ceil_div_ll(max_kv_len, chunk) : 1;
-    S = std::max(1, std::min(S, needed));
     if (S > 1) {
-        const size_t need = dap_workspace_bytes(B, Hq, Hkv, D, S);
+        const size_t need = multi ? dap_workspace_bytes_multi(rows, Hq, D, S) : dap_workspace_bytes(rows, Hq, Hkv, D, S);
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DAP_ERR_WORKSPACE;
     }
     *S_out = S;
-    *chunk_out = chunk;
+    *chunk_out = dap_chunk_tokens(max_kv_len, S);
     return DAP_OK;
 }
 
@@ -158,9 +164,23 @@ int dap_plan_splits(int sm_count, int B, int Hq, int Hkv, int D, int page_size, 
     return (int)std::max<long long>(1, S);
 }
 
+int dap_resolve_splits(int num_splits, int sm_count, int B, int Hq, int Hkv, int D, int page_size, int max_kv_len,
+                       long long total_kv) {
+    if (num_splits < DAP_SPLITS_BALANCED || B < 0 || Hq < 1 || Hkv < 1 || D < 1 || max_kv_len < 0) return 0;
+    if (num_splits == DAP_SPLITS_BALANCED) return B <= kMaxBalancedBatch ? DAP_SPLITS_BALANCED : 1;
+    const int S = num_splits == 0 ? dap_plan_splits(sm_count, B, Hq, Hkv, D, page_size, max_kv_len, total_kv)
+                                  : num_splits;
+    // splits that could never hold a token are dropped: S chunks must cover max_kv_len
+    const int chunk = dap_chunk_tokens(max_kv_len, S);
+    const int needed = max_kv_len > 0 ? (int)ceil_div_ll(max_kv_len, chunk) : 1;
+    return std::max(1, std::min(S, needed));
+}
+
 size_t dap_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits) {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_splits < 0 || num_splits == 1) return 0;
-    if (num_splits == 0) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || num_splits < DAP_SPLITS_BALANCED || num_splits == 0 ||
+        num_splits == 1)
+        return 0;
+    if (num_splits == DAP_SPLITS_BALANCED) {
         if (B > kMaxBalancedBatch || Hq % Hkv != 0) return 0;
         const int G = Hq / Hkv;
         const int hg = balanced_kv_heads_per_unit(D, G);
@@ -176,7 +196,7 @@ dap_status decode_attn_paged(const void *q, long long q_stride_b, long long q_st
                              int num_splits, void *workspace, size_t workspace_bytes, void *out,
                              long long out_stride_b, long long out_stride_h, void *stream) {
     dap_status st = check_common(q, q_stride_b, q_stride_h, seq_lens, max_kv_len, B, Hq, Hkv, D,
-                                 scale, num_splits, out, out_stride_b, out_stride_h);
+                                 scale, num_splits, out, out_stride_b, out_stride_h, true);
     if (st != DAP_OK || B == 0) return st;
     if (num_pages < 1 || page_size < 1 || max_pages < 1 ||
         (long long)max_kv_len > (long long)max_pages * page_size)
@@ -207,7 +227,7 @@ dap_status decode_attn_paged(const void *q, long long q_stride_b, long long q_st
     a.out = out;
     a.o_sb = out_stride_b;
     a.o_sh = out_stride_h;
-    st = resolve_splits(B, Hq, Hkv, D, page_size, max_kv_len, num_splits, workspace, workspace_bytes,
+    st = resolve_splits(B, B, Hq, Hkv, D, page_size, max_kv_len, num_splits, workspace, workspace_bytes, false,
                         &a.num_splits, &a.chunk);
     if (st != DAP_OK) return st;
     return launch_decode(a, static_cast<cudaStream_t>(stream));
@@ -219,7 +239,7 @@ dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_s
                               void *workspace, size_t workspace_bytes, void *out,
                               long long out_stride_b, long long out_stride_h, void *stream) {
     dap_status st = check_common(q, q_stride_b, q_stride_h, seq_lens, max_kv_len, B, Hq, Hkv, D,
-                                 scale, num_splits, out, out_stride_b, out_stride_h);
+                                 scale, num_splits, out, out_stride_b, out_stride_h, true);
     if (st != DAP_OK || B == 0) return st;
     if (max_len < 1 || max_kv_len > max_len) return DAP_ERR_SHAPE;
     if (!k || !v) return DAP_ERR_NULL;
@@ -247,7 +267,7 @@ dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_s
     a.out = out;
     a.o_sb = out_stride_b;
     a.o_sh = out_stride_h;
-    st = resolve_splits(B, Hq, Hkv, D, max_len, max_kv_len, num_splits, workspace, workspace_bytes,
+    st = resolve_splits(B, B, Hq, Hkv, D, max_len, max_kv_len, num_splits, workspace, workspace_bytes, false,
                         &a.num_splits, &a.chunk);
     if (st != DAP_OK) return st;
     return launch_decode(a, static_cast<cudaStream_t>(stream));
@@ -314,19 +334,10 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
         return DAP_ERR_ALIGN;
     if (page_size % 8 != 0 || !(D == 64 || D == 128)) return DAP_ERR_UNSUPPORTED;
     if ((st = check_mask(mask, mask_stride, max_kv_len)) != DAP_OK) return st;
-    int S = num_splits;
-    if (S == 0) {
-        const int sms = dap_device_sm_count();
-        if (sms <= 0) return DAP_ERR_CUDA;
-        S = dap_plan_splits(sms, num_tiles, Hq, Hkv, D, page_size, max_kv_len, 0);
-    }
-    const int chunk = dap_chunk_tokens(max_kv_len, S);
-    const int needed = max_kv_len > 0 ? (int)ceil_div_ll(max_kv_len, chunk) : 1;
-    S = std::max(1, std::min(S, needed));
-    if (S > 1) {
-        const size_t need = dap_workspace_bytes_multi(total_q, Hq, D, S);
-        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DAP_ERR_WORKSPACE;
-    }
+    int S = 0, chunk = 0;
+    if ((st = resolve_splits(num_tiles, total_q, Hq, Hkv, D, page_size, max_kv_len, num_splits, workspace,
+                             workspace_bytes, true, &S, &chunk)) != DAP_OK)
+        return st;
     DecodeArgs a = {};
     a.paged = true;
     a.q = q;
@@ -378,19 +389,10 @@ dap_status decode_attn_paged_masked(const void *q, long long q_stride_b, long lo
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table)) return DAP_ERR_ALIGN;
     if (page_size % 8 != 0 || !(D == 64 || D == 128)) return DAP_ERR_UNSUPPORTED;
     if ((st = check_mask(mask, mask_stride, max_kv_len)) != DAP_OK) return st;
-    int S = num_splits;
-    if (S == 0) {
-        const int sms = dap_device_sm_count();
-        if (sms <= 0) return DAP_ERR_CUDA;
-        S = dap_plan_splits(sms, B, Hq, Hkv, D, page_size, max_kv_len, 0);
-    }
-    const int chunk = dap_chunk_tokens(max_kv_len, S);
-    const int needed = max_kv_len > 0 ? (int)ceil_div_ll(max_kv_len, chunk) : 1;
-    S = std::max(1, std::min(S, needed));
-    if (S > 1) {
-        const size_t need = dap_workspace_bytes(B, Hq, Hkv, D, S);
-        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DAP_ERR_WORKSPACE;
-    }
+    int S = 0, chunk = 0;
+    if ((st = resolve_splits(B, B, Hq, Hkv, D, page_size, max_kv_len, num_splits, workspace, workspace_bytes, false,
+                             &S, &chunk)) != DAP_OK)
+        return st;
     DecodeArgs a = {};
     a.paged = true;
     a.q = q;
@@ -439,19 +441,10 @@ dap_status decode_attn_paged_fp8kv(const void *q, long long q_stride_b, long lon
     if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scale) || !aligned16(v_scale) ||
         !aligned4(block_table))
         return DAP_ERR_ALIGN;
-    int S = num_splits;
-    if (S == 0) {
-        const int sms = dap_device_sm_count();
-        if (sms <= 0) return DAP_ERR_CUDA;
-        S = dap_plan_splits(sms, B, Hq, Hkv, D, page_size, max_kv_len, 0);
-    }
-    const int chunk = dap_chunk_tokens(max_kv_len, S);
-    const int needed = max_kv_len > 0 ? (int)ceil_div_ll(max_kv_len, chunk) : 1;
-    S = std::max(1, std::min(S, needed));
-    if (S > 1) {
-        const size_t need = dap_workspace_bytes(B, Hq, Hkv, D, S);
-        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DAP_ERR_WORKSPACE;
-    }
+    int S = 0, chunk = 0;
+    if ((st = resolve_splits(B, B, Hq, Hkv, D, page_size, max_kv_len, num_splits, workspace, workspace_bytes, false,
+                             &S, &chunk)) != DAP_OK)
+        return st;
     DecodeArgs a = {};
     a.paged = true;
     a.q = q;

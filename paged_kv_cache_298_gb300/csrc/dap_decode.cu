@@ -1039,7 +1039,7 @@ dap_status launch_per_sequence(const DecodeArgs &a, SplitParams &p, cudaStream_t
         !encode_cache_map<C>(&mv, a.v, a.D, a.Hkv, rows, outer, R))
         return DAP_ERR_CUDA;
     auto kern = split_kernel<C, PAGED>;
-    static int occ = 0;
+    static PerDeviceOcc occ = {};
     if (prepare_kernel(kern, C::THREADS, C::SMEM, &occ) <= 0) return DAP_ERR_CUDA;
     const long long grid = (long long)a.B * (a.Hkv / C::HG) * a.num_splits;
     if (grid > 0x7FFFFFFFLL) return DAP_ERR_SHAPE;
@@ -1070,7 +1070,7 @@ dap_status launch_balanced(const DecodeArgs &a, SplitParams &p, cudaStream_t str
         !encode_cache_map<C>(&mv, a.v, a.D, a.Hkv, rows, outer, R) || !encode_q_map(&mq, a, C::HPU))
         return DAP_ERR_CUDA;
     auto kern = balanced_kernel<C, PAGED>;
-    static int occ = 0;
+    static PerDeviceOcc occ = {};
     const int per_sm = prepare_kernel(kern, C::THREADS, C::SMEM, &occ);
     const int sms = dap_device_sm_count();
     if (per_sm <= 0 || sms <= 0) return DAP_ERR_CUDA;

@@ -550,7 +550,7 @@ dap_status launch_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
         !encode_factors(&mvs, a.v_scale, a.Hkv, a.page_size, a.num_pages, R, HG))
         return DAP_ERR_CUDA;
     auto kern = fp8kv_kernel<C>;
-    static int occ = 0;
+    static PerDeviceOcc occ = {};
     if (prepare_kernel(kern, C::THREADS, C::SMEM, &occ) <= 0) return DAP_ERR_CUDA;
     const long long grid = (long long)a.B * (a.Hkv / HG) * a.num_splits;
     if (grid > 0x7FFFFFFFLL) return DAP_ERR_SHAPE;

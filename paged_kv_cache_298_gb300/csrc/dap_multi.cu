@@ -578,7 +578,7 @@ dap_status launch_multi(const DecodeArgs &a, SplitParams &p, cudaStream_t stream
         (MASK && !encode_mask_map(&mm, a.mask, a.mask_stride, a.total_q, C::QT)))
         return DAP_ERR_CUDA;
     auto kern = multi_kernel<C>;
-    static int occ = 0;
+    static PerDeviceOcc occ = {};
     if (prepare_kernel(kern, C::THREADS, C::SMEM, &occ) <= 0) return DAP_ERR_CUDA;
     const long long grid = (long long)a.num_tiles * a.Hkv * a.num_splits;
     if (grid > 0x7FFFFFFFLL) return DAP_ERR_SHAPE;

@@ -306,15 +306,24 @@ int gcd_int(int x, int y) {
 
 std::mutex g_attr_mu;
 
-// Raise the dynamic shared-memory limit of `kern` once, and return its resident CTAs per SM.
+// Function attributes belong to a device's context, so a kernel is prepared once per device.
+constexpr int kMaxDevices = 64;
+struct PerDeviceOcc {
+    int occ[kMaxDevices];
+};
+
+// Raise the dynamic shared-memory limit of `kern` once per device (the current one), and
+// return its resident CTAs per SM there (0 on failure).
 template <class K>
-int prepare_kernel(K kern, int threads, int smem, int *cached_occ) {
+int prepare_kernel(K kern, int threads, int smem, PerDeviceOcc *cache) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     std::lock_guard<std::mutex> lock(g_attr_mu);
-    if (*cached_occ > 0) return *cached_occ;
+    if (cache->occ[dev] > 0) return cache->occ[dev];
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem) != cudaSuccess) return 0;
-    *cached_occ = occ;
+    cache->occ[dev] = occ;
     return occ;
 }
 

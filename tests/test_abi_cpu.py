@@ -68,11 +68,40 @@ def test_workspace_bytes():
     n = binding.workspace_bytes(16, 32, 8, 128, 8)
     assert n >= 16 * 8 * 32 * (128 + 2) * 4 and n % 256 == 0
     # balanced schedule: two partial slots per persistent CTA (up to 1024) + unit records
-    bal = binding.workspace_bytes(128, 32, 8, 128, 0)
+    bal = binding.workspace_bytes(128, 32, 8, 128, binding.SPLITS_BALANCED)
     assert bal >= 2 * 1024 * 4 * (128 + 2) * 4 + 128 * 8 * 8
     assert bal < 8 << 20
-    assert binding.workspace_bytes(5000, 32, 8, 128, 0) == 0      # huge batches run one CTA per unit
-    assert binding.workspace_bytes(16, 32, 8, 128, -1) == 0
+    assert binding.workspace_bytes(5000, 32, 8, 128, binding.SPLITS_BALANCED) == 0  # one CTA per unit
+    assert binding.workspace_bytes(16, 32, 8, 128, 0) == 0       # 0 is not a split count
+    assert binding.workspace_bytes(16, 32, 8, 128, -2) == 0
+
+
+def test_resolve_splits_is_the_planner_for_zero_and_clamps_explicit_counts():
+    """num_splits = 0 means the planner's S on every decode entry point; explicit counts are
+    kept unless more chunks than the longest sequence can fill; -1 selects the balanced
+    schedule (one CTA per unit past 4096 sequences); anything below is invalid."""
+    cases = [(152, 1, 64, 8, 128, 64, 32768, 32768), (152, 4, 64, 8, 128, 64, 32768, 4 * 32768),
+             (152, 16, 32, 8, 128, 16, 2048, 16 * 2048), (152, 128, 32, 8, 128, 16, 4096, 278000),
+             (152, 3, 8, 2, 64, 16, 100, 0), (152, 2048, 8, 2, 64, 16, 40, 0), (132, 7, 16, 4, 256, 8, 999, 0)]
+    def clamp(S, L):   # splits beyond the chunks the longest sequence fills are dropped
+        chunk = binding.chunk_tokens(L, S)
+        return max(1, min(S, -(-L // chunk) if L > 0 else 1))
+
+    for sms, B, Hq, Hkv, D, ps, L, tot in cases:
+        plan = binding.plan_splits(sms, B, Hq, Hkv, D, ps, L, tot)
+        assert binding.resolve_splits(0, sms, B, Hq, Hkv, D, ps, L, tot) == clamp(plan, L)
+        for S in (1, 2, 7, 64, 1000):
+            r = binding.resolve_splits(S, sms, B, Hq, Hkv, D, ps, L, tot)
+            assert r == clamp(S, L)
+            assert 1 <= r <= S and (r == S or r * binding.chunk_tokens(L, S) >= L)
+    # long context B=1: the planner's 38 splits of 896-token chunks leave the 38th empty
+    assert binding.plan_splits(152, 1, 64, 8, 128, 64, 32768, 32768) == 38
+    assert binding.resolve_splits(0, 152, 1, 64, 8, 128, 64, 32768, 32768) == 37
+    for sms, B, Hq, Hkv, D, ps, L, tot in cases:
+        assert binding.resolve_splits(-1, sms, B, Hq, Hkv, D, ps, L, tot) == binding.SPLITS_BALANCED
+    assert binding.resolve_splits(-1, 152, 5000, 32, 8, 128, 16, 100, 0) == 1
+    assert binding.resolve_splits(-2, 152, 4, 32, 8, 128, 16, 100, 0) == 0
+    assert binding.resolve_splits(3, 152, 4, 32, 8, 128, 16, 0, 0) == 1     # nothing to split
 
 
 FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails validation first
@@ -91,7 +120,7 @@ def paged_call(lib, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(B=-1), 2), (dict(Hq=30), 2), (dict(Hkv=0), 2), (dict(maxlen=-1), 2),
-    (dict(maxlen=8 * 16 + 1), 2), (dict(ps=0), 2), (dict(P=0), 2), (dict(S=-1), 2),
+    (dict(maxlen=8 * 16 + 1), 2), (dict(ps=0), 2), (dict(P=0), 2), (dict(S=-2), 2),
     (dict(scale=float("nan")), 2), (dict(qsh=-8), 2),
     (dict(q=None), 1), (dict(out=None), 1), (dict(k=None), 1), (dict(table=None), 1),
     (dict(lens=None), 1),
@@ -100,7 +129,7 @@ def paged_call(lib, **kw):
     (dict(D=32, qsb=32 * 32, qsh=32, osb=32 * 32, osh=32, ps=4, maxlen=30), 3),
     (dict(q=ctypes.c_void_p((1 << 20) + 8)), 5), (dict(qsh=130), 5), (dict(osb=4100), 5),
     (dict(k=ctypes.c_void_p((1 << 20) + 4)), 5),
-    (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=16), 4), (dict(S=0), 4),
+    (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=16), 4), (dict(S=-1), 4), (dict(S=-1, ws=FAKE, wsb=4096), 4),
     (dict(qsh=0), 2), (dict(osb=0), 2),
 ])
 def test_paged_validation(lib, kw, status):
@@ -206,7 +235,7 @@ def multi_call(lib, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(totq=-1), 2), (dict(ntiles=0), 2), (dict(totq=0), 2), (dict(ntiles=9), 2), (dict(B=0), 2),
-    (dict(Hq=30), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(S=-1), 2), (dict(qsh=0), 2),
+    (dict(Hq=30), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(S=-2), 2), (dict(S=-1), 3), (dict(qsh=0), 2),
     (dict(q=None), 1), (dict(qi=None), 1), (dict(tb=None), 1), (dict(ti=None), 1), (dict(table=None), 1),
     (dict(D=96), 3), (dict(ps=12, maxlen=90), 3), (dict(Hq=64, Hkv=4), 3),
     (dict(D=256, qst=32 * 256, qsh=256, ost=32 * 256, osh=256), 3),
@@ -236,7 +265,8 @@ def fp8kv_call(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(B=-1), 2), (dict(Hq=30), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(S=-1), 2), (dict(P=0), 2),
+    (dict(B=-1), 2), (dict(Hq=30), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(S=-2), 2), (dict(S=-1), 3),
+    (dict(P=0), 2),
     (dict(kc=None), 1), (dict(ks=None), 1), (dict(vs=None), 1), (dict(table=None), 1), (dict(q=None), 1),
     (dict(D=64, qsb=32 * 64, qsh=64, osb=32 * 64, osh=64), 3), (dict(ps=12, maxlen=90), 3), (dict(Hq=64, Hkv=4), 3),
     (dict(ks=ctypes.c_void_p((1 << 20) + 8)), 5), (dict(kc=ctypes.c_void_p((1 << 20) + 4)), 5),
@@ -277,7 +307,7 @@ def masked_call(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(B=-1), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(mst=96), 2), (dict(S=-1), 2),
+    (dict(B=-1), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(mst=96), 2), (dict(S=-2), 2), (dict(S=-1), 3),
     (dict(mask=None), 1), (dict(q=None), 1), (dict(table=None), 1),
     (dict(D=96), 3), (dict(ps=12, maxlen=90), 3), (dict(D=32, qsb=32 * 32, qsh=32, osb=32 * 32, osh=32), 3),
     (dict(mst=120), 5), (dict(mask=ctypes.c_void_p((1 << 20) + 8)), 5),
@@ -289,3 +319,51 @@ def test_masked_validation(lib, kw, status):
 
 def test_masked_empty_batch_is_a_no_op(lib):
     assert masked_call(lib, B=0, q=None, out=None, lens=None, mask=None, k=None, table=None) == 0
+
+
+# ---- the binding refuses tensors the kernels could not use ---------------------------------
+
+def test_binding_refuses_cpu_tensors_before_any_launch():
+    """A CPU tensor would reach the kernels as a host address; the binding raises DapError
+    (status None) before the library is called."""
+    import torch
+    from paged_kv_cache_298_gb300 import inputs
+    case = inputs.tiny_paged()                      # every tensor on the CPU
+    kw = dict(max_kv_len=case.max_kv_len, num_splits=1)
+    with pytest.raises(binding.DapError) as e:
+        binding.decode_attn_paged(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, **kw)
+    assert e.value.status is None and "CUDA" in str(e.value)
+    with pytest.raises(binding.DapError):
+        binding.decode_attn_paged_noalloc(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                                          max_kv_len=case.max_kv_len)
+    f = inputs.make_fp8_case(1, 128, 512, 2, 16, 8, 5)
+    with pytest.raises(binding.DapError):
+        binding.decode_attn_paged_fp8(f.q, f.kv_cache, f.inv_scale, f.indices, f.lens)
+    with pytest.raises(binding.DapError):
+        binding.kv_append_paged(case.q[:, :2], case.q[:, :2], case.k_cache, case.v_cache, case.block_table,
+                                case.seq_lens)
+    del torch
+
+
+class _Fake:
+    """Stands in for a tensor or stream on a given device (only what the binding's device
+    rule reads), so the rule can be checked without a GPU."""
+
+    def __init__(self, kind, index=None):
+        import torch
+        self.is_cuda = kind == "cuda"
+        self.device = torch.device(kind, index) if index is not None else torch.device(kind)
+
+
+def test_binding_refuses_tensors_and_streams_on_another_device():
+    import torch
+    dev = binding._device_of("call", _Fake("cuda", 0), k=_Fake("cuda", 0), workspace=None)
+    assert dev == torch.device("cuda", 0)
+    with pytest.raises(binding.DapError) as e:
+        binding._device_of("call", _Fake("cuda", 0), k=_Fake("cuda", 0), v=_Fake("cuda", 1))
+    assert e.value.status is None and "v is on cuda:1" in str(e.value)
+    with pytest.raises(binding.DapError) as e:
+        binding._device_of("call", _Fake("cuda", 0), out=_Fake("cpu"))
+    assert "out is not a CUDA tensor" in str(e.value)
+    with pytest.raises(binding.DapError):
+        binding._stream(_Fake("cuda", 1), torch.device("cuda", 0))

@@ -16,6 +16,7 @@ from paged_kv_cache_298_gb300 import binding, inputs
 pytestmark = pytest.mark.gpu
 
 ATOL = RTOL = 1e-2
+BAL = binding.SPLITS_BALANCED
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
@@ -50,7 +51,7 @@ def _clean_errors():
 def test_tiny_workload_all_split_counts():
     case = inputs.tiny_paged().to("cuda")
     ref = oracle_paged(case)
-    for S in [0, 1, 2, 3, 4]:
+    for S in [BAL, 0, 1, 2, 3, 4]:
         assert_close(gpu_paged(case, S), ref, f"S={S}")
     assert binding.get_device_errors() == 0
 
@@ -79,7 +80,7 @@ def test_paged_parity(shape):
     B, Hq, Hkv, D, ps, lens = shape
     case = inputs.make_paged_case(B, Hq, Hkv, D, ps, lens, 1000 + sum(lens)).to("cuda")
     ref = oracle_paged(case)
-    for S in [0, 1, 2, 5, 20]:    # 20: more than 16 splits, the CTA-per-row combine
+    for S in [BAL, 0, 1, 2, 5, 20]:    # 20: more than 16 splits, the CTA-per-row combine
         assert_close(gpu_paged(case, S), ref, f"S={S}")
     assert binding.get_device_errors() == 0
 
@@ -88,7 +89,7 @@ def test_contiguous_matches_oracle_and_paged_bit_for_bit():
     case = inputs.make_paged_case(4, 32, 8, 128, 16, [300, 1, 64, 129], 77).to("cuda")
     k, v = inputs.logical_kv(case, max_len=320)
     ref = oracle.decode_contig(bits(case.q), bits(k), bits(v), case.seq_lens.cpu().numpy(), case.scale)
-    for S in [0, 1, 3]:
+    for S in [BAL, 0, 1, 3]:
         c = binding.decode_attn_contig(case.q, k, v, case.seq_lens, max_kv_len=case.max_kv_len,
                                        num_splits=S)
         assert_close(c, ref, f"contig S={S}")
@@ -102,7 +103,7 @@ def test_page_permutation_is_bit_identical():
     moved = inputs.PagedCase(case.q, case.k_cache[perm].contiguous(), case.v_cache[perm].contiguous(),
                              inv[case.block_table.long()].to(torch.int32).contiguous(), case.seq_lens,
                              case.page_size, case.scale)
-    for S in [0, 1, 4, 9]:
+    for S in [BAL, 0, 1, 4, 9]:
         assert torch.equal(gpu_paged(case, S), gpu_paged(moved, S)), f"S={S}"
 
 
@@ -126,7 +127,7 @@ def test_balanced_schedule_many_short_and_empty_sequences():
     lens[299] = 0
     case = inputs.make_paged_case(300, 8, 2, 64, 16, lens, 84).to("cuda")
     ref = oracle_paged(case)
-    assert_close(gpu_paged(case, 0), ref, "balanced B=300")
+    assert_close(gpu_paged(case, BAL), ref, "balanced B=300")
     assert binding.get_device_errors() == 0
 
 
@@ -135,7 +136,7 @@ def test_balanced_schedule_fewer_tiles_than_ctas():
     # CTAs get an empty range, and the combine must skip them
     case = inputs.make_paged_case(2, 16, 2, 128, 16, [40, 20], 85, max_pages=64).to("cuda")
     out = binding.decode_attn_paged(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
-                                    max_kv_len=1000, num_splits=0)
+                                    max_kv_len=1000, num_splits=BAL)
     assert_close(out, oracle_paged(case), "tiny balanced")
     assert binding.get_device_errors() == 0
 
@@ -143,7 +144,7 @@ def test_balanced_schedule_fewer_tiles_than_ctas():
 @pytest.mark.parametrize("max_kv_len", [0, 64])
 def test_every_sequence_empty_gives_zero_rows(max_kv_len):
     case = inputs.make_paged_case(4, 16, 4, 128, 16, [0, 0, 0, 0], 86, max_pages=4).to("cuda")
-    for S in [0, 1, 3]:
+    for S in [BAL, 0, 1, 3]:
         out = torch.full_like(case.q, 5.0)
         binding.decode_attn_paged(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
                                   max_kv_len=max_kv_len, num_splits=S, out=out)
@@ -168,7 +169,7 @@ def test_strided_q_and_out_and_garbage_workspace():
     q = qbig[:, :, 128:256]                      # stride_h = 384
     obig = torch.full((3, 16, 2 * 128), 7.0, dtype=torch.bfloat16, device="cuda")
     out = obig[:, :, :128]
-    for S in [0, 4]:
+    for S in [BAL, 4]:
         ws = torch.full((binding.workspace_bytes(3, 16, 4, 128, S),), 0xFF, dtype=torch.uint8, device="cuda")
         binding.decode_attn_paged(q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
                                   max_kv_len=case.max_kv_len, num_splits=S, workspace=ws, out=out)
@@ -178,9 +179,8 @@ def test_strided_q_and_out_and_garbage_workspace():
 
 def test_repeat_runs_are_identical():
     case = inputs.make_paged_case(4, 32, 8, 128, 16, [1000, 2000, 10, 555], 81).to("cuda")
-    a = gpu_paged(case, 0)
-    b = gpu_paged(case, 0)
-    assert torch.equal(a, b)
+    for S in [BAL, 0]:
+        assert torch.equal(gpu_paged(case, S), gpu_paged(case, S))
 
 
 def test_seq_len_above_bound_is_flagged_and_clamped():
@@ -219,43 +219,56 @@ def test_page_index_outside_pool_is_flagged():
     del out
 
 
-# ---- the named workloads at full size: sampled rows against the oracle ------------------
-
-def sampled_rows(case, out, n=48, seed=0):
-    g = np.random.default_rng(seed)
-    rows = g.choice(case.B * case.Hq, size=min(n, case.B * case.Hq), replace=False)
-    ref = oracle.decode_paged_rows(bits(case.q), bits(case.k_cache), bits(case.v_cache),
-                                   case.block_table.cpu().numpy(), case.seq_lens.cpu().numpy(),
-                                   case.scale, rows)
-    got = out.reshape(-1, case.D)[torch.as_tensor(rows, device=out.device)]
-    assert torch.isfinite(out.float()).all()
-    assert_close(got, ref, case.name)
-
+# ---- the named workloads at full size: every output element against the oracle -----------
 
 def test_llama_workload_paged_and_contiguous():
     case = inputs.llama_paged(device="cuda")
+    ref = oracle_paged(case)
     out = gpu_paged(case, 0)
-    sampled_rows(case, out)
+    assert_close(out, ref, case.name)
+    assert_close(gpu_paged(case, BAL), ref, case.name + ", balanced")
     k, v = inputs.logical_kv(case)
     c = binding.decode_attn_contig(case.q, k, v, case.seq_lens, max_kv_len=case.max_kv_len)
     assert torch.equal(c, out)
+    assert binding.get_device_errors() == 0
 
 
 def test_ragged_workload():
+    """The benchmark's launch (the planner's S with the summed lengths known) and the
+    planner's S without them, on all 128 x 32 x 128 outputs."""
     case = inputs.ragged_paged(device="cuda")
-    out = gpu_paged(case, 0)
-    sampled_rows(case, out, n=64)
+    ref = oracle_paged(case)
+    assert_close(gpu_paged(case, 0, total_kv=case.total_kv), ref, case.name)
+    assert_close(gpu_paged(case, 0), ref, case.name + ", S resolved by the library")
+    assert_close(gpu_paged(case, BAL), ref, case.name + ", balanced")
     assert binding.get_device_errors() == 0
 
 
 @pytest.mark.parametrize("B", [1, 4])
 def test_long_context_workload_split_sweep(B):
     case = inputs.long_paged(B=B, device="cuda")
-    outs = {}
-    for S in [0, 1, 8, 32, 128]:
-        outs[S] = gpu_paged(case, S)
-        sampled_rows(case, outs[S], n=16, seed=S)
+    ref = oracle_paged(case)
+    for S in [BAL, 0, 1, 8, 32, 128]:
+        assert_close(gpu_paged(case, S), ref, f"{case.name} S={S}")
     assert binding.get_device_errors() == 0
+
+
+@pytest.mark.parametrize("shape", [(3, 8, 2, 64, 16, [100, 37, 300]), (130, 32, 8, 128, 16, None),
+                                   (1, 64, 8, 128, 64, [20000])])
+def test_zero_splits_is_the_resolved_planner_count(shape):
+    """num_splits = 0 passed through the C ABI runs dap_resolve_splits(0, ...)'s S: the same
+    bits as that explicit count, on the paged and the contiguous cache."""
+    B, Hq, Hkv, D, ps, lens = shape
+    lens = lens or inputs.uniform_lengths(B, 1, 3000, 90)
+    case = inputs.make_paged_case(B, Hq, Hkv, D, ps, lens, 91 + B).to("cuda")
+    S = binding.resolve_splits(0, binding.device_sm_count(), B, Hq, Hkv, D, ps, case.max_kv_len)
+    a = gpu_paged(case, 0)
+    assert torch.equal(a, gpu_paged(case, S)), f"planner S={S}"
+    k, v = inputs.logical_kv(case)
+    c0 = binding.decode_attn_contig(case.q, k, v, case.seq_lens, max_kv_len=case.max_kv_len, num_splits=0)
+    cS = binding.decode_attn_contig(case.q, k, v, case.seq_lens, max_kv_len=case.max_kv_len, num_splits=S)
+    assert torch.equal(c0, cS) and torch.equal(c0, a)
+    assert_close(a, oracle_paged(case), f"planner S={S}")
 
 
 @pytest.mark.parametrize("D", [32, 256])
@@ -263,7 +276,7 @@ def test_contiguous_head_dims_32_and_256(D):
     case = inputs.make_paged_case(3, 16, 4, D, 16, [150, 1, 64], 79 + D).to("cuda")
     k, v = inputs.logical_kv(case, max_len=160)
     ref = oracle.decode_contig(bits(case.q), bits(k), bits(v), case.seq_lens.cpu().numpy(), case.scale)
-    for S in [0, 1, 3]:
+    for S in [BAL, 0, 1, 3]:
         c = binding.decode_attn_contig(case.q, k, v, case.seq_lens, max_kv_len=case.max_kv_len, num_splits=S)
         assert_close(c, ref, f"contig D={D} S={S}")
         assert torch.equal(c, gpu_paged(case, S))

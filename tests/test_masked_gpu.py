@@ -98,18 +98,14 @@ def test_bool_mask_with_wide_rows():
     assert_close(gpu_masked(case, full.cuda(), 2), ref, "bool mask")
 
 
-def test_full_size_ragged_with_mask_sampled_rows():
+def test_full_size_ragged_with_mask():
+    """The benchmark's masked workload (the ragged batch, 90% of keys kept) at its launch
+    configuration; every output element against the oracle."""
     case = inputs.ragged_paged(device="cuda")
     full, _ = make_mask(case.B, case.max_kv_len, 6400, p_keep=0.9)
     out = gpu_masked(case, full.cuda(), 0, total_kv=case.total_kv)
-    torch.cuda.synchronize()
+    assert_close(out, oracle_masked(case, full), "full size")
     assert binding.get_device_errors() == 0
-    rng = np.random.default_rng(13)
-    rows = sorted(rng.choice(case.B, size=12, replace=False).tolist())
-    idx = torch.as_tensor(rows, device="cuda")
-    sub = inputs.PagedCase(case.q[idx], case.k_cache, case.v_cache, case.block_table[idx], case.seq_lens[idx],
-                           case.page_size, case.scale)
-    assert_close(out[idx], oracle_masked(sub, full[rows]), "full size, sampled")
 
 
 # ---- multi-token decode with a mask ---------------------------------------------------
