@@ -47,7 +47,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
-LEGS = ("llama", "llama_contig", "long1", "long4", "fp8", "multi", "fp8kv", "masked")
+LEGS = ("llama", "llama_contig", "long1", "long4", "fp8", "multi", "multi_g8", "multi_g8_q8", "fp8kv", "masked")
 WORKLOADS = ("ragged",) + LEGS + ("append",)
 
 
@@ -286,6 +286,8 @@ def make_case(key, device, batch=0):
         return inputs.fp8_swa(device=device)
     if key == "multi":
         return inputs.spec_verify_paged(device=device, B=batch or 128)
+    if key in ("multi_g8", "multi_g8_q8"):   # G = 8: Hq=64, Hkv=8, 4 or 8 new tokens
+        return inputs.spec_verify_paged(device=device, B=batch or 128, q_len=8 if key.endswith("q8") else 4, Hq=64)
     if key == "fp8kv":
         return inputs.ragged_fp8kv(device=device, B=batch or 128)
     if key == "masked":
@@ -337,7 +339,7 @@ def oracle_sample(key, case) -> OracleSample:
              case.lens.cpu().numpy())
         return OracleSample(case.T, timed(lambda n: oracle.fp8_swa(*a, case.block_size, case.scale, tokens=(0, n))),
                             lambda n: fp8_algorithmic(case, n)[0], "tokens")
-    if key == "multi":
+    if key.startswith("multi"):
         kv = case.kv
         q, k, v = bits(case.q), bits(kv.k_cache), bits(kv.v_cache)
         table, lens = kv.block_table.cpu().numpy(), kv.seq_lens.cpu().numpy()
@@ -494,7 +496,7 @@ def prepare_leg(key, case, dev, l2, splits=None) -> Leg:
                    nbytes, "swa_kernel", call, (h2d, call, d2h), hq.numel() * 2 + hidx.numel() * 8 + hln.numel() * 8,
                    ho.numel() * 2, 1, n, trace=False, extra={"flops": flops})
 
-    if key == "multi":
+    if key.startswith("multi"):
         kv = case.kv
         mplan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, dev)
         S = plan(mplan.num_tiles, kv.Hq, kv.Hkv, kv.D, kv.page_size, kv.max_kv_len, kv.total_kv)
@@ -532,7 +534,8 @@ def prepare_leg(key, case, dev, l2, splits=None) -> Leg:
         flops = sum(4 * kv.Hq * kv.D * sum(L - ql + i + 1 for i in range(ql)) for L, ql in zip(lens, case.q_lens))
         cfg = {"workload": kv.name, "B": len(case.q_lens), "q_len": case.q_lens[0], "total_q": case.total_q,
                "Hq": kv.Hq, "Hkv": kv.Hkv, "D": kv.D, "page_size": kv.page_size, "total_kv": kv.total_kv,
-               "num_tiles": mplan.num_tiles, "num_splits": run, "kv_dtype": "bf16",
+               "num_tiles": mplan.num_tiles, "tokens_per_tile": mplan.tokens_per_tile, "num_splits": run,
+               "kv_dtype": "bf16",
                "cold_kv": f"{n} rotated input copies of {footprint / 1e9:.2f} GB each (> 2x L2)"}
         return Leg(key, "multi-token paged decode achieved HBM GB/s (algorithmic bytes), cold KV", cfg,
                    multi_algorithmic(case), "multi_kernel", call, (h2d, call, d2h),
@@ -936,6 +939,8 @@ def run_reference(args):
     name = getattr(c, "name", "") or getattr(getattr(c, "kv", None), "name", key)
     metric = {"fp8": "fp8 sliding-window latent decode achieved HBM GB/s (algorithmic bytes), cold inputs",
               "multi": "multi-token paged decode achieved HBM GB/s (algorithmic bytes), cold KV",
+              "multi_g8": "multi-token paged decode achieved HBM GB/s (algorithmic bytes), cold KV",
+              "multi_g8_q8": "multi-token paged decode achieved HBM GB/s (algorithmic bytes), cold KV",
               "fp8kv": "paged decode attention over an e4m3 KV cache, achieved HBM GB/s (algorithmic bytes), cold KV",
               "masked": "masked paged decode achieved HBM GB/s (algorithmic bytes), cold KV",
               "llama_contig": "contiguous-cache decode achieved HBM GB/s (algorithmic bytes), cold KV"}.get(

@@ -249,17 +249,21 @@ dap_status kv_append_paged_fp8(const void *k_new, const void *v_new, uint8_t *k_
  * (With q_len[b] = 1 this is decode_attn_paged.)  A token with p < 0 (q_len[b] > seq_lens[b],
  * flagged DAP_DEVERR_SEQLEN) gives a zero row.
  *
- * Work map: every sequence's tokens are cut into tiles of tokens_per_tile =
- * dap_multi_tokens_per_tile(Hq, Hkv) = 16 / G tokens (16 query columns of G heads each per
- * tile); tile w covers tokens [tile_index[w] * tokens_per_tile, ...) of sequence
- * tile_batch[w].  dap_q_tile_map builds it on the host:
+ * Work map: every sequence's tokens are cut into tiles of tokens_per_tile tokens; tile w
+ * covers tokens [tile_index[w] * tokens_per_tile, ...) of sequence tile_batch[w].  A tile's
+ * tokens x the G heads of a kv head are its query columns, and every tile streams its
+ * sequence's keys once, so the fewer tiles a sequence has, the fewer times its K/V are
+ * read.  Two tile sizes: 16 / G tokens (16 columns) or 32 / G tokens (32 columns; not with a
+ * mask).  dap_multi_tokens_per_tile(Hq, Hkv, max_q_len) picks the smaller when the longest
+ * new-token count fits it, else the larger (G = 8: 2 tokens up to q_len 2, then 4).
+ * dap_q_tile_map builds the map on the host:
  *   q_lens      host int32 [B], each >= 0.
  *   qo_indptr   host int32 [B + 1] (written).
  *   tile_batch, tile_index   host int32 [max_tiles] (written).
  * Returns the number of tiles, or -1 when max_tiles is too small or an input is invalid.
  * Pure host functions; no CUDA call.
  */
-int dap_multi_tokens_per_tile(int Hq, int Hkv);
+int dap_multi_tokens_per_tile(int Hq, int Hkv, int max_q_len);
 int dap_q_tile_map(const int32_t *q_lens, int B, int tokens_per_tile, int32_t *qo_indptr,
                    int32_t *tile_batch, int32_t *tile_index, int max_tiles);
 
@@ -272,7 +276,9 @@ size_t dap_workspace_bytes_multi(int total_q, int Hq, int D, int num_splits);
  *   k_cache, v_cache, block_table, num_pages, page_size, max_pages: as decode_attn_paged.
  *   seq_lens     device int32 [B], in [q_len[b], max_kv_len].
  *   qo_indptr    device int32 [B + 1]; tile_batch, tile_index device int32 [num_tiles]: the
- *                work map above (copies of dap_q_tile_map's output).
+ *                work map above (copies of dap_q_tile_map's output), built with
+ *   tokens_per_tile  16 / G or 32 / G (else DAP_ERR_SHAPE; 32 / G with a mask:
+ *                DAP_ERR_UNSUPPORTED).
  *   num_splits   >= 1: the per-sequence schedule of decode_attn_paged, per tile: the tile's
  *                keys (up to its last token's position) are cut into chunks of
  *                dap_chunk_tokens(max_kv_len, num_splits) keys, one CTA per (tile, kv head,
@@ -297,7 +303,7 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
                                    int page_size, const int32_t *block_table, int max_pages,
                                    const int32_t *seq_lens, const int32_t *qo_indptr,
                                    const int32_t *tile_batch, const int32_t *tile_index,
-                                   int num_tiles, int total_q, const uint8_t *mask,
+                                   int num_tiles, int tokens_per_tile, int total_q, const uint8_t *mask,
                                    long long mask_stride, int max_kv_len, int B, int Hq, int Hkv,
                                    int D, float scale, int num_splits, void *workspace,
                                    size_t workspace_bytes, void *out, long long out_stride_t,

@@ -101,14 +101,14 @@ def load(build_if_missing: bool = True):
         lib.kv_append_paged.restype = I
         lib.kv_append_fp8.argtypes = [P, P, P, P, I, I, I, I, P]
         lib.kv_append_fp8.restype = I
-        lib.dap_multi_tokens_per_tile.argtypes = [I, I]
+        lib.dap_multi_tokens_per_tile.argtypes = [I, I, I]
         lib.dap_multi_tokens_per_tile.restype = I
         lib.dap_q_tile_map.argtypes = [P, I, I, P, P, P, I]
         lib.dap_q_tile_map.restype = I
         lib.dap_workspace_bytes_multi.argtypes = [I, I, I, I]
         lib.dap_workspace_bytes_multi.restype = SZ
-        lib.decode_attn_paged_multi.argtypes = [P, LL, LL, P, P, I, I, P, I, P, P, P, P, I, I, P, LL, I, I, I, I,
-                                                I, F, I, P, SZ, P, LL, LL, P]
+        lib.decode_attn_paged_multi.argtypes = [P, LL, LL, P, P, I, I, P, I, P, P, P, P, I, I, I, P, LL, I, I, I,
+                                                I, I, F, I, P, SZ, P, LL, LL, P]
         lib.decode_attn_paged_masked.argtypes = [P, LL, LL, P, P, I, I, P, I, P, P, LL, I, I, I, I, I, F, I, P, SZ,
                                                  P, LL, LL, P]
         lib.decode_attn_paged_masked.restype = I
@@ -448,8 +448,9 @@ def decode_attn_paged_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, 
 
 # ---- multi-token decode ------------------------------------------------------------------
 
-def multi_tokens_per_tile(Hq: int, Hkv: int) -> int:
-    return load().dap_multi_tokens_per_tile(int(Hq), int(Hkv))
+def multi_tokens_per_tile(Hq: int, Hkv: int, max_q_len: int = 0) -> int:
+    """include/dap.h: dap_multi_tokens_per_tile (16 / G, or 32 / G for longer new-token runs)."""
+    return load().dap_multi_tokens_per_tile(int(Hq), int(Hkv), int(max_q_len))
 
 
 def workspace_bytes_multi(total_q, Hq, D, num_splits) -> int:
@@ -474,8 +475,11 @@ class MultiPlan:
     """The work map of one batch of new-token counts, copied to the device once so that
     repeated decode calls on the same counts pass it straight to the library."""
 
-    def __init__(self, q_lens, Hq: int, Hkv: int, device):
-        self.tokens_per_tile = multi_tokens_per_tile(Hq, Hkv)
+    def __init__(self, q_lens, Hq: int, Hkv: int, device, tokens_per_tile: int | None = None):
+        ql = [int(x) for x in torch.as_tensor(q_lens).reshape(-1).tolist()]
+        if tokens_per_tile is None:
+            tokens_per_tile = multi_tokens_per_tile(Hq, Hkv, max(ql, default=0))
+        self.tokens_per_tile = int(tokens_per_tile)
         _need(self.tokens_per_tile > 0, "Hq must be a multiple of Hkv with G <= 16")
         qi, tb, ti = q_tile_map(q_lens, self.tokens_per_tile)
         self.B = qi.numel() - 1
@@ -525,7 +529,8 @@ def decode_attn_paged_multi(q, k_cache, v_cache, block_table, seq_lens, plan: Mu
         st = lib.decode_attn_paged_multi(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
                                          _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
                                          _ptr(plan.qo_indptr), _ptr(plan.tile_batch), _ptr(plan.tile_index),
-                                         plan.num_tiles, total_q, _ptr(mask), 0 if mask is None else mask.stride(0),
+                                         plan.num_tiles, plan.tokens_per_tile, total_q, _ptr(mask),
+                                         0 if mask is None else mask.stride(0),
                                          int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S), _ptr(workspace),
                                          wbytes, _ptr(out), out.stride(0), out.stride(1), _stream(stream, dev))
     _check(st, "decode_attn_paged_multi")

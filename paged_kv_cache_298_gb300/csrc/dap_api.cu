@@ -273,9 +273,9 @@ dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_s
     return launch_decode(a, static_cast<cudaStream_t>(stream));
 }
 
-int dap_multi_tokens_per_tile(int Hq, int Hkv) {
+int dap_multi_tokens_per_tile(int Hq, int Hkv, int max_q_len) {
     if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return 0;
-    return multi_tokens_per_tile(Hq / Hkv);
+    return multi_tokens_per_tile(Hq / Hkv, max_q_len);
 }
 
 int dap_q_tile_map(const int32_t *q_lens, int B, int tokens_per_tile, int32_t *qo_indptr, int32_t *tile_batch,
@@ -314,7 +314,8 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
                                    const void *k_cache, const void *v_cache, int num_pages, int page_size,
                                    const int32_t *block_table, int max_pages, const int32_t *seq_lens,
                                    const int32_t *qo_indptr, const int32_t *tile_batch,
-                                   const int32_t *tile_index, int num_tiles, int total_q, const uint8_t *mask,
+                                   const int32_t *tile_index, int num_tiles, int tokens_per_tile, int total_q,
+                                   const uint8_t *mask,
                                    long long mask_stride, int max_kv_len, int B, int Hq, int Hkv, int D,
                                    float scale, int num_splits, void *workspace, size_t workspace_bytes,
                                    void *out, long long out_stride_t, long long out_stride_h, void *stream) {
@@ -333,6 +334,11 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
         !aligned4(tile_batch) || !aligned4(tile_index))
         return DAP_ERR_ALIGN;
     if (page_size % 8 != 0 || !(D == 64 || D == 128)) return DAP_ERR_UNSUPPORTED;
+    {
+        const int G = Hq / Hkv;
+        if (tokens_per_tile * G != 16 && tokens_per_tile * G != 32) return DAP_ERR_SHAPE;
+        if (mask && tokens_per_tile * G != 16) return DAP_ERR_UNSUPPORTED;
+    }
     if ((st = check_mask(mask, mask_stride, max_kv_len)) != DAP_OK) return st;
     int S = 0, chunk = 0;
     if ((st = resolve_splits(num_tiles, total_q, Hq, Hkv, D, page_size, max_kv_len, num_splits, workspace,
@@ -366,6 +372,7 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
     a.tile_batch = tile_batch;
     a.tile_index = tile_index;
     a.num_tiles = num_tiles;
+    a.tokens_per_tile = tokens_per_tile;
     a.total_q = total_q;
     a.mask = mask;
     a.mask_stride = mask_stride;
@@ -418,6 +425,7 @@ dap_status decode_attn_paged_masked(const void *q, long long q_stride_b, long lo
     a.o_sb = out_stride_b;
     a.o_sh = out_stride_h;
     a.num_tiles = B;  // one token per sequence, no work map
+    a.tokens_per_tile = 1;
     a.total_q = B;
     a.mask = mask;
     a.mask_stride = mask_stride;

@@ -61,28 +61,27 @@ constexpr int kHeads = 128;         // heads per CTA = MMA M
 constexpr int kMaxRows = 128;       // window rows a CTA holds
 constexpr int kHalf = kHD / 2;      // output columns per CTA
 constexpr int kThreads = 256;       // 8 warps: warps w and w+4 share TMEM lanes
-constexpr int kQStages = 4;
+constexpr int kQBlocks = kHD / 64;  // q arrives as 8 blocks of 64 values per head
 // shared-memory map (offsets from a 1024-byte aligned base)
-constexpr int kQOff = 0;                                    // q ring: 4 stages of 128 heads x 64
-constexpr int kQStage = kHeads * 128;                       // 16 KB per stage
-constexpr int kPOff = kQOff;                                // P: 2 blocks of 128 heads x 64, after q
-constexpr int kKvOff = kQOff + kQStages * kQStage;          // 65536: KV tile [8 blocks][n16 rows][128 B]
-constexpr int kOOff = kKvOff;                               // bf16 output staging after PV (64 KB)
-constexpr int kPBlock = kHeads * 128;                       // 16 KB per 64-wide row block
-constexpr int kXchOff = kKvOff + 8 * kMaxRows * 128;        // softmax max/sum exchange (2 KB)
-constexpr int kRowsOff = kXchOff + 4 * kHeads * 4;          // int32 slot per kept row
-constexpr int kInvOff = kRowsOff + kMaxRows * 4;            // f32 inverse scale per kept row
-constexpr int kCntOff = kInvOff + kMaxRows * 4;             // per-warp counts [0..7], abort [12]
+constexpr int kQOff = 0;                                    // q landing zone: 8 blocks of 128 heads x 64
+constexpr int kQBlock = kHeads * 128;                       // 16 KB per block
+constexpr int kKvOff = 0;                                   // KV tile [8 blocks][n16 rows][128 B], once q
+                                                            // has moved into tensor memory
+constexpr int kOOff = 0;                                    // bf16 output staging after PV (64 KB)
+constexpr int kPOff = kQOff + kQBlocks * kQBlock;           // 131072: P, 2 blocks of 128 heads x 64 keys
+constexpr int kPBlock = kHeads * 128;                       // 16 KB per 64-key block
+constexpr int kXchOff = kPOff + 2 * kPBlock;                // softmax max/sum exchange (2 KB)
+constexpr int kCntOff = kXchOff + 4 * kHeads * 4;           // per-warp row counts [0..7], abort [12]
 constexpr int kBarOff = kCntOff + 64;                       // mbarriers
-constexpr int kNumBars = kQStages + 2;                      // q_full[4], mma_done[2]
+constexpr int kNumBars = kQBlocks + 2;                      // q_full[8], s_done, o_done
 constexpr int kTmemOff = kBarOff + kNumBars * 8;
 constexpr int kSmemUsed = kTmemOff + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;                // slack to align the base
 constexpr int kTmemCols = 512;  // q: cols [0,256) (two bf16 per column) until S is complete,
                                 // then O: [0,256); S: [256,384)
 constexpr int kSCol = 256;
-static_assert(kOOff + kHeads * kHalf * 2 <= kXchOff, "the output staging fits in the KV tile");
-static_assert(kPOff + 2 * kPBlock <= kKvOff, "P fits in the q ring");
+static_assert(8 * kMaxRows * 128 <= kPOff, "the KV tile fits in the q landing zone");
+static_assert(kOOff + kHeads * kHalf * 2 <= kPOff, "the output staging fits in the KV tile");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // ---- tcgen05 / descriptor helpers ---------------------------------------------------------
@@ -214,39 +213,58 @@ struct Params {
     const __nv_bfloat16 *inv_scale;
     const int64_t *slot_idx;
     const int64_t *lens;
-    __nv_bfloat16 *out;
     int T, NH, W;
     long long max_slots;
     float qscale;  // scale * log2(e)
 };
 
+// 2D tiled TMA store shared -> global (bulk group; the caller commits and waits).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int c0, int c1, const void *src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(smem_addr(src))
+                 : "memory");
+}
 
-// Moves the four q blocks of ring round `round` (blocks 4 round .. 4 round + 3) into tensor
-// memory: thread (head h, half c) waits for each stage, reads its 32 values (64 bytes, four
-// 128B-swizzled chunks) of row h and stores them at columns 32 block + 16 c of lane h (two
-// bf16 per column, the lower index in the low half).  A wait that gives up sets the abort
-// word; the caller still reaches every barrier.
-__device__ __forceinline__ void q_to_tmem(uint8_t *smem, uint64_t *q_full, uint32_t tmem_lane, int h, int c,
-                                          int round, int *cnt) {
+// The four e4m3 codes of `w` times the fp32 factor `f`: byte k moved to bits 24..31 and
+// shifted right arithmetically by 4 lands as an fp32 bit pattern whose exponent field is the
+// code's exponent field and whose mantissa starts with the code's three mantissa bits (the
+// sign, replicated, is masked back to bit 31), i.e. the code's value times 2^-120, exact for
+// subnormal codes too (an fp32 subnormal; nothing here flushes to zero); multiplying by
+// 2^120 restores it exactly, and its product with a bf16 factor (a 4-bit by an 8-bit
+// significand) is exact in fp32.  Codes S.1111.111 are NaN in OCP E4M3FN and come out NaN.
+__device__ __forceinline__ void e4m3x4_times(uint32_t w, float f, float (&o)[4]) {
 #pragma unroll
-    for (int st = 0; st < kQStages; ++st) {
-        if (!mbar_wait(&q_full[st], round & 1)) cnt[12] = 1;
-        const uint8_t *blk = smem + kQOff + st * kQStage;
-        uint32_t r[16];
+    for (int k = 0; k < 4; ++k) {
+        const int y = (int)(w << (24 - 8 * k));
+        o[k] = (__uint_as_float((uint32_t)(y >> 4) & 0x87F00000u) * 0x1p120f) * f;
+    }
+    if ((((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u) != 0u) {  // a NaN code (rare)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(blk + sw128_off(h, 4 * c + i));
-            r[4 * i] = v.x;
-            r[4 * i + 1] = v.y;
-            r[4 * i + 2] = v.z;
-            r[4 * i + 3] = v.w;
-        }
-        tmem_st16(tmem_lane + (round * kQStages + st) * 32 + 16 * c, r);
+        for (int k = 0; k < 4; ++k)
+            if (((w >> (8 * k)) & 0x7Fu) == 0x7Fu) o[k] = __uint_as_float(0x7FC00000u);
     }
 }
 
+// One CTA per (head half of HD, head group of 128, token).  The chain, shortened to two
+// dependent global round trips before the products (slots, then rows and their inverse
+// scales together) with q landing in full meanwhile:
+//   1. thread 0 issues all eight q blocks by TMA at entry (128 KB landing zone); every
+//      warp loads the slots of its 16 window positions and the token's length;
+//   2. each warp gathers the rows of its kept positions into registers (a half-warp per
+//      256-byte half of a row) together with their inverse scales; per-warp counts give
+//      every kept row its place in window order;
+//   3. q moves into tensor memory block by block as it lands (head = TMEM lane, two bf16
+//      per column);
+//   4. the rows are dequantised (e4m3 decoded by integer ops, times the f32 inverse scale,
+//      one bf16 rounding) into a 128-byte-swizzled [hd block][row][64] tile where q landed;
+//   5. S = Q . KV^T (M=128, N=n16, K=512), A from tensor memory;
+//   6. softmax: two threads per head, 32-column chunks alternating between them;
+//   7. O[:, half] = P . KV[:, half] (M=128, N=256, K=n16) into the columns q held;
+//   8. out = O / l in bf16, staged swizzled and written by TMA stores.
 __global__ void __launch_bounds__(kThreads, 1)
-    swa_kernel(const __grid_constant__ CUtensorMap qmap, const Params p) {
+    swa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+               const Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the 128-byte swizzle is a function of address bits 4..9: tiles start 1024-aligned
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -254,14 +272,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col_half = blockIdx.x;    // which 256 output columns
     const int hg = blockIdx.y;          // head group of 128
     const int t = blockIdx.z;           // decode token
-    int *rows = reinterpret_cast<int *>(smem + kRowsOff);
-    float *invs = reinterpret_cast<float *>(smem + kInvOff);
     int *cnt = reinterpret_cast<int *>(smem + kCntOff);     // [0..7] warp counts, [12] abort
     uint64_t *q_full = reinterpret_cast<uint64_t *>(smem + kBarOff);
-    uint64_t *mma_done = q_full + kQStages;
+    uint64_t *s_done = q_full + kQBlocks;
+    uint64_t *o_done = s_done + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
 
-    // thread = (head hrow = TMEM lane, half qhalf of q's 512 values / of the score columns):
+    // thread = (head hrow = TMEM lane, half chalf of q's 512 values / of the columns):
     // warps w and w + 4 serve the same 32 lanes
     const int hrow = tid & (kHeads - 1);
     const int chalf = warp >> 2;
@@ -271,11 +288,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Barriers and tensor memory touch nothing the previous kernel writes: they are set up
     // before the wait below, overlapping that kernel's end.
     if (tid == 0) {
-        for (int i = 0; i < kQStages; ++i) mbar_init(&q_full[i], 1);
-        mbar_init(&mma_done[0], 1);
-        mbar_init(&mma_done[1], 1);
+        for (int i = 0; i < kNumBars; ++i) mbar_init(&q_full[i], 1);
         cnt[12] = 0;
         fence_barrier_init();
+        prefetch_tensormap(&qmap);
+        prefetch_tensormap(&omap);
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -289,162 +306,167 @@ __global__ void __launch_bounds__(kThreads, 1)
     // slot table); the next launch may start at once (it waits the same way).
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // ---- 1a. q's first four 64-wide blocks, right away: they travel during the compaction
+    // ---- 1. all of q, right away; the window's slots and length ------------------------------
     if (tid == 0) {
-        for (int kb = 0; kb < kQStages; ++kb) {
-            mbar_arrive_expect_tx(&q_full[kb], kQStage);
-            tma_load_2d(smem + kQOff + kb * kQStage, &qmap, kb * 64, qrow, &q_full[kb]);
+        for (int kb = 0; kb < kQBlocks; ++kb) {
+            mbar_arrive_expect_tx(&q_full[kb], kQBlock);
+            tma_load_2d(smem + kQOff + kb * kQBlock, &qmap, kb * 64, qrow, &q_full[kb]);
         }
     }
-
-    // ---- 1b. compact the window: slots of the rows that take part, in window order ---------
-    // (the slot is loaded together with the length, not after it)
+    // warp w holds window positions 16 w .. 16 w + 15, lanes l and l + 16 the same one
+    const int jpos = 16 * warp + (lane & 15);
     long long slot = -1;
-    if (tid < p.W) slot = p.slot_idx[(long long)t * p.W + tid];
+    if (jpos < p.W) slot = p.slot_idx[(long long)t * p.W + jpos];
     long long len = p.lens[t];
     len = len < 0 ? 0 : (len > p.W ? p.W : len);
-    int keep = 0;
-    if (tid < len) {
+    bool keep = false;
+    if (jpos < len) {
         if (slot >= p.max_slots) {
-            flag_error(DAP_DEVERR_SLOT);
+            if (lane < 16) flag_error(DAP_DEVERR_SLOT);
             slot = -1;
         }
         keep = slot >= 0;
     }
-    const unsigned ball = __ballot_sync(0xFFFFFFFFu, keep);
+    const uint32_t ball = __ballot_sync(0xFFFFFFFFu, keep) & 0xFFFFu;
+
+    // ---- 2. the kept rows into registers, with their inverse scales --------------------------
+    // row piece of this lane: bytes 16 (l % 16) + 256 (l / 16) of each row (16 e4m3 codes)
+    uint4 raw[16];
+    float invf = 0.f;
+    if (keep) invf = __bfloat162float(p.inv_scale[slot]);
+    const uint8_t *piece = p.kv_cache + (lane & 15) * 16 + (lane >> 4) * 256;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const long long s = __shfl_sync(0xFFFFFFFFu, slot, i);
+        raw[i] = make_uint4(0u, 0u, 0u, 0u);
+        if ((ball >> i) & 1u) raw[i] = __ldg(reinterpret_cast<const uint4 *>(piece + s * kHD));
+    }
     if (lane == 0) cnt[warp] = __popc(ball);
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // barrier init, TMEM address and the counts are visible
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += cnt[w];
-    int n = 0;
-    for (int w = 0; w < kThreads / 32; ++w) n += cnt[w];
-    if (keep) {
-        const int pos = base + __popc(ball & ((1u << lane) - 1u));
-        rows[pos] = (int)slot;
-        invs[pos] = __bfloat162float(p.inv_scale[slot]);
+    int base = 0, n = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        const int c = cnt[w];
+        base += w < warp ? c : 0;
+        n += c;
     }
     const int n16 = (n + 15) & ~15;
     const int kvb = n16 * 128;  // bytes per 64-wide hd block of the KV tile
-    __syncthreads();  // rows[] / invs[] complete
 
-    // ---- 2. gather + dequantise the rows into the swizzled KV tile -------------------------
-    // Every thread issues all its 16-byte loads (at most kBatch: one pass covers 128 rows)
-    // before converting any of them; while they travel, q blocks 0..3 move from the ring
-    // into tensor memory (q_to_tmem) and thread 0 refills the ring with blocks 4..7 once
-    // every thread has read its stage.
-    constexpr int kBatch = 16;
-    static_assert(kMaxRows * 32 <= kThreads * kBatch, "one pass of loads covers the window");
-    const int total = n16 * 32;  // 16-byte pieces: 32 per 512-byte fp8 row
-    uint4 raw[kBatch];
+    // ---- 3. q into tensor memory as it lands ---------------------------------------------------
+    // thread (head hrow, half chalf) moves its 32 values of each block: four 16-byte chunks
+    // of row hrow of the 128B-swizzled block, to columns 32 kb + 16 chalf of lane hrow
+#pragma unroll 1
+    for (int kb = 0; kb < kQBlocks; ++kb) {
+        if (!mbar_wait(&q_full[kb], 0)) cnt[12] = 1;
+        const uint8_t *blk = smem + kQOff + kb * kQBlock;
+        uint32_t r[16];
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-        const int item = k * kThreads + tid;
-        const int r = item >> 5;
-        raw[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (item < total && r < n)
-            raw[k] = __ldg(reinterpret_cast<const uint4 *>(p.kv_cache + (long long)rows[r] * kHD) + (item & 31));
-    }
-    q_to_tmem(smem, q_full, tmem + lane_base, hrow, chalf, 0, cnt);
-    __syncthreads();  // the ring is read
-    if (tid == 0) {
-        for (int kb = 0; kb < kQStages; ++kb) {
-            mbar_arrive_expect_tx(&q_full[kb], kQStage);
-            tma_load_2d(smem + kQOff + kb * kQStage, &qmap, (kb + kQStages) * 64, qrow, &q_full[kb]);
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(blk + sw128_off(hrow, 4 * chalf + i));
+            r[4 * i] = v.x;
+            r[4 * i + 1] = v.y;
+            r[4 * i + 2] = v.z;
+            r[4 * i + 3] = v.w;
         }
+        tmem_st16(tmem + lane_base + kb * 32 + 16 * chalf, r);
     }
-    if (n > 0) {
+    tmem_wait_st();   // this thread's q columns are in tensor memory
+    __syncthreads();  // every thread has read the landing zone: the KV tile may overwrite it
+
+    // ---- 4. dequantise the rows into the swizzled KV tile ------------------------------------
+    {
+        const int blk = (lane & 15) / 4 + 4 * (lane >> 4);  // 64-wide hd block of this piece
+        const int k0 = ((lane & 15) % 4) * 2;               // first 16-byte chunk in the 128-byte row
+        uint8_t *tile = smem + kKvOff + blk * kvb;
+        int r = base;
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            const int item = k * kThreads + tid;
-            if (item < total) {
-                const int r = item >> 5;   // row
-                const int c = item & 31;   // 16-byte piece = 16 hd values
-                uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                if (r < n) {
-                    const float inv = invs[r];
-                    const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-                    uint32_t o[8];
+        for (int i = 0; i < 16; ++i) {
+            const float inv = __shfl_sync(0xFFFFFFFFu, invf, i);
+            if ((ball >> i) & 1u) {
+                const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+                uint32_t o[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            const __nv_fp8x2_storage_t pr =
-                                (__nv_fp8x2_storage_t)((w4[i] >> (16 * j)) & 0xFFFFu);
-                            const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
-                            const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * inv, f.y * inv);
-                            o[2 * i + j] = *reinterpret_cast<const uint32_t *>(&b);
-                        }
-                    }
-                    lo = make_uint4(o[0], o[1], o[2], o[3]);
-                    hi = make_uint4(o[4], o[5], o[6], o[7]);
+                for (int q = 0; q < 4; ++q) {
+                    float f[4];
+                    e4m3x4_times(w4[q], inv, f);
+                    o[2 * q] = pack_bf16(f[0], f[1]);
+                    o[2 * q + 1] = pack_bf16(f[2], f[3]);
                 }
-                const int blk = c >> 2;       // 64-wide hd block
-                const int k0 = (c & 3) * 2;   // first 16-byte chunk inside the 128-byte row
-                uint8_t *tile = smem + kKvOff + blk * kvb;
-                *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0)) = lo;
-                *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0 + 1)) = hi;
+                *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0)) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+                ++r;
             }
         }
+        // rows n .. n16 - 1 take part in the products as zeros
+        for (int idx = tid; idx < (n16 - n) * 64; idx += kThreads) {
+            const int rr = n + idx / 64, c = idx % 64;
+            *reinterpret_cast<uint4 *>(smem + kKvOff + (c >> 3) * kvb + sw128_off(rr, c & 7)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
     }
-    q_to_tmem(smem, q_full, tmem + lane_base, hrow, chalf, 1, cnt);  // blocks 4..7
-    tmem_wait_st();  // this thread's q columns are in tensor memory
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
     const uint32_t tS = tmem + kSCol;
-    // ---- 3. S = Q . KV^T, one thread issues; A = q from tensor memory ------------------------
-    if (tid == 0 && n > 0) {
+    // ---- 5. S = Q . KV^T, one thread issues; A = q from tensor memory ------------------------
+    if (tid == 0 && n > 0 && cnt[12] == 0) {
         const uint32_t idS = idesc_bf16(kHeads, n16, 0);
-        for (int kb = 0; kb < 8; ++kb) {
+        for (int kb = 0; kb < kQBlocks; ++kb) {
             const uint32_t kva = smem_addr(smem + kKvOff + kb * kvb);
 #pragma unroll
             for (int k16 = 0; k16 < 4; ++k16)  // 16 values = 8 columns of q per product
                 umma_bf16_tmem_a(tS, tmem + kb * 32 + k16 * 8, sw128_desc(kva + 32 * k16, 16, 1024), idS,
                                  (kb | k16) != 0);
         }
-        umma_commit(&mma_done[0]);
+        umma_commit(s_done);
     }
 
-    // ---- 4. softmax: thread = head = TMEM lane -------------------------------------------------
+    // ---- 6. softmax: thread = head = TMEM lane, 32-column chunks chalf, chalf + 2 ---------------
     bool waited = true;
-    if (n > 0) waited = mbar_wait(&mma_done[0], 0);
+    const bool run = n > 0 && cnt[12] == 0;
+    if (run) waited = mbar_wait(s_done, 0);
     const int good = __syncthreads_and(waited && cnt[12] == 0);
     tc_fence_after();
     float *xch = reinterpret_cast<float *>(smem + kXchOff);  // [2][128] max, then [2][128] sum
     float l = 0.f;
     if (good && n > 0) {
-        const int c0 = chalf * 64;
-        float v[64];
+        float v[2][32];
         float m = -INFINITY;
-        if (c0 < n16) {  // columns past n16 are read but masked
-            tmem_ld64(tS + lane_base + c0, v);
 #pragma unroll
-            for (int i = 0; i < 64; ++i)
-                if (c0 + i < n) m = fmaxf(m, v[i] * p.qscale);
+        for (int u = 0; u < 2; ++u) {
+            const int c0 = 32 * (chalf + 2 * u);
+            if (c0 < n16) {  // columns n .. n16 - 1 are read but masked
+                tmem_ld32(tS + lane_base + c0, v[u]);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (c0 + i < n) m = fmaxf(m, v[u][i] * p.qscale);
+            }
         }
         xch[chalf * kHeads + hrow] = m;
         __syncthreads();
         m = fmaxf(xch[hrow], xch[kHeads + hrow]);
         float lp = 0.f;
-        if (c0 < n16) {
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                const int j0 = c0 + 8 * g;
-                if (j0 < n16) {
+        for (int u = 0; u < 2; ++u) {
+            const int c0 = 32 * (chalf + 2 * u);
+            if (c0 < n16) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const int j0 = c0 + 8 * g;
                     uint32_t pk[4];
 #pragma unroll
                     for (int e = 0; e < 8; e += 2) {
-                        const float p0 = (j0 + e < n) ? ex2(v[8 * g + e] * p.qscale - m) : 0.f;
-                        const float p1 = (j0 + e + 1 < n) ? ex2(v[8 * g + e + 1] * p.qscale - m) : 0.f;
+                        const float p0 = (j0 + e < n) ? ex2(v[u][8 * g + e] * p.qscale - m) : 0.f;
+                        const float p1 = (j0 + e + 1 < n) ? ex2(v[u][8 * g + e + 1] * p.qscale - m) : 0.f;
                         const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
-                        const float2 r = __bfloat1622float2(b);
-                        lp += r.x + r.y;  // the sum of the weights PV actually uses
+                        const float2 r2 = __bfloat1622float2(b);
+                        lp += r2.x + r2.y;  // the sum of the weights PV actually uses
                         pk[e / 2] = *reinterpret_cast<const uint32_t *>(&b);
                     }
                     uint8_t *tile = smem + kPOff + (j0 >> 6) * kPBlock;
@@ -462,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
 
-    // ---- 5. O[:, half] = P . KV[:, half], into the columns q held (S is complete) --------------
+    // ---- 7. O[:, half] = P . KV[:, half], into the columns q held (S is complete) --------------
     if (tid == 0 && good && n > 0) {
         const uint32_t idO = idesc_bf16(kHeads, kHalf, 1);
         const uint32_t pa = smem_addr(smem + kPOff);
@@ -470,21 +492,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k16 = 0; k16 < n16 / 16; ++k16)
             umma_bf16(tmem, sw128_desc(pa + (k16 >> 2) * kPBlock + (k16 & 3) * 32, 16, 1024),
                       sw128_desc(kvh + k16 * 2048, (uint32_t)kvb, 1024), idO, k16 > 0);
-        umma_commit(&mma_done[0]);
+        umma_commit(o_done);
     }
     bool waited2 = true;
-    if (good && n > 0) waited2 = mbar_wait(&mma_done[0], 1);
+    if (good && n > 0) waited2 = mbar_wait(o_done, 0);
     const int good2 = __syncthreads_and(good && waited2);
     tc_fence_after();
 
-    // ---- 6. out = O / l --------------------------------------------------------------------------
-    // Each thread turns half of its head's 256 columns into bf16 in a staging area (the KV
-    // tile, read by no one now; 16-byte chunk c of row h at chunk c ^ (h mod 32),
-    // conflict-free both ways); then the CTA writes the 128 rows out with fully coalesced
-    // 16-byte stores.
+    // ---- 8. out = O / l ----------------------------------------------------------------------------
+    // Each thread turns half of its head's 256 columns into bf16, staged as four 64-column
+    // blocks of 128 rows x 128 bytes with the 128-byte swizzle (the KV tile's space, read by
+    // no one now); thread 0 then writes them with four TMA stores.
     if (good2) {
-        uint8_t *ostage = smem + kOOff;
         const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
         for (int c0 = chalf * (kHalf / 2); c0 < (chalf + 1) * (kHalf / 2); c0 += 64) {
             float v[64];
             if (n > 0) {
@@ -493,29 +514,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 64; ++i) v[i] = 0.f;
             }
+            uint8_t *ob = smem + kOOff + (c0 >> 6) * kQBlock;
 #pragma unroll
             for (int q8 = 0; q8 < 8; ++q8) {
                 uint32_t pk[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) pk[i] = pack_bf16(v[8 * q8 + 2 * i] * inv, v[8 * q8 + 2 * i + 1] * inv);
-                const int ch = c0 / 8 + q8;  // 0..31
-                *reinterpret_cast<uint4 *>(ostage + hrow * (kHalf * 2) + ((ch ^ (hrow & 31)) << 4)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4 *>(ob + sw128_off(hrow, q8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
         }
+        fence_async_smem();
         __syncthreads();
-        __nv_bfloat16 *obase = p.out + ((long long)t * p.NH + hg * kHeads) * kHD + col_half * kHalf;
-        for (int idx = tid; idx < kHeads * 32; idx += kThreads) {
-            const int row = idx >> 5, ch = idx & 31;
-            const uint4 val = *reinterpret_cast<const uint4 *>(ostage + row * (kHalf * 2) + ((ch ^ (row & 31)) << 4));
-            *reinterpret_cast<uint4 *>(obase + (long long)row * kHD + ch * 8) = val;
+        if (tid == 0) {
+            for (int b = 0; b < kHalf / 64; ++b)
+                tma_store_2d(&omap, col_half * kHalf + b * 64, qrow, smem + kOOff + b * kQBlock);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            // the staging must have been read before the CTA's shared memory is released
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         }
     } else if (tid == 0) {
         // A wait gave up.  Let the copies and products still in flight land (bounded) before
         // the tensor memory and the shared memory are released.
-        for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_full[i], 1);
-        umma_commit(&mma_done[1]);
-        (void)mbar_wait(&mma_done[1], 0);
+        for (int i = 0; i < kQBlocks; ++i) (void)mbar_wait(&q_full[i], 0);
+        umma_commit(o_done);
+        (void)mbar_wait(o_done, (good && n > 0) ? 1 : 0);
     }
     tc_fence_before();
     __syncthreads();
@@ -545,12 +567,17 @@ dap_status launch_fp8(const Fp8Args &a, cudaStream_t stream) {
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return DAP_ERR_CUDA;
+    // out as the same [T*NH, 512] bf16 matrix; a TMA store box is 128 heads x 64 values
+    CUtensorMap omap;
+    if (enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return DAP_ERR_CUDA;
     fp8::Params p;
     p.kv_cache = a.kv_cache;
     p.inv_scale = static_cast<const __nv_bfloat16 *>(a.inv_scale);
     p.slot_idx = a.slot_idx;
     p.lens = a.lens;
-    p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.T = a.T;
     p.NH = a.NH;
     p.W = a.W;
@@ -569,7 +596,7 @@ dap_status launch_fp8(const Fp8Args &a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, fp8::swa_kernel, qmap, p) != cudaSuccess) return DAP_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, fp8::swa_kernel, qmap, omap, p) != cudaSuccess) return DAP_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DAP_OK : DAP_ERR_CUDA;
 }
 

@@ -64,7 +64,7 @@ struct DecodeArgs {
     // multi-token decode only: packed-q work map (q_sb / o_sb are then token strides); none
     // (all NULL) for masked single-token decode
     const int32_t *qo_indptr, *tile_batch, *tile_index;
-    int num_tiles, total_q;
+    int num_tiles, total_q, tokens_per_tile;
     // optional bool mask [total_q, mask_stride] bytes (nonzero = keep)
     const uint8_t *mask;
     long long mask_stride;
@@ -74,7 +74,7 @@ dap_status launch_decode(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_multi(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_masked(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_fp8kv(const DecodeArgs &a, cudaStream_t stream);
-int multi_tokens_per_tile(int G);
+int multi_tokens_per_tile(int G, int max_q_len);
 
 // Events of dap_set_trace_events (nullptr when tracing is off).
 struct TraceEvents {

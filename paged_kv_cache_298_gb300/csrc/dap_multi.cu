@@ -22,16 +22,21 @@ namespace dap {
 // (the per-sequence schedule gives each CTA one unit), and the four warps merge their
 // partial states in quarters of D.
 
-// NT n8 tiles of query columns (2 for multi-token decode; 1 for masked single-token decode,
-// whose tiles hold one token); MASK: a bool mask tile rides with every K/V tile.
-template <int D_, int G_, int NT_ = 2, bool MASK_ = false>
+// NT n8 tiles of query columns per warp (2 for multi-token decode; 1 for masked single-token
+// decode, whose tiles hold one token); CG column groups (1, or 2 for 32-column tiles: warps
+// w and w + 4 take the same 16 keys of every tile for columns 0..15 and 16..31, so all
+// of a sequence's new tokens meet each K/V tile once); MASK: a bool mask tile rides with
+// every K/V tile.
+template <int D_, int G_, int NT_ = 2, bool MASK_ = false, int CG_ = 1>
 struct MultiCfg {
-    static constexpr int D = D_, G = G_, HG = 1, NWC = 4, BT = 64, NS = 3, MINB = 2;
+    static constexpr int CG = CG_, KW = 4;           // column groups, key slices
+    static constexpr int D = D_, G = G_, HG = 1, NWC = KW * CG, BT = 64;
+    static constexpr int NS = CG == 2 ? 5 : 3, MINB = CG == 2 ? 1 : 2;
     static constexpr bool MMA = true, SWZ = true, MASK = MASK_;
     static constexpr int NT = NT_;
-    static constexpr int NCOL = 8 * NT;             // query columns
+    static constexpr int NCOL = 8 * NT * CG;        // query columns
     static constexpr int QT = NCOL / G;             // new tokens per work tile
-    static constexpr int WPH = NWC, KPW = BT / NWC;
+    static constexpr int WPH = NWC, KPW = BT / KW;
     static constexpr int ROWB = D * 2, HPU = G, SWB = 128, NBLK = ROWB / SWB, CPB = SWB / 16;
     static constexpr int TILE_BYTES = BT * ROWB;
     static constexpr int QBYTES = 0;
@@ -39,15 +44,16 @@ struct MultiCfg {
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES + (MASK ? 1024 : 0);
     static constexpr int NPART = 4;                 // merge in quarters of D
     static constexpr int MRG_OFF = NS * STAGE_BYTES;
-    static constexpr int MRG_BYTES = NWC * NCOL * (D / NPART + 2) * 4;
+    static constexpr int MRG_BYTES = KW * NCOL * (D / NPART + 2) * 4;
     static constexpr int HDR_OFF = MRG_OFF + MRG_BYTES;
     static constexpr int HDR_INTS = 8;
     static constexpr int MISC_OFF = HDR_OFF + NS * HDR_INTS * 4;
     static constexpr int BAR_OFF = (MISC_OFF + 16 + 7) & ~7;
     static constexpr int SMEM = BAR_OFF + (2 * NS + 1) * 8 + 1024;
     static constexpr int THREADS = (NWC + 1) * 32;
-    static_assert(KPW == 16 && NCOL % G == 0 && QT >= 1 && STAGE_BYTES % 1024 == 0 && QT * BT <= 1024,
+    static_assert(KPW == 16 && NCOL % G == 0 && QT >= 1 && STAGE_BYTES % 1024 == 0 && (!MASK || QT * BT <= 1024),
                   "multi-token tiling");
+    static_assert(!MASK || CG == 1, "masked tiles use one column group");
 };
 
 template <class C>
@@ -57,7 +63,7 @@ struct MultiConsumer {
     float acc[KS][NT][4];
     float m_run[NT][2], l_run[NT][2];
     float qscale;
-    int warp, lane, g, t, key0, nq, p_base;
+    int warp, lane, g, t, kw, key0, col0, nq, p_base;
     static constexpr int hh = 0;
 
     __device__ __forceinline__ void init(int w, int l, uint8_t *) {
@@ -65,7 +71,9 @@ struct MultiConsumer {
         lane = l;
         g = l >> 2;
         t = l & 3;
-        key0 = w * C::KPW;
+        kw = w % C::KW;
+        key0 = kw * C::KPW;
+        col0 = (w / C::KW) * (8 * NT);  // first query column of this warp's group
     }
 
     __device__ __forceinline__ void reset() {
@@ -92,7 +100,7 @@ struct MultiConsumer {
         p_base = pos0;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-            const int c = n * 8 + g;
+            const int c = col0 + n * 8 + g;
             const int ti = c / G, hc = c % G;
 #pragma unroll
             for (int k = 0; k < KS; ++k) {
@@ -151,7 +159,7 @@ struct MultiConsumer {
             float s[4];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int col = n * 8 + 2 * t + j;
+                const int col = col0 + n * 8 + 2 * t + j;
                 const int ti = col / G;
                 const int lim = p_base + ti;  // this column's token sees keys <= lim
                 bool keep0 = ti < nq && g < nv && kpos0 <= lim;
@@ -209,10 +217,10 @@ struct MultiConsumer {
         }
     }
 
-    // merge the four warps per column in C::NPART parts of D; emit(col, d, a0, a1, M, l)
+    // merge the four key slices per column in C::NPART parts of D; emit(col, d, a0, a1, M, l)
     template <class Sync, class Emit>
     __device__ __forceinline__ bool finish(float *mrg, Sync sync, Emit emit) {
-        constexpr int NWC = C::NWC, NC = C::NCOL, DP = D / C::NPART, MP = KS / C::NPART;
+        constexpr int NWC = C::NWC, KW = C::KW, NC = C::NCOL, DP = D / C::NPART, MP = KS / C::NPART;
 #pragma unroll
         for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -220,15 +228,15 @@ struct MultiConsumer {
                 l_run[n][0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[n][0], o);
                 l_run[n][1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[n][1], o);
             }
-        float *macc = mrg;               // [NWC][NC][DP]
-        float *mml = mrg + NWC * NC * DP;  // [NWC][NC][2]
+        float *macc = mrg;               // [KW][NC][DP]
+        float *mml = mrg + KW * NC * DP;   // [KW][NC][2]
         if (g == 0) {
 #pragma unroll
             for (int n = 0; n < NT; ++n)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    mml[(warp * NC + n * 8 + 2 * t + j) * 2 + 0] = m_run[n][j];
-                    mml[(warp * NC + n * 8 + 2 * t + j) * 2 + 1] = l_run[n][j];
+                    mml[(kw * NC + col0 + n * 8 + 2 * t + j) * 2 + 0] = m_run[n][j];
+                    mml[(kw * NC + col0 + n * 8 + 2 * t + j) * 2 + 1] = l_run[n][j];
                 }
         }
         const int tid = warp * 32 + lane;
@@ -241,7 +249,7 @@ struct MultiConsumer {
                 for (int n = 0; n < NT; ++n)
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        float *row = macc + (warp * NC + n * 8 + 2 * t + j) * DP;
+                        float *row = macc + (kw * NC + col0 + n * 8 + 2 * t + j) * DP;
                         row[d] = acc[m][n][j];
                         row[d + 8] = acc[m][n][j + 2];
                     }
@@ -252,11 +260,11 @@ struct MultiConsumer {
                 if (col / G < nq) {
                     float M = -INFINITY;
 #pragma unroll
-                    for (int w = 0; w < NWC; ++w) M = fmaxf(M, mml[(w * NC + col) * 2]);
+                    for (int w = 0; w < KW; ++w) M = fmaxf(M, mml[(w * NC + col) * 2]);
                     const float Mu = (M == -INFINITY) ? 0.f : M;
                     float a0 = 0.f, a1 = 0.f, lv = 0.f;
 #pragma unroll
-                    for (int w = 0; w < NWC; ++w) {
+                    for (int w = 0; w < KW; ++w) {
                         const float f = ex2(mml[(w * NC + col) * 2] - Mu);
                         lv = fmaf(f, mml[(w * NC + col) * 2 + 1], lv);
                         const float2 x = *reinterpret_cast<const float2 *>(macc + (w * NC + col) * DP + dd);
@@ -566,9 +574,9 @@ bool encode_mask_map(CUtensorMap *map, const void *base, long long stride, long 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int G, int NT, bool MASK>
+template <int D, int G, int NT, bool MASK, int CG>
 dap_status launch_multi(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
-    using C = MultiCfg<D, G, NT, MASK>;
+    using C = MultiCfg<D, G, NT, MASK, CG>;
     const int R = gcd_int(a.page_size, C::BT);
     p.box_rows = R;
     CUtensorMap mk, mv, mm;
@@ -608,40 +616,50 @@ dap_status launch_multi(const DecodeArgs &a, SplitParams &p, cudaStream_t stream
 
 }  // namespace
 
-int multi_tokens_per_tile(int G) { return G >= 1 && G <= 16 ? 16 / G : 0; }
+int multi_tokens_per_tile(int G, int max_q_len) {
+    if (G < 1 || G > 16) return 0;
+    return max_q_len <= 16 / G ? 16 / G : 32 / G;
+}
 
 namespace {
 
-template <int D, int NT, bool MASK>
+template <int D, int NT, bool MASK, int CG>
 dap_status dispatch_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
     switch (a.Hq / a.Hkv) {
-        case 1: return launch_multi<D, 1, NT, MASK>(a, p, stream);
-        case 2: return launch_multi<D, 2, NT, MASK>(a, p, stream);
-        case 4: return launch_multi<D, 4, NT, MASK>(a, p, stream);
-        case 8: return launch_multi<D, 8, NT, MASK>(a, p, stream);
+        case 1: return launch_multi<D, 1, NT, MASK, CG>(a, p, stream);
+        case 2: return launch_multi<D, 2, NT, MASK, CG>(a, p, stream);
+        case 4: return launch_multi<D, 4, NT, MASK, CG>(a, p, stream);
+        case 8: return launch_multi<D, 8, NT, MASK, CG>(a, p, stream);
     }
     return DAP_ERR_UNSUPPORTED;
 }
 
-template <int NT, bool MASK>
+template <int NT, bool MASK, int CG>
 dap_status dispatch_d(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
-    if (a.D == 128) return dispatch_g<128, NT, MASK>(a, p, stream);
-    if (a.D == 64) return dispatch_g<64, NT, MASK>(a, p, stream);
+    if (a.D == 128) return dispatch_g<128, NT, MASK, CG>(a, p, stream);
+    if (a.D == 64) return dispatch_g<64, NT, MASK, CG>(a, p, stream);
     return DAP_ERR_UNSUPPORTED;
 }
 
 }  // namespace
 
+// Multi-token decode: 16-column tiles (tokens_per_tile = 16 / G), or 32-column tiles
+// (32 / G) in two column groups; with a mask, 16-column tiles only.
 dap_status launch_decode_multi(const DecodeArgs &a, cudaStream_t stream) {
     SplitParams p = make_params(a);
-    return a.mask ? dispatch_d<2, true>(a, p, stream) : dispatch_d<2, false>(a, p, stream);
+    const int G = a.Hq / a.Hkv;
+    if (a.tokens_per_tile * G == 32) {
+        if (a.mask) return DAP_ERR_UNSUPPORTED;
+        return dispatch_d<2, false, 2>(a, p, stream);
+    }
+    return a.mask ? dispatch_d<2, true, 1>(a, p, stream) : dispatch_d<2, false, 1>(a, p, stream);
 }
 
 // Masked single-token decode: one token per sequence with no work map (tile w = sequence w),
 // one n8 tile of query columns (G heads of the one token).
 dap_status launch_decode_masked(const DecodeArgs &a, cudaStream_t stream) {
     SplitParams p = make_params(a);
-    return dispatch_d<1, true>(a, p, stream);
+    return dispatch_d<1, true, 1>(a, p, stream);
 }
 
 bool read_errors_multi(unsigned int *flags, bool clear) {

@@ -378,13 +378,13 @@ def long_paged(B=1, device="cpu") -> PagedCase:
                                 f"L=32768")
 
 
-def spec_verify_paged(device="cpu", B=128, q_len=4) -> MultiCase:
-    """Speculative-decoding verification: the ragged decode batch (B=128, Hq=32, Hkv=8,
-    D=128, page_size 16, kv_len U{256..4096}) with q_len new tokens per sequence attending
-    causally."""
+def spec_verify_paged(device="cpu", B=128, q_len=4, Hq=32) -> MultiCase:
+    """Speculative-decoding verification: the ragged decode batch (B=128, Hq=32 or 64,
+    Hkv=8, D=128, page_size 16, kv_len U{256..4096}) with q_len new tokens per sequence
+    attending causally."""
     lens = uniform_lengths(B, 256, 4096, 298003)
-    return make_multi_case(B, 32, 8, 128, 16, lens, [q_len] * B, 298006, device=device,
-                           name=f"multi-token GQA decode B={B} q_len={q_len} Hq=32 Hkv=8 D=128 ps=16 "
+    return make_multi_case(B, Hq, 8, 128, 16, lens, [q_len] * B, 298006, device=device,
+                           name=f"multi-token GQA decode B={B} q_len={q_len} Hq={Hq} Hkv=8 D=128 ps=16 "
                                 f"L~U[256,4096]")
 
 

@@ -178,7 +178,12 @@ def test_append_validation(lib):
 # ---- multi-token decode: host work map and validation -------------------------------------
 
 def test_multi_tokens_per_tile(lib):
+    # 16 query columns while the longest new-token run fits them, else 32 (one K/V stream
+    # for up to 32 / G tokens of a sequence)
     assert [binding.multi_tokens_per_tile(8 * g, 8) for g in (1, 2, 4, 8)] == [16, 8, 4, 2]
+    assert [binding.multi_tokens_per_tile(8 * g, 8, 4) for g in (1, 2, 4, 8)] == [16, 8, 4, 4]
+    assert [binding.multi_tokens_per_tile(8 * g, 8, 17) for g in (1, 2, 4, 8)] == [32, 16, 8, 4]
+    assert binding.multi_tokens_per_tile(64, 8, 2) == 2 and binding.multi_tokens_per_tile(64, 8, 3) == 4
     assert binding.multi_tokens_per_tile(30, 8) == 0 and binding.multi_tokens_per_tile(8, 0) == 0
 
 
@@ -223,11 +228,11 @@ def test_workspace_bytes_multi():
 
 def multi_call(lib, **kw):
     a = dict(q=FAKE, qst=32 * 128, qsh=128, k=FAKE, v=FAKE, P=64, ps=16, table=FAKE, maxp=8, lens=FAKE,
-             qi=FAKE, tb=FAKE, ti=FAKE, ntiles=2, totq=8, maxlen=100, B=2, Hq=32, Hkv=8, D=128, scale=0.088,
+             qi=FAKE, tb=FAKE, ti=FAKE, ntiles=2, tpt=4, totq=8, maxlen=100, B=2, Hq=32, Hkv=8, D=128, scale=0.088,
              S=1, ws=None, wsb=0, out=FAKE, ost=32 * 128, osh=128)
     a.update(kw)
     return lib.decode_attn_paged_multi(a["q"], a["qst"], a["qsh"], a["k"], a["v"], a["P"], a["ps"], a["table"],
-                                       a["maxp"], a["lens"], a["qi"], a["tb"], a["ti"], a["ntiles"], a["totq"],
+                                       a["maxp"], a["lens"], a["qi"], a["tb"], a["ti"], a["ntiles"], a["tpt"], a["totq"],
                                        a.get("mask"), a.get("mst", 0), a["maxlen"], a["B"], a["Hq"], a["Hkv"],
                                        a["D"], a["scale"], a["S"], a["ws"], a["wsb"], a["out"], a["ost"], a["osh"],
                                        None)
@@ -242,6 +247,7 @@ def multi_call(lib, **kw):
     (dict(qi=ctypes.c_void_p((1 << 20) + 2)), 5), (dict(qst=4100), 5),
     (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=16), 4),
     (dict(mask=FAKE, mst=96), 2), (dict(mask=FAKE, mst=120), 5), (dict(mask=ctypes.c_void_p((1 << 20) + 4), mst=128), 5),
+    (dict(tpt=3), 2), (dict(tpt=16), 2), (dict(tpt=0), 2), (dict(tpt=8, mask=FAKE, mst=128), 3),
 ])
 def test_multi_validation(lib, kw, status):
     assert multi_call(lib, **kw) == status

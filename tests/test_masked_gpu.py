@@ -119,7 +119,8 @@ def test_multi_token_mask_with_causal_rule(Hq, Hkv, D, qlens):
     qi = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
     ref = oracle.decode_paged_multi(bits(case.q), bits(kv.k_cache), bits(kv.v_cache), kv.block_table.cpu().numpy(),
                                     kv.seq_lens.cpu().numpy(), qi, kv.scale, mask=full.numpy())
-    plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, "cuda")
+    # a mask rides with 16-column tiles
+    plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, "cuda", tokens_per_tile=binding.multi_tokens_per_tile(kv.Hq, kv.Hkv))
     for S in [1, 3]:
         got = binding.decode_attn_paged_multi(case.q, kv.k_cache, kv.v_cache, kv.block_table, kv.seq_lens, plan,
                                               max_kv_len=kv.max_kv_len, scale=kv.scale, num_splits=S,

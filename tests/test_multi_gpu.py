@@ -52,12 +52,20 @@ def _clean_errors():
     yield
 
 
+def tile_sizes(Hq, Hkv):
+    """Both tile sizes of the work map: 16 and 32 query columns."""
+    G = Hq // Hkv
+    return [16 // G, 32 // G]
+
+
 def test_small_case_several_tiles_and_split_counts():
-    # G = 4: 4 tokens per q tile; 9 new tokens -> three tiles, the last ragged
+    # G = 4: 4 (or 8) tokens per q tile; 9 new tokens -> three (two) tiles, the last ragged
     case = inputs.make_multi_case(3, 8, 2, 64, 16, [100, 37, 300], [5, 1, 9], 4001).to("cuda")
     ref = oracle_multi(case)
-    for S in [0, 1, 2, 3, 5]:
-        assert_close(gpu_multi(case, S), ref, f"S={S}")
+    for tpt in tile_sizes(8, 2):
+        plan = binding.MultiPlan(case.q_lens, 8, 2, "cuda", tokens_per_tile=tpt)
+        for S in [0, 1, 2, 3, 5]:
+            assert_close(gpu_multi(case, S, plan=plan), ref, f"tpt={tpt} S={S}")
     assert binding.get_device_errors() == 0
 
 
@@ -75,8 +83,10 @@ SHAPES = [
 def test_parity_across_groups_and_dims(B, Hq, Hkv, D, ps, lens, qlens):
     case = inputs.make_multi_case(B, Hq, Hkv, D, ps, lens, qlens, 4100 + Hq + D).to("cuda")
     ref = oracle_multi(case)
-    for S in [1, 4]:
-        assert_close(gpu_multi(case, S), ref, f"G={Hq // Hkv} D={D} S={S}")
+    for tpt in tile_sizes(Hq, Hkv):
+        plan = binding.MultiPlan(case.q_lens, Hq, Hkv, "cuda", tokens_per_tile=tpt)
+        for S in [0, 1, 4]:
+            assert_close(gpu_multi(case, S, plan=plan), ref, f"G={Hq // Hkv} D={D} tpt={tpt} S={S}")
     assert binding.get_device_errors() == 0
 
 
@@ -131,6 +141,19 @@ def test_full_size_speculative_verification():
     out = gpu_multi(case, 0, total_kv=case.kv.total_kv)
     assert_close(out, ref, "full size, benchmark launch")
     assert_close(gpu_multi(case, 0), ref, "full size, S resolved by the library")
+    assert binding.get_device_errors() == 0
+
+
+@pytest.mark.parametrize("q_len", [4, 8])
+def test_full_size_eight_heads_per_kv_head(q_len):
+    """The ragged B=128 batch at Hq=64, Hkv=8 (G = 8) with 4 or 8 new tokens per sequence:
+    32-column tiles put all of a sequence's tokens (or half of them, at 8) against one K/V
+    stream; every output element against the oracle, at the planner's split count."""
+    case = inputs.spec_verify_paged(device="cuda", q_len=q_len, Hq=64)
+    plan = binding.MultiPlan(case.q_lens, 64, 8, "cuda")
+    assert plan.tokens_per_tile == 4 and plan.num_tiles == 128 * (q_len // 4)
+    ref = oracle_multi(case)
+    assert_close(gpu_multi(case, 0, plan=plan, total_kv=case.kv.total_kv), ref, f"G=8 q_len={q_len}")
     assert binding.get_device_errors() == 0
 
 
