@@ -294,9 +294,9 @@ size_t dap_workspace_bytes_multi(int total_q, int Hq, int D, int num_splits);
  *   workspace    device, >= dap_workspace_bytes_multi(total_q, Hq, D, S) bytes for the
  *                split count S used, 16-byte aligned.
  *   out          device bf16 [total_q, Hq, D], strides (out_stride_t, out_stride_h, 1).
- *   Supported: D in {64, 128}; G in {1, 2, 4, 8}; page_size a multiple of 8; alignment and
- *   strides as decode_attn_paged.  A work-map entry that names no token of its sequence is
- *   skipped and flagged (DAP_DEVERR_QMAP).
+ *   Supported: D in {32, 64, 128, 256}; G in {1, 2, 4, 8}; page_size a multiple of 8;
+ *   alignment and strides as decode_attn_paged.  A work-map entry that names no token of its
+ *   sequence is skipped and flagged (DAP_DEVERR_QMAP).
  */
 dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long long q_stride_h,
                                    const void *k_cache, const void *v_cache, int num_pages,
@@ -319,8 +319,8 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
  *                (dap_resolve_splits(0, SMs, B, Hq, Hkv, D, page_size, max_kv_len, 0)).
  *                DAP_SPLITS_BALANCED is not supported here.
  *   workspace    >= dap_workspace_bytes(B, Hq, Hkv, D, S) for the S used.
- *   Everything else as decode_attn_paged.  Supported: D in {64, 128}; G in {1, 2, 4, 8};
- *   page_size a multiple of 8.
+ *   Everything else as decode_attn_paged.  Supported: D in {32, 64, 128, 256}; G in
+ *   {1, 2, 4, 8}; page_size a multiple of 8.
  */
 dap_status decode_attn_paged_masked(const void *q, long long q_stride_b, long long q_stride_h,
                                     const void *k_cache, const void *v_cache, int num_pages,

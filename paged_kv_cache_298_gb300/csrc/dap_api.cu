@@ -333,7 +333,7 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table) || !aligned4(qo_indptr) ||
         !aligned4(tile_batch) || !aligned4(tile_index))
         return DAP_ERR_ALIGN;
-    if (page_size % 8 != 0 || !(D == 64 || D == 128)) return DAP_ERR_UNSUPPORTED;
+    if (page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
     {
         const int G = Hq / Hkv;
         if (tokens_per_tile * G != 16 && tokens_per_tile * G != 32) return DAP_ERR_SHAPE;
@@ -394,7 +394,7 @@ dap_status decode_attn_paged_masked(const void *q, long long q_stride_b, long lo
     if (!k_cache || !v_cache || !block_table) return DAP_ERR_NULL;
     if (!mask) return DAP_ERR_NULL;
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table)) return DAP_ERR_ALIGN;
-    if (page_size % 8 != 0 || !(D == 64 || D == 128)) return DAP_ERR_UNSUPPORTED;
+    if (page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
     if ((st = check_mask(mask, mask_stride, max_kv_len)) != DAP_OK) return st;
     int S = 0, chunk = 0;
     if ((st = resolve_splits(B, B, Hq, Hkv, D, page_size, max_kv_len, num_splits, workspace, workspace_bytes, false,

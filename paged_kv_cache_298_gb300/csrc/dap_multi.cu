@@ -27,22 +27,26 @@ namespace dap {
 // w and w + 4 take the same 16 keys of every tile for columns 0..15 and 16..31, so all
 // of a sequence's new tokens meet each K/V tile once); MASK: a bool mask tile rides with
 // every K/V tile.
+// Head dims: 64 and 128 in 64-key tiles of 128-byte-swizzled column blocks; 256 in 32-key
+// tiles (two key slices, so a stage stays near 32 KB at two CTAs per SM); 32 in 64-key
+// tiles of 64-byte rows with the 64-byte swizzle, six stages.
 template <int D_, int G_, int NT_ = 2, bool MASK_ = false, int CG_ = 1>
 struct MultiCfg {
-    static constexpr int CG = CG_, KW = 4;           // column groups, key slices
-    static constexpr int D = D_, G = G_, HG = 1, NWC = KW * CG, BT = 64;
-    static constexpr int NS = CG == 2 ? 5 : 3, MINB = CG == 2 ? 1 : 2;
+    static constexpr int CG = CG_, KW = D_ == 256 ? 2 : 4;  // column groups, key slices
+    static constexpr int D = D_, G = G_, HG = 1, NWC = KW * CG, BT = 16 * KW;
+    static constexpr int NS = D == 32 ? 6 : (CG == 2 ? 5 : 3);
+    static constexpr int MINB = D == 32 ? (CG == 2 ? 2 : 3) : (CG == 2 ? 1 : 2);
     static constexpr bool MMA = true, SWZ = true, MASK = MASK_;
     static constexpr int NT = NT_;
     static constexpr int NCOL = 8 * NT * CG;        // query columns
     static constexpr int QT = NCOL / G;             // new tokens per work tile
     static constexpr int WPH = NWC, KPW = BT / KW;
-    static constexpr int ROWB = D * 2, HPU = G, SWB = 128, NBLK = ROWB / SWB, CPB = SWB / 16;
+    static constexpr int ROWB = D * 2, HPU = G, SWB = D >= 64 ? 128 : 64, NBLK = ROWB / SWB, CPB = SWB / 16;
     static constexpr int TILE_BYTES = BT * ROWB;
     static constexpr int QBYTES = 0;
     static constexpr int MASK_OFF = 2 * TILE_BYTES;  // [QT tokens][BT keys] bytes, 1024-aligned
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES + (MASK ? 1024 : 0);
-    static constexpr int NPART = 4;                 // merge in quarters of D
+    static constexpr int NPART = D == 32 ? 2 : 4;   // merge in parts of D (16 dims or more each)
     static constexpr int MRG_OFF = NS * STAGE_BYTES;
     static constexpr int MRG_BYTES = KW * NCOL * (D / NPART + 2) * 4;
     static constexpr int HDR_OFF = MRG_OFF + MRG_BYTES;
@@ -54,6 +58,7 @@ struct MultiCfg {
     static_assert(KPW == 16 && NCOL % G == 0 && QT >= 1 && STAGE_BYTES % 1024 == 0 && (!MASK || QT * BT <= 1024),
                   "multi-token tiling");
     static_assert(!MASK || CG == 1, "masked tiles use one column group");
+    static_assert((D / 16) % NPART == 0 && ROWB % SWB == 0, "whole 16-dim steps per merge part");
 };
 
 template <class C>
@@ -115,9 +120,13 @@ struct MultiConsumer {
         }
     }
 
+    // byte offset of (key, dim) in a swizzled [NBLK][BT][SWB] tile: the 128-byte swizzle XORs
+    // the 16-byte chunk index with key & 7, the 64-byte one with (key >> 1) & 3
     static __device__ __forceinline__ uint32_t off(int key, int dim) {
-        const int chunk = (dim & 63) >> 3;
-        return (uint32_t)((dim >> 6) * (C::BT * 128) + key * 128 + ((chunk ^ (key & 7)) << 4));
+        const int byte = dim * 2;
+        const int chunk = (byte % C::SWB) >> 4;
+        const int sw = C::SWB == 128 ? (key & 7) : ((key >> 1) & 3);
+        return (uint32_t)((byte / C::SWB) * (C::BT * C::SWB) + key * C::SWB + ((chunk ^ sw) << 4));
     }
 
     // tile_pos: absolute position of the tile's first key
@@ -125,12 +134,12 @@ struct MultiConsumer {
         const int nv = nvalid - key0;
         if (nv <= 0) return;
         uint8_t *sV = stage + C::TILE_BYTES;
-        if (nv < 16) {
-            for (int i = lane; i < (16 - nv) * C::NBLK * 8; i += 32) {
-                const int row = key0 + nv + i / (C::NBLK * 8);
-                const int rest = i % (C::NBLK * 8);
-                *reinterpret_cast<uint4 *>(sV + (rest >> 3) * (C::BT * 128) + row * 128 + (rest & 7) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
+        if (nv < 16) {  // rows past the end may hold anything: zero their V so 0 * V stays 0
+            for (int i = lane; i < (16 - nv) * C::NBLK * C::CPB; i += 32) {
+                const int row = key0 + nv + i / (C::NBLK * C::CPB);
+                const int rest = i % (C::NBLK * C::CPB);
+                *reinterpret_cast<uint4 *>(sV + (rest / C::CPB) * (C::BT * C::SWB) + row * C::SWB +
+                                           (rest % C::CPB) * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -415,7 +424,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
                 issue_kv_box<C>(smem + st * C::STAGE_BYTES, lane, R, &mapK, &mapV, kvh, tt % p.page_size, pg,
                                 &full[st]);
             }
-            // the tile's mask bytes: keys [t, t + 64) of the tile's tokens (zeros past the ends)
+            // the tile's mask bytes: keys [t, t + BT) of the tile's tokens (zeros past the ends)
             if (C::MASK && lane == 31)
                 tma_load_3d(smem + st * C::STAGE_BYTES + C::MASK_OFF, &mapM, t, tl.q0 + tl.i0, 0, &full[st]);
             issued = i + 1;
@@ -561,13 +570,13 @@ __global__ void __launch_bounds__(256) combine_multi_kernel(const SplitParams p,
 
 namespace {
 
-// mask [rows, mask_stride] bytes viewed as [mask_stride, rows, 1]; box [64, QT, 1]
-bool encode_mask_map(CUtensorMap *map, const void *base, long long stride, long long rows, int qt) {
+// mask [rows, mask_stride] bytes viewed as [mask_stride, rows, 1]; box [BT, QT, 1]
+bool encode_mask_map(CUtensorMap *map, const void *base, long long stride, long long rows, int qt, int bt) {
     EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)stride, (cuuint64_t)rows, 1u};
     const cuuint64_t strides[2] = {(cuuint64_t)stride, (cuuint64_t)(stride * rows)};
-    const cuuint32_t box[3] = {64u, (cuuint32_t)qt, 1u};
+    const cuuint32_t box[3] = {(cuuint32_t)bt, (cuuint32_t)qt, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -583,7 +592,7 @@ dap_status launch_multi(const DecodeArgs &a, SplitParams &p, cudaStream_t stream
     memset(&mm, 0, sizeof mm);
     if (!encode_cache_map<C>(&mk, a.k, a.D, a.Hkv, a.page_size, a.num_pages, R) ||
         !encode_cache_map<C>(&mv, a.v, a.D, a.Hkv, a.page_size, a.num_pages, R) ||
-        (MASK && !encode_mask_map(&mm, a.mask, a.mask_stride, a.total_q, C::QT)))
+        (MASK && !encode_mask_map(&mm, a.mask, a.mask_stride, a.total_q, C::QT, C::BT)))
         return DAP_ERR_CUDA;
     auto kern = multi_kernel<C>;
     static PerDeviceOcc occ = {};
@@ -636,8 +645,12 @@ dap_status dispatch_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) 
 
 template <int NT, bool MASK, int CG>
 dap_status dispatch_d(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
-    if (a.D == 128) return dispatch_g<128, NT, MASK, CG>(a, p, stream);
-    if (a.D == 64) return dispatch_g<64, NT, MASK, CG>(a, p, stream);
+    switch (a.D) {
+        case 32: return dispatch_g<32, NT, MASK, CG>(a, p, stream);
+        case 64: return dispatch_g<64, NT, MASK, CG>(a, p, stream);
+        case 128: return dispatch_g<128, NT, MASK, CG>(a, p, stream);
+        case 256: return dispatch_g<256, NT, MASK, CG>(a, p, stream);
+    }
     return DAP_ERR_UNSUPPORTED;
 }
 

@@ -243,7 +243,6 @@ def multi_call(lib, **kw):
     (dict(Hq=30), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(S=-2), 2), (dict(S=-1), 3), (dict(qsh=0), 2),
     (dict(q=None), 1), (dict(qi=None), 1), (dict(tb=None), 1), (dict(ti=None), 1), (dict(table=None), 1),
     (dict(D=96), 3), (dict(ps=12, maxlen=90), 3), (dict(Hq=64, Hkv=4), 3),
-    (dict(D=256, qst=32 * 256, qsh=256, ost=32 * 256, osh=256), 3),
     (dict(qi=ctypes.c_void_p((1 << 20) + 2)), 5), (dict(qst=4100), 5),
     (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=16), 4),
     (dict(mask=FAKE, mst=96), 2), (dict(mask=FAKE, mst=120), 5), (dict(mask=ctypes.c_void_p((1 << 20) + 4), mst=128), 5),
@@ -315,7 +314,7 @@ def masked_call(lib, **kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(B=-1), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(mst=96), 2), (dict(S=-2), 2), (dict(S=-1), 3),
     (dict(mask=None), 1), (dict(q=None), 1), (dict(table=None), 1),
-    (dict(D=96), 3), (dict(ps=12, maxlen=90), 3), (dict(D=32, qsb=32 * 32, qsh=32, osb=32 * 32, osh=32), 3),
+    (dict(D=96), 3), (dict(ps=12, maxlen=90), 3), (dict(D=48, qsb=32 * 48, qsh=48, osb=32 * 48, osh=48), 3),
     (dict(mst=120), 5), (dict(mask=ctypes.c_void_p((1 << 20) + 8)), 5),
     (dict(S=4), 4),
 ])

@@ -62,6 +62,10 @@ SHAPES = [
     (4, 16, 8, 64, 32, [65, 130, 9, 500]),     # G=2
     (3, 32, 8, 128, 16, [257, 1000, 17]),      # G=4
     (2, 64, 8, 128, 64, [128, 777]),           # G=8
+    (3, 16, 4, 256, 16, [300, 17, 64]),        # D=256: 32-key tiles, two key slices
+    (2, 64, 8, 256, 8, [100, 513]),            # D=256, G=8, page 8
+    (3, 16, 16, 32, 16, [1, 200, 65]),         # D=32: 64-byte swizzle, G=1
+    (2, 32, 4, 32, 32, [700, 5]),              # D=32, G=8
 ]
 
 
@@ -110,7 +114,8 @@ def test_full_size_ragged_with_mask():
 
 # ---- multi-token decode with a mask ---------------------------------------------------
 
-@pytest.mark.parametrize("Hq,Hkv,D,qlens", [(8, 2, 64, [5, 1, 9]), (32, 8, 128, [4, 4, 2]), (16, 2, 128, [3, 2, 1])])
+@pytest.mark.parametrize("Hq,Hkv,D,qlens", [(8, 2, 64, [5, 1, 9]), (32, 8, 128, [4, 4, 2]), (16, 2, 128, [3, 2, 1]),
+                                            (16, 4, 256, [5, 1, 7]), (64, 8, 32, [2, 1, 2])])
 def test_multi_token_mask_with_causal_rule(Hq, Hkv, D, qlens):
     lens = [100, 37, 300]
     case = inputs.make_multi_case(3, Hq, Hkv, D, 16, lens, qlens, 6500 + Hq).to("cuda")

@@ -76,6 +76,10 @@ SHAPES = [
     (2, 32, 8, 128, 16, [257, 1000], [4, 13]),                 # G=4, tile edges at 4
     (3, 64, 8, 128, 64, [128, 1, 777], [2, 1, 7]),              # G=8: 2 tokens per tile, L = q_len
     (2, 16, 2, 64, 8, [300, 64], [30, 64]),                     # G=8, D=64, every key new
+    (3, 16, 4, 256, 16, [300, 17, 64], [9, 3, 5]),              # D=256 (32-key tiles), G=4
+    (2, 64, 8, 256, 8, [100, 513], [3, 6]),                      # D=256, G=8, page 8
+    (3, 16, 16, 32, 16, [1, 200, 65], [1, 20, 33]),              # D=32 (64-byte swizzle), G=1
+    (2, 32, 4, 32, 32, [700, 5], [11, 5]),                       # D=32, G=8
 ]
 
 
