@@ -391,7 +391,7 @@ class Leg:
     extra: dict = field(default_factory=dict)
 
 
-def prepare_leg(key, case, dev, l2, splits=None) -> Leg:
+def prepare_leg(key, case, dev, l2, splits=None, tpt=None) -> Leg:
     """Rotated device copies of the inputs, the step, the end-to-end copies and the bytes."""
     from paged_kv_cache_298_gb300 import binding, inputs
     sms = binding.device_sm_count()
@@ -498,14 +498,15 @@ def prepare_leg(key, case, dev, l2, splits=None) -> Leg:
 
     if key.startswith("multi"):
         kv = case.kv
-        mplan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, dev)
+        mplan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, dev, tokens_per_tile=tpt)
         S = plan(mplan.num_tiles, kv.Hq, kv.Hkv, kv.D, kv.page_size, kv.max_kv_len, kv.total_kv)
         run = binding.resolve_splits(S, sms, mplan.num_tiles, kv.Hq, kv.Hkv, kv.D, kv.page_size, kv.max_kv_len)
         parts = (case.q, kv.k_cache, kv.v_cache, kv.block_table, kv.seq_lens)
         footprint = sum(t.numel() * t.element_size() for t in parts)
         sets = rotated(lambda i: parts if i == 0 else tuple(t.clone() for t in parts), footprint, l2)
         n = len(sets)
-        plans = [binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, dev) for _ in sets]
+        plans = [binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, dev, tokens_per_tile=mplan.tokens_per_tile)
+                 for _ in sets]
         ws = [torch.empty(max(1, binding.workspace_bytes_multi(case.total_q, kv.Hq, kv.D, run)), dtype=torch.uint8,
                           device=dev) for _ in sets]
         outs = [torch.empty_like(case.q) for _ in sets]
@@ -784,7 +785,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     key = args.workload or "ragged"
     case = make_case(key, dev, args.batch)
-    leg = prepare_leg(key, case, dev, l2, args.splits)
+    leg = prepare_leg(key, case, dev, l2, args.splits, args.tpt or None)
     K, W = args.steps, args.warmup
     clocks = ClockSampler(local)
     r = measure(leg, K, W, stream, world, clocks)
@@ -969,6 +970,8 @@ def main():
     ap.add_argument("--splits", type=int, default=None,
                     help="num_splits passed to the library (default: the planner's S made with the summed "
                          "lengths; 0 = the library's own plan; -1 = balanced schedule; S > 0 = per-sequence)")
+    ap.add_argument("--tpt", type=int, default=0,
+                    help="multi-token workloads: tokens per work-map tile (0 = the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-legs", action="store_true", help="the headline only")
     ap.add_argument("--batch", type=int, default=0,

@@ -148,14 +148,34 @@ def _device_of(what: str, first, **others) -> torch.device:
     if not getattr(first, "is_cuda", False):
         raise DapError(None, f"{what}: the first tensor must be a CUDA tensor")
     dev = first.device
+    idx = dev.index
     for name, t in others.items():
         if t is None:
             continue
         if not t.is_cuda:
             raise DapError(None, f"{what}: {name} is not a CUDA tensor")
-        if t.device != dev:
+        if t.device.index != idx:
             raise DapError(None, f"{what}: {name} is on {t.device}, the call's tensors on {dev}")
     return dev
+
+
+class _on:
+    """Makes `dev` the current device for the library call (skipped when it already is)."""
+
+    def __init__(self, dev):
+        self.idx = dev.index
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.idx:
+            self.prev = cur
+            torch.cuda.set_device(self.idx)
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+        return False
 
 
 def _stream(stream, dev: torch.device):
@@ -163,7 +183,7 @@ def _stream(stream, dev: torch.device):
     or that device's current stream."""
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    elif stream.device != dev:
+    elif stream.device.index != dev.index:
         raise DapError(None, f"the stream belongs to {stream.device}, the call's tensors to {dev}")
     return ctypes.c_void_p(stream.cuda_stream)
 
@@ -271,7 +291,7 @@ def decode_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, max_kv_len:
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     _bf16_3d(out, "out")
     lib = load()
-    with torch.cuda.device(dev):
+    with _on(dev):
         S, run = _splits(lib, num_splits, B, Hq, Hkv, D, ps, max_kv_len, total_kv)
         workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes(B, Hq, Hkv, D, run), dev)
         st = lib.decode_attn_paged(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
@@ -301,7 +321,7 @@ def decode_attn_paged_noalloc(q, k_cache, v_cache, block_table, seq_lens, *, max
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     _bf16_3d(out, "out")
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load().decode_attn_paged_noalloc(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P,
                                               ps, _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
                                               int(max_kv_len), B, Hq, Hkv, D, float(scale), int(num_splits),
@@ -329,7 +349,7 @@ def decode_attn_contig(q, k, v, seq_lens, *, max_kv_len: int, scale: float | Non
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     _bf16_3d(out, "out")
     lib = load()
-    with torch.cuda.device(dev):
+    with _on(dev):
         S, run = _splits(lib, num_splits, B, Hq, Hkv, D, max_len, max_kv_len, total_kv)
         workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes(B, Hq, Hkv, D, run), dev)
         st = lib.decode_attn_contig(_ptr(q), q.stride(0), q.stride(1), _ptr(k), _ptr(v), max_len,
@@ -360,7 +380,7 @@ def decode_attn_paged_fp8(q, kv_cache, inv_scale, slot_idx, lens, *, scale: floa
     if out is None:
         out = torch.empty((T, NH, HD), dtype=torch.bfloat16, device=dev)
     _need(out.dtype == torch.bfloat16 and out.shape == q.shape and out.is_contiguous(), "out must match q")
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load().decode_attn_paged_fp8(_ptr(q), _ptr(kv_cache), _ptr(inv_scale), _ptr(slot_idx), _ptr(lens),
                                           T, NH, HD, slot_idx.shape[1], NB, bs, float(scale), _ptr(out),
                                           _stream(stream, dev))
@@ -387,7 +407,7 @@ def decode_attn_paged_masked(q, k_cache, v_cache, block_table, seq_lens, mask, *
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     _bf16_3d(out, "out")
     lib = load()
-    with torch.cuda.device(dev):
+    with _on(dev):
         S, run = _splits(lib, num_splits, B, Hq, Hkv, D, ps, max_kv_len, total_kv)
         workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes(B, Hq, Hkv, D, run), dev)
         st = lib.decode_attn_paged_masked(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
@@ -434,7 +454,7 @@ def decode_attn_paged_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, 
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     _bf16_3d(out, "out")
     lib = load()
-    with torch.cuda.device(dev):
+    with _on(dev):
         S, run = _splits(lib, num_splits, B, Hq, Hkv, D, ps, max_kv_len, total_kv)
         workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes(B, Hq, Hkv, D, run), dev)
         st = lib.decode_attn_paged_fp8kv(_ptr(q), q.stride(0), q.stride(1), _ptr(k_codes), _ptr(v_codes),
@@ -523,7 +543,7 @@ def decode_attn_paged_multi(q, k_cache, v_cache, block_table, seq_lens, plan: Mu
     _bf16_3d(out, "out")
     lib = load()
     mask = _mask(mask, total_q, int(max_kv_len))
-    with torch.cuda.device(dev):
+    with _on(dev):
         S, run = _splits(lib, num_splits, max(plan.num_tiles, 0), Hq, Hkv, D, ps, max_kv_len, total_kv)
         workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes_multi(total_q, Hq, D, run), dev)
         st = lib.decode_attn_paged_multi(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
@@ -555,7 +575,7 @@ def kv_append_paged(k_new, v_new, k_cache, v_cache, block_table, positions, *, s
           and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
     _need(positions.dtype == torch.int32 and positions.numel() == B and positions.is_contiguous(),
           "positions must be contiguous int32 [B]")
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load().kv_append_paged(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
                                     k_cache.shape[1], _ptr(block_table), block_table.shape[1], _ptr(positions), B,
                                     Hkv, D, _stream(stream, dev))
@@ -575,7 +595,7 @@ def kv_append_fp8(rows, kv_cache, inv_scale, slots, *, stream=None):
     _need(inv_scale.dtype == torch.bfloat16 and inv_scale.is_contiguous() and inv_scale.numel() >= NB * bs,
           "inv_scale must be contiguous bf16 with one entry per slot")
     _need(slots.dtype == torch.int64 and slots.numel() == T and slots.is_contiguous(), "slots must be int64 [T]")
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load().kv_append_fp8(_ptr(rows), _ptr(kv_cache), _ptr(inv_scale), _ptr(slots), T, HD, NB, bs,
                                   _stream(stream, dev))
     _check(st, "kv_append_fp8")
@@ -598,7 +618,7 @@ def kv_append_paged_fp8(k_new, v_new, k_codes, v_codes, k_scale, v_scale, block_
           and block_table.shape[0] == B, "block_table must be contiguous int32 [B, max_pages]")
     _need(positions.dtype == torch.int32 and positions.numel() == B and positions.is_contiguous(),
           "positions must be contiguous int32 [B]")
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = load().kv_append_paged_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
                                         _ptr(v_scale), P, ps, _ptr(block_table), block_table.shape[1],
                                         _ptr(positions), B, Hkv, D, _stream(stream, dev))

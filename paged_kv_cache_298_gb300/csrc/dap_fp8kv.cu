@@ -380,7 +380,7 @@ struct Consumer {
 };
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXREG)
+__global__ void __maxnreg__(C::MAXREG)
     fp8kv_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                  const __grid_constant__ CUtensorMap mapKS, const __grid_constant__ CUtensorMap mapVS,
                  const SplitParams p) {
