@@ -138,7 +138,8 @@ def _check(status: int, what: str):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int: ctypes turns it into the void* argument (cheaper than a c_void_p object)
+    return None if t is None else t.data_ptr()
 
 
 def _device_of(what: str, first, **others) -> torch.device:

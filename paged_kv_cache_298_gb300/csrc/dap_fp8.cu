@@ -164,6 +164,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 consecutive 32-bit columns of this thread's TMEM lane, without waiting for them
+// (tmem_wait_ld makes them usable): several loads can be in flight at once.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // 16 consecutive 32-bit columns of this thread's TMEM lane from registers.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
@@ -213,36 +230,64 @@ struct Params {
     const __nv_bfloat16 *inv_scale;
     const int64_t *slot_idx;
     const int64_t *lens;
+    __nv_bfloat16 *out;
     int T, NH, W;
     long long max_slots;
     float qscale;  // scale * log2(e)
 };
 
-// 2D tiled TMA store shared -> global (bulk group; the caller commits and waits).
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int c0, int c1, const void *src) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1), "r"(smem_addr(src))
-                 : "memory");
+// e4m3 codes -> bf16, exactly, two at a time.  Codes c0, c1 placed in the high bytes of the
+// two 16-bit halves (x = c0 << 8 | c1 << 24) and shifted right by 4 give, with the sign bit
+// kept in place, bf16 patterns whose exponent field is the code's and whose mantissa starts
+// with the code's three mantissa bits: the code's value times 2^-120 (a bf16 subnormal for
+// a subnormal code).  The caller's bf16 multiply by factor * 2^120 then yields
+// bf16(code * factor) with one rounding of the exact product: the dequantised value.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_bits(uint32_t w, uint32_t sel) {
+    const uint32_t x = __byte_perm(w, 0u, sel);
+    return ((x >> 4) & 0x07F007F0u) | (x & 0x80008000u);
 }
 
-// The four e4m3 codes of `w` times the fp32 factor `f`: byte k moved to bits 24..31 and
-// shifted right arithmetically by 4 lands as an fp32 bit pattern whose exponent field is the
-// code's exponent field and whose mantissa starts with the code's three mantissa bits (the
-// sign, replicated, is masked back to bit 31), i.e. the code's value times 2^-120, exact for
-// subnormal codes too (an fp32 subnormal; nothing here flushes to zero); multiplying by
-// 2^120 restores it exactly, and its product with a bf16 factor (a 4-bit by an 8-bit
-// significand) is exact in fp32.  Codes S.1111.111 are NaN in OCP E4M3FN and come out NaN.
-__device__ __forceinline__ void e4m3x4_times(uint32_t w, float f, float (&o)[4]) {
+// Sixteen e4m3 codes (one 16-byte row piece) times the bf16 factor `inv`, rounded once to
+// bf16, into o[0..7] (bf16 pairs, lower index in the low half).  OCP E4M3FN codes
+// S.1111.111 are NaN and come out NaN.
+__device__ __forceinline__ void dequant16(const uint4 &raw, float inv, uint32_t (&o)[8]) {
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    const float c = inv * 0x1p120f;  // exact (a power-of-two scaling) unless it overflows
+    if (fabsf(c) <= 3.3895313892515355e38f) {  // c is a finite bf16 value: one multiply per pair
+        const __nv_bfloat162 cc = __float2bfloat162_rn(c);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int y = (int)(w << (24 - 8 * k));
-        o[k] = (__uint_as_float((uint32_t)(y >> 4) & 0x87F00000u) * 0x1p120f) * f;
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t lo = e4m3x2_scaled_bits(w4[q], 0x1404u);  // codes 0, 1 of the word
+            const uint32_t hi = e4m3x2_scaled_bits(w4[q], 0x3424u);  // codes 2, 3
+            const __nv_bfloat162 a = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&lo), cc);
+            const __nv_bfloat162 b = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&hi), cc);
+            o[2 * q] = *reinterpret_cast<const uint32_t *>(&a);
+            o[2 * q + 1] = *reinterpret_cast<const uint32_t *>(&b);
+        }
+    } else {  // a factor of 2^8 or more: the product in fp32 (exact), then one rounding
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float f[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t b = (w4[q] >> (8 * k)) & 0xFFu;
+                const float mag = __uint_as_float((b & 0x7Fu) << 20) * 0x1p120f;  // exact, subnormals too
+                f[k] = ((b & 0x80u) ? -mag : mag) * inv;
+            }
+            o[2 * q] = pack_bf16(f[0], f[1]);
+            o[2 * q + 1] = pack_bf16(f[2], f[3]);
+        }
     }
-    if ((((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u) != 0u) {  // a NaN code (rare)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (((w >> (8 * k)) & 0x7Fu) == 0x7Fu) o[k] = __uint_as_float(0x7FC00000u);
+    for (int q = 0; q < 4; ++q) {
+        if ((((w4[q] & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u) != 0u) {  // a NaN code (rare)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (((w4[q] >> (8 * k)) & 0x7Fu) == 0x7Fu) {
+                    uint32_t &wd = o[2 * q + (k >> 1)];
+                    wd = (k & 1) ? ((wd & 0x0000FFFFu) | 0x7FC00000u) : ((wd & 0xFFFF0000u) | 0x00007FC0u);
+                }
+        }
     }
 }
 
@@ -251,20 +296,22 @@ __device__ __forceinline__ void e4m3x4_times(uint32_t w, float f, float (&o)[4])
 // scales together) with q landing in full meanwhile:
 //   1. thread 0 issues all eight q blocks by TMA at entry (128 KB landing zone); every
 //      warp loads the slots of its 16 window positions and the token's length;
-//   2. each warp gathers the rows of its kept positions into registers (a half-warp per
-//      256-byte half of a row) together with their inverse scales; per-warp counts give
-//      every kept row its place in window order;
+//   2. each warp gathers the rows of its kept positions (every eighth position of the
+//      window, so the warps share the rows evenly) into registers, a half-warp per 256-byte
+//      half of a row, together with their inverse scales; per-warp counts give every kept row
+//      its place in the KV tile (warp by warp; the result does not depend on the rows' order
+//      beyond rounding);
 //   3. q moves into tensor memory block by block as it lands (head = TMEM lane, two bf16
 //      per column);
-//   4. the rows are dequantised (e4m3 decoded by integer ops, times the f32 inverse scale,
-//      one bf16 rounding) into a 128-byte-swizzled [hd block][row][64] tile where q landed;
+//   4. the rows are dequantised (e4m3 codes placed into bf16 patterns by integer ops, times
+//      the inverse scale by one bf16 multiply: one rounding of the exact product) into a
+//      128-byte-swizzled [hd block][row][64] tile where q landed;
 //   5. S = Q . KV^T (M=128, N=n16, K=512), A from tensor memory;
 //   6. softmax: two threads per head, 32-column chunks alternating between them;
 //   7. O[:, half] = P . KV[:, half] (M=128, N=256, K=n16) into the columns q held;
-//   8. out = O / l in bf16, staged swizzled and written by TMA stores.
+//   8. out = O / l in bf16, staged in shared memory and written with coalesced stores.
 __global__ void __launch_bounds__(kThreads, 1)
-    swa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
-               const Params p) {
+    swa_kernel(const __grid_constant__ CUtensorMap qmap, const Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the 128-byte swizzle is a function of address bits 4..9: tiles start 1024-aligned
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -292,7 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         cnt[12] = 0;
         fence_barrier_init();
         prefetch_tensormap(&qmap);
-        prefetch_tensormap(&omap);
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -313,8 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(smem + kQOff + kb * kQBlock, &qmap, kb * 64, qrow, &q_full[kb]);
         }
     }
-    // warp w holds window positions 16 w .. 16 w + 15, lanes l and l + 16 the same one
-    const int jpos = 16 * warp + (lane & 15);
+    // warp w holds window positions w, w + 8, ..., w + 120 (lanes l and l + 16 the same one),
+    // so that every warp holds about an eighth of the rows of any window
+    const int jpos = warp + 8 * (lane & 15);
     long long slot = -1;
     if (jpos < p.W) slot = p.slot_idx[(long long)t * p.W + jpos];
     long long len = p.lens[t];
@@ -387,15 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i) {
             const float inv = __shfl_sync(0xFFFFFFFFu, invf, i);
             if ((ball >> i) & 1u) {
-                const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
                 uint32_t o[8];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float f[4];
-                    e4m3x4_times(w4[q], inv, f);
-                    o[2 * q] = pack_bf16(f[0], f[1]);
-                    o[2 * q + 1] = pack_bf16(f[2], f[3]);
-                }
+                dequant16(raw[i], inv, o);
                 *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0)) = make_uint4(o[0], o[1], o[2], o[3]);
                 *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
                 ++r;
@@ -438,11 +478,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (good && n > 0) {
         float v[2][32];
         float m = -INFINITY;
+        {   // both chunks' loads in flight together (columns n .. n16 - 1 are read but masked)
+            uint32_t r[2][32];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (32 * (chalf + 2 * u) < n16) tmem_ld32_issue(tS + lane_base + 32 * (chalf + 2 * u), r[u]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[u][i] = __uint_as_float(r[u][i]);
+        }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int c0 = 32 * (chalf + 2 * u);
-            if (c0 < n16) {  // columns n .. n16 - 1 are read but masked
-                tmem_ld32(tS + lane_base + c0, v[u]);
+            if (c0 < n16) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     if (c0 + i < n) m = fmaxf(m, v[u][i] * p.qscale);
@@ -500,10 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
 
     // ---- 8. out = O / l ----------------------------------------------------------------------------
-    // Each thread turns half of its head's 256 columns into bf16, staged as four 64-column
-    // blocks of 128 rows x 128 bytes with the 128-byte swizzle (the KV tile's space, read by
-    // no one now); thread 0 then writes them with four TMA stores.
+    // Each thread turns half of its head's 256 columns into bf16 in a staging area (the KV
+    // tile, read by no one now; 16-byte chunk c of row h at chunk c ^ (h mod 32),
+    // conflict-free both ways); then the CTA writes the 128 rows out with fully coalesced
+    // 16-byte stores.
     if (good2) {
+        uint8_t *ostage = smem + kOOff;
         const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
         for (int c0 = chalf * (kHalf / 2); c0 < (chalf + 1) * (kHalf / 2); c0 += 64) {
@@ -514,23 +566,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 64; ++i) v[i] = 0.f;
             }
-            uint8_t *ob = smem + kOOff + (c0 >> 6) * kQBlock;
 #pragma unroll
             for (int q8 = 0; q8 < 8; ++q8) {
                 uint32_t pk[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) pk[i] = pack_bf16(v[8 * q8 + 2 * i] * inv, v[8 * q8 + 2 * i + 1] * inv);
-                *reinterpret_cast<uint4 *>(ob + sw128_off(hrow, q8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                const int ch = c0 / 8 + q8;  // 0..31
+                *reinterpret_cast<uint4 *>(ostage + hrow * (kHalf * 2) + ((ch ^ (hrow & 31)) << 4)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
         }
-        fence_async_smem();
         __syncthreads();
-        if (tid == 0) {
-            for (int b = 0; b < kHalf / 64; ++b)
-                tma_store_2d(&omap, col_half * kHalf + b * 64, qrow, smem + kOOff + b * kQBlock);
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            // the staging must have been read before the CTA's shared memory is released
-            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __nv_bfloat16 *obase = p.out + (long long)qrow * kHD + col_half * kHalf;
+        for (int idx = tid; idx < kHeads * 32; idx += kThreads) {
+            const int row = idx >> 5, ch = idx & 31;
+            const uint4 val = *reinterpret_cast<const uint4 *>(ostage + row * (kHalf * 2) + ((ch ^ (row & 31)) << 4));
+            *reinterpret_cast<uint4 *>(obase + (long long)row * kHD + ch * 8) = val;
         }
     } else if (tid == 0) {
         // A wait gave up.  Let the copies and products still in flight land (bounded) before
@@ -567,15 +618,10 @@ dap_status launch_fp8(const Fp8Args &a, cudaStream_t stream) {
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return DAP_ERR_CUDA;
-    // out as the same [T*NH, 512] bf16 matrix; a TMA store box is 128 heads x 64 values
-    CUtensorMap omap;
-    if (enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return DAP_ERR_CUDA;
     fp8::Params p;
     p.kv_cache = a.kv_cache;
     p.inv_scale = static_cast<const __nv_bfloat16 *>(a.inv_scale);
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.slot_idx = a.slot_idx;
     p.lens = a.lens;
     p.T = a.T;
@@ -596,7 +642,7 @@ dap_status launch_fp8(const Fp8Args &a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, fp8::swa_kernel, qmap, omap, p) != cudaSuccess) return DAP_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, fp8::swa_kernel, qmap, p) != cudaSuccess) return DAP_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? DAP_OK : DAP_ERR_CUDA;
 }
 

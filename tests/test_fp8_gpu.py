@@ -79,3 +79,23 @@ def test_fp8_repeat_is_deterministic():
     a = binding.decode_attn_paged_fp8(case.q, case.kv_cache, case.inv_scale, case.indices, case.lens)
     b = binding.decode_attn_paged_fp8(case.q, case.kv_cache, case.inv_scale, case.indices, case.lens)
     assert torch.equal(a, b)
+
+
+def test_single_row_windows_return_the_dequantised_row_exactly():
+    """With one participating row the softmax weight is exactly 1, so every head's output is
+    that row's dequantised value bf16(e4m3(code) * inv_scale) bit for bit.  The row holds all
+    256 codes twice (subnormals, zeros, both signs and the NaN codes), and the tokens use
+    inverse scales from 2^-100 to 3e30 (those of 2^8 or more take the kernel's fp32 path)."""
+    inv_values = [1.0, 0.5, 2.0, 1.75, 0.5390625, 255.0, 256.0, 1000.0, 2.0 ** -20, 3e30, 2.0 ** -100, 1.0 / 3.0]
+    T = len(inv_values)
+    case = inputs.make_fp8_case(T, 128, 512, 1, 16, 4, 7400, lens=[1] * T)
+    codes = torch.arange(512, dtype=torch.int64) % 256
+    case.kv_cache[0, :T] = codes.to(torch.uint8)[None, :]
+    case.inv_scale[:T, 0] = torch.tensor(inv_values, dtype=torch.float32).to(torch.bfloat16)
+    case.indices[:] = -1
+    case.indices[:, 0] = torch.arange(T)
+    got = run(case).float().cpu().double().numpy()
+    want = ref(case)
+    nan = np.isnan(want)
+    assert nan.any() and np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
