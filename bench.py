@@ -511,9 +511,11 @@ def prepare_leg(key, case, dev, l2, splits=None, tpt=None) -> Leg:
                           device=dev) for _ in sets]
         outs = [torch.empty_like(case.q) for _ in sets]
 
+        maxlen = kv.max_kv_len   # host values only inside the step (no device read per call)
+
         def call(i):
             j = i % n
-            binding.decode_attn_paged_multi(*sets[j], plans[j], max_kv_len=kv.max_kv_len, scale=kv.scale,
+            binding.decode_attn_paged_multi(*sets[j], plans[j], max_kv_len=maxlen, scale=kv.scale,
                                             num_splits=S, workspace=ws[j], out=outs[j])
 
         host = [parts[k].cpu().pin_memory() for k in (0, 3, 4)]
@@ -555,9 +557,11 @@ def prepare_leg(key, case, dev, l2, splits=None, tpt=None) -> Leg:
                           device=dev) for _ in sets]
         outs = [torch.empty_like(case.q) for _ in sets]
 
+        maxlen = case.max_kv_len   # host values only inside the step (no device read per call)
+
         def call(i):
             j = i % n
-            binding.decode_attn_paged_fp8kv(*sets[j], max_kv_len=case.max_kv_len, scale=case.scale, num_splits=S,
+            binding.decode_attn_paged_fp8kv(*sets[j], max_kv_len=maxlen, scale=case.scale, num_splits=S,
                                             workspace=ws[j], out=outs[j])
 
         host = [parts[k].cpu().pin_memory() for k in (0, 5, 6)]

@@ -294,8 +294,9 @@ __device__ __forceinline__ void dequant16(const uint4 &raw, float inv, uint32_t 
 // One CTA per (head half of HD, head group of 128, token).  The chain, shortened to two
 // dependent global round trips before the products (slots, then rows and their inverse
 // scales together) with q landing in full meanwhile:
-//   1. thread 0 issues all eight q blocks by TMA at entry (128 KB landing zone); every
-//      warp loads the slots of its 16 window positions and the token's length;
+//   1. thread 0 issues four of the eight q blocks by TMA at entry, the other four once its
+//      row loads are issued (128 KB landing zone); every warp loads the slots of its 16
+//      window positions and the token's length;
 //   2. each warp gathers the rows of its kept positions (every eighth position of the
 //      window, so the warps share the rows evenly) into registers, a half-warp per 256-byte
 //      half of a row, together with their inverse scales; per-warp counts give every kept row
@@ -352,13 +353,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // slot table); the next launch may start at once (it waits the same way).
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // ---- 1. all of q, right away; the window's slots and length ------------------------------
-    if (tid == 0) {
-        for (int kb = 0; kb < kQBlocks; ++kb) {
+    // ---- 1. half of q right away, the window's slots and length -----------------------------
+    // (the other half follows the row loads, which are on the critical path: issued before
+    // the whole of q, the rows would queue behind 128 KB per CTA in the memory system)
+    auto issue_q = [&](int kb0) {
+        for (int kb = kb0; kb < kb0 + kQBlocks / 2; ++kb) {
             mbar_arrive_expect_tx(&q_full[kb], kQBlock);
             tma_load_2d(smem + kQOff + kb * kQBlock, &qmap, kb * 64, qrow, &q_full[kb]);
         }
-    }
+    };
+    if (tid == 0) issue_q(0);
     // warp w holds window positions w, w + 8, ..., w + 120 (lanes l and l + 16 the same one),
     // so that every warp holds about an eighth of the rows of any window
     const int jpos = warp + 8 * (lane & 15);
@@ -388,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         raw[i] = make_uint4(0u, 0u, 0u, 0u);
         if ((ball >> i) & 1u) raw[i] = __ldg(reinterpret_cast<const uint4 *>(piece + s * kHD));
     }
+    if (tid == 0) issue_q(kQBlocks / 2);
     if (lane == 0) cnt[warp] = __popc(ball);
     tc_fence_before();
     __syncthreads();  // barrier init, TMEM address and the counts are visible
