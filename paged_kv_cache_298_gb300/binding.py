@@ -179,32 +179,41 @@ class _on:
         return False
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream, dev: torch.device):
     """The stream handle for a call on `dev`: the given stream (which must belong to `dev`)
     or that device's current stream."""
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(dev.index)
         stream = torch.cuda.current_stream(dev)
     elif stream.device.index != dev.index:
         raise DapError(None, f"the stream belongs to {stream.device}, the call's tensors to {dev}")
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _splits(lib, num_splits, units, Hq, Hkv, D, page_size, max_kv_len, total_kv):
-    """(split count passed to the library, split count it runs) for a call on the current
-    device.  num_splits 0 is the planner's choice: the library resolves it with the summed
-    lengths unknown; when the caller knows them (`total_kv`), the plan is made here with
-    them and passed as an explicit count."""
+    """The split count passed to the library.  num_splits 0 is the planner's choice: the
+    library resolves it with the summed lengths unknown; when the caller knows them
+    (`total_kv`), the plan is made here with them and passed as an explicit count."""
     S = int(num_splits)
-    sms = lib.dap_device_sm_count() if S == 0 else 0
     if S == 0 and total_kv:
-        S = lib.dap_resolve_splits(0, sms, units, Hq, Hkv, D, page_size, int(max_kv_len), int(total_kv))
-    run = lib.dap_resolve_splits(S, sms, units, Hq, Hkv, D, page_size, int(max_kv_len), 0)
-    return S, run
+        S = lib.dap_resolve_splits(0, lib.dap_device_sm_count(), units, Hq, Hkv, D, page_size, int(max_kv_len),
+                                   int(total_kv))
+    return S
 
 
-def _workspace(workspace, need: int, dev):
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+def _workspace(lib, workspace, S, units, Hq, Hkv, D, page_size, max_kv_len, need_of, dev):
+    """The caller's workspace, or one allocated for the split count the call will run
+    (dap_resolve_splits); returns (tensor or None, its bytes)."""
+    if workspace is None:
+        sms = lib.dap_device_sm_count() if S == 0 else 0
+        run = lib.dap_resolve_splits(S, sms, units, Hq, Hkv, D, page_size, int(max_kv_len), 0)
+        need = need_of(run)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     return workspace, (0 if workspace is None else workspace.numel() * workspace.element_size())
 
 
@@ -293,8 +302,9 @@ def decode_attn_paged(q, k_cache, v_cache, block_table, seq_lens, *, max_kv_len:
     _bf16_3d(out, "out")
     lib = load()
     with _on(dev):
-        S, run = _splits(lib, num_splits, B, Hq, Hkv, D, ps, max_kv_len, total_kv)
-        workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes(B, Hq, Hkv, D, run), dev)
+        S = _splits(lib, num_splits, B, Hq, Hkv, D, ps, max_kv_len, total_kv)
+        workspace, wbytes = _workspace(lib, workspace, S, B, Hq, Hkv, D, ps, max_kv_len,
+                                       lambda r: lib.dap_workspace_bytes(B, Hq, Hkv, D, r), dev)
         st = lib.decode_attn_paged(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
                                    _ptr(block_table), block_table.shape[1], _ptr(seq_lens), int(max_kv_len),
                                    B, Hq, Hkv, D, float(scale), int(S), _ptr(workspace), wbytes, _ptr(out),
@@ -351,8 +361,9 @@ def decode_attn_contig(q, k, v, seq_lens, *, max_kv_len: int, scale: float | Non
     _bf16_3d(out, "out")
     lib = load()
     with _on(dev):
-        S, run = _splits(lib, num_splits, B, Hq, Hkv, D, max_len, max_kv_len, total_kv)
-        workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes(B, Hq, Hkv, D, run), dev)
+        S = _splits(lib, num_splits, B, Hq, Hkv, D, max_len, max_kv_len, total_kv)
+        workspace, wbytes = _workspace(lib, workspace, S, B, Hq, Hkv, D, max_len, max_kv_len,
+                                       lambda r: lib.dap_workspace_bytes(B, Hq, Hkv, D, r), dev)
         st = lib.decode_attn_contig(_ptr(q), q.stride(0), q.stride(1), _ptr(k), _ptr(v), max_len,
                                     _ptr(seq_lens), int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S),
                                     _ptr(workspace), wbytes, _ptr(out), out.stride(0), out.stride(1),
@@ -409,8 +420,9 @@ def decode_attn_paged_masked(q, k_cache, v_cache, block_table, seq_lens, mask, *
     _bf16_3d(out, "out")
     lib = load()
     with _on(dev):
-        S, run = _splits(lib, num_splits, B, Hq, Hkv, D, ps, max_kv_len, total_kv)
-        workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes(B, Hq, Hkv, D, run), dev)
+        S = _splits(lib, num_splits, B, Hq, Hkv, D, ps, max_kv_len, total_kv)
+        workspace, wbytes = _workspace(lib, workspace, S, B, Hq, Hkv, D, ps, max_kv_len,
+                                       lambda r: lib.dap_workspace_bytes(B, Hq, Hkv, D, r), dev)
         st = lib.decode_attn_paged_masked(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
                                           _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(mask),
                                           mask.stride(0), int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S),
@@ -456,8 +468,9 @@ def decode_attn_paged_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, 
     _bf16_3d(out, "out")
     lib = load()
     with _on(dev):
-        S, run = _splits(lib, num_splits, B, Hq, Hkv, D, ps, max_kv_len, total_kv)
-        workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes(B, Hq, Hkv, D, run), dev)
+        S = _splits(lib, num_splits, B, Hq, Hkv, D, ps, max_kv_len, total_kv)
+        workspace, wbytes = _workspace(lib, workspace, S, B, Hq, Hkv, D, ps, max_kv_len,
+                                       lambda r: lib.dap_workspace_bytes(B, Hq, Hkv, D, r), dev)
         st = lib.decode_attn_paged_fp8kv(_ptr(q), q.stride(0), q.stride(1), _ptr(k_codes), _ptr(v_codes),
                                          _ptr(k_scale), _ptr(v_scale), P, ps, _ptr(block_table), block_table.shape[1],
                                          _ptr(seq_lens), int(max_kv_len), B, Hq, Hkv, D, float(scale), int(S),
@@ -545,8 +558,9 @@ def decode_attn_paged_multi(q, k_cache, v_cache, block_table, seq_lens, plan: Mu
     lib = load()
     mask = _mask(mask, total_q, int(max_kv_len))
     with _on(dev):
-        S, run = _splits(lib, num_splits, max(plan.num_tiles, 0), Hq, Hkv, D, ps, max_kv_len, total_kv)
-        workspace, wbytes = _workspace(workspace, lib.dap_workspace_bytes_multi(total_q, Hq, D, run), dev)
+        S = _splits(lib, num_splits, max(plan.num_tiles, 0), Hq, Hkv, D, ps, max_kv_len, total_kv)
+        workspace, wbytes = _workspace(lib, workspace, S, max(plan.num_tiles, 0), Hq, Hkv, D, ps, max_kv_len,
+                                       lambda r: lib.dap_workspace_bytes_multi(total_q, Hq, D, r), dev)
         st = lib.decode_attn_paged_multi(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), P, ps,
                                          _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
                                          _ptr(plan.qo_indptr), _ptr(plan.tile_batch), _ptr(plan.tile_index),

@@ -17,17 +17,20 @@
 // One CTA per (token, head group of 128, half of HD):
 //   1. q[t, heads, :] streams in by TMA (128B swizzle, eight 64-wide blocks through a
 //      4-stage ring started at entry) and moves on into tensor memory (head = TMEM lane, two
-//      bf16 per column): blocks 0..3 once the token's window has been compacted to its n
-//      participating slots (order kept), 4..7 (the ring refilled meanwhile) after step 2;
-//   2. the n rows are gathered, dequantised (e4m3 -> f16 -> f32, times the f32 inverse scale,
-//      rounded once to bf16: the same single rounding the page's fallback does) and stored
-//      in shared memory as a 128-byte-swizzled [hd block][row][64] tile; rows n..n16-1 are
-//      zero (n16 = n rounded up to 16);
+//      bf16 per column): blocks 0..3 while the rows travel, 4..7 (the ring refilled
+//      meanwhile) after step 2;
+//   2. every warp loads the slots of every eighth window position and, right after, the rows
+//      of its kept positions (a half-warp per 256-byte half of a row) with their inverse
+//      scales: two dependent round trips; the rows are dequantised (each e4m3 code placed
+//      into a bf16 pattern by integer ops, then one bf16 multiply by the inverse scale: one
+//      rounding of the exact product, as the page's fallback rounds) into a
+//      128-byte-swizzled [hd block][row][64] tile in shared memory, rows in warp order;
+//      rows n..n16-1 are zero (n16 = n rounded up to 16);
 //   3. one thread issues S = Q . KV^T (M=128, N=n16, K=512) into TMEM, A (q) read from
 //      tensor memory, B (the rows) from shared memory;
-//   4. two threads own each head (one TMEM lane, half of the score columns each): base-2
-//      softmax over its n scores, the probabilities rounded to bf16 into a swizzled P tile,
-//      l = their sum;
+//   4. two threads own each head (one TMEM lane, alternate 32-column chunks of the scores):
+//      base-2 softmax over its n scores, the probabilities rounded to bf16 into a swizzled
+//      P tile, l = their sum;
 //   5. O[:, half] = P . KV[:, half] (M=128, N=256, K=n16) reads the same KV tile as an
 //      MN-major operand, into the tensor-memory columns q held;
 //   6. out = O / l in bf16.
@@ -61,27 +64,26 @@ constexpr int kHeads = 128;         // heads per CTA = MMA M
 constexpr int kMaxRows = 128;       // window rows a CTA holds
 constexpr int kHalf = kHD / 2;      // output columns per CTA
 constexpr int kThreads = 256;       // 8 warps: warps w and w+4 share TMEM lanes
-constexpr int kQBlocks = kHD / 64;  // q arrives as 8 blocks of 64 values per head
+constexpr int kQStages = 4;
 // shared-memory map (offsets from a 1024-byte aligned base)
-constexpr int kQOff = 0;                                    // q landing zone: 8 blocks of 128 heads x 64
-constexpr int kQBlock = kHeads * 128;                       // 16 KB per block
-constexpr int kKvOff = 0;                                   // KV tile [8 blocks][n16 rows][128 B], once q
-                                                            // has moved into tensor memory
-constexpr int kOOff = 0;                                    // bf16 output staging after PV (64 KB)
-constexpr int kPOff = kQOff + kQBlocks * kQBlock;           // 131072: P, 2 blocks of 128 heads x 64 keys
-constexpr int kPBlock = kHeads * 128;                       // 16 KB per 64-key block
-constexpr int kXchOff = kPOff + 2 * kPBlock;                // softmax max/sum exchange (2 KB)
+constexpr int kQOff = 0;                                    // q ring: 4 stages of 128 heads x 64
+constexpr int kQStage = kHeads * 128;                       // 16 KB per stage
+constexpr int kPOff = kQOff;                                // P: 2 blocks of 128 heads x 64, after q
+constexpr int kKvOff = kQOff + kQStages * kQStage;          // 65536: KV tile [8 blocks][n16 rows][128 B]
+constexpr int kOOff = kKvOff;                               // bf16 output staging after PV (64 KB)
+constexpr int kPBlock = kHeads * 128;                       // 16 KB per 64-wide row block
+constexpr int kXchOff = kKvOff + 8 * kMaxRows * 128;        // softmax max/sum exchange (2 KB)
 constexpr int kCntOff = kXchOff + 4 * kHeads * 4;           // per-warp row counts [0..7], abort [12]
 constexpr int kBarOff = kCntOff + 64;                       // mbarriers
-constexpr int kNumBars = kQBlocks + 2;                      // q_full[8], s_done, o_done
+constexpr int kNumBars = kQStages + 2;                      // q_full[4], mma_done[2]
 constexpr int kTmemOff = kBarOff + kNumBars * 8;
 constexpr int kSmemUsed = kTmemOff + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;                // slack to align the base
 constexpr int kTmemCols = 512;  // q: cols [0,256) (two bf16 per column) until S is complete,
                                 // then O: [0,256); S: [256,384)
 constexpr int kSCol = 256;
-static_assert(8 * kMaxRows * 128 <= kPOff, "the KV tile fits in the q landing zone");
-static_assert(kOOff + kHeads * kHalf * 2 <= kPOff, "the output staging fits in the KV tile");
+static_assert(kOOff + kHeads * kHalf * 2 <= kXchOff, "the output staging fits in the KV tile");
+static_assert(kPOff + 2 * kPBlock <= kKvOff, "P fits in the q ring");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // ---- tcgen05 / descriptor helpers ---------------------------------------------------------
@@ -236,6 +238,7 @@ struct Params {
     float qscale;  // scale * log2(e)
 };
 
+
 // e4m3 codes -> bf16, exactly, two at a time.  Codes c0, c1 placed in the high bytes of the
 // two 16-bit halves (x = c0 << 8 | c1 << 24) and shifted right by 4 give, with the sign bit
 // kept in place, bf16 patterns whose exponent field is the code's and whose mantissa starts
@@ -291,26 +294,30 @@ __device__ __forceinline__ void dequant16(const uint4 &raw, float inv, uint32_t 
     }
 }
 
-// One CTA per (head half of HD, head group of 128, token).  The chain, shortened to two
-// dependent global round trips before the products (slots, then rows and their inverse
-// scales together) with q landing in full meanwhile:
-//   1. thread 0 issues four of the eight q blocks by TMA at entry, the other four once its
-//      row loads are issued (128 KB landing zone); every warp loads the slots of its 16
-//      window positions and the token's length;
-//   2. each warp gathers the rows of its kept positions (every eighth position of the
-//      window, so the warps share the rows evenly) into registers, a half-warp per 256-byte
-//      half of a row, together with their inverse scales; per-warp counts give every kept row
-//      its place in the KV tile (warp by warp; the result does not depend on the rows' order
-//      beyond rounding);
-//   3. q moves into tensor memory block by block as it lands (head = TMEM lane, two bf16
-//      per column);
-//   4. the rows are dequantised (e4m3 codes placed into bf16 patterns by integer ops, times
-//      the inverse scale by one bf16 multiply: one rounding of the exact product) into a
-//      128-byte-swizzled [hd block][row][64] tile where q landed;
-//   5. S = Q . KV^T (M=128, N=n16, K=512), A from tensor memory;
-//   6. softmax: two threads per head, 32-column chunks alternating between them;
-//   7. O[:, half] = P . KV[:, half] (M=128, N=256, K=n16) into the columns q held;
-//   8. out = O / l in bf16, staged in shared memory and written with coalesced stores.
+// Moves the four q blocks of ring round `round` (blocks 4 round .. 4 round + 3) into tensor
+// memory: thread (head h, half c) waits for each stage, reads its 32 values (64 bytes, four
+// 128B-swizzled chunks) of row h and stores them at columns 32 block + 16 c of lane h (two
+// bf16 per column, the lower index in the low half).  A wait that gives up sets the abort
+// word; the caller still reaches every barrier.
+__device__ __forceinline__ void q_to_tmem(uint8_t *smem, uint64_t *q_full, uint32_t tmem_lane, int h, int c,
+                                          int round, int *cnt) {
+#pragma unroll
+    for (int st = 0; st < kQStages; ++st) {
+        if (!mbar_wait(&q_full[st], round & 1)) cnt[12] = 1;
+        const uint8_t *blk = smem + kQOff + st * kQStage;
+        uint32_t r[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(blk + sw128_off(h, 4 * c + i));
+            r[4 * i] = v.x;
+            r[4 * i + 1] = v.y;
+            r[4 * i + 2] = v.z;
+            r[4 * i + 3] = v.w;
+        }
+        tmem_st16(tmem_lane + (round * kQStages + st) * 32 + 16 * c, r);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     swa_kernel(const __grid_constant__ CUtensorMap qmap, const Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -322,11 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = blockIdx.z;           // decode token
     int *cnt = reinterpret_cast<int *>(smem + kCntOff);     // [0..7] warp counts, [12] abort
     uint64_t *q_full = reinterpret_cast<uint64_t *>(smem + kBarOff);
-    uint64_t *s_done = q_full + kQBlocks;
-    uint64_t *o_done = s_done + 1;
+    uint64_t *mma_done = q_full + kQStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kTmemOff);
 
-    // thread = (head hrow = TMEM lane, half chalf of q's 512 values / of the columns):
+    // thread = (head hrow = TMEM lane, half qhalf of q's 512 values / of the score columns):
     // warps w and w + 4 serve the same 32 lanes
     const int hrow = tid & (kHeads - 1);
     const int chalf = warp >> 2;
@@ -336,10 +342,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Barriers and tensor memory touch nothing the previous kernel writes: they are set up
     // before the wait below, overlapping that kernel's end.
     if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) mbar_init(&q_full[i], 1);
+        for (int i = 0; i < kQStages; ++i) mbar_init(&q_full[i], 1);
+        mbar_init(&mma_done[0], 1);
+        mbar_init(&mma_done[1], 1);
         cnt[12] = 0;
         fence_barrier_init();
-        prefetch_tensormap(&qmap);
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -353,18 +360,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // slot table); the next launch may start at once (it waits the same way).
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // ---- 1. half of q right away, the window's slots and length -----------------------------
-    // (the other half follows the row loads, which are on the critical path: issued before
-    // the whole of q, the rows would queue behind 128 KB per CTA in the memory system)
-    auto issue_q = [&](int kb0) {
-        for (int kb = kb0; kb < kb0 + kQBlocks / 2; ++kb) {
-            mbar_arrive_expect_tx(&q_full[kb], kQBlock);
-            tma_load_2d(smem + kQOff + kb * kQBlock, &qmap, kb * 64, qrow, &q_full[kb]);
+    // ---- 1a. q's first four 64-wide blocks, right away: they travel during the compaction
+    if (tid == 0) {
+        for (int kb = 0; kb < kQStages; ++kb) {
+            mbar_arrive_expect_tx(&q_full[kb], kQStage);
+            tma_load_2d(smem + kQOff + kb * kQStage, &qmap, kb * 64, qrow, &q_full[kb]);
         }
-    };
-    if (tid == 0) issue_q(0);
-    // warp w holds window positions w, w + 8, ..., w + 120 (lanes l and l + 16 the same one),
-    // so that every warp holds about an eighth of the rows of any window
+    }
+
+    // ---- 1b. the window's slots and length; 2. the kept rows and their inverse scales --------
+    // Warp w holds window positions w, w + 8, ..., w + 120 (lanes l and l + 16 the same
+    // one), so every warp holds about an eighth of any window's rows.  Each warp loads the
+    // rows of its kept positions into registers right after the slots, a half-warp per
+    // 256-byte half of a row (16 codes per lane), with their inverse scales: two dependent
+    // round trips in all before the rows are in registers.
     const int jpos = warp + 8 * (lane & 15);
     long long slot = -1;
     if (jpos < p.W) slot = p.slot_idx[(long long)t * p.W + jpos];
@@ -379,9 +388,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         keep = slot >= 0;
     }
     const uint32_t ball = __ballot_sync(0xFFFFFFFFu, keep) & 0xFFFFu;
-
-    // ---- 2. the kept rows into registers, with their inverse scales --------------------------
-    // row piece of this lane: bytes 16 (l % 16) + 256 (l / 16) of each row (16 e4m3 codes)
     uint4 raw[16];
     float invf = 0.f;
     if (keep) invf = __bfloat162float(p.inv_scale[slot]);
@@ -392,10 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         raw[i] = make_uint4(0u, 0u, 0u, 0u);
         if ((ball >> i) & 1u) raw[i] = __ldg(reinterpret_cast<const uint4 *>(piece + s * kHD));
     }
-    if (tid == 0) issue_q(kQBlocks / 2);
     if (lane == 0) cnt[warp] = __popc(ball);
     tc_fence_before();
-    __syncthreads();  // barrier init, TMEM address and the counts are visible
+    __syncthreads();  // the counts and the TMEM address are visible
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     int base = 0, n = 0;
@@ -408,28 +413,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n16 = (n + 15) & ~15;
     const int kvb = n16 * 128;  // bytes per 64-wide hd block of the KV tile
 
-    // ---- 3. q into tensor memory as it lands ---------------------------------------------------
-    // thread (head hrow, half chalf) moves its 32 values of each block: four 16-byte chunks
-    // of row hrow of the 128B-swizzled block, to columns 32 kb + 16 chalf of lane hrow
-#pragma unroll 1
-    for (int kb = 0; kb < kQBlocks; ++kb) {
-        if (!mbar_wait(&q_full[kb], 0)) cnt[12] = 1;
-        const uint8_t *blk = smem + kQOff + kb * kQBlock;
-        uint32_t r[16];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(blk + sw128_off(hrow, 4 * chalf + i));
-            r[4 * i] = v.x;
-            r[4 * i + 1] = v.y;
-            r[4 * i + 2] = v.z;
-            r[4 * i + 3] = v.w;
+    // While the rows travel, q blocks 0..3 move from the ring into tensor memory and thread
+    // 0 refills the ring with blocks 4..7 once every thread has read its stage.
+    q_to_tmem(smem, q_full, tmem + lane_base, hrow, chalf, 0, cnt);
+    __syncthreads();  // the ring is read
+    if (tid == 0) {
+        for (int kb = 0; kb < kQStages; ++kb) {
+            mbar_arrive_expect_tx(&q_full[kb], kQStage);
+            tma_load_2d(smem + kQOff + kb * kQStage, &qmap, (kb + kQStages) * 64, qrow, &q_full[kb]);
         }
-        tmem_st16(tmem + lane_base + kb * 32 + 16 * chalf, r);
     }
-    tmem_wait_st();   // this thread's q columns are in tensor memory
-    __syncthreads();  // every thread has read the landing zone: the KV tile may overwrite it
-
-    // ---- 4. dequantise the rows into the swizzled KV tile ------------------------------------
+    // dequantise the rows (one bf16 multiply of the exact code: one rounding of the exact
+    // product) into the swizzled KV tile, rows in warp order (the result does not depend on
+    // the rows' order beyond rounding)
     {
         const int blk = (lane & 15) / 4 + 4 * (lane >> 4);  // 64-wide hd block of this piece
         const int k0 = ((lane & 15) % 4) * 2;               // first 16-byte chunk in the 128-byte row
@@ -453,29 +449,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_uint4(0u, 0u, 0u, 0u);
         }
     }
+    q_to_tmem(smem, q_full, tmem + lane_base, hrow, chalf, 1, cnt);  // blocks 4..7
+    tmem_wait_st();  // this thread's q columns are in tensor memory
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
     const uint32_t tS = tmem + kSCol;
-    // ---- 5. S = Q . KV^T, one thread issues; A = q from tensor memory ------------------------
-    if (tid == 0 && n > 0 && cnt[12] == 0) {
+    // ---- 3. S = Q . KV^T, one thread issues; A = q from tensor memory ------------------------
+    if (tid == 0 && n > 0) {
         const uint32_t idS = idesc_bf16(kHeads, n16, 0);
-        for (int kb = 0; kb < kQBlocks; ++kb) {
+        for (int kb = 0; kb < 8; ++kb) {
             const uint32_t kva = smem_addr(smem + kKvOff + kb * kvb);
 #pragma unroll
             for (int k16 = 0; k16 < 4; ++k16)  // 16 values = 8 columns of q per product
                 umma_bf16_tmem_a(tS, tmem + kb * 32 + k16 * 8, sw128_desc(kva + 32 * k16, 16, 1024), idS,
                                  (kb | k16) != 0);
         }
-        umma_commit(s_done);
+        umma_commit(&mma_done[0]);
     }
 
-    // ---- 6. softmax: thread = head = TMEM lane, 32-column chunks chalf, chalf + 2 ---------------
+    // ---- 4. softmax: thread = head = TMEM lane, 32-column chunks chalf, chalf + 2 ---------------
     bool waited = true;
-    const bool run = n > 0 && cnt[12] == 0;
-    if (run) waited = mbar_wait(s_done, 0);
+    if (n > 0) waited = mbar_wait(&mma_done[0], 0);
     const int good = __syncthreads_and(waited && cnt[12] == 0);
     tc_fence_after();
     float *xch = reinterpret_cast<float *>(smem + kXchOff);  // [2][128] max, then [2][128] sum
@@ -539,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
 
-    // ---- 7. O[:, half] = P . KV[:, half], into the columns q held (S is complete) --------------
+    // ---- 5. O[:, half] = P . KV[:, half], into the columns q held (S is complete) --------------
     if (tid == 0 && good && n > 0) {
         const uint32_t idO = idesc_bf16(kHeads, kHalf, 1);
         const uint32_t pa = smem_addr(smem + kPOff);
@@ -547,14 +544,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k16 = 0; k16 < n16 / 16; ++k16)
             umma_bf16(tmem, sw128_desc(pa + (k16 >> 2) * kPBlock + (k16 & 3) * 32, 16, 1024),
                       sw128_desc(kvh + k16 * 2048, (uint32_t)kvb, 1024), idO, k16 > 0);
-        umma_commit(o_done);
+        umma_commit(&mma_done[0]);
     }
     bool waited2 = true;
-    if (good && n > 0) waited2 = mbar_wait(o_done, 0);
+    if (good && n > 0) waited2 = mbar_wait(&mma_done[0], 1);
     const int good2 = __syncthreads_and(good && waited2);
     tc_fence_after();
 
-    // ---- 8. out = O / l ----------------------------------------------------------------------------
+    // ---- 6. out = O / l --------------------------------------------------------------------------
     // Each thread turns half of its head's 256 columns into bf16 in a staging area (the KV
     // tile, read by no one now; 16-byte chunk c of row h at chunk c ^ (h mod 32),
     // conflict-free both ways); then the CTA writes the 128 rows out with fully coalesced
@@ -562,7 +559,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (good2) {
         uint8_t *ostage = smem + kOOff;
         const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
         for (int c0 = chalf * (kHalf / 2); c0 < (chalf + 1) * (kHalf / 2); c0 += 64) {
             float v[64];
             if (n > 0) {
@@ -582,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncthreads();
-        __nv_bfloat16 *obase = p.out + (long long)qrow * kHD + col_half * kHalf;
+        __nv_bfloat16 *obase = p.out + ((long long)t * p.NH + hg * kHeads) * kHD + col_half * kHalf;
         for (int idx = tid; idx < kHeads * 32; idx += kThreads) {
             const int row = idx >> 5, ch = idx & 31;
             const uint4 val = *reinterpret_cast<const uint4 *>(ostage + row * (kHalf * 2) + ((ch ^ (row & 31)) << 4));
@@ -591,9 +587,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (tid == 0) {
         // A wait gave up.  Let the copies and products still in flight land (bounded) before
         // the tensor memory and the shared memory are released.
-        for (int i = 0; i < kQBlocks; ++i) (void)mbar_wait(&q_full[i], 0);
-        umma_commit(o_done);
-        (void)mbar_wait(o_done, (good && n > 0) ? 1 : 0);
+        for (int i = 0; i < kQStages; ++i) (void)mbar_wait(&q_full[i], 1);
+        umma_commit(&mma_done[1]);
+        (void)mbar_wait(&mma_done[1], 0);
     }
     tc_fence_before();
     __syncthreads();
@@ -626,9 +622,9 @@ dap_status launch_fp8(const Fp8Args &a, cudaStream_t stream) {
     fp8::Params p;
     p.kv_cache = a.kv_cache;
     p.inv_scale = static_cast<const __nv_bfloat16 *>(a.inv_scale);
-    p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.slot_idx = a.slot_idx;
     p.lens = a.lens;
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.T = a.T;
     p.NH = a.NH;
     p.W = a.W;
