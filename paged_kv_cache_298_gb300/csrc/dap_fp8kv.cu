@@ -71,9 +71,6 @@ template <int G_, int HG_, int HPW_ = 1>
 struct Cfg {
     static constexpr int D = kD, G = G_, HG = HG_, HPW = HPW_, KW = 4, NWC = KW * (HG / HPW), BT = 64;
     static constexpr int NS = HG == 2 ? 3 : 4, MINB = HG == 2 ? 2 : 3;
-    // registers per thread for MINB CTAs per SM (whole warps, in units of 8 registers)
-    static constexpr int MAXREG = (65536 / (MINB * ((NWC + 1) * 32)) / 8 * 8) > 255 ? 255
-                                  : (65536 / (MINB * ((NWC + 1) * 32)) / 8 * 8);
     static constexpr bool SWZ = true;
     static constexpr int THREADS = (NWC + 1) * 32;
     static constexpr int KPW = BT / KW;                   // 16 keys per consumer warp
@@ -192,21 +189,12 @@ struct Consumer {
         w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
     }
 
-    // One staged tile.  Every shared-memory read of the tile comes first (the factors, V, then
-    // K, whose codes go straight into the QK products); then this lane arrives on the
-    // stage's `empty` barrier (one arrival per lane, so each lane's own reads are ordered
-    // before the producer may refill the stage) and the softmax and PV run on registers
-    // while the next tile travels into the stage.
-    __device__ __forceinline__ void tile(const uint8_t *stage, int nvalid, uint64_t *empty) {
+    __device__ __forceinline__ void tile(const uint8_t *stage, int nvalid) {
         const int nv = nvalid - key0;
-        if (nv <= 0) {
-            mbar_arrive(empty);
-            return;
-        }
+        if (nv <= 0) return;
         const bool v0 = g < nv, v1 = g + 8 < nv;
-        static_assert(HW == 1, "one kv head per consumer warp");
-        {
-            constexpr int h = 0;
+#pragma unroll
+        for (int h = 0; h < HW; ++h) {
             const uint8_t *sK = stage, *sV = stage + C::CODE_BYTES;
             const int l0 = line0 + h * hline, l1 = line1 + h * hline;
             const int o0 = f0 + h * hfac, o1 = f1 + h * hfac;
@@ -236,7 +224,6 @@ struct Consumer {
                     mma_f16_16816(c, a, qb[h][m][0], qb[h][m][1]);
                 }
             }
-            mbar_arrive(empty);  // the stage may be refilled: what this lane needs of it is in registers
             const float ks0 = kfac0 * qscale[h], ks1 = kfac1 * qscale[h];
             float s[4];
             s[0] = v0 ? c[0] * ks0 : -INFINITY;
@@ -380,7 +367,7 @@ struct Consumer {
 };
 
 template <class C>
-__global__ void __maxnreg__(C::MAXREG)
+__global__ void __launch_bounds__(C::THREADS, C::MINB)
     fp8kv_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                  const __grid_constant__ CUtensorMap mapKS, const __grid_constant__ CUtensorMap mapVS,
                  const SplitParams p) {
@@ -424,7 +411,7 @@ __global__ void __maxnreg__(C::MAXREG)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], NWC * 32);  // every consumer lane arrives
+            mbar_init(&empty[i], NWC);
         }
         misc[0] = 0;
         misc[1] = 0;
@@ -494,7 +481,9 @@ __global__ void __maxnreg__(C::MAXREG)
             misc[1] = 1;
             break;
         }
-        cs.tile(smem + st * C::STAGE_BYTES, min(BT, tok1 - (tok0 + i * BT)), &empty[st]);
+        cs.tile(smem + st * C::STAGE_BYTES, min(BT, tok1 - (tok0 + i * BT)));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
         consumed = i + 1;
     }
     __syncthreads();  // every tile consumed; stage 0 is free for the merge
