@@ -21,10 +21,10 @@
 //      meanwhile) after step 2;
 //   2. every warp loads the slots of every eighth window position and, right after, the rows
 //      of its kept positions (a half-warp per 256-byte half of a row) with their inverse
-//      scales: two dependent round trips; the rows are dequantised (each e4m3 code placed
-//      into a bf16 pattern by integer ops, then one bf16 multiply by the inverse scale: one
-//      rounding of the exact product, as the page's fallback rounds) into a
-//      128-byte-swizzled [hd block][row][64] tile in shared memory, rows in warp order;
+//      scales: two dependent round trips; the rows are dequantised (e4m3 -> f16 -> f32,
+//      times the f32 inverse scale, rounded once to bf16: the same single rounding the
+//      page's fallback does) into a 128-byte-swizzled [hd block][row][64] tile in shared
+//      memory, rows in warp order;
 //      rows n..n16-1 are zero (n16 = n rounded up to 16);
 //   3. one thread issues S = Q . KV^T (M=128, N=n16, K=512) into TMEM, A (q) read from
 //      tensor memory, B (the rows) from shared memory;
@@ -239,61 +239,6 @@ struct Params {
 };
 
 
-// e4m3 codes -> bf16, exactly, two at a time.  Codes c0, c1 placed in the high bytes of the
-// two 16-bit halves (x = c0 << 8 | c1 << 24) and shifted right by 4 give, with the sign bit
-// kept in place, bf16 patterns whose exponent field is the code's and whose mantissa starts
-// with the code's three mantissa bits: the code's value times 2^-120 (a bf16 subnormal for
-// a subnormal code).  The caller's bf16 multiply by factor * 2^120 then yields
-// bf16(code * factor) with one rounding of the exact product: the dequantised value.
-__device__ __forceinline__ uint32_t e4m3x2_scaled_bits(uint32_t w, uint32_t sel) {
-    const uint32_t x = __byte_perm(w, 0u, sel);
-    return ((x >> 4) & 0x07F007F0u) | (x & 0x80008000u);
-}
-
-// Sixteen e4m3 codes (one 16-byte row piece) times the bf16 factor `inv`, rounded once to
-// bf16, into o[0..7] (bf16 pairs, lower index in the low half).  OCP E4M3FN codes
-// S.1111.111 are NaN and come out NaN.
-__device__ __forceinline__ void dequant16(const uint4 &raw, float inv, uint32_t (&o)[8]) {
-    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-    const float c = inv * 0x1p120f;  // exact (a power-of-two scaling) unless it overflows
-    if (fabsf(c) <= 3.3895313892515355e38f) {  // c is a finite bf16 value: one multiply per pair
-        const __nv_bfloat162 cc = __float2bfloat162_rn(c);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint32_t lo = e4m3x2_scaled_bits(w4[q], 0x1404u);  // codes 0, 1 of the word
-            const uint32_t hi = e4m3x2_scaled_bits(w4[q], 0x3424u);  // codes 2, 3
-            const __nv_bfloat162 a = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&lo), cc);
-            const __nv_bfloat162 b = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&hi), cc);
-            o[2 * q] = *reinterpret_cast<const uint32_t *>(&a);
-            o[2 * q + 1] = *reinterpret_cast<const uint32_t *>(&b);
-        }
-    } else {  // a factor of 2^8 or more: the product in fp32 (exact), then one rounding
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float f[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t b = (w4[q] >> (8 * k)) & 0xFFu;
-                const float mag = __uint_as_float((b & 0x7Fu) << 20) * 0x1p120f;  // exact, subnormals too
-                f[k] = ((b & 0x80u) ? -mag : mag) * inv;
-            }
-            o[2 * q] = pack_bf16(f[0], f[1]);
-            o[2 * q + 1] = pack_bf16(f[2], f[3]);
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        if ((((w4[q] & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u) != 0u) {  // a NaN code (rare)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (((w4[q] >> (8 * k)) & 0x7Fu) == 0x7Fu) {
-                    uint32_t &wd = o[2 * q + (k >> 1)];
-                    wd = (k & 1) ? ((wd & 0x0000FFFFu) | 0x7FC00000u) : ((wd & 0xFFFF0000u) | 0x00007FC0u);
-                }
-        }
-    }
-}
-
 // Moves the four q blocks of ring round `round` (blocks 4 round .. 4 round + 3) into tensor
 // memory: thread (head h, half c) waits for each stage, reads its 32 values (64 bytes, four
 // 128B-swizzled chunks) of row h and stores them at columns 32 block + 16 c of lane h (two
@@ -423,9 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(smem + kQOff + kb * kQStage, &qmap, (kb + kQStages) * 64, qrow, &q_full[kb]);
         }
     }
-    // dequantise the rows (one bf16 multiply of the exact code: one rounding of the exact
-    // product) into the swizzled KV tile, rows in warp order (the result does not depend on
-    // the rows' order beyond rounding)
+    // dequantise the rows into the swizzled KV tile (e4m3 -> f16 exactly, to f32, times the
+    // inverse scale: the product of a 4-bit and an 8-bit significand is exact in fp32, then
+    // one bf16 rounding, the page's fallback's one rounding), rows in warp order (the result
+    // does not depend on the rows' order beyond rounding)
     {
         const int blk = (lane & 15) / 4 + 4 * (lane >> 4);  // 64-wide hd block of this piece
         const int k0 = ((lane & 15) % 4) * 2;               // first 16-byte chunk in the 128-byte row
@@ -436,7 +382,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = __shfl_sync(0xFFFFFFFFu, invf, i);
             if ((ball >> i) & 1u) {
                 uint32_t o[8];
-                dequant16(raw[i], inv, o);
+                const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w4[q] >> (16 * jj)) & 0xFFFFu);
+                        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+                        const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * inv, f.y * inv);
+                        o[2 * q + jj] = *reinterpret_cast<const uint32_t *>(&b);
+                    }
+                }
                 *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0)) = make_uint4(o[0], o[1], o[2], o[3]);
                 *reinterpret_cast<uint4 *>(tile + sw128_off(r, k0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
                 ++r;
