@@ -84,8 +84,9 @@ int dap_device_sm_count(void);
  * cut into chunks of dap_chunk_tokens(max_kv_len, S) tokens, so sequence b runs
  * ceil(seq_lens[b] / chunk) splits (at least 1).  When B * Hkv (sequence, kv head) units
  * are fewer than the GPU's resident CTAs (2 per SM), S is the number of chunks that fills
- * one wave; otherwise S keeps the largest chunk near a tenth of one SM's share of the KV
- * rows.  S never exceeds the number of 64-token chunks of the longest sequence.  Every decode
+ * one wave (8 instead of more while 8 chunks fill at least four fifths of it: up to 8 chunks
+ * merge inside a thread-block cluster); otherwise S keeps the largest chunk near a tenth of
+ * one SM's share of the KV rows.  S never exceeds the number of 64-token chunks of the longest sequence.  Every decode
  * entry point runs this plan when given num_splits = 0 (see dap_resolve_splits).
  *   sm_count   SMs available (dap_device_sm_count()).
  *   total_kv   sum of seq_lens (host); 0 means "unknown", taken as B * max_kv_len.
@@ -146,7 +147,9 @@ size_t dap_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits);
  *   scale        softmax scale applied in fp32 to q . k (normally 1/sqrt(D)).
  *   num_splits   S > 0 = per-sequence schedule: every sequence is cut into chunks of
  *                dap_chunk_tokens(max_kv_len, S) tokens, one CTA each, and the splits of a
- *                sequence are merged by a combine kernel.  0 = the same schedule with the
+ *                sequence are merged by a combine kernel (or, when 2 <= S <= 8 and the grid
+ *                fits one wave, inside the thread-block cluster its CTAs form: the same
+ *                arithmetic, no second kernel).  0 = the same schedule with the
  *                planner's S (dap_plan_splits with total_kv = 0; a caller that knows the
  *                summed lengths can pass its own plan instead).  DAP_SPLITS_BALANCED =
  *                balanced schedule: a persistent grid of SMs x resident CTAs cuts the

@@ -150,8 +150,11 @@ int dap_plan_splits(int sm_count, int B, int Hq, int Hkv, int D, int page_size, 
     if (units < slots) {
         // Too few units to fill the GPU: cut every sequence into as many chunks as fit one
         // wave, so equal-length batches finish together (AstrAI csrc log, split-KV commit:
-        // choose the split count to fill the device).
+        // choose the split count to fill the device).  Up to 8 chunks of a unit merge inside
+        // one thread-block cluster, with no combine kernel: 8 is preferred to more while 8
+        // chunks still fill four fifths of the wave.
         S = slots / units;
+        if (S > 8 && 8 * units * 5 >= slots * 4) S = 8;
     } else {
         // Enough units: keep the largest unit a small fraction of one SM's share of the KV
         // rows so the last units to finish leave little of the GPU idle.

@@ -543,7 +543,31 @@ using ConsumerOf = typename std::conditional<C::MMA, MmaConsumer<C>, Consumer<C>
 
 // ---- per-sequence schedule: one CTA per (unit, split) ------------------------------------
 
-template <class C, bool PAGED>
+// ---- thread-block cluster pieces (the in-cluster merge of a unit's splits) --------------
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of shared-memory location `saddr` of this CTA mapped into CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_u4(uint32_t addr, const uint4 &v) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// CLUSTER: the num_splits CTAs of a unit form one thread-block cluster (blockIdx.x = unit *
+// num_splits + split = cluster rank); instead of writing partials for a combine kernel,
+// every CTA stages its (acc, m, l) in shared memory, ranks 1.. copy theirs into rank 0's
+// shared memory, and rank 0 merges them in split order (the combine kernel's arithmetic,
+// so the result is the same bit for bit) and writes the output.
+template <class C, bool PAGED, bool CLUSTER = false>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
     split_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                  const SplitParams p) {
@@ -554,8 +578,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
 
     const int nkvg = p.Hkv / HG;
     const int units = p.B * nkvg;
-    const int s = blockIdx.x / units;
-    const int rem = blockIdx.x - s * units;
+    const int s = CLUSTER ? (int)(blockIdx.x % (unsigned)p.num_splits) : (int)(blockIdx.x / units);
+    const int rem = CLUSTER ? (int)(blockIdx.x / (unsigned)p.num_splits) : (int)(blockIdx.x - s * units);
     const int b = rem / nkvg;
     const int kvg = rem - b * nkvg;
     // The pipeline barriers and the tensor maps touch nothing the previous kernel writes:
@@ -597,7 +621,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
         L = min(max(L, 0), p.max_kv_len);
     }
     const int nsplit = max(1, (L + p.chunk - 1) / p.chunk);
-    if (s >= nsplit) return;
+    if (!CLUSTER && s >= nsplit) return;  // (in a cluster every CTA takes part in the merge)
     const int tok0 = s * p.chunk;
     const int tok1 = min(L, tok0 + p.chunk);
     const int ntiles = tok1 > tok0 ? (tok1 - tok0 + BT - 1) / BT : 0;
@@ -665,6 +689,49 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     if (misc[1]) {    // a wait timed out: drain the copies still in flight (bounded), write nothing
         if (threadIdx.x == 0)
             for (int i = consumed; i < misc[0]; ++i) (void)mbar_wait(&full[i % NS], (i / NS) & 1);
+        if constexpr (!CLUSTER) return;
+        cs.reset();  // (in a cluster: take part in the merge with an empty partial)
+    }
+    if constexpr (CLUSTER) {
+        // stage this CTA's (acc, m, l) at the start of its (now idle) stage ring: [G][D] acc,
+        // then [G] (m, l); ranks 1.. copy theirs into rank 0's ring at slot `rank`
+        constexpr int SLOT = (G * (D + 2) + 3) & ~3;  // floats, a whole number of 16-byte chunks
+        static_assert(C::HG == 1 && (SLOT * 4) % 16 == 0, "one kv head per CTA; 16-byte slots");
+        static_assert(8 * SLOT * 4 <= C::NS * C::STAGE_BYTES, "eight slots fit the stage ring");
+        float *stg = reinterpret_cast<float *>(smem);
+        cs.finish(reinterpret_cast<float *>(smem + C::MRG_OFF),
+                  [] { named_sync(1, NWC * 32); return true; },
+                  [&](int, int g, int d, float a0, float a1, float M, float lv) {
+                      *reinterpret_cast<float2 *>(stg + g * D + d) = make_float2(a0, a1);
+                      if (d == 0) *reinterpret_cast<float2 *>(stg + G * D + g * 2) = make_float2(M, lv);
+                  });
+        cluster_sync_all();  // every CTA of the cluster has staged its partial and is done with its ring
+        const int tid = threadIdx.x;
+        if (s != 0) {
+            const uint32_t dst = cluster_map(smem_addr(stg + s * SLOT), 0);
+            for (int i = tid; i < SLOT / 4; i += NWC * 32)
+                st_cluster_u4(dst + i * 16, *reinterpret_cast<const uint4 *>(stg + 4 * i));
+        }
+        cluster_sync_all();  // rank 0 holds every partial
+        if (s == 0) {
+            for (int e = tid * 2; e < G * D; e += NWC * 32 * 2) {
+                const int g = e / D, d = e - g * D;
+                float M = -INFINITY;
+                for (int k = 0; k < p.num_splits; ++k) M = fmaxf(M, stg[k * SLOT + G * D + g * 2]);
+                const float Mu = (M == -INFINITY) ? 0.f : M;
+                float a0 = 0.f, a1 = 0.f, lsum = 0.f;
+                for (int k = 0; k < p.num_splits; ++k) {
+                    const float *sl = stg + k * SLOT;
+                    const float f = ex2(sl[G * D + g * 2] - Mu);
+                    lsum = fmaf(f, sl[G * D + g * 2 + 1], lsum);
+                    const float2 x = *reinterpret_cast<const float2 *>(sl + g * D + d);
+                    a0 = fmaf(f, x.x, a0);
+                    a1 = fmaf(f, x.y, a1);
+                }
+                const int hq = kvg * G + g;
+                store_out_pair(p.out + (long long)b * p.o_sb + (long long)hq * p.o_sh + d, a0, a1, lsum);
+            }
+        }
         return;
     }
     const bool direct = (nsplit == 1);
@@ -1038,21 +1105,30 @@ dap_status launch_per_sequence(const DecodeArgs &a, SplitParams &p, cudaStream_t
     if (!encode_cache_map<C>(&mk, a.k, a.D, a.Hkv, rows, outer, R) ||
         !encode_cache_map<C>(&mv, a.v, a.D, a.Hkv, rows, outer, R))
         return DAP_ERR_CUDA;
-    auto kern = split_kernel<C, PAGED>;
-    static PerDeviceOcc occ = {};
-    if (prepare_kernel(kern, C::THREADS, C::SMEM, &occ) <= 0) return DAP_ERR_CUDA;
+    auto kern = split_kernel<C, PAGED, false>;
+    auto kern_cl = split_kernel<C, PAGED, true>;
+    static PerDeviceOcc occ = {}, occ_cl = {};
+    const int per_sm = prepare_kernel(kern, C::THREADS, C::SMEM, &occ);
+    if (per_sm <= 0 || prepare_kernel(kern_cl, C::THREADS, C::SMEM, &occ_cl) <= 0) return DAP_ERR_CUDA;
     const long long grid = (long long)a.B * (a.Hkv / C::HG) * a.num_splits;
     if (grid > 0x7FFFFFFFLL) return DAP_ERR_SHAPE;
+    // A unit's splits merge inside a thread-block cluster (no combine kernel, no partials in
+    // the workspace) when there are 2..8 of them and the grid is one wave: every cluster is
+    // then resident from the start.
+    const int sms = dap_device_sm_count();
+    const bool cluster = a.num_splits >= 2 && a.num_splits <= 8 && sms > 0 && grid <= (long long)sms * per_sm;
     p.o_part = static_cast<float *>(a.workspace);
     p.ml_part = a.num_splits > 1 ? reinterpret_cast<float *>(static_cast<char *>(a.workspace) +
                                                              partial_acc_bytes(a.B, a.Hq, a.D, a.num_splits))
                                  : nullptr;
     if (g_trace.split_begin) cudaEventRecord(g_trace.split_begin, stream);
-    if (launch_dependent_smem(kern, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, stream, mk, mv, p) !=
-        cudaSuccess)
-        return DAP_ERR_CUDA;
+    const cudaError_t e =
+        cluster ? launch_cluster_dependent_smem(kern_cl, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM,
+                                                a.num_splits, stream, mk, mv, p)
+                : launch_dependent_smem(kern, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, stream, mk, mv, p);
+    if (e != cudaSuccess) return DAP_ERR_CUDA;
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
-    if (a.num_splits > 1) {
+    if (a.num_splits > 1 && !cluster) {
         if (launch_combine<C::D>(p, a.B, a.Hq, a.num_splits, stream) != cudaSuccess) return DAP_ERR_CUDA;
     }
     if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);

@@ -344,6 +344,27 @@ cudaError_t launch_dependent_smem(K kern, dim3 grid, dim3 block, int smem, cudaS
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// The same, as thread-block clusters of `cluster_x` CTAs along x.
+template <class K, class... Args>
+cudaError_t launch_cluster_dependent_smem(K kern, dim3 grid, dim3 block, int smem, int cluster_x,
+                                          cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <class K, class... Args>
 cudaError_t launch_dependent(K kern, dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
     cudaLaunchConfig_t cfg = {};

@@ -107,6 +107,25 @@ def test_page_permutation_is_bit_identical():
         assert torch.equal(gpu_paged(case, S), gpu_paged(moved, S)), f"S={S}"
 
 
+def test_cluster_merge_equals_the_combine_kernel_bit_for_bit():
+    """2..8 splits of a one-wave grid merge inside a thread-block cluster; the same sequences
+    in a batch too large for one wave merge in the combine kernel.  Same arithmetic, same
+    order: the outputs agree bit for bit (and with the oracle)."""
+    lens = [700, 33, 1024, 5, 260, 1]
+    small = inputs.make_paged_case(6, 32, 8, 128, 16, lens, 92).to("cuda")
+    reps = 120   # 720 sequences x 8 kv heads x S CTAs: several waves
+    big = inputs.PagedCase(small.q.repeat(reps, 1, 1), small.k_cache, small.v_cache, small.block_table.repeat(reps, 1),
+                           small.seq_lens.repeat(reps), small.page_size, small.scale)
+    ref = oracle_paged(small)
+    for S in [2, 3, 5, 8]:
+        a = gpu_paged(small, S)
+        bb = binding.decode_attn_paged(big.q, big.k_cache, big.v_cache, big.block_table, big.seq_lens,
+                                       max_kv_len=small.max_kv_len, scale=small.scale, num_splits=S)
+        assert torch.equal(a, bb[:6]), f"S={S}"
+        assert_close(a, ref, f"S={S}")
+    assert binding.get_device_errors() == 0
+
+
 def test_split_count_sweep_stays_within_tolerance():
     case = inputs.make_paged_case(2, 64, 8, 128, 64, [4096, 2500], 79).to("cuda")
     ref = oracle_paged(case)
