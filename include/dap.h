@@ -164,10 +164,10 @@ size_t dap_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits);
  *                afterwards.
  *   out          device bf16 [B, Hq, D], element strides (out_stride_b, out_stride_h, 1).
  *                Written in full (an empty sequence gives a zero row).
- *   Supported: D in {32, 64, 128, 256}; G in {1, 2, 4, 8}; any page_size >= 1 for D in
- *   {64, 128}, a multiple of 8 for D in {32, 256}.  q, out, k_cache and v_cache 16-byte
- *   aligned; q/out strides multiples of 8 elements, nonzero where the extent they step
- *   over is above 1.
+ *   Supported: D in {32, 64, 128, 256}; G in {1, 2, 4, 8}; any page_size >= 1 (page sizes
+ *   that are multiples of 8 move K/V in TMA boxes, others row by row with 16-byte copies
+ *   into the same tiles).  q, out, k_cache and v_cache 16-byte aligned; q/out strides
+ *   multiples of 8 elements, nonzero where the extent they step over is above 1.
  *   The result is bit-identical under any permutation of the physical pages for a fixed
  *   num_splits (the summation order depends only on logical positions).
  */
@@ -297,7 +297,7 @@ size_t dap_workspace_bytes_multi(int total_q, int Hq, int D, int num_splits);
  *   workspace    device, >= dap_workspace_bytes_multi(total_q, Hq, D, S) bytes for the
  *                split count S used, 16-byte aligned.
  *   out          device bf16 [total_q, Hq, D], strides (out_stride_t, out_stride_h, 1).
- *   Supported: D in {32, 64, 128, 256}; G in {1, 2, 4, 8}; page_size a multiple of 8;
+ *   Supported: D in {32, 64, 128, 256}; G in {1, 2, 4, 8}; any page_size >= 1;
  *   alignment and strides as decode_attn_paged.  A work-map entry that names no token of its
  *   sequence is skipped and flagged (DAP_DEVERR_QMAP).
  */
@@ -323,7 +323,7 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
  *                DAP_SPLITS_BALANCED is not supported here.
  *   workspace    >= dap_workspace_bytes(B, Hq, Hkv, D, S) for the S used.
  *   Everything else as decode_attn_paged.  Supported: D in {32, 64, 128, 256}; G in
- *   {1, 2, 4, 8}; page_size a multiple of 8.
+ *   {1, 2, 4, 8}; any page_size >= 1.
  */
 dap_status decode_attn_paged_masked(const void *q, long long q_stride_b, long long q_stride_h,
                                     const void *k_cache, const void *v_cache, int num_pages,

@@ -206,7 +206,6 @@ dap_status decode_attn_paged(const void *q, long long q_stride_b, long long q_st
         return DAP_ERR_SHAPE;
     if (!k_cache || !v_cache || !block_table) return DAP_ERR_NULL;
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table)) return DAP_ERR_ALIGN;
-    if ((D == 32 || D == 256) && page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
     DecodeArgs a = {};
     a.paged = true;
     a.q = q;
@@ -336,7 +335,6 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table) || !aligned4(qo_indptr) ||
         !aligned4(tile_batch) || !aligned4(tile_index))
         return DAP_ERR_ALIGN;
-    if (page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
     {
         const int G = Hq / Hkv;
         if (tokens_per_tile * G != 16 && tokens_per_tile * G != 32) return DAP_ERR_SHAPE;
@@ -397,7 +395,6 @@ dap_status decode_attn_paged_masked(const void *q, long long q_stride_b, long lo
     if (!k_cache || !v_cache || !block_table) return DAP_ERR_NULL;
     if (!mask) return DAP_ERR_NULL;
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned4(block_table)) return DAP_ERR_ALIGN;
-    if (page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
     if ((st = check_mask(mask, mask_stride, max_kv_len)) != DAP_OK) return st;
     int S = 0, chunk = 0;
     if ((st = resolve_splits(B, B, Hq, Hkv, D, page_size, max_kv_len, num_splits, workspace, workspace_bytes, false,
@@ -576,9 +573,11 @@ dap_status dap_get_device_errors(unsigned int *flags, int clear) {
     *flags = 0;
     if (cudaDeviceSynchronize() != cudaSuccess) return DAP_ERR_CUDA;
     if (!read_errors_decode(flags, clear != 0)) return DAP_ERR_CUDA;
+    if (!read_errors_decode_gather(flags, clear != 0)) return DAP_ERR_CUDA;
     if (!read_errors_fp8(flags, clear != 0)) return DAP_ERR_CUDA;
     if (!read_errors_append(flags, clear != 0)) return DAP_ERR_CUDA;
     if (!read_errors_multi(flags, clear != 0)) return DAP_ERR_CUDA;
+    if (!read_errors_multi_gather(flags, clear != 0)) return DAP_ERR_CUDA;
     if (!read_errors_fp8kv(flags, clear != 0)) return DAP_ERR_CUDA;
     return DAP_OK;
 }

@@ -71,6 +71,10 @@ struct DecodeArgs {
 };
 
 dap_status launch_decode(const DecodeArgs &a, cudaStream_t stream);
+// paged cache with a page size that is not a multiple of 8 (row-gather producer)
+dap_status launch_decode_gather(const DecodeArgs &a, cudaStream_t stream);
+dap_status launch_decode_multi_gather(const DecodeArgs &a, cudaStream_t stream);
+dap_status launch_decode_masked_gather(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_multi(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_masked(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_fp8kv(const DecodeArgs &a, cudaStream_t stream);
@@ -105,12 +109,14 @@ dap_status launch_append_paged_fp8(const void *k_new, const void *v_new, uint8_t
                                    const int32_t *block_table, int max_pages, const int32_t *pos, int B, int Hkv,
                                    int D, cudaStream_t stream);
 bool read_errors_multi(unsigned int *flags, bool clear);
+bool read_errors_multi_gather(unsigned int *flags, bool clear);
 bool read_errors_fp8kv(unsigned int *flags, bool clear);
 bool read_errors_append(unsigned int *flags, bool clear);
 
 // Host readers of each translation unit's device error word (cudaMemcpyFromSymbol on the
 // current device); `clear` resets it.  Return false when the copy fails.
 bool read_errors_decode(unsigned int *flags, bool clear);
+bool read_errors_decode_gather(unsigned int *flags, bool clear);
 dap_status launch_selftest_wait(cudaStream_t stream);
 bool read_errors_fp8(unsigned int *flags, bool clear);
 

@@ -18,6 +18,7 @@ namespace dap {
 struct SplitParams {
     const __nv_bfloat16 *q;
     long long q_sb, q_sh;
+    const __nv_bfloat16 *k_cache, *v_cache;  // read directly by the row-gather producer
     const int32_t *block_table;
     int max_pages;
     const int32_t *seq_lens;
@@ -82,6 +83,85 @@ __device__ __forceinline__ void issue_kv_box(uint8_t *stage, int j, int R, const
         tma_load_4d(dst, mk, 0, kvh0, row, page, bar);
         tma_load_4d(dst + C::TILE_BYTES, mv, 0, kvh0, row, page, bar);
     }
+}
+
+// ---- row gather: page sizes that are not multiples of 8 ---------------------------------
+// Such a page size splits a tile into boxes of fewer than 8 rows, which could not start on
+// the 1024-byte boundaries of the swizzle pattern, so the producer warp copies the rows
+// itself: 16-byte cp.async chunks written straight to the swizzled positions the consumers
+// read, every lane arriving on the stage's full barrier once its own copies have landed.
+
+template <class C>
+struct RowPages {
+    static constexpr int N = (C::BT + 31) / 32;  // tile rows per lane: lane, lane + 32, ...
+    int pg[N], slot[N];
+};
+
+// Raw page ids (block-table entries) and in-page slots of this lane's rows of a tile whose
+// first token is `tok`; rows at or past `nvalid` get page 0.  The loads are only issued
+// here: the values are first used by gather_kv_tile, one tile later.
+template <class C>
+__device__ __forceinline__ void lookup_rows(RowPages<C> &rp, const int32_t *table, int tok, int nvalid,
+                                            int page_size, int lane) {
+#pragma unroll
+    for (int k = 0; k < RowPages<C>::N; ++k) {
+        const int r = lane + 32 * k;
+        rp.pg[k] = 0;
+        rp.slot[k] = 0;
+        if (r < nvalid) {
+            const int t = tok + r;
+            rp.pg[k] = __ldg(table + t / page_size);
+            rp.slot[k] = t % page_size;
+        }
+    }
+}
+
+// Copy rows [0, nvalid) of kv head `kvh` of K and V into the stage's [NBLK][BT][SWB] tiles
+// (128-byte swizzle: 16-byte chunk index XOR row & 7; 64-byte: XOR (row >> 1) & 3).  Lanes
+// take consecutive chunks, so each warp-wide copy reads whole rows.  Page ids outside the
+// pool are read as page 0 and flagged, as in the TMA path.
+template <class C>
+__device__ __forceinline__ void gather_kv_tile(uint8_t *stage, const RowPages<C> &rp, int nvalid, int kvh,
+                                               const SplitParams &p, int lane) {
+    constexpr int CPR = C::ROWB / 16;  // 16-byte chunks per row
+    constexpr int N = RowPages<C>::N;
+    long long row[N];                  // element offset of this lane's rows in the cache
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+        int pg = rp.pg[k];
+        if (lane + 32 * k < nvalid && (pg < 0 || pg >= p.num_pages)) {
+            flag_error(DAP_DEVERR_PAGE);
+            pg = 0;
+        }
+        row[k] = (((long long)pg * p.page_size + rp.slot[k]) * p.Hkv + kvh) * C::D;
+    }
+    const uint32_t sk = smem_addr(stage), sv = sk + C::TILE_BYTES;
+    const int n = nvalid * CPR;
+    for (int i0 = 0; i0 < n; i0 += 32) {  // the same trip count on every lane (shuffles below)
+        const int i = i0 + lane;
+        const int r = i / CPR, c = i % CPR;
+        long long off = 0;
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+            const long long x = __shfl_sync(0xFFFFFFFFu, row[k], r & 31);
+            if ((r >> 5) == k) off = x;
+        }
+        if (i < n) {
+            const int blk = c / C::CPB, cib = c % C::CPB;
+            const int sw = C::SWB == 128 ? (r & 7) : ((r >> 1) & 3);
+            const uint32_t dst = (uint32_t)(blk * (C::BT * C::SWB) + r * C::SWB + ((cib ^ sw) << 4));
+            cp_async_16(sk + dst, p.k_cache + off + c * 8);
+            cp_async_16(sv + dst, p.v_cache + off + c * 8);
+        }
+    }
+}
+
+// Arrivals a stage's full barrier expects: one (the producer's arrive with the TMA byte
+// count), or in row-gather mode one per producer lane plus lane 0's own arrive (which
+// carries the bytes of any TMA copy the tile also takes: q, mask).
+template <class C>
+__host__ __device__ constexpr uint32_t full_arrivals() {
+    return C::GATHER ? 33u : 1u;
 }
 
 // Merge of split partials for one output row, one warp, lanes over D: M = max_s m_s,
@@ -394,6 +474,8 @@ SplitParams make_params(const DecodeArgs &a) {
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
     p.q_sb = a.q_sb;
     p.q_sh = a.q_sh;
+    p.k_cache = static_cast<const __nv_bfloat16 *>(a.k);
+    p.v_cache = static_cast<const __nv_bfloat16 *>(a.v);
     p.block_table = a.block_table;
     p.max_pages = a.max_pages;
     p.seq_lens = a.seq_lens;

@@ -125,8 +125,6 @@ def paged_call(lib, **kw):
     (dict(q=None), 1), (dict(out=None), 1), (dict(k=None), 1), (dict(table=None), 1),
     (dict(lens=None), 1),
     (dict(D=96), 3), (dict(Hq=48, Hkv=3), 3), (dict(Hq=64, Hkv=4), 3),
-    (dict(D=256, qsb=32 * 256, qsh=256, osb=32 * 256, osh=256, ps=12, maxlen=90), 3),
-    (dict(D=32, qsb=32 * 32, qsh=32, osb=32 * 32, osh=32, ps=4, maxlen=30), 3),
     (dict(q=ctypes.c_void_p((1 << 20) + 8)), 5), (dict(qsh=130), 5), (dict(osb=4100), 5),
     (dict(k=ctypes.c_void_p((1 << 20) + 4)), 5),
     (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=16), 4), (dict(S=-1), 4), (dict(S=-1, ws=FAKE, wsb=4096), 4),
@@ -242,7 +240,7 @@ def multi_call(lib, **kw):
     (dict(totq=-1), 2), (dict(ntiles=0), 2), (dict(totq=0), 2), (dict(ntiles=9), 2), (dict(B=0), 2),
     (dict(Hq=30), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(S=-2), 2), (dict(S=-1), 3), (dict(qsh=0), 2),
     (dict(q=None), 1), (dict(qi=None), 1), (dict(tb=None), 1), (dict(ti=None), 1), (dict(table=None), 1),
-    (dict(D=96), 3), (dict(ps=12, maxlen=90), 3), (dict(Hq=64, Hkv=4), 3),
+    (dict(D=96), 3), (dict(Hq=64, Hkv=4), 3),
     (dict(qi=ctypes.c_void_p((1 << 20) + 2)), 5), (dict(qst=4100), 5),
     (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=16), 4),
     (dict(mask=FAKE, mst=96), 2), (dict(mask=FAKE, mst=120), 5), (dict(mask=ctypes.c_void_p((1 << 20) + 4), mst=128), 5),
@@ -314,7 +312,7 @@ def masked_call(lib, **kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(B=-1), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(mst=96), 2), (dict(S=-2), 2), (dict(S=-1), 3),
     (dict(mask=None), 1), (dict(q=None), 1), (dict(table=None), 1),
-    (dict(D=96), 3), (dict(ps=12, maxlen=90), 3), (dict(D=48, qsb=32 * 48, qsh=48, osb=32 * 48, osh=48), 3),
+    (dict(D=96), 3), (dict(D=48, qsb=32 * 48, qsh=48, osb=32 * 48, osh=48), 3),
     (dict(mst=120), 5), (dict(mask=ctypes.c_void_p((1 << 20) + 8)), 5),
     (dict(S=4), 4),
 ])

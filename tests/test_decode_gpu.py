@@ -301,9 +301,53 @@ def test_contiguous_head_dims_32_and_256(D):
         assert torch.equal(c, gpu_paged(case, S))
 
 
-@pytest.mark.parametrize("D", [32, 256])
-def test_head_dims_32_and_256_refuse_unaligned_pages(D):
-    case = inputs.make_paged_case(2, 8, 2, D, 12, [30, 50], 81).to("cuda")
-    with pytest.raises(binding.DapError) as e:
-        gpu_paged(case, 1)
-    assert e.value.status == 3
+# page sizes that are not multiples of 8: rows copied one by one into the swizzled tiles
+ODD_PAGES = [
+    # Hq, Hkv, D, ps
+    (8, 2, 32, 12), (16, 16, 32, 3), (16, 2, 64, 1), (8, 8, 64, 7), (32, 8, 128, 12),
+    (64, 8, 128, 100), (16, 8, 128, 5), (8, 2, 256, 12), (16, 2, 256, 5), (8, 8, 256, 1),
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,ps", ODD_PAGES, ids=[f"Hq{a}_Hkv{b}_D{c}_ps{d}" for a, b, c, d in ODD_PAGES])
+def test_page_sizes_that_are_not_multiples_of_8(Hq, Hkv, D, ps):
+    """Every head dim and schedule on page sizes off the TMA grid: the oracle within
+    tolerance, and the contiguous cache (TMA tiles) bit for bit, since the tiles hold the
+    same rows whichever way they were filled."""
+    case = inputs.make_paged_case(4, Hq, Hkv, D, ps, [1, 150, 333, 64], 83 + D + ps).to("cuda")
+    ref = oracle_paged(case)
+    k, v = inputs.logical_kv(case)
+    for S in [BAL, 0, 1, 3]:
+        got = gpu_paged(case, S)
+        assert_close(got, ref, f"D={D} ps={ps} S={S}")
+        c = binding.decode_attn_contig(case.q, k, v, case.seq_lens, max_kv_len=case.max_kv_len, scale=case.scale,
+                                       num_splits=S)
+        assert torch.equal(got, c), f"D={D} ps={ps} S={S}: paged (row gather) != contiguous"
+    assert binding.get_device_errors() == 0
+
+
+def test_row_gather_page_permutation_and_bad_page_id():
+    """Page size 12: a permutation of the physical pages gives the same bits; a page id
+    outside the pool is read as page 0 and flagged, as on the TMA path."""
+    case = inputs.make_paged_case(5, 32, 8, 128, 12, [700, 33, 1024, 5, 260], 84).to("cuda")
+    perm = torch.randperm(case.num_pages, generator=torch.Generator().manual_seed(6)).cuda()
+    inv = torch.argsort(perm)
+    moved = inputs.PagedCase(case.q, case.k_cache[perm].contiguous(), case.v_cache[perm].contiguous(),
+                             inv[case.block_table.long()].to(torch.int32).contiguous(), case.seq_lens,
+                             case.page_size, case.scale)
+    for S in [BAL, 0, 1, 4, 9]:
+        assert torch.equal(gpu_paged(case, S), gpu_paged(moved, S)), f"S={S}"
+    assert binding.get_device_errors() == 0
+    bad = case.block_table.clone()
+    bad[1, 0] = case.num_pages + 5
+    out = binding.decode_attn_paged(case.q, case.k_cache, case.v_cache, bad, case.seq_lens,
+                                    max_kv_len=case.max_kv_len, scale=case.scale, num_splits=1)
+    torch.cuda.synchronize()
+    assert binding.get_device_errors(clear=True) & binding.DEVERR_PAGE
+    fixed = bad.clone()
+    fixed[1, 0] = 0
+    want = binding.decode_attn_paged(case.q, case.k_cache, case.v_cache, fixed, case.seq_lens,
+                                     max_kv_len=case.max_kv_len, scale=case.scale, num_splits=1)
+    # (page 0 may be an unused, NaN-filled page: compare bits)
+    assert torch.equal(out.view(torch.int16), want.view(torch.int16))
+    assert binding.get_device_errors(clear=True) == 0

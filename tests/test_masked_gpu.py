@@ -66,6 +66,11 @@ SHAPES = [
     (2, 64, 8, 256, 8, [100, 513]),            # D=256, G=8, page 8
     (3, 16, 16, 32, 16, [1, 200, 65]),         # D=32: 64-byte swizzle, G=1
     (2, 32, 4, 32, 32, [700, 5]),              # D=32, G=8
+    # page sizes that are not multiples of 8 (rows copied one by one into the tiles)
+    (3, 32, 8, 128, 12, [257, 1000, 17]),      # G=4, page 12
+    (2, 16, 4, 256, 5, [300, 64]),             # D=256, page 5
+    (2, 32, 4, 32, 3, [700, 5]),               # D=32, page 3
+    (3, 8, 8, 64, 1, [1, 33, 64]),             # D=64, page 1
 ]
 
 
@@ -114,11 +119,13 @@ def test_full_size_ragged_with_mask():
 
 # ---- multi-token decode with a mask ---------------------------------------------------
 
-@pytest.mark.parametrize("Hq,Hkv,D,qlens", [(8, 2, 64, [5, 1, 9]), (32, 8, 128, [4, 4, 2]), (16, 2, 128, [3, 2, 1]),
-                                            (16, 4, 256, [5, 1, 7]), (64, 8, 32, [2, 1, 2])])
-def test_multi_token_mask_with_causal_rule(Hq, Hkv, D, qlens):
+@pytest.mark.parametrize("Hq,Hkv,D,qlens,ps", [(8, 2, 64, [5, 1, 9], 16), (32, 8, 128, [4, 4, 2], 16),
+                                               (16, 2, 128, [3, 2, 1], 16), (16, 4, 256, [5, 1, 7], 16),
+                                               (64, 8, 32, [2, 1, 2], 16), (32, 8, 128, [4, 4, 2], 12),
+                                               (16, 4, 256, [5, 1, 7], 3)])
+def test_multi_token_mask_with_causal_rule(Hq, Hkv, D, qlens, ps):
     lens = [100, 37, 300]
-    case = inputs.make_multi_case(3, Hq, Hkv, D, 16, lens, qlens, 6500 + Hq).to("cuda")
+    case = inputs.make_multi_case(3, Hq, Hkv, D, ps, lens, qlens, 6500 + Hq).to("cuda")
     kv = case.kv
     full, _ = make_mask(case.total_q, max(lens), 6501 + D, p_keep=0.6)
     qi = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)

@@ -80,6 +80,12 @@ SHAPES = [
     (2, 64, 8, 256, 8, [100, 513], [3, 6]),                      # D=256, G=8, page 8
     (3, 16, 16, 32, 16, [1, 200, 65], [1, 20, 33]),              # D=32 (64-byte swizzle), G=1
     (2, 32, 4, 32, 32, [700, 5], [11, 5]),                       # D=32, G=8
+    # page sizes that are not multiples of 8 (rows copied one by one into the tiles)
+    (3, 32, 8, 128, 12, [257, 1000, 5], [4, 13, 5]),            # G=4, page 12
+    (2, 64, 8, 128, 5, [128, 333], [2, 7]),                      # G=8, page 5
+    (2, 16, 4, 256, 3, [300, 64], [9, 5]),                       # D=256, page 3
+    (2, 32, 4, 32, 1, [200, 65], [11, 5]),                       # D=32, page 1
+    (3, 16, 8, 64, 100, [650, 9, 301], [8, 9, 2]),               # D=64, page 100
 ]
 
 
