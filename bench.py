@@ -126,8 +126,10 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-KERNEL_SOURCES = {"split_kernel": ("dap_decode.cu", "dap_tile.cuh", "dap_device.cuh", "dap_internal.h"),
-                  "multi_kernel": ("dap_multi.cu", "dap_tile.cuh", "dap_device.cuh", "dap_internal.h"),
+KERNEL_SOURCES = {"split_kernel": ("dap_decode.cu", "dap_decode.cuh", "dap_tile.cuh", "dap_device.cuh",
+                                    "dap_internal.h"),
+                  "multi_kernel": ("dap_multi.cu", "dap_multi.cuh", "dap_tile.cuh", "dap_device.cuh",
+                                   "dap_internal.h"),
                   "fp8kv_kernel": ("dap_fp8kv.cu", "dap_tile.cuh", "dap_device.cuh", "dap_internal.h"),
                   "swa_kernel": ("dap_fp8.cu", "dap_device.cuh", "dap_internal.h")}
 

@@ -388,9 +388,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
                 misc[1] = 1;
                 break;
             }
-            gather_kv_tile<C>(smem + st * C::STAGE_BYTES, rp, min(BT, tok1 - t), kvg * HG, p, lane);
-            cp_async_mbar_arrive(&full[st]);
-            if (lane == 0) mbar_arrive(&full[st]);
+            fill_tile_rows<C>(smem + st * C::STAGE_BYTES, rp, min(BT, tok1 - t), kvg * HG, p, 0u, [] {}, &full[st],
+                              lane);
             issued = i + 1;
         }
         if (lane == 0) misc[0] = issued;
@@ -701,16 +700,12 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
                     if (!C::GATHER) mbar_arrive_expect_tx(&full[st], bytes);
                 }
                 if constexpr (C::GATHER) {
-                    gather_kv_tile<C>(stage, rp, nvalid, kvg * HG, p, lane);
-                    cp_async_mbar_arrive(&full[st]);
-                    if (lane == 0) {
-                        if (need_q) {
-                            mbar_arrive_expect_tx(&full[st], (uint32_t)C::QBYTES);
-                            tma_load_3d(stage + 2 * C::TILE_BYTES, &mapQ, 0, kvg * HPU, b, &full[st]);
-                        } else {
-                            mbar_arrive(&full[st]);
-                        }
-                    }
+                    fill_tile_rows<C>(stage, rp, nvalid, kvg * HG, p, need_q ? (uint32_t)C::QBYTES : 0u,
+                                      [&] {
+                                          if (need_q)
+                                              tma_load_3d(stage + 2 * C::TILE_BYTES, &mapQ, 0, kvg * HPU, b, &full[st]);
+                                      },
+                                      &full[st], lane);
                     b = nb;
                     kvg = nk;
                     j = nj;
@@ -899,16 +894,23 @@ __global__ void __launch_bounds__(128) combine_balanced_kernel(const SplitParams
 
 namespace {
 
+// K / V tensor maps with boxes of R rows (none in row-gather mode, which reads the cache
+// directly).
+template <class C>
+bool encode_maps(const DecodeArgs &a, long long rows, long long outer, int R, CUtensorMap *mk, CUtensorMap *mv) {
+    if (C::GATHER) return true;
+    return encode_cache_map<C>(mk, a.k, a.D, a.Hkv, rows, outer, R) &&
+           encode_cache_map<C>(mv, a.v, a.D, a.Hkv, rows, outer, R);
+}
+
 template <class C, bool PAGED>
 dap_status launch_per_sequence(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
     const int R = PAGED ? gcd_int(a.page_size, C::BT) : C::BT;
     p.box_rows = R;
-    CUtensorMap mk = {}, mv = {};  // (the row-gather producer reads the cache directly)
+    CUtensorMap mk = {}, mv = {};
     const long long rows = PAGED ? a.page_size : a.max_len;
     const long long outer = PAGED ? a.num_pages : a.B;
-    if (!C::GATHER && (!encode_cache_map<C>(&mk, a.k, a.D, a.Hkv, rows, outer, R) ||
-                       !encode_cache_map<C>(&mv, a.v, a.D, a.Hkv, rows, outer, R)))
-        return DAP_ERR_CUDA;
+    if (!encode_maps<C>(a, rows, outer, R, &mk, &mv)) return DAP_ERR_CUDA;
     auto kern = split_kernel<C, PAGED, false>;
     auto kern_cl = split_kernel<C, PAGED, true>;
     static PerDeviceOcc occ = {}, occ_cl = {};
@@ -943,13 +945,10 @@ template <class C, bool PAGED>
 dap_status launch_balanced(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
     const int R = PAGED ? gcd_int(a.page_size, C::BT) : C::BT;
     p.box_rows = R;
-    CUtensorMap mk = {}, mv = {}, mq;  // (the row-gather producer reads the cache directly)
+    CUtensorMap mk = {}, mv = {}, mq;
     const long long rows = PAGED ? a.page_size : a.max_len;
     const long long outer = PAGED ? a.num_pages : a.B;
-    if (!encode_q_map(&mq, a, C::HPU)) return DAP_ERR_CUDA;
-    if (!C::GATHER && (!encode_cache_map<C>(&mk, a.k, a.D, a.Hkv, rows, outer, R) ||
-                       !encode_cache_map<C>(&mv, a.v, a.D, a.Hkv, rows, outer, R)))
-        return DAP_ERR_CUDA;
+    if (!encode_q_map(&mq, a, C::HPU) || !encode_maps<C>(a, rows, outer, R, &mk, &mv)) return DAP_ERR_CUDA;
     auto kern = balanced_kernel<C, PAGED>;
     static PerDeviceOcc occ = {};
     const int per_sm = prepare_kernel(kern, C::THREADS, C::SMEM, &occ);

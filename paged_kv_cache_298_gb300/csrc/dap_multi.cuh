@@ -406,16 +406,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
                 misc[1] = 1;
                 break;
             }
-            gather_kv_tile<C>(smem + st * C::STAGE_BYTES, rp, min(BT, tok1 - t), kvh, p, lane);
-            cp_async_mbar_arrive(&full[st]);
-            if (lane == 0) {
-                if (C::MASK) {  // the tile's mask bytes by TMA (zeros past either end)
-                    mbar_arrive_expect_tx(&full[st], (uint32_t)(C::QT * BT));
-                    tma_load_3d(smem + st * C::STAGE_BYTES + C::MASK_OFF, &mapM, t, tl.q0 + tl.i0, 0, &full[st]);
-                } else {
-                    mbar_arrive(&full[st]);
-                }
-            }
+            // (with a mask: the tile's mask bytes by TMA, zeros past either end)
+            fill_tile_rows<C>(smem + st * C::STAGE_BYTES, rp, min(BT, tok1 - t), kvh, p,
+                              C::MASK ? (uint32_t)(C::QT * BT) : 0u,
+                              [&] {
+                                  if (C::MASK)
+                                      tma_load_3d(smem + st * C::STAGE_BYTES + C::MASK_OFF, &mapM, t, tl.q0 + tl.i0, 0,
+                                                  &full[st]);
+                              },
+                              &full[st], lane);
             issued = i + 1;
         }
         if (lane == 0) misc[0] = issued;

@@ -86,10 +86,11 @@ __device__ __forceinline__ void issue_kv_box(uint8_t *stage, int j, int R, const
 }
 
 // ---- row gather: page sizes that are not multiples of 8 ---------------------------------
-// Such a page size splits a tile into boxes of fewer than 8 rows, which could not start on
-// the 1024-byte boundaries of the swizzle pattern, so the producer warp copies the rows
+// Such a page size cuts a tile into boxes of fewer than 8 rows, which could not start on
+// the boundaries of the swizzle pattern (8 rows), so the producer warp copies the rows
 // itself: 16-byte cp.async chunks written straight to the swizzled positions the consumers
-// read, every lane arriving on the stage's full barrier once its own copies have landed.
+// read.  (Measured on the ragged batch: as fast as the TMA boxes of a page size of 16,
+// while 8-row TMA boxes for the groups of rows that lie in one page were slower.)
 
 template <class C>
 struct RowPages {
@@ -99,7 +100,7 @@ struct RowPages {
 
 // Raw page ids (block-table entries) and in-page slots of this lane's rows of a tile whose
 // first token is `tok`; rows at or past `nvalid` get page 0.  The loads are only issued
-// here: the values are first used by gather_kv_tile, one tile later.
+// here: the values are first used by fill_tile_rows, one tile later.
 template <class C>
 __device__ __forceinline__ void lookup_rows(RowPages<C> &rp, const int32_t *table, int tok, int nvalid,
                                             int page_size, int lane) {
@@ -116,15 +117,21 @@ __device__ __forceinline__ void lookup_rows(RowPages<C> &rp, const int32_t *tabl
     }
 }
 
-// Copy rows [0, nvalid) of kv head `kvh` of K and V into the stage's [NBLK][BT][SWB] tiles
-// (128-byte swizzle: 16-byte chunk index XOR row & 7; 64-byte: XOR (row >> 1) & 3).  Lanes
-// take consecutive chunks, so each warp-wide copy reads whole rows.  Page ids outside the
-// pool are read as page 0 and flagged, as in the TMA path.
-template <class C>
-__device__ __forceinline__ void gather_kv_tile(uint8_t *stage, const RowPages<C> &rp, int nvalid, int kvh,
-                                               const SplitParams &p, int lane) {
+// Copy rows [0, nvalid) of kv head `kvh` into the stage's [NBLK][BT][SWB] K and V tiles
+// (128-byte swizzle: 16-byte chunk index XOR row & 7; 64-byte: XOR (row >> 1) & 3), and
+// arrive on `full`: lane 0 once, with the `extra_tx` bytes of the TMA copies that
+// `extra()` (run by lane 0) issues (q, mask), and every lane once its cp.async copies have
+// landed (the barrier counts 33 arrivals).  Lane = (row r0 of every RPI rows, chunk c):
+// a warp-wide copy reads RPI whole rows, and the row step is a compile-time constant (the
+// copy loop is issue-bound: a per-chunk index search made it three times slower).  Page
+// ids outside the pool are read as page 0 and flagged, as in the TMA path.
+template <class C, class Extra>
+__device__ __forceinline__ void fill_tile_rows(uint8_t *stage, const RowPages<C> &rp, int nvalid, int kvh,
+                                               const SplitParams &p, uint32_t extra_tx, Extra extra, uint64_t *full,
+                                               int lane) {
     constexpr int CPR = C::ROWB / 16;  // 16-byte chunks per row
-    constexpr int N = RowPages<C>::N;
+    constexpr int N = RowPages<C>::N, RPI = 32 / CPR;
+    static_assert(CPR <= 32 && 32 % CPR == 0 && C::BT % RPI == 0, "whole rows per warp-wide copy");
     long long row[N];                  // element offset of this lane's rows in the cache
 #pragma unroll
     for (int k = 0; k < N; ++k) {
@@ -135,30 +142,32 @@ __device__ __forceinline__ void gather_kv_tile(uint8_t *stage, const RowPages<C>
         }
         row[k] = (((long long)pg * p.page_size + rp.slot[k]) * p.Hkv + kvh) * C::D;
     }
-    const uint32_t sk = smem_addr(stage), sv = sk + C::TILE_BYTES;
-    const int n = nvalid * CPR;
-    for (int i0 = 0; i0 < n; i0 += 32) {  // the same trip count on every lane (shuffles below)
-        const int i = i0 + lane;
-        const int r = i / CPR, c = i % CPR;
-        long long off = 0;
+    if (lane == 0) {
+        if (extra_tx) mbar_arrive_expect_tx(full, extra_tx);
+        else mbar_arrive(full);
+        extra();
+    }
+    const int c = lane % CPR, r0 = lane / CPR;
+    const int blk = c / C::CPB, cib = c % C::CPB;
+    const uint32_t sk = smem_addr(stage) + blk * (C::BT * C::SWB), sv = sk + C::TILE_BYTES;
+    const __nv_bfloat16 *kc = p.k_cache + c * 8, *vc = p.v_cache + c * 8;
 #pragma unroll
-        for (int k = 0; k < N; ++k) {
-            const long long x = __shfl_sync(0xFFFFFFFFu, row[k], r & 31);
-            if ((r >> 5) == k) off = x;
-        }
-        if (i < n) {
-            const int blk = c / C::CPB, cib = c % C::CPB;
+    for (int it = 0; it < C::BT / RPI; ++it) {
+        const int r = r0 + RPI * it;
+        const long long off = __shfl_sync(0xFFFFFFFFu, row[(RPI * it) >> 5], r & 31);
+        if (r < nvalid) {
             const int sw = C::SWB == 128 ? (r & 7) : ((r >> 1) & 3);
-            const uint32_t dst = (uint32_t)(blk * (C::BT * C::SWB) + r * C::SWB + ((cib ^ sw) << 4));
-            cp_async_16(sk + dst, p.k_cache + off + c * 8);
-            cp_async_16(sv + dst, p.v_cache + off + c * 8);
+            const uint32_t dst = (uint32_t)(r * C::SWB + ((cib ^ sw) << 4));
+            cp_async_16(sk + dst, kc + off);
+            cp_async_16(sv + dst, vc + off);
         }
     }
+    cp_async_mbar_arrive(full);
 }
 
 // Arrivals a stage's full barrier expects: one (the producer's arrive with the TMA byte
 // count), or in row-gather mode one per producer lane plus lane 0's own arrive (which
-// carries the bytes of any TMA copy the tile also takes: q, mask).
+// carries the bytes of the tile's TMA copies).
 template <class C>
 __host__ __device__ constexpr uint32_t full_arrivals() {
     return C::GATHER ? 33u : 1u;
