@@ -209,8 +209,9 @@ dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_s
  *                     DAP_SPLITS_BALANCED is not supported here.
  *   workspace         >= dap_workspace_bytes(B, Hq, Hkv, D, S) for the S used.
  *   q, out, block_table, seq_lens, max_kv_len, scale, strides: as decode_attn_paged.
- *   Supported: D = 128; G in {1, 2, 4, 8}; page_size a multiple of 8; codes and factor
- *   arrays 16-byte aligned.  q is used in f16 after an exact power-of-two shift (so any
+ *   Supported: D in {64, 128, 256}; G in {1, 2, 4, 8}; any page_size >= 1 (page sizes
+ *   that are multiples of 8 move codes and factors in TMA boxes, others row by row); codes
+ *   and factor arrays 16-byte aligned.  q is used in f16 after an exact power-of-two shift (so any
  *   finite bf16 q is representable); the result is within the bf16 path's tolerance of
  *   the exact dequantised attention.
  */

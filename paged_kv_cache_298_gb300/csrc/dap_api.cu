@@ -445,7 +445,7 @@ dap_status decode_attn_paged_fp8kv(const void *q, long long q_stride_b, long lon
         (long long)max_kv_len > (long long)max_pages * page_size)
         return DAP_ERR_SHAPE;
     if (!k_codes || !v_codes || !k_scale || !v_scale || !block_table) return DAP_ERR_NULL;
-    if (D != 128 || page_size % 8 != 0) return DAP_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128 && D != 256) return DAP_ERR_UNSUPPORTED;
     if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scale) || !aligned16(v_scale) ||
         !aligned4(block_table))
         return DAP_ERR_ALIGN;

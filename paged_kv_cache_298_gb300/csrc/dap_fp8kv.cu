@@ -1,28 +1,35 @@
 // dap_fp8kv.cu -- GQA decode attention over a paged e4m3 (fp8) K/V cache.
 //
 // Operation: the paged GQA decode of dap_decode.cu with K and V stored as OCP e4m3 codes
-// [num_pages, page_size, Hkv, 128] and one bf16 dequantisation factor per (slot, kv head)
+// [num_pages, page_size, Hkv, D] (D in {64, 128, 256}) and one bf16 dequantisation factor
+// per (slot, kv head)
 // for each, laid out [num_pages, Hkv, page_size]: the key of logical position t is
 // e4m3(code) * factor (the decode side of the fp8 cache convention of
 // nvfp4-megamoe-kernel native_swa_decode.py, applied per kv head), likewise the value.
 //
 // Schedule and data movement: the per-sequence split schedule of dap_decode.cu (one CTA
 // per (sequence, pair of kv heads, split), split partials merged by the shared combine
-// kernel).  Per 64-key tile the producer warp issues four TMA boxes per page run: the K and
-// V code rows of both kv heads (128 bytes per row and head, 128-byte swizzled) and the two
-// factor runs of the head pair, which the [pages, Hkv, page_size] layout keeps contiguous.
-// A stage carries as many bytes as a bf16 stage of one kv head, so three stages at two
-// CTAs per SM keep the same bytes in flight.
+// kernel; one kv head per CTA at D = 256 or an odd Hkv).  Code rows are stored in lines of
+// LB = min(D, 128) bytes (two column blocks at D = 256), 128-byte swizzled (64-byte at
+// D = 64).  Page sizes that are multiples of 8: per 64-key tile the producer warp issues,
+// per page run, TMA boxes of the K and V code rows of the CTA's kv heads and the factor
+// runs of those heads, which the [pages, Hkv, page_size] layout keeps contiguous.  Other
+// page sizes: the producer copies every code row in 16-byte cp.async chunks to its
+// swizzled position and stores the factors it loaded one tile earlier (the row gather of
+// the bf16 kernels).  At D = 128 a stage carries as many bytes as a bf16 stage of one kv
+// head, so three stages at two CTAs per SM keep the same bytes in flight.
 //
 // Arithmetic (tensor cores, mma.m16n8k16 in f16): every e4m3 value is an f16 value, so the
 // hardware conversion (two e4m3 codes -> one f16 pair) turns codes into operands exactly,
-// straight from the swizzled tile.  QK: A = the codes of 16 keys, B = q in f16; the factor
+// straight from the swizzled tile.  QK: A = the codes of 16 keys (lane t holding D / 4
+// consecutive dims of every line block), B = q in f16 in the same dim order; the factor
 // of each key and the softmax scale are applied to the fp32 scores (scale after the dot
 // product, as the AstrAI csrc log's numerics commit asks); q is converted to f16 after an
 // exact power-of-two shift that keeps its largest element below 2^15 (the shift goes back
 // into the scale).  PV: the A operand wants pairs of keys of one dim, so each lane reads
-// 16 dims of four key rows and byte-interleaves two keys' codes before the conversion (dims
-// 16g+2m, 16g+2m+1 in rows g, g+8 of step m); the probabilities times each key's V factor
+// DPL = D / 8 dims of four key rows and byte-interleaves two keys' codes before the
+// conversion (dims DPL g + 2m, DPL g + 2m + 1 in rows g, g+8 of step m); the probabilities
+// times each key's V factor
 // form the f16 B operand, measured in a per-warp power-of-two unit (above the largest
 // factor seen so far) so they stay within [0, 1); the accumulator is rescaled exactly when
 // the unit grows and multiplied back at the end.
@@ -31,8 +38,6 @@
 namespace dap {
 namespace f8kv {
 
-constexpr int kD = 128;
-
 // Four e4m3 codes [c0 c1 c2 c3] (low byte first) -> the f16 pairs (c0, c1) and (c2, c3),
 // exactly (the NaN codes 0x7F / 0xFF become f16 NaNs; the cache writers never produce them)
 __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
@@ -40,11 +45,6 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t
         "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
         : "=r"(lo), "=r"(hi)
         : "r"(w));
-}
-
-// word i (0..3) of a 16-byte vector
-__device__ __forceinline__ uint32_t u4_word(const uint4 &v, int i) {
-    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
 // 2^(E - 127) for a biased exponent E in 1..254 (exact)
@@ -63,18 +63,24 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], const uint32_t (&a)
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// HG kv heads per CTA (2 when Hkv is even): one TMA box carries both heads' rows of a page
-// run and the shared tile is head-major [box][head][row][128 B].  Consumer warp w serves
-// the 16-key slice w % 4 of every tile for HPW kv heads (the heads as independent streams),
-// so a CTA runs 4 * HG / HPW consumer warps.
-template <int G_, int HG_, int HPW_ = 1>
+// HG kv heads per CTA (2 when Hkv is even and D <= 128): one TMA box carries both heads'
+// rows of a page run and the shared tile is [column block][box][head][row][LB bytes].
+// Consumer warp w serves the 16-key slice w % 4 of every tile for HPW kv heads (the heads as
+// independent streams), so a CTA runs 4 * HG / HPW consumer warps.  GATHER: page sizes that
+// are not multiples of 8, the tile filled row by row as one box of BT rows.
+template <int D_, int G_, int HG_, bool GATHER_ = false, int HPW_ = 1>
 struct Cfg {
-    static constexpr int D = kD, G = G_, HG = HG_, HPW = HPW_, KW = 4, NWC = KW * (HG / HPW), BT = 64;
-    static constexpr int NS = HG == 2 ? 3 : 4, MINB = HG == 2 ? 2 : 3;
+    static constexpr int D = D_, G = G_, HG = HG_, HPW = HPW_, KW = 4, NWC = KW * (HG / HPW), BT = 64;
+    static constexpr bool GATHER = GATHER_;
     static constexpr bool SWZ = true;
+    static constexpr int LB = D < 128 ? D : 128;          // bytes of a code line (one row block)
+    static constexpr int NB = D / LB;                     // line blocks per code row
+    static constexpr int CODE_BLK = BT * HG * LB;         // one line block of a code tile
+    static constexpr int CODE_BYTES = NB * CODE_BLK;      // one tile of K (or V) codes
+    static constexpr bool BIG = 2 * CODE_BYTES >= 32768;  // stage near 33 KB: 3 stages, 2 CTAs / SM
+    static constexpr int NS = BIG ? 3 : 4, MINB = BIG ? 2 : 3;
     static constexpr int THREADS = (NWC + 1) * 32;
     static constexpr int KPW = BT / KW;                   // 16 keys per consumer warp
-    static constexpr int CODE_BYTES = BT * HG * D;        // one tile of K (or V) codes
     // The tile's K factors, then its V factors: box j (HG x R factors, R <= 64) lands in its
     // own slot, a tensor copy's shared destination being 128-byte aligned.
     static constexpr int FSLOT = 128 * HG;
@@ -86,13 +92,18 @@ struct Cfg {
     static constexpr int BAR_OFF = MISC_OFF + 16;
     static constexpr int SMEM = BAR_OFF + 2 * NS * 8 + 1024;
     static_assert(KPW == 16 && HG % HPW == 0 && MRG_BYTES <= STAGE_BYTES && FSLOT >= 2 * HG * BT, "fp8 tiling");
+    static_assert((D == 64 || D == 128 || D == 256) && (D <= 128 || HG == 1), "fp8 head dims");
 };
 
 template <class C>
 struct Consumer {
     static constexpr int D = C::D, G = C::G, HG = C::HG, HW = C::HPW, KS = D / 16;
-    uint32_t qb[HW][KS][2];  // q (f16) B fragments of head g of each kv head: dims 32t+4m+0, 1 | +2, 3
-    float acc[HW][KS][4];    // O^T: dims 16g+2m, +1 x heads 2t, 2t+1, in units of 2^(vE-127)
+    static constexpr int LB = C::LB, NB = C::NB, WPB = LB / 16;  // QK code words per lane per line block
+    static constexpr int DPL = D / 8, VW = D / 32;               // PV: dims per lane, code words per key row
+    // QK dim order: word m of a lane's codes = dims qdim(m) .. qdim(m) + 3
+    static __device__ __forceinline__ int qdim(int m, int t) { return (m / WPB) * LB + t * (LB / 4) + 4 * (m % WPB); }
+    uint32_t qb[HW][KS][2];  // q (f16) B fragments of head g of each kv head: dims qdim(m)+0, 1 | +2, 3
+    float acc[HW][KS][4];    // O^T: dims DPL g + 2m, +1 x heads 2t, 2t+1, in units of 2^(vE-127)
     float m_run[HW][2], l_run[HW][2];
     float qscale[HW];        // scale * log2(e) * 2^qshift
     int vE[HW];              // biased exponent of the V-factor unit (0 = none yet)
@@ -150,11 +161,13 @@ struct Consumer {
     // q of the G query heads of the warp's kv head h (head g at base + g * hstride);
     // qs = scale * log2(e).
     __device__ __forceinline__ void load_q(int h, const __nv_bfloat16 *base, long long hstride, float qs) {
-        uint32_t w[16];
+        constexpr int NQ = D / 8;  // bf16 pairs of a lane: LB / 4 dims of every line block
+        uint32_t w[NQ];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < NQ / 4; ++i) {
+            const int blk = i / (LB / 32), k = i % (LB / 32);
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (g < G) v = reinterpret_cast<const uint4 *>(base + g * hstride + 32 * t)[i];
+            if (g < G) v = reinterpret_cast<const uint4 *>(base + g * hstride + blk * LB + t * (LB / 4))[k];
             w[4 * i] = v.x;
             w[4 * i + 1] = v.y;
             w[4 * i + 2] = v.z;
@@ -162,7 +175,7 @@ struct Consumer {
         }
         float amax = 0.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < NQ; ++k) {
             const float2 f = bf16x2_to_float2(w[k]);
             amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
         }
@@ -175,18 +188,51 @@ struct Consumer {
 #pragma unroll
         for (int m = 0; m < KS; ++m) {
             const float2 lo = bf16x2_to_float2(w[2 * m]), hi = bf16x2_to_float2(w[2 * m + 1]);
-            qb[h][m][0] = pack_f16x2(lo.x * sh, lo.y * sh);  // dims 4m+0, 4m+1 (of 32t..)
-            qb[h][m][1] = pack_f16x2(hi.x * sh, hi.y * sh);  // dims 4m+2, 4m+3
+            qb[h][m][0] = pack_f16x2(lo.x * sh, lo.y * sh);  // dims qdim(m) + 0, 1
+            qb[h][m][1] = pack_f16x2(hi.x * sh, hi.y * sh);  // dims qdim(m) + 2, 3
         }
         qscale[h] = qs * pow2_biased(127 + e);
     }
 
-    // 32 code bytes of a 128-byte line for this lane (dims 32t .. 32t+31), 128-byte swizzled
-    __device__ __forceinline__ void line_words(const uint8_t *tile, int line, uint32_t (&w)[8]) const {
-        const uint4 a = lds128(tile + line * 128 + (((2 * t) ^ (line & 7)) << 4));
-        const uint4 b = lds128(tile + line * 128 + (((2 * t + 1) ^ (line & 7)) << 4));
-        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    // Byte offset of 16-byte chunk `ch` of line `line` in a line block: 128-byte swizzle
+    // (chunk XOR line & 7) for 128-byte lines, 64-byte (chunk XOR (line >> 1) & 3) for 64.
+    static __device__ __forceinline__ int chunk_off(int line, int ch) {
+        return line * LB + ((LB == 128 ? (ch ^ (line & 7)) : (ch ^ ((line >> 1) & 3))) << 4);
+    }
+
+    // This lane's QK code words of a key row: LB / 4 bytes of every line block (words in
+    // qdim order)
+    __device__ __forceinline__ void line_words(const uint8_t *tile, int line, uint32_t (&w)[KS]) const {
+#pragma unroll
+        for (int blk = 0; blk < NB; ++blk) {
+#pragma unroll
+            for (int k = 0; k < WPB / 4; ++k) {
+                const uint4 a = lds128(tile + blk * C::CODE_BLK + chunk_off(line, (WPB / 4) * t + k));
+                w[blk * WPB + 4 * k] = a.x;
+                w[blk * WPB + 4 * k + 1] = a.y;
+                w[blk * WPB + 4 * k + 2] = a.z;
+                w[blk * WPB + 4 * k + 3] = a.w;
+            }
+        }
+    }
+
+    // This lane's PV code words of a key row: dims DPL g .. DPL g + DPL - 1
+    __device__ __forceinline__ void v_words(const uint8_t *tile, int line, uint32_t (&w)[VW]) const {
+        if constexpr (VW == 2) {  // 8 bytes: half g & 1 of chunk g >> 1 (64-byte lines)
+            const uint2 a = *reinterpret_cast<const uint2 *>(tile + chunk_off(line, g >> 1) + (g & 1) * 8);
+            w[0] = a.x;
+            w[1] = a.y;
+        } else {  // 16-byte chunks (DPL g) / 16 .. of line block (DPL g) / LB
+#pragma unroll
+            for (int k = 0; k < VW / 4; ++k) {
+                const int byte = DPL * g + 16 * k;
+                const uint4 a = lds128(tile + (byte / LB) * C::CODE_BLK + chunk_off(line, (byte % LB) >> 4));
+                w[4 * k] = a.x;
+                w[4 * k + 1] = a.y;
+                w[4 * k + 2] = a.z;
+                w[4 * k + 3] = a.w;
+            }
+        }
     }
 
     __device__ __forceinline__ void tile(const uint8_t *stage, int nvalid) {
@@ -202,18 +248,15 @@ struct Consumer {
             const float kfac1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::KS_OFF + o1));
             const float vfac0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::VS_OFF + o0));
             const float vfac1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(stage + C::VS_OFF + o1));
-            // V: dims 16g .. 16g+15 of keys 2t, 2t+1, 2t+8, 2t+9 (128-byte swizzle: line & 7 =
-            // key & 7, the boxes being multiples of 8 rows)
-            uint4 vw[4];
+            // V: dims DPL g .. of keys 2t, 2t+1, 2t+8, 2t+9 (the boxes being multiples of 8
+            // rows, an even key and the next one are consecutive lines)
+            uint32_t vw[4][VW];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int ln = (j < 2 ? vline0 : vline2) + (j & 1) + h * hline;
-                vw[j] = lds128(sV + ln * 128 + ((g ^ (ln & 7)) << 4));
-            }
+            for (int j = 0; j < 4; ++j) v_words(sV, (j < 2 ? vline0 : vline2) + (j & 1) + h * hline, vw[j]);
             // S^T = K . Q^T (keys g, g+8 x heads 2t, 2t+1)
             float c[4] = {0.f, 0.f, 0.f, 0.f};
             {
-                uint32_t k0[8], k1[8];
+                uint32_t k0[KS], k1[KS];
                 line_words(sK, l0, k0);
                 line_words(sK, l1, k1);
 #pragma unroll
@@ -278,16 +321,18 @@ struct Consumer {
             if (nv < 16) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (2 * t + (j & 1) + 8 * (j >> 1) >= nv) vw[j] = make_uint4(0u, 0u, 0u, 0u);
+                    if (2 * t + (j & 1) + 8 * (j >> 1) >= nv)
+#pragma unroll
+                        for (int k = 0; k < VW; ++k) vw[j][k] = 0u;
             }
-            // A rows g, g+8 = dims 16g+2m, 16g+2m+1; k = keys: byte-interleave keys 2t, 2t+1
+            // A rows g, g+8 = dims DPL g + 2m, + 1; k = keys: byte-interleave keys 2t, 2t+1
             // (and 2t+8, 2t+9) so that one conversion yields a key pair of one dim
 #pragma unroll
             for (int m = 0; m < KS; ++m) {
                 const int wi = m >> 1;
                 const uint32_t sel = (m & 1) ? 0x7362u : 0x5140u;
-                const uint32_t ab = __byte_perm(u4_word(vw[0], wi), u4_word(vw[1], wi), sel);
-                const uint32_t cd = __byte_perm(u4_word(vw[2], wi), u4_word(vw[3], wi), sel);
+                const uint32_t ab = __byte_perm(vw[0][wi], vw[1][wi], sel);
+                const uint32_t cd = __byte_perm(vw[2][wi], vw[3][wi], sel);
                 uint32_t a[4];
                 e4m3x4_to_f16(ab, a[0], a[1]);
                 e4m3x4_to_f16(cd, a[2], a[3]);
@@ -323,14 +368,14 @@ struct Consumer {
         const int tid = warp * 32 + lane;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            if ((g >> 2) == half) {  // this lane's dims 16g .. 16g+15 lie in this half
+            if ((g >> 2) == half) {  // this lane's dims DPL g .. DPL g + DPL - 1 lie in this half
 #pragma unroll
                 for (int h = 0; h < HW; ++h) {
-                    // back from units of 2^(vE - 127) (V factors); dims 16g+2m, +1
+                    // back from units of 2^(vE - 127) (V factors); dims DPL g + 2m, +1
                     const float unit = vE[h] > 0 ? pow2_biased(vE[h]) : 0.f;
 #pragma unroll
                     for (int m = 0; m < KS; ++m) {
-                        const int dlo = 16 * g + 2 * m - half * DH;
+                        const int dlo = DPL * g + 2 * m - half * DH;
 #pragma unroll
                         for (int j = 0; j < 2; ++j) {
                             if (2 * t + j < G) {
@@ -366,6 +411,98 @@ struct Consumer {
     }
 };
 
+// ---- row gather (page sizes that are not multiples of 8) -------------------------------
+// The tile is one box of BT rows: code line of (row r, head h) = h * BT + r, factors at
+// byte (h * BT + r) * 2 of the tile's factor slots.  Page ids are looked up one tile ahead,
+// factors loaded one tile ahead (after the page ids have landed), so that the copy of a
+// tile never waits on a global load.
+
+template <class C>
+struct GatherPages {
+    static constexpr int N = C::BT / 32;  // rows per lane: lane, lane + 32
+    int pg[N], slot[N];
+    __device__ __forceinline__ void lookup(const int32_t *table, int tok, int nvalid, int page_size, int lane) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+            const int r = lane + 32 * k;
+            pg[k] = 0;
+            slot[k] = 0;
+            if (r < nvalid) {
+                pg[k] = __ldg(table + (tok + r) / page_size);
+                slot[k] = (tok + r) % page_size;
+            }
+        }
+    }
+    // page ids outside the pool are read as page 0 and flagged
+    __device__ __forceinline__ void check(int nvalid, int num_pages, int lane) {
+#pragma unroll
+        for (int k = 0; k < N; ++k)
+            if (lane + 32 * k < nvalid && (pg[k] < 0 || pg[k] >= num_pages)) {
+                flag_error(DAP_DEVERR_PAGE);
+                pg[k] = 0;
+            }
+    }
+    // the K and V factor bits of this lane's rows, heads kvh0 .. kvh0 + HG - 1
+    __device__ __forceinline__ void load_factors(uint32_t (&f)[N][C::HG], const SplitParams &p, int kvh0,
+                                                 int nvalid, int lane) const {
+        const uint16_t *ks = reinterpret_cast<const uint16_t *>(p.k_scale);
+        const uint16_t *vs = reinterpret_cast<const uint16_t *>(p.v_scale);
+#pragma unroll
+        for (int k = 0; k < N; ++k)
+#pragma unroll
+            for (int h = 0; h < C::HG; ++h) {
+                f[k][h] = 0u;
+                if (lane + 32 * k < nvalid) {
+                    const long long i = ((long long)pg[k] * p.Hkv + kvh0 + h) * p.page_size + slot[k];
+                    f[k][h] = (uint32_t)__ldg(ks + i) | ((uint32_t)__ldg(vs + i) << 16);
+                }
+            }
+    }
+};
+
+// Copy rows [0, nvalid) of the CTA's kv heads into the stage (codes by cp.async, factors
+// stored from registers) and arrive on `full` twice per lane: once when its copies have
+// landed, once after its factor stores (64 arrivals).
+template <class C>
+__device__ __forceinline__ void gather_codes(uint8_t *stage, const GatherPages<C> &gp,
+                                             const uint32_t (&fac)[GatherPages<C>::N][C::HG], int nvalid, int kvh0,
+                                             const SplitParams &p, uint64_t *full, int lane) {
+    constexpr int D = C::D, LB = C::LB, BT = C::BT, HG = C::HG, N = GatherPages<C>::N;
+    constexpr int CPR = D / 16, IPI = 32 / CPR;  // chunks per code row; (row, head) items per copy
+    long long row[N];                            // byte offset of this lane's rows (head kvh0)
+#pragma unroll
+    for (int k = 0; k < N; ++k) row[k] = (((long long)gp.pg[k] * p.page_size + gp.slot[k]) * p.Hkv + kvh0) * D;
+    // lane = (item r0 of every IPI items, chunk c); item = h * BT + r
+    const int c = lane % CPR, r0 = lane / CPR;
+    const int blk = c / (LB / 16), cib = c % (LB / 16);
+    const uint32_t sk = smem_addr(stage) + blk * C::CODE_BLK, sv = sk + C::CODE_BYTES;
+    const uint8_t *kc = p.k_codes + c * 16, *vc = p.v_codes + c * 16;
+#pragma unroll
+    for (int it = 0; it < HG * BT / IPI; ++it) {
+        const int h = (IPI * it) / BT, r = (IPI * it) % BT + r0;
+        const long long off = __shfl_sync(0xFFFFFFFFu, row[((IPI * it) % BT) >> 5], r & 31) + h * D;
+        if (r < nvalid) {
+            const int line = h * BT + r;
+            const int sw = LB == 128 ? (line & 7) : ((line >> 1) & 3);
+            const uint32_t dst = (uint32_t)(line * LB + ((cib ^ sw) << 4));
+            cp_async_16(sk + dst, kc + off);
+            cp_async_16(sv + dst, vc + off);
+        }
+    }
+    uint16_t *fk = reinterpret_cast<uint16_t *>(stage + C::KS_OFF);
+    uint16_t *fv = reinterpret_cast<uint16_t *>(stage + C::VS_OFF);
+#pragma unroll
+    for (int k = 0; k < N; ++k)
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+            const int r = lane + 32 * k;
+            fk[h * BT + r] = (uint16_t)(fac[k][h] & 0xFFFFu);
+            fv[h * BT + r] = (uint16_t)(fac[k][h] >> 16);
+        }
+    cp_async_mbar_arrive(full);
+    mbar_arrive(full);  // (release: this lane's factor stores)
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
     fp8kv_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
@@ -388,9 +525,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int L = p.seq_lens[b];
-    const int R = p.box_rows;
+    const int R = C::GATHER ? BT : p.box_rows;  // (row gather: the tile is one box of BT rows)
     int pg_first = 0;  // loaded with the length (entries past the end are read, not used)
-    if (warp == NWC && lane * R < BT) {
+    if (!C::GATHER && warp == NWC && lane * R < BT) {
         const long long t = (long long)s * p.chunk + lane * R;
         if (t < (long long)p.max_pages * p.page_size)
             pg_first = __ldg(p.block_table + (long long)b * p.max_pages + t / p.page_size);
@@ -410,7 +547,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     int *misc = reinterpret_cast<int *>(smem + C::MISC_OFF);  // [0] tiles issued, [1] abort
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], C::GATHER ? 64u : 1u);  // row gather: two arrivals per producer lane
             mbar_init(&empty[i], NWC);
         }
         misc[0] = 0;
@@ -419,6 +556,39 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     }
     __syncthreads();
 
+    if (C::GATHER && warp == NWC) {  // ---- producer warp, row gather
+        const int32_t *table = p.block_table + (long long)b * p.max_pages;
+        GatherPages<C> gp_next;
+        uint32_t fac[GatherPages<C>::N][HG];  // (K | V << 16) factor bits of the tile being filled
+        if (ntiles > 0) {
+            gp_next.lookup(table, tok0, min(BT, tok1 - tok0), p.page_size, lane);
+            gp_next.check(min(BT, tok1 - tok0), p.num_pages, lane);
+            gp_next.load_factors(fac, p, kvg * HG, min(BT, tok1 - tok0), lane);
+        }
+        int issued = 0;
+        for (int i = 0; i < ntiles; ++i) {
+            const int st = i % NS;
+            const int t = tok0 + i * BT;
+            const int nvalid = min(BT, tok1 - t), nnext = min(BT, tok1 - t - BT);
+            const GatherPages<C> gp = gp_next;
+            if (i + 1 < ntiles) gp_next.lookup(table, t + BT, nnext, p.page_size, lane);
+            if (i >= NS && !__all_sync(0xFFFFFFFFu, mbar_wait(&empty[st], ((i / NS) - 1) & 1))) {
+                misc[1] = 1;
+                break;
+            }
+            gather_codes<C>(smem + st * C::STAGE_BYTES, gp, fac, nvalid, kvg * HG, p, &full[st], lane);
+            issued = i + 1;
+            // the next tile's factors, loaded while this one's copies land (its page ids
+            // were issued at the top of this iteration)
+            if (i + 1 < ntiles) {
+                gp_next.check(nnext, p.num_pages, lane);
+                gp_next.load_factors(fac, p, kvg * HG, nnext, lane);
+            }
+        }
+        if (lane == 0) misc[0] = issued;
+        __syncthreads();
+        return;
+    }
     if (warp == NWC) {  // ---- producer warp
         if (lane == 0) {
             prefetch_tensormap(&mapK);
@@ -454,8 +624,12 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
             if (lane < nbox) {
                 uint8_t *stage = smem + st * C::STAGE_BYTES;
                 const int row = (t + lane * R) % p.page_size;
-                tma_load_4d(stage + lane * R * HG * D, &mapK, 0, row, kvg * HG, pg, &full[st]);
-                tma_load_4d(stage + C::CODE_BYTES + lane * R * HG * D, &mapV, 0, row, kvg * HG, pg, &full[st]);
+#pragma unroll
+                for (int blk = 0; blk < C::NB; ++blk) {
+                    uint8_t *dst = stage + blk * C::CODE_BLK + lane * R * HG * C::LB;
+                    tma_load_4d(dst, &mapK, blk * C::LB, row, kvg * HG, pg, &full[st]);
+                    tma_load_4d(dst + C::CODE_BYTES, &mapV, blk * C::LB, row, kvg * HG, pg, &full[st]);
+                }
                 tma_load_3d(stage + C::KS_OFF + lane * C::FSLOT, &mapKS, row, kvg * HG, pg, &full[st]);
                 tma_load_3d(stage + C::VS_OFF + lane * C::FSLOT, &mapVS, row, kvg * HG, pg, &full[st]);
             }
@@ -520,13 +694,14 @@ bool encode_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, i
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// codes [P, ps, Hkv, 128] bytes viewed as [128, ps, Hkv, P] (the head dim outside the slot
-// dim); box [128, R, HG, 1] lands head-major, 128-byte swizzled
-bool encode_codes(CUtensorMap *map, const void *base, int Hkv, int ps, int P, int R, int HG) {
-    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)ps, (cuuint64_t)Hkv, (cuuint64_t)P};
-    const cuuint64_t strides[3] = {(cuuint64_t)Hkv * kD, (cuuint64_t)kD, (cuuint64_t)ps * Hkv * kD};
-    const cuuint32_t box[4] = {(cuuint32_t)kD, (cuuint32_t)R, (cuuint32_t)HG, 1u};
-    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+// codes [P, ps, Hkv, D] bytes viewed as [D, ps, Hkv, P] (the head dim outside the slot
+// dim); box [LB, R, HG, 1] lands head-major, 128-byte swizzled (64-byte for 64-byte lines)
+bool encode_codes(CUtensorMap *map, const void *base, int D, int LB, int Hkv, int ps, int P, int R, int HG) {
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)ps, (cuuint64_t)Hkv, (cuuint64_t)P};
+    const cuuint64_t strides[3] = {(cuuint64_t)Hkv * D, (cuuint64_t)D, (cuuint64_t)ps * Hkv * D};
+    const cuuint32_t box[4] = {(cuuint32_t)LB, (cuuint32_t)R, (cuuint32_t)HG, 1u};
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 4, dims, strides, box,
+                      LB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // factors [P, Hkv, ps] bf16 viewed as [ps, Hkv, P]; box [R, HG, 1]
@@ -538,16 +713,16 @@ bool encode_factors(CUtensorMap *map, const void *base, int Hkv, int ps, int P, 
                       CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <int G, int HG>
+template <int D, int G, int HG, bool GATHER>
 dap_status launch_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
-    using C = Cfg<G, HG>;
+    using C = Cfg<D, G, HG, GATHER>;
     const int R = gcd_int(a.page_size, C::BT);
     p.box_rows = R;
-    CUtensorMap mk, mv, mks, mvs;
-    if (!encode_codes(&mk, a.k, a.Hkv, a.page_size, a.num_pages, R, HG) ||
-        !encode_codes(&mv, a.v, a.Hkv, a.page_size, a.num_pages, R, HG) ||
-        !encode_factors(&mks, a.k_scale, a.Hkv, a.page_size, a.num_pages, R, HG) ||
-        !encode_factors(&mvs, a.v_scale, a.Hkv, a.page_size, a.num_pages, R, HG))
+    CUtensorMap mk = {}, mv = {}, mks = {}, mvs = {};  // (the row-gather producer reads the cache directly)
+    if (!GATHER && (!encode_codes(&mk, a.k, D, C::LB, a.Hkv, a.page_size, a.num_pages, R, HG) ||
+                    !encode_codes(&mv, a.v, D, C::LB, a.Hkv, a.page_size, a.num_pages, R, HG) ||
+                    !encode_factors(&mks, a.k_scale, a.Hkv, a.page_size, a.num_pages, R, HG) ||
+                    !encode_factors(&mvs, a.v_scale, a.Hkv, a.page_size, a.num_pages, R, HG)))
         return DAP_ERR_CUDA;
     auto kern = fp8kv_kernel<C>;
     static PerDeviceOcc occ = {};
@@ -564,26 +739,42 @@ dap_status launch_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
         return DAP_ERR_CUDA;
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
     if (a.num_splits > 1) {
-        if (launch_combine<kD>(p, a.B, a.Hq, a.num_splits, stream) != cudaSuccess) return DAP_ERR_CUDA;
+        if (launch_combine<D>(p, a.B, a.Hq, a.num_splits, stream) != cudaSuccess) return DAP_ERR_CUDA;
     }
     if (g_trace.combine_end) cudaEventRecord(g_trace.combine_end, stream);
     return DAP_OK;
+}
+
+// two kv heads per CTA when they pair up and a row is at most 128 bytes
+template <int D, bool GATHER>
+dap_status launch_d(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
+    constexpr bool WIDE = D > 128;
+    const bool pair = !WIDE && a.Hkv % 2 == 0;
+    switch (a.Hq / a.Hkv) {
+        case 1: return pair ? launch_g<D, 1, WIDE ? 1 : 2, GATHER>(a, p, stream) : launch_g<D, 1, 1, GATHER>(a, p, stream);
+        case 2: return pair ? launch_g<D, 2, WIDE ? 1 : 2, GATHER>(a, p, stream) : launch_g<D, 2, 1, GATHER>(a, p, stream);
+        case 4: return pair ? launch_g<D, 4, WIDE ? 1 : 2, GATHER>(a, p, stream) : launch_g<D, 4, 1, GATHER>(a, p, stream);
+        case 8: return pair ? launch_g<D, 8, WIDE ? 1 : 2, GATHER>(a, p, stream) : launch_g<D, 8, 1, GATHER>(a, p, stream);
+    }
+    return DAP_ERR_UNSUPPORTED;
+}
+
+template <bool GATHER>
+dap_status launch_any(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
+    switch (a.D) {
+        case 64: return launch_d<64, GATHER>(a, p, stream);
+        case 128: return launch_d<128, GATHER>(a, p, stream);
+        case 256: return launch_d<256, GATHER>(a, p, stream);
+    }
+    return DAP_ERR_UNSUPPORTED;
 }
 
 }  // namespace
 }  // namespace f8kv
 
 dap_status launch_decode_fp8kv(const DecodeArgs &a, cudaStream_t stream) {
-    if (a.D != f8kv::kD) return DAP_ERR_UNSUPPORTED;
     SplitParams p = make_params(a);
-    const bool pair = a.Hkv % 2 == 0;  // two kv heads per CTA when they pair up
-    switch (a.Hq / a.Hkv) {
-        case 1: return pair ? f8kv::launch_g<1, 2>(a, p, stream) : f8kv::launch_g<1, 1>(a, p, stream);
-        case 2: return pair ? f8kv::launch_g<2, 2>(a, p, stream) : f8kv::launch_g<2, 1>(a, p, stream);
-        case 4: return pair ? f8kv::launch_g<4, 2>(a, p, stream) : f8kv::launch_g<4, 1>(a, p, stream);
-        case 8: return pair ? f8kv::launch_g<8, 2>(a, p, stream) : f8kv::launch_g<8, 1>(a, p, stream);
-    }
-    return DAP_ERR_UNSUPPORTED;
+    return a.page_size % 8 == 0 ? f8kv::launch_any<false>(a, p, stream) : f8kv::launch_any<true>(a, p, stream);
 }
 
 bool read_errors_fp8kv(unsigned int *flags, bool clear) {

@@ -19,6 +19,8 @@ struct SplitParams {
     const __nv_bfloat16 *q;
     long long q_sb, q_sh;
     const __nv_bfloat16 *k_cache, *v_cache;  // read directly by the row-gather producer
+    const uint8_t *k_codes, *v_codes;        // e4m3 cache (row gather): codes and factors
+    const void *k_scale, *v_scale;
     const int32_t *block_table;
     int max_pages;
     const int32_t *seq_lens;
@@ -485,6 +487,10 @@ SplitParams make_params(const DecodeArgs &a) {
     p.q_sh = a.q_sh;
     p.k_cache = static_cast<const __nv_bfloat16 *>(a.k);
     p.v_cache = static_cast<const __nv_bfloat16 *>(a.v);
+    p.k_codes = static_cast<const uint8_t *>(a.k);
+    p.v_codes = static_cast<const uint8_t *>(a.v);
+    p.k_scale = a.k_scale;
+    p.v_scale = a.v_scale;
     p.block_table = a.block_table;
     p.max_pages = a.max_pages;
     p.seq_lens = a.seq_lens;

@@ -271,7 +271,7 @@ def fp8kv_call(lib, **kw):
     (dict(B=-1), 2), (dict(Hq=30), 2), (dict(maxlen=8 * 16 + 1), 2), (dict(S=-2), 2), (dict(S=-1), 3),
     (dict(P=0), 2),
     (dict(kc=None), 1), (dict(ks=None), 1), (dict(vs=None), 1), (dict(table=None), 1), (dict(q=None), 1),
-    (dict(D=64, qsb=32 * 64, qsh=64, osb=32 * 64, osh=64), 3), (dict(ps=12, maxlen=90), 3), (dict(Hq=64, Hkv=4), 3),
+    (dict(D=32, qsb=32 * 32, qsh=32, osb=32 * 32, osh=32), 3), (dict(Hq=64, Hkv=4), 3),
     (dict(ks=ctypes.c_void_p((1 << 20) + 8)), 5), (dict(kc=ctypes.c_void_p((1 << 20) + 4)), 5),
     (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=64), 4),
 ])

@@ -71,6 +71,63 @@ def test_parity_across_groups_pages_and_splits(B, Hq, Hkv, ps, lens):
     assert binding.get_device_errors() == 0
 
 
+# head dims 64 and 256 (64-byte lines with the 64-byte swizzle; two 128-byte line blocks,
+# one kv head per CTA), and page sizes that are not multiples of 8 (rows copied one by one,
+# factors stored by the producer), at every head dim
+OTHER = [
+    # B, Hq, Hkv, D, ps, lens
+    (3, 32, 8, 64, 16, [257, 1000, 17]),      # D=64, kv-head pairs
+    (3, 12, 3, 64, 8, [40, 300, 129]),        # D=64, odd kv head count
+    (2, 64, 8, 256, 16, [128, 777]),          # D=256, G=8
+    (4, 16, 8, 256, 32, [65, 130, 0, 500]),   # D=256, G=2, an empty sequence
+    (3, 32, 8, 128, 12, [257, 1000, 17]),     # page 12
+    (2, 8, 1, 128, 1, [100, 3]),              # page 1, one kv head
+    (3, 16, 4, 64, 5, [100, 47, 400]),        # D=64, page 5
+    (3, 12, 3, 256, 3, [40, 300, 129]),       # D=256, page 3
+    (5, 16, 2, 128, 100, [1, 2, 63, 64, 650]),  # page 100, lengths around one tile
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,ps,lens", OTHER, ids=[f"D{o[3]}_ps{o[4]}_G{o[1] // o[2]}" for o in OTHER])
+def test_head_dims_64_256_and_any_page_size(B, Hq, Hkv, D, ps, lens):
+    case = inputs.make_fp8kv_case(B, Hq, Hkv, D, ps, lens, 5300 + D + ps).to("cuda")
+    ref = oracle_fp8kv(case)
+    for S in [0, 1, 3, 7]:
+        assert_close(gpu_fp8kv(case, S), ref, f"D={D} ps={ps} S={S}")
+    assert binding.get_device_errors() == 0
+
+
+def test_row_gather_page_permutation_and_bad_page_id():
+    """Page size 12: the same bits under a permutation of the physical pages; a page id
+    outside the pool is read as page 0 and flagged."""
+    case = inputs.make_fp8kv_case(4, 32, 8, 128, 12, [700, 33, 1024, 260], 5400).to("cuda")
+    P = case.k_codes.shape[0]
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(7)).cuda()
+    inv = torch.argsort(perm)
+    table = inv[case.block_table.long()].to(torch.int32).contiguous()
+    for S in [0, 1, 5]:
+        a = gpu_fp8kv(case, S)
+        b = binding.decode_attn_paged_fp8kv(case.q, case.k_codes[perm].contiguous(), case.v_codes[perm].contiguous(),
+                                            case.k_scale[perm].contiguous(), case.v_scale[perm].contiguous(), table,
+                                            case.seq_lens, max_kv_len=case.max_kv_len, scale=case.scale,
+                                            num_splits=S)
+        assert torch.equal(a, b), f"S={S}"
+    assert binding.get_device_errors() == 0
+    bad = case.block_table.clone()
+    bad[1, 0] = P + 3
+    fixed = bad.clone()
+    fixed[1, 0] = 0
+    kw = dict(max_kv_len=case.max_kv_len, scale=case.scale, num_splits=1)
+    out = binding.decode_attn_paged_fp8kv(case.q, case.k_codes, case.v_codes, case.k_scale, case.v_scale, bad,
+                                          case.seq_lens, **kw)
+    torch.cuda.synchronize()
+    assert binding.get_device_errors(clear=True) & binding.DEVERR_PAGE
+    want = binding.decode_attn_paged_fp8kv(case.q, case.k_codes, case.v_codes, case.k_scale, case.v_scale, fixed,
+                                           case.seq_lens, **kw)
+    assert torch.equal(out.view(torch.int16), want.view(torch.int16))
+    assert binding.get_device_errors(clear=True) == 0
+
+
 def test_wide_factor_range_and_q_beyond_f16():
     # factors spread over 2^-6 .. 2^7 within every page; q times 2^16 (most elements beyond
     # f16's range before the kernel's power-of-two shift) with the softmax scale divided by
