@@ -557,33 +557,48 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
     __syncthreads();
 
     if (C::GATHER && warp == NWC) {  // ---- producer warp, row gather
+        // Software pipeline over three buffers, each one tile's page ids and factors: at the
+        // start of step i, buffer A holds tile i (both landed), B tile i + 1 (factors in
+        // flight), C tile i + 2 (page ids in flight).  Step i fills tile i from A, then loads
+        // C's factors and issues A's page ids for tile i + 3; the next step takes (B, C, A).
+        // The roles rotate by unrolling three steps, so no register that a load in flight
+        // will write is ever copied (a copy waits for the load: rotating by copies left a
+        // full memory latency in every step and held the copy to a third of the TMA path).
+        struct Buf {
+            GatherPages<C> g;
+            uint32_t f[GatherPages<C>::N][HG];  // (K | V << 16) factor bits
+        };
         const int32_t *table = p.block_table + (long long)b * p.max_pages;
-        GatherPages<C> gp_next;
-        uint32_t fac[GatherPages<C>::N][HG];  // (K | V << 16) factor bits of the tile being filled
-        if (ntiles > 0) {
-            gp_next.lookup(table, tok0, min(BT, tok1 - tok0), p.page_size, lane);
-            gp_next.check(min(BT, tok1 - tok0), p.num_pages, lane);
-            gp_next.load_factors(fac, p, kvg * HG, min(BT, tok1 - tok0), lane);
-        }
+        const int kvh0 = kvg * HG;
+        auto nval = [&](int i) { return max(0, min(BT, tok1 - (tok0 + i * BT))); };
+        Buf A, B2, C2;
+        A.g.lookup(table, tok0, nval(0), p.page_size, lane);
+        B2.g.lookup(table, tok0 + BT, nval(1), p.page_size, lane);
+        C2.g.lookup(table, tok0 + 2 * BT, nval(2), p.page_size, lane);
+        A.g.check(nval(0), p.num_pages, lane);
+        A.g.load_factors(A.f, p, kvh0, nval(0), lane);
+        B2.g.check(nval(1), p.num_pages, lane);
+        B2.g.load_factors(B2.f, p, kvh0, nval(1), lane);
         int issued = 0;
-        for (int i = 0; i < ntiles; ++i) {
+        // one step: fill tile i from x, load z's factors (tile i + 2), issue x's page ids
+        // for tile i + 3; false when a wait gave up
+        auto step = [&](int i, Buf &x, Buf &z) -> bool {
             const int st = i % NS;
-            const int t = tok0 + i * BT;
-            const int nvalid = min(BT, tok1 - t), nnext = min(BT, tok1 - t - BT);
-            const GatherPages<C> gp = gp_next;
-            if (i + 1 < ntiles) gp_next.lookup(table, t + BT, nnext, p.page_size, lane);
             if (i >= NS && !__all_sync(0xFFFFFFFFu, mbar_wait(&empty[st], ((i / NS) - 1) & 1))) {
                 misc[1] = 1;
-                break;
+                return false;
             }
-            gather_codes<C>(smem + st * C::STAGE_BYTES, gp, fac, nvalid, kvg * HG, p, &full[st], lane);
+            gather_codes<C>(smem + st * C::STAGE_BYTES, x.g, x.f, nval(i), kvh0, p, &full[st], lane);
             issued = i + 1;
-            // the next tile's factors, loaded while this one's copies land (its page ids
-            // were issued at the top of this iteration)
-            if (i + 1 < ntiles) {
-                gp_next.check(nnext, p.num_pages, lane);
-                gp_next.load_factors(fac, p, kvg * HG, nnext, lane);
-            }
+            z.g.check(nval(i + 2), p.num_pages, lane);
+            z.g.load_factors(z.f, p, kvh0, nval(i + 2), lane);
+            x.g.lookup(table, tok0 + (i + 3) * BT, nval(i + 3), p.page_size, lane);
+            return true;
+        };
+        for (int i = 0; i < ntiles; i += 3) {
+            if (!step(i, A, C2) || i + 1 >= ntiles) break;
+            if (!step(i + 1, B2, A) || i + 2 >= ntiles) break;
+            if (!step(i + 2, C2, B2)) break;
         }
         if (lane == 0) misc[0] = issued;
         __syncthreads();
@@ -745,10 +760,11 @@ dap_status launch_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
     return DAP_OK;
 }
 
-// two kv heads per CTA when they pair up and a row is at most 128 bytes
+// two kv heads per CTA when they pair up, a row is at most 128 bytes and the tiles come by
+// TMA (the row-gather producer's registers spilled at two heads per CTA)
 template <int D, bool GATHER>
 dap_status launch_d(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
-    constexpr bool WIDE = D > 128;
+    constexpr bool WIDE = D > 128 || GATHER;
     const bool pair = !WIDE && a.Hkv % 2 == 0;
     switch (a.Hq / a.Hkv) {
         case 1: return pair ? launch_g<D, 1, WIDE ? 1 : 2, GATHER>(a, p, stream) : launch_g<D, 1, 1, GATHER>(a, p, stream);
