@@ -106,15 +106,16 @@ struct MmaConsumer {
     float acc[KS][4];    // O^T fragments: dims 16m+g, 16m+g+8 x heads 2t, 2t+1
     float m_run[2], l_run[2];
     float qscale;
-    int warp, lane, g, t, key0;
+    int warp, lane, g, t, key0, rb;  // rb: log2 of the tile's box rows (tile_off)
     static constexpr int hh = 0;
 
-    __device__ __forceinline__ void init(int w, int l, uint8_t *) {
+    __device__ __forceinline__ void init(int w, int l, uint8_t *, int box_rows_log2) {
         warp = w;
         lane = l;
         g = l >> 2;
         t = l & 3;
         key0 = w * C::KPW;
+        rb = box_rows_log2;
     }
 
     __device__ __forceinline__ void reset() {
@@ -143,14 +144,8 @@ struct MmaConsumer {
         }
     }
 
-    // byte offset of (key, dim) in a swizzled [NBLK][BT][SWB] tile: the 128-byte swizzle XORs
-    // the 16-byte chunk index with key & 7, the 64-byte one with (key >> 1) & 3
-    static __device__ __forceinline__ uint32_t off(int key, int dim) {
-        const int byte = dim * 2;
-        const int chunk = (byte % C::SWB) >> 4;
-        const int sw = C::SWB == 128 ? (key & 7) : ((key >> 1) & 3);
-        return (uint32_t)((byte / C::SWB) * (C::BT * C::SWB) + key * C::SWB + ((chunk ^ sw) << 4));
-    }
+    // byte offset of (key, dim) in the swizzled tile (tile_off)
+    __device__ __forceinline__ uint32_t off(int key, int dim) const { return tile_off<C>(key, dim >> 3, rb); }
 
     __device__ __forceinline__ void tile(uint8_t *stage, int nvalid) {
         const int nv = nvalid - key0;
@@ -159,9 +154,8 @@ struct MmaConsumer {
         if (nv < 16) {  // rows past the end may hold anything: zero their V so 0 * V stays 0
             for (int i = lane; i < (16 - nv) * C::NBLK * C::CPB; i += 32) {
                 const int row = key0 + nv + i / (C::NBLK * C::CPB);
-                const int rest = i % (C::NBLK * C::CPB);
-                *reinterpret_cast<uint4 *>(sV + (rest / C::CPB) * (C::BT * C::SWB) + row * C::SWB +
-                                           (rest % C::CPB) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(sV + tile_off<C>(row, i % (C::NBLK * C::CPB), rb)) =
+                    make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -439,7 +433,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
 
     // ---- consumer warps
     ConsumerOf<C> cs;
-    cs.init(warp, lane, smem);
+    cs.init(warp, lane, smem, 31 - __clz(PAGED && !C::GATHER ? R : BT));
     cs.reset();
     const int kvh = kvg * HG + cs.hh;
     cs.load_q(p.q + (long long)b * p.q_sb + (long long)kvh * G * p.q_sh, p.q_sh, p.qscale);
@@ -740,7 +734,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
 
     // ---- consumer warps
     ConsumerOf<C> cs;
-    cs.init(warp, lane, smem);
+    cs.init(warp, lane, smem, 31 - __clz(PAGED && !C::GATHER ? p.box_rows : BT));
     cs.reset();
     float *mrg = reinterpret_cast<float *>(smem + C::MRG_OFF);
     ConsumerBarrier cb{cbar, 0u};

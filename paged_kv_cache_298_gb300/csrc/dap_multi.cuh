@@ -73,12 +73,13 @@ struct MultiConsumer {
     float acc[KS][NT][4];
     float m_run[NT][2], l_run[NT][2];
     float qscale;
-    int warp, lane, g, t, kw, key0, col0, nq, p_base;
+    int warp, lane, g, t, kw, key0, col0, nq, p_base, rb;  // rb: log2 of the tile's box rows (tile_off)
     static constexpr int hh = 0;
 
-    __device__ __forceinline__ void init(int w, int l, uint8_t *) {
+    __device__ __forceinline__ void init(int w, int l, uint8_t *, int box_rows_log2) {
         warp = w;
         lane = l;
+        rb = box_rows_log2;
         g = l >> 2;
         t = l & 3;
         kw = w % C::KW;
@@ -125,14 +126,8 @@ struct MultiConsumer {
         }
     }
 
-    // byte offset of (key, dim) in a swizzled [NBLK][BT][SWB] tile: the 128-byte swizzle XORs
-    // the 16-byte chunk index with key & 7, the 64-byte one with (key >> 1) & 3
-    static __device__ __forceinline__ uint32_t off(int key, int dim) {
-        const int byte = dim * 2;
-        const int chunk = (byte % C::SWB) >> 4;
-        const int sw = C::SWB == 128 ? (key & 7) : ((key >> 1) & 3);
-        return (uint32_t)((byte / C::SWB) * (C::BT * C::SWB) + key * C::SWB + ((chunk ^ sw) << 4));
-    }
+    // byte offset of (key, dim) in the swizzled tile (tile_off)
+    __device__ __forceinline__ uint32_t off(int key, int dim) const { return tile_off<C>(key, dim >> 3, rb); }
 
     // tile_pos: absolute position of the tile's first key
     __device__ __forceinline__ void tile(uint8_t *stage, int nvalid, int tile_pos) {
@@ -142,9 +137,8 @@ struct MultiConsumer {
         if (nv < 16) {  // rows past the end may hold anything: zero their V so 0 * V stays 0
             for (int i = lane; i < (16 - nv) * C::NBLK * C::CPB; i += 32) {
                 const int row = key0 + nv + i / (C::NBLK * C::CPB);
-                const int rest = i % (C::NBLK * C::CPB);
-                *reinterpret_cast<uint4 *>(sV + (rest / C::CPB) * (C::BT * C::SWB) + row * C::SWB +
-                                           (rest % C::CPB) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(sV + tile_off<C>(row, i % (C::NBLK * C::CPB), rb)) =
+                    make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -471,7 +465,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MINB)
 
     // ---- consumer warps
     MultiConsumer<C> cs;
-    cs.init(warp, lane, smem);
+    cs.init(warp, lane, smem, 31 - __clz(C::GATHER ? BT : R));
     cs.reset();
     cs.load_q(p.q + (long long)(tl.q0 + tl.i0) * p.q_sb + (long long)kvh * G * p.q_sh, p.q_sb, p.q_sh, tl.ntok,
               tl.pos0, p.qscale);

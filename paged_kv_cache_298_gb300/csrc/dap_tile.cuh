@@ -68,23 +68,29 @@ struct ConsumerBarrier {
     }
 };
 
-// The K and V boxes of one producer lane: box j of the stage covers tile rows
-// [j*R, (j+1)*R).  Swizzled configurations split every row into 128-byte column blocks.
+// K / V tile layout: boxes of R = 2^rb rows (R = gcd(page size, BT) for TMA-fed paged
+// tiles, BT for the contiguous cache and the row gather), each box [NBLK column blocks][R
+// rows][SWB bytes], SWB-byte swizzled (the layout one 5-D TMA box over [SWB/2 dims, rows,
+// column block, kv head, page] produces).  Byte offset of 16-byte chunk `ch` (0 .. NBLK * CPB
+// - 1) of tile row `key`; the 128-byte swizzle XORs the chunk index within its block with
+// key & 7, the 64-byte one with (key >> 1) & 3 (every box segment starts on a swizzle atom).
+template <class C>
+__device__ __forceinline__ uint32_t tile_off(int key, int ch, int rb) {
+    const int blk = ch / C::CPB, cib = ch % C::CPB;
+    const int sw = C::SWB == 128 ? (key & 7) : ((key >> 1) & 3);
+    return (uint32_t)((((key >> rb) * C::NBLK + blk) << rb) * C::SWB + (key & ((1 << rb) - 1)) * C::SWB +
+                      ((cib ^ sw) << 4));
+}
+
+// The K and V boxes of one producer lane: box j of the stage covers tile rows [j*R,
+// (j+1)*R), every column block of them (one TMA copy per tensor).
 template <class C>
 __device__ __forceinline__ void issue_kv_box(uint8_t *stage, int j, int R, const CUtensorMap *mk,
                                              const CUtensorMap *mv, int kvh0, int row, int page, uint64_t *bar) {
-    if constexpr (C::SWZ) {
-#pragma unroll
-        for (int h = 0; h < C::NBLK; ++h) {
-            uint8_t *dst = stage + h * (C::BT * C::SWB) + j * R * C::SWB;
-            tma_load_4d(dst, mk, (C::SWB / 2) * h, kvh0, row, page, bar);
-            tma_load_4d(dst + C::TILE_BYTES, mv, (C::SWB / 2) * h, kvh0, row, page, bar);
-        }
-    } else {
-        uint8_t *dst = stage + j * R * C::HG * C::ROWB;
-        tma_load_4d(dst, mk, 0, kvh0, row, page, bar);
-        tma_load_4d(dst + C::TILE_BYTES, mv, 0, kvh0, row, page, bar);
-    }
+    static_assert(C::SWZ, "swizzled tiles");
+    uint8_t *dst = stage + j * R * C::ROWB;
+    tma_load_5d(dst, mk, 0, row, 0, kvh0, page, bar);
+    tma_load_5d(dst + C::TILE_BYTES, mv, 0, row, 0, kvh0, page, bar);
 }
 
 // ---- row gather: page sizes that are not multiples of 8 ---------------------------------
@@ -359,20 +365,21 @@ bool encode_bf16(CUtensorMap *map, const void *base, int rank, const cuuint64_t 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [D, Hkv, rows, outer] view of a cache.  Box [D, HG, box_rows, 1] unswizzled, or, for the
-// swizzled layout, [64, 1, box_rows, 1] with the 128-byte swizzle (one column block).
+// [rows, Hkv, D] cache (per page, or per sequence for the contiguous cache) viewed for the
+// swizzled tile layout (see tile_off).
 template <class C>
 bool encode_cache_map(CUtensorMap *map, const void *base, int D, int Hkv, long long rows, long long outer,
                       int box_rows) {
-    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows, (cuuint64_t)outer};
-    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)rows * Hkv * D * 2};
-    if constexpr (C::SWZ) {
-        const cuuint32_t box[4] = {(cuuint32_t)(C::SWB / 2), 1u, (cuuint32_t)box_rows, 1u};
-        return encode_bf16(map, base, 4, dims, strides, box,
-                           C::SWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-    }
-    const cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)C::HG, (cuuint32_t)box_rows, 1u};
-    return encode_bf16(map, base, 4, dims, strides, box);
+    static_assert(C::SWZ, "swizzled tiles");
+    // [SWB/2 dims, rows, column block, kv head, page]: one box = box_rows rows of every
+    // column block of one kv head, landing block-major
+    const cuuint64_t dims[5] = {(cuuint64_t)(C::SWB / 2), (cuuint64_t)rows, (cuuint64_t)(D * 2 / C::SWB),
+                                (cuuint64_t)Hkv, (cuuint64_t)outer};
+    const cuuint64_t strides[4] = {(cuuint64_t)Hkv * D * 2, (cuuint64_t)C::SWB, (cuuint64_t)D * 2,
+                                   (cuuint64_t)rows * Hkv * D * 2};
+    const cuuint32_t box[5] = {(cuuint32_t)(C::SWB / 2), (cuuint32_t)box_rows, (cuuint32_t)(D * 2 / C::SWB), 1u, 1u};
+    return encode_bf16(map, base, 5, dims, strides, box,
+                       C::SWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // [D, Hq, B] view of q with its strides, box [D, hpu, 1].
