@@ -78,6 +78,16 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point_and_the_oracle():
     assert binding.get_device_errors() == 0
 
 
+def test_page_size_that_is_not_a_multiple_of_8():
+    """Page size 12 (rows copied one by one into the tiles): the same bits as the workspace
+    entry point at the planner's split count, and the oracle."""
+    case = inputs.make_paged_case(5, 32, 8, 128, 12, [700, 33, 1024, 5, 260], 9007, device="cuda")
+    got, want = run_both(case, 0)
+    assert torch.equal(got, want)
+    assert_close(got, oracle_paged(case), "page 12 vs oracle")
+    assert binding.get_device_errors() == 0
+
+
 def test_head_dim_256_with_eight_heads_per_kv_head():
     """D = 256, G = 8: the planner's partials fit, the balanced schedule's (16 MiB of
     accumulators alone) do not and are refused."""
