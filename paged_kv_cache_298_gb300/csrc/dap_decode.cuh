@@ -176,10 +176,10 @@ struct MmaConsumer {
         // online softmax, base 2; keys g (c0, c1) and g + 8 (c2, c3)
         const bool v0 = g < nv, v1 = g + 8 < nv;
         float s[4];
-        s[0] = v0 ? c[0] * qscale : -INFINITY;
-        s[1] = v0 ? c[1] * qscale : -INFINITY;
-        s[2] = v1 ? c[2] * qscale : -INFINITY;
-        s[3] = v1 ? c[3] * qscale : -INFINITY;
+        s[0] = v0 ? __fmul_rn(c[0], qscale) : -INFINITY;  // (rounded once: the same value feeds max and exp)
+        s[1] = v0 ? __fmul_rn(c[1], qscale) : -INFINITY;
+        s[2] = v1 ? __fmul_rn(c[2], qscale) : -INFINITY;
+        s[3] = v1 ? __fmul_rn(c[3], qscale) : -INFINITY;
         float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {

@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c0 < n16) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    if (c0 + i < n) m = fmaxf(m, v[u][i] * p.qscale);
+                    if (c0 + i < n) m = fmaxf(m, __fmul_rn(v[u][i], p.qscale));
             }
         }
         xch[chalf * kHeads + hrow] = m;
@@ -471,8 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[4];
 #pragma unroll
                     for (int e = 0; e < 8; e += 2) {
-                        const float p0 = (j0 + e < n) ? ex2(v[u][8 * g + e] * p.qscale - m) : 0.f;
-                        const float p1 = (j0 + e + 1 < n) ? ex2(v[u][8 * g + e + 1] * p.qscale - m) : 0.f;
+                        const float p0 = (j0 + e < n) ? ex2(__fmul_rn(v[u][8 * g + e], p.qscale) - m) : 0.f;
+                        const float p1 = (j0 + e + 1 < n) ? ex2(__fmul_rn(v[u][8 * g + e + 1], p.qscale) - m) : 0.f;
                         const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
                         const float2 r2 = __bfloat1622float2(b);
                         lp += r2.x + r2.y;  // the sum of the weights PV actually uses

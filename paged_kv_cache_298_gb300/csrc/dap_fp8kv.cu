@@ -269,10 +269,10 @@ struct Consumer {
             }
             const float ks0 = kfac0 * qscale[h], ks1 = kfac1 * qscale[h];
             float s[4];
-            s[0] = v0 ? c[0] * ks0 : -INFINITY;
-            s[1] = v0 ? c[1] * ks0 : -INFINITY;
-            s[2] = v1 ? c[2] * ks1 : -INFINITY;
-            s[3] = v1 ? c[3] * ks1 : -INFINITY;
+            s[0] = v0 ? __fmul_rn(c[0], ks0) : -INFINITY;  // (rounded once: the same value feeds max and exp)
+            s[1] = v0 ? __fmul_rn(c[1], ks0) : -INFINITY;
+            s[2] = v1 ? __fmul_rn(c[2], ks1) : -INFINITY;
+            s[3] = v1 ? __fmul_rn(c[3], ks1) : -INFINITY;
             float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
             float vm = fmaxf(v0 ? vfac0 : 0.f, v1 ? vfac1 : 0.f);
 #pragma unroll

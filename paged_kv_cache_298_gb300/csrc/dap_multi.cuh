@@ -177,8 +177,8 @@ struct MultiConsumer {
                     keep0 = keep0 && mk[0] != 0;
                     keep1 = keep1 && mk[8] != 0;
                 }
-                s[j] = keep0 ? c[n][j] * qscale : -INFINITY;
-                s[j + 2] = keep1 ? c[n][j + 2] * qscale : -INFINITY;
+                s[j] = keep0 ? __fmul_rn(c[n][j], qscale) : -INFINITY;  // (rounded once: feeds max and exp)
+                s[j + 2] = keep1 ? __fmul_rn(c[n][j + 2], qscale) : -INFINITY;
             }
             float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
 #pragma unroll

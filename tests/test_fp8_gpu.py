@@ -83,19 +83,37 @@ def test_fp8_repeat_is_deterministic():
 
 def test_single_row_windows_return_the_dequantised_row_exactly():
     """With one participating row the softmax weight is exactly 1, so every head's output is
-    that row's dequantised value bf16(e4m3(code) * inv_scale) bit for bit.  The row holds all
-    256 codes twice (subnormals, zeros, both signs and the NaN codes), and the tokens use
-    inverse scales from 2^-100 to 3e30 (those of 2^8 or more take the kernel's fp32 path)."""
-    inv_values = [1.0, 0.5, 2.0, 1.75, 0.5390625, 255.0, 256.0, 1000.0, 2.0 ** -20, 3e30, 2.0 ** -100, 1.0 / 3.0]
+    that row's dequantised value bf16(e4m3(code) * inv_scale) bit for bit.  The row holds
+    every non-NaN code twice (subnormals, zeros, both signs, the largest magnitudes), and
+    the tokens use inverse scales from 2^-100 to 3e30 (scores near 1e34: the kernel rounds
+    each score once, so the largest one minus the maximum is exactly 0)."""
+    inv_values = [1.0, 0.5, 2.0, 1.75, 0.5390625, 255.0, 256.0, 1000.0, 2.0 ** -20, 3e30, 2.0 ** -100, 1.0 / 3.0,
+                  2.0 ** 60]
     T = len(inv_values)
     case = inputs.make_fp8_case(T, 128, 512, 1, 16, 4, 7400, lens=[1] * T)
-    codes = torch.arange(512, dtype=torch.int64) % 256
-    case.kv_cache[0, :T] = codes.to(torch.uint8)[None, :]
+    finite = torch.tensor([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=torch.uint8)
+    row = torch.cat([finite, finite, torch.zeros(512 - 2 * finite.numel(), dtype=torch.uint8)])
+    case.kv_cache[0, :T] = row[None, :]
     case.inv_scale[:T, 0] = torch.tensor(inv_values, dtype=torch.float32).to(torch.bfloat16)
     case.indices[:] = -1
     case.indices[:, 0] = torch.arange(T)
     got = run(case).float().cpu().double().numpy()
     want = ref(case)
-    nan = np.isnan(want)
-    assert nan.any() and np.array_equal(np.isnan(got), nan)
-    assert np.array_equal(got[~nan], want[~nan])
+    assert np.isfinite(want).all()
+    assert np.array_equal(got, want)
+    # the output of every head is the same dequantised row
+    assert np.array_equal(want[:, :1, :].repeat(128, axis=1), want)
+
+
+def test_a_nan_code_in_a_row_makes_the_token_nan_like_the_fallback():
+    """A NaN code (0x7F) in a participating row turns its scores into NaN; the fallback's
+    softmax then gives NaN for every head of the token, and so does the kernel."""
+    case = inputs.make_fp8_case(2, 128, 512, 1, 16, 4, 7401, lens=[2, 2])
+    case.indices[:] = -1
+    case.indices[0, :2] = torch.tensor([0, 1])
+    case.indices[1, :2] = torch.tensor([2, 3])
+    case.kv_cache[0, 1, 100] = 0x7F
+    got = run(case).float().cpu().numpy()
+    want = ref(case)
+    assert np.isnan(want[0]).all() and np.isnan(got[0]).all()
+    assert_close(torch.from_numpy(got[1:]), want[1:], "token without NaN codes")
