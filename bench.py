@@ -769,6 +769,7 @@ def compact(leg: Leg, r, hbm_peak, cpu):
            "us_per_call": round(r["call_ms"] * 1e3, 2), "gb_s": gbs(r["call_ms"]),
            "frac": round(leg.nbytes / (r["call_ms"] * 1e-3) / 1e9 / hbm_peak, 4),
            "graph_us_per_call": round(r["graph_ms"] * 1e3, 2), "graph_gb_s": gbs(r["graph_ms"]),
+           "graph_frac": round(leg.nbytes / (r["graph_ms"] * 1e-3) / 1e9 / hbm_peak, 4),
            "kernel": {"name": leg.kernel, "us": round(r["kern_ms"] * 1e3, 2), "gb_s": gbs(r["kern_ms"]),
                       "frac": round(leg.nbytes / (r["kern_ms"] * 1e-3) / 1e9 / hbm_peak, 4),
                       "timing": r["kernel_timing"],
@@ -812,6 +813,7 @@ def run_ours(args):
         "metric": leg.metric, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms, 5), "us_per_call": round(r["call_ms"] * 1e3, 2),
         "graph_us_per_call": round(r["graph_ms"] * 1e3, 2),
+        "graph_frac": round(leg.nbytes / (r["graph_ms"] * 1e-3) / 1e9 / hbm_peak, 4),
         "statistic": "value and ms_per_step: the K-step region bracketed by two CUDA events; us_per_call: median "
                      "of K per-call times (events at every call boundary, host binding included); "
                      "graph_us_per_call: the same calls replayed from a CUDA graph (device time per call)",
