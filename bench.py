@@ -130,8 +130,10 @@ KERNEL_SOURCES = {"split_kernel": ("dap_decode.cu", "dap_decode.cuh", "dap_tile.
                                     "dap_internal.h"),
                   "multi_kernel": ("dap_multi.cu", "dap_multi.cuh", "dap_tile.cuh", "dap_device.cuh",
                                    "dap_internal.h"),
+                  "multi_tc_kernel": ("dap_multi_tc.cu", "dap_multi.cuh", "dap_tile.cuh", "dap_device.cuh",
+                                      "dap_tc.cuh", "dap_internal.h"),
                   "fp8kv_kernel": ("dap_fp8kv.cu", "dap_tile.cuh", "dap_device.cuh", "dap_internal.h"),
-                  "swa_kernel": ("dap_fp8.cu", "dap_device.cuh", "dap_internal.h")}
+                  "swa_kernel": ("dap_fp8.cu", "dap_device.cuh", "dap_tc.cuh", "dap_internal.h")}
 
 
 def kernel_source_sha(kernel: str) -> str:
@@ -500,7 +502,9 @@ def prepare_leg(key, case, dev, l2, splits=None, tpt=None) -> Leg:
 
     if key.startswith("multi"):
         kv = case.kv
-        mplan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, dev, tokens_per_tile=tpt)
+        mplan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, dev, tokens_per_tile=tpt, D=kv.D)
+        # 128 query rows per tile: the tcgen05 consumer; 16 or 32 columns: the mma.sync one
+        mkernel = "multi_tc_kernel" if mplan.tokens_per_tile * (kv.Hq // kv.Hkv) == 128 else "multi_kernel"
         S = plan(mplan.num_tiles, kv.Hq, kv.Hkv, kv.D, kv.page_size, kv.max_kv_len, kv.total_kv)
         run = binding.resolve_splits(S, sms, mplan.num_tiles, kv.Hq, kv.Hkv, kv.D, kv.page_size, kv.max_kv_len)
         parts = (case.q, kv.k_cache, kv.v_cache, kv.block_table, kv.seq_lens)
@@ -543,7 +547,7 @@ def prepare_leg(key, case, dev, l2, splits=None, tpt=None) -> Leg:
                "kv_dtype": "bf16",
                "cold_kv": f"{n} rotated input copies of {footprint / 1e9:.2f} GB each (> 2x L2)"}
         return Leg(key, "multi-token paged decode achieved HBM GB/s (algorithmic bytes), cold KV", cfg,
-                   multi_algorithmic(case), "multi_kernel", call, (h2d, call, d2h),
+                   multi_algorithmic(case), mkernel, call, (h2d, call, d2h),
                    sum(h.numel() * h.element_size() for h in host + hmap), ho.numel() * 2, 2 if run != 1 else 1, n,
                    extra={"flops": flops})
 

@@ -257,9 +257,12 @@ dap_status kv_append_paged_fp8(const void *k_new, const void *v_new, uint8_t *k_
  * covers tokens [tile_index[w] * tokens_per_tile, ...) of sequence tile_batch[w].  A tile's
  * tokens x the G heads of a kv head are its query columns, and every tile streams its
  * sequence's keys once, so the fewer tiles a sequence has, the fewer times its K/V are
- * read.  Two tile sizes: 16 / G tokens (16 columns) or 32 / G tokens (32 columns; not with a
- * mask).  dap_multi_tokens_per_tile(Hq, Hkv, max_q_len) picks the smaller when the longest
- * new-token count fits it, else the larger (G = 8: 2 tokens up to q_len 2, then 4).
+ * read.  Three tile sizes: 16 / G tokens (16 columns), 32 / G tokens (32 columns; not with a
+ * mask) and, for D 64 and 128 without a mask, 128 / G tokens (128 query rows of tensor-
+ * memory products: up to 16 tokens at G = 8 against one K/V stream).
+ * dap_multi_tokens_per_tile(Hq, Hkv, D, max_q_len) picks 16 / G when the longest new-token
+ * count fits it, else 128 / G where D allows (D = 0: head dim not known, no 128-row tiles),
+ * else 32 / G (G = 8, D = 128: 2 tokens up to q_len 2, then 16).
  * dap_q_tile_map builds the map on the host:
  *   q_lens      host int32 [B], each >= 0.
  *   qo_indptr   host int32 [B + 1] (written).
@@ -267,7 +270,7 @@ dap_status kv_append_paged_fp8(const void *k_new, const void *v_new, uint8_t *k_
  * Returns the number of tiles, or -1 when max_tiles is too small or an input is invalid.
  * Pure host functions; no CUDA call.
  */
-int dap_multi_tokens_per_tile(int Hq, int Hkv, int max_q_len);
+int dap_multi_tokens_per_tile(int Hq, int Hkv, int D, int max_q_len);
 int dap_q_tile_map(const int32_t *q_lens, int B, int tokens_per_tile, int32_t *qo_indptr,
                    int32_t *tile_batch, int32_t *tile_index, int max_tiles);
 

@@ -101,7 +101,7 @@ def load(build_if_missing: bool = True):
         lib.kv_append_paged.restype = I
         lib.kv_append_fp8.argtypes = [P, P, P, P, I, I, I, I, P]
         lib.kv_append_fp8.restype = I
-        lib.dap_multi_tokens_per_tile.argtypes = [I, I, I]
+        lib.dap_multi_tokens_per_tile.argtypes = [I, I, I, I]
         lib.dap_multi_tokens_per_tile.restype = I
         lib.dap_q_tile_map.argtypes = [P, I, I, P, P, P, I]
         lib.dap_q_tile_map.restype = I
@@ -482,9 +482,10 @@ def decode_attn_paged_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, 
 
 # ---- multi-token decode ------------------------------------------------------------------
 
-def multi_tokens_per_tile(Hq: int, Hkv: int, max_q_len: int = 0) -> int:
-    """include/dap.h: dap_multi_tokens_per_tile (16 / G, or 32 / G for longer new-token runs)."""
-    return load().dap_multi_tokens_per_tile(int(Hq), int(Hkv), int(max_q_len))
+def multi_tokens_per_tile(Hq: int, Hkv: int, max_q_len: int = 0, D: int = 0) -> int:
+    """include/dap.h: dap_multi_tokens_per_tile (16 / G; for longer new-token runs 128 / G
+    where the head dim D has the 128-row tiles, else 32 / G; D = 0: not known)."""
+    return load().dap_multi_tokens_per_tile(int(Hq), int(Hkv), int(D), int(max_q_len))
 
 
 def workspace_bytes_multi(total_q, Hq, D, num_splits) -> int:
@@ -507,12 +508,15 @@ def q_tile_map(q_lens, tokens_per_tile: int):
 
 class MultiPlan:
     """The work map of one batch of new-token counts, copied to the device once so that
-    repeated decode calls on the same counts pass it straight to the library."""
+    repeated decode calls on the same counts pass it straight to the library.  Without
+    tokens_per_tile the library's rule picks it from the longest count and the head dim D
+    (None: not known, so no 128-row tiles)."""
 
-    def __init__(self, q_lens, Hq: int, Hkv: int, device, tokens_per_tile: int | None = None):
+    def __init__(self, q_lens, Hq: int, Hkv: int, device, tokens_per_tile: int | None = None,
+                 D: int | None = None):
         ql = [int(x) for x in torch.as_tensor(q_lens).reshape(-1).tolist()]
         if tokens_per_tile is None:
-            tokens_per_tile = multi_tokens_per_tile(Hq, Hkv, max(ql, default=0))
+            tokens_per_tile = multi_tokens_per_tile(Hq, Hkv, max(ql, default=0), D or 0)
         self.tokens_per_tile = int(tokens_per_tile)
         _need(self.tokens_per_tile > 0, "Hq must be a multiple of Hkv with G <= 16")
         qi, tb, ti = q_tile_map(q_lens, self.tokens_per_tile)

@@ -275,9 +275,9 @@ dap_status decode_attn_contig(const void *q, long long q_stride_b, long long q_s
     return launch_decode(a, static_cast<cudaStream_t>(stream));
 }
 
-int dap_multi_tokens_per_tile(int Hq, int Hkv, int max_q_len) {
-    if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return 0;
-    return multi_tokens_per_tile(Hq / Hkv, max_q_len);
+int dap_multi_tokens_per_tile(int Hq, int Hkv, int D, int max_q_len) {
+    if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 0) return 0;
+    return multi_tokens_per_tile(Hq / Hkv, D, max_q_len);
 }
 
 int dap_q_tile_map(const int32_t *q_lens, int B, int tokens_per_tile, int32_t *qo_indptr, int32_t *tile_batch,
@@ -337,8 +337,10 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
         return DAP_ERR_ALIGN;
     {
         const int G = Hq / Hkv;
-        if (tokens_per_tile * G != 16 && tokens_per_tile * G != 32) return DAP_ERR_SHAPE;
-        if (mask && tokens_per_tile * G != 16) return DAP_ERR_UNSUPPORTED;
+        const int cols = tokens_per_tile * G;
+        if (cols != 16 && cols != 32 && cols != 128) return DAP_ERR_SHAPE;
+        if (mask && cols != 16) return DAP_ERR_UNSUPPORTED;
+        if (cols == 128 && D != 64 && D != 128) return DAP_ERR_UNSUPPORTED;
     }
     if ((st = check_mask(mask, mask_stride, max_kv_len)) != DAP_OK) return st;
     int S = 0, chunk = 0;
@@ -578,6 +580,7 @@ dap_status dap_get_device_errors(unsigned int *flags, int clear) {
     if (!read_errors_append(flags, clear != 0)) return DAP_ERR_CUDA;
     if (!read_errors_multi(flags, clear != 0)) return DAP_ERR_CUDA;
     if (!read_errors_multi_gather(flags, clear != 0)) return DAP_ERR_CUDA;
+    if (!read_errors_multi_tc(flags, clear != 0)) return DAP_ERR_CUDA;
     if (!read_errors_fp8kv(flags, clear != 0)) return DAP_ERR_CUDA;
     return DAP_OK;
 }

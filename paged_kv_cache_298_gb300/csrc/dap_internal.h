@@ -74,11 +74,12 @@ dap_status launch_decode(const DecodeArgs &a, cudaStream_t stream);
 // paged cache with a page size that is not a multiple of 8 (row-gather producer)
 dap_status launch_decode_gather(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_multi_gather(const DecodeArgs &a, cudaStream_t stream);
+dap_status launch_decode_multi_tc(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_masked_gather(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_multi(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_masked(const DecodeArgs &a, cudaStream_t stream);
 dap_status launch_decode_fp8kv(const DecodeArgs &a, cudaStream_t stream);
-int multi_tokens_per_tile(int G, int max_q_len);
+int multi_tokens_per_tile(int G, int D, int max_q_len);
 
 // Events of dap_set_trace_events (nullptr when tracing is off).
 struct TraceEvents {
@@ -110,6 +111,7 @@ dap_status launch_append_paged_fp8(const void *k_new, const void *v_new, uint8_t
                                    int D, cudaStream_t stream);
 bool read_errors_multi(unsigned int *flags, bool clear);
 bool read_errors_multi_gather(unsigned int *flags, bool clear);
+bool read_errors_multi_tc(unsigned int *flags, bool clear);
 bool read_errors_fp8kv(unsigned int *flags, bool clear);
 bool read_errors_append(unsigned int *flags, bool clear);
 

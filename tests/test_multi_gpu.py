@@ -41,7 +41,7 @@ def oracle_multi(case: inputs.MultiCase):
 def gpu_multi(case: inputs.MultiCase, S=0, plan=None, **kw):
     kv = case.kv
     if plan is None:
-        plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, case.q.device)
+        plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, case.q.device, D=kv.D)
     return binding.decode_attn_paged_multi(case.q, kv.k_cache, kv.v_cache, kv.block_table, kv.seq_lens, plan,
                                            max_kv_len=kv.max_kv_len, scale=kv.scale, num_splits=S, **kw)
 
@@ -52,17 +52,18 @@ def _clean_errors():
     yield
 
 
-def tile_sizes(Hq, Hkv):
-    """Both tile sizes of the work map: 16 and 32 query columns."""
+def tile_sizes(Hq, Hkv, D=None):
+    """Every tile size of the work map: 16 and 32 query columns, and 128 query rows of the
+    tensor-memory tiles where the head dim has them (64 and 128)."""
     G = Hq // Hkv
-    return [16 // G, 32 // G]
+    return [16 // G, 32 // G] + ([128 // G] if D in (64, 128) else [])
 
 
 def test_small_case_several_tiles_and_split_counts():
     # G = 4: 4 (or 8) tokens per q tile; 9 new tokens -> three (two) tiles, the last ragged
     case = inputs.make_multi_case(3, 8, 2, 64, 16, [100, 37, 300], [5, 1, 9], 4001).to("cuda")
     ref = oracle_multi(case)
-    for tpt in tile_sizes(8, 2):
+    for tpt in tile_sizes(8, 2, 64):
         plan = binding.MultiPlan(case.q_lens, 8, 2, "cuda", tokens_per_tile=tpt)
         for S in [0, 1, 2, 3, 5]:
             assert_close(gpu_multi(case, S, plan=plan), ref, f"tpt={tpt} S={S}")
@@ -86,6 +87,11 @@ SHAPES = [
     (2, 16, 4, 256, 3, [300, 64], [9, 5]),                       # D=256, page 3
     (2, 32, 4, 32, 1, [200, 65], [11, 5]),                       # D=32, page 1
     (3, 16, 8, 64, 100, [650, 9, 301], [8, 9, 2]),               # D=64, page 100
+    # the tensor-memory tiles' other K/V layouts: 8-row boxes, 32-row boxes, more than one
+    # 128-row tile per sequence
+    (2, 32, 8, 128, 8, [300, 77], [6, 40]),                      # G=4, page 8
+    (3, 64, 8, 128, 32, [500, 90, 2100], [16, 9, 17]),           # G=8, page 32
+    (2, 8, 8, 64, 16, [400, 150], [130, 3]),                     # G=1, D=64
 ]
 
 
@@ -93,7 +99,7 @@ SHAPES = [
 def test_parity_across_groups_and_dims(B, Hq, Hkv, D, ps, lens, qlens):
     case = inputs.make_multi_case(B, Hq, Hkv, D, ps, lens, qlens, 4100 + Hq + D).to("cuda")
     ref = oracle_multi(case)
-    for tpt in tile_sizes(Hq, Hkv):
+    for tpt in tile_sizes(Hq, Hkv, D):
         plan = binding.MultiPlan(case.q_lens, Hq, Hkv, "cuda", tokens_per_tile=tpt)
         for S in [0, 1, 4]:
             assert_close(gpu_multi(case, S, plan=plan), ref, f"G={Hq // Hkv} D={D} tpt={tpt} S={S}")
@@ -156,9 +162,10 @@ def test_full_size_speculative_verification():
 
 @pytest.mark.parametrize("q_len", [4, 8])
 def test_full_size_eight_heads_per_kv_head(q_len):
-    """The ragged B=128 batch at Hq=64, Hkv=8 (G = 8) with 4 or 8 new tokens per sequence:
-    32-column tiles put all of a sequence's tokens (or half of them, at 8) against one K/V
-    stream; every output element against the oracle, at the planner's split count."""
+    """The ragged B=128 batch at Hq=64, Hkv=8 (G = 8) with 4 or 8 new tokens per sequence in
+    32-column tiles (the head-dim-agnostic rule's choice): all of a sequence's tokens (or
+    half of them, at 8) against one K/V stream; every output element against the oracle,
+    at the planner's split count."""
     case = inputs.spec_verify_paged(device="cuda", q_len=q_len, Hq=64)
     plan = binding.MultiPlan(case.q_lens, 64, 8, "cuda")
     assert plan.tokens_per_tile == 4 and plan.num_tiles == 128 * (q_len // 4)
@@ -167,16 +174,42 @@ def test_full_size_eight_heads_per_kv_head(q_len):
     assert binding.get_device_errors() == 0
 
 
+@pytest.mark.parametrize("q_len", [4, 8, 16])
+def test_full_size_eight_heads_tensor_memory_tiles(q_len):
+    """The same G = 8 batch in 128-row tiles (16 tokens x 8 heads): one tile, and so one
+    K/V stream, per sequence and kv head at every q_len up to 16; every output element
+    against the oracle at the planner's split count and at one split."""
+    case = inputs.spec_verify_paged(device="cuda", q_len=q_len, Hq=64)
+    plan = binding.MultiPlan(case.q_lens, 64, 8, "cuda", D=128)
+    assert plan.tokens_per_tile == 16 and plan.num_tiles == 128
+    ref = oracle_multi(case)
+    assert_close(gpu_multi(case, 0, plan=plan, total_kv=case.kv.total_kv), ref, f"G=8 q_len={q_len} 128 rows")
+    assert_close(gpu_multi(case, 1, plan=plan), ref, f"G=8 q_len={q_len} 128 rows, one split")
+    assert binding.get_device_errors() == 0
+
+
+def test_tensor_memory_tiles_repeat_bit_identically():
+    case = inputs.make_multi_case(4, 64, 8, 128, 16, [500, 800, 90, 1500], [5, 16, 1, 9], 4650).to("cuda")
+    plan = binding.MultiPlan(case.q_lens, 64, 8, "cuda", tokens_per_tile=16)
+    a = gpu_multi(case, 3, plan=plan)
+    b = gpu_multi(case, 3, plan=plan)
+    assert torch.equal(a, b)
+    assert_close(a, oracle_multi(case), "repeat")
+
+
 def test_more_new_tokens_than_keys_gives_zero_rows_and_a_flag():
     # sequence 1 claims 6 new tokens but holds only 4 keys: its first two tokens would sit
     # before the cache start, attend nothing and come out zero (as in the oracle)
     case = inputs.make_multi_case(2, 8, 2, 64, 16, [50, 4], [3, 6], 4400).to("cuda")
-    out = gpu_multi(case, 1)
-    torch.cuda.synchronize()
-    assert binding.get_device_errors() & binding.DEVERR_SEQLEN
     ref = oracle_multi(case)
-    assert_close(out, ref, "q_len > L")
-    assert (out[3:5].float() == 0).all()
+    for tpt in tile_sizes(8, 2, 64):
+        binding.get_device_errors(clear=True)
+        plan = binding.MultiPlan(case.q_lens, 8, 2, "cuda", tokens_per_tile=tpt)
+        out = gpu_multi(case, 1, plan=plan)
+        torch.cuda.synchronize()
+        assert binding.get_device_errors() & binding.DEVERR_SEQLEN
+        assert_close(out, ref, f"q_len > L, tpt={tpt}")
+        assert (out[3:5].float() == 0).all()
 
 
 def test_bad_work_map_entry_is_skipped_and_flagged():
