@@ -12,12 +12,12 @@
 //                                 (bf16 pairs) overwrites the first 16 columns of its half
 //                                 once they are read;
 //   O  columns [128, 128 + D)    fp32 output accumulator.
-// Warps: four consumers (rows), a producer (K/V tiles) and an MMA warp whose one thread
+// Warps: four consumers (rows), a producer (K/V tiles) and two MMA warps: one thread
 // issues, per half tile, S = Q . K^T (A = q from tensor memory, B = the K tile K-major from
-// shared memory) and, once the consumers have turned the row of scores into P, O += P . V
-// (A = P from tensor memory, B = the V tile MN-major); the commit of a tile's last product
-// frees its stage.  The scores of the next half tile are computed while the consumers work
-// on the current one.  Consumer thread r masks its row causally (key position <= the
+// shared memory), another, once the consumers have turned the row of scores into P,
+// O += P . V (A = P from tensor memory, B = the V tile MN-major); the commit of a tile's
+// last product frees its stage.  The scores of the next half tile are computed while the
+// consumers work on the current one.  Consumer thread r masks its row causally (key position <= the
 // token's position) and takes the base-2 online softmax; the running max is moved lazily:
 // O and l are rescaled only when a half tile's max exceeds the reference by more than 2^8
 // (the weights stay <= 256, far inside fp32), and the reference is stored with the
@@ -43,13 +43,14 @@ struct TcCfg {
     static constexpr int TILE_BYTES = BT * ROWB, STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int NS = 98304 / STAGE_BYTES;  // 96 KB of stages: two CTAs per SM
     static constexpr int ROWS = 128, QT = ROWS / G;  // query rows = TMEM lanes; tokens per tile
-    static constexpr int NWC = 4, PRODUCER = 4, ISSUER = 5, THREADS = 6 * 32;
+    // warps: 4 consumers, the producer, the S issuer, the PV issuer
+    static constexpr int NWC = 4, PRODUCER = 4, S_ISSUER = 5, PV_ISSUER = 6, THREADS = 7 * 32;
     // tensor-memory columns: q, the two half-tile score buffers (P over their first 16
     // columns), O
     static constexpr int TQ = 0, TS0 = 64, TS1 = 96, TO = 128, TMEM_COLS = 256;
-    // barriers: full[NS], empty[NS], s_done[2], p_ready[2], o_done, q_ready, fin
+    // barriers: full[NS], empty[NS], s_done[2], p_ready[2], pv_done[2], q_ready, fin[2]
     static constexpr int BAR_OFF = NS * STAGE_BYTES;
-    static constexpr int NBAR = 2 * NS + 7;
+    static constexpr int NBAR = 2 * NS + 9;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SMEM = MISC_OFF + 32 + 1024;  // + slack to align the base to 1024
     static_assert((D == 64 || D == 128) && ROWS % G == 0 && NS >= 2, "tcgen05 multi-token tiling");
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(C::THREADS, 2)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
     uint64_t *empty = full + NS;
     uint64_t *s_done = empty + NS, *p_ready = s_done + 2;
-    uint64_t *o_done = p_ready + 2, *q_ready = o_done + 1, *fin = o_done + 2;
+    uint64_t *pv_done = p_ready + 2, *q_ready = pv_done + 2, *fin = q_ready + 1;
     int *misc = reinterpret_cast<int *>(smem + C::MISC_OFF);  // [0] tiles issued, [1] abort, [2] tiles landed
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc + 4);
 
@@ -116,9 +117,11 @@ __global__ void __launch_bounds__(C::THREADS, 2)
             mbar_init(&s_done[b], 1);
             mbar_init(&p_ready[b], (uint32_t)max(active, 1));  // one arrival per active warp
         }
-        mbar_init(o_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&pv_done[b], 1);
+            mbar_init(&fin[b], 1);
+        }
         mbar_init(q_ready, NWC);
-        mbar_init(fin, 1);
         misc[0] = misc[1] = misc[2] = 0;
         fence_barrier_init();
     }
@@ -198,17 +201,25 @@ __global__ void __launch_bounds__(C::THREADS, 2)
             }
             if (lane == 0) misc[0] = issued;
         }
-    } else if (work && warp == C::ISSUER) {
-        // ---- the MMA thread.  Half tile j (keys [32 (j & 1), +32) of tile j / 2) has its
-        // scores in buffer j & 1; S(j + 2) reuses the buffer PV(j) reads P from, so it is
-        // issued once PV(j) has completed, while the consumers work on half tile j + 1.
+    } else if (work && warp == C::S_ISSUER) {
+        // ---- the S thread.  Half tile j (keys [32 (j & 1), +32) of tile j / 2) has its
+        // scores in buffer j & 1; S(j) reuses the buffer PV(j - 2) reads P from, so it is
+        // issued once that product has completed.  (One warp issues about one tcgen05.mma
+        // per hundred cycles whatever N is, so the S and PV products have a warp each.)
         if (lane == 0) {
             bool ok = mbar_wait(q_ready, 0);
             int landed = 0;
-            auto issue_s = [&](int j) -> bool {
+            for (int j = 0; ok && j < J; ++j) {
                 const int i = j >> 1, h = j & 1, st = i % NS;
+                if (j >= 2 && !mbar_wait(&pv_done[h], ((j >> 1) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
                 if (h == 0) {
-                    if (!mbar_wait(&full[st], (i / NS) & 1)) return false;
+                    if (!mbar_wait(&full[st], (i / NS) & 1)) {
+                        ok = false;
+                        break;
+                    }
                     landed = i + 1;
                 }
                 tc_fence_after();
@@ -219,11 +230,18 @@ __global__ void __launch_bounds__(C::THREADS, 2)
                     umma_bf16_tmem_a(tS, tQ + k16 * 8, sw128_desc(sK + (k16 >> 2) * CS + (k16 & 3) * 32, 16, 1024),
                                      idS, k16 > 0);
                 umma_commit(&s_done[h]);
-                return true;
-            };
-            if (ok && J > 0) ok = issue_s(0);
-            if (ok && J > 1) ok = issue_s(1);
-            for (int j = 0; ok && j < J; ++j) {
+            }
+            if (!ok) misc[1] = 1;
+            misc[2] = landed;
+            umma_commit(&fin[0]);  // this thread's products have completed when fin[0] completes
+        }
+        __syncwarp();
+    } else if (work && warp == C::PV_ISSUER) {
+        // ---- the PV thread: O += P(j) . V once the consumers have written P(j); the commit
+        // after a tile's second half frees its stage (its S products completed before P)
+        if (lane == 0) {
+            bool ok = true;
+            for (int j = 0; j < J; ++j) {
                 const int i = j >> 1, h = j & 1, st = i % NS;
                 if (!mbar_wait(&p_ready[h], (j >> 1) & 1)) {
                     ok = false;
@@ -236,18 +254,10 @@ __global__ void __launch_bounds__(C::THREADS, 2)
                 for (int kk = 0; kk * 16 < nv; ++kk)
                     umma_bf16_tmem_a(tO, tP + kk * 8, sw128_desc(sV + kk * 2048, CS, 1024), idO, j > 0 || kk > 0);
                 if (h == 1) umma_commit(&empty[st]);
-                umma_commit(o_done);
-                if (j + 2 < J) {
-                    if (!mbar_wait(o_done, j & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    ok = issue_s(j + 2);
-                }
+                umma_commit(&pv_done[h]);
             }
             if (!ok) misc[1] = 1;
-            misc[2] = landed;
-            umma_commit(fin);  // every product issued above has completed when fin completes
+            umma_commit(&fin[1]);
         }
         __syncwarp();
     }
@@ -333,8 +343,9 @@ __global__ void __launch_bounds__(C::THREADS, 2)
                     }
                 }
                 if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
-                    // O holds PV(j - 1) once that product completes (o_done phase j - 1)
-                    const bool g = __all_sync(0xFFFFFFFFu, mbar_wait(o_done, (j - 1) & 1));
+                    // O holds PV(j - 1) once that product completes
+                    const bool g =
+                        __all_sync(0xFFFFFFFFu, mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1));
                     tc_fence_after();
                     if (!g) {
                         misc[1] = 1;
@@ -386,8 +397,9 @@ __global__ void __launch_bounds__(C::THREADS, 2)
     }
     __syncthreads();
     if (warp < NWC && work) {
-        // every product has completed once fin does (the MMA thread commits it last)
-        const bool g = __all_sync(0xFFFFFFFFu, mbar_wait(fin, 0));
+        // every product has completed once both fin barriers have (each issuing thread
+        // commits its own last)
+        const bool g = __all_sync(0xFFFFFFFFu, mbar_wait(&fin[0], 0) && mbar_wait(&fin[1], 0));
         tc_fence_after();
         if (g && misc[1] == 0 && __any_sync(0xFFFFFFFFu, rvalid)) {  // (tcgen05.ld is warp-wide)
             const long long rq = tl.q0 + tl.i0 + ti;
@@ -424,7 +436,7 @@ __global__ void __launch_bounds__(C::THREADS, 2)
         }
         if (threadIdx.x == 0 && misc[1]) {
             // A wait gave up: let the copies still in flight land (bounded) before the shared
-            // memory is released (the products have, with fin).
+            // memory is released (the products have, with the fin barriers).
             for (int i = misc[2]; i < misc[0]; ++i) (void)mbar_wait(&full[i % NS], (i / NS) & 1);
         }
     }
