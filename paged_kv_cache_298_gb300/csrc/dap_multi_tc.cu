@@ -35,14 +35,18 @@ namespace dap {
 
 namespace {
 
-template <int D_, int G_, bool GATHER_>
+template <int D_, int G_, bool MASK_, bool GATHER_>
 struct TcCfg {
-    static constexpr bool GATHER = GATHER_, SWZ = true;
+    static constexpr bool GATHER = GATHER_, MASK = MASK_, SWZ = true;
     static constexpr int D = D_, G = G_, BT = 64, HT = 32;  // keys per K/V tile, per half tile
     static constexpr int ROWB = D * 2, SWB = 128, NBLK = ROWB / SWB, CPB = SWB / 16;
-    static constexpr int TILE_BYTES = BT * ROWB, STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int NS = 98304 / STAGE_BYTES;  // 96 KB of stages: two CTAs per SM
     static constexpr int ROWS = 128, QT = ROWS / G;  // query rows = TMEM lanes; tokens per tile
+    static constexpr int TILE_BYTES = BT * ROWB;
+    // a stage: the K and V tiles, then (with a mask) the tile's mask bytes [QT tokens][BT keys]
+    static constexpr int MASK_OFF = 2 * TILE_BYTES, MASK_BYTES = MASK ? QT * BT : 0;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES + (MASK_BYTES + 1023) / 1024 * 1024;
+    // 96 KB of stages (up to 108 KB with masks): two CTAs per SM
+    static constexpr int NS = (MASK ? 110592 : 98304) / STAGE_BYTES;
     // warps: 4 consumers, the producer, the S issuer, the PV issuer
     static constexpr int NWC = 4, PRODUCER = 4, S_ISSUER = 5, PV_ISSUER = 6, THREADS = 7 * 32;
     // tensor-memory columns: q, the two half-tile score buffers (P over their first 16
@@ -53,14 +57,14 @@ struct TcCfg {
     static constexpr int NBAR = 2 * NS + 9;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SMEM = MISC_OFF + 32 + 1024;  // + slack to align the base to 1024
-    static_assert((D == 64 || D == 128) && ROWS % G == 0 && NS >= 2, "tcgen05 multi-token tiling");
+    static_assert((D == 64 || D == 128) && ROWS % G == 0 && NS >= 2 && SMEM <= 113 * 1024, "tcgen05 multi-token tiling");
     static_assert(TQ + D / 2 <= TS0 && TS1 + HT <= TO && TO + D <= TMEM_COLS, "tensor-memory columns");
 };
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 2)
     multi_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
-                    const SplitParams p) {
+                    const __grid_constant__ CUtensorMap mapM, const SplitParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = aligned_smem<C>(smem_raw);
     constexpr int G = C::G, NWC = C::NWC, BT = C::BT, HT = C::HT, NS = C::NS, D = C::D;
@@ -138,6 +142,7 @@ __global__ void __launch_bounds__(C::THREADS, 2)
 
     if (work && warp == C::PRODUCER) {
         if (C::GATHER) {  // ---- producer warp, row gather
+            if (C::MASK && lane == 0) prefetch_tensormap(&mapM);
             const int32_t *table = p.block_table + (long long)tl.b * p.max_pages;
             RowPages<C> rp_next;
             if (ntiles > 0) lookup_rows<C>(rp_next, table, tok0, min(BT, tok1 - tok0), p.page_size, lane);
@@ -152,8 +157,14 @@ __global__ void __launch_bounds__(C::THREADS, 2)
                     misc[1] = 1;
                     break;
                 }
-                fill_tile_rows<C>(smem + st * C::STAGE_BYTES, rp, min(BT, tok1 - t), kvh, p, 0u, [] {}, &full[st],
-                                  lane);
+                // (with a mask: the tile's mask bytes by TMA, zeros past either end)
+                fill_tile_rows<C>(smem + st * C::STAGE_BYTES, rp, min(BT, tok1 - t), kvh, p, (uint32_t)C::MASK_BYTES,
+                                  [&] {
+                                      if (C::MASK)
+                                          tma_load_3d(smem + st * C::STAGE_BYTES + C::MASK_OFF, &mapM, t,
+                                                      tl.q0 + tl.i0, 0, &full[st]);
+                                  },
+                                  &full[st], lane);
                 issued = i + 1;
             }
             if (lane == 0) misc[0] = issued;
@@ -161,6 +172,7 @@ __global__ void __launch_bounds__(C::THREADS, 2)
             if (lane == 0) {
                 prefetch_tensormap(&mapK);
                 prefetch_tensormap(&mapV);
+                if (C::MASK) prefetch_tensormap(&mapM);
             }
             const int32_t *table = p.block_table + (long long)tl.b * p.max_pages;
             auto lookup = [&](int tile) -> int {
@@ -185,7 +197,7 @@ __global__ void __launch_bounds__(C::THREADS, 2)
                 }
                 const int t = tok0 + i * BT;
                 const int nbox = (min(BT, tok1 - t) + R - 1) / R;
-                if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)(nbox * R * C::ROWB * 2));
+                if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)(nbox * R * C::ROWB * 2 + C::MASK_BYTES));
                 __syncwarp();
                 // lane (box j, column block cb) copies rows [j R, (j + 1) R) of block cb;
                 // the page id of box j is in lane j
@@ -197,6 +209,9 @@ __global__ void __launch_bounds__(C::THREADS, 2)
                     tma_load_5d(dst, &mapK, 0, row, cb, kvh, pj, &full[st]);
                     tma_load_5d(dst + C::TILE_BYTES, &mapV, 0, row, cb, kvh, pj, &full[st]);
                 }
+                // the tile's mask bytes: keys [t, t + BT) of the tile's tokens (zeros past the ends)
+                if (C::MASK && lane == 31)
+                    tma_load_3d(smem + st * C::STAGE_BYTES + C::MASK_OFF, &mapM, t, tl.q0 + tl.i0, 0, &full[st]);
                 issued = i + 1;
             }
             if (lane == 0) misc[0] = issued;
@@ -302,7 +317,9 @@ __global__ void __launch_bounds__(C::THREADS, 2)
             const int t = tok0 + i * BT + h * HT;  // position of the half tile's first key
             const int nvalid = min(BT, tok1 - (tok0 + i * BT));
             const uint32_t tS = tmem + (h ? C::TS1 : C::TS0) + lane_base;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&s_done[h], (j >> 1) & 1))) {
+            // (the mask bytes are read by these threads: they see the stage land themselves)
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&s_done[h], (j >> 1) & 1) &&
+                                             (!C::MASK || h == 1 || mbar_wait(&full[st], (i / NS) & 1)))) {
                 misc[1] = 1;
                 break;
             }
@@ -319,7 +336,21 @@ __global__ void __launch_bounds__(C::THREADS, 2)
                 // keys [0, klim) of the half tile are seen by this row; scores rounded once
                 // (they feed the max and the exponent)
                 const int klim = min(nvalid - h * HT, lim - t + 1);
-                if (__all_sync(0xFFFFFFFFu, !rvalid || klim >= HT)) {
+                if (C::MASK) {  // the row's token's mask bytes of these 32 keys
+                    uint4 mb[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+                    if (rvalid) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(smem + st * C::STAGE_BYTES + C::MASK_OFF +
+                                                                           ti * BT + h * HT);
+                        mb[0] = src[0];
+                        mb[1] = src[1];
+                    }
+                    const uint32_t w[8] = {mb[0].x, mb[0].y, mb[0].z, mb[0].w, mb[1].x, mb[1].y, mb[1].z, mb[1].w};
+#pragma unroll
+                    for (int k = 0; k < HT; ++k) {
+                        const bool keep = rvalid && k < klim && ((w[k >> 2] >> (8 * (k & 3))) & 0xFFu) != 0u;
+                        sv[k] = keep ? __fmul_rn(sv[k], p.qscale) : -INFINITY;
+                    }
+                } else if (__all_sync(0xFFFFFFFFu, !rvalid || klim >= HT)) {
 #pragma unroll
                     for (int k = 0; k < HT; ++k) sv[k] = __fmul_rn(sv[k], p.qscale);
                 } else {
@@ -460,15 +491,17 @@ bool encode_block_map(CUtensorMap *map, const void *base, int D, int Hkv, int pa
     return encode_bf16(map, base, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int D, int G, bool GATHER>
+template <int D, int G, bool MASK, bool GATHER>
 dap_status launch_multi_tc(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
-    using C = TcCfg<D, G, GATHER>;
+    using C = TcCfg<D, G, MASK, GATHER>;
     const int R = GATHER ? C::BT : gcd_int(a.page_size, C::BT);
     p.box_rows = R;
     CUtensorMap mk = {}, mv = {};  // (the row-gather producer reads the cache directly)
     if (!GATHER && (!encode_block_map(&mk, a.k, a.D, a.Hkv, a.page_size, a.num_pages, R) ||
                     !encode_block_map(&mv, a.v, a.D, a.Hkv, a.page_size, a.num_pages, R)))
         return DAP_ERR_CUDA;
+    CUtensorMap mm = {};
+    if (MASK && !encode_mask_map(&mm, a.mask, a.mask_stride, a.total_q, C::QT, C::BT)) return DAP_ERR_CUDA;
     auto kern = multi_tc_kernel<C>;
     static PerDeviceOcc occ = {};
     if (prepare_kernel(kern, C::THREADS, C::SMEM, &occ) <= 0) return DAP_ERR_CUDA;
@@ -479,7 +512,7 @@ dap_status launch_multi_tc(const DecodeArgs &a, SplitParams &p, cudaStream_t str
                                                              partial_acc_bytes(a.total_q, a.Hq, a.D, a.num_splits))
                                  : nullptr;
     if (g_trace.split_begin) cudaEventRecord(g_trace.split_begin, stream);
-    if (launch_dependent_smem(kern, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, stream, mk, mv, p) !=
+    if (launch_dependent_smem(kern, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM, stream, mk, mv, mm, p) !=
         cudaSuccess)
         return DAP_ERR_CUDA;
     if (g_trace.split_end) cudaEventRecord(g_trace.split_end, stream);
@@ -497,33 +530,34 @@ dap_status launch_multi_tc(const DecodeArgs &a, SplitParams &p, cudaStream_t str
     return DAP_OK;
 }
 
-template <int D, bool GATHER>
+template <int D, bool MASK, bool GATHER>
 dap_status dispatch_tc_g(const DecodeArgs &a, SplitParams &p, cudaStream_t stream) {
     switch (a.Hq / a.Hkv) {
-        case 1: return launch_multi_tc<D, 1, GATHER>(a, p, stream);
-        case 2: return launch_multi_tc<D, 2, GATHER>(a, p, stream);
-        case 4: return launch_multi_tc<D, 4, GATHER>(a, p, stream);
-        case 8: return launch_multi_tc<D, 8, GATHER>(a, p, stream);
+        case 1: return launch_multi_tc<D, 1, MASK, GATHER>(a, p, stream);
+        case 2: return launch_multi_tc<D, 2, MASK, GATHER>(a, p, stream);
+        case 4: return launch_multi_tc<D, 4, MASK, GATHER>(a, p, stream);
+        case 8: return launch_multi_tc<D, 8, MASK, GATHER>(a, p, stream);
     }
     return DAP_ERR_UNSUPPORTED;
 }
 
-template <bool GATHER>
+template <bool MASK, bool GATHER>
 dap_status dispatch_tc(const DecodeArgs &a, cudaStream_t stream) {
     SplitParams p = make_params(a);
     switch (a.D) {
-        case 64: return dispatch_tc_g<64, GATHER>(a, p, stream);
-        case 128: return dispatch_tc_g<128, GATHER>(a, p, stream);
+        case 64: return dispatch_tc_g<64, MASK, GATHER>(a, p, stream);
+        case 128: return dispatch_tc_g<128, MASK, GATHER>(a, p, stream);
     }
     return DAP_ERR_UNSUPPORTED;
 }
 
 }  // namespace
 
-// Multi-token decode with 128 / G tokens per work tile (no mask; D 64 or 128).
+// Multi-token decode with 128 / G tokens per work tile (D 64 or 128; with or without a mask).
 dap_status launch_decode_multi_tc(const DecodeArgs &a, cudaStream_t stream) {
-    if (a.mask) return DAP_ERR_UNSUPPORTED;
-    return a.page_size % 8 != 0 ? dispatch_tc<true>(a, stream) : dispatch_tc<false>(a, stream);
+    const bool gather = a.page_size % 8 != 0;
+    if (a.mask) return gather ? dispatch_tc<true, true>(a, stream) : dispatch_tc<true, false>(a, stream);
+    return gather ? dispatch_tc<false, true>(a, stream) : dispatch_tc<false, false>(a, stream);
 }
 
 bool read_errors_multi_tc(unsigned int *flags, bool clear) {

@@ -252,7 +252,7 @@ def multi_call(lib, **kw):
     (dict(tpt=3), 2), (dict(tpt=16), 2), (dict(tpt=0), 2), (dict(tpt=8, mask=FAKE, mst=128), 3),
     # 128-row tiles (tokens_per_tile = 128 / G): D 64 and 128 only, no mask
     (dict(tpt=32, D=256, qsh=256, qst=32 * 256, osh=256, ost=32 * 256), 3), (dict(tpt=32, D=32), 3),
-    (dict(tpt=32, mask=FAKE, mst=128), 3), (dict(tpt=64), 2),
+    (dict(tpt=32, mask=FAKE, mst=128, D=256, qsh=256, qst=32 * 256, osh=256, ost=32 * 256), 3), (dict(tpt=64), 2),
 ])
 def test_multi_validation(lib, kw, status):
     assert multi_call(lib, **kw) == status

@@ -122,7 +122,8 @@ def test_full_size_ragged_with_mask():
 @pytest.mark.parametrize("Hq,Hkv,D,qlens,ps", [(8, 2, 64, [5, 1, 9], 16), (32, 8, 128, [4, 4, 2], 16),
                                                (16, 2, 128, [3, 2, 1], 16), (16, 4, 256, [5, 1, 7], 16),
                                                (64, 8, 32, [2, 1, 2], 16), (32, 8, 128, [4, 4, 2], 12),
-                                               (16, 4, 256, [5, 1, 7], 3)])
+                                               (16, 4, 256, [5, 1, 7], 3), (64, 8, 128, [16, 9, 3], 16),
+                                               (64, 8, 128, [16, 9, 3], 5), (8, 8, 64, [30, 1, 17], 8)])
 def test_multi_token_mask_with_causal_rule(Hq, Hkv, D, qlens, ps):
     lens = [100, 37, 300]
     case = inputs.make_multi_case(3, Hq, Hkv, D, ps, lens, qlens, 6500 + Hq).to("cuda")
@@ -131,11 +132,32 @@ def test_multi_token_mask_with_causal_rule(Hq, Hkv, D, qlens, ps):
     qi = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
     ref = oracle.decode_paged_multi(bits(case.q), bits(kv.k_cache), bits(kv.v_cache), kv.block_table.cpu().numpy(),
                                     kv.seq_lens.cpu().numpy(), qi, kv.scale, mask=full.numpy())
-    # a mask rides with 16-column tiles
-    plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, "cuda", tokens_per_tile=binding.multi_tokens_per_tile(kv.Hq, kv.Hkv))
-    for S in [1, 3]:
-        got = binding.decode_attn_paged_multi(case.q, kv.k_cache, kv.v_cache, kv.block_table, kv.seq_lens, plan,
-                                              max_kv_len=kv.max_kv_len, scale=kv.scale, num_splits=S,
-                                              mask=full.cuda())
-        assert_close(got, ref, f"G={Hq // Hkv} S={S}")
+    # a mask rides with 16-column tiles and, at D 64 and 128, with 128-row tiles
+    G = Hq // Hkv
+    for tpt in [16 // G] + ([128 // G] if D in (64, 128) else []):
+        plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, "cuda", tokens_per_tile=tpt)
+        for S in [1, 3]:
+            got = binding.decode_attn_paged_multi(case.q, kv.k_cache, kv.v_cache, kv.block_table, kv.seq_lens, plan,
+                                                  max_kv_len=kv.max_kv_len, scale=kv.scale, num_splits=S,
+                                                  mask=full.cuda())
+            assert_close(got, ref, f"G={G} tpt={tpt} S={S}")
+    assert binding.get_device_errors() == 0
+
+
+def test_full_size_multi_token_mask_in_128_row_tiles():
+    """The G = 8 speculative-verification batch (B=128, q_len 8, ragged lengths) with a
+    random 3-D mask (70% kept), in 128-row tiles at the planner's split count: every output
+    element against the oracle."""
+    case = inputs.spec_verify_paged(device="cuda", q_len=8, Hq=64)
+    kv = case.kv
+    full, _ = make_mask(case.total_q, kv.max_kv_len, 6600, p_keep=0.7)
+    qi = np.concatenate([[0], np.cumsum(case.q_lens)]).astype(np.int32)
+    ref = oracle.decode_paged_multi(bits(case.q), bits(kv.k_cache), bits(kv.v_cache), kv.block_table.cpu().numpy(),
+                                    kv.seq_lens.cpu().numpy(), qi, kv.scale, mask=full.numpy())
+    plan = binding.MultiPlan(case.q_lens, 64, 8, "cuda", D=128)
+    assert plan.tokens_per_tile == 16
+    got = binding.decode_attn_paged_multi(case.q, kv.k_cache, kv.v_cache, kv.block_table, kv.seq_lens, plan,
+                                          max_kv_len=kv.max_kv_len, scale=kv.scale, num_splits=0,
+                                          total_kv=kv.total_kv, mask=full.cuda())
+    assert_close(got, ref, "full size, G=8 q_len=8, mask")
     assert binding.get_device_errors() == 0
