@@ -156,8 +156,8 @@ size_t dap_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits);
  *                flattened (sequence, kv head, 64-token tile) space into equal contiguous
  *                ranges, whatever the length mix, and a combine kernel merges the pieces
  *                of a sequence (B > 4096 runs one CTA per sequence and kv head instead).
- *                The planner's schedule measures faster on most batches; the balanced one
- *                on a single long sequence.
+ *                The planner's schedule measures faster on every batch measured (a single
+ *                long sequence included).
  *   workspace    device scratch of at least dap_workspace_bytes(B, Hq, Hkv, D,
  *                dap_resolve_splits(num_splits, ...)) bytes, 16-byte aligned (may be NULL
  *                when that is 0).  Needs no initialisation; its contents are undefined
