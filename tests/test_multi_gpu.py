@@ -212,11 +212,14 @@ def test_more_new_tokens_than_keys_gives_zero_rows_and_a_flag():
         assert (out[3:5].float() == 0).all()
 
 
-def test_bad_work_map_entry_is_skipped_and_flagged():
+@pytest.mark.parametrize("tpt", [4, 32])
+def test_bad_work_map_entry_is_skipped_and_flagged(tpt):
+    # 4 tokens per tile: the mma.sync consumer; 32 (128 rows at G = 4): the tcgen05 one
     case = inputs.make_multi_case(2, 8, 2, 64, 16, [50, 40], [3, 2], 4500).to("cuda")
     kv = case.kv
-    plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, "cuda")
+    plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, "cuda", tokens_per_tile=tpt)
     good = gpu_multi(case, 1, plan=plan).clone()
+    binding.get_device_errors(clear=True)
     plan.tile_batch[1] = 7          # names no sequence
     out = torch.zeros_like(good)
     gpu_multi(case, 1, plan=plan, out=out)
@@ -224,6 +227,23 @@ def test_bad_work_map_entry_is_skipped_and_flagged():
     assert binding.get_device_errors() & binding.DEVERR_QMAP
     assert torch.equal(out[:3], good[:3])   # the first tile is unaffected
     assert (out[3:] == 0).all()              # the skipped tile's rows are left as they were
+
+
+@pytest.mark.parametrize("ps", [16, 5])
+def test_tensor_memory_tiles_flag_a_bad_page_id(ps):
+    """A block-table entry outside the pool is read as page 0 and flagged (TMA and row-gather
+    producers of the 128-row tiles); the other sequence's rows are unaffected."""
+    case = inputs.make_multi_case(2, 64, 8, 128, ps, [300, 200], [9, 4], 4750).to("cuda")
+    kv = case.kv
+    plan = binding.MultiPlan(case.q_lens, 64, 8, "cuda", D=128)
+    assert plan.tokens_per_tile == 16
+    good = gpu_multi(case, 2, plan=plan).clone()
+    binding.get_device_errors(clear=True)
+    kv.block_table[1, 3] = kv.num_pages + 5
+    out = gpu_multi(case, 2, plan=plan)
+    torch.cuda.synchronize()
+    assert binding.get_device_errors() & binding.DEVERR_PAGE
+    assert torch.equal(out[:9], good[:9])
 
 
 def test_repeat_is_deterministic():
