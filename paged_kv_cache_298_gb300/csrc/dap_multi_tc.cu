@@ -17,10 +17,11 @@
 // shared memory), another, once the consumers have turned the row of scores into P,
 // O += P . V (A = P from tensor memory, B = the V tile MN-major); the commit of a tile's
 // last product frees its stage.  The scores of the next half tile are computed while the
-// consumers work on the current one.  Consumer thread r masks its row causally (key position <= the
-// token's position) and takes the base-2 online softmax; the running max is moved lazily:
-// O and l are rescaled only when a half tile's max exceeds the reference by more than 2^8
-// (the weights stay <= 256, far inside fp32), and the reference is stored with the
+// consumers work on the current one.  Consumer thread r masks its row causally (key
+// position <= the token's position; with a bool mask, also by the token's mask byte, which
+// rides with the stage) and takes the base-2 online softmax; the running max is moved
+// lazily: O and l are rescaled only when a half tile's max exceeds the reference by more
+// than 2^8 (the weights stay <= 256, far inside fp32), and the reference is stored with the
 // partial, so the merge and the final division see the same softmax.
 // The K/V tiles are laid out column block major, [D / 64 blocks][64 keys][128 bytes] with
 // the 128-byte swizzle, whatever the page size: the layout the row gather (page sizes that
