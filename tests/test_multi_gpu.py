@@ -188,6 +188,17 @@ def test_full_size_eight_heads_tensor_memory_tiles(q_len):
     assert binding.get_device_errors() == 0
 
 
+@pytest.mark.parametrize("S", [1, 2])
+def test_tensor_memory_tiles_long_sequence(S):
+    """A 20,000-key sequence in one or two splits (over 150 K/V tiles per CTA: every stage
+    and buffer barrier turns many times) next to a short one, 16 tokens at G = 8."""
+    case = inputs.make_multi_case(2, 64, 8, 128, 16, [20000, 70], [16, 3], 4680).to("cuda")
+    plan = binding.MultiPlan(case.q_lens, 64, 8, "cuda", D=128)
+    assert plan.tokens_per_tile == 16
+    assert_close(gpu_multi(case, S, plan=plan), oracle_multi(case), f"long sequence, S={S}")
+    assert binding.get_device_errors() == 0
+
+
 def test_tensor_memory_tiles_repeat_bit_identically():
     case = inputs.make_multi_case(4, 64, 8, 128, 16, [500, 800, 90, 1500], [5, 16, 1, 9], 4650).to("cuda")
     plan = binding.MultiPlan(case.q_lens, 64, 8, "cuda", tokens_per_tile=16)
