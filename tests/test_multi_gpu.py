@@ -133,7 +133,9 @@ def test_one_new_token_each_matches_single_token_decode():
     assert torch.allclose(multi.float(), single.float(), atol=ATOL, rtol=RTOL)
 
 
-def test_strided_q_and_out():
+@pytest.mark.parametrize("D", [None, 128])
+def test_strided_q_and_out(D):
+    # D=None: 32-column tiles; D=128: the 128-row tcgen05 tiles
     case = inputs.make_multi_case(2, 16, 4, 128, 16, [90, 400], [6, 3], 4300).to("cuda")
     big_q = torch.zeros(case.total_q, 24, 136, dtype=torch.bfloat16, device="cuda")
     big_q[:, :16, :128] = case.q
@@ -141,7 +143,7 @@ def test_strided_q_and_out():
     out_big = torch.full((case.total_q, 20, 256), 7.0, dtype=torch.bfloat16, device="cuda")
     out = out_big[:, 2:18, 64:192]
     kv = case.kv
-    plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, "cuda")
+    plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, "cuda", D=D)
     binding.decode_attn_paged_multi(q, kv.k_cache, kv.v_cache, kv.block_table, kv.seq_lens, plan,
                                     max_kv_len=kv.max_kv_len, num_splits=2, out=out)
     assert_close(out, oracle_multi(case), "strided")
