@@ -258,8 +258,8 @@ dap_status kv_append_paged_fp8(const void *k_new, const void *v_new, uint8_t *k_
  * tokens x the G heads of a kv head are its query columns, and every tile streams its
  * sequence's keys once, so the fewer tiles a sequence has, the fewer times its K/V are
  * read.  Three tile sizes: 16 / G tokens (16 columns), 32 / G tokens (32 columns; not with a
- * mask) and, for D 64 and 128, 128 / G tokens (128 query rows of tensor-memory products: up
- * to 16 tokens at G = 8 against one K/V stream).
+ * mask) and, for D 64, 128 and 256, 128 / G tokens (128 query rows of tensor-memory
+ * products: up to 16 tokens at G = 8 against one K/V stream).
  * dap_multi_tokens_per_tile(Hq, Hkv, D, max_q_len) picks 16 / G when the longest new-token
  * count fits it, else 128 / G where D allows (D = 0: head dim not known, no 128-row tiles),
  * else 32 / G (G = 8, D = 128: 2 tokens up to q_len 2, then 16).
@@ -284,8 +284,8 @@ size_t dap_workspace_bytes_multi(int total_q, int Hq, int D, int num_splits);
  *   seq_lens     device int32 [B], in [q_len[b], max_kv_len].
  *   qo_indptr    device int32 [B + 1]; tile_batch, tile_index device int32 [num_tiles]: the
  *                work map above (copies of dap_q_tile_map's output), built with
- *   tokens_per_tile  16 / G, 32 / G or, at D 64 and 128, 128 / G (else DAP_ERR_SHAPE;
- *                32 / G with a mask, 128 / G at other head dims: DAP_ERR_UNSUPPORTED).
+ *   tokens_per_tile  16 / G, 32 / G or, at D 64, 128 and 256, 128 / G (else DAP_ERR_SHAPE;
+ *                32 / G with a mask, 128 / G at D = 32: DAP_ERR_UNSUPPORTED).
  *   num_splits   >= 1: the per-sequence schedule of decode_attn_paged, per tile: the tile's
  *                keys (up to its last token's position) are cut into chunks of
  *                dap_chunk_tokens(max_kv_len, num_splits) keys, one CTA per (tile, kv head,

@@ -484,7 +484,7 @@ def decode_attn_paged_fp8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, 
 
 def multi_tokens_per_tile(Hq: int, Hkv: int, max_q_len: int = 0, D: int = 0) -> int:
     """include/dap.h: dap_multi_tokens_per_tile (16 / G; for longer new-token runs 128 / G
-    where the head dim D has the 128-row tiles, else 32 / G; D = 0: not known)."""
+    where the head dim D has the 128-row tiles (64, 128, 256), else 32 / G; D = 0: not known)."""
     return load().dap_multi_tokens_per_tile(int(Hq), int(Hkv), int(D), int(max_q_len))
 
 

@@ -340,7 +340,7 @@ dap_status decode_attn_paged_multi(const void *q, long long q_stride_t, long lon
         const int cols = tokens_per_tile * G;
         if (cols != 16 && cols != 32 && cols != 128) return DAP_ERR_SHAPE;
         if (mask && cols == 32) return DAP_ERR_UNSUPPORTED;
-        if (cols == 128 && D != 64 && D != 128) return DAP_ERR_UNSUPPORTED;
+        if (cols == 128 && D != 64 && D != 128 && D != 256) return DAP_ERR_UNSUPPORTED;
     }
     if ((st = check_mask(mask, mask_stride, max_kv_len)) != DAP_OK) return st;
     int S = 0, chunk = 0;

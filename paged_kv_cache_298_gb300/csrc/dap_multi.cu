@@ -6,12 +6,12 @@
 namespace dap {
 
 // 16 / G tokens (mma.sync consumer, 16 columns) while they hold the longest run of new
-// tokens; beyond that the 128-row tensor-memory tiles where the head dim has them (one K/V
-// stream for up to 128 / G tokens), else 32 / G (two column groups).
+// tokens; beyond that the 128-row tensor-memory tiles where the head dim has them (64, 128
+// and 256: one K/V stream for up to 128 / G tokens), else 32 / G (two column groups).
 int multi_tokens_per_tile(int G, int D, int max_q_len) {
     if (G < 1 || G > 16) return 0;
     if (max_q_len <= 16 / G) return 16 / G;
-    return (D == 64 || D == 128) ? 128 / G : 32 / G;
+    return (D == 64 || D == 128 || D == 256) ? 128 / G : 32 / G;
 }
 
 dap_status launch_decode_multi(const DecodeArgs &a, cudaStream_t stream) {

@@ -46,24 +46,30 @@ struct TcCfg {
     // a stage: the K and V tiles, then (with a mask) the tile's mask bytes [QT tokens][BT keys]
     static constexpr int MASK_OFF = 2 * TILE_BYTES, MASK_BYTES = MASK ? QT * BT : 0;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES + (MASK_BYTES + 1023) / 1024 * 1024;
-    // 96 KB of stages (up to 108 KB with masks): two CTAs per SM
-    static constexpr int NS = (MASK ? 110592 : 98304) / STAGE_BYTES;
+    // 96 KB of stages (up to 108 KB with masks): two CTAs per SM; D = 256: three stages of
+    // 64 KB (and the masks) at one CTA per SM
+    static constexpr int MINB = D == 256 ? 1 : 2;
+    static constexpr int NS = D == 256 ? 3 : (MASK ? 110592 : 98304) / STAGE_BYTES;
     // warps: 4 consumers, the producer, the S issuer, the PV issuer
     static constexpr int NWC = 4, PRODUCER = 4, S_ISSUER = 5, PV_ISSUER = 6, THREADS = 7 * 32;
     // tensor-memory columns: q, the two half-tile score buffers (P over their first 16
     // columns), O
-    static constexpr int TQ = 0, TS0 = 64, TS1 = 96, TO = 128, TMEM_COLS = 256;
+    // (D = 256: q [0, 128), scores [128, 192), O [256, 512) of 512 columns)
+    static constexpr int TQ = 0, TS0 = D == 256 ? 128 : 64, TS1 = TS0 + 32, TO = D == 256 ? 256 : 128;
+    static constexpr int TMEM_COLS = D == 256 ? 512 : 256;
     // barriers: full[NS], empty[NS], s_done[2], p_ready[2], pv_done[2], q_ready, fin[2]
     static constexpr int BAR_OFF = NS * STAGE_BYTES;
     static constexpr int NBAR = 2 * NS + 9;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr int SMEM = MISC_OFF + 32 + 1024;  // + slack to align the base to 1024
-    static_assert((D == 64 || D == 128) && ROWS % G == 0 && NS >= 2 && SMEM <= 113 * 1024, "tcgen05 multi-token tiling");
+    static_assert((D == 64 || D == 128 || D == 256) && ROWS % G == 0 && NS >= 2 &&
+                      SMEM <= (MINB == 2 ? 113 : 227) * 1024,
+                  "tcgen05 multi-token tiling");
     static_assert(TQ + D / 2 <= TS0 && TS1 + HT <= TO && TO + D <= TMEM_COLS, "tensor-memory columns");
 };
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS, 2)
+__global__ void __launch_bounds__(C::THREADS, C::MINB)
     multi_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                     const __grid_constant__ CUtensorMap mapM, const SplitParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -548,6 +554,7 @@ dap_status dispatch_tc(const DecodeArgs &a, cudaStream_t stream) {
     switch (a.D) {
         case 64: return dispatch_tc_g<64, MASK, GATHER>(a, p, stream);
         case 128: return dispatch_tc_g<128, MASK, GATHER>(a, p, stream);
+        case 256: return dispatch_tc_g<256, MASK, GATHER>(a, p, stream);
     }
     return DAP_ERR_UNSUPPORTED;
 }

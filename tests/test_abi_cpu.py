@@ -183,10 +183,10 @@ def test_multi_tokens_per_tile(lib):
     assert [binding.multi_tokens_per_tile(8 * g, 8, 17) for g in (1, 2, 4, 8)] == [32, 16, 8, 4]
     assert binding.multi_tokens_per_tile(64, 8, 2) == 2 and binding.multi_tokens_per_tile(64, 8, 3) == 4
     assert binding.multi_tokens_per_tile(30, 8) == 0 and binding.multi_tokens_per_tile(8, 0) == 0
-    # with the head dim: 128-row tiles (128 / G tokens) past 16 / G tokens at D 64 and 128
+    # with the head dim: 128-row tiles (128 / G tokens) past 16 / G tokens at D 64, 128, 256
     assert [binding.multi_tokens_per_tile(8 * g, 8, 4, 128) for g in (1, 2, 4, 8)] == [16, 8, 4, 16]
     assert [binding.multi_tokens_per_tile(8 * g, 8, 17, 64) for g in (1, 2, 4, 8)] == [128, 64, 32, 16]
-    assert [binding.multi_tokens_per_tile(64, 8, 3, d) for d in (32, 64, 128, 256)] == [4, 16, 16, 4]
+    assert [binding.multi_tokens_per_tile(64, 8, 3, d) for d in (32, 64, 128, 256)] == [4, 16, 16, 16]
     assert binding.multi_tokens_per_tile(64, 8, 2, 128) == 2 and binding.multi_tokens_per_tile(64, 8, 3, -1) == 0
 
 
@@ -250,9 +250,8 @@ def multi_call(lib, **kw):
     (dict(S=4), 4), (dict(S=4, ws=FAKE, wsb=16), 4),
     (dict(mask=FAKE, mst=96), 2), (dict(mask=FAKE, mst=120), 5), (dict(mask=ctypes.c_void_p((1 << 20) + 4), mst=128), 5),
     (dict(tpt=3), 2), (dict(tpt=16), 2), (dict(tpt=0), 2), (dict(tpt=8, mask=FAKE, mst=128), 3),
-    # 128-row tiles (tokens_per_tile = 128 / G): D 64 and 128 only, no mask
-    (dict(tpt=32, D=256, qsh=256, qst=32 * 256, osh=256, ost=32 * 256), 3), (dict(tpt=32, D=32), 3),
-    (dict(tpt=32, mask=FAKE, mst=128, D=256, qsh=256, qst=32 * 256, osh=256, ost=32 * 256), 3), (dict(tpt=64), 2),
+    # 128-row tiles (tokens_per_tile = 128 / G): D 64, 128 and 256 only
+    (dict(tpt=32, D=32), 3), (dict(tpt=32, mask=FAKE, mst=128, D=32), 3), (dict(tpt=64), 2),
 ])
 def test_multi_validation(lib, kw, status):
     assert multi_call(lib, **kw) == status

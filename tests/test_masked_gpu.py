@@ -132,9 +132,9 @@ def test_multi_token_mask_with_causal_rule(Hq, Hkv, D, qlens, ps):
     qi = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
     ref = oracle.decode_paged_multi(bits(case.q), bits(kv.k_cache), bits(kv.v_cache), kv.block_table.cpu().numpy(),
                                     kv.seq_lens.cpu().numpy(), qi, kv.scale, mask=full.numpy())
-    # a mask rides with 16-column tiles and, at D 64 and 128, with 128-row tiles
+    # a mask rides with 16-column tiles and, at D 64, 128 and 256, with 128-row tiles
     G = Hq // Hkv
-    for tpt in [16 // G] + ([128 // G] if D in (64, 128) else []):
+    for tpt in [16 // G] + ([128 // G] if D in (64, 128, 256) else []):
         plan = binding.MultiPlan(case.q_lens, kv.Hq, kv.Hkv, "cuda", tokens_per_tile=tpt)
         for S in [1, 3]:
             got = binding.decode_attn_paged_multi(case.q, kv.k_cache, kv.v_cache, kv.block_table, kv.seq_lens, plan,

@@ -54,9 +54,9 @@ def _clean_errors():
 
 def tile_sizes(Hq, Hkv, D=None):
     """Every tile size of the work map: 16 and 32 query columns, and 128 query rows of the
-    tensor-memory tiles where the head dim has them (64 and 128)."""
+    tensor-memory tiles where the head dim has them (64, 128 and 256)."""
     G = Hq // Hkv
-    return [16 // G, 32 // G] + ([128 // G] if D in (64, 128) else [])
+    return [16 // G, 32 // G] + ([128 // G] if D in (64, 128, 256) else [])
 
 
 def test_small_case_several_tiles_and_split_counts():
@@ -187,6 +187,21 @@ def test_full_size_eight_heads_tensor_memory_tiles(q_len):
     ref = oracle_multi(case)
     assert_close(gpu_multi(case, 0, plan=plan, total_kv=case.kv.total_kv), ref, f"G=8 q_len={q_len} 128 rows")
     assert_close(gpu_multi(case, 1, plan=plan), ref, f"G=8 q_len={q_len} 128 rows, one split")
+    assert binding.get_device_errors() == 0
+
+
+@pytest.mark.parametrize("ps", [16, 7])
+def test_tensor_memory_tiles_head_dim_256(ps):
+    """D = 256 in 128-row tiles (one CTA per SM, 64 KB stages, O in tensor-memory columns
+    256..511), 16 tokens per sequence at G = 8, TMA boxes and the row gather, against the
+    oracle at three split counts."""
+    lens = [2900, 700, 65, 1800, 16, 3000]
+    case = inputs.make_multi_case(6, 64, 8, 256, ps, lens, [16, 9, 16, 1, 16, 12], 4690 + ps).to("cuda")
+    plan = binding.MultiPlan(case.q_lens, 64, 8, "cuda", D=256)
+    assert plan.tokens_per_tile == 16
+    ref = oracle_multi(case)
+    for S in [0, 1, 3]:
+        assert_close(gpu_multi(case, S, plan=plan), ref, f"D=256 ps={ps} S={S}")
     assert binding.get_device_errors() == 0
 
 
